@@ -1,0 +1,242 @@
+/*
+ * rf.h -- C ABI of the row-window dequant-GEMV library for GB300 (sm_103a).
+ *
+ * Batch-1 decode multiplies quantized weights straight from their raw
+ * GGUF-style block bytes, one row window of output neurons at a time.  A
+ * weight matrix is row-major [out][in] (RAMforge, "Milestone 6 - True
+ * Out-of-Core Integrity", matrix layout: y[o] = sum_i W[o*in+i] * x[i]); a row
+ * is a whole number of 32-element blocks (neurostream, "The idea").
+ *
+ * Conventions for every call:
+ *   - W, x, y, logits, workspace and out are CUDA device pointers unless the
+ *     name says host.  All buffers belong to the caller; the library keeps no
+ *     pointer past the call except inside an rf_arena it created.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     stream ordered and return after enqueueing; no call blocks the host on
+ *     GPU work except rf_device_status and rf_arena_destroy.
+ *   - Argument errors are detected on the host before anything is enqueued;
+ *     the call then returns an error and enqueues nothing.  Launch errors
+ *     return RF_ERR_CUDA.  Kernels never trap: a kernel whose internal wait
+ *     exceeds its time limit records RF_ERR_TIMEOUT in a device status word
+ *     that rf_device_status reports.
+ *   - Weight pointers must be 16-byte aligned.  A kernel may read whole
+ *     16-byte aligned chunks that contain bytes of the rows it was given (so
+ *     up to 15 bytes before the first and after the last row byte, never in
+ *     another 16-byte chunk); it never writes weight memory.
+ *   - There is no CPU fallback: without a CUDA device every compute call
+ *     returns RF_ERR_CUDA.
+ */
+#ifndef RF_H
+#define RF_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define RF_API __attribute__((visibility("default")))
+#else
+#define RF_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- formats */
+/* Block formats, numbered like the GGML type ids.
+ *   RF_Q4_0 : 18 B per 32 weights: fp16 scale d, then 16 bytes of 4-bit q;
+ *             w = d*(q-8) (RAMforge, "Milestone 5 - Native Quantized Tensor
+ *             Support").  Element j<16 is the low nibble of quant byte j and
+ *             element j+16 its high nibble.
+ *   RF_Q8_0 : 34 B per 32 weights: fp16 scale d, then 32 int8 q; w = d*q
+ *             (same section).
+ *   RF_MXFP4: 17 B per 32 weights: E8M0 scale byte E, then 16 bytes of FP4
+ *             E2M1 codes in the Q4_0 nibble order; w = e2m1(c) * 2^(E-127)
+ *             (named by neurostream, "The idea"; layout per the OCP MX
+ *             definition, which the pages do not print). */
+#define RF_Q4_0 2
+#define RF_Q8_0 8
+#define RF_MXFP4 39
+
+typedef enum rf_status {
+    RF_OK = 0,
+    RF_ERR_INVALID_ARG = 1,     /* null pointer, bad size, in_dim % 32 != 0, ... */
+    RF_ERR_UNSUPPORTED_FMT = 2, /* fmt is not one of RF_Q4_0, RF_Q8_0, RF_MXFP4 */
+    RF_ERR_NOT_PINNED = 3,      /* a host weight pointer is not page-locked */
+    RF_ERR_ARENA_TOO_SMALL = 4, /* depth+1 one-row blocks do not fit the arena */
+    RF_ERR_CUDA = 5,            /* a CUDA runtime call or launch failed */
+    RF_ERR_TIMEOUT = 6,         /* a device wait exceeded its limit */
+    RF_ERR_OOM = 7,             /* device or host allocation failed */
+    RF_ERR_MISALIGNED = 8,      /* a weight pointer is not 16-byte aligned */
+    RF_ERR_TOO_LARGE = 9        /* a size exceeds a documented kernel limit */
+} rf_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+RF_API const char *rf_status_str(int status);
+
+/* Library ABI version (major*10000 + minor*100 + patch). */
+RF_API int rf_version(void);
+
+/* Bytes per 32-weight block: 18 (Q4_0), 34 (Q8_0), 17 (MXFP4); 0 if unknown. */
+RF_API size_t rf_block_bytes(int fmt);
+
+/* Bytes per row of in_dim weights (in_dim/32 blocks); 0 if fmt is unknown or
+ * in_dim is not a positive multiple of 32. */
+RF_API size_t rf_row_bytes(int fmt, int64_t in_dim);
+
+/* Largest in_dim the GEMV kernels accept for `fmt` with `n_x` distinct
+ * activation vectors in one launch (their fixed-point digits are kept in
+ * shared memory); 0 without a CUDA device. */
+RF_API int64_t rf_max_in_dim(int fmt, int n_x);
+
+/* ------------------------------------------------------------- dequantize */
+/* Decode n_blocks consecutive blocks at W (device) into out (device,
+ * 32*n_blocks floats).  Every dequantized value is exactly representable in
+ * fp32, so the result is bit-exact.  Errors: RF_ERR_UNSUPPORTED_FMT,
+ * RF_ERR_INVALID_ARG (null pointer, n_blocks < 0). */
+RF_API rf_status rf_dequantize(int fmt, const void *W, int64_t n_blocks, float *out,
+                               void *stream);
+
+/* ------------------------------------------------------------------- GEMV */
+/* Fused dequant-GEMV over one row window (neurostream, "How it works" 4-5:
+ * stream_linear walks [row_start,row_end) and the fused kernel multiplies
+ * straight from the quantized bytes):
+ *     y[r - row_start] = sum_i w[r,i] * x[i]   for r in [row_start, row_end)
+ * W   : device, 16-byte aligned, row 0 of a row-major matrix of
+ *       rf_row_bytes(fmt,in_dim)-byte rows; only the window's rows are read.
+ * x   : device, in_dim floats.   y : device, row_end-row_start floats.
+ * The result of a row depends only on that row and x, never on the window,
+ * so any split of a matrix into windows gives bit-identical outputs.
+ * Errors: RF_ERR_UNSUPPORTED_FMT; RF_ERR_INVALID_ARG (null pointer,
+ * in_dim % 32 != 0, row_start < 0, row_end < row_start); RF_ERR_MISALIGNED;
+ * RF_ERR_TOO_LARGE (in_dim > rf_max_in_dim(fmt,1)).  An empty window is a
+ * no-op. */
+RF_API rf_status rf_gemv(int fmt, const void *W, int64_t row_start, int64_t row_end,
+                         int64_t in_dim, const float *x, float *y, void *stream);
+
+/* One row window for rf_gemv_batch (all device pointers). */
+typedef struct rf_window {
+    const void *W;      /* row 0 of the matrix (16-byte aligned) */
+    int64_t row_start;  /* first row of the window */
+    int64_t row_end;    /* one past the last row */
+    const float *x;     /* in_dim floats */
+    float *y;           /* row_end-row_start floats */
+} rf_window;
+
+/* Several row windows of matrices with the same fmt and in_dim in ONE kernel
+ * launch (e.g. the Q, K and V projections of a decode step).  `windows` is a
+ * host array; at most 8 distinct x pointers per call.  Each window's output is
+ * bit-identical to rf_gemv on it.  Errors as rf_gemv, plus RF_ERR_TOO_LARGE
+ * for more than 64 windows or 8 distinct x. */
+RF_API rf_status rf_gemv_batch(int fmt, int64_t in_dim, int n_windows,
+                               const rf_window *windows, void *stream);
+
+/* ------------------------------------------------------------ activations */
+/* h[i] = silu(g[i]) * u[i], silu(z) = z/(1+exp(-z)) (RAMforge, "Milestone 3";
+ * the SwiGLU between gate/up and down).  Device pointers, n >= 0. */
+RF_API rf_status rf_swiglu(const float *g, const float *u, float *h, int64_t n, void *stream);
+
+/* h[i] = 0.5*z[i]*(1+erf(z[i]/sqrt(2))) (erf form of GELU).  Device. */
+RF_API rf_status rf_gelu(const float *z, float *h, int64_t n, void *stream);
+
+/* --------------------------------------------------------- dense SwiGLU FFN */
+/* Two-phase FFN (neurostream, "How it works", FFN paragraph): walk gate and up
+ * by neuron to get h = silu(gate.x) * (up.x) (one launch, SwiGLU fused into
+ * its epilogue), then walk down by output dimension (one launch).
+ * gate, up: [n_ff][n_embd]; down: [n_embd][n_ff]; x: n_embd; y: n_embd;
+ * h: n_ff floats of caller memory that receives the activations.
+ * All device.  Errors as rf_gemv. */
+RF_API rf_status rf_ffn_swiglu(int fmt, const void *gate, const void *up, const void *down,
+                               int64_t n_ff, int64_t n_embd, const float *x, float *y,
+                               float *h, void *stream);
+
+/* ------------------------------------------- host-streamed row windows */
+/* An arena is a bounded ring of device memory plus a copy stream and events
+ * (neurostream, "How it works" 6: every in-flight block holds a byte
+ * reservation, and allocation waits until one retires).  rf_arena_create
+ * allocates `bytes` (plus a little alignment slack) of device memory on the
+ * current device.  An arena is used by one host thread at a time. */
+typedef struct rf_arena rf_arena;
+RF_API rf_status rf_arena_create(size_t bytes, rf_arena **out);
+/* Waits for the arena's outstanding copies and readers, then frees it.
+ * NULL is a no-op. */
+RF_API void rf_arena_destroy(rf_arena *arena);
+
+/* Host-side block plan for walking n_rows rows of rf_row_bytes(fmt,in_dim)
+ * bytes in blocks of block_rows rows (0 = the whole window) with `depth`
+ * blocks in flight: blocks shrink until depth+1 of them fit arena_bytes
+ * (neurostream, "The idea"; "Bugs worth knowing about": the pipeline holds
+ * depth+1 blocks).  Outputs (each may be NULL) the effective rows per block,
+ * the block count and the peak arena bytes.  RF_ERR_ARENA_TOO_SMALL if one
+ * row per block does not fit; never touches a GPU. */
+RF_API rf_status rf_stream_plan(int fmt, int64_t in_dim, int64_t n_rows, int64_t block_rows,
+                                int depth, size_t arena_bytes, int64_t *eff_rows,
+                                int64_t *n_blocks, size_t *peak_bytes);
+
+/* stream_linear over weights held in page-locked host memory (neurostream,
+ * "How it works" 3-4 and 6): for each planned block of rows in
+ * [row_start,row_end), copy its raw bytes host->arena slot on the arena's copy
+ * stream, then run the fused GEMV on that slot in `stream`; a slot is reused
+ * only after the GEMV that read it has finished, so at most `depth` copies
+ * run ahead of the multiply and depth+1 slots are held.  The host never
+ * blocks.  host_W: page-locked host pointer to row 0 of the [out][in] matrix
+ * (16-byte aligned); x, y: device.  Output is bit-identical to rf_gemv on the
+ * same rows for every block_rows and depth.
+ * Errors: as rf_gemv; RF_ERR_NOT_PINNED if host_W is not page-locked;
+ * RF_ERR_ARENA_TOO_SMALL; RF_ERR_INVALID_ARG for depth < 0 or depth > 64. */
+RF_API rf_status rf_stream_linear(int fmt, const void *host_W, int64_t in_dim,
+                                  int64_t row_start, int64_t row_end, int64_t block_rows,
+                                  int depth, rf_arena *arena, const float *x, float *y,
+                                  void *stream);
+
+/* Counters of an arena (each one is exercised by a test). */
+typedef struct rf_stream_stats {
+    uint64_t calls;          /* rf_stream_linear calls enqueued */
+    uint64_t blocks;         /* blocks copied and multiplied */
+    uint64_t bytes_copied;   /* host->device bytes enqueued */
+    uint64_t peak_bytes;     /* largest arena bytes reserved at once (planned) */
+    uint64_t slot_bytes;     /* bytes per slot in the last call */
+    uint64_t arena_bytes;    /* arena capacity */
+    int32_t slots;           /* slots (depth+1) in the last call */
+    int32_t last_block_rows; /* effective rows per block in the last call */
+} rf_stream_stats;
+RF_API rf_status rf_stream_stats_get(const rf_arena *arena, rf_stream_stats *out);
+
+/* ------------------------------------------------------------------- MoE */
+/* Device top-k router (neurostream, "How it works" 2: the router names the
+ * active experts and only those are read): idx[k] = the k-th largest logit's
+ * expert (ties to the lower index), w[k] = softmax over the selected logits.
+ * logits: device n_expert floats; idx: device top_k int32; w: device top_k
+ * floats.  1 <= top_k <= min(n_expert, 8), n_expert <= 1024. */
+RF_API rf_status rf_moe_route(const float *logits, int n_expert, int top_k, int32_t *idx,
+                              float *w, void *stream);
+
+/* Bytes of caller scratch rf_moe_ffn needs (routing result + activations). */
+RF_API size_t rf_moe_workspace_bytes(int top_k, int64_t n_ff, int64_t n_embd,
+                                     int64_t block_rows);
+
+/* Routed MoE SwiGLU FFN over stacked expert tensors (neurostream, "The idea"
+ * and "How it works" 2-5): route on device, then walk each selected expert's
+ * row windows [e*out + j*block_rows, ...) of gate and up in ONE launch (SwiGLU
+ * in the epilogue), then the down windows of all selected experts in ONE
+ * launch that also forms y = sum_k w_k * down_k(h_k) in selection order.
+ * No host synchronisation.  gate, up: (n_expert, n_ff, n_embd);
+ * down: (n_expert, n_embd, n_ff); router_logits: n_expert floats; x, y:
+ * n_embd floats; workspace: rf_moe_workspace_bytes(...) bytes, 256-byte
+ * aligned.  All device.  block_rows 0 = whole expert.  Errors as rf_gemv and
+ * rf_moe_route. */
+RF_API rf_status rf_moe_ffn(int fmt, const float *router_logits, int n_expert, int top_k,
+                            const void *gate, const void *up, const void *down, int64_t n_ff,
+                            int64_t n_embd, int64_t block_rows, const float *x, float *y,
+                            void *workspace, void *stream);
+
+/* --------------------------------------------------------------- status */
+/* Synchronizes the current device, then reports and clears the device status
+ * word that kernels set when a bounded wait times out (RF_OK if none).
+ * Returns RF_ERR_CUDA if the device reports an error. */
+RF_API rf_status rf_device_status(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RF_H */

@@ -1,0 +1,283 @@
+// rf_api.cu -- C ABI entry points: sizes, status, dequantize, GEMV, batched
+// windows, elementwise activations and the two-phase dense SwiGLU FFN.
+#include <cuda_fp16.h>
+
+#include <cstring>
+
+#include "rf_device.cuh"
+#include "rf_internal.h"
+
+namespace rf {
+namespace {
+
+// ---------------------------------------------------------------- dequantize
+// One thread per block: decode 32 weights to fp32.  Every value d*q,
+// d*(q-8) and e2m1*2^(E-127) is exactly representable, so any correct
+// multiply is bit-exact (RAMforge, "Milestone 5 - Native Quantized Tensor
+// Support" for Q4_0/Q8_0; OCP MX E2M1/E8M0 for MXFP4).
+__device__ __forceinline__ float e2m1_value(uint32_t c)
+{
+    // magnitude by code bits e1 e0 m: 0, .5, 1, 1.5, 2, 3, 4, 6
+    const uint32_t e = (c >> 1) & 3u, m = c & 1u;
+    const float mag = e == 0 ? 0.5f * (float)m
+                             : __uint_as_float((uint32_t)(126 + e) << 23) * (1.0f + 0.5f * (float)m);
+    return (c & 8u) ? -mag : mag;
+}
+
+__device__ __forceinline__ float e8m0_value(uint32_t E)
+{
+    // 2^(E-127); E = 0 is the subnormal 2^-127; E = 255 is NaN in the format.
+    if (E == 255u) return __uint_as_float(0x7fc00000u);
+    return E == 0u ? __uint_as_float(0x00400000u) : __uint_as_float(E << 23);
+}
+
+template <int FMT>
+__global__ void dequant_kernel(const uint8_t *__restrict__ W, int64_t n_blocks,
+                               float *__restrict__ out)
+{
+    const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= n_blocks) return;
+    float *o = out + 32 * b;
+    if constexpr (FMT == RF_Q8_0) {
+        const uint8_t *p = W + 34 * b;
+        const float d = __half2float(__ushort_as_half((unsigned short)(p[0] | (p[1] << 8))));
+        for (int j = 0; j < 32; ++j) o[j] = d * (float)(int8_t)p[2 + j];
+    } else if constexpr (FMT == RF_Q4_0) {
+        const uint8_t *p = W + 18 * b;
+        const float d = __half2float(__ushort_as_half((unsigned short)(p[0] | (p[1] << 8))));
+        for (int j = 0; j < 16; ++j) {
+            o[j] = d * (float)((int)(p[2 + j] & 15) - 8);
+            o[j + 16] = d * (float)((int)(p[2 + j] >> 4) - 8);
+        }
+    } else {
+        const uint8_t *p = W + 17 * b;
+        const float s = e8m0_value(p[0]);
+        for (int j = 0; j < 16; ++j) {
+            o[j] = e2m1_value(p[1 + j] & 15u) * s;
+            o[j + 16] = e2m1_value(p[1 + j] >> 4) * s;
+        }
+    }
+}
+
+// -------------------------------------------------------------- activations
+__global__ void swiglu_kernel(const float *__restrict__ g, const float *__restrict__ u,
+                              float *__restrict__ h, int64_t n)
+{
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const float z = g[i];
+        h[i] = z / (1.f + expf(-z)) * u[i];
+    }
+}
+
+__global__ void gelu_kernel(const float *__restrict__ z, float *__restrict__ h, int64_t n)
+{
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const float v = z[i];
+        h[i] = 0.5f * v * (1.f + erff(v * 0.70710678118654752f));
+    }
+}
+
+int elementwise_grid(int64_t n)
+{
+    const int64_t want = (n + 255) / 256;
+    const int64_t cap = (int64_t)num_sms() * 8;
+    return (int)(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
+}  // namespace
+}  // namespace rf
+
+using namespace rf;
+
+extern "C" {
+
+const char *rf_status_str(int status)
+{
+    switch (status) {
+    case RF_OK: return "RF_OK";
+    case RF_ERR_INVALID_ARG: return "RF_ERR_INVALID_ARG";
+    case RF_ERR_UNSUPPORTED_FMT: return "RF_ERR_UNSUPPORTED_FMT";
+    case RF_ERR_NOT_PINNED: return "RF_ERR_NOT_PINNED";
+    case RF_ERR_ARENA_TOO_SMALL: return "RF_ERR_ARENA_TOO_SMALL";
+    case RF_ERR_CUDA: return "RF_ERR_CUDA";
+    case RF_ERR_TIMEOUT: return "RF_ERR_TIMEOUT";
+    case RF_ERR_OOM: return "RF_ERR_OOM";
+    case RF_ERR_MISALIGNED: return "RF_ERR_MISALIGNED";
+    case RF_ERR_TOO_LARGE: return "RF_ERR_TOO_LARGE";
+    default: return "RF_ERR_UNKNOWN";
+    }
+}
+
+int rf_version(void) { return 100; }
+
+size_t rf_block_bytes(int fmt) { return block_bytes_of(fmt); }
+
+size_t rf_row_bytes(int fmt, int64_t in_dim)
+{
+    if (!fmt_ok(fmt) || in_dim <= 0 || in_dim % 32 != 0) return 0;
+    return (size_t)(in_dim / 32) * block_bytes_of(fmt);
+}
+
+int64_t rf_max_in_dim(int fmt, int n_x) { return max_in_dim(fmt, n_x); }
+
+rf_status rf_dequantize(int fmt, const void *W, int64_t n_blocks, float *out, void *stream)
+{
+    if (!fmt_ok(fmt)) return RF_ERR_UNSUPPORTED_FMT;
+    if (n_blocks < 0 || (n_blocks > 0 && (!W || !out))) return RF_ERR_INVALID_ARG;
+    if (n_blocks == 0) return RF_OK;
+    const int threads = 128;
+    const int64_t grid = (n_blocks + threads - 1) / threads;
+    if (grid > 0x7fffffff) return RF_ERR_TOO_LARGE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const uint8_t *w = static_cast<const uint8_t *>(W);
+    switch (fmt) {
+    case RF_Q4_0: dequant_kernel<RF_Q4_0><<<(unsigned)grid, threads, 0, s>>>(w, n_blocks, out); break;
+    case RF_Q8_0: dequant_kernel<RF_Q8_0><<<(unsigned)grid, threads, 0, s>>>(w, n_blocks, out); break;
+    default: dequant_kernel<RF_MXFP4><<<(unsigned)grid, threads, 0, s>>>(w, n_blocks, out); break;
+    }
+    return last_cuda_error();
+}
+
+rf_status rf_gemv(int fmt, const void *W, int64_t row_start, int64_t row_end, int64_t in_dim,
+                  const float *x, float *y, void *stream)
+{
+    if (!fmt_ok(fmt)) return RF_ERR_UNSUPPORTED_FMT;
+    if (!W || !x || !y || in_dim <= 0 || in_dim % 32 != 0 || row_start < 0 ||
+        row_end < row_start)
+        return RF_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(W) & 15u) != 0) return RF_ERR_MISALIGNED;
+    if (row_end - row_start > 0x7fffffffLL) return RF_ERR_TOO_LARGE;
+    if (row_end == row_start) return RF_OK;
+    if (in_dim > max_in_dim(fmt, 1)) return RF_ERR_TOO_LARGE;
+    Job J;
+    std::memset(&J, 0, sizeof(J));
+    J.term[0] = Term{static_cast<const uint8_t *>(W), 0, -1};
+    J.y = y;
+    J.row0 = row_start;
+    J.n_rows = (int32_t)(row_end - row_start);
+    J.n_terms = 1;
+    J.combine = kCombineSum;
+    LaunchDesc d;
+    d.fmt = fmt;
+    d.in_dim = in_dim;
+    d.jobs = &J;
+    d.n_jobs = 1;
+    d.x[0] = x;
+    d.n_x = 1;
+    return launch_rowwin(d, static_cast<cudaStream_t>(stream));
+}
+
+rf_status rf_gemv_batch(int fmt, int64_t in_dim, int n_windows, const rf_window *windows,
+                        void *stream)
+{
+    if (!fmt_ok(fmt)) return RF_ERR_UNSUPPORTED_FMT;
+    if (in_dim <= 0 || in_dim % 32 != 0 || n_windows < 0 || (n_windows > 0 && !windows))
+        return RF_ERR_INVALID_ARG;
+    if (n_windows > kMaxJobs) return RF_ERR_TOO_LARGE;
+    Job jobs[kMaxJobs];
+    LaunchDesc d;
+    d.fmt = fmt;
+    d.in_dim = in_dim;
+    int n_x = 0;
+    for (int i = 0; i < n_windows; ++i) {
+        const rf_window &w = windows[i];
+        if (!w.W || !w.x || !w.y || w.row_start < 0 || w.row_end < w.row_start)
+            return RF_ERR_INVALID_ARG;
+        if ((reinterpret_cast<uintptr_t>(w.W) & 15u) != 0) return RF_ERR_MISALIGNED;
+        if (w.row_end - w.row_start > 0x7fffffffLL) return RF_ERR_TOO_LARGE;
+        int slot = -1;
+        for (int s = 0; s < n_x; ++s)
+            if (d.x[s] == w.x) slot = s;
+        if (slot < 0) {
+            if (n_x == kMaxX) return RF_ERR_TOO_LARGE;
+            d.x[n_x] = w.x;
+            slot = n_x++;
+        }
+        std::memset(&jobs[i], 0, sizeof(Job));
+        jobs[i].term[0] = Term{static_cast<const uint8_t *>(w.W), slot, -1};
+        jobs[i].y = w.y;
+        jobs[i].row0 = w.row_start;
+        jobs[i].n_rows = (int32_t)(w.row_end - w.row_start);
+        jobs[i].n_terms = 1;
+        jobs[i].combine = kCombineSum;
+    }
+    if (n_windows == 0) return RF_OK;
+    if (in_dim > max_in_dim(fmt, n_x)) return RF_ERR_TOO_LARGE;
+    d.jobs = jobs;
+    d.n_jobs = n_windows;
+    d.n_x = n_x;
+    return launch_rowwin(d, static_cast<cudaStream_t>(stream));
+}
+
+rf_status rf_swiglu(const float *g, const float *u, float *h, int64_t n, void *stream)
+{
+    if (n < 0 || (n > 0 && (!g || !u || !h))) return RF_ERR_INVALID_ARG;
+    if (n == 0) return RF_OK;
+    swiglu_kernel<<<elementwise_grid(n), 256, 0, static_cast<cudaStream_t>(stream)>>>(g, u, h, n);
+    return last_cuda_error();
+}
+
+rf_status rf_gelu(const float *z, float *h, int64_t n, void *stream)
+{
+    if (n < 0 || (n > 0 && (!z || !h))) return RF_ERR_INVALID_ARG;
+    if (n == 0) return RF_OK;
+    gelu_kernel<<<elementwise_grid(n), 256, 0, static_cast<cudaStream_t>(stream)>>>(z, h, n);
+    return last_cuda_error();
+}
+
+rf_status rf_ffn_swiglu(int fmt, const void *gate, const void *up, const void *down,
+                        int64_t n_ff, int64_t n_embd, const float *x, float *y, float *h,
+                        void *stream)
+{
+    if (!fmt_ok(fmt)) return RF_ERR_UNSUPPORTED_FMT;
+    if (!gate || !up || !down || !x || !y || !h || n_ff <= 0 || n_embd <= 0 ||
+        n_ff % 32 != 0 || n_embd % 32 != 0)
+        return RF_ERR_INVALID_ARG;
+    if (n_ff > 0x7fffffffLL || n_embd > 0x7fffffffLL) return RF_ERR_TOO_LARGE;
+    for (const void *p : {gate, up, down})
+        if ((reinterpret_cast<uintptr_t>(p) & 15u) != 0) return RF_ERR_MISALIGNED;
+    if (n_embd > max_in_dim(fmt, 1) || n_ff > max_in_dim(fmt, 1)) return RF_ERR_TOO_LARGE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // Phase 1: walk gate and up by neuron; SwiGLU in the epilogue.
+    Job J;
+    std::memset(&J, 0, sizeof(J));
+    J.term[0] = Term{static_cast<const uint8_t *>(gate), 0, -1};
+    J.term[1] = Term{static_cast<const uint8_t *>(up), 0, -1};
+    J.y = h;
+    J.n_rows = (int32_t)n_ff;
+    J.n_terms = 2;
+    J.combine = kCombineSwiGLU;
+    LaunchDesc d1;
+    d1.fmt = fmt;
+    d1.in_dim = n_embd;
+    d1.jobs = &J;
+    d1.n_jobs = 1;
+    d1.x[0] = x;
+    d1.n_x = 1;
+    rf_status st = launch_rowwin(d1, s);
+    if (st != RF_OK) return st;
+    // Phase 2: walk down by output dimension (programmatic dependent launch:
+    // its weight copies overlap the tail of phase 1).
+    Job K;
+    std::memset(&K, 0, sizeof(K));
+    K.term[0] = Term{static_cast<const uint8_t *>(down), 0, -1};
+    K.y = y;
+    K.n_rows = (int32_t)n_embd;
+    K.n_terms = 1;
+    K.combine = kCombineSum;
+    LaunchDesc d2;
+    d2.fmt = fmt;
+    d2.in_dim = n_ff;
+    d2.jobs = &K;
+    d2.n_jobs = 1;
+    d2.x[0] = h;
+    d2.n_x = 1;
+    d2.pdl = true;
+    return launch_rowwin(d2, s);
+}
+
+rf_status rf_device_status(void) { return read_and_clear_device_status(); }
+
+}  // extern "C"

@@ -1,0 +1,697 @@
+// rf_gemv.cu -- the fused row-window dequant-GEMV kernel for sm_103a.
+//
+// What it computes (neurostream, "How it works" 4-5; RAMforge, "Milestone 6",
+// matrix layout): for every row r of a window, y[r] = sum_i w[r,i] * x[i],
+// multiplying straight from the raw quantized block bytes.  Batch-1 GEMV is
+// bound by HBM bandwidth, not by a dense contraction, so no tensor cores are
+// used; the design targets the per-byte instruction budget instead.
+//
+// Design (GB300):
+//   * Lane-per-row.  A warp owns 32 consecutive rows; every lane walks its own
+//     row, so every lane needs the same activation block at the same time and
+//     the activation reads are shared-memory broadcasts.
+//   * K split over the 8 warps of a CTA.  Warp w walks blocks
+//     [G*floor(w*nG/8), G*floor((w+1)*nG/8)) of each of the 32 rows (G = the
+//     format's alignment group, nG = ceil(nb/G)); the CTA sums the 8 warp
+//     partials of a row in warp order.  The split depends only on (format,
+//     in_dim), so a row's result is the same in every window and every launch.
+//   * Weights move global -> shared with 1-D bulk copies (TMA), one copy per
+//     lane per chunk of KC blocks, into a per-warp ring of `stages` slots
+//     guarded by mbarriers (expect_tx byte counts).  A copy starts at the
+//     16-byte boundary at or before the chunk and ends at the one at or after
+//     it, so any row alignment works; rows that are 16-byte aligned (row bytes
+//     a multiple of 16) are decoded with static 16-byte shared loads.
+//   * Integer dot products.  Each 32-element activation block is turned once
+//     per CTA into a fixed-point integer X = rint(x * 2^s) (|X| < 2^22, s
+//     chosen from the block maximum) split into three byte planes.  The block
+//     dot sum_j q_j X_j is then three exact dp4a chains over the raw quant
+//     bytes (Q8_0 bytes are used as they are; Q4_0 nibbles need two masks;
+//     MXFP4 codes go through a byte-permute lookup of 2*e2m1), and one fp32
+//     FMA per block applies d * 2^-s.  Q4_0's "-8" is folded into the
+//     accumulator's start value (-8 * sum_j X_j, precomputed per block).
+//     Error: |x - X*2^-s| <= 2^-23 * max|x_block|, far inside the parity
+//     tolerance 1e-3*||W_r||*||x||; products and in-block sums are exact.
+//   * Persistent CTAs (one per SM; shared memory bounds residency) each take a
+//     contiguous range of 32-row groups across all jobs of the launch.
+//   * Programmatic dependent launch: weight copies for the first chunks are
+//     issued before griddepcontrol.wait, so they overlap the previous kernel.
+#include <cuda_fp16.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "rf_device.cuh"
+#include "rf_internal.h"
+
+namespace rf {
+
+namespace {
+
+// Device status word (see rf_device_status).
+__device__ int g_device_status = 0;
+
+constexpr int kNW = 8;
+constexpr int kThreads = kNW * 32;
+constexpr int kRows = 32;   // rows per group (one per lane)
+
+// Fixed-point digits of one 32-element activation block.
+struct __align__(16) XRec {
+    uint32_t p0[8];      // byte 0 of X (unsigned), 4 elements per word
+    uint32_t p1[8];      // byte 1 of X (unsigned)
+    uint32_t p2[8];      // byte 2 of X (signed: X >> 16)
+    int32_t c0, c1, c2;  // accumulator start values (Q4_0: -8 * sum of the plane)
+    float scale;         // 2^-s
+};
+static_assert(sizeof(XRec) == 112, "XRec layout");
+
+template <int FMT>
+struct FmtT;
+template <>
+struct FmtT<RF_Q4_0> {
+    static constexpr int BS = 18, HDR = 2, QW = 4, G = 8, KC = 16;
+};
+template <>
+struct FmtT<RF_Q8_0> {
+    static constexpr int BS = 34, HDR = 2, QW = 8, G = 8, KC = 8;
+};
+template <>
+struct FmtT<RF_MXFP4> {
+    static constexpr int BS = 17, HDR = 1, QW = 4, G = 16, KC = 16;
+};
+
+// Slot bytes: KC blocks plus up to 15 bytes of rounding on either side, padded
+// to an odd number of 16-byte units so that 16-byte loads of the 32 lanes'
+// slots hit distinct banks.
+template <int FMT>
+__host__ __device__ constexpr int slot_bytes()
+{
+    return (((FmtT<FMT>::KC * FmtT<FMT>::BS + 30 + 15) / 16) % 2 == 0)
+               ? (FmtT<FMT>::KC * FmtT<FMT>::BS + 30 + 15) / 16 * 16 + 16
+               : (FmtT<FMT>::KC * FmtT<FMT>::BS + 30 + 15) / 16 * 16;
+}
+
+struct KParams {
+    Job jobs[kMaxJobs];
+    const float *x[kMaxX];
+    const int32_t *expert_idx;
+    int32_t n_jobs, n_x, nb, total_groups, stages, prefetch_early;
+};
+
+// Element of the 32-block packed into byte `byte` of plane word `word`, in the
+// order the format's decoder produces quant bytes.
+template <int FMT>
+__device__ __forceinline__ int elem_of(int word, int byte)
+{
+    if constexpr (FMT == RF_MXFP4) {
+        // Decoder order per code word k: (4k, 4k+16, 4k+1, 4k+17) then
+        // (4k+2, 4k+18, 4k+3, 4k+19).
+        return 4 * (word >> 1) + 2 * (word & 1) + (byte >> 1) + 16 * (byte & 1);
+    } else {
+        return 4 * word + byte;
+    }
+}
+
+template <int FMT>
+__device__ void make_xrec(const float *xb, XRec *out)
+{
+    float v[32];
+    if ((reinterpret_cast<uintptr_t>(xb) & 15u) == 0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 f = reinterpret_cast<const float4 *>(xb)[i];
+            v[4 * i] = f.x;
+            v[4 * i + 1] = f.y;
+            v[4 * i + 2] = f.z;
+            v[4 * i + 3] = f.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = xb[i];
+    }
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(v[i]));
+    int e = 0;
+    frexpf(m, &e);         // m = f * 2^e, f in [0.5, 1); m == 0 gives e = 0
+    const int s = 22 - e;  // |x * 2^s| < 2^22
+    int X[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) X[i] = __float2int_rn(ldexpf(v[i], s));
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        uint32_t b0 = 0, b1 = 0, b2 = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const int xe = X[elem_of<FMT>(w, b)];
+            b0 |= (uint32_t)(xe & 0xff) << (8 * b);
+            b1 |= (uint32_t)((xe >> 8) & 0xff) << (8 * b);
+            b2 |= (uint32_t)((xe >> 16) & 0xff) << (8 * b);
+        }
+        out->p0[w] = b0;
+        out->p1[w] = b1;
+        out->p2[w] = b2;
+    }
+    int c0 = 0, c1 = 0, c2 = 0;
+    if constexpr (FMT == RF_Q4_0) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            c0 += X[i] & 0xff;
+            c1 += (X[i] >> 8) & 0xff;
+            c2 += X[i] >> 16;
+        }
+        c0 *= -8;
+        c1 *= -8;
+        c2 *= -8;
+    }
+    out->c0 = c0;
+    out->c1 = c1;
+    out->c2 = c2;
+    out->scale = ldexpf(1.0f, -s);
+}
+
+// sum_j q_j * X_j of one block from its three exact partial sums.
+__device__ __forceinline__ float join3(int s0, int s1, int s2)
+{
+    return fmaf((float)s2, 65536.f, (float)(s1 * 256 + s0));
+}
+
+// Integer dot of one block's quant words with the block's digit planes.
+template <int FMT>
+__device__ __forceinline__ float block_idot(const uint32_t (&q)[FmtT<FMT>::QW], const XRec &r)
+{
+    const uint4 *P0 = reinterpret_cast<const uint4 *>(r.p0);
+    const uint4 *P1 = reinterpret_cast<const uint4 *>(r.p1);
+    const uint4 *P2 = reinterpret_cast<const uint4 *>(r.p2);
+    const uint4 a0 = P0[0], a1 = P0[1], b0 = P1[0], b1 = P1[1], c0 = P2[0], c1 = P2[1];
+    const uint32_t p0[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const uint32_t p1[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+    const uint32_t p2[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    int s0, s1, s2;
+    if constexpr (FMT == RF_Q4_0) {
+        const int4 cc = *reinterpret_cast<const int4 *>(&r.c0);
+        s0 = cc.x;
+        s1 = cc.y;
+        s2 = cc.z;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t lo = q[k] & 0x0f0f0f0fu;          // elements 4k..4k+3
+            const uint32_t hi = (q[k] >> 4) & 0x0f0f0f0fu;   // elements 16+4k..
+            s0 = dp4a_uu(lo, p0[k], s0);
+            s1 = dp4a_uu(lo, p1[k], s1);
+            s2 = dp4a_us(lo, p2[k], s2);
+            s0 = dp4a_uu(hi, p0[k + 4], s0);
+            s1 = dp4a_uu(hi, p1[k + 4], s1);
+            s2 = dp4a_us(hi, p2[k + 4], s2);
+        }
+    } else if constexpr (FMT == RF_Q8_0) {
+        s0 = s1 = s2 = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            s0 = dp4a_su(q[k], p0[k], s0);
+            s1 = dp4a_su(q[k], p1[k], s1);
+            s2 = dp4a_ss(q[k], p2[k], s2);
+        }
+    } else {
+        // MXFP4: 2*e2m1 as signed bytes through a byte-permute lookup.
+        // Positive table {0,1,2,3,4,6,8,12}, negative table its negation;
+        // the sign bit of each code picks between them.
+        constexpr uint32_t kPosLo = 0x03020100u, kPosHi = 0x0c080604u;
+        constexpr uint32_t kNegLo = 0xfdfeff00u, kNegHi = 0xf4f8fafcu;
+        s0 = s1 = s2 = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t v = q[k];
+            const uint32_t m = v & 0x77777777u;
+            const uint32_t vs = v << 4;
+            const uint32_t mh = m >> 16;
+            const uint32_t pa = prmt(kPosLo, kPosHi, m), na = prmt(kNegLo, kNegHi, m);
+            const uint32_t sa = prmt(vs, v, 0xd9c8u);   // sign masks of the 4 codes
+            const uint32_t pb = prmt(kPosLo, kPosHi, mh), nb = prmt(kNegLo, kNegHi, mh);
+            const uint32_t sb = prmt(vs, v, 0xfbeau);
+            const uint32_t wa = (pa & ~sa) | (na & sa);
+            const uint32_t wb = (pb & ~sb) | (nb & sb);
+            s0 = dp4a_su(wa, p0[2 * k], s0);
+            s1 = dp4a_su(wa, p1[2 * k], s1);
+            s2 = dp4a_ss(wa, p2[2 * k], s2);
+            s0 = dp4a_su(wb, p0[2 * k + 1], s0);
+            s1 = dp4a_su(wb, p1[2 * k + 1], s1);
+            s2 = dp4a_ss(wb, p2[2 * k + 1], s2);
+        }
+    }
+    return join3(s0, s1, s2);
+}
+
+// Block scale (times the activation block's 2^-s) from the header bits.
+template <int FMT>
+__device__ __forceinline__ float block_scale(uint32_t hdr, float xscale)
+{
+    if constexpr (FMT == RF_MXFP4) {
+        // The lookup holds 2*e2m1, so the scale is 2^(E-128).
+        const uint32_t E = hdr & 0xffu;
+        const uint32_t bits = E >= 2u ? (E - 1u) << 23 : (0x00200000u << E);
+        return __uint_as_float(bits) * xscale;
+    } else {
+        return __half2float(__ushort_as_half((unsigned short)(hdr & 0xffffu))) * xscale;
+    }
+}
+
+__device__ __forceinline__ uint32_t word_at(const uint32_t *v, int byte)
+{
+    const int w = byte >> 2, sh = byte & 3;
+    return sh ? __funnelshift_r(v[w], v[w + 1], 8 * sh) : v[w];
+}
+
+// Aligned chunk: `kn` blocks (a multiple of G) at a 16-byte aligned address.
+template <int FMT>
+__device__ __forceinline__ float chunk_aligned(const uint8_t *src, int kn, const XRec *xr,
+                                               float acc)
+{
+    using F = FmtT<FMT>;
+    constexpr int NV = F::G * F::BS / 16;   // 16-byte units per group of G blocks
+    for (int g0 = 0; g0 < kn; g0 += F::G) {
+        uint32_t v[4 * NV + 1];
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const uint4 t = reinterpret_cast<const uint4 *>(src + g0 * F::BS)[i];
+            v[4 * i] = t.x;
+            v[4 * i + 1] = t.y;
+            v[4 * i + 2] = t.z;
+            v[4 * i + 3] = t.w;
+        }
+        v[4 * NV] = 0;
+#pragma unroll
+        for (int b = 0; b < F::G; ++b) {
+            const int o = b * F::BS;
+            const uint32_t hdr = word_at(v, o);
+            uint32_t q[F::QW];
+#pragma unroll
+            for (int k = 0; k < F::QW; ++k) q[k] = word_at(v, o + F::HDR + 4 * k);
+            const XRec &r = xr[g0 + b];
+            acc = fmaf(block_idot<FMT>(q, r), block_scale<FMT>(hdr, r.scale), acc);
+        }
+    }
+    return acc;
+}
+
+// Any alignment: `kn` blocks starting `phi` bytes into a 16-byte aligned slot.
+template <int FMT>
+__device__ __forceinline__ float chunk_generic(const uint8_t *slot, int phi, int kn,
+                                               const XRec *xr, float acc)
+{
+    using F = FmtT<FMT>;
+    for (int b = 0; b < kn; ++b) {
+        const int o = phi + b * F::BS;
+        uint32_t hdr;
+        if constexpr (FMT == RF_MXFP4)
+            hdr = slot[o];
+        else
+            hdr = *reinterpret_cast<const uint16_t *>(slot + o);   // o is even
+        const int qa = o + F::HDR;
+        const uint32_t *wp = reinterpret_cast<const uint32_t *>(slot + (qa & ~3));
+        const int sh = 8 * (qa & 3);
+        uint32_t w[F::QW + 1];
+#pragma unroll
+        for (int k = 0; k <= F::QW; ++k) w[k] = wp[k];
+        uint32_t q[F::QW];
+#pragma unroll
+        for (int k = 0; k < F::QW; ++k) q[k] = __funnelshift_r(w[k], w[k + 1], sh);
+        const XRec &r = xr[b];
+        acc = fmaf(block_idot<FMT>(q, r), block_scale<FMT>(hdr, r.scale), acc);
+    }
+    return acc;
+}
+
+// Walks the (group, term, chunk) items of one warp in order.
+struct Cursor {
+    int g, j, t, c;
+    bool valid;
+};
+
+__device__ __forceinline__ int groups_of(const Job &J) { return (J.n_rows + kRows - 1) / kRows; }
+
+__device__ __forceinline__ void cursor_fix_job(const KParams &p, Cursor &cu)
+{
+    while (cu.j < p.n_jobs && cu.g >= p.jobs[cu.j].group_begin + groups_of(p.jobs[cu.j])) ++cu.j;
+}
+
+__device__ __forceinline__ void cursor_advance(const KParams &p, Cursor &cu, int n_chunks,
+                                               int g_hi)
+{
+    if (++cu.c < n_chunks) return;
+    cu.c = 0;
+    if (++cu.t < p.jobs[cu.j].n_terms) return;
+    cu.t = 0;
+    if (++cu.g >= g_hi) {
+        cu.valid = false;
+        return;
+    }
+    cursor_fix_job(p, cu);
+}
+
+__device__ __forceinline__ const uint8_t *term_matrix(const KParams &p, const Job &J, int t,
+                                                      int64_t row_bytes)
+{
+    const Term &T = J.term[t];
+    const uint8_t *W = T.W;
+    if (T.expert_slot >= 0) W += (int64_t)p.expert_idx[T.expert_slot] * J.expert_rows * row_bytes;
+    return W;
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads, 1) rowwin_kernel(const __grid_constant__ KParams p)
+{
+    using F = FmtT<FMT>;
+    constexpr int SLOT = slot_bytes<FMT>();
+    extern __shared__ __align__(128) uint8_t smem[];
+
+    const int nb = p.nb;
+    const int ST = p.stages;
+    const int64_t RB = (int64_t)nb * F::BS;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    XRec *xrec = reinterpret_cast<XRec *>(smem);
+    size_t off = (size_t)p.n_x * nb * sizeof(XRec);
+    uint8_t *slots = smem + off;
+    off += (size_t)kNW * ST * kRows * SLOT;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + off);
+    off += (size_t)kNW * ST * sizeof(uint64_t);
+    float *red = reinterpret_cast<float *>(smem + off);
+
+    const int G_total = p.total_groups;
+    const int g_lo = (int)((int64_t)blockIdx.x * G_total / gridDim.x);
+    const int g_hi = (int)((int64_t)(blockIdx.x + 1) * G_total / gridDim.x);
+
+    // This warp's K part, in blocks.
+    const int nG = (nb + F::G - 1) / F::G;
+    const int kb_lo = min(nb, F::G * (warp * nG / kNW));
+    const int kb_hi = min(nb, F::G * ((warp + 1) * nG / kNW));
+    const int n_chunks = (kb_hi - kb_lo + F::KC - 1) / F::KC;
+
+    if (lane < ST) mbar_init(&bars[warp * ST + lane], 32);
+    fence_barrier_init();
+    __syncthreads();
+
+    uint8_t *my_slots = slots + (size_t)warp * ST * kRows * SLOT;
+    uint64_t *my_bars = bars + warp * ST;
+
+    Cursor ic{g_lo, 0, 0, 0, g_lo < g_hi && n_chunks > 0};
+    if (ic.valid) cursor_fix_job(p, ic);
+    long issued = 0;
+
+    auto issue = [&](const Cursor &cu) {
+        const int stage = (int)(issued % ST);
+        uint64_t *bar = &my_bars[stage];
+        const Job &J = p.jobs[cu.j];
+        const int64_t rowrel = (int64_t)(cu.g - J.group_begin) * kRows + lane;
+        if (rowrel < J.n_rows) {
+            const uint8_t *W = term_matrix(p, J, cu.t, RB);
+            const int kb = kb_lo + cu.c * F::KC;
+            const int kn = min(F::KC, kb_hi - kb);
+            const uintptr_t s = reinterpret_cast<uintptr_t>(W + (J.row0 + rowrel) * RB +
+                                                            (int64_t)kb * F::BS);
+            const uintptr_t a = s & ~(uintptr_t)15;
+            const uintptr_t e = (s + (uintptr_t)kn * F::BS + 15) & ~(uintptr_t)15;
+            const uint32_t bytes = (uint32_t)(e - a);
+            mbar_arrive_expect_tx(bar, bytes);
+            bulk_g2s(my_slots + ((size_t)stage * kRows + lane) * SLOT,
+                     reinterpret_cast<const void *>(a), bytes, bar);
+        } else {
+            mbar_arrive(bar);
+        }
+        ++issued;
+    };
+
+    // Weights never depend on the previous kernel: start their copies first
+    // (unless the rows come from a routing result the previous kernel writes).
+    if (p.prefetch_early) {
+        for (int s = 0; s < ST && ic.valid; ++s) {
+            issue(ic);
+            cursor_advance(p, ic, n_chunks, g_hi);
+        }
+    }
+    pdl_launch_dependents();
+    pdl_wait();
+    if (!p.prefetch_early) {
+        for (int s = 0; s < ST && ic.valid; ++s) {
+            issue(ic);
+            cursor_advance(p, ic, n_chunks, g_hi);
+        }
+    }
+
+    // Activation digits for every x of the launch, once per CTA.
+    for (int idx = threadIdx.x; idx < p.n_x * nb; idx += kThreads) {
+        const int s = idx / nb, b = idx - s * nb;
+        make_xrec<FMT>(p.x[s] + 32 * (int64_t)b, &xrec[idx]);
+    }
+    __syncthreads();
+
+    long consumed = 0;
+    int j = 0;
+    for (int g = g_lo; g < g_hi; ++g) {
+        while (j < p.n_jobs && g >= p.jobs[j].group_begin + groups_of(p.jobs[j])) ++j;
+        const Job &J = p.jobs[j];
+        const int64_t rowrel = (int64_t)(g - J.group_begin) * kRows + lane;
+        const bool row_ok = rowrel < J.n_rows;
+        float yacc = 0.f, gate = 0.f;
+        for (int t = 0; t < J.n_terms; ++t) {
+            float acc = 0.f;
+            int phi = 0;
+            if (!J.aligned && row_ok) {
+                const uint8_t *W = term_matrix(p, J, t, RB);
+                phi = (int)(reinterpret_cast<uintptr_t>(W + (J.row0 + rowrel) * RB +
+                                                        (int64_t)kb_lo * F::BS) &
+                            15);
+            }
+            const XRec *xr_row = xrec + (size_t)J.term[t].xslot * nb;
+            for (int c = 0; c < n_chunks; ++c) {
+                const int stage = (int)(consumed % ST);
+                const uint32_t parity = (uint32_t)((consumed / ST) & 1);
+                mbar_wait_bounded(&my_bars[stage], parity, &g_device_status);
+                const uint8_t *slot = my_slots + ((size_t)stage * kRows + lane) * SLOT;
+                const int kb = kb_lo + c * F::KC;
+                const int kn = min(F::KC, kb_hi - kb);
+                // Chunks start at multiples of KC*BS bytes past kb_lo, and
+                // KC*BS is a multiple of 16, so phi is the same for all chunks.
+                if (J.aligned)
+                    acc = chunk_aligned<FMT>(slot, kn, xr_row + kb, acc);
+                else
+                    acc = chunk_generic<FMT>(slot, phi, kn, xr_row + kb, acc);
+                __syncwarp();
+                ++consumed;
+                if (ic.valid) {
+                    issue(ic);
+                    cursor_advance(p, ic, n_chunks, g_hi);
+                }
+            }
+            red[warp * 32 + lane] = acc;
+            __syncthreads();
+            if (warp == 0) {
+                float dot = red[lane];
+#pragma unroll
+                for (int w = 1; w < kNW; ++w) dot += red[w * 32 + lane];
+                if (J.combine == kCombineSwiGLU) {
+                    if (t == 0)
+                        gate = dot;
+                    else
+                        yacc = gate / (1.f + expf(-gate)) * dot;
+                } else if (J.weights) {
+                    yacc = fmaf(J.weights[t], dot, yacc);
+                } else {
+                    yacc = t == 0 ? dot : yacc + dot;
+                }
+            }
+            __syncthreads();
+        }
+        if (warp == 0 && row_ok) {
+            float out = yacc;
+            if (J.act == kActGelu) out = 0.5f * out * (1.f + erff(out * 0.70710678118654752f));
+            J.y[rowrel] = out;
+        }
+    }
+}
+
+int g_max_smem[64];
+std::once_flag g_smem_once[64];
+
+int max_smem_optin(int dev)
+{
+    std::call_once(g_smem_once[dev & 63], [dev] {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        g_max_smem[dev & 63] = v;
+    });
+    return g_max_smem[dev & 63];
+}
+
+template <int FMT>
+size_t smem_bytes(int n_x, int nb, int stages)
+{
+    return (size_t)n_x * nb * sizeof(XRec) + (size_t)kNW * stages * kRows * slot_bytes<FMT>() +
+           (size_t)kNW * stages * sizeof(uint64_t) + (size_t)kNW * 32 * sizeof(float);
+}
+
+size_t smem_for(int fmt, int n_x, int nb, int stages)
+{
+    switch (fmt) {
+    case RF_Q4_0: return smem_bytes<RF_Q4_0>(n_x, nb, stages);
+    case RF_Q8_0: return smem_bytes<RF_Q8_0>(n_x, nb, stages);
+    default: return smem_bytes<RF_MXFP4>(n_x, nb, stages);
+    }
+}
+
+template <int FMT>
+rf_status launch_fmt(const KParams &p, int grid, size_t smem, bool pdl, cudaStream_t stream)
+{
+    static std::once_flag attr_once[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int maxs = max_smem_optin(dev);
+    std::call_once(attr_once[dev & 63], [maxs] {
+        cudaFuncSetAttribute(rowwin_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, maxs);
+    });
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    if (cudaLaunchKernelEx(&cfg, rowwin_kernel<FMT>, p) != cudaSuccess) return RF_ERR_CUDA;
+    return RF_OK;
+}
+
+}  // namespace
+
+rf_status read_and_clear_device_status()
+{
+    if (cudaDeviceSynchronize() != cudaSuccess) return RF_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) return RF_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess)
+            return RF_ERR_CUDA;
+    }
+    return static_cast<rf_status>(v);
+}
+
+bool fmt_ok(int fmt) { return fmt == RF_Q4_0 || fmt == RF_Q8_0 || fmt == RF_MXFP4; }
+
+size_t block_bytes_of(int fmt)
+{
+    switch (fmt) {
+    case RF_Q4_0: return 18;
+    case RF_Q8_0: return 34;
+    case RF_MXFP4: return 17;
+    default: return 0;
+    }
+}
+
+rf_status last_cuda_error() { return cudaGetLastError() == cudaSuccess ? RF_OK : RF_ERR_CUDA; }
+
+int num_sms()
+{
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+}
+
+int64_t max_in_dim(int fmt, int n_x)
+{
+    if (!fmt_ok(fmt) || n_x < 1 || n_x > kMaxX) return 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    const size_t maxs = (size_t)max_smem_optin(dev);
+    const size_t fixed = smem_for(fmt, n_x, 0, 1);
+    if (maxs <= fixed) return 0;
+    return (int64_t)((maxs - fixed) / ((size_t)n_x * sizeof(XRec))) * 32;
+}
+
+rf_status launch_rowwin(const LaunchDesc &d, cudaStream_t stream)
+{
+    if (!fmt_ok(d.fmt)) return RF_ERR_UNSUPPORTED_FMT;
+    if (d.in_dim <= 0 || d.in_dim % 32 != 0) return RF_ERR_INVALID_ARG;
+    if (d.n_jobs < 0 || d.n_x < 1 || d.n_x > kMaxX) return RF_ERR_INVALID_ARG;
+    if (d.n_jobs > 0 && !d.jobs) return RF_ERR_INVALID_ARG;
+    for (int s = 0; s < d.n_x; ++s)
+        if (!d.x[s]) return RF_ERR_INVALID_ARG;
+    if (d.any_expert && !d.expert_idx) return RF_ERR_INVALID_ARG;
+    const int64_t nb64 = d.in_dim / 32;
+    if (nb64 > (1 << 24)) return RF_ERR_TOO_LARGE;
+    const int nb = (int)nb64;
+    const int64_t RB = nb64 * (int64_t)block_bytes_of(d.fmt);
+
+    // Validate every job before enqueueing anything.
+    for (int i = 0; i < d.n_jobs; ++i) {
+        const Job &J = d.jobs[i];
+        if (J.n_rows < 0 || J.row0 < 0 || J.n_terms < 1 || J.n_terms > kMaxTerms)
+            return RF_ERR_INVALID_ARG;
+        if (J.n_rows > 0 && !J.y) return RF_ERR_INVALID_ARG;
+        if (J.combine == kCombineSwiGLU && J.n_terms != 2) return RF_ERR_INVALID_ARG;
+        for (int t = 0; t < J.n_terms; ++t) {
+            const Term &T = J.term[t];
+            if (!T.W) return RF_ERR_INVALID_ARG;
+            if ((reinterpret_cast<uintptr_t>(T.W) & 15u) != 0) return RF_ERR_MISALIGNED;
+            if (T.xslot < 0 || T.xslot >= d.n_x) return RF_ERR_INVALID_ARG;
+            if (T.expert_slot >= kMaxTerms) return RF_ERR_INVALID_ARG;
+            if (T.expert_slot >= 0 && (!d.expert_idx || J.expert_rows <= 0))
+                return RF_ERR_INVALID_ARG;
+        }
+    }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return RF_ERR_CUDA;
+    }
+    const size_t maxs = (size_t)max_smem_optin(dev);
+    if (maxs == 0) return RF_ERR_CUDA;
+    int stages = 3;
+    while (stages > 0 && smem_for(d.fmt, d.n_x, nb, stages) > maxs) --stages;
+    if (stages == 0) return RF_ERR_TOO_LARGE;
+    const size_t smem = smem_for(d.fmt, d.n_x, nb, stages);
+    const int sms = num_sms();
+
+    // Launch in batches of kMaxJobs windows.
+    for (int base = 0; base < d.n_jobs; base += kMaxJobs) {
+        static thread_local KParams p;   // large (about 13 KB): keep it off the stack
+        std::memset(&p, 0, sizeof(p));
+        const int nj = std::min(kMaxJobs, d.n_jobs - base);
+        int total = 0;
+        for (int i = 0; i < nj; ++i) {
+            p.jobs[i] = d.jobs[base + i];
+            p.jobs[i].group_begin = total;
+            p.jobs[i].aligned = (RB % 16 == 0) ? 1 : 0;
+            total += (p.jobs[i].n_rows + kRows - 1) / kRows;
+        }
+        if (total == 0) continue;
+        for (int s = 0; s < d.n_x; ++s) p.x[s] = d.x[s];
+        p.expert_idx = d.expert_idx;
+        p.n_jobs = nj;
+        p.n_x = d.n_x;
+        p.nb = nb;
+        p.total_groups = total;
+        p.stages = stages;
+        p.prefetch_early = d.any_expert ? 0 : 1;
+        const int grid = std::min(total, sms);
+        rf_status st;
+        switch (d.fmt) {
+        case RF_Q4_0: st = launch_fmt<RF_Q4_0>(p, grid, smem, d.pdl, stream); break;
+        case RF_Q8_0: st = launch_fmt<RF_Q8_0>(p, grid, smem, d.pdl, stream); break;
+        default: st = launch_fmt<RF_MXFP4>(p, grid, smem, d.pdl, stream); break;
+        }
+        if (st != RF_OK) return st;
+    }
+    return RF_OK;
+}
+
+}  // namespace rf

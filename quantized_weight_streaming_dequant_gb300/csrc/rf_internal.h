@@ -1,0 +1,72 @@
+// rf_internal.h -- host-side interface between the C ABI entry points and the
+// row-window GEMV launcher.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "rf.h"
+
+namespace rf {
+
+constexpr int kMaxTerms = 8;   // matrices combined per output row (top-k of a MoE down)
+constexpr int kMaxJobs = 64;   // row windows per launch
+constexpr int kMaxX = 8;       // distinct activation vectors per launch
+
+// How the per-term row dots of a job become the output row.
+enum Combine : int32_t {
+    kCombineSum = 0,     // y = sum_t weight_t * dot_t (weight 1 when weights == nullptr)
+    kCombineSwiGLU = 1,  // y = silu(dot_0) * dot_1  (gate, up)
+};
+enum Act : int32_t { kActNone = 0, kActGelu = 1 };
+
+struct Term {
+    const uint8_t *W;     // row 0 of the matrix (or of the stacked tensor)
+    int32_t xslot;        // which activation vector multiplies this matrix
+    int32_t expert_slot;  // >= 0: add expert_idx[expert_slot]*expert_rows rows to W
+};
+
+// One window of rows [row0, row0+n_rows) taken from every term's matrix.
+struct Job {
+    Term term[kMaxTerms];
+    float *y;               // n_rows outputs
+    const float *weights;   // per-term weights (device) for kCombineSum, or nullptr
+    int64_t row0;
+    int64_t expert_rows;
+    int32_t n_rows;
+    int32_t n_terms;
+    int32_t combine;
+    int32_t act;
+    int32_t group_begin;    // filled by the launcher
+    int32_t aligned;        // filled by the launcher
+};
+
+struct LaunchDesc {
+    int fmt = 0;
+    int64_t in_dim = 0;
+    const Job *jobs = nullptr;
+    int n_jobs = 0;
+    const float *x[kMaxX] = {};
+    int n_x = 0;
+    const int32_t *expert_idx = nullptr;   // device, for expert_slot terms
+    bool pdl = false;                      // programmatic dependent launch
+    bool any_expert = false;               // some term resolves an expert on device
+};
+
+// Validates and launches the row-window GEMV kernel (in batches of kMaxJobs
+// windows).  Host-side argument checks return an error before anything is
+// enqueued.
+rf_status launch_rowwin(const LaunchDesc &d, cudaStream_t stream);
+
+bool fmt_ok(int fmt);
+size_t block_bytes_of(int fmt);
+rf_status last_cuda_error();
+rf_status read_and_clear_device_status();
+int num_sms();
+int64_t max_in_dim(int fmt, int n_x);
+
+rf_status launch_router(const float *logits, int n_expert, int top_k, int32_t *idx, float *w,
+                        cudaStream_t stream);
+
+}  // namespace rf

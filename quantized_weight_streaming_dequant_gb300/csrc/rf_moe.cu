@@ -1,0 +1,223 @@
+// rf_moe.cu -- device top-k router and the routed MoE SwiGLU FFN.
+//
+// neurostream, "How it works" 2: the router runs first and names the experts
+// this token needs; only those are read.  "The idea": expert e owns rows
+// [e*out, (e+1)*out) of each stacked (n_expert, out, in) tensor and is walked
+// in row windows of block_rows rows like any other projection.  The routing
+// result stays on the device: the GEMV launches resolve expert ids from it,
+// so there is no host synchronisation between routing and the projections.
+#include <cfloat>
+#include <cstring>
+
+#include "rf_device.cuh"
+#include "rf_internal.h"
+
+namespace rf {
+namespace {
+
+constexpr int kRouterThreads = 1024;
+constexpr int kMaxTopK = kMaxTerms;
+
+// One CTA: k rounds of a block-wide argmax (largest logit, lowest index on
+// ties), then a softmax over the k selected logits.
+__global__ void __launch_bounds__(kRouterThreads) router_kernel(const float *__restrict__ logits,
+                                                                int n_expert, int top_k,
+                                                                int32_t *__restrict__ idx,
+                                                                float *__restrict__ w)
+{
+    __shared__ float s_val[32];
+    __shared__ int s_idx[32];
+    __shared__ int s_sel[kMaxTopK];
+    __shared__ float s_logit[kMaxTopK];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int n_warps = blockDim.x >> 5;
+    const float v0 = tid < n_expert ? logits[tid] : -FLT_MAX;
+    bool taken = tid >= n_expert;
+    for (int k = 0; k < top_k; ++k) {
+        float v = taken ? -INFINITY : v0;
+        int i = taken ? 0x7fffffff : tid;
+        // (v, i) beats (v2, i2) if v > v2, or v == v2 and i < i2.
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
+            const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
+            if (v2 > v || (v2 == v && i2 < i)) {
+                v = v2;
+                i = i2;
+            }
+        }
+        if (lane == 0) {
+            s_val[warp] = v;
+            s_idx[warp] = i;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            v = lane < n_warps ? s_val[lane] : -INFINITY;
+            i = lane < n_warps ? s_idx[lane] : 0x7fffffff;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
+                const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
+                if (v2 > v || (v2 == v && i2 < i)) {
+                    v = v2;
+                    i = i2;
+                }
+            }
+            if (lane == 0) {
+                s_sel[k] = i;
+                s_logit[k] = v;
+            }
+        }
+        __syncthreads();
+        if (tid == s_sel[k]) taken = true;
+    }
+    if (tid == 0) {
+        const float m = s_logit[0];
+        float e[kMaxTopK];
+        float sum = 0.f;
+        for (int k = 0; k < top_k; ++k) {
+            e[k] = expf(s_logit[k] - m);
+            sum += e[k];
+        }
+        for (int k = 0; k < top_k; ++k) {
+            idx[k] = s_sel[k];
+            w[k] = e[k] / sum;
+        }
+    }
+}
+
+size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
+
+}  // namespace
+
+rf_status launch_router(const float *logits, int n_expert, int top_k, int32_t *idx, float *w,
+                        cudaStream_t stream)
+{
+    if (!logits || !idx || !w) return RF_ERR_INVALID_ARG;
+    if (n_expert < 1 || n_expert > kRouterThreads || top_k < 1 || top_k > kMaxTopK ||
+        top_k > n_expert)
+        return RF_ERR_INVALID_ARG;
+    const int threads = ((n_expert + 31) / 32) * 32;
+    router_kernel<<<1, threads, 0, stream>>>(logits, n_expert, top_k, idx, w);
+    return last_cuda_error();
+}
+
+}  // namespace rf
+
+using namespace rf;
+
+extern "C" {
+
+rf_status rf_moe_route(const float *logits, int n_expert, int top_k, int32_t *idx, float *w,
+                       void *stream)
+{
+    return launch_router(logits, n_expert, top_k, idx, w, static_cast<cudaStream_t>(stream));
+}
+
+size_t rf_moe_workspace_bytes(int top_k, int64_t n_ff, int64_t n_embd, int64_t block_rows)
+{
+    (void)n_embd;
+    (void)block_rows;
+    if (top_k < 1 || top_k > kMaxTopK || n_ff <= 0) return 0;
+    return align256(sizeof(int32_t) * kMaxTopK) + align256(sizeof(float) * kMaxTopK) +
+           align256(sizeof(float) * (size_t)top_k * (size_t)n_ff);
+}
+
+rf_status rf_moe_ffn(int fmt, const float *router_logits, int n_expert, int top_k,
+                     const void *gate, const void *up, const void *down, int64_t n_ff,
+                     int64_t n_embd, int64_t block_rows, const float *x, float *y,
+                     void *workspace, void *stream)
+{
+    if (!fmt_ok(fmt)) return RF_ERR_UNSUPPORTED_FMT;
+    if (!router_logits || !gate || !up || !down || !x || !y || !workspace)
+        return RF_ERR_INVALID_ARG;
+    if (n_expert < 1 || n_expert > kRouterThreads || top_k < 1 || top_k > kMaxTopK ||
+        top_k > n_expert)
+        return RF_ERR_INVALID_ARG;
+    if (n_ff <= 0 || n_embd <= 0 || n_ff % 32 != 0 || n_embd % 32 != 0 || block_rows < 0)
+        return RF_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return RF_ERR_MISALIGNED;
+    for (const void *p : {gate, up, down})
+        if ((reinterpret_cast<uintptr_t>(p) & 15u) != 0) return RF_ERR_MISALIGNED;
+    if ((int64_t)n_expert * n_ff > 0x7fffffffLL || (int64_t)n_expert * n_embd > 0x7fffffffLL)
+        return RF_ERR_TOO_LARGE;
+    if (n_embd > max_in_dim(fmt, 1) || n_ff > max_in_dim(fmt, top_k)) return RF_ERR_TOO_LARGE;
+
+    const int64_t br_ff = block_rows == 0 ? n_ff : block_rows;
+    const int64_t br_embd = block_rows == 0 ? n_embd : block_rows;
+    const int64_t win_ff = (n_ff + br_ff - 1) / br_ff;
+    const int64_t win_embd = (n_embd + br_embd - 1) / br_embd;
+    if (top_k * win_ff > 4 * kMaxJobs || win_embd > 4 * kMaxJobs) return RF_ERR_TOO_LARGE;
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    int32_t *idx = reinterpret_cast<int32_t *>(ws);
+    float *wts = reinterpret_cast<float *>(ws + align256(sizeof(int32_t) * kMaxTopK));
+    float *h = reinterpret_cast<float *>(ws + align256(sizeof(int32_t) * kMaxTopK) +
+                                         align256(sizeof(float) * kMaxTopK));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    rf_status st = launch_router(router_logits, n_expert, top_k, idx, wts, s);
+    if (st != RF_OK) return st;
+
+    // Gate/up: one job per (selected expert k, row window j); the SwiGLU
+    // epilogue writes h_k[window].
+    static thread_local Job jobs[4 * kMaxJobs];
+    int nj = 0;
+    for (int k = 0; k < top_k; ++k) {
+        for (int64_t j = 0; j < win_ff; ++j) {
+            Job &J = jobs[nj++];
+            std::memset(&J, 0, sizeof(J));
+            const int64_t r0 = j * br_ff;
+            J.term[0] = Term{static_cast<const uint8_t *>(gate), 0, k};
+            J.term[1] = Term{static_cast<const uint8_t *>(up), 0, k};
+            J.y = h + (int64_t)k * n_ff + r0;
+            J.row0 = r0;
+            J.expert_rows = n_ff;
+            J.n_rows = (int32_t)(r0 + br_ff < n_ff ? br_ff : n_ff - r0);
+            J.n_terms = 2;
+            J.combine = kCombineSwiGLU;
+        }
+    }
+    LaunchDesc d1;
+    d1.fmt = fmt;
+    d1.in_dim = n_embd;
+    d1.jobs = jobs;
+    d1.n_jobs = nj;
+    d1.x[0] = x;
+    d1.n_x = 1;
+    d1.expert_idx = idx;
+    d1.any_expert = true;
+    d1.pdl = true;
+    st = launch_rowwin(d1, s);
+    if (st != RF_OK) return st;
+
+    // Down: one job per output row window with one term per selected expert;
+    // y = sum_k w_k * down_k . h_k in selection order.
+    nj = 0;
+    for (int64_t j = 0; j < win_embd; ++j) {
+        Job &J = jobs[nj++];
+        std::memset(&J, 0, sizeof(J));
+        const int64_t r0 = j * br_embd;
+        for (int k = 0; k < top_k; ++k) J.term[k] = Term{static_cast<const uint8_t *>(down), k, k};
+        J.y = y + r0;
+        J.weights = wts;
+        J.row0 = r0;
+        J.expert_rows = n_embd;
+        J.n_rows = (int32_t)(r0 + br_embd < n_embd ? br_embd : n_embd - r0);
+        J.n_terms = top_k;
+        J.combine = kCombineSum;
+    }
+    LaunchDesc d2;
+    d2.fmt = fmt;
+    d2.in_dim = n_ff;
+    d2.jobs = jobs;
+    d2.n_jobs = nj;
+    for (int k = 0; k < top_k; ++k) d2.x[k] = h + (int64_t)k * n_ff;
+    d2.n_x = top_k;
+    d2.expert_idx = idx;
+    d2.any_expert = true;
+    d2.pdl = true;
+    return launch_rowwin(d2, s);
+}
+
+}  // extern "C"

@@ -1,0 +1,249 @@
+// rf_stream.cu -- bounded device arena and host-streamed row windows.
+//
+// neurostream, "How it works":
+//   3. the BlockPrefetcher keeps `depth` blocks in flight and refills as each
+//      retires;
+//   4. stream_linear walks a row window: read a block, multiply, accumulate,
+//      retire it, take the next;
+//   6. every in-flight block holds an arena reservation, and allocation waits
+//      until one retires (back-pressure instead of a runaway prefetcher).
+// "Bugs worth knowing about": the block being multiplied keeps its lease until
+// its output exists, so the pipeline holds depth+1 blocks.
+//
+// GB300 form: the arena is one device allocation cut into depth+1 slots.  The
+// prefetcher is a dedicated copy stream; each block is a cudaMemcpyAsync from
+// page-locked host memory into its slot, followed by an event that the compute
+// stream waits on before the fused GEMV reads the slot.  After the GEMV a
+// "slot free" event is recorded on the compute stream; the copy that next
+// reuses the slot waits on it.  Reservations and back-pressure are therefore
+// stream-ordered dependencies: the host enqueues a whole walk without
+// blocking, and consecutive calls keep the copy engine busy across call
+// boundaries (no drain between projections).
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "rf_internal.h"
+
+using namespace rf;
+
+struct rf_arena {
+    static constexpr int kMaxSlots = 65;   // depth <= 64
+    uint8_t *base = nullptr;
+    size_t bytes = 0;          // capacity promised to the caller
+    size_t alloc_bytes = 0;    // allocation (capacity + alignment slack)
+    int device = 0;
+    cudaStream_t copy_stream = nullptr;
+    cudaEvent_t copied[kMaxSlots] = {};
+    cudaEvent_t freed[kMaxSlots] = {};
+    bool freed_recorded[kMaxSlots] = {};
+    int next_slot = 0;
+    int last_slots = 0;
+    size_t last_stride = 0;
+    rf_stream_stats stats = {};
+    std::mutex mu;
+};
+
+namespace {
+
+int64_t plan_rows(int64_t row_bytes, int64_t n_rows, int64_t block_rows, int depth,
+                  size_t arena_bytes)
+{
+    int64_t want = (block_rows == 0 || block_rows > n_rows) ? n_rows : block_rows;
+    if (want < 1) want = 1;
+    const int64_t fit = (int64_t)(arena_bytes / ((size_t)(depth + 1) * (size_t)row_bytes));
+    if (fit < 1) return -1;
+    return std::min(want, fit);
+}
+
+}  // namespace
+
+extern "C" {
+
+rf_status rf_stream_plan(int fmt, int64_t in_dim, int64_t n_rows, int64_t block_rows, int depth,
+                         size_t arena_bytes, int64_t *eff_rows, int64_t *n_blocks,
+                         size_t *peak_bytes)
+{
+    if (!fmt_ok(fmt)) return RF_ERR_UNSUPPORTED_FMT;
+    if (in_dim <= 0 || in_dim % 32 != 0 || n_rows < 0 || block_rows < 0 || depth < 0 ||
+        depth > rf_arena::kMaxSlots - 1)
+        return RF_ERR_INVALID_ARG;
+    const int64_t rb = (in_dim / 32) * (int64_t)block_bytes_of(fmt);
+    const int64_t eff = plan_rows(rb, n_rows, block_rows, depth, arena_bytes);
+    if (eff < 0) return RF_ERR_ARENA_TOO_SMALL;
+    const int64_t nblk = n_rows == 0 ? 0 : (n_rows + eff - 1) / eff;
+    // Peak: the bytes of a block being multiplied plus the depth blocks
+    // fetched ahead of it, maximised over the walk.
+    size_t peak = 0;
+    for (int64_t i = 0; i < nblk; ++i) {
+        size_t held = 0;
+        for (int64_t k = i; k < std::min(nblk, i + depth + 1); ++k)
+            held += (size_t)(std::min(eff, n_rows - k * eff) * rb);
+        peak = std::max(peak, held);
+        if (i + depth + 1 >= nblk) break;   // later windows are subsets
+    }
+    if (eff_rows) *eff_rows = eff;
+    if (n_blocks) *n_blocks = nblk;
+    if (peak_bytes) *peak_bytes = peak;
+    return RF_OK;
+}
+
+rf_status rf_arena_create(size_t bytes, rf_arena **out)
+{
+    if (!out || bytes == 0) return RF_ERR_INVALID_ARG;
+    *out = nullptr;
+    rf_arena *a = new (std::nothrow) rf_arena();
+    if (!a) return RF_ERR_OOM;
+    if (cudaGetDevice(&a->device) != cudaSuccess) {
+        cudaGetLastError();
+        delete a;
+        return RF_ERR_CUDA;
+    }
+    // Slack for rounding every slot up to 256 bytes.
+    a->bytes = bytes;
+    a->alloc_bytes = bytes + 256 * rf_arena::kMaxSlots;
+    if (cudaMalloc(&a->base, a->alloc_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        delete a;
+        return RF_ERR_OOM;
+    }
+    if (cudaStreamCreateWithFlags(&a->copy_stream, cudaStreamNonBlocking) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(a->base);
+        delete a;
+        return RF_ERR_CUDA;
+    }
+    for (int i = 0; i < rf_arena::kMaxSlots; ++i) {
+        if (cudaEventCreateWithFlags(&a->copied[i], cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&a->freed[i], cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();
+            rf_arena_destroy(a);
+            return RF_ERR_CUDA;
+        }
+    }
+    a->stats.arena_bytes = bytes;
+    *out = a;
+    return RF_OK;
+}
+
+void rf_arena_destroy(rf_arena *a)
+{
+    if (!a) return;
+    int prev = 0;
+    cudaGetDevice(&prev);
+    cudaSetDevice(a->device);
+    // Copies may still be writing the arena and GEMVs may still read it:
+    // wait for both before freeing.
+    if (a->copy_stream) cudaStreamSynchronize(a->copy_stream);
+    for (int i = 0; i < rf_arena::kMaxSlots; ++i) {
+        if (a->freed[i]) {
+            if (a->freed_recorded[i]) cudaEventSynchronize(a->freed[i]);
+            cudaEventDestroy(a->freed[i]);
+        }
+        if (a->copied[i]) cudaEventDestroy(a->copied[i]);
+    }
+    if (a->copy_stream) cudaStreamDestroy(a->copy_stream);
+    if (a->base) cudaFree(a->base);
+    cudaSetDevice(prev);
+    delete a;
+}
+
+rf_status rf_stream_stats_get(const rf_arena *a, rf_stream_stats *out)
+{
+    if (!a || !out) return RF_ERR_INVALID_ARG;
+    *out = a->stats;
+    return RF_OK;
+}
+
+rf_status rf_stream_linear(int fmt, const void *host_W, int64_t in_dim, int64_t row_start,
+                           int64_t row_end, int64_t block_rows, int depth, rf_arena *a,
+                           const float *x, float *y, void *stream)
+{
+    if (!fmt_ok(fmt)) return RF_ERR_UNSUPPORTED_FMT;
+    if (!host_W || !a || !x || !y || in_dim <= 0 || in_dim % 32 != 0 || row_start < 0 ||
+        row_end < row_start || block_rows < 0 || depth < 0 || depth > rf_arena::kMaxSlots - 1)
+        return RF_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(host_W) & 15u) != 0) return RF_ERR_MISALIGNED;
+    if (in_dim > max_in_dim(fmt, 1)) return RF_ERR_TOO_LARGE;
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, host_W) != cudaSuccess) {
+        cudaGetLastError();
+        return RF_ERR_NOT_PINNED;
+    }
+    if (attr.type != cudaMemoryTypeHost) return RF_ERR_NOT_PINNED;
+    const int64_t n_rows = row_end - row_start;
+    const int64_t rb = (in_dim / 32) * (int64_t)block_bytes_of(fmt);
+    const int64_t eff = plan_rows(rb, std::max<int64_t>(n_rows, 1), block_rows, depth, a->bytes);
+    if (eff < 0) return RF_ERR_ARENA_TOO_SMALL;
+    if (n_rows == 0) return RF_OK;
+    if (eff > 0x7fffffffLL) return RF_ERR_TOO_LARGE;
+
+    std::lock_guard<std::mutex> lock(a->mu);
+    const int slots = depth + 1;
+    const size_t stride = ((size_t)(eff * rb) + 255) & ~(size_t)255;
+    if ((size_t)slots * stride > a->alloc_bytes) return RF_ERR_ARENA_TOO_SMALL;
+    // A new slot layout overlaps the old one: the copy stream first waits for
+    // every old slot's last reader.
+    if (a->last_slots != slots || a->last_stride != stride) {
+        for (int i = 0; i < rf_arena::kMaxSlots; ++i)
+            if (a->freed_recorded[i] &&
+                cudaStreamWaitEvent(a->copy_stream, a->freed[i], 0) != cudaSuccess)
+                return RF_ERR_CUDA;
+        a->next_slot = 0;
+        a->last_slots = slots;
+        a->last_stride = stride;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const uint8_t *hw = static_cast<const uint8_t *>(host_W);
+    size_t peak = 0;
+    rf_stream_plan(fmt, in_dim, n_rows, block_rows, depth, a->bytes, nullptr, nullptr, &peak);
+
+    int64_t blocks = 0;
+    for (int64_t r0 = row_start; r0 < row_end; r0 += eff) {
+        const int64_t nr = std::min(eff, row_end - r0);
+        const int slot = a->next_slot;
+        a->next_slot = (a->next_slot + 1) % slots;
+        uint8_t *dst = a->base + (size_t)slot * stride;
+        const size_t bytes = (size_t)(nr * rb);
+        // Reservation: the slot's previous GEMV must have finished reading it.
+        if (a->freed_recorded[slot] &&
+            cudaStreamWaitEvent(a->copy_stream, a->freed[slot], 0) != cudaSuccess)
+            return RF_ERR_CUDA;
+        if (cudaMemcpyAsync(dst, hw + r0 * rb, bytes, cudaMemcpyHostToDevice, a->copy_stream) !=
+                cudaSuccess ||
+            cudaEventRecord(a->copied[slot], a->copy_stream) != cudaSuccess ||
+            cudaStreamWaitEvent(s, a->copied[slot], 0) != cudaSuccess)
+            return RF_ERR_CUDA;
+        Job J;
+        std::memset(&J, 0, sizeof(J));
+        J.term[0] = Term{dst, 0, -1};
+        J.y = y + (r0 - row_start);
+        J.n_rows = (int32_t)nr;
+        J.n_terms = 1;
+        J.combine = kCombineSum;
+        LaunchDesc d;
+        d.fmt = fmt;
+        d.in_dim = in_dim;
+        d.jobs = &J;
+        d.n_jobs = 1;
+        d.x[0] = x;
+        d.n_x = 1;
+        const rf_status st = launch_rowwin(d, s);
+        if (st != RF_OK) return st;
+        // Retire: the slot is free once this GEMV has run.
+        if (cudaEventRecord(a->freed[slot], s) != cudaSuccess) return RF_ERR_CUDA;
+        a->freed_recorded[slot] = true;
+        a->stats.bytes_copied += bytes;
+        ++blocks;
+    }
+    a->stats.calls += 1;
+    a->stats.blocks += (uint64_t)blocks;
+    a->stats.peak_bytes = std::max<uint64_t>(a->stats.peak_bytes, peak);
+    a->stats.slot_bytes = stride;
+    a->stats.slots = slots;
+    a->stats.last_block_rows = (int32_t)eff;
+    return RF_OK;
+}
+
+}  // extern "C"
