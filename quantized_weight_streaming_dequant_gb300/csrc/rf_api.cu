@@ -150,7 +150,7 @@ rf_status rf_gemv(int fmt, const void *W, int64_t row_start, int64_t row_end, in
     if ((reinterpret_cast<uintptr_t>(W) & 15u) != 0) return RF_ERR_MISALIGNED;
     if (row_end - row_start > 0x7fffffffLL) return RF_ERR_TOO_LARGE;
     if (row_end == row_start) return RF_OK;
-    if (in_dim > max_in_dim(fmt, 1)) return RF_ERR_TOO_LARGE;
+    if (const rf_status c = check_in_dim(fmt, in_dim, 1)) return c;
     Job J;
     std::memset(&J, 0, sizeof(J));
     J.term[0] = Term{static_cast<const uint8_t *>(W), 0, -1};
@@ -204,7 +204,7 @@ rf_status rf_gemv_batch(int fmt, int64_t in_dim, int n_windows, const rf_window 
         jobs[i].combine = kCombineSum;
     }
     if (n_windows == 0) return RF_OK;
-    if (in_dim > max_in_dim(fmt, n_x)) return RF_ERR_TOO_LARGE;
+    if (const rf_status c = check_in_dim(fmt, in_dim, n_x)) return c;
     d.jobs = jobs;
     d.n_jobs = n_windows;
     d.n_x = n_x;
@@ -238,7 +238,8 @@ rf_status rf_ffn_swiglu(int fmt, const void *gate, const void *up, const void *d
     if (n_ff > 0x7fffffffLL || n_embd > 0x7fffffffLL) return RF_ERR_TOO_LARGE;
     for (const void *p : {gate, up, down})
         if ((reinterpret_cast<uintptr_t>(p) & 15u) != 0) return RF_ERR_MISALIGNED;
-    if (n_embd > max_in_dim(fmt, 1) || n_ff > max_in_dim(fmt, 1)) return RF_ERR_TOO_LARGE;
+    if (const rf_status c = check_in_dim(fmt, n_embd, 1)) return c;
+    if (const rf_status c = check_in_dim(fmt, n_ff, 1)) return c;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // Phase 1: walk gate and up by neuron; SwiGLU in the epilogue.
     Job J;

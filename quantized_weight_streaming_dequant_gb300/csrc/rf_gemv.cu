@@ -617,6 +617,13 @@ int64_t max_in_dim(int fmt, int n_x)
     return (int64_t)((maxs - fixed) / ((size_t)n_x * sizeof(XRec))) * 32;
 }
 
+rf_status check_in_dim(int fmt, int64_t in_dim, int n_x)
+{
+    const int64_t m = max_in_dim(fmt, n_x);
+    if (m == 0) return RF_ERR_CUDA;
+    return in_dim > m ? RF_ERR_TOO_LARGE : RF_OK;
+}
+
 rf_status launch_rowwin(const LaunchDesc &d, cudaStream_t stream)
 {
     if (!fmt_ok(d.fmt)) return RF_ERR_UNSUPPORTED_FMT;

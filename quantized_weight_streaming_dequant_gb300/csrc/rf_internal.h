@@ -65,6 +65,8 @@ rf_status last_cuda_error();
 rf_status read_and_clear_device_status();
 int num_sms();
 int64_t max_in_dim(int fmt, int n_x);
+// RF_OK, RF_ERR_TOO_LARGE (in_dim above max_in_dim) or RF_ERR_CUDA (no device).
+rf_status check_in_dim(int fmt, int64_t in_dim, int n_x);
 
 rf_status launch_router(const float *logits, int n_expert, int top_k, int32_t *idx, float *w,
                         cudaStream_t stream);

@@ -141,7 +141,8 @@ rf_status rf_moe_ffn(int fmt, const float *router_logits, int n_expert, int top_
         if ((reinterpret_cast<uintptr_t>(p) & 15u) != 0) return RF_ERR_MISALIGNED;
     if ((int64_t)n_expert * n_ff > 0x7fffffffLL || (int64_t)n_expert * n_embd > 0x7fffffffLL)
         return RF_ERR_TOO_LARGE;
-    if (n_embd > max_in_dim(fmt, 1) || n_ff > max_in_dim(fmt, top_k)) return RF_ERR_TOO_LARGE;
+    if (const rf_status c = check_in_dim(fmt, n_embd, 1)) return c;
+    if (const rf_status c = check_in_dim(fmt, n_ff, top_k)) return c;
 
     const int64_t br_ff = block_rows == 0 ? n_ff : block_rows;
     const int64_t br_embd = block_rows == 0 ? n_embd : block_rows;

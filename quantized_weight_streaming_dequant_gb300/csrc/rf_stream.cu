@@ -165,7 +165,7 @@ rf_status rf_stream_linear(int fmt, const void *host_W, int64_t in_dim, int64_t 
         row_end < row_start || block_rows < 0 || depth < 0 || depth > rf_arena::kMaxSlots - 1)
         return RF_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(host_W) & 15u) != 0) return RF_ERR_MISALIGNED;
-    if (in_dim > max_in_dim(fmt, 1)) return RF_ERR_TOO_LARGE;
+    if (const rf_status c = check_in_dim(fmt, in_dim, 1)) return c;
     cudaPointerAttributes attr;
     if (cudaPointerGetAttributes(&attr, host_W) != cudaSuccess) {
         cudaGetLastError();

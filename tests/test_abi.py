@@ -1,0 +1,129 @@
+"""The C ABI library: loads, exports every declared symbol, and its host-side
+logic (sizes, block planning, argument validation) -- no GPU needed."""
+import ctypes
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+import quantized_weight_streaming_dequant_gb300 as rf
+
+FMTS = [rf.Q8_0, rf.Q4_0, rf.MXFP4]
+
+
+@pytest.fixture(scope="module")
+def L():
+    from quantized_weight_streaming_dequant_gb300 import build
+    build.build()
+    return rf.lib()
+
+
+def has_gpu():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+def test_exports_every_declared_symbol(L):
+    declared = rf.header_symbols()
+    assert len(declared) >= 20
+    for name in declared:
+        assert hasattr(L, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", str(rf.SO)], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if ln.strip()}
+    assert set(declared) <= exported
+    # the binding declares a signature for each of them
+    assert set(declared) == set(rf._SIGS)
+
+
+def test_status_strings(L):
+    for code, name in rf.STATUS.items():
+        assert rf.status_str(code) == name
+    assert rf.status_str(12345) == "RF_ERR_UNKNOWN"
+    assert L.rf_version() >= 100
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_sizes_match_oracle(L, fmt):
+    assert rf.block_bytes(fmt) == oracle.block_bytes(fmt)
+    for in_dim in (32, 64, 2048, 2880, 4096, 11008, 24576):
+        assert rf.row_bytes(fmt, in_dim) == oracle.row_bytes(fmt, in_dim)
+    assert rf.row_bytes(fmt, 33) == 0 and rf.row_bytes(fmt, 0) == 0
+    assert rf.block_bytes(7) == 0
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("n_rows,block_rows,depth,arena_rows", [
+    (2880, 128, 1, 1000), (2880, 1024, 4, 10000), (37, 3, 0, 64), (37, 0, 4, 64),
+    (512, 128, 4, 100000), (24576, 512, 4, 2600), (5, 8, 1, 2), (1, 1, 0, 1), (0, 4, 2, 50)])
+def test_stream_plan_matches_oracle(L, fmt, n_rows, block_rows, depth, arena_rows):
+    in_dim = 2880
+    rb = oracle.row_bytes(fmt, in_dim)
+    arena = arena_rows * rb + 7
+    want = oracle.plan_block_rows(rb, n_rows, block_rows, depth, arena)
+    if want < 0:
+        with pytest.raises(rf.RFError) as e:
+            rf.stream_plan(fmt, in_dim, n_rows, block_rows, depth, arena)
+        assert e.value.code == 4
+        return
+    eff, nblk, peak = rf.stream_plan(fmt, in_dim, n_rows, block_rows, depth, arena)
+    assert eff == want
+    assert nblk == (0 if n_rows == 0 else -(-n_rows // eff))
+    if n_rows:
+        W = np.zeros((n_rows, rb), np.uint8)
+        _, e2, n2, p2 = oracle.stream_linear(fmt, W, 0, n_rows, in_dim, block_rows, depth,
+                                             arena, np.zeros(in_dim, np.float32))
+        assert (e2, n2, p2) == (eff, nblk, peak)
+        assert peak <= arena
+
+
+def test_stream_plan_page_example(L):
+    """2,880-row MXFP4 expert, 128-row blocks, one block of lookahead: 0.39 MB."""
+    eff, nblk, peak = rf.stream_plan(rf.MXFP4, 2880, 2880, 128, 1, 1 << 20)
+    assert (eff, nblk, peak) == (128, 23, 391_680)
+
+
+def test_argument_errors_before_any_gpu_work(L):
+    buf = (ctypes.c_uint8 * 4096)()
+    p = ctypes.addressof(buf)
+    p16 = (p + 15) & ~15
+    # unknown format
+    assert L.rf_gemv(7, p16, 0, 1, 32, p16, p16, None) == 2
+    assert L.rf_dequantize(7, p16, 1, p16, None) == 2
+    # null pointers / bad sizes
+    assert L.rf_gemv(rf.Q8_0, None, 0, 1, 32, p16, p16, None) == 1
+    assert L.rf_gemv(rf.Q8_0, p16, 0, 1, 33, p16, p16, None) == 1
+    assert L.rf_gemv(rf.Q8_0, p16, 5, 4, 32, p16, p16, None) == 1
+    assert L.rf_gemv(rf.Q8_0, p16, -1, 4, 32, p16, p16, None) == 1
+    assert L.rf_dequantize(rf.Q8_0, p16, -1, p16, None) == 1
+    # misaligned weights
+    assert L.rf_gemv(rf.Q8_0, p16 + 2, 0, 1, 32, p16, p16, None) == 8
+    # empty window: no-op
+    assert L.rf_gemv(rf.Q8_0, p16, 3, 3, 32, p16, p16, None) == 0
+    assert L.rf_dequantize(rf.Q4_0, p16, 0, p16, None) == 0
+    # router / MoE argument checks
+    assert L.rf_moe_route(p16, 4, 5, p16, p16, None) == 1
+    assert L.rf_moe_route(p16, 4, 0, p16, p16, None) == 1
+    assert L.rf_moe_route(p16, 2000, 2, p16, p16, None) == 1
+    assert L.rf_moe_workspace_bytes(4, 2880, 2880, 512) == 256 + 256 + 4 * 2880 * 4
+    assert L.rf_moe_workspace_bytes(0, 2880, 2880, 512) == 0
+    # activations
+    assert L.rf_swiglu(None, p16, p16, 4, None) == 1
+    assert L.rf_gelu(p16, p16, 0, None) == 0
+    # stream: bad depth
+    assert L.rf_stream_linear(rf.Q8_0, p16, 32, 0, 1, 1, -1, p16, p16, p16, None) == 1
+    assert L.rf_stream_linear(rf.Q8_0, p16, 32, 0, 1, 1, 65, p16, p16, p16, None) == 1
+
+
+@pytest.mark.skipif(has_gpu(), reason="checks the behaviour on a machine without a GPU")
+def test_no_gpu_means_cuda_error_not_fallback(L):
+    buf = (ctypes.c_uint8 * 4096)()
+    p16 = (ctypes.addressof(buf) + 15) & ~15
+    assert L.rf_gemv(rf.Q8_0, p16, 0, 1, 32, p16, p16, None) == 5
+    assert L.rf_max_in_dim(rf.Q8_0, 1) == 0
+    h = ctypes.c_void_p()
+    assert L.rf_arena_create(1 << 20, ctypes.byref(h)) in (5, 7)
