@@ -1,0 +1,557 @@
+"""Benchmark: effective weight GB/s of the fused dequant-GEMV path.
+
+Headline workload (default, one line of JSON from rank 0): a dense decode
+layer held resident in HBM, Q4_0 -- Q/K/V/O 4096x4096, gate/up 11008x4096,
+down 4096x11008, SwiGLU between gate/up and down, batch 1, x ~ N(0,1).  One
+step = one pass of the layer for one token: 4 kernel launches (QKV batched,
+O, gate/up with the SwiGLU epilogue, down).  Eight distinct layer copies
+(910 MB, > L2) are walked round-robin so every step reads its weights from
+HBM.  value = weight bytes streamed per second (whole job over all ranks);
+tokens/s equivalent = value / active bytes per token (one layer here).
+
+Also reported (each its own sub-object): the host-streamed Q8_0 GEMV
+(512x2048, 128-row blocks), the routed MXFP4 MoE FFN (128 experts, top-4,
+512-row windows) and the host-streamed 44-layer Q8_0 FFN (24576x6144,
+256 MiB arena, 512-row blocks, depth 4) measured against the pinned
+host-to-device bandwidth probed in the same run.
+
+--impl reference times the CPU oracle (plain C, fp64, one host core) on a
+bounded sample of the same workload and prints the same line with
+"impl": "reference".  Under torchrun (N > 1) every rank runs its own replica
+(no data-path collective: the layer is replicated, not sharded); value sums
+the ranks' bytes over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from pathlib import Path
+
+import numpy as np
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+import synthetic as syn  # noqa: E402
+
+METRIC = "effective weight GB/s of dequant-GEMV (% of HBM / H2D peak); tokens/s equivalent"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------- helpers
+
+def load_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            d = json.loads(p.read_text())
+            return float(d["hbm_gbs"]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("rf_gemv.cu", "rf_device.cuh", "rf_internal.h"):
+        h.update((ROOT / "quantized_weight_streaming_dequant_gb300" / "csrc" / name).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """Per-launch DRAM bytes of the GEMV kernel from the committed ncu summary,
+    or None if the kernel source changed since it was captured."""
+    p = ROOT / "profiles" / "ncu_traffic.txt"
+    if not p.exists():
+        return None
+    cur = kernel_source_hash()
+    for line in p.read_text().splitlines():
+        if line.startswith("#") or not line.strip():
+            continue
+        parts = line.split()
+        if len(parts) >= 3 and parts[0] == workload and parts[1] == cur:
+            return float(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,utilization.gpu,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            p = [v.strip() for v in ln.split(",")]
+            if len(p) < 8:
+                continue
+            try:
+                sm.append(float(p[0]))
+                mx.append(float(p[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def h2d_probe(torch, device, nbytes: int, reps: int = 5):
+    """Pinned host->device copy bandwidth (GB/s) for transfers of nbytes."""
+    src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    s = torch.cuda.current_stream()
+    dst.copy_(src, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(reps):
+        dst.copy_(src, non_blocking=True)
+    e1.record(s)
+    torch.cuda.synchronize()
+    return nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9
+
+
+# ------------------------------------------------------------- workloads
+
+def build_dense_layers(torch, rf, device, copies: int, seed: int):
+    from quantized_weight_streaming_dequant_gb300.layer import DenseLayer
+    fmt, d, f = syn.Q4_0, syn.C2["d_model"], syn.C2["d_ff"]
+    layers = []
+    for c in range(copies):
+        s = seed * 1000 + 10 * c
+        mats = [syn.quant_matrix(fmt, d, d, s + i, threads=8) for i in range(4)]
+        mats += [syn.quant_matrix(fmt, f, d, s + 4, threads=8),
+                 syn.quant_matrix(fmt, f, d, s + 5, threads=8),
+                 syn.quant_matrix(fmt, d, f, s + 6, threads=8)]
+        dev = [torch.from_numpy(m).to(device) for m in mats]
+        layers.append(DenseLayer(fmt, d, f, *dev))
+    return layers
+
+
+def dense_outputs(torch, device):
+    d, f = syn.C2["d_model"], syn.C2["d_ff"]
+    return {k: torch.empty(n, dtype=torch.float32, device=device)
+            for k, n in (("q", d), ("k", d), ("v", d), ("o", d), ("h", f), ("y", d))}
+
+
+def run_dense(args, torch, rf, device, rank, world, dist):
+    layers = build_dense_layers(torch, rf, device, syn.C2["copies"], syn.C2["seed"] + rank)
+    d = syn.C2["d_model"]
+    x = torch.from_numpy(syn.normal_f32(d, 101 + rank)).to(device)
+    attn = torch.from_numpy(syn.normal_f32(d, 102 + rank)).to(device)
+    x_ffn = torch.from_numpy(syn.normal_f32(d, 103 + rank)).to(device)
+    out = dense_outputs(torch, device)
+    wbytes = layers[0].weight_bytes()
+    stream = torch.cuda.Stream(device)
+    nL = len(layers)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            layers[i % nL].step(x, attn, x_ffn, out, stream=stream)
+    torch.cuda.synchronize()
+
+    # One CUDA graph per layer copy (4 launches each, programmatic dependent
+    # launch edges kept); replayed round-robin.
+    graphs = []
+    use_graph = not args.no_graph
+    if use_graph:
+        try:
+            for L in layers:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    L.step(x, attn, x_ffn, out, stream=stream)
+                graphs.append(g)
+            with torch.cuda.stream(stream):
+                for i in range(nL):
+                    graphs[i].replay()
+            torch.cuda.synchronize()
+        except Exception as e:  # capture unsupported: time the eager path
+            print(f"# graph capture failed ({e}); timing eager launches", file=sys.stderr)
+            use_graph, graphs = False, []
+
+    def one_step(i):
+        if use_graph:
+            graphs[i % nL].replay()
+        else:
+            layers[i % nL].step(x, attn, x_ffn, out, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            one_step(i)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(device.index or 0) as clk:
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for i in range(args.steps):
+                one_step(i)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+    ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    gbs = wbytes * args.steps * world / (ms * 1e-3) / 1e9
+
+    # Per-phase launch durations (eager, events around each launch) for the
+    # roofline breakdown.
+    phases = per_phase_times(torch, rf, layers, x, attn, x_ffn, out, stream, reps=40)
+
+    # End to end through the public API: H2D of the step's inputs from pinned
+    # host memory, the 4 launches, D2H of the step's outputs, every step.
+    e2e = dense_e2e(torch, layers, out, device, stream, steps=min(args.steps, 400) or 1)
+    return dict(ms=ms / args.steps, gbs=gbs, wbytes=wbytes, use_graph=use_graph,
+                clocks=clk.summary(), phases=phases, e2e=e2e)
+
+
+def per_phase_times(torch, rf, layers, x, attn, x_ffn, out, stream, reps):
+    """Eager launches with events around each phase: QKV (one batched launch),
+    O (one launch), FFN (gate/up with SwiGLU epilogue + down: two launches)."""
+    d, f, fmt = syn.C2["d_model"], syn.C2["d_ff"], syn.Q4_0
+    rb_d, rb_f = rf.row_bytes(fmt, d), rf.row_bytes(fmt, f)
+    nbytes = {"qkv": 3 * d * rb_d, "o": d * rb_d, "ffn": 2 * f * rb_d + d * rb_f}
+    acc = {k: 0.0 for k in nbytes}
+    nL = len(layers)
+    with torch.cuda.stream(stream):
+        for it in range(reps):
+            L = layers[it % nL]
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            ev[0].record(stream)
+            rf.gemv_batch(fmt, d, [(L.wq, 0, d, x, out["q"]), (L.wk, 0, d, x, out["k"]),
+                                   (L.wv, 0, d, x, out["v"])], stream=stream)
+            ev[1].record(stream)
+            rf.gemv(fmt, L.wo, 0, d, d, attn, out["o"], stream=stream)
+            ev[2].record(stream)
+            rf.ffn_swiglu(fmt, L.w_gate, L.w_up, L.w_down, f, d, x_ffn, out["y"], out["h"],
+                          stream=stream)
+            ev[3].record(stream)
+            torch.cuda.synchronize()
+            acc["qkv"] += ev[0].elapsed_time(ev[1])
+            acc["o"] += ev[1].elapsed_time(ev[2])
+            acc["ffn"] += ev[2].elapsed_time(ev[3])
+    res = {}
+    for k, b in nbytes.items():
+        ms = acc[k] / reps
+        res[k] = {"ms": ms, "bytes": b, "gbs": b / (ms * 1e-3) / 1e9}
+    return res
+
+
+def dense_e2e(torch, layers, out, device, stream, steps):
+    d = syn.C2["d_model"]
+    h_in = torch.from_numpy(np.concatenate([syn.normal_f32(d, s) for s in (101, 102, 103)]))
+    h_in = h_in.pin_memory()
+    d_in = torch.empty(3 * d, dtype=torch.float32, device=device)
+    outs = ["q", "k", "v", "o", "y"]
+    h_out = torch.empty(len(outs) * d, dtype=torch.float32).pin_memory()
+    d_out = torch.empty(len(outs) * d, dtype=torch.float32, device=device)
+    nL = len(layers)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            d_in.copy_(h_in, non_blocking=True)
+            layers[i % nL].step(d_in[:d], d_in[d:2 * d], d_in[2 * d:], out, stream=stream)
+            torch.cat([out[k] for k in outs], out=d_out)
+            h_out.copy_(d_out, non_blocking=True)
+            stream.synchronize()
+    dt = time.perf_counter() - t0
+    wbytes = layers[0].weight_bytes()
+    return {"value": wbytes * steps / dt / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": int(h_in.numel() * 4), "d2h_bytes_per_step": int(h_out.numel() * 4),
+            "ms_per_step": dt / steps * 1e3, "steps": steps}
+
+
+def run_streamed_gemv(torch, rf, device, depth: int, reps: int = 50):
+    """Q8_0 512x2048 streamed from pinned host memory in 128-row blocks."""
+    c = syn.C1
+    fmt, rows, in_dim = c["fmt"], c["out_dim"], c["in_dim"]
+    W = syn.quant_matrix(fmt, rows, in_dim, c["seed"])
+    host = torch.from_numpy(W).pin_memory()
+    x = torch.from_numpy(syn.normal_f32(in_dim, c["seed"] + 1)).to(device)
+    y = torch.empty(rows, device=device)
+    arena = rf.Arena(c["arena_bytes"])
+    s = torch.cuda.current_stream()
+    try:
+        for _ in range(5):
+            arena.stream_linear(fmt, host, in_dim, 0, rows, c["block_rows"], depth, x, y)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(reps):
+            arena.stream_linear(fmt, host, in_dim, 0, rows, c["block_rows"], depth, x, y)
+        e1.record(s)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+    finally:
+        arena.close()
+    nbytes = W.nbytes
+    probe = h2d_probe(torch, device, c["block_rows"] * rf.row_bytes(fmt, in_dim), reps=200)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": c["name"], "depth": depth, "ms_per_gemv": ms, "value": gbs, "unit": "GB/s",
+            "h2d_probe_block_gbs": probe, "frac_of_block_h2d": gbs / probe}
+
+
+def run_moe(torch, rf, device, steps: int = 200):
+    c = syn.C3
+    fmt, E, n_ff, n_embd, k, br = c["fmt"], c["n_expert"], c["n_ff"], c["n_embd"], c["top_k"], \
+        c["block_rows"]
+    G = torch.from_numpy(syn.stacked_experts(fmt, E, n_ff, n_embd, c["seed"], threads=8)).to(device)
+    U = torch.from_numpy(syn.stacked_experts(fmt, E, n_ff, n_embd, c["seed"] + 1, threads=8)).to(
+        device)
+    D = torch.from_numpy(syn.stacked_experts(fmt, E, n_embd, n_ff, c["seed"] + 2, threads=8)).to(
+        device)
+    x = torch.from_numpy(syn.normal_f32(n_embd, c["seed"] + 3)).to(device)
+    # fresh router logits per token so the expert windows vary
+    logits = torch.from_numpy(np.stack([syn.router_logits(E, 1000 + t) for t in range(steps)])).to(
+        device)
+    y = torch.empty(n_embd, device=device)
+    ws = rf.moe_workspace(k, n_ff, n_embd, br, device)
+    s = torch.cuda.current_stream()
+    for t in range(10):
+        rf.moe_ffn(fmt, logits[t], k, G, U, D, n_ff, n_embd, br, x, y, ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for t in range(steps):
+        rf.moe_ffn(fmt, logits[t], k, G, U, D, n_ff, n_embd, br, x, y, ws)
+    e1.record(s)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    active = k * 3 * n_ff * rf.row_bytes(fmt, n_embd)
+    return {"workload": c["name"], "ms_per_token": ms, "active_bytes": active,
+            "value": active / (ms * 1e-3) / 1e9, "unit": "GB/s", "launches_per_token": 3}
+
+
+def run_streamed_ffn(torch, rf, device, n_layer: int):
+    from quantized_weight_streaming_dequant_gb300.layer import StreamedFFN
+    c = syn.C4
+    fmt, d, f = c["fmt"], c["d_model"], c["d_ff"]
+    layers = []
+    for l in range(n_layer):
+        up = torch.empty((f, rf.row_bytes(fmt, d)), dtype=torch.uint8).pin_memory()
+        dn = torch.empty((d, rf.row_bytes(fmt, f)), dtype=torch.uint8).pin_memory()
+        syn.quant_matrix(fmt, f, d, c["seed"] * 1000 + 2 * l, out=up.numpy(), threads=16)
+        syn.quant_matrix(fmt, d, f, c["seed"] * 1000 + 2 * l + 1, out=dn.numpy(), threads=16)
+        layers.append(StreamedFFN(fmt, d, f, up, dn))
+    xs = [torch.from_numpy(syn.normal_f32(d, 5000 + l)).to(device) for l in range(n_layer)]
+    u = torch.empty(f, device=device)
+    h = torch.empty(f, device=device)
+    y = torch.empty(d, device=device)
+    arena = rf.Arena(c["arena_bytes"])
+    s = torch.cuda.current_stream()
+    try:
+        for l in range(min(2, n_layer)):
+            layers[l].step(arena, xs[l], u, h, y, c["block_rows"], c["depth"])
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        e0.record(s)
+        for l in range(n_layer):
+            layers[l].step(arena, xs[l], u, h, y, c["block_rows"], c["depth"])
+        e1.record(s)
+        torch.cuda.synchronize()
+        host_s = time.perf_counter() - t0
+        ms = e0.elapsed_time(e1)
+        stats = arena.stats()
+    finally:
+        arena.close()
+    nbytes = sum(L.weight_bytes() for L in layers)
+    probe_big = h2d_probe(torch, device, 256 << 20)
+    probe_blk = h2d_probe(torch, device, c["block_rows"] * rf.row_bytes(fmt, f), reps=20)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": c["name"], "layers": n_layer, "ms_per_token": ms,
+            "bytes_per_token": nbytes, "value": gbs, "unit": "GB/s",
+            "h2d_probe_256mib_gbs": probe_big, "h2d_probe_block_gbs": probe_blk,
+            "frac_of_h2d": gbs / probe_big, "tokens_per_s": 1e3 / ms,
+            "host_enqueue_s": host_s, "arena_peak_bytes": stats["peak_bytes"],
+            "blocks_per_token": stats["blocks"] // (n_layer + min(2, n_layer))}
+
+
+# ------------------------------------------------------------- reference
+
+def cpu_oracle_dense(fraction: float, min_seconds: float):
+    """The oracle on the first `fraction` of every matrix's rows of one C2
+    layer; repeats until min_seconds of CPU time; returns (GB/s, seconds,
+    bytes per pass)."""
+    import oracle
+    fmt, d, f = syn.Q4_0, syn.C2["d_model"], syn.C2["d_ff"]
+    shapes = [(d, d)] * 4 + [(f, d)] * 2 + [(d, f)]
+    mats = [syn.quant_matrix(fmt, max(1, int(r * fraction)), c, 7 + i)
+            for i, (r, c) in enumerate(shapes)]
+    xs = {c: syn.normal_f32(c, c) for c in (d, f)}
+    nbytes = sum(m.nbytes for m in mats)
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        for m, (r, c) in zip(mats, shapes):
+            oracle.gemv(fmt, m, 0, m.shape[0], c, xs[c])
+        passes += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds:
+            break
+    return nbytes * passes / dt / 1e9, dt / passes, nbytes
+
+
+def run_reference(args, rank: int):
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    total = args.steps + args.warmup
+    # size each step so the whole run takes about a minute of one core
+    _, t_full_frac, _ = cpu_oracle_dense(1 / 64, 0.0)
+    frac = max(1 / 4096, min(1.0, (60.0 / max(total, 1)) / (t_full_frac * 64)))
+    gbs, _, nbytes = cpu_oracle_dense(frac, 0.0)
+    for _ in range(args.warmup):
+        cpu_oracle_dense(frac, 0.0)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        cpu_oracle_dense(frac, 0.0)
+    dt = time.perf_counter() - t0
+    value = nbytes * args.steps / dt / 1e9
+    sample = (f"first {frac:.4%} of the rows of each of the 7 matrices of one Q4_0 "
+              f"4096/11008 layer ({nbytes} weight bytes) per step")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / max(args.steps, 1) * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": syn.C2["name"], "d_model": 4096, "d_ff": 11008,
+                       "format": "Q4_0", "batch": 1},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ------------------------------------------------------------------ main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--ffn-layers", type=int, default=syn.C4["n_layer"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank)
+
+    import torch
+    import quantized_weight_streaming_dequant_gb300 as rf
+    from quantized_weight_streaming_dequant_gb300 import build
+    build.build()
+    rf.lib()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl", device_id=device)
+        dist = tdist
+
+    res = run_dense(args, torch, rf, device, rank, world, dist)
+    peak, peak_kind = load_peaks()
+    wbytes = res["wbytes"]
+    launches = 4 * args.steps
+    achieved = res["gbs"] / world    # all GEMV launches of the step: the only kernels in it
+    traffic = ncu_traffic("q4_0_dense_layer_4096x11008")
+    line = {"metric": METRIC, "value": res["gbs"], "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "q4_0 x int24 (dp4a), fp32 accumulate", "data": "synthetic",
+            "config": {"workload": syn.C2["name"], "format": "Q4_0", "d_model": 4096,
+                       "d_ff": 11008, "batch": 1, "layer_copies": syn.C2["copies"],
+                       "weight_bytes_per_step": wbytes, "l2": "inputs > L2 (8 layer copies, "
+                       f"{8 * wbytes / 1e6:.0f} MB, round-robin)",
+                       "parallelism": f"replicas x{world}", "cuda_graph": res["use_graph"]},
+            "tokens_per_s_equiv": res["gbs"] / (wbytes / 1e9),
+            "frac_of_hbm_peak": achieved / peak,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": peak_kind,
+                         "kernel": "rowwin_kernel<Q4_0> (all 4 launches of the step)",
+                         "traffic": traffic},
+            "phases": res["phases"], "clocks": res["clocks"], "e2e": res["e2e"],
+            "gpu_launches": launches}
+    if rank == 0 and world == 1 and not args.headline_only:
+        extra = {}
+        try:
+            extra["streamed_gemv_q8_0_512x2048"] = [run_streamed_gemv(torch, rf, device, dp)
+                                                    for dp in (4, 1)]
+            extra["moe_mxfp4"] = run_moe(torch, rf, device)
+            if args.ffn_layers > 0:
+                extra["streamed_ffn_q8_0"] = run_streamed_ffn(torch, rf, device, args.ffn_layers)
+        except Exception as e:  # extras never hide the headline
+            extra["error"] = repr(e)
+        line["extra"] = extra
+        gbs_cpu, _, _ = cpu_oracle_dense(1 / 16, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": gbs_cpu, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                "sample": "first 1/16 of the rows of each matrix of one layer, "
+                                          f"repeated for {args.cpu_seconds:.0f} s on one core"}
+    if rank == 0:
+        print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
