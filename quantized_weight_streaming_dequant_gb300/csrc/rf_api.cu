@@ -153,7 +153,7 @@ rf_status rf_gemv(int fmt, const void *W, int64_t row_start, int64_t row_end, in
     if (const rf_status c = check_in_dim(fmt, in_dim, 1)) return c;
     Job J;
     std::memset(&J, 0, sizeof(J));
-    J.term[0] = Term{static_cast<const uint8_t *>(W), 0, -1};
+    J.term[0] = Term{static_cast<const uint8_t *>(W), 0, -1, 0, 0};
     J.y = y;
     J.row0 = row_start;
     J.n_rows = (int32_t)(row_end - row_start);
@@ -196,7 +196,7 @@ rf_status rf_gemv_batch(int fmt, int64_t in_dim, int n_windows, const rf_window 
             slot = n_x++;
         }
         std::memset(&jobs[i], 0, sizeof(Job));
-        jobs[i].term[0] = Term{static_cast<const uint8_t *>(w.W), slot, -1};
+        jobs[i].term[0] = Term{static_cast<const uint8_t *>(w.W), slot, -1, 0, 0};
         jobs[i].y = w.y;
         jobs[i].row0 = w.row_start;
         jobs[i].n_rows = (int32_t)(w.row_end - w.row_start);
@@ -244,8 +244,8 @@ rf_status rf_ffn_swiglu(int fmt, const void *gate, const void *up, const void *d
     // Phase 1: walk gate and up by neuron; SwiGLU in the epilogue.
     Job J;
     std::memset(&J, 0, sizeof(J));
-    J.term[0] = Term{static_cast<const uint8_t *>(gate), 0, -1};
-    J.term[1] = Term{static_cast<const uint8_t *>(up), 0, -1};
+    J.term[0] = Term{static_cast<const uint8_t *>(gate), 0, -1, 0, 0};
+    J.term[1] = Term{static_cast<const uint8_t *>(up), 0, -1, 0, 0};
     J.y = h;
     J.n_rows = (int32_t)n_ff;
     J.n_terms = 2;
@@ -263,7 +263,7 @@ rf_status rf_ffn_swiglu(int fmt, const void *gate, const void *up, const void *d
     // its weight copies overlap the tail of phase 1).
     Job K;
     std::memset(&K, 0, sizeof(K));
-    K.term[0] = Term{static_cast<const uint8_t *>(down), 0, -1};
+    K.term[0] = Term{static_cast<const uint8_t *>(down), 0, -1, 0, 0};
     K.y = y;
     K.n_rows = (int32_t)n_embd;
     K.n_terms = 1;

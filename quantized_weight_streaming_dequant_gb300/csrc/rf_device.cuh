@@ -100,6 +100,17 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// 2-D tiled tensor copy global -> shared: the box at coordinates (x, y) of the
+// tensor map lands densely in shared memory (128-byte aligned destination).
+__device__ __forceinline__ void tma_2d_g2s(void *dst, const void *tmap, int x, int y, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
 // ------------------------------------------------------ programmatic launch
 // Wait until the grids this launch depends on have completed and flushed
 // (no-op when launched without a programmatic dependency).

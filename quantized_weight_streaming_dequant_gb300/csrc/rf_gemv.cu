@@ -16,25 +16,30 @@
 //     partials of a row in warp order.  The split depends only on (format,
 //     in_dim), so a row's result is the same in every window and every launch.
 //   * Weights move global -> shared with 1-D bulk copies (TMA), one copy per
-//     lane per chunk of KC blocks, into a per-warp ring of `stages` slots
+//     lane per chunk of kc blocks, into a per-warp ring of `stages` slots
 //     guarded by mbarriers (expect_tx byte counts).  A copy starts at the
 //     16-byte boundary at or before the chunk and ends at the one at or after
 //     it, so any row alignment works; rows that are 16-byte aligned (row bytes
-//     a multiple of 16) are decoded with static 16-byte shared loads.
+//     a multiple of 16) are copied exactly and decoded with static 16-byte
+//     shared loads.  Chunk and slot sizes are launch parameters chosen so that
+//     two CTAs fit on an SM when shared memory allows.
 //   * Integer dot products.  Each 32-element activation block is turned once
-//     per CTA into a fixed-point integer X = rint(x * 2^s) (|X| < 2^22, s
-//     chosen from the block maximum) split into three byte planes.  The block
-//     dot sum_j q_j X_j is then three exact dp4a chains over the raw quant
-//     bytes (Q8_0 bytes are used as they are; Q4_0 nibbles need two masks;
-//     MXFP4 codes go through a byte-permute lookup of 2*e2m1), and one fp32
-//     FMA per block applies d * 2^-s.  Q4_0's "-8" is folded into the
-//     accumulator's start value (-8 * sum_j X_j, precomputed per block).
-//     Error: |x - X*2^-s| <= 2^-23 * max|x_block|, far inside the parity
-//     tolerance 1e-3*||W_r||*||x||; products and in-block sums are exact.
-//   * Persistent CTAs (one per SM; shared memory bounds residency) each take a
-//     contiguous range of 32-row groups across all jobs of the launch.
+//     per CTA into a fixed-point integer X = rint(x * 2^s) with |X| < 2^15
+//     (s from the block maximum) split into two byte planes.  The block dot
+//     sum_j q_j X_j is then exact dp4a chains over the raw quant bytes (Q8_0
+//     bytes are used as they are; Q4_0 nibbles are masked in place, the high
+//     ones scaled by 16; MXFP4 codes go through a byte-permute lookup of
+//     2*e2m1), and one fp32 FMA per block applies d * 2^-s.  Q4_0's "-8" is
+//     the per-block constant -8 * sum_j X_j.
+//     Error: |x_j - X_j*2^-s| <= 2^-15 * max|x_block|, so by Cauchy-Schwarz
+//     the activation rounding moves y_r by at most sqrt(32)*2^-15*||W_r||*||x||
+//     (< 1.8e-4 * ||W_r||*||x||), inside the parity tolerance 1e-3*||W_r||*||x||.
+//   * Persistent CTAs each take a contiguous range of 32-row groups across all
+//     jobs of the launch.
 //   * Programmatic dependent launch: weight copies for the first chunks are
 //     issued before griddepcontrol.wait, so they overlap the previous kernel.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -57,45 +62,38 @@ constexpr int kRows = 32;   // rows per group (one per lane)
 
 // Fixed-point digits of one 32-element activation block.
 struct __align__(16) XRec {
-    uint32_t p0[8];      // byte 0 of X (unsigned), 4 elements per word
-    uint32_t p1[8];      // byte 1 of X (unsigned)
-    uint32_t p2[8];      // byte 2 of X (signed: X >> 16)
-    int32_t c0, c1, c2;  // accumulator start values (Q4_0: -8 * sum of the plane)
-    float scale;         // 2^-s
+    uint32_t p0[8];   // byte 0 of X (unsigned), 4 elements per word
+    uint32_t p1[8];   // byte 1 of X (signed: X >> 8)
+    int32_t corr;     // Q4_0: -8 * sum_j X_j (else 0)
+    float scale;      // 2^-s
+    int32_t pad[2];
 };
-static_assert(sizeof(XRec) == 112, "XRec layout");
+static_assert(sizeof(XRec) == 80, "XRec layout");
 
 template <int FMT>
 struct FmtT;
 template <>
 struct FmtT<RF_Q4_0> {
-    static constexpr int BS = 18, HDR = 2, QW = 4, G = 8, KC = 16;
+    static constexpr int BS = 18, HDR = 2, QW = 4, G = 8;
 };
 template <>
 struct FmtT<RF_Q8_0> {
-    static constexpr int BS = 34, HDR = 2, QW = 8, G = 8, KC = 8;
+    static constexpr int BS = 34, HDR = 2, QW = 8, G = 8;
 };
 template <>
 struct FmtT<RF_MXFP4> {
-    static constexpr int BS = 17, HDR = 1, QW = 4, G = 16, KC = 16;
+    static constexpr int BS = 17, HDR = 1, QW = 4, G = 16;
 };
 
-// Slot bytes: KC blocks plus up to 15 bytes of rounding on either side, padded
-// to an odd number of 16-byte units so that 16-byte loads of the 32 lanes'
-// slots hit distinct banks.
-template <int FMT>
-__host__ __device__ constexpr int slot_bytes()
-{
-    return (((FmtT<FMT>::KC * FmtT<FMT>::BS + 30 + 15) / 16) % 2 == 0)
-               ? (FmtT<FMT>::KC * FmtT<FMT>::BS + 30 + 15) / 16 * 16 + 16
-               : (FmtT<FMT>::KC * FmtT<FMT>::BS + 30 + 15) / 16 * 16;
-}
+constexpr int kMaxMaps = 16;   // distinct weight tensors per launch (tensor-map path)
 
 struct KParams {
+    CUtensorMap maps[kMaxMaps];   // 2-D views [rows][row bytes] of 16-byte aligned rows
     Job jobs[kMaxJobs];
     const float *x[kMaxX];
     const int32_t *expert_idx;
-    int32_t n_jobs, n_x, nb, total_groups, stages, prefetch_early;
+    int32_t n_jobs, n_x, nb, total_groups;
+    int32_t stages, kc, slot, prefetch_early;
 };
 
 // Element of the 32-block packed into byte `byte` of plane word `word`, in the
@@ -110,6 +108,13 @@ __device__ __forceinline__ int elem_of(int word, int byte)
     } else {
         return 4 * word + byte;
     }
+}
+
+// 2^k as a float for k in [-149, 127].
+__device__ __forceinline__ float exp2i(int k)
+{
+    return k >= -126 ? __uint_as_float((uint32_t)(k + 127) << 23)
+                     : __uint_as_float(1u << (k + 149));
 }
 
 template <int FMT>
@@ -132,93 +137,78 @@ __device__ void make_xrec(const float *xb, XRec *out)
     float m = 0.f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(v[i]));
-    int e = 0;
-    frexpf(m, &e);         // m = f * 2^e, f in [0.5, 1); m == 0 gives e = 0
-    const int s = 22 - e;  // |x * 2^s| < 2^22
+    // m < 2^e with e from the exponent field (zero/subnormal m: e = -125).
+    const int biased = (int)(__float_as_uint(m) >> 23);
+    const int e = biased == 0 ? -125 : biased - 126;
+    const int s = 15 - e;   // |x * 2^s| < 2^15; s in [-114, 140]
+    const float f1 = exp2i(min(s, 127)), f2 = exp2i(max(s - 127, 0));
     int X[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) X[i] = __float2int_rn(ldexpf(v[i], s));
+    for (int i = 0; i < 32; ++i) {
+        // round to nearest even through the 1.5*2^23 magic constant
+        const float t = (v[i] * f1) * f2 + 12582912.0f;
+        const int q = (int)(__float_as_uint(t) - 0x4b400000u);
+        X[i] = max(-32767, min(32767, q));
+    }
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
-        uint32_t b0 = 0, b1 = 0, b2 = 0;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const int xe = X[elem_of<FMT>(w, b)];
-            b0 |= (uint32_t)(xe & 0xff) << (8 * b);
-            b1 |= (uint32_t)((xe >> 8) & 0xff) << (8 * b);
-            b2 |= (uint32_t)((xe >> 16) & 0xff) << (8 * b);
-        }
-        out->p0[w] = b0;
-        out->p1[w] = b1;
-        out->p2[w] = b2;
+        const uint32_t a = (uint32_t)X[elem_of<FMT>(w, 0)], b = (uint32_t)X[elem_of<FMT>(w, 1)];
+        const uint32_t c = (uint32_t)X[elem_of<FMT>(w, 2)], d = (uint32_t)X[elem_of<FMT>(w, 3)];
+        out->p0[w] = prmt(prmt(a, b, 0x0040u), prmt(c, d, 0x0040u), 0x5410u);
+        out->p1[w] = prmt(prmt(a, b, 0x0051u), prmt(c, d, 0x0051u), 0x5410u);
     }
-    int c0 = 0, c1 = 0, c2 = 0;
+    int corr = 0;
     if constexpr (FMT == RF_Q4_0) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            c0 += X[i] & 0xff;
-            c1 += (X[i] >> 8) & 0xff;
-            c2 += X[i] >> 16;
-        }
-        c0 *= -8;
-        c1 *= -8;
-        c2 *= -8;
+        for (int i = 0; i < 32; ++i) corr += X[i];
+        corr *= -8;
     }
-    out->c0 = c0;
-    out->c1 = c1;
-    out->c2 = c2;
-    out->scale = ldexpf(1.0f, -s);
+    out->corr = corr;
+    out->scale = exp2i(-s);
+    out->pad[0] = out->pad[1] = 0;
 }
 
-// sum_j q_j * X_j of one block from its three exact partial sums.
-__device__ __forceinline__ float join3(int s0, int s1, int s2)
-{
-    return fmaf((float)s2, 65536.f, (float)(s1 * 256 + s0));
-}
-
-// Integer dot of one block's quant words with the block's digit planes.
+// Integer dot of one block's quant words with the block's digit planes;
+// returns sum_j q_j X_j as a float.
 template <int FMT>
 __device__ __forceinline__ float block_idot(const uint32_t (&q)[FmtT<FMT>::QW], const XRec &r)
 {
     const uint4 *P0 = reinterpret_cast<const uint4 *>(r.p0);
     const uint4 *P1 = reinterpret_cast<const uint4 *>(r.p1);
-    const uint4 *P2 = reinterpret_cast<const uint4 *>(r.p2);
-    const uint4 a0 = P0[0], a1 = P0[1], b0 = P1[0], b1 = P1[1], c0 = P2[0], c1 = P2[1];
+    const uint4 a0 = P0[0], a1 = P0[1], b0 = P1[0], b1 = P1[1];
     const uint32_t p0[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
     const uint32_t p1[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-    const uint32_t p2[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-    int s0, s1, s2;
     if constexpr (FMT == RF_Q4_0) {
-        const int4 cc = *reinterpret_cast<const int4 *>(&r.c0);
-        s0 = cc.x;
-        s1 = cc.y;
-        s2 = cc.z;
+        // Low nibbles are elements 4k..4k+3, high nibbles 16+4k..; the high
+        // ones stay in place (16*q), and the exact sums are divided by 16.
+        int l0 = 0, l1 = 0, h0 = 0, h1 = 0;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const uint32_t lo = q[k] & 0x0f0f0f0fu;          // elements 4k..4k+3
-            const uint32_t hi = (q[k] >> 4) & 0x0f0f0f0fu;   // elements 16+4k..
-            s0 = dp4a_uu(lo, p0[k], s0);
-            s1 = dp4a_uu(lo, p1[k], s1);
-            s2 = dp4a_us(lo, p2[k], s2);
-            s0 = dp4a_uu(hi, p0[k + 4], s0);
-            s1 = dp4a_uu(hi, p1[k + 4], s1);
-            s2 = dp4a_us(hi, p2[k + 4], s2);
+            const uint32_t lo = q[k] & 0x0f0f0f0fu;
+            const uint32_t hi = q[k] & 0xf0f0f0f0u;
+            l0 = dp4a_uu(lo, p0[k], l0);
+            l1 = dp4a_us(lo, p1[k], l1);
+            h0 = dp4a_uu(hi, p0[k + 4], h0);
+            h1 = dp4a_us(hi, p1[k + 4], h1);
         }
+        return (float)((l1 + (h1 >> 4)) * 256 + l0 + (h0 >> 4) + r.corr);
     } else if constexpr (FMT == RF_Q8_0) {
-        s0 = s1 = s2 = 0;
+        int a = 0, b = 0, c = 0, d = 0;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            s0 = dp4a_su(q[k], p0[k], s0);
-            s1 = dp4a_su(q[k], p1[k], s1);
-            s2 = dp4a_ss(q[k], p2[k], s2);
+        for (int k = 0; k < 8; k += 2) {
+            a = dp4a_su(q[k], p0[k], a);
+            b = dp4a_ss(q[k], p1[k], b);
+            c = dp4a_su(q[k + 1], p0[k + 1], c);
+            d = dp4a_ss(q[k + 1], p1[k + 1], d);
         }
+        return (float)((b + d) * 256 + a + c);
     } else {
         // MXFP4: 2*e2m1 as signed bytes through a byte-permute lookup.
         // Positive table {0,1,2,3,4,6,8,12}, negative table its negation;
         // the sign bit of each code picks between them.
         constexpr uint32_t kPosLo = 0x03020100u, kPosHi = 0x0c080604u;
         constexpr uint32_t kNegLo = 0xfdfeff00u, kNegHi = 0xf4f8fafcu;
-        s0 = s1 = s2 = 0;
+        int a = 0, b = 0, c = 0, d = 0;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const uint32_t v = q[k];
@@ -231,15 +221,13 @@ __device__ __forceinline__ float block_idot(const uint32_t (&q)[FmtT<FMT>::QW], 
             const uint32_t sb = prmt(vs, v, 0xfbeau);
             const uint32_t wa = (pa & ~sa) | (na & sa);
             const uint32_t wb = (pb & ~sb) | (nb & sb);
-            s0 = dp4a_su(wa, p0[2 * k], s0);
-            s1 = dp4a_su(wa, p1[2 * k], s1);
-            s2 = dp4a_ss(wa, p2[2 * k], s2);
-            s0 = dp4a_su(wb, p0[2 * k + 1], s0);
-            s1 = dp4a_su(wb, p1[2 * k + 1], s1);
-            s2 = dp4a_ss(wb, p2[2 * k + 1], s2);
+            a = dp4a_su(wa, p0[2 * k], a);
+            b = dp4a_ss(wa, p1[2 * k], b);
+            c = dp4a_su(wb, p0[2 * k + 1], c);
+            d = dp4a_ss(wb, p1[2 * k + 1], d);
         }
+        return (float)((b + d) * 256 + a + c);
     }
-    return join3(s0, s1, s2);
 }
 
 // Block scale (times the activation block's 2^-s) from the header bits.
@@ -358,20 +346,24 @@ __device__ __forceinline__ const uint8_t *term_matrix(const KParams &p, const Jo
     return W;
 }
 
-template <int FMT>
-__global__ void __launch_bounds__(kThreads, 1) rowwin_kernel(const __grid_constant__ KParams p)
+// TMA = true: rows are 16-byte aligned and each chunk of a warp (32 rows x kc
+// blocks) is one 2-D tensor copy issued by lane 0.  TMA = false: any
+// alignment; each lane copies its own row's chunk with a 1-D bulk copy.
+template <int FMT, bool TMA>
+__global__ void __launch_bounds__(kThreads, 2) rowwin_kernel(const __grid_constant__ KParams p)
 {
     using F = FmtT<FMT>;
-    constexpr int SLOT = slot_bytes<FMT>();
     extern __shared__ __align__(128) uint8_t smem[];
 
     const int nb = p.nb;
     const int ST = p.stages;
+    const int KC = p.kc;
+    const int SLOT = p.slot;
     const int64_t RB = (int64_t)nb * F::BS;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     XRec *xrec = reinterpret_cast<XRec *>(smem);
-    size_t off = (size_t)p.n_x * nb * sizeof(XRec);
+    size_t off = ((size_t)p.n_x * nb * sizeof(XRec) + 127) & ~(size_t)127;
     uint8_t *slots = smem + off;
     off += (size_t)kNW * ST * kRows * SLOT;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + off);
@@ -386,9 +378,9 @@ __global__ void __launch_bounds__(kThreads, 1) rowwin_kernel(const __grid_consta
     const int nG = (nb + F::G - 1) / F::G;
     const int kb_lo = min(nb, F::G * (warp * nG / kNW));
     const int kb_hi = min(nb, F::G * ((warp + 1) * nG / kNW));
-    const int n_chunks = (kb_hi - kb_lo + F::KC - 1) / F::KC;
+    const int n_chunks = (kb_hi - kb_lo + KC - 1) / KC;
 
-    if (lane < ST) mbar_init(&bars[warp * ST + lane], 32);
+    if (lane < ST) mbar_init(&bars[warp * ST + lane], TMA ? 1 : 32);
     fence_barrier_init();
     __syncthreads();
 
@@ -397,17 +389,30 @@ __global__ void __launch_bounds__(kThreads, 1) rowwin_kernel(const __grid_consta
 
     Cursor ic{g_lo, 0, 0, 0, g_lo < g_hi && n_chunks > 0};
     if (ic.valid) cursor_fix_job(p, ic);
-    long issued = 0;
+    int issued = 0;
 
     auto issue = [&](const Cursor &cu) {
-        const int stage = (int)(issued % ST);
+        const int stage = issued % ST;
         uint64_t *bar = &my_bars[stage];
         const Job &J = p.jobs[cu.j];
+        if constexpr (TMA) {
+            if (lane == 0) {
+                const Term &T = J.term[cu.t];
+                int64_t y = J.row0 + (int64_t)(cu.g - J.group_begin) * kRows;
+                if (T.expert_slot >= 0) y += (int64_t)p.expert_idx[T.expert_slot] * J.expert_rows;
+                const int x = (kb_lo + cu.c * KC) * F::BS / 2;   // uint16 units
+                mbar_arrive_expect_tx(bar, (uint32_t)(kRows * SLOT));
+                tma_2d_g2s(my_slots + (size_t)stage * kRows * SLOT, &p.maps[T.tmap], x, (int)y,
+                           bar);
+            }
+            ++issued;
+            return;
+        }
         const int64_t rowrel = (int64_t)(cu.g - J.group_begin) * kRows + lane;
         if (rowrel < J.n_rows) {
             const uint8_t *W = term_matrix(p, J, cu.t, RB);
-            const int kb = kb_lo + cu.c * F::KC;
-            const int kn = min(F::KC, kb_hi - kb);
+            const int kb = kb_lo + cu.c * KC;
+            const int kn = min(KC, kb_hi - kb);
             const uintptr_t s = reinterpret_cast<uintptr_t>(W + (J.row0 + rowrel) * RB +
                                                             (int64_t)kb * F::BS);
             const uintptr_t a = s & ~(uintptr_t)15;
@@ -446,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1) rowwin_kernel(const __grid_consta
     }
     __syncthreads();
 
-    long consumed = 0;
+    int consumed = 0;
     int j = 0;
     for (int g = g_lo; g < g_hi; ++g) {
         while (j < p.n_jobs && g >= p.jobs[j].group_begin + groups_of(p.jobs[j])) ++j;
@@ -456,27 +461,24 @@ __global__ void __launch_bounds__(kThreads, 1) rowwin_kernel(const __grid_consta
         float yacc = 0.f, gate = 0.f;
         for (int t = 0; t < J.n_terms; ++t) {
             float acc = 0.f;
-            int phi = 0;
-            if (!J.aligned && row_ok) {
-                const uint8_t *W = term_matrix(p, J, t, RB);
-                phi = (int)(reinterpret_cast<uintptr_t>(W + (J.row0 + rowrel) * RB +
-                                                        (int64_t)kb_lo * F::BS) &
-                            15);
-            }
+            uintptr_t row_src = 0;
+            if (!TMA && !J.aligned && row_ok)
+                row_src = reinterpret_cast<uintptr_t>(term_matrix(p, J, t, RB) +
+                                                      (J.row0 + rowrel) * RB);
             const XRec *xr_row = xrec + (size_t)J.term[t].xslot * nb;
             for (int c = 0; c < n_chunks; ++c) {
-                const int stage = (int)(consumed % ST);
+                const int stage = consumed % ST;
                 const uint32_t parity = (uint32_t)((consumed / ST) & 1);
                 mbar_wait_bounded(&my_bars[stage], parity, &g_device_status);
                 const uint8_t *slot = my_slots + ((size_t)stage * kRows + lane) * SLOT;
-                const int kb = kb_lo + c * F::KC;
-                const int kn = min(F::KC, kb_hi - kb);
-                // Chunks start at multiples of KC*BS bytes past kb_lo, and
-                // KC*BS is a multiple of 16, so phi is the same for all chunks.
-                if (J.aligned)
+                const int kb = kb_lo + c * KC;
+                const int kn = min(KC, kb_hi - kb);
+                if (TMA || J.aligned) {
                     acc = chunk_aligned<FMT>(slot, kn, xr_row + kb, acc);
-                else
+                } else {
+                    const int phi = (int)((row_src + (uintptr_t)kb * F::BS) & 15);
                     acc = chunk_generic<FMT>(slot, phi, kn, xr_row + kb, acc);
+                }
                 __syncwarp();
                 ++consumed;
                 if (ic.valid) {
@@ -511,44 +513,101 @@ __global__ void __launch_bounds__(kThreads, 1) rowwin_kernel(const __grid_consta
     }
 }
 
-int g_max_smem[64];
-std::once_flag g_smem_once[64];
+struct DevInfo {
+    int max_smem_block = 0;   // opt-in maximum per CTA
+    int max_smem_sm = 0;
+    int reserved_per_block = 0;
+    int sms = 1;
+};
+DevInfo g_dev[64];
+std::once_flag g_dev_once[64];
 
-int max_smem_optin(int dev)
+const DevInfo &dev_info(int dev)
 {
-    std::call_once(g_smem_once[dev & 63], [dev] {
-        int v = 0;
-        cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        g_max_smem[dev & 63] = v;
+    std::call_once(g_dev_once[dev & 63], [dev] {
+        DevInfo &d = g_dev[dev & 63];
+        cudaDeviceGetAttribute(&d.max_smem_block, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        cudaDeviceGetAttribute(&d.max_smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+        cudaDeviceGetAttribute(&d.reserved_per_block, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaGetLastError();
+        if (d.sms < 1) d.sms = 1;
     });
-    return g_max_smem[dev & 63];
+    return g_dev[dev & 63];
 }
 
-template <int FMT>
-size_t smem_bytes(int n_x, int nb, int stages)
+int fmt_group(int fmt) { return fmt == RF_MXFP4 ? 16 : 8; }
+
+// Chunk of `kc` blocks and its slot size.  Aligned rows copy exactly KC*BS
+// bytes; others need up to 15 bytes of rounding on either side.  Slots are an
+// odd number of 16-byte units so the 32 lanes' 16-byte loads spread over all
+// banks.
+struct ChunkGeom {
+    int kc, slot;
+};
+ChunkGeom chunk_geom(int fmt, bool aligned)
 {
-    return (size_t)n_x * nb * sizeof(XRec) + (size_t)kNW * stages * kRows * slot_bytes<FMT>() +
+    const int bs = (int)block_bytes_of(fmt);
+    if (aligned) {
+        // A dense [32][kc*bs] tensor box; kc*bs = 144 or 272 bytes, an odd
+        // number of 16-byte units.
+        const int kc = fmt_group(fmt);
+        return {kc, kc * bs};
+    }
+    const int kc = 8;
+    int n = (kc * bs + 30 + 15) / 16 * 16;
+    if ((n / 16) % 2 == 0) n += 16;
+    return {kc, n};
+}
+
+size_t smem_bytes(int n_x, int nb, int stages, int slot)
+{
+    return (((size_t)n_x * nb * sizeof(XRec) + 127) & ~(size_t)127) +
+           (size_t)kNW * stages * kRows * slot +
            (size_t)kNW * stages * sizeof(uint64_t) + (size_t)kNW * 32 * sizeof(float);
 }
 
-size_t smem_for(int fmt, int n_x, int nb, int stages)
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 {
-    switch (fmt) {
-    case RF_Q4_0: return smem_bytes<RF_Q4_0>(n_x, nb, stages);
-    case RF_Q8_0: return smem_bytes<RF_Q8_0>(n_x, nb, stages);
-    default: return smem_bytes<RF_MXFP4>(n_x, nb, stages);
-    }
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        cudaGetLastError();
+    });
+    return fn;
 }
 
-template <int FMT>
-rf_status launch_fmt(const KParams &p, int grid, size_t smem, bool pdl, cudaStream_t stream)
+// 2-D view of `rows` rows of `rb` bytes at `base` as uint16 elements; boxes of
+// 32 rows x `chunk` bytes.
+bool encode_rows_map(CUtensorMap *m, const void *base, int64_t rows, int64_t rb, int chunk)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)(rb / 2), (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)rb};
+    const cuuint32_t box[2] = {(cuuint32_t)(chunk / 2), (cuuint32_t)kRows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int FMT, bool TMA>
+rf_status launch_fmt(const KParams &p, int grid, size_t smem, bool pdl, cudaStream_t stream,
+                     int dev)
 {
     static std::once_flag attr_once[64];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    const int maxs = max_smem_optin(dev);
+    const int maxs = dev_info(dev).max_smem_block;
     std::call_once(attr_once[dev & 63], [maxs] {
-        cudaFuncSetAttribute(rowwin_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, maxs);
+        cudaFuncSetAttribute(rowwin_kernel<FMT, TMA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             maxs);
     });
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
@@ -562,7 +621,7 @@ rf_status launch_fmt(const KParams &p, int grid, size_t smem, bool pdl, cudaStre
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    if (cudaLaunchKernelEx(&cfg, rowwin_kernel<FMT>, p) != cudaSuccess) return RF_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, rowwin_kernel<FMT, TMA>, p) != cudaSuccess) return RF_ERR_CUDA;
     return RF_OK;
 }
 
@@ -597,10 +656,12 @@ rf_status last_cuda_error() { return cudaGetLastError() == cudaSuccess ? RF_OK :
 
 int num_sms()
 {
-    int dev = 0, n = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    return n > 0 ? n : 1;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 1;
+    }
+    return dev_info(dev).sms;
 }
 
 int64_t max_in_dim(int fmt, int n_x)
@@ -611,8 +672,9 @@ int64_t max_in_dim(int fmt, int n_x)
         cudaGetLastError();
         return 0;
     }
-    const size_t maxs = (size_t)max_smem_optin(dev);
-    const size_t fixed = smem_for(fmt, n_x, 0, 1);
+    const size_t maxs = (size_t)dev_info(dev).max_smem_block;
+    const int slot = std::max(chunk_geom(fmt, true).slot, chunk_geom(fmt, false).slot);
+    const size_t fixed = smem_bytes(n_x, 0, 1, slot);
     if (maxs <= fixed) return 0;
     return (int64_t)((maxs - fixed) / ((size_t)n_x * sizeof(XRec))) * 32;
 }
@@ -660,13 +722,29 @@ rf_status launch_rowwin(const LaunchDesc &d, cudaStream_t stream)
         cudaGetLastError();
         return RF_ERR_CUDA;
     }
-    const size_t maxs = (size_t)max_smem_optin(dev);
-    if (maxs == 0) return RF_ERR_CUDA;
-    int stages = 3;
-    while (stages > 0 && smem_for(d.fmt, d.n_x, nb, stages) > maxs) --stages;
-    if (stages == 0) return RF_ERR_TOO_LARGE;
-    const size_t smem = smem_for(d.fmt, d.n_x, nb, stages);
-    const int sms = num_sms();
+    const DevInfo &di = dev_info(dev);
+    if (di.max_smem_block == 0) return RF_ERR_CUDA;
+
+    // Rows are 16-byte aligned when the row bytes are (weights are 16-byte
+    // aligned): then chunks are copied exactly.
+    const bool aligned = RB % 16 == 0;
+    const ChunkGeom geo = chunk_geom(d.fmt, aligned);
+    // Prefer two CTAs per SM (16 warps) with at least 2 stages; else one CTA
+    // with up to 4 stages.
+    const size_t per2 = (size_t)di.max_smem_sm / 2 - (size_t)di.reserved_per_block;
+    int ctas_per_sm = 0, stages = 0;
+    for (int st = 4; st >= 2 && !ctas_per_sm; --st)
+        if (smem_bytes(d.n_x, nb, st, geo.slot) <= per2) {
+            ctas_per_sm = 2;
+            stages = st;
+        }
+    for (int st = 4; st >= 1 && !ctas_per_sm; --st)
+        if (smem_bytes(d.n_x, nb, st, geo.slot) <= (size_t)di.max_smem_block) {
+            ctas_per_sm = 1;
+            stages = st;
+        }
+    if (!ctas_per_sm) return RF_ERR_TOO_LARGE;
+    const size_t smem = smem_bytes(d.n_x, nb, stages, geo.slot);
 
     // Launch in batches of kMaxJobs windows.
     for (int base = 0; base < d.n_jobs; base += kMaxJobs) {
@@ -677,10 +755,39 @@ rf_status launch_rowwin(const LaunchDesc &d, cudaStream_t stream)
         for (int i = 0; i < nj; ++i) {
             p.jobs[i] = d.jobs[base + i];
             p.jobs[i].group_begin = total;
-            p.jobs[i].aligned = (RB % 16 == 0) ? 1 : 0;
+            p.jobs[i].aligned = aligned ? 1 : 0;
             total += (p.jobs[i].n_rows + kRows - 1) / kRows;
         }
         if (total == 0) continue;
+        if (aligned) {
+            // One tensor map per distinct weight base, covering every row the
+            // batch's jobs can touch.
+            const void *bases[kMaxMaps];
+            int64_t extent[kMaxMaps];
+            int n_maps = 0;
+            for (int i = 0; i < nj; ++i) {
+                Job &J = p.jobs[i];
+                for (int t = 0; t < J.n_terms; ++t) {
+                    Term &T = J.term[t];
+                    const int64_t need = T.expert_slot >= 0 ? J.expert_count * J.expert_rows
+                                                            : J.row0 + J.n_rows;
+                    int m = 0;
+                    while (m < n_maps && bases[m] != T.W) ++m;
+                    if (m == n_maps) {
+                        if (n_maps == kMaxMaps) return RF_ERR_TOO_LARGE;
+                        bases[m] = T.W;
+                        extent[m] = 0;
+                        ++n_maps;
+                    }
+                    extent[m] = std::max(extent[m], need);
+                    T.tmap = m;
+                }
+            }
+            for (int m = 0; m < n_maps; ++m)
+                if (extent[m] > 0x7fffffffLL ||
+                    !encode_rows_map(&p.maps[m], bases[m], extent[m], RB, geo.slot))
+                    return RF_ERR_CUDA;
+        }
         for (int s = 0; s < d.n_x; ++s) p.x[s] = d.x[s];
         p.expert_idx = d.expert_idx;
         p.n_jobs = nj;
@@ -688,13 +795,23 @@ rf_status launch_rowwin(const LaunchDesc &d, cudaStream_t stream)
         p.nb = nb;
         p.total_groups = total;
         p.stages = stages;
+        p.kc = geo.kc;
+        p.slot = geo.slot;
         p.prefetch_early = d.any_expert ? 0 : 1;
-        const int grid = std::min(total, sms);
+        const int grid = std::min(total, ctas_per_sm * di.sms);
         rf_status st;
-        switch (d.fmt) {
-        case RF_Q4_0: st = launch_fmt<RF_Q4_0>(p, grid, smem, d.pdl, stream); break;
-        case RF_Q8_0: st = launch_fmt<RF_Q8_0>(p, grid, smem, d.pdl, stream); break;
-        default: st = launch_fmt<RF_MXFP4>(p, grid, smem, d.pdl, stream); break;
+        if (aligned) {
+            switch (d.fmt) {
+            case RF_Q4_0: st = launch_fmt<RF_Q4_0, true>(p, grid, smem, d.pdl, stream, dev); break;
+            case RF_Q8_0: st = launch_fmt<RF_Q8_0, true>(p, grid, smem, d.pdl, stream, dev); break;
+            default: st = launch_fmt<RF_MXFP4, true>(p, grid, smem, d.pdl, stream, dev); break;
+            }
+        } else {
+            switch (d.fmt) {
+            case RF_Q4_0: st = launch_fmt<RF_Q4_0, false>(p, grid, smem, d.pdl, stream, dev); break;
+            case RF_Q8_0: st = launch_fmt<RF_Q8_0, false>(p, grid, smem, d.pdl, stream, dev); break;
+            default: st = launch_fmt<RF_MXFP4, false>(p, grid, smem, d.pdl, stream, dev); break;
+            }
         }
         if (st != RF_OK) return st;
     }

@@ -25,6 +25,8 @@ struct Term {
     const uint8_t *W;     // row 0 of the matrix (or of the stacked tensor)
     int32_t xslot;        // which activation vector multiplies this matrix
     int32_t expert_slot;  // >= 0: add expert_idx[expert_slot]*expert_rows rows to W
+    int32_t tmap;         // filled by the launcher: tensor map of W (aligned rows)
+    int32_t pad;
 };
 
 // One window of rows [row0, row0+n_rows) taken from every term's matrix.
@@ -34,6 +36,7 @@ struct Job {
     const float *weights;   // per-term weights (device) for kCombineSum, or nullptr
     int64_t row0;
     int64_t expert_rows;
+    int64_t expert_count;   // experts in the stacked tensor (expert terms)
     int32_t n_rows;
     int32_t n_terms;
     int32_t combine;

@@ -169,11 +169,12 @@ rf_status rf_moe_ffn(int fmt, const float *router_logits, int n_expert, int top_
             Job &J = jobs[nj++];
             std::memset(&J, 0, sizeof(J));
             const int64_t r0 = j * br_ff;
-            J.term[0] = Term{static_cast<const uint8_t *>(gate), 0, k};
-            J.term[1] = Term{static_cast<const uint8_t *>(up), 0, k};
+            J.term[0] = Term{static_cast<const uint8_t *>(gate), 0, k, 0, 0};
+            J.term[1] = Term{static_cast<const uint8_t *>(up), 0, k, 0, 0};
             J.y = h + (int64_t)k * n_ff + r0;
             J.row0 = r0;
             J.expert_rows = n_ff;
+            J.expert_count = n_expert;
             J.n_rows = (int32_t)(r0 + br_ff < n_ff ? br_ff : n_ff - r0);
             J.n_terms = 2;
             J.combine = kCombineSwiGLU;
@@ -199,11 +200,12 @@ rf_status rf_moe_ffn(int fmt, const float *router_logits, int n_expert, int top_
         Job &J = jobs[nj++];
         std::memset(&J, 0, sizeof(J));
         const int64_t r0 = j * br_embd;
-        for (int k = 0; k < top_k; ++k) J.term[k] = Term{static_cast<const uint8_t *>(down), k, k};
+        for (int k = 0; k < top_k; ++k) J.term[k] = Term{static_cast<const uint8_t *>(down), k, k, 0, 0};
         J.y = y + r0;
         J.weights = wts;
         J.row0 = r0;
         J.expert_rows = n_embd;
+        J.expert_count = n_expert;
         J.n_rows = (int32_t)(r0 + br_embd < n_embd ? br_embd : n_embd - r0);
         J.n_terms = top_k;
         J.combine = kCombineSum;

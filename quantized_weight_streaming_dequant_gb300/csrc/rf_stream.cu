@@ -217,7 +217,7 @@ rf_status rf_stream_linear(int fmt, const void *host_W, int64_t in_dim, int64_t 
             return RF_ERR_CUDA;
         Job J;
         std::memset(&J, 0, sizeof(J));
-        J.term[0] = Term{dst, 0, -1};
+        J.term[0] = Term{dst, 0, -1, 0, 0};
         J.y = y + (r0 - row_start);
         J.n_rows = (int32_t)nr;
         J.n_terms = 1;
