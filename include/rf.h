@@ -131,6 +131,23 @@ typedef struct rf_window {
 RF_API rf_status rf_gemv_batch(int fmt, int64_t in_dim, int n_windows,
                                const rf_window *windows, void *stream);
 
+/* Launch flags for the *_ex variants.
+ * RF_CHAIN: no kernel still pending on `stream` writes the weights of this call
+ *   (weights are static during inference).  The launch may then start before
+ *   the previous kernel on the stream finishes and copy its weights while that
+ *   kernel drains (programmatic dependent launch); it still waits for that
+ *   kernel before reading x.  Copies and memsets are never overtaken.  Without
+ *   the flag a launch starts only after the previous work completes. */
+#define RF_CHAIN 1u
+
+/* rf_gemv / rf_gemv_batch with launch flags (RF_CHAIN); otherwise identical,
+ * including bit-identical results. */
+RF_API rf_status rf_gemv_ex(int fmt, const void *W, int64_t row_start, int64_t row_end,
+                            int64_t in_dim, const float *x, float *y, unsigned flags,
+                            void *stream);
+RF_API rf_status rf_gemv_batch_ex(int fmt, int64_t in_dim, int n_windows,
+                                  const rf_window *windows, unsigned flags, void *stream);
+
 /* ------------------------------------------------------------ activations */
 /* h[i] = silu(g[i]) * u[i], silu(z) = z/(1+exp(-z)) (RAMforge, "Milestone 3";
  * the SwiGLU between gate/up and down).  Device pointers, n >= 0. */
@@ -149,6 +166,12 @@ RF_API rf_status rf_gelu(const float *z, float *h, int64_t n, void *stream);
 RF_API rf_status rf_ffn_swiglu(int fmt, const void *gate, const void *up, const void *down,
                                int64_t n_ff, int64_t n_embd, const float *x, float *y,
                                float *h, void *stream);
+
+/* rf_ffn_swiglu with launch flags: RF_CHAIN applies to its first launch (the
+ * second one is always chained to the first). */
+RF_API rf_status rf_ffn_swiglu_ex(int fmt, const void *gate, const void *up, const void *down,
+                                  int64_t n_ff, int64_t n_embd, const float *x, float *y,
+                                  float *h, unsigned flags, void *stream);
 
 /* ------------------------------------------- host-streamed row windows */
 /* An arena is a bounded ring of device memory plus a copy stream and events

@@ -21,6 +21,7 @@ FORMATS = {"Q4_0": Q4_0, "Q8_0": Q8_0, "MXFP4": MXFP4}
 BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, MXFP4: 17}
 
 OK = 0
+CHAIN = 1   # RF_CHAIN launch flag
 STATUS = {0: "RF_OK", 1: "RF_ERR_INVALID_ARG", 2: "RF_ERR_UNSUPPORTED_FMT",
           3: "RF_ERR_NOT_PINNED", 4: "RF_ERR_ARENA_TOO_SMALL", 5: "RF_ERR_CUDA",
           6: "RF_ERR_TIMEOUT", 7: "RF_ERR_OOM", 8: "RF_ERR_MISALIGNED", 9: "RF_ERR_TOO_LARGE"}
@@ -54,6 +55,9 @@ _SIGS = {
     "rf_dequantize": ([_I, _P, _I64, _P, _P], _I),
     "rf_gemv": ([_I, _P, _I64, _I64, _I64, _P, _P, _P], _I),
     "rf_gemv_batch": ([_I, _I64, _I, ctypes.POINTER(Window), _P], _I),
+    "rf_gemv_ex": ([_I, _P, _I64, _I64, _I64, _P, _P, ctypes.c_uint, _P], _I),
+    "rf_gemv_batch_ex": ([_I, _I64, _I, ctypes.POINTER(Window), ctypes.c_uint, _P], _I),
+    "rf_ffn_swiglu_ex": ([_I, _P, _P, _P, _I64, _I64, _P, _P, _P, ctypes.c_uint, _P], _I),
     "rf_swiglu": ([_P, _P, _P, _I64, _P], _I),
     "rf_gelu": ([_P, _P, _I64, _P], _I),
     "rf_ffn_swiglu": ([_I, _P, _P, _P, _I64, _I64, _P, _P, _P, _P], _I),
@@ -142,21 +146,23 @@ def dequantize(fmt: int, W, n_blocks: int | None = None, out=None, stream=None):
     return out
 
 
-def gemv(fmt: int, W, row_start: int, row_end: int, in_dim: int, x, y=None, stream=None):
+def gemv(fmt: int, W, row_start: int, row_end: int, in_dim: int, x, y=None, stream=None,
+         flags: int = 0):
     import torch
     if y is None:
         y = torch.empty(max(row_end - row_start, 0), dtype=torch.float32, device=x.device)
-    _check(lib().rf_gemv(fmt, _dev_ptr(W, "W"), row_start, row_end, in_dim, _dev_ptr(x, "x"),
-                         _dev_ptr(y, "y") if y.numel() else 1, _stream(stream)), "rf_gemv")
+    _check(lib().rf_gemv_ex(fmt, _dev_ptr(W, "W"), row_start, row_end, in_dim, _dev_ptr(x, "x"),
+                            _dev_ptr(y, "y") if y.numel() else 1, flags, _stream(stream)),
+           "rf_gemv")
     return y
 
 
-def gemv_batch(fmt: int, in_dim: int, windows, stream=None):
+def gemv_batch(fmt: int, in_dim: int, windows, stream=None, flags: int = 0):
     """windows: list of (W, row_start, row_end, x, y) with device tensors."""
     arr = (Window * max(len(windows), 1))()
     for i, (W, r0, r1, x, y) in enumerate(windows):
         arr[i] = Window(_dev_ptr(W, "W"), r0, r1, _dev_ptr(x, "x"), _dev_ptr(y, "y"))
-    _check(lib().rf_gemv_batch(fmt, in_dim, len(windows), arr, _stream(stream)),
+    _check(lib().rf_gemv_batch_ex(fmt, in_dim, len(windows), arr, flags, _stream(stream)),
            "rf_gemv_batch")
 
 
@@ -177,13 +183,13 @@ def gelu(z, h=None, stream=None):
 
 
 def ffn_swiglu(fmt: int, gate, up, down, n_ff: int, n_embd: int, x, y=None, h=None,
-               stream=None):
+               stream=None, flags: int = 0):
     import torch
     y = torch.empty(n_embd, dtype=torch.float32, device=x.device) if y is None else y
     h = torch.empty(n_ff, dtype=torch.float32, device=x.device) if h is None else h
-    _check(lib().rf_ffn_swiglu(fmt, _dev_ptr(gate, "gate"), _dev_ptr(up, "up"),
-                               _dev_ptr(down, "down"), n_ff, n_embd, _dev_ptr(x, "x"),
-                               _dev_ptr(y, "y"), _dev_ptr(h, "h"), _stream(stream)),
+    _check(lib().rf_ffn_swiglu_ex(fmt, _dev_ptr(gate, "gate"), _dev_ptr(up, "up"),
+                                  _dev_ptr(down, "down"), n_ff, n_embd, _dev_ptr(x, "x"),
+                                  _dev_ptr(y, "y"), _dev_ptr(h, "h"), flags, _stream(stream)),
            "rf_ffn_swiglu")
     return y, h
 

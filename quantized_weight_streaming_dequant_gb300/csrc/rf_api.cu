@@ -143,6 +143,12 @@ rf_status rf_dequantize(int fmt, const void *W, int64_t n_blocks, float *out, vo
 rf_status rf_gemv(int fmt, const void *W, int64_t row_start, int64_t row_end, int64_t in_dim,
                   const float *x, float *y, void *stream)
 {
+    return rf_gemv_ex(fmt, W, row_start, row_end, in_dim, x, y, 0u, stream);
+}
+
+rf_status rf_gemv_ex(int fmt, const void *W, int64_t row_start, int64_t row_end, int64_t in_dim,
+                     const float *x, float *y, unsigned flags, void *stream)
+{
     if (!fmt_ok(fmt)) return RF_ERR_UNSUPPORTED_FMT;
     if (!W || !x || !y || in_dim <= 0 || in_dim % 32 != 0 || row_start < 0 ||
         row_end < row_start)
@@ -166,11 +172,18 @@ rf_status rf_gemv(int fmt, const void *W, int64_t row_start, int64_t row_end, in
     d.n_jobs = 1;
     d.x[0] = x;
     d.n_x = 1;
+    d.pdl = (flags & RF_CHAIN) != 0;
     return launch_rowwin(d, static_cast<cudaStream_t>(stream));
 }
 
 rf_status rf_gemv_batch(int fmt, int64_t in_dim, int n_windows, const rf_window *windows,
                         void *stream)
+{
+    return rf_gemv_batch_ex(fmt, in_dim, n_windows, windows, 0u, stream);
+}
+
+rf_status rf_gemv_batch_ex(int fmt, int64_t in_dim, int n_windows, const rf_window *windows,
+                           unsigned flags, void *stream)
 {
     if (!fmt_ok(fmt)) return RF_ERR_UNSUPPORTED_FMT;
     if (in_dim <= 0 || in_dim % 32 != 0 || n_windows < 0 || (n_windows > 0 && !windows))
@@ -208,6 +221,7 @@ rf_status rf_gemv_batch(int fmt, int64_t in_dim, int n_windows, const rf_window 
     d.jobs = jobs;
     d.n_jobs = n_windows;
     d.n_x = n_x;
+    d.pdl = (flags & RF_CHAIN) != 0;
     return launch_rowwin(d, static_cast<cudaStream_t>(stream));
 }
 
@@ -230,6 +244,13 @@ rf_status rf_gelu(const float *z, float *h, int64_t n, void *stream)
 rf_status rf_ffn_swiglu(int fmt, const void *gate, const void *up, const void *down,
                         int64_t n_ff, int64_t n_embd, const float *x, float *y, float *h,
                         void *stream)
+{
+    return rf_ffn_swiglu_ex(fmt, gate, up, down, n_ff, n_embd, x, y, h, 0u, stream);
+}
+
+rf_status rf_ffn_swiglu_ex(int fmt, const void *gate, const void *up, const void *down,
+                           int64_t n_ff, int64_t n_embd, const float *x, float *y, float *h,
+                           unsigned flags, void *stream)
 {
     if (!fmt_ok(fmt)) return RF_ERR_UNSUPPORTED_FMT;
     if (!gate || !up || !down || !x || !y || !h || n_ff <= 0 || n_embd <= 0 ||
@@ -257,6 +278,7 @@ rf_status rf_ffn_swiglu(int fmt, const void *gate, const void *up, const void *d
     d1.n_jobs = 1;
     d1.x[0] = x;
     d1.n_x = 1;
+    d1.pdl = (flags & RF_CHAIN) != 0;
     rf_status st = launch_rowwin(d1, s);
     if (st != RF_OK) return st;
     // Phase 2: walk down by output dimension (programmatic dependent launch:

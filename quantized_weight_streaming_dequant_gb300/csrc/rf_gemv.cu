@@ -93,7 +93,7 @@ struct KParams {
     const float *x[kMaxX];
     const int32_t *expert_idx;
     int32_t n_jobs, n_x, nb, total_groups;
-    int32_t stages, kc, slot, prefetch_early;
+    int32_t stages, kc, slot, prefetch_early, max_terms, pad;
 };
 
 // Element of the 32-block packed into byte `byte` of plane word `word`, in the
@@ -117,55 +117,71 @@ __device__ __forceinline__ float exp2i(int k)
                      : __uint_as_float(1u << (k + 149));
 }
 
+// Fixed-point digits of one 32-element activation block, computed by a quad
+// of consecutive lanes: lane `part` of the quad owns plane words 2*part and
+// 2*part+1 (8 elements).  All 32 lanes of the warp must call it (shuffles);
+// lanes with active == false only take part in the shuffles.
 template <int FMT>
-__device__ void make_xrec(const float *xb, XRec *out)
+__device__ __forceinline__ void make_xrec_quad(const float *xb, int part, bool active, XRec *out)
 {
-    float v[32];
-    if ((reinterpret_cast<uintptr_t>(xb) & 15u) == 0) {
+    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (active) {
+        // element index of v[i] within the block
+        int ei[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float4 f = reinterpret_cast<const float4 *>(xb)[i];
-            v[4 * i] = f.x;
-            v[4 * i + 1] = f.y;
-            v[4 * i + 2] = f.z;
-            v[4 * i + 3] = f.w;
+        for (int i = 0; i < 8; ++i) ei[i] = elem_of<FMT>(2 * part + (i >> 2), i & 3);
+        if ((reinterpret_cast<uintptr_t>(xb) & 15u) == 0) {
+            if constexpr (FMT == RF_MXFP4) {
+                const float4 a = reinterpret_cast<const float4 *>(xb)[part];       // 4k..4k+3
+                const float4 b = reinterpret_cast<const float4 *>(xb)[4 + part];   // 16+4k..
+                v[0] = a.x; v[1] = b.x; v[2] = a.y; v[3] = b.y;
+                v[4] = a.z; v[5] = b.z; v[6] = a.w; v[7] = b.w;
+            } else {
+                const float4 a = reinterpret_cast<const float4 *>(xb)[2 * part];
+                const float4 b = reinterpret_cast<const float4 *>(xb)[2 * part + 1];
+                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+                v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = xb[ei[i]];
         }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = xb[i];
     }
     float m = 0.f;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(v[i]));
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
     // m < 2^e with e from the exponent field (zero/subnormal m: e = -125).
     const int biased = (int)(__float_as_uint(m) >> 23);
     const int e = biased == 0 ? -125 : biased - 126;
     const int s = 15 - e;   // |x * 2^s| < 2^15; s in [-114, 140]
     const float f1 = exp2i(min(s, 127)), f2 = exp2i(max(s - 127, 0));
-    int X[32];
+    int X[8];
+    int sum = 0;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
+    for (int i = 0; i < 8; ++i) {
         // round to nearest even through the 1.5*2^23 magic constant
         const float t = (v[i] * f1) * f2 + 12582912.0f;
         const int q = (int)(__float_as_uint(t) - 0x4b400000u);
         X[i] = max(-32767, min(32767, q));
+        sum += X[i];
     }
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    if (!active) return;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) {
-        const uint32_t a = (uint32_t)X[elem_of<FMT>(w, 0)], b = (uint32_t)X[elem_of<FMT>(w, 1)];
-        const uint32_t c = (uint32_t)X[elem_of<FMT>(w, 2)], d = (uint32_t)X[elem_of<FMT>(w, 3)];
-        out->p0[w] = prmt(prmt(a, b, 0x0040u), prmt(c, d, 0x0040u), 0x5410u);
-        out->p1[w] = prmt(prmt(a, b, 0x0051u), prmt(c, d, 0x0051u), 0x5410u);
+    for (int h = 0; h < 2; ++h) {
+        const uint32_t a = (uint32_t)X[4 * h], b = (uint32_t)X[4 * h + 1];
+        const uint32_t c = (uint32_t)X[4 * h + 2], d = (uint32_t)X[4 * h + 3];
+        out->p0[2 * part + h] = prmt(prmt(a, b, 0x0040u), prmt(c, d, 0x0040u), 0x5410u);
+        out->p1[2 * part + h] = prmt(prmt(a, b, 0x0051u), prmt(c, d, 0x0051u), 0x5410u);
     }
-    int corr = 0;
-    if constexpr (FMT == RF_Q4_0) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) corr += X[i];
-        corr *= -8;
+    if (part == 0) {
+        out->corr = FMT == RF_Q4_0 ? -8 * sum : 0;
+        out->scale = exp2i(-s);
+        out->pad[0] = out->pad[1] = 0;
     }
-    out->corr = corr;
-    out->scale = exp2i(-s);
-    out->pad[0] = out->pad[1] = 0;
 }
 
 // Integer dot of one block's quant words with the block's digit planes;
@@ -250,34 +266,54 @@ __device__ __forceinline__ uint32_t word_at(const uint32_t *v, int byte)
     return sh ? __funnelshift_r(v[w], v[w + 1], 8 * sh) : v[w];
 }
 
+// One group of G blocks (a multiple of 16 bytes) held in registers.
+template <int FMT>
+struct GroupRegs {
+    static constexpr int NV = FmtT<FMT>::G * FmtT<FMT>::BS / 16;
+    uint32_t v[4 * NV + 1];
+};
+
+template <int FMT>
+__device__ __forceinline__ void load_group(const uint8_t *src, GroupRegs<FMT> &r)
+{
+#pragma unroll
+    for (int i = 0; i < GroupRegs<FMT>::NV; ++i) {
+        const uint4 t = reinterpret_cast<const uint4 *>(src)[i];
+        r.v[4 * i] = t.x;
+        r.v[4 * i + 1] = t.y;
+        r.v[4 * i + 2] = t.z;
+        r.v[4 * i + 3] = t.w;
+    }
+    r.v[4 * GroupRegs<FMT>::NV] = 0;
+}
+
+template <int FMT>
+__device__ __forceinline__ float compute_group(const GroupRegs<FMT> &r, const XRec *xr, float acc)
+{
+    using F = FmtT<FMT>;
+#pragma unroll
+    for (int b = 0; b < F::G; ++b) {
+        const int o = b * F::BS;
+        const uint32_t hdr = word_at(r.v, o);
+        uint32_t q[F::QW];
+#pragma unroll
+        for (int k = 0; k < F::QW; ++k) q[k] = word_at(r.v, o + F::HDR + 4 * k);
+        const XRec &x = xr[b];
+        acc = fmaf(block_idot<FMT>(q, x), block_scale<FMT>(hdr, x.scale), acc);
+    }
+    return acc;
+}
+
 // Aligned chunk: `kn` blocks (a multiple of G) at a 16-byte aligned address.
 template <int FMT>
 __device__ __forceinline__ float chunk_aligned(const uint8_t *src, int kn, const XRec *xr,
                                                float acc)
 {
     using F = FmtT<FMT>;
-    constexpr int NV = F::G * F::BS / 16;   // 16-byte units per group of G blocks
     for (int g0 = 0; g0 < kn; g0 += F::G) {
-        uint32_t v[4 * NV + 1];
-#pragma unroll
-        for (int i = 0; i < NV; ++i) {
-            const uint4 t = reinterpret_cast<const uint4 *>(src + g0 * F::BS)[i];
-            v[4 * i] = t.x;
-            v[4 * i + 1] = t.y;
-            v[4 * i + 2] = t.z;
-            v[4 * i + 3] = t.w;
-        }
-        v[4 * NV] = 0;
-#pragma unroll
-        for (int b = 0; b < F::G; ++b) {
-            const int o = b * F::BS;
-            const uint32_t hdr = word_at(v, o);
-            uint32_t q[F::QW];
-#pragma unroll
-            for (int k = 0; k < F::QW; ++k) q[k] = word_at(v, o + F::HDR + 4 * k);
-            const XRec &r = xr[g0 + b];
-            acc = fmaf(block_idot<FMT>(q, r), block_scale<FMT>(hdr, r.scale), acc);
-        }
+        GroupRegs<FMT> r;
+        load_group<FMT>(src + g0 * F::BS, r);
+        acc = compute_group<FMT>(r, xr + g0, acc);
     }
     return acc;
 }
@@ -349,8 +385,15 @@ __device__ __forceinline__ const uint8_t *term_matrix(const KParams &p, const Jo
 // TMA = true: rows are 16-byte aligned and each chunk of a warp (32 rows x kc
 // blocks) is one 2-D tensor copy issued by lane 0.  TMA = false: any
 // alignment; each lane copies its own row's chunk with a 1-D bulk copy.
+// Minimum CTAs per SM the register budget is sized for: 272-byte aligned
+// chunks (Q8_0, MXFP4) need more registers and their shared memory allows
+// one CTA per SM anyway.
 template <int FMT, bool TMA>
-__global__ void __launch_bounds__(kThreads, 2) rowwin_kernel(const __grid_constant__ KParams p)
+constexpr int min_ctas() { return (TMA && FMT != RF_Q4_0) ? 1 : 2; }
+
+template <int FMT, bool TMA>
+__global__ void __launch_bounds__(kThreads, min_ctas<FMT, TMA>())
+    rowwin_kernel(const __grid_constant__ KParams p)
 {
     using F = FmtT<FMT>;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -359,6 +402,7 @@ __global__ void __launch_bounds__(kThreads, 2) rowwin_kernel(const __grid_consta
     const int ST = p.stages;
     const int KC = p.kc;
     const int SLOT = p.slot;
+    const int NT = p.max_terms;
     const int64_t RB = (int64_t)nb * F::BS;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -368,7 +412,9 @@ __global__ void __launch_bounds__(kThreads, 2) rowwin_kernel(const __grid_consta
     off += (size_t)kNW * ST * kRows * SLOT;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + off);
     off += (size_t)kNW * ST * sizeof(uint64_t);
-    float *red = reinterpret_cast<float *>(smem + off);
+    float *red = reinterpret_cast<float *>(smem + off);   // [2][NT][kNW][32]
+    off += (size_t)2 * NT * kNW * 32 * sizeof(float);
+    int *cnt = reinterpret_cast<int *>(smem + off);       // arrivals per parity, then groups done
 
     const int G_total = p.total_groups;
     const int g_lo = (int)((int64_t)blockIdx.x * G_total / gridDim.x);
@@ -381,6 +427,7 @@ __global__ void __launch_bounds__(kThreads, 2) rowwin_kernel(const __grid_consta
     const int n_chunks = (kb_hi - kb_lo + KC - 1) / KC;
 
     if (lane < ST) mbar_init(&bars[warp * ST + lane], TMA ? 1 : 32);
+    if (threadIdx.x < 3) cnt[threadIdx.x] = 0;
     fence_barrier_init();
     __syncthreads();
 
@@ -389,11 +436,12 @@ __global__ void __launch_bounds__(kThreads, 2) rowwin_kernel(const __grid_consta
 
     Cursor ic{g_lo, 0, 0, 0, g_lo < g_hi && n_chunks > 0};
     if (ic.valid) cursor_fix_job(p, ic);
-    int issued = 0;
+    int is = 0;   // stage of the next copy
 
     auto issue = [&](const Cursor &cu) {
-        const int stage = issued % ST;
-        uint64_t *bar = &my_bars[stage];
+        uint64_t *bar = &my_bars[is];
+        uint8_t *dst = my_slots + (size_t)is * kRows * SLOT;
+        if (++is == ST) is = 0;
         const Job &J = p.jobs[cu.j];
         if constexpr (TMA) {
             if (lane == 0) {
@@ -402,29 +450,25 @@ __global__ void __launch_bounds__(kThreads, 2) rowwin_kernel(const __grid_consta
                 if (T.expert_slot >= 0) y += (int64_t)p.expert_idx[T.expert_slot] * J.expert_rows;
                 const int x = (kb_lo + cu.c * KC) * F::BS / 2;   // uint16 units
                 mbar_arrive_expect_tx(bar, (uint32_t)(kRows * SLOT));
-                tma_2d_g2s(my_slots + (size_t)stage * kRows * SLOT, &p.maps[T.tmap], x, (int)y,
-                           bar);
+                tma_2d_g2s(dst, &p.maps[T.tmap], x, (int)y, bar);
             }
-            ++issued;
-            return;
-        }
-        const int64_t rowrel = (int64_t)(cu.g - J.group_begin) * kRows + lane;
-        if (rowrel < J.n_rows) {
-            const uint8_t *W = term_matrix(p, J, cu.t, RB);
-            const int kb = kb_lo + cu.c * KC;
-            const int kn = min(KC, kb_hi - kb);
-            const uintptr_t s = reinterpret_cast<uintptr_t>(W + (J.row0 + rowrel) * RB +
-                                                            (int64_t)kb * F::BS);
-            const uintptr_t a = s & ~(uintptr_t)15;
-            const uintptr_t e = (s + (uintptr_t)kn * F::BS + 15) & ~(uintptr_t)15;
-            const uint32_t bytes = (uint32_t)(e - a);
-            mbar_arrive_expect_tx(bar, bytes);
-            bulk_g2s(my_slots + ((size_t)stage * kRows + lane) * SLOT,
-                     reinterpret_cast<const void *>(a), bytes, bar);
         } else {
-            mbar_arrive(bar);
+            const int64_t rowrel = (int64_t)(cu.g - J.group_begin) * kRows + lane;
+            if (rowrel < J.n_rows) {
+                const uint8_t *W = term_matrix(p, J, cu.t, RB);
+                const int kb = kb_lo + cu.c * KC;
+                const int kn = min(KC, kb_hi - kb);
+                const uintptr_t s = reinterpret_cast<uintptr_t>(W + (J.row0 + rowrel) * RB +
+                                                                (int64_t)kb * F::BS);
+                const uintptr_t a = s & ~(uintptr_t)15;
+                const uintptr_t e = (s + (uintptr_t)kn * F::BS + 15) & ~(uintptr_t)15;
+                const uint32_t bytes = (uint32_t)(e - a);
+                mbar_arrive_expect_tx(bar, bytes);
+                bulk_g2s(dst + (size_t)lane * SLOT, reinterpret_cast<const void *>(a), bytes, bar);
+            } else {
+                mbar_arrive(bar);
+            }
         }
-        ++issued;
     };
 
     // Weights never depend on the previous kernel: start their copies first
@@ -444,54 +488,104 @@ __global__ void __launch_bounds__(kThreads, 2) rowwin_kernel(const __grid_consta
         }
     }
 
-    // Activation digits for every x of the launch, once per CTA.
-    for (int idx = threadIdx.x; idx < p.n_x * nb; idx += kThreads) {
-        const int s = idx / nb, b = idx - s * nb;
-        make_xrec<FMT>(p.x[s] + 32 * (int64_t)b, &xrec[idx]);
+    // Activation digits for every x of the launch, once per CTA, four lanes
+    // per 32-element block.
+    {
+        const int n_rec = p.n_x * nb;
+        for (int base = 0; base < 4 * n_rec; base += kThreads) {
+            const int idx = base + (int)threadIdx.x;
+            const bool active = idx < 4 * n_rec;
+            const int rec = active ? idx >> 2 : 0;
+            const int sl = rec / nb, b = rec - sl * nb;
+            make_xrec_quad<FMT>(p.x[sl] + 32 * (int64_t)b, idx & 3, active, &xrec[rec]);
+        }
     }
     __syncthreads();
 
-    int consumed = 0;
+    int cs = 0;          // stage of the next chunk to consume
+    uint32_t cph = 0;    // its mbarrier phase parity
     int j = 0;
     for (int g = g_lo; g < g_hi; ++g) {
         while (j < p.n_jobs && g >= p.jobs[j].group_begin + groups_of(p.jobs[j])) ++j;
         const Job &J = p.jobs[j];
+        const int n_terms = J.n_terms;
+        const bool aligned = TMA || J.aligned;
         const int64_t rowrel = (int64_t)(g - J.group_begin) * kRows + lane;
         const bool row_ok = rowrel < J.n_rows;
-        float yacc = 0.f, gate = 0.f;
-        for (int t = 0; t < J.n_terms; ++t) {
+        const int gi = g - g_lo, par = gi & 1;
+        float *red_g = red + (size_t)par * NT * kNW * 32;
+        // The partial buffer of this parity was last used by group gi-2; wait
+        // until that group has been combined.
+        if (gi >= 2) {
+            volatile int *done = cnt + 2;
+            if (*done < gi - 1) {
+                const unsigned long long t0 = globaltimer_ns();
+                while (*done < gi - 1) {
+                    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                        record_status(&g_device_status, RF_ERR_TIMEOUT);
+                        break;
+                    }
+                }
+            }
+            __threadfence_block();
+        }
+        for (int t = 0; t < n_terms; ++t) {
             float acc = 0.f;
             uintptr_t row_src = 0;
-            if (!TMA && !J.aligned && row_ok)
+            if (!aligned && row_ok)
                 row_src = reinterpret_cast<uintptr_t>(term_matrix(p, J, t, RB) +
                                                       (J.row0 + rowrel) * RB);
             const XRec *xr_row = xrec + (size_t)J.term[t].xslot * nb;
             for (int c = 0; c < n_chunks; ++c) {
-                const int stage = consumed % ST;
-                const uint32_t parity = (uint32_t)((consumed / ST) & 1);
-                mbar_wait_bounded(&my_bars[stage], parity, &g_device_status);
-                const uint8_t *slot = my_slots + ((size_t)stage * kRows + lane) * SLOT;
+                mbar_wait_bounded(&my_bars[cs], cph, &g_device_status);
+                const uint8_t *slot = my_slots + ((size_t)cs * kRows + lane) * SLOT;
+                if (++cs == ST) {
+                    cs = 0;
+                    cph ^= 1u;
+                }
                 const int kb = kb_lo + c * KC;
                 const int kn = min(KC, kb_hi - kb);
-                if (TMA || J.aligned) {
+                if constexpr (TMA) {
+                    // A chunk is exactly one group: copy it to registers, hand
+                    // the slot straight back to the copy engine, then compute.
+                    GroupRegs<FMT> r;
+                    load_group<FMT>(slot, r);
+                    __syncwarp();
+                    if (ic.valid) {
+                        issue(ic);
+                        cursor_advance(p, ic, n_chunks, g_hi);
+                    }
+                    acc = compute_group<FMT>(r, xr_row + kb, acc);
+                    continue;
+                }
+                if (aligned) {
                     acc = chunk_aligned<FMT>(slot, kn, xr_row + kb, acc);
                 } else {
                     const int phi = (int)((row_src + (uintptr_t)kb * F::BS) & 15);
                     acc = chunk_generic<FMT>(slot, phi, kn, xr_row + kb, acc);
                 }
                 __syncwarp();
-                ++consumed;
                 if (ic.valid) {
                     issue(ic);
                     cursor_advance(p, ic, n_chunks, g_hi);
                 }
             }
-            red[warp * 32 + lane] = acc;
-            __syncthreads();
-            if (warp == 0) {
-                float dot = red[lane];
+            red_g[((size_t)t * kNW + warp) * 32 + lane] = acc;
+        }
+        // The last warp to finish this group sums the partials in warp order.
+        __syncwarp();
+        __threadfence_block();
+        int arrived = 0;
+        if (lane == 0) arrived = atomicAdd(&cnt[par], 1);
+        arrived = __shfl_sync(0xffffffffu, arrived, 0);
+        if (arrived == kNW - 1) {
+            __threadfence_block();
+            float yacc = 0.f, gate = 0.f;
+            for (int t = 0; t < n_terms; ++t) {
+                const float *rt = red_g + (size_t)t * kNW * 32 + lane;
+                float dot = rt[0];
 #pragma unroll
-                for (int w = 1; w < kNW; ++w) dot += red[w * 32 + lane];
+                for (int w = 1; w < kNW; ++w) dot += rt[w * 32];
                 if (J.combine == kCombineSwiGLU) {
                     if (t == 0)
                         gate = dot;
@@ -503,12 +597,17 @@ __global__ void __launch_bounds__(kThreads, 2) rowwin_kernel(const __grid_consta
                     yacc = t == 0 ? dot : yacc + dot;
                 }
             }
-            __syncthreads();
-        }
-        if (warp == 0 && row_ok) {
-            float out = yacc;
-            if (J.act == kActGelu) out = 0.5f * out * (1.f + erff(out * 0.70710678118654752f));
-            J.y[rowrel] = out;
+            if (row_ok) {
+                float out = yacc;
+                if (J.act == kActGelu) out = 0.5f * out * (1.f + erff(out * 0.70710678118654752f));
+                J.y[rowrel] = out;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                cnt[par] = 0;
+                __threadfence_block();
+                atomicAdd(&cnt[2], 1);
+            }
         }
     }
 }
@@ -560,11 +659,11 @@ ChunkGeom chunk_geom(int fmt, bool aligned)
     return {kc, n};
 }
 
-size_t smem_bytes(int n_x, int nb, int stages, int slot)
+size_t smem_bytes(int n_x, int nb, int stages, int slot, int max_terms)
 {
     return (((size_t)n_x * nb * sizeof(XRec) + 127) & ~(size_t)127) +
-           (size_t)kNW * stages * kRows * slot +
-           (size_t)kNW * stages * sizeof(uint64_t) + (size_t)kNW * 32 * sizeof(float);
+           (size_t)kNW * stages * kRows * slot + (size_t)kNW * stages * sizeof(uint64_t) +
+           (size_t)2 * max_terms * kNW * 32 * sizeof(float) + 4 * sizeof(int);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
@@ -674,7 +773,7 @@ int64_t max_in_dim(int fmt, int n_x)
     }
     const size_t maxs = (size_t)dev_info(dev).max_smem_block;
     const int slot = std::max(chunk_geom(fmt, true).slot, chunk_geom(fmt, false).slot);
-    const size_t fixed = smem_bytes(n_x, 0, 1, slot);
+    const size_t fixed = smem_bytes(n_x, 0, 1, slot, kMaxTerms);
     if (maxs <= fixed) return 0;
     return (int64_t)((maxs - fixed) / ((size_t)n_x * sizeof(XRec))) * 32;
 }
@@ -729,22 +828,25 @@ rf_status launch_rowwin(const LaunchDesc &d, cudaStream_t stream)
     // aligned): then chunks are copied exactly.
     const bool aligned = RB % 16 == 0;
     const ChunkGeom geo = chunk_geom(d.fmt, aligned);
+    int max_terms = 1;
+    for (int i = 0; i < d.n_jobs; ++i) max_terms = std::max(max_terms, (int)d.jobs[i].n_terms);
     // Prefer two CTAs per SM (16 warps) with at least 2 stages; else one CTA
     // with up to 4 stages.
     const size_t per2 = (size_t)di.max_smem_sm / 2 - (size_t)di.reserved_per_block;
     int ctas_per_sm = 0, stages = 0;
-    for (int st = 4; st >= 2 && !ctas_per_sm; --st)
-        if (smem_bytes(d.n_x, nb, st, geo.slot) <= per2) {
+    const bool two_ok = !aligned || d.fmt == RF_Q4_0;   // register budget (min_ctas)
+    for (int st = 4; st >= 2 && !ctas_per_sm && two_ok; --st)
+        if (smem_bytes(d.n_x, nb, st, geo.slot, max_terms) <= per2) {
             ctas_per_sm = 2;
             stages = st;
         }
     for (int st = 4; st >= 1 && !ctas_per_sm; --st)
-        if (smem_bytes(d.n_x, nb, st, geo.slot) <= (size_t)di.max_smem_block) {
+        if (smem_bytes(d.n_x, nb, st, geo.slot, max_terms) <= (size_t)di.max_smem_block) {
             ctas_per_sm = 1;
             stages = st;
         }
     if (!ctas_per_sm) return RF_ERR_TOO_LARGE;
-    const size_t smem = smem_bytes(d.n_x, nb, stages, geo.slot);
+    const size_t smem = smem_bytes(d.n_x, nb, stages, geo.slot, max_terms);
 
     // Launch in batches of kMaxJobs windows.
     for (int base = 0; base < d.n_jobs; base += kMaxJobs) {
@@ -797,6 +899,7 @@ rf_status launch_rowwin(const LaunchDesc &d, cudaStream_t stream)
         p.stages = stages;
         p.kc = geo.kc;
         p.slot = geo.slot;
+        p.max_terms = max_terms;
         p.prefetch_early = d.any_expert ? 0 : 1;
         const int grid = std::min(total, ctas_per_sm * di.sms);
         rf_status st;

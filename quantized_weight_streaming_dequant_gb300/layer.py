@@ -31,14 +31,17 @@ class DenseLayer:
     w_up: object
     w_down: object
 
-    def step(self, x, attn, x_ffn, out, stream=None):
-        """out: dict of device tensors q, k, v, o, h, y (preallocated)."""
+    def step(self, x, attn, x_ffn, out, stream=None, chain: bool = True):
+        """out: dict of device tensors q, k, v, o, h, y (preallocated).  With
+        `chain`, each launch copies its (static) weights while the previous
+        kernel on the stream drains (RF_CHAIN)."""
         d = self.d_model
+        fl = rf.CHAIN if chain else 0
         rf.gemv_batch(self.fmt, d, [(self.wq, 0, d, x, out["q"]), (self.wk, 0, d, x, out["k"]),
-                                    (self.wv, 0, d, x, out["v"])], stream=stream)
-        rf.gemv(self.fmt, self.wo, 0, d, d, attn, out["o"], stream=stream)
+                                    (self.wv, 0, d, x, out["v"])], stream=stream, flags=fl)
+        rf.gemv(self.fmt, self.wo, 0, d, d, attn, out["o"], stream=stream, flags=fl)
         rf.ffn_swiglu(self.fmt, self.w_gate, self.w_up, self.w_down, self.d_ff, d, x_ffn,
-                      out["y"], out["h"], stream=stream)
+                      out["y"], out["h"], stream=stream, flags=fl)
 
     def weight_bytes(self) -> int:
         rb_d = rf.row_bytes(self.fmt, self.d_model)

@@ -1,0 +1,131 @@
+"""GPU parity at the workloads' full sizes, in the launch configuration the
+benchmark times, against the oracle on every row (the oracle is fast enough
+for these) or on sampled rows (host-streamed FFN)."""
+import numpy as np
+import pytest
+
+import oracle
+import synthetic as syn
+from gpu_helpers import assert_gemv_close, dev_tensor, gemv_tol, swiglu_h_tol
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def rf():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import quantized_weight_streaming_dequant_gb300 as m
+    from quantized_weight_streaming_dequant_gb300 import build
+    build.build()
+    m.lib()
+    yield m
+    assert m.device_status() == m.OK
+
+
+def bits(a):
+    return np.asarray(a, dtype=np.float32).view(np.uint32)
+
+
+def test_streamed_q8_0_gemv_512x2048(rf):
+    """512x2048 Q8_0 streamed from pinned host memory in 128-row blocks."""
+    import torch
+    c = syn.C1
+    fmt, rows, in_dim = c["fmt"], c["out_dim"], c["in_dim"]
+    W = syn.quant_matrix(fmt, rows, in_dim, c["seed"])
+    x = syn.normal_f32(in_dim, c["seed"] + 1)
+    arena = rf.Arena(c["arena_bytes"])
+    try:
+        host = torch.from_numpy(W).pin_memory()
+        for depth in (c["depth"], 1):
+            y = arena.stream_linear(fmt, host, in_dim, 0, rows, c["block_rows"], depth,
+                                    dev_tensor(x)).cpu().numpy()
+            ref = oracle.gemv(fmt, W, 0, rows, in_dim, x)
+            assert_gemv_close(y, ref, gemv_tol(fmt, W, 0, rows, in_dim, x), f"depth {depth}")
+            assert arena.stats()["last_block_rows"] == 128
+        resident = rf.gemv(fmt, dev_tensor(W), 0, rows, in_dim, dev_tensor(x)).cpu().numpy()
+        assert np.array_equal(bits(y), bits(resident))
+    finally:
+        arena.close()
+
+
+def test_dense_q4_0_layer_4096_11008(rf):
+    """One dense decode layer: QKV batched, O, gate/up + SwiGLU, down; every row
+    of every projection against the oracle; chained and unchained launches give
+    identical bits."""
+    import torch
+    from quantized_weight_streaming_dequant_gb300.layer import DenseLayer
+    fmt, d, f = syn.Q4_0, syn.C2["d_model"], syn.C2["d_ff"]
+    s = syn.C2["seed"] * 1000
+    mats = [syn.quant_matrix(fmt, d, d, s + i, threads=8) for i in range(4)]
+    mats += [syn.quant_matrix(fmt, f, d, s + 4, threads=8), syn.quant_matrix(fmt, f, d, s + 5, threads=8),
+             syn.quant_matrix(fmt, d, f, s + 6, threads=8)]
+    L = DenseLayer(fmt, d, f, *[dev_tensor(m) for m in mats])
+    x, attn, x_ffn = (syn.normal_f32(d, 101), syn.normal_f32(d, 102), syn.normal_f32(d, 103))
+    outs = []
+    for chain in (False, True):
+        out = {k: torch.empty(n, device="cuda") for k, n in
+               (("q", d), ("k", d), ("v", d), ("o", d), ("h", f), ("y", d))}
+        L.step(dev_tensor(x), dev_tensor(attn), dev_tensor(x_ffn), out, chain=chain)
+        torch.cuda.synchronize()
+        outs.append({k: v.cpu().numpy() for k, v in out.items()})
+    for k in outs[0]:
+        assert np.array_equal(bits(outs[0][k]), bits(outs[1][k])), k
+    o = outs[1]
+    for name, M, inp in (("q", mats[0], x), ("k", mats[1], x), ("v", mats[2], x),
+                         ("o", mats[3], attn)):
+        assert_gemv_close(o[name], oracle.gemv(fmt, M, 0, d, d, inp), gemv_tol(fmt, M, 0, d, d, inp),
+                          name)
+    g_ref = oracle.gemv(fmt, mats[4], 0, f, d, x_ffn)
+    u_ref = oracle.gemv(fmt, mats[5], 0, f, d, x_ffn)
+    h_ref = oracle.silu_vec(g_ref) * u_ref
+    assert_gemv_close(o["h"], h_ref, swiglu_h_tol(g_ref, u_ref, gemv_tol(fmt, mats[4], 0, f, d, x_ffn),
+                                                  gemv_tol(fmt, mats[5], 0, f, d, x_ffn)), "h")
+    assert_gemv_close(o["y"], oracle.gemv(fmt, mats[6], 0, d, f, o["h"].astype(np.float64)),
+                      gemv_tol(fmt, mats[6], 0, d, f, o["h"]), "y")
+
+
+def test_moe_mxfp4_128x2880x2880_top4(rf):
+    from test_gpu_parity import moe_check
+    c = syn.C3
+    moe_check(rf, c["fmt"], c["n_expert"], c["n_ff"], c["n_embd"], c["top_k"], c["block_rows"],
+              seed=c["seed"])
+
+
+def test_streamed_ffn_q8_0_24576x6144_sampled(rf):
+    """Two layers of the host-streamed FFN at full size (256 MiB arena,
+    512-row blocks, depth 4); 256 sampled rows of each projection against the
+    oracle, fed the GPU's own intermediate activations."""
+    import torch
+    from quantized_weight_streaming_dequant_gb300.layer import StreamedFFN
+    c = syn.C4
+    fmt, d, f = c["fmt"], c["d_model"], c["d_ff"]
+    rng = np.random.default_rng(0)
+    arena = rf.Arena(c["arena_bytes"])
+    try:
+        for l in range(2):
+            up = torch.empty((f, rf.row_bytes(fmt, d)), dtype=torch.uint8).pin_memory()
+            dn = torch.empty((d, rf.row_bytes(fmt, f)), dtype=torch.uint8).pin_memory()
+            syn.quant_matrix(fmt, f, d, c["seed"] * 1000 + 2 * l, out=up.numpy(), threads=8)
+            syn.quant_matrix(fmt, d, f, c["seed"] * 1000 + 2 * l + 1, out=dn.numpy(), threads=8)
+            layer = StreamedFFN(fmt, d, f, up, dn)
+            x = syn.normal_f32(d, 5000 + l)
+            u = torch.empty(f, device="cuda")
+            h = torch.empty(f, device="cuda")
+            y = torch.empty(d, device="cuda")
+            layer.step(arena, dev_tensor(x), u, h, y, c["block_rows"], c["depth"])
+            torch.cuda.synchronize()
+            u_, h_, y_ = u.cpu().numpy(), h.cpu().numpy(), y.cpu().numpy()
+            W_up, W_dn = up.numpy(), dn.numpy()
+            for r in rng.choice(f, 256, replace=False):
+                ref = oracle.gemv(fmt, W_up, int(r), int(r) + 1, d, x)
+                assert_gemv_close(u_[r:r + 1], ref, gemv_tol(fmt, W_up, int(r), int(r) + 1, d, x))
+            assert np.allclose(h_, oracle.gelu_vec(u_), rtol=1e-5, atol=1e-6)
+            for r in rng.choice(d, 256, replace=False):
+                ref = oracle.gemv(fmt, W_dn, int(r), int(r) + 1, f, h_.astype(np.float64))
+                assert_gemv_close(y_[r:r + 1], ref, gemv_tol(fmt, W_dn, int(r), int(r) + 1, f, h_))
+        st = arena.stats()
+        assert st["last_block_rows"] == 512 and st["slots"] == 5
+        assert st["peak_bytes"] == 5 * 512 * rf.row_bytes(fmt, f)
+    finally:
+        arena.close()
