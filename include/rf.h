@@ -253,6 +253,27 @@ RF_API rf_status rf_moe_ffn(int fmt, const float *router_logits, int n_expert, i
                             int64_t n_embd, int64_t block_rows, const float *x, float *y,
                             void *workspace, void *stream);
 
+/* rf_moe_ffn without a workspace argument, for callers that cannot allocate
+ * device memory: for example an engine that plans all of its device memory
+ * once at start-up and forbids allocations afterwards, or a decode loop that
+ * must not call cudaMalloc/cudaFree because those synchronize the device.
+ * (The source pages have no counterpart to this entry point.)
+ * The scratch it needs lives in a fixed device array inside the library,
+ * RF_MOE_STATIC_MAX_H floats of activations plus the routing result, which
+ * every GPU that loads the library keeps until the process exits.  Limit:
+ * top_k * n_ff <= RF_MOE_STATIC_MAX_H, else RF_ERR_TOO_LARGE before any work.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the one array and it keeps the last call's
+ * contents; nothing in it needs to start at zero.  Calls whose kernels
+ * overlap on the GPU (different streams, or different host threads) race on
+ * it: serialise them.  Arguments and results otherwise as rf_moe_ffn. */
+#define RF_MOE_STATIC_MAX_H 65536
+RF_API rf_status rf_moe_ffn_noalloc(int fmt, const float *router_logits, int n_expert, int top_k,
+                                    const void *gate, const void *up, const void *down,
+                                    int64_t n_ff, int64_t n_embd, int64_t block_rows,
+                                    const float *x, float *y, void *stream);
+
 /* --------------------------------------------------------------- status */
 /* Synchronizes the current device, then reports and clears the device status
  * word that kernels set when a bounded wait times out (RF_OK if none).

@@ -70,6 +70,7 @@ _SIGS = {
     "rf_moe_route": ([_P, _I, _I, _P, _P, _P], _I),
     "rf_moe_workspace_bytes": ([_I, _I64, _I64, _I64], _SZ),
     "rf_moe_ffn": ([_I, _P, _I, _I, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P], _I),
+    "rf_moe_ffn_noalloc": ([_I, _P, _I, _I, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P], _I),
     "rf_device_status": ([], _I),
 }
 
@@ -275,6 +276,18 @@ def moe_ffn(fmt: int, logits, top_k: int, gate, up, down, n_ff: int, n_embd: int
                             n_ff, n_embd, block_rows, _dev_ptr(x, "x"), _dev_ptr(y, "y"),
                             _dev_ptr(workspace, "workspace"), _stream(stream)), "rf_moe_ffn")
     return y, workspace
+
+
+def moe_ffn_noalloc(fmt: int, logits, top_k: int, gate, up, down, n_ff: int, n_embd: int,
+                    block_rows: int, x, y, stream=None):
+    """rf_moe_ffn_noalloc: the library's own fixed scratch instead of a
+    workspace; y must be preallocated."""
+    _check(lib().rf_moe_ffn_noalloc(fmt, _dev_ptr(logits, "logits"), logits.numel(), top_k,
+                                    _dev_ptr(gate, "gate"), _dev_ptr(up, "up"),
+                                    _dev_ptr(down, "down"), n_ff, n_embd, block_rows,
+                                    _dev_ptr(x, "x"), _dev_ptr(y, "y"), _stream(stream)),
+           "rf_moe_ffn_noalloc")
+    return y
 
 
 def moe_workspace_views(workspace, top_k: int, n_ff: int):

@@ -8,6 +8,7 @@
 // so there is no host synchronisation between routing and the projections.
 #include <cfloat>
 #include <cstring>
+#include <mutex>
 
 #include "rf_device.cuh"
 #include "rf_internal.h"
@@ -87,6 +88,37 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const float *__r
 }
 
 size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
+
+// Scratch for rf_moe_ffn_noalloc: routing result (two 256-byte slots) and up
+// to RF_MOE_STATIC_MAX_H activations, laid out like an rf_moe_ffn workspace.
+constexpr size_t kStaticScratchBytes = 512 + sizeof(float) * (size_t)RF_MOE_STATIC_MAX_H;
+static __device__ __align__(256) unsigned char g_moe_scratch[kStaticScratchBytes];
+
+// Device address of g_moe_scratch per device.  In host code the symbol is
+// only a stand-in; its device address comes from cudaGetSymbolAddress with
+// the device current.
+std::mutex g_scratch_mu;
+void *g_scratch_ptr[64] = {};
+
+rf_status static_scratch(void **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return RF_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_moe_scratch) != cudaSuccess || !ptr) {
+            cudaGetLastError();
+            return RF_ERR_CUDA;
+        }
+        g_scratch_ptr[dev] = ptr;
+    }
+    *out = g_scratch_ptr[dev];
+    return RF_OK;
+}
 
 }  // namespace
 
@@ -221,6 +253,21 @@ rf_status rf_moe_ffn(int fmt, const float *router_logits, int n_expert, int top_
     d2.any_expert = true;
     d2.pdl = true;
     return launch_rowwin(d2, s);
+}
+
+rf_status rf_moe_ffn_noalloc(int fmt, const float *router_logits, int n_expert, int top_k,
+                             const void *gate, const void *up, const void *down, int64_t n_ff,
+                             int64_t n_embd, int64_t block_rows, const float *x, float *y,
+                             void *stream)
+{
+    if (top_k < 1 || top_k > kMaxTopK || n_ff <= 0) return RF_ERR_INVALID_ARG;
+    if ((int64_t)top_k * n_ff > RF_MOE_STATIC_MAX_H) return RF_ERR_TOO_LARGE;
+    if (rf_moe_workspace_bytes(top_k, n_ff, n_embd, block_rows) > kStaticScratchBytes)
+        return RF_ERR_TOO_LARGE;
+    void *scratch = nullptr;
+    if (const rf_status st = static_scratch(&scratch)) return st;
+    return rf_moe_ffn(fmt, router_logits, n_expert, top_k, gate, up, down, n_ff, n_embd,
+                      block_rows, x, y, scratch, stream);
 }
 
 }  // extern "C"
