@@ -181,8 +181,9 @@ RF_API rf_status rf_ffn_swiglu_ex(int fmt, const void *gate, const void *up, con
  * current device.  An arena is used by one host thread at a time. */
 typedef struct rf_arena rf_arena;
 RF_API rf_status rf_arena_create(size_t bytes, rf_arena **out);
-/* Waits for the arena's outstanding copies and readers, then frees it.
- * NULL is a no-op. */
+/* Waits for the arena's outstanding eager copies and readers, then frees it
+ * (launches of graphs captured with it must have finished).  NULL is a
+ * no-op. */
 RF_API void rf_arena_destroy(rf_arena *arena);
 
 /* Host-side block plan for walking n_rows rows of rf_row_bytes(fmt,in_dim)
@@ -205,6 +206,14 @@ RF_API rf_status rf_stream_plan(int fmt, int64_t in_dim, int64_t n_rows, int64_t
  * blocks.  host_W: page-locked host pointer to row 0 of the [out][in] matrix
  * (16-byte aligned); x, y: device.  Output is bit-identical to rf_gemv on the
  * same rows for every block_rows and depth.
+ * The call may be made while `stream` is being captured into a CUDA graph:
+ * the copies and GEMVs become graph nodes with the same dependencies, and
+ * later captured calls on the same arena keep prefetching across call
+ * boundaries.  The first call after a switch between eager use and a capture
+ * (or between two captures) is ordered after all work already on `stream`;
+ * a graph must be launched on the stream it was captured from (or after the
+ * arena's earlier work has finished), and one capture at a time may use an
+ * arena.
  * Errors: as rf_gemv; RF_ERR_NOT_PINNED if host_W is not page-locked;
  * RF_ERR_ARENA_TOO_SMALL; RF_ERR_INVALID_ARG for depth < 0 or depth > 64. */
 RF_API rf_status rf_stream_linear(int fmt, const void *host_W, int64_t in_dim,

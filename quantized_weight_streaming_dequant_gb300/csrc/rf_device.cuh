@@ -100,6 +100,22 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared issued by one thread (LDGSTS);
+// dst and src 16-byte aligned.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+                 : "memory");
+}
+
+// Arrive on `bar` once all of this thread's earlier cp.async copies have
+// landed (the barrier's expected count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
 // 2-D tiled tensor copy global -> shared: the box at coordinates (x, y) of the
 // tensor map lands densely in shared memory (128-byte aligned destination).
 __device__ __forceinline__ void tma_2d_g2s(void *dst, const void *tmap, int x, int y, uint64_t *bar)

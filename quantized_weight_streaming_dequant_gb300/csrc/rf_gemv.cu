@@ -87,14 +87,19 @@ struct FmtT<RF_MXFP4> {
 
 constexpr int kMaxMaps = 16;   // distinct weight tensors per launch (tensor-map path)
 
-struct KParams {
-    CUtensorMap maps[kMaxMaps];   // 2-D views [rows][row bytes] of 16-byte aligned rows
-    Job jobs[kMaxJobs];
+// Kernel parameters.  Two sizes: launches with at most 4 windows and 4 weight
+// tensors (nearly all of them) pass about 1.6 KB instead of 18 KB per launch.
+template <int NJ, int NM>
+struct KParamsT {
+    CUtensorMap maps[NM];   // 2-D views [rows][row bytes] of 16-byte aligned rows
+    Job jobs[NJ];
     const float *x[kMaxX];
     const int32_t *expert_idx;
     int32_t n_jobs, n_x, nb, total_groups;
-    int32_t stages, kc, slot, prefetch_early, max_terms, pad;
+    int32_t stages, kc, slot, prefetch_early, max_terms, n_maps;
 };
+using KParamsSmall = KParamsT<4, 4>;
+using KParamsLarge = KParamsT<kMaxJobs, kMaxMaps>;
 
 // Element of the 32-block packed into byte `byte` of plane word `word`, in the
 // order the format's decoder produces quant bytes.
@@ -354,31 +359,31 @@ struct Cursor {
 
 __device__ __forceinline__ int groups_of(const Job &J) { return (J.n_rows + kRows - 1) / kRows; }
 
-__device__ __forceinline__ void cursor_fix_job(const KParams &p, Cursor &cu)
+__device__ __forceinline__ void cursor_fix_job(const Job *jobs, int n_jobs, Cursor &cu)
 {
-    while (cu.j < p.n_jobs && cu.g >= p.jobs[cu.j].group_begin + groups_of(p.jobs[cu.j])) ++cu.j;
+    while (cu.j < n_jobs && cu.g >= jobs[cu.j].group_begin + groups_of(jobs[cu.j])) ++cu.j;
 }
 
-__device__ __forceinline__ void cursor_advance(const KParams &p, Cursor &cu, int n_chunks,
-                                               int g_hi)
+__device__ __forceinline__ void cursor_advance(const Job *jobs, int n_jobs, Cursor &cu,
+                                               int n_chunks, int g_hi)
 {
     if (++cu.c < n_chunks) return;
     cu.c = 0;
-    if (++cu.t < p.jobs[cu.j].n_terms) return;
+    if (++cu.t < jobs[cu.j].n_terms) return;
     cu.t = 0;
     if (++cu.g >= g_hi) {
         cu.valid = false;
         return;
     }
-    cursor_fix_job(p, cu);
+    cursor_fix_job(jobs, n_jobs, cu);
 }
 
-__device__ __forceinline__ const uint8_t *term_matrix(const KParams &p, const Job &J, int t,
-                                                      int64_t row_bytes)
+__device__ __forceinline__ const uint8_t *term_matrix(const int32_t *expert_idx, const Job &J,
+                                                      int t, int64_t row_bytes)
 {
     const Term &T = J.term[t];
     const uint8_t *W = T.W;
-    if (T.expert_slot >= 0) W += (int64_t)p.expert_idx[T.expert_slot] * J.expert_rows * row_bytes;
+    if (T.expert_slot >= 0) W += (int64_t)expert_idx[T.expert_slot] * J.expert_rows * row_bytes;
     return W;
 }
 
@@ -391,9 +396,9 @@ __device__ __forceinline__ const uint8_t *term_matrix(const KParams &p, const Jo
 template <int FMT, bool TMA>
 constexpr int min_ctas() { return (TMA && FMT != RF_Q4_0) ? 1 : 2; }
 
-template <int FMT, bool TMA>
+template <int FMT, bool TMA, class KP>
 __global__ void __launch_bounds__(kThreads, min_ctas<FMT, TMA>())
-    rowwin_kernel(const __grid_constant__ KParams p)
+    rowwin_kernel(const __grid_constant__ KP p)
 {
     using F = FmtT<FMT>;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -415,6 +420,9 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, TMA>())
     float *red = reinterpret_cast<float *>(smem + off);   // [2][NT][kNW][32]
     off += (size_t)2 * NT * kNW * 32 * sizeof(float);
     int *cnt = reinterpret_cast<int *>(smem + off);       // arrivals per parity, then groups done
+    off += 4 * sizeof(int);
+    Job *jobs = reinterpret_cast<Job *>(smem + off);      // this launch's jobs, read once
+    const int n_jobs = p.n_jobs;
 
     const int G_total = p.total_groups;
     const int g_lo = (int)((int64_t)blockIdx.x * G_total / gridDim.x);
@@ -428,6 +436,17 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, TMA>())
 
     if (lane < ST) mbar_init(&bars[warp * ST + lane], TMA ? 1 : 32);
     if (threadIdx.x < 3) cnt[threadIdx.x] = 0;
+    if constexpr (TMA) {
+        if ((int)threadIdx.x < p.n_maps)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.maps[threadIdx.x]))
+                         : "memory");
+    }
+    {   // copy the job table out of parameter space in one parallel pass
+        const int words = n_jobs * (int)(sizeof(Job) / 4);
+        const uint32_t *src = reinterpret_cast<const uint32_t *>(p.jobs);
+        uint32_t *dst = reinterpret_cast<uint32_t *>(jobs);
+        for (int i = threadIdx.x; i < words; i += kThreads) dst[i] = src[i];
+    }
     fence_barrier_init();
     __syncthreads();
 
@@ -435,14 +454,14 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, TMA>())
     uint64_t *my_bars = bars + warp * ST;
 
     Cursor ic{g_lo, 0, 0, 0, g_lo < g_hi && n_chunks > 0};
-    if (ic.valid) cursor_fix_job(p, ic);
+    if (ic.valid) cursor_fix_job(jobs, n_jobs, ic);
     int is = 0;   // stage of the next copy
 
     auto issue = [&](const Cursor &cu) {
         uint64_t *bar = &my_bars[is];
         uint8_t *dst = my_slots + (size_t)is * kRows * SLOT;
         if (++is == ST) is = 0;
-        const Job &J = p.jobs[cu.j];
+        const Job &J = jobs[cu.j];
         if constexpr (TMA) {
             if (lane == 0) {
                 const Term &T = J.term[cu.t];
@@ -453,40 +472,39 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, TMA>())
                 tma_2d_g2s(dst, &p.maps[T.tmap], x, (int)y, bar);
             }
         } else {
+            // Each lane copies its own row's chunk, rounded out to 16-byte
+            // boundaries, with 16-byte cp.async (issued by all lanes at once).
             const int64_t rowrel = (int64_t)(cu.g - J.group_begin) * kRows + lane;
             if (rowrel < J.n_rows) {
-                const uint8_t *W = term_matrix(p, J, cu.t, RB);
+                const uint8_t *W = term_matrix(p.expert_idx, J, cu.t, RB);
                 const int kb = kb_lo + cu.c * KC;
                 const int kn = min(KC, kb_hi - kb);
                 const uintptr_t s = reinterpret_cast<uintptr_t>(W + (J.row0 + rowrel) * RB +
                                                                 (int64_t)kb * F::BS);
                 const uintptr_t a = s & ~(uintptr_t)15;
                 const uintptr_t e = (s + (uintptr_t)kn * F::BS + 15) & ~(uintptr_t)15;
-                const uint32_t bytes = (uint32_t)(e - a);
-                mbar_arrive_expect_tx(bar, bytes);
-                bulk_g2s(dst + (size_t)lane * SLOT, reinterpret_cast<const void *>(a), bytes, bar);
-            } else {
-                mbar_arrive(bar);
+                uint8_t *d = dst + (size_t)lane * SLOT;
+                for (uintptr_t q = a; q < e; q += 16, d += 16)
+                    cp_async16(d, reinterpret_cast<const void *>(q));
             }
+            cp_async_arrive(bar);
         }
     };
 
-    // Weights never depend on the previous kernel: start their copies first
-    // (unless the rows come from a routing result the previous kernel writes).
+    // Weights never depend on the previous kernel: when this launch may
+    // overlap it (programmatic dependent launch), fill every stage before
+    // waiting (unless the rows come from a routing result the previous
+    // kernel writes).  A CTA that becomes resident while the previous kernel
+    // runs then holds its first chunks by the time the activations exist.
+    int primed = 0;
     if (p.prefetch_early) {
-        for (int s = 0; s < ST && ic.valid; ++s) {
+        for (; primed < ST && ic.valid; ++primed) {
             issue(ic);
-            cursor_advance(p, ic, n_chunks, g_hi);
+            cursor_advance(jobs, n_jobs, ic, n_chunks, g_hi);
         }
     }
     pdl_launch_dependents();
     pdl_wait();
-    if (!p.prefetch_early) {
-        for (int s = 0; s < ST && ic.valid; ++s) {
-            issue(ic);
-            cursor_advance(p, ic, n_chunks, g_hi);
-        }
-    }
 
     // Activation digits for every x of the launch, once per CTA, four lanes
     // per 32-element block.
@@ -506,8 +524,8 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, TMA>())
     uint32_t cph = 0;    // its mbarrier phase parity
     int j = 0;
     for (int g = g_lo; g < g_hi; ++g) {
-        while (j < p.n_jobs && g >= p.jobs[j].group_begin + groups_of(p.jobs[j])) ++j;
-        const Job &J = p.jobs[j];
+        while (j < n_jobs && g >= jobs[j].group_begin + groups_of(jobs[j])) ++j;
+        const Job &J = jobs[j];
         const int n_terms = J.n_terms;
         const bool aligned = TMA || J.aligned;
         const int64_t rowrel = (int64_t)(g - J.group_begin) * kRows + lane;
@@ -533,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, TMA>())
             float acc = 0.f;
             uintptr_t row_src = 0;
             if (!aligned && row_ok)
-                row_src = reinterpret_cast<uintptr_t>(term_matrix(p, J, t, RB) +
+                row_src = reinterpret_cast<uintptr_t>(term_matrix(p.expert_idx, J, t, RB) +
                                                       (J.row0 + rowrel) * RB);
             const XRec *xr_row = xrec + (size_t)J.term[t].xslot * nb;
             for (int c = 0; c < n_chunks; ++c) {
@@ -553,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, TMA>())
                     __syncwarp();
                     if (ic.valid) {
                         issue(ic);
-                        cursor_advance(p, ic, n_chunks, g_hi);
+                        cursor_advance(jobs, n_jobs, ic, n_chunks, g_hi);
                     }
                     acc = compute_group<FMT>(r, xr_row + kb, acc);
                     continue;
@@ -567,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, TMA>())
                 __syncwarp();
                 if (ic.valid) {
                     issue(ic);
-                    cursor_advance(p, ic, n_chunks, g_hi);
+                    cursor_advance(jobs, n_jobs, ic, n_chunks, g_hi);
                 }
             }
             red_g[((size_t)t * kNW + warp) * 32 + lane] = acc;
@@ -659,11 +677,12 @@ ChunkGeom chunk_geom(int fmt, bool aligned)
     return {kc, n};
 }
 
-size_t smem_bytes(int n_x, int nb, int stages, int slot, int max_terms)
+size_t smem_bytes(int n_x, int nb, int stages, int slot, int max_terms, int n_jobs)
 {
     return (((size_t)n_x * nb * sizeof(XRec) + 127) & ~(size_t)127) +
            (size_t)kNW * stages * kRows * slot + (size_t)kNW * stages * sizeof(uint64_t) +
-           (size_t)2 * max_terms * kNW * 32 * sizeof(float) + 4 * sizeof(int);
+           (size_t)2 * max_terms * kNW * 32 * sizeof(float) + 4 * sizeof(int) +
+           (size_t)n_jobs * sizeof(Job);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
@@ -698,15 +717,14 @@ bool encode_rows_map(CUtensorMap *m, const void *base, int64_t rows, int64_t rb,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int FMT, bool TMA>
-rf_status launch_fmt(const KParams &p, int grid, size_t smem, bool pdl, cudaStream_t stream,
-                     int dev)
+template <int FMT, bool TMA, class KP>
+rf_status launch_fmt(const KP &p, int grid, size_t smem, bool pdl, cudaStream_t stream, int dev)
 {
     static std::once_flag attr_once[64];
     const int maxs = dev_info(dev).max_smem_block;
     std::call_once(attr_once[dev & 63], [maxs] {
-        cudaFuncSetAttribute(rowwin_kernel<FMT, TMA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             maxs);
+        cudaFuncSetAttribute(rowwin_kernel<FMT, TMA, KP>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, maxs);
     });
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
@@ -720,8 +738,62 @@ rf_status launch_fmt(const KParams &p, int grid, size_t smem, bool pdl, cudaStre
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    if (cudaLaunchKernelEx(&cfg, rowwin_kernel<FMT, TMA>, p) != cudaSuccess) return RF_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, rowwin_kernel<FMT, TMA, KP>, p) != cudaSuccess) return RF_ERR_CUDA;
     return RF_OK;
+}
+
+template <class KP>
+rf_status launch_any(int fmt, bool tma, const KP &p, int grid, size_t smem, bool pdl,
+                     cudaStream_t stream, int dev)
+{
+    if (tma) {
+        switch (fmt) {
+        case RF_Q4_0: return launch_fmt<RF_Q4_0, true>(p, grid, smem, pdl, stream, dev);
+        case RF_Q8_0: return launch_fmt<RF_Q8_0, true>(p, grid, smem, pdl, stream, dev);
+        default: return launch_fmt<RF_MXFP4, true>(p, grid, smem, pdl, stream, dev);
+        }
+    }
+    switch (fmt) {
+    case RF_Q4_0: return launch_fmt<RF_Q4_0, false>(p, grid, smem, pdl, stream, dev);
+    case RF_Q8_0: return launch_fmt<RF_Q8_0, false>(p, grid, smem, pdl, stream, dev);
+    default: return launch_fmt<RF_MXFP4, false>(p, grid, smem, pdl, stream, dev);
+    }
+}
+
+// Tensor maps of recent weight tensors (host-side encoding is not free and
+// the same tensors recur every token).
+struct MapKey {
+    const void *base;
+    int64_t rows, rb;
+    int chunk, dev;
+    bool operator==(const MapKey &o) const
+    {
+        return base == o.base && rows == o.rows && rb == o.rb && chunk == o.chunk && dev == o.dev;
+    }
+};
+constexpr int kMapCache = 64;
+std::mutex g_map_mu;
+MapKey g_map_key[kMapCache];
+CUtensorMap g_map_val[kMapCache];
+int g_map_next = 0;
+
+bool cached_rows_map(CUtensorMap *m, const void *base, int64_t rows, int64_t rb, int chunk, int dev)
+{
+    const MapKey k{base, rows, rb, chunk, dev};
+    {
+        std::lock_guard<std::mutex> lock(g_map_mu);
+        for (int i = 0; i < kMapCache; ++i)
+            if (g_map_key[i] == k) {
+                *m = g_map_val[i];
+                return true;
+            }
+    }
+    if (!encode_rows_map(m, base, rows, rb, chunk)) return false;
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    g_map_key[g_map_next] = k;
+    g_map_val[g_map_next] = *m;
+    g_map_next = (g_map_next + 1) % kMapCache;
+    return true;
 }
 
 }  // namespace
@@ -773,7 +845,7 @@ int64_t max_in_dim(int fmt, int n_x)
     }
     const size_t maxs = (size_t)dev_info(dev).max_smem_block;
     const int slot = std::max(chunk_geom(fmt, true).slot, chunk_geom(fmt, false).slot);
-    const size_t fixed = smem_bytes(n_x, 0, 1, slot, kMaxTerms);
+    const size_t fixed = smem_bytes(n_x, 0, 1, slot, kMaxTerms, kMaxJobs);
     if (maxs <= fixed) return 0;
     return (int64_t)((maxs - fixed) / ((size_t)n_x * sizeof(XRec))) * 32;
 }
@@ -836,39 +908,38 @@ rf_status launch_rowwin(const LaunchDesc &d, cudaStream_t stream)
     int ctas_per_sm = 0, stages = 0;
     const bool two_ok = !aligned || d.fmt == RF_Q4_0;   // register budget (min_ctas)
     for (int st = 4; st >= 2 && !ctas_per_sm && two_ok; --st)
-        if (smem_bytes(d.n_x, nb, st, geo.slot, max_terms) <= per2) {
+        if (smem_bytes(d.n_x, nb, st, geo.slot, max_terms, std::min(d.n_jobs, kMaxJobs)) <= per2) {
             ctas_per_sm = 2;
             stages = st;
         }
     for (int st = 4; st >= 1 && !ctas_per_sm; --st)
-        if (smem_bytes(d.n_x, nb, st, geo.slot, max_terms) <= (size_t)di.max_smem_block) {
+        if (smem_bytes(d.n_x, nb, st, geo.slot, max_terms, std::min(d.n_jobs, kMaxJobs)) <= (size_t)di.max_smem_block) {
             ctas_per_sm = 1;
             stages = st;
         }
     if (!ctas_per_sm) return RF_ERR_TOO_LARGE;
-    const size_t smem = smem_bytes(d.n_x, nb, stages, geo.slot, max_terms);
+    const size_t smem = smem_bytes(d.n_x, nb, stages, geo.slot, max_terms, std::min(d.n_jobs, kMaxJobs));
 
     // Launch in batches of kMaxJobs windows.
     for (int base = 0; base < d.n_jobs; base += kMaxJobs) {
-        static thread_local KParams p;   // large (about 13 KB): keep it off the stack
-        std::memset(&p, 0, sizeof(p));
         const int nj = std::min(kMaxJobs, d.n_jobs - base);
+        static thread_local Job jobs[kMaxJobs];
         int total = 0;
         for (int i = 0; i < nj; ++i) {
-            p.jobs[i] = d.jobs[base + i];
-            p.jobs[i].group_begin = total;
-            p.jobs[i].aligned = aligned ? 1 : 0;
-            total += (p.jobs[i].n_rows + kRows - 1) / kRows;
+            jobs[i] = d.jobs[base + i];
+            jobs[i].group_begin = total;
+            jobs[i].aligned = aligned ? 1 : 0;
+            total += (jobs[i].n_rows + kRows - 1) / kRows;
         }
         if (total == 0) continue;
+        // One tensor map per distinct weight base, covering every row the
+        // batch's jobs can touch.
+        const void *bases[kMaxMaps];
+        int64_t extent[kMaxMaps];
+        int n_maps = 0;
         if (aligned) {
-            // One tensor map per distinct weight base, covering every row the
-            // batch's jobs can touch.
-            const void *bases[kMaxMaps];
-            int64_t extent[kMaxMaps];
-            int n_maps = 0;
             for (int i = 0; i < nj; ++i) {
-                Job &J = p.jobs[i];
+                Job &J = jobs[i];
                 for (int t = 0; t < J.n_terms; ++t) {
                     Term &T = J.term[t];
                     const int64_t need = T.expert_slot >= 0 ? J.expert_count * J.expert_rows
@@ -886,35 +957,41 @@ rf_status launch_rowwin(const LaunchDesc &d, cudaStream_t stream)
                 }
             }
             for (int m = 0; m < n_maps; ++m)
-                if (extent[m] > 0x7fffffffLL ||
-                    !encode_rows_map(&p.maps[m], bases[m], extent[m], RB, geo.slot))
-                    return RF_ERR_CUDA;
+                if (extent[m] > 0x7fffffffLL) return RF_ERR_TOO_LARGE;
         }
-        for (int s = 0; s < d.n_x; ++s) p.x[s] = d.x[s];
-        p.expert_idx = d.expert_idx;
-        p.n_jobs = nj;
-        p.n_x = d.n_x;
-        p.nb = nb;
-        p.total_groups = total;
-        p.stages = stages;
-        p.kc = geo.kc;
-        p.slot = geo.slot;
-        p.max_terms = max_terms;
-        p.prefetch_early = d.any_expert ? 0 : 1;
-        const int grid = std::min(total, ctas_per_sm * di.sms);
+        // Same number of groups (or one fewer) on every CTA.
+        const int max_grid = ctas_per_sm * di.sms;
+        const int per_cta = (total + max_grid - 1) / max_grid;
+        const int grid = (total + per_cta - 1) / per_cta;
+
+        auto fill = [&](auto &p) -> rf_status {
+            std::memcpy(p.jobs, jobs, sizeof(Job) * nj);
+            for (int m = 0; m < n_maps; ++m)
+                if (!cached_rows_map(&p.maps[m], bases[m], extent[m], RB, geo.slot, dev))
+                    return RF_ERR_CUDA;
+            for (int s2 = 0; s2 < kMaxX; ++s2) p.x[s2] = s2 < d.n_x ? d.x[s2] : nullptr;
+            p.expert_idx = d.expert_idx;
+            p.n_jobs = nj;
+            p.n_x = d.n_x;
+            p.nb = nb;
+            p.total_groups = total;
+            p.stages = stages;
+            p.kc = geo.kc;
+            p.slot = geo.slot;
+            p.prefetch_early = (d.pdl && !d.any_expert) ? 1 : 0;
+            p.max_terms = max_terms;
+            p.n_maps = n_maps;
+            return RF_OK;
+        };
         rf_status st;
-        if (aligned) {
-            switch (d.fmt) {
-            case RF_Q4_0: st = launch_fmt<RF_Q4_0, true>(p, grid, smem, d.pdl, stream, dev); break;
-            case RF_Q8_0: st = launch_fmt<RF_Q8_0, true>(p, grid, smem, d.pdl, stream, dev); break;
-            default: st = launch_fmt<RF_MXFP4, true>(p, grid, smem, d.pdl, stream, dev); break;
-            }
+        if (nj <= 4 && n_maps <= 4) {
+            KParamsSmall p;
+            if ((st = fill(p)) != RF_OK) return st;
+            st = launch_any(d.fmt, aligned, p, grid, smem, d.pdl, stream, dev);
         } else {
-            switch (d.fmt) {
-            case RF_Q4_0: st = launch_fmt<RF_Q4_0, false>(p, grid, smem, d.pdl, stream, dev); break;
-            case RF_Q8_0: st = launch_fmt<RF_Q8_0, false>(p, grid, smem, d.pdl, stream, dev); break;
-            default: st = launch_fmt<RF_MXFP4, false>(p, grid, smem, d.pdl, stream, dev); break;
-            }
+            static thread_local KParamsLarge p;   // about 18 KB: keep it off the stack
+            if ((st = fill(p)) != RF_OK) return st;
+            st = launch_any(d.fmt, aligned, p, grid, smem, d.pdl, stream, dev);
         }
         if (st != RF_OK) return st;
     }

@@ -19,6 +19,12 @@
 // stream-ordered dependencies: the host enqueues a whole walk without
 // blocking, and consecutive calls keep the copy engine busy across call
 // boundaries (no drain between projections).
+//
+// A walk can also be captured into a CUDA graph (the copy stream joins the
+// capture through a fork event), so a whole token's walks replay with one
+// host call.  Slot-free events only order walks of the same epoch: the eager
+// epoch, or one capture.  The first walk of a new epoch starts after
+// everything already enqueued on its stream instead.
 #include <algorithm>
 #include <cstring>
 #include <mutex>
@@ -38,6 +44,8 @@ struct rf_arena {
     cudaEvent_t copied[kMaxSlots] = {};
     cudaEvent_t freed[kMaxSlots] = {};
     bool freed_recorded[kMaxSlots] = {};
+    cudaEvent_t fork = nullptr;       // joins the copy stream to the caller's stream
+    unsigned long long epoch = 0;     // 0: eager; else the id of the capture
     int next_slot = 0;
     int last_slots = 0;
     size_t last_stride = 0;
@@ -114,6 +122,11 @@ rf_status rf_arena_create(size_t bytes, rf_arena **out)
         delete a;
         return RF_ERR_CUDA;
     }
+    if (cudaEventCreateWithFlags(&a->fork, cudaEventDisableTiming) != cudaSuccess) {
+        cudaGetLastError();
+        rf_arena_destroy(a);
+        return RF_ERR_CUDA;
+    }
     for (int i = 0; i < rf_arena::kMaxSlots; ++i) {
         if (cudaEventCreateWithFlags(&a->copied[i], cudaEventDisableTiming) != cudaSuccess ||
             cudaEventCreateWithFlags(&a->freed[i], cudaEventDisableTiming) != cudaSuccess) {
@@ -134,11 +147,13 @@ void rf_arena_destroy(rf_arena *a)
     cudaGetDevice(&prev);
     cudaSetDevice(a->device);
     // Copies may still be writing the arena and GEMVs may still read it:
-    // wait for both before freeing.
+    // wait for both before freeing.  (Launches of captured graphs are the
+    // caller's to finish.)
     if (a->copy_stream) cudaStreamSynchronize(a->copy_stream);
+    if (a->fork) cudaEventDestroy(a->fork);
     for (int i = 0; i < rf_arena::kMaxSlots; ++i) {
         if (a->freed[i]) {
-            if (a->freed_recorded[i]) cudaEventSynchronize(a->freed[i]);
+            if (a->freed_recorded[i] && a->epoch == 0) cudaEventSynchronize(a->freed[i]);
             cudaEventDestroy(a->freed[i]);
         }
         if (a->copied[i]) cudaEventDestroy(a->copied[i]);
@@ -183,6 +198,28 @@ rf_status rf_stream_linear(int fmt, const void *host_W, int64_t in_dim, int64_t 
     const int slots = depth + 1;
     const size_t stride = ((size_t)(eff * rb) + 255) & ~(size_t)255;
     if ((size_t)slots * stride > a->alloc_bytes) return RF_ERR_ARENA_TOO_SMALL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    unsigned long long cap_id = 0;
+    if (cudaStreamGetCaptureInfo(s, &cap, &cap_id) != cudaSuccess) {
+        cudaGetLastError();
+        return RF_ERR_CUDA;
+    }
+    if (cap == cudaStreamCaptureStatusInvalidated) return RF_ERR_CUDA;
+    const unsigned long long epoch = cap == cudaStreamCaptureStatusActive ? cap_id : 0;
+    if (epoch != a->epoch) {
+        // The slot-free events belong to another epoch: order this walk
+        // after all work already enqueued on `stream` (which includes every
+        // earlier reader of the slots when the graph is launched there).
+        if (cudaEventRecord(a->fork, s) != cudaSuccess ||
+            cudaStreamWaitEvent(a->copy_stream, a->fork, 0) != cudaSuccess)
+            return RF_ERR_CUDA;
+        for (int i = 0; i < rf_arena::kMaxSlots; ++i) a->freed_recorded[i] = false;
+        a->next_slot = 0;
+        a->last_slots = slots;
+        a->last_stride = stride;
+        a->epoch = epoch;
+    }
     // A new slot layout overlaps the old one: the copy stream first waits for
     // every old slot's last reader.
     if (a->last_slots != slots || a->last_stride != stride) {
@@ -194,7 +231,6 @@ rf_status rf_stream_linear(int fmt, const void *host_W, int64_t in_dim, int64_t 
         a->last_slots = slots;
         a->last_stride = stride;
     }
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     const uint8_t *hw = static_cast<const uint8_t *>(host_W);
     size_t peak = 0;
     rf_stream_plan(fmt, in_dim, n_rows, block_rows, depth, a->bytes, nullptr, nullptr, &peak);

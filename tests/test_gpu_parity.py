@@ -213,6 +213,42 @@ def test_stream_linear_bit_identical_to_resident(rf, fmt):
         arena.close()
 
 
+def test_stream_linear_captured_in_cuda_graph(rf):
+    """Walks captured into a CUDA graph (two calls with different slot layouts
+    in one capture) replay to the same bits as the eager walk, several times
+    in a row, and eager use of the arena works again afterwards."""
+    import torch
+    fmt, rows, in_dim = syn.Q8_0, 1000, 1024
+    W = syn.quant_matrix(fmt, rows, in_dim, seed=91)
+    xd = dev_tensor(syn.normal_f32(in_dim, 92))
+    host = torch.from_numpy(W).pin_memory()
+    arena = rf.Arena(400 * rf.row_bytes(fmt, in_dim))
+    try:
+        eager = arena.stream_linear(fmt, host, in_dim, 0, rows, 96, 3, xd).cpu().numpy()
+        ref = oracle.gemv(fmt, W, 0, rows, in_dim, syn.normal_f32(in_dim, 92))
+        assert_gemv_close(eager, ref, gemv_tol(fmt, W, 0, rows, in_dim, syn.normal_f32(in_dim, 92)))
+        s = torch.cuda.Stream()
+        yg = torch.full((rows,), float("nan"), device="cuda")
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            arena.stream_linear(fmt, host, in_dim, 0, 600, 96, 3, xd, yg[:600], stream=s)
+            arena.stream_linear(fmt, host, in_dim, 600, rows, 128, 2, xd, yg[600:], stream=s)
+        for rep in range(3):
+            yg.fill_(float("nan"))
+            torch.cuda.synchronize()
+            with torch.cuda.stream(s):
+                g.replay()
+            torch.cuda.synchronize()
+            assert np.array_equal(bits(yg.cpu().numpy()), bits(eager)), rep
+        again = arena.stream_linear(fmt, host, in_dim, 0, rows, 64, 4, xd).cpu().numpy()
+        assert np.array_equal(bits(again), bits(eager))
+        del g
+    finally:
+        torch.cuda.synchronize()
+        arena.close()
+
+
 def test_stream_linear_refusals(rf):
     import torch
     fmt, in_dim = syn.Q8_0, 256
