@@ -124,34 +124,35 @@ __device__ __forceinline__ float exp2i(int k)
 
 // Fixed-point digits of one 32-element activation block, computed by a quad
 // of consecutive lanes: lane `part` of the quad owns plane words 2*part and
-// 2*part+1 (8 elements).  All 32 lanes of the warp must call it (shuffles);
-// lanes with active == false only take part in the shuffles.
+// 2*part+1 (8 elements).  xrec_load fetches the lane's 8 elements (in plane
+// byte order); xrec_build turns them into digits.  All 32 lanes of the warp
+// must call xrec_build (shuffles); inactive lanes only take part in them.
 template <int FMT>
-__device__ __forceinline__ void make_xrec_quad(const float *xb, int part, bool active, XRec *out)
+__device__ __forceinline__ void xrec_load(const float *xb, int part, bool active, float (&v)[8])
 {
-    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    if (active) {
-        // element index of v[i] within the block
-        int ei[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) ei[i] = elem_of<FMT>(2 * part + (i >> 2), i & 3);
-        if ((reinterpret_cast<uintptr_t>(xb) & 15u) == 0) {
-            if constexpr (FMT == RF_MXFP4) {
-                const float4 a = reinterpret_cast<const float4 *>(xb)[part];       // 4k..4k+3
-                const float4 b = reinterpret_cast<const float4 *>(xb)[4 + part];   // 16+4k..
-                v[0] = a.x; v[1] = b.x; v[2] = a.y; v[3] = b.y;
-                v[4] = a.z; v[5] = b.z; v[6] = a.w; v[7] = b.w;
-            } else {
-                const float4 a = reinterpret_cast<const float4 *>(xb)[2 * part];
-                const float4 b = reinterpret_cast<const float4 *>(xb)[2 * part + 1];
-                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-                v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-            }
+    for (int i = 0; i < 8; ++i) v[i] = 0.f;
+    if (!active) return;
+    if ((reinterpret_cast<uintptr_t>(xb) & 15u) == 0) {
+        if constexpr (FMT == RF_MXFP4) {
+            const float4 a = reinterpret_cast<const float4 *>(xb)[part];       // 4k..4k+3
+            const float4 b = reinterpret_cast<const float4 *>(xb)[4 + part];   // 16+4k..
+            v[0] = a.x; v[1] = b.x; v[2] = a.y; v[3] = b.y;
+            v[4] = a.z; v[5] = b.z; v[6] = a.w; v[7] = b.w;
         } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = xb[ei[i]];
+            const float4 a = reinterpret_cast<const float4 *>(xb)[2 * part];
+            const float4 b = reinterpret_cast<const float4 *>(xb)[2 * part + 1];
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+            v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
         }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = xb[elem_of<FMT>(2 * part + (i >> 2), i & 3)];
     }
+}
+template <int FMT>
+__device__ __forceinline__ void xrec_build(const float (&v)[8], int part, bool active, XRec *out)
+{
     float m = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
@@ -176,11 +177,11 @@ __device__ __forceinline__ void make_xrec_quad(const float *xb, int part, bool a
     sum += __shfl_xor_sync(0xffffffffu, sum, 2);
     if (!active) return;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const uint32_t a = (uint32_t)X[4 * h], b = (uint32_t)X[4 * h + 1];
-        const uint32_t c = (uint32_t)X[4 * h + 2], d = (uint32_t)X[4 * h + 3];
-        out->p0[2 * part + h] = prmt(prmt(a, b, 0x0040u), prmt(c, d, 0x0040u), 0x5410u);
-        out->p1[2 * part + h] = prmt(prmt(a, b, 0x0051u), prmt(c, d, 0x0051u), 0x5410u);
+    for (int hh = 0; hh < 2; ++hh) {
+        const uint32_t a = (uint32_t)X[4 * hh], b = (uint32_t)X[4 * hh + 1];
+        const uint32_t c = (uint32_t)X[4 * hh + 2], d = (uint32_t)X[4 * hh + 3];
+        out->p0[2 * part + hh] = prmt(prmt(a, b, 0x0040u), prmt(c, d, 0x0040u), 0x5410u);
+        out->p1[2 * part + hh] = prmt(prmt(a, b, 0x0051u), prmt(c, d, 0x0051u), 0x5410u);
     }
     if (part == 0) {
         out->corr = FMT == RF_Q4_0 ? -8 * sum : 0;
@@ -507,15 +508,48 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, TMA>())
     pdl_wait();
 
     // Activation digits for every x of the launch, once per CTA, four lanes
-    // per 32-element block.
+    // per 32-element block.  The first kXPre passes' loads go out before the
+    // remaining weight copies, so they do not queue behind them.
     {
+        constexpr int kXPre = 8;
         const int n_rec = p.n_x * nb;
-        for (int base = 0; base < 4 * n_rec; base += kThreads) {
-            const int idx = base + (int)threadIdx.x;
-            const bool active = idx < 4 * n_rec;
-            const int rec = active ? idx >> 2 : 0;
+        const int passes = (4 * n_rec + kThreads - 1) / kThreads;
+        auto pass_src = [&](int ps, bool &active, int &rec) -> const float * {
+            const int idx = ps * kThreads + (int)threadIdx.x;
+            active = idx < 4 * n_rec;
+            rec = active ? idx >> 2 : 0;
             const int sl = rec / nb, b = rec - sl * nb;
-            make_xrec_quad<FMT>(p.x[sl] + 32 * (int64_t)b, idx & 3, active, &xrec[rec]);
+            return p.x[sl] + 32 * (int64_t)b;
+        };
+        float v[kXPre][8];
+        bool act[kXPre];
+        int rec[kXPre];
+#pragma unroll
+        for (int ps = 0; ps < kXPre; ++ps) {
+            act[ps] = false;
+            rec[ps] = 0;
+            if (ps < passes) {
+                const float *xb = pass_src(ps, act[ps], rec[ps]);
+                xrec_load<FMT>(xb, threadIdx.x & 3, act[ps], v[ps]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[ps][i] = 0.f;
+            }
+        }
+        for (int s = primed; s < ST && ic.valid; ++s) {
+            issue(ic);
+            cursor_advance(jobs, n_jobs, ic, n_chunks, g_hi);
+        }
+#pragma unroll
+        for (int ps = 0; ps < kXPre; ++ps)
+            if (ps < passes) xrec_build<FMT>(v[ps], threadIdx.x & 3, act[ps], &xrec[rec[ps]]);
+        for (int ps = kXPre; ps < passes; ++ps) {
+            bool a = false;
+            int rc = 0;
+            const float *xb = pass_src(ps, a, rc);
+            float w[8];
+            xrec_load<FMT>(xb, threadIdx.x & 3, a, w);
+            xrec_build<FMT>(w, threadIdx.x & 3, a, &xrec[rc]);
         }
     }
     __syncthreads();
