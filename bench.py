@@ -321,7 +321,8 @@ def dense_e2e(torch, layers, out, device, stream, steps):
 
 
 def run_streamed_gemv(torch, rf, device, depth: int, reps: int = 50):
-    """Q8_0 512x2048 streamed from pinned host memory in 128-row blocks."""
+    """Q8_0 512x2048 streamed from pinned host memory in 128-row blocks, eager
+    calls and the same calls captured into one CUDA graph."""
     c = syn.C1
     fmt, rows, in_dim = c["fmt"], c["out_dim"], c["in_dim"]
     W = syn.quant_matrix(fmt, rows, in_dim, c["seed"])
@@ -329,24 +330,42 @@ def run_streamed_gemv(torch, rf, device, depth: int, reps: int = 50):
     x = torch.from_numpy(syn.normal_f32(in_dim, c["seed"] + 1)).to(device)
     y = torch.empty(rows, device=device)
     arena = rf.Arena(c["arena_bytes"])
-    s = torch.cuda.current_stream()
+    s = torch.cuda.Stream(device)
+    s.wait_stream(torch.cuda.current_stream())
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     try:
-        for _ in range(5):
-            arena.stream_linear(fmt, host, in_dim, 0, rows, c["block_rows"], depth, x, y)
+        with torch.cuda.stream(s):
+            for _ in range(5):
+                arena.stream_linear(fmt, host, in_dim, 0, rows, c["block_rows"], depth, x, y, stream=s)
+            s.synchronize()
+            e0.record(s)
+            for _ in range(reps):
+                arena.stream_linear(fmt, host, in_dim, 0, rows, c["block_rows"], depth, x, y, stream=s)
+            e1.record(s)
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(s)
-        for _ in range(reps):
-            arena.stream_linear(fmt, host, in_dim, 0, rows, c["block_rows"], depth, x, y)
-        e1.record(s)
+        eager_ms = e0.elapsed_time(e1) / reps
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(reps):
+                arena.stream_linear(fmt, host, in_dim, 0, rows, c["block_rows"], depth, x, y, stream=s)
+        with torch.cuda.stream(s):
+            g.replay()
+            e0.record(s)
+            for _ in range(4):
+                g.replay()
+            e1.record(s)
         torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / reps
+        graph_ms = e0.elapsed_time(e1) / (4 * reps)
+        del g
     finally:
+        torch.cuda.synchronize()
         arena.close()
     nbytes = W.nbytes
     probe = h2d_probe(torch, device, c["block_rows"] * rf.row_bytes(fmt, in_dim), reps=200)
+    ms = min(eager_ms, graph_ms)
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {"workload": c["name"], "depth": depth, "ms_per_gemv": ms, "value": gbs, "unit": "GB/s",
+            "eager_ms_per_gemv": eager_ms, "graph_ms_per_gemv": graph_ms,
             "h2d_probe_block_gbs": probe, "frac_of_block_h2d": gbs / probe}
 
 
@@ -365,20 +384,34 @@ def run_moe(torch, rf, device, steps: int = 200):
         device)
     y = torch.empty(n_embd, device=device)
     ws = rf.moe_workspace(k, n_ff, n_embd, br, device)
-    s = torch.cuda.current_stream()
-    for t in range(10):
-        rf.moe_ffn(fmt, logits[t], k, G, U, D, n_ff, n_embd, br, x, y, ws)
+    s = torch.cuda.Stream(device)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for t in range(10):
+            rf.moe_ffn(fmt, logits[t], k, G, U, D, n_ff, n_embd, br, x, y, ws, stream=s)
     torch.cuda.synchronize()
+    # One graph holds `per_graph` tokens, each with its own logits, replayed
+    # until `steps` tokens have run (three launches per token).
+    per_graph = 20
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for t in range(per_graph):
+            rf.moe_ffn(fmt, logits[t], k, G, U, D, n_ff, n_embd, br, x, y, ws, stream=s)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(s)
-    for t in range(steps):
-        rf.moe_ffn(fmt, logits[t], k, G, U, D, n_ff, n_embd, br, x, y, ws)
-    e1.record(s)
+    reps = max(1, steps // per_graph)
+    with torch.cuda.stream(s):
+        g.replay()
+        e0.record(s)
+        for _ in range(reps):
+            g.replay()
+        e1.record(s)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / steps
+    ms = e0.elapsed_time(e1) / (reps * per_graph)
+    del g
     active = k * 3 * n_ff * rf.row_bytes(fmt, n_embd)
     return {"workload": c["name"], "ms_per_token": ms, "active_bytes": active,
-            "value": active / (ms * 1e-3) / 1e9, "unit": "GB/s", "launches_per_token": 3}
+            "value": active / (ms * 1e-3) / 1e9, "unit": "GB/s", "launches_per_token": 3,
+            "cuda_graph": True, "tokens_per_graph": per_graph}
 
 
 def run_streamed_ffn(torch, rf, device, n_layer: int):
@@ -462,6 +495,93 @@ def run_streamed_ffn(torch, rf, device, n_layer: int):
             "blocks_per_token": stats["blocks"] // (n_layer + min(2, n_layer))}
 
 
+def run_sweep(torch, rf, device, peak_hbm: float):
+    """The format x in_dim x out_dim x block_rows sweep, resident and
+    host-streamed.  Resident: the row windows of block_rows rows (whole =
+    one window) go to rf_gemv_batch (at most 64 windows per launch); copies of
+    the matrix are rotated until at least 4 x L2 is read between reuses; one
+    CUDA graph holds one pass over the copies.  Streamed: rf_stream_linear
+    from page-locked host memory, 256 MiB arena, depth 4, calls captured into
+    one CUDA graph.  Each cell has its own seeded matrix."""
+    l2 = 129 << 20
+    h2d = h2d_probe(torch, device, 256 << 20)
+    arena = rf.Arena(256 << 20)
+    s = torch.cuda.Stream(device)
+    s.wait_stream(torch.cuda.current_stream())
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cells = []
+
+    def timed_graph(fn, units):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            fn()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            fn()
+        with torch.cuda.stream(s):
+            g.replay()
+            e0.record(s)
+            reps = 0
+            while True:
+                g.replay()
+                reps += 1
+                if reps >= 3:
+                    break
+            e1.record(s)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / (reps * units)
+        del g
+        return ms
+
+    try:
+        for c in syn.sweep_cells():
+            fmt, in_dim, out, br = c["fmt"], c["in_dim"], c["out_dim"], c["block_rows"]
+            W = syn.quant_matrix(fmt, out, in_dim, c["seed"], threads=16)
+            nbytes = W.nbytes
+            x = torch.from_numpy(syn.normal_f32(in_dim, c["seed"] + 1)).to(device)
+            y = torch.empty(out, device=device)
+            w_rows = out if br == 0 else br
+            wins = [(r0, min(out, r0 + w_rows)) for r0 in range(0, out, w_rows)]
+            copies = max(1, min(64, -(-4 * l2 // nbytes)))
+            Wd = torch.from_numpy(W).to(device)
+            Ws = [Wd] + [Wd.clone() for _ in range(copies - 1)]
+
+            def resident():
+                for Wc in Ws:
+                    for b in range(0, len(wins), 64):
+                        rf.gemv_batch(fmt, in_dim, [(Wc, r0, r1, x, y[r0:r1]) for r0, r1 in
+                                                    wins[b:b + 64]], stream=s, flags=rf.CHAIN)
+            res_ms = timed_graph(resident, copies)
+            del Ws, Wd
+            host = torch.from_numpy(W).pin_memory()
+            n_calls = max(2, min(50, -(-(64 << 20) // nbytes)))
+
+            def streamed():
+                for _ in range(n_calls):
+                    arena.stream_linear(fmt, host, in_dim, 0, out, br, 4, x, y, stream=s)
+            str_ms = timed_graph(streamed, n_calls)
+            eff = arena.stats()["last_block_rows"]
+            del host
+            res_gbs = nbytes / (res_ms * 1e-3) / 1e9
+            str_gbs = nbytes / (str_ms * 1e-3) / 1e9
+            cells.append({"fmt": {syn.Q8_0: "Q8_0", syn.Q4_0: "Q4_0", syn.MXFP4: "MXFP4"}[fmt],
+                          "in": in_dim, "out": out, "block_rows": br or "whole",
+                          "bytes": nbytes, "resident_gbs": round(res_gbs, 1),
+                          "resident_frac_hbm": round(res_gbs / peak_hbm, 4),
+                          "streamed_gbs": round(str_gbs, 1),
+                          "streamed_frac_h2d": round(str_gbs / h2d, 4),
+                          "streamed_block_rows_eff": eff, "launches_per_resident_pass":
+                          -(-len(wins) // 64)})
+    finally:
+        torch.cuda.synchronize()
+        arena.close()
+    rf_ = sorted(cl["resident_frac_hbm"] for cl in cells)
+    sf_ = sorted(cl["streamed_frac_h2d"] for cl in cells)
+    return {"h2d_probe_256mib_gbs": h2d, "cells": cells,
+            "resident_frac_hbm_median": rf_[len(rf_) // 2],
+            "streamed_frac_h2d_median": sf_[len(sf_) // 2]}
+
+
 # ------------------------------------------------------------- reference
 
 def cpu_oracle_dense(fraction: float, min_seconds: float):
@@ -531,6 +651,8 @@ def main():
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--ffn-layers", type=int, default=syn.C4["n_layer"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--sweep", action="store_true",
+                    help="also run the format x shape x block_rows sweep (several minutes)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -583,6 +705,8 @@ def main():
             extra["moe_mxfp4"] = run_moe(torch, rf, device)
             if args.ffn_layers > 0:
                 extra["streamed_ffn_q8_0"] = run_streamed_ffn(torch, rf, device, args.ffn_layers)
+            if args.sweep:
+                extra["sweep"] = run_sweep(torch, rf, device, peak)
         except Exception as e:  # extras never hide the headline
             extra["error"] = repr(e)
         line["extra"] = extra

@@ -45,6 +45,7 @@
 #include <algorithm>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "rf_device.cuh"
 #include "rf_internal.h"
@@ -891,6 +892,28 @@ rf_status check_in_dim(int fmt, int64_t in_dim, int n_x)
     return in_dim > m ? RF_ERR_TOO_LARGE : RF_OK;
 }
 
+namespace {
+
+// B starts where A ends, with identical terms and epilogue.
+bool continues(const Job &A, const Job &B)
+{
+    if (A.n_terms != B.n_terms || A.combine != B.combine || A.act != B.act ||
+        A.weights != B.weights || A.expert_rows != B.expert_rows ||
+        A.expert_count != B.expert_count)
+        return false;
+    if (B.row0 != A.row0 + A.n_rows || B.y != A.y + A.n_rows) return false;
+    if ((int64_t)A.n_rows + B.n_rows > 0x7fffffffLL) return false;
+    for (int t = 0; t < A.n_terms; ++t)
+        if (A.term[t].W != B.term[t].W || A.term[t].xslot != B.term[t].xslot ||
+            A.term[t].expert_slot != B.term[t].expert_slot)
+            return false;
+    return true;
+}
+
+}  // namespace
+
+static rf_status launch_merged(const LaunchDesc &d, int nb, int64_t RB, cudaStream_t stream);
+
 rf_status launch_rowwin(const LaunchDesc &d, cudaStream_t stream)
 {
     if (!fmt_ok(d.fmt)) return RF_ERR_UNSUPPORTED_FMT;
@@ -922,6 +945,28 @@ rf_status launch_rowwin(const LaunchDesc &d, cudaStream_t stream)
                 return RF_ERR_INVALID_ARG;
         }
     }
+    // Windows that continue one another (same matrices, activations and
+    // epilogue; the next rows of the matrix written to the next outputs) are
+    // one window to the kernel.  Every output row's arithmetic is unchanged.
+    static thread_local std::vector<Job> merged;
+    merged.clear();
+    for (int i = 0; i < d.n_jobs; ++i) {
+        const Job &J = d.jobs[i];
+        if (J.n_rows == 0) continue;
+        if (!merged.empty() && continues(merged.back(), J)) {
+            merged.back().n_rows += J.n_rows;
+            continue;
+        }
+        merged.push_back(J);
+    }
+    LaunchDesc dm = d;
+    dm.jobs = merged.data();
+    dm.n_jobs = (int)merged.size();
+    return launch_merged(dm, nb, RB, stream);
+}
+
+static rf_status launch_merged(const LaunchDesc &d, int nb, int64_t RB, cudaStream_t stream)
+{
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();

@@ -129,3 +129,30 @@ def test_streamed_ffn_q8_0_24576x6144_sampled(rf):
         assert st["peak_bytes"] == 5 * 512 * rf.row_bytes(fmt, f)
     finally:
         arena.close()
+
+
+@pytest.mark.parametrize("fmt,in_dim,out_dim", sorted({(c["fmt"], c["in_dim"], c["out_dim"])
+                                                       for c in syn.sweep_cells()}))
+def test_sweep_shapes_resident_windows_and_streamed(rf, fmt, in_dim, out_dim):
+    """Every format x shape of the sweep at 512-row windows: the resident
+    batch of windows and the host-streamed walk both match the oracle on every
+    row and agree with each other bit for bit."""
+    import torch
+    cell = next(c for c in syn.sweep_cells() if (c["fmt"], c["in_dim"], c["out_dim"],
+                                                  c["block_rows"]) == (fmt, in_dim, out_dim, 512))
+    W = syn.quant_matrix(fmt, out_dim, in_dim, cell["seed"], threads=8)
+    x = syn.normal_f32(in_dim, cell["seed"] + 1)
+    Wd, xd = dev_tensor(W), dev_tensor(x)
+    y = torch.empty(out_dim, device="cuda")
+    rf.gemv_batch(fmt, in_dim, [(Wd, r0, min(out_dim, r0 + 512), xd, y[r0:min(out_dim, r0 + 512)])
+                                for r0 in range(0, out_dim, 512)])
+    resident = y.cpu().numpy()
+    ref = oracle.gemv(fmt, W, 0, out_dim, in_dim, x)
+    assert_gemv_close(resident, ref, gemv_tol(fmt, W, 0, out_dim, in_dim, x), "resident")
+    arena = rf.Arena(256 << 20)
+    try:
+        host = torch.from_numpy(W).pin_memory()
+        streamed = arena.stream_linear(fmt, host, in_dim, 0, out_dim, 512, 4, xd).cpu().numpy()
+    finally:
+        arena.close()
+    assert np.array_equal(bits(streamed), bits(resident))
