@@ -81,6 +81,21 @@ def ncu_traffic(workload: str):
     return None
 
 
+def reduce_time_max(torch, dist, ms: float, device) -> float:
+    """The slowest rank's timed region (max over ranks); unchanged on one rank."""
+    if not dist:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_step: int, steps: int, world: int, ms_total: float) -> float:
+    """Bytes every rank streamed (each rank runs its own replica) over the
+    slowest rank's time."""
+    return bytes_per_step * steps * world / (ms_total * 1e-3) / 1e9
+
+
 class ClockSampler:
     """nvidia-smi samples (200 ms) while the timed region runs."""
 
@@ -245,12 +260,8 @@ def run_dense(args, torch, rf, device, rank, world, dist):
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
-    ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    gbs = wbytes * args.steps * world / (ms * 1e-3) / 1e9
+    ms = reduce_time_max(torch, dist, e0.elapsed_time(e1), device)
+    gbs = whole_job_gbs(wbytes, args.steps, world, ms)
 
     # Per-phase launch durations (eager, events around each launch) for the
     # roofline breakdown.
