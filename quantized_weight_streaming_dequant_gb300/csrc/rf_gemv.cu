@@ -34,6 +34,11 @@
 //     Error: |x_j - X_j*2^-s| <= 2^-15 * max|x_block|, so by Cauchy-Schwarz
 //     the activation rounding moves y_r by at most sqrt(32)*2^-15*||W_r||*||x||
 //     (< 1.8e-4 * ||W_r||*||x||), inside the parity tolerance 1e-3*||W_r||*||x||.
+//   * Rows whose byte length is not a multiple of 16 but whose 32-row group
+//     fits a shared-memory stage are staged whole: one 1-D bulk copy per
+//     (group, term) holds the group's rows back to back (the rows of a window
+//     are contiguous in memory), all 8 warps read their K parts from it, and
+//     the last warp to finish with a stage issues the copy that refills it.
 //   * Persistent CTAs each take a contiguous range of 32-row groups across all
 //     jobs of the launch.
 //   * Programmatic dependent launch: weight copies for the first chunks are
@@ -86,7 +91,8 @@ struct FmtT<RF_MXFP4> {
     static constexpr int BS = 17, HDR = 1, QW = 4, G = 16;
 };
 
-constexpr int kMaxMaps = 16;   // distinct weight tensors per launch (tensor-map path)
+constexpr int kMaxMaps = 16;
+constexpr int kCntInts = 16;   // group counters (4) + flat-mode stage counters (up to 8), padded   // distinct weight tensors per launch (tensor-map path)
 
 // Kernel parameters.  Two sizes: launches with at most 4 windows and 4 weight
 // tensors (nearly all of them) pass about 1.6 KB instead of 18 KB per launch.
@@ -389,20 +395,25 @@ __device__ __forceinline__ const uint8_t *term_matrix(const int32_t *expert_idx,
     return W;
 }
 
-// TMA = true: rows are 16-byte aligned and each chunk of a warp (32 rows x kc
-// blocks) is one 2-D tensor copy issued by lane 0.  TMA = false: any
+// Modes: kModeTensor -- rows are 16-byte aligned and each chunk of a warp (32
+// rows x kc blocks) is one 2-D tensor copy issued by lane 0.  kModeFlat --
+// one 1-D bulk copy per (group, term) into a CTA-wide ring.  kModePerLane -- any
 // alignment; each lane copies its own row's chunk with a 1-D bulk copy.
 // Minimum CTAs per SM the register budget is sized for: 272-byte aligned
 // chunks (Q8_0, MXFP4) need more registers and their shared memory allows
 // one CTA per SM anyway.
-template <int FMT, bool TMA>
-constexpr int min_ctas() { return (TMA && FMT != RF_Q4_0) ? 1 : 2; }
+constexpr int kModePerLane = 0, kModeTensor = 1, kModeFlat = 2;
 
-template <int FMT, bool TMA, class KP>
-__global__ void __launch_bounds__(kThreads, min_ctas<FMT, TMA>())
+template <int FMT, int MODE>
+constexpr int min_ctas() { return (MODE == kModeTensor && FMT != RF_Q4_0) ? 1 : 2; }
+
+template <int FMT, int MODE, class KP>
+__global__ void __launch_bounds__(kThreads, min_ctas<FMT, MODE>())
     rowwin_kernel(const __grid_constant__ KP p)
 {
     using F = FmtT<FMT>;
+    constexpr bool TMA = MODE == kModeTensor;
+    constexpr bool FLAT = MODE == kModeFlat;
     extern __shared__ __align__(128) uint8_t smem[];
 
     const int nb = p.nb;
@@ -416,13 +427,14 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, TMA>())
     XRec *xrec = reinterpret_cast<XRec *>(smem);
     size_t off = ((size_t)p.n_x * nb * sizeof(XRec) + 127) & ~(size_t)127;
     uint8_t *slots = smem + off;
-    off += (size_t)kNW * ST * kRows * SLOT;
+    off += FLAT ? (size_t)ST * SLOT : (size_t)kNW * ST * kRows * SLOT;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + off);
-    off += (size_t)kNW * ST * sizeof(uint64_t);
+    off += (size_t)(FLAT ? ST : kNW * ST) * sizeof(uint64_t);
     float *red = reinterpret_cast<float *>(smem + off);   // [2][NT][kNW][32]
     off += (size_t)2 * NT * kNW * 32 * sizeof(float);
     int *cnt = reinterpret_cast<int *>(smem + off);       // arrivals per parity, then groups done
-    off += 4 * sizeof(int);
+    int *emp = cnt + 4;                                   // flat mode: readers done per stage
+    off += kCntInts * sizeof(int);
     Job *jobs = reinterpret_cast<Job *>(smem + off);      // this launch's jobs, read once
     const int n_jobs = p.n_jobs;
 
@@ -435,9 +447,16 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, TMA>())
     const int kb_lo = min(nb, F::G * (warp * nG / kNW));
     const int kb_hi = min(nb, F::G * ((warp + 1) * nG / kNW));
     const int n_chunks = (kb_hi - kb_lo + KC - 1) / KC;
+    // Items a cursor walks per (group, term): this warp's chunks, or one
+    // CTA-wide stage in flat mode.
+    const int cur_chunks = FLAT ? 1 : n_chunks;
 
-    if (lane < ST) mbar_init(&bars[warp * ST + lane], TMA ? 1 : 32);
-    if (threadIdx.x < 3) cnt[threadIdx.x] = 0;
+    if constexpr (FLAT) {
+        if ((int)threadIdx.x < ST) mbar_init(&bars[threadIdx.x], 1);
+    } else {
+        if (lane < ST) mbar_init(&bars[warp * ST + lane], TMA ? 1 : 32);
+    }
+    if (threadIdx.x < kCntInts) cnt[threadIdx.x] = 0;
     if constexpr (TMA) {
         if ((int)threadIdx.x < p.n_maps)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.maps[threadIdx.x]))
@@ -455,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, TMA>())
     uint8_t *my_slots = slots + (size_t)warp * ST * kRows * SLOT;
     uint64_t *my_bars = bars + warp * ST;
 
-    Cursor ic{g_lo, 0, 0, 0, g_lo < g_hi && n_chunks > 0};
+    Cursor ic{g_lo, 0, 0, 0, g_lo < g_hi && cur_chunks > 0};
     if (ic.valid) cursor_fix_job(jobs, n_jobs, ic);
     int is = 0;   // stage of the next copy
 
@@ -493,6 +512,31 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, TMA>())
         }
     };
 
+    // Flat mode: the rows of (group, term) of cursor `cu`, back to back, into
+    // CTA stage `st` (one thread).  The copy starts at the 16-byte boundary at
+    // or before the group and ends at the one at or after it.
+    auto issue_flat = [&](const Cursor &cu, int st) {
+        const Job &J = jobs[cu.j];
+        const int64_t rel = (int64_t)(cu.g - J.group_begin) * kRows;
+        const int64_t nr = min((int64_t)kRows, (int64_t)J.n_rows - rel);
+        const uintptr_t src =
+            reinterpret_cast<uintptr_t>(term_matrix(p.expert_idx, J, cu.t, RB) + (J.row0 + rel) * RB);
+        const uintptr_t a = src & ~(uintptr_t)15;
+        const uintptr_t e = (src + (uintptr_t)(nr * RB) + 15) & ~(uintptr_t)15;
+        mbar_arrive_expect_tx(&bars[st], (uint32_t)(e - a));
+        bulk_g2s(slots + (size_t)st * SLOT, reinterpret_cast<const void *>(a), (uint32_t)(e - a),
+                 &bars[st]);
+    };
+    // Next copy at priming time: this warp's chunk, or (one thread) a stage.
+    auto prime = [&](int st) {
+        if constexpr (FLAT) {
+            if (threadIdx.x == 0) issue_flat(ic, st);
+        } else {
+            issue(ic);
+        }
+        cursor_advance(jobs, n_jobs, ic, cur_chunks, g_hi);
+    };
+
     // Weights never depend on the previous kernel: when this launch may
     // overlap it (programmatic dependent launch), fill every stage before
     // waiting (unless the rows come from a routing result the previous
@@ -500,10 +544,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, TMA>())
     // runs then holds its first chunks by the time the activations exist.
     int primed = 0;
     if (p.prefetch_early) {
-        for (; primed < ST && ic.valid; ++primed) {
-            issue(ic);
-            cursor_advance(jobs, n_jobs, ic, n_chunks, g_hi);
-        }
+        for (; primed < ST && ic.valid; ++primed) prime(primed);
     }
     pdl_launch_dependents();
     pdl_wait();
@@ -537,10 +578,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, TMA>())
                 for (int i = 0; i < 8; ++i) v[ps][i] = 0.f;
             }
         }
-        for (int s = primed; s < ST && ic.valid; ++s) {
-            issue(ic);
-            cursor_advance(jobs, n_jobs, ic, n_chunks, g_hi);
-        }
+        for (int s = primed; s < ST && ic.valid; ++s) prime(s);
 #pragma unroll
         for (int ps = 0; ps < kXPre; ++ps)
             if (ps < passes) xrec_build<FMT>(v[ps], threadIdx.x & 3, act[ps], &xrec[rec[ps]]);
@@ -585,11 +623,37 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, TMA>())
         for (int t = 0; t < n_terms; ++t) {
             float acc = 0.f;
             uintptr_t row_src = 0;
-            if (!aligned && row_ok)
+            if (!FLAT && !aligned && row_ok)
                 row_src = reinterpret_cast<uintptr_t>(term_matrix(p.expert_idx, J, t, RB) +
                                                       (J.row0 + rowrel) * RB);
             const XRec *xr_row = xrec + (size_t)J.term[t].xslot * nb;
-            for (int c = 0; c < n_chunks; ++c) {
+            if constexpr (FLAT) {
+                // Every warp waits for the stage (so none runs ahead of the
+                // ring), reads its K part of its lane's row, then counts
+                // itself out; the last one refills the stage.
+                const int st = cs;
+                mbar_wait_bounded(&bars[st], cph, &g_device_status);
+                if (row_ok && kb_hi > kb_lo) {
+                    const uintptr_t src = reinterpret_cast<uintptr_t>(
+                        term_matrix(p.expert_idx, J, t, RB) + (J.row0 + rowrel - lane) * RB);
+                    const uintptr_t rp = reinterpret_cast<uintptr_t>(slots + (size_t)st * SLOT) +
+                                         (src & 15) + (uintptr_t)((int64_t)lane * RB) +
+                                         (uintptr_t)kb_lo * F::BS;
+                    acc = chunk_generic<FMT>(reinterpret_cast<const uint8_t *>(rp & ~(uintptr_t)3),
+                                             (int)(rp & 3), kb_hi - kb_lo, xr_row + kb_lo, acc);
+                }
+                if (++cs == ST) {
+                    cs = 0;
+                    cph ^= 1u;
+                }
+                __syncwarp();
+                if (lane == 0 && atomicAdd(&emp[st], 1) == kNW - 1) {
+                    emp[st] = 0;
+                    if (ic.valid) issue_flat(ic, st);
+                }
+                if (ic.valid) cursor_advance(jobs, n_jobs, ic, 1, g_hi);
+            }
+            for (int c = 0; c < (FLAT ? 0 : n_chunks); ++c) {
                 mbar_wait_bounded(&my_bars[cs], cph, &g_device_status);
                 const uint8_t *slot = my_slots + ((size_t)cs * kRows + lane) * SLOT;
                 if (++cs == ST) {
@@ -712,11 +776,17 @@ ChunkGeom chunk_geom(int fmt, bool aligned)
     return {kc, n};
 }
 
-size_t smem_bytes(int n_x, int nb, int stages, int slot, int max_terms, int n_jobs)
+// Flat mode: a stage holds one 32-row group back to back, plus the 16-byte
+// rounding at both ends and a word of overrun for the last row's decode.
+int flat_slot(int64_t row_bytes) { return (int)((kRows * row_bytes + 32 + 127) / 128 * 128); }
+
+size_t smem_bytes(int n_x, int nb, int stages, int slot, int max_terms, int n_jobs,
+                  bool flat = false)
 {
     return (((size_t)n_x * nb * sizeof(XRec) + 127) & ~(size_t)127) +
-           (size_t)kNW * stages * kRows * slot + (size_t)kNW * stages * sizeof(uint64_t) +
-           (size_t)2 * max_terms * kNW * 32 * sizeof(float) + 4 * sizeof(int) +
+           (flat ? (size_t)stages * slot : (size_t)kNW * stages * kRows * slot) +
+           (size_t)(flat ? stages : kNW * stages) * sizeof(uint64_t) +
+           (size_t)2 * max_terms * kNW * 32 * sizeof(float) + kCntInts * sizeof(int) +
            (size_t)n_jobs * sizeof(Job);
 }
 
@@ -752,13 +822,13 @@ bool encode_rows_map(CUtensorMap *m, const void *base, int64_t rows, int64_t rb,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int FMT, bool TMA, class KP>
+template <int FMT, int MODE, class KP>
 rf_status launch_fmt(const KP &p, int grid, size_t smem, bool pdl, cudaStream_t stream, int dev)
 {
     static std::once_flag attr_once[64];
     const int maxs = dev_info(dev).max_smem_block;
     std::call_once(attr_once[dev & 63], [maxs] {
-        cudaFuncSetAttribute(rowwin_kernel<FMT, TMA, KP>,
+        cudaFuncSetAttribute(rowwin_kernel<FMT, MODE, KP>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, maxs);
     });
     cudaLaunchConfig_t cfg = {};
@@ -773,26 +843,28 @@ rf_status launch_fmt(const KP &p, int grid, size_t smem, bool pdl, cudaStream_t 
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    if (cudaLaunchKernelEx(&cfg, rowwin_kernel<FMT, TMA, KP>, p) != cudaSuccess) return RF_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, rowwin_kernel<FMT, MODE, KP>, p) != cudaSuccess) return RF_ERR_CUDA;
     return RF_OK;
 }
 
+template <int MODE, class KP>
+rf_status launch_mode(int fmt, const KP &p, int grid, size_t smem, bool pdl, cudaStream_t stream,
+                      int dev)
+{
+    switch (fmt) {
+    case RF_Q4_0: return launch_fmt<RF_Q4_0, MODE>(p, grid, smem, pdl, stream, dev);
+    case RF_Q8_0: return launch_fmt<RF_Q8_0, MODE>(p, grid, smem, pdl, stream, dev);
+    default: return launch_fmt<RF_MXFP4, MODE>(p, grid, smem, pdl, stream, dev);
+    }
+}
+
 template <class KP>
-rf_status launch_any(int fmt, bool tma, const KP &p, int grid, size_t smem, bool pdl,
+rf_status launch_any(int fmt, int mode, const KP &p, int grid, size_t smem, bool pdl,
                      cudaStream_t stream, int dev)
 {
-    if (tma) {
-        switch (fmt) {
-        case RF_Q4_0: return launch_fmt<RF_Q4_0, true>(p, grid, smem, pdl, stream, dev);
-        case RF_Q8_0: return launch_fmt<RF_Q8_0, true>(p, grid, smem, pdl, stream, dev);
-        default: return launch_fmt<RF_MXFP4, true>(p, grid, smem, pdl, stream, dev);
-        }
-    }
-    switch (fmt) {
-    case RF_Q4_0: return launch_fmt<RF_Q4_0, false>(p, grid, smem, pdl, stream, dev);
-    case RF_Q8_0: return launch_fmt<RF_Q8_0, false>(p, grid, smem, pdl, stream, dev);
-    default: return launch_fmt<RF_MXFP4, false>(p, grid, smem, pdl, stream, dev);
-    }
+    if (mode == kModeTensor) return launch_mode<kModeTensor>(fmt, p, grid, smem, pdl, stream, dev);
+    if (mode == kModeFlat) return launch_mode<kModeFlat>(fmt, p, grid, smem, pdl, stream, dev);
+    return launch_mode<kModePerLane>(fmt, p, grid, smem, pdl, stream, dev);
 }
 
 // Tensor maps of recent weight tensors (host-side encoding is not free and
@@ -978,26 +1050,48 @@ static rf_status launch_merged(const LaunchDesc &d, int nb, int64_t RB, cudaStre
     // Rows are 16-byte aligned when the row bytes are (weights are 16-byte
     // aligned): then chunks are copied exactly.
     const bool aligned = RB % 16 == 0;
-    const ChunkGeom geo = chunk_geom(d.fmt, aligned);
+    ChunkGeom geo = chunk_geom(d.fmt, aligned);
     int max_terms = 1;
     for (int i = 0; i < d.n_jobs; ++i) max_terms = std::max(max_terms, (int)d.jobs[i].n_terms);
-    // Prefer two CTAs per SM (16 warps) with at least 2 stages; else one CTA
-    // with up to 4 stages.
+    const int nj_max = std::min(d.n_jobs, kMaxJobs);
     const size_t per2 = (size_t)di.max_smem_sm / 2 - (size_t)di.reserved_per_block;
+    int mode = aligned ? kModeTensor : kModePerLane;
     int ctas_per_sm = 0, stages = 0;
+    // Misaligned rows: stage whole 32-row groups when two of them fit (two
+    // CTAs per SM if possible).
+    if (!aligned) {
+        const int fs = flat_slot(RB);
+        for (int st = 3; st >= 2 && !ctas_per_sm; --st)
+            if (smem_bytes(d.n_x, nb, st, fs, max_terms, nj_max, true) <= per2) {
+                ctas_per_sm = 2;
+                stages = st;
+            }
+        for (int st = 4; st >= 2 && !ctas_per_sm; --st)
+            if (smem_bytes(d.n_x, nb, st, fs, max_terms, nj_max, true) <=
+                (size_t)di.max_smem_block) {
+                ctas_per_sm = 1;
+                stages = st;
+            }
+        if (ctas_per_sm) {
+            mode = kModeFlat;
+            geo = {1, fs};
+        }
+    }
+    // Otherwise per-warp rings: prefer two CTAs per SM (16 warps) with at
+    // least 2 stages; else one CTA with up to 4 stages.
     const bool two_ok = !aligned || d.fmt == RF_Q4_0;   // register budget (min_ctas)
     for (int st = 4; st >= 2 && !ctas_per_sm && two_ok; --st)
-        if (smem_bytes(d.n_x, nb, st, geo.slot, max_terms, std::min(d.n_jobs, kMaxJobs)) <= per2) {
+        if (smem_bytes(d.n_x, nb, st, geo.slot, max_terms, nj_max) <= per2) {
             ctas_per_sm = 2;
             stages = st;
         }
     for (int st = 4; st >= 1 && !ctas_per_sm; --st)
-        if (smem_bytes(d.n_x, nb, st, geo.slot, max_terms, std::min(d.n_jobs, kMaxJobs)) <= (size_t)di.max_smem_block) {
+        if (smem_bytes(d.n_x, nb, st, geo.slot, max_terms, nj_max) <= (size_t)di.max_smem_block) {
             ctas_per_sm = 1;
             stages = st;
         }
     if (!ctas_per_sm) return RF_ERR_TOO_LARGE;
-    const size_t smem = smem_bytes(d.n_x, nb, stages, geo.slot, max_terms, std::min(d.n_jobs, kMaxJobs));
+    const size_t smem = smem_bytes(d.n_x, nb, stages, geo.slot, max_terms, nj_max, mode == kModeFlat);
 
     // Launch in batches of kMaxJobs windows.
     for (int base = 0; base < d.n_jobs; base += kMaxJobs) {
@@ -1066,11 +1160,11 @@ static rf_status launch_merged(const LaunchDesc &d, int nb, int64_t RB, cudaStre
         if (nj <= 4 && n_maps <= 4) {
             KParamsSmall p;
             if ((st = fill(p)) != RF_OK) return st;
-            st = launch_any(d.fmt, aligned, p, grid, smem, d.pdl, stream, dev);
+            st = launch_any(d.fmt, mode, p, grid, smem, d.pdl, stream, dev);
         } else {
             static thread_local KParamsLarge p;   // about 18 KB: keep it off the stack
             if ((st = fill(p)) != RF_OK) return st;
-            st = launch_any(d.fmt, aligned, p, grid, smem, d.pdl, stream, dev);
+            st = launch_any(d.fmt, mode, p, grid, smem, d.pdl, stream, dev);
         }
         if (st != RF_OK) return st;
     }

@@ -67,6 +67,7 @@ SHAPES = [  # (rows, in_dim, window) -- several 32-row groups, ragged tails,
     (70, 32, (1, 70)),           # one block per row
     (300, 96, (5, 299)),         # nb = 3 < warps
     (64, 24576, (0, 64)),        # the host-streamed FFN's down width
+    (100, 3104, (2, 99)),        # whole-group staging with one CTA per SM
 ]
 
 
