@@ -91,8 +91,10 @@ struct FmtT<RF_MXFP4> {
     static constexpr int BS = 17, HDR = 1, QW = 4, G = 16;
 };
 
-constexpr int kMaxMaps = 16;
-constexpr int kCntInts = 16;   // group counters (4) + flat-mode stage counters (up to 8), padded   // distinct weight tensors per launch (tensor-map path)
+constexpr int kMaxMaps = 16;   // distinct weight tensors per launch (tensor-map path)
+// Shared ints: group counters (4), flat-mode stage counters (up to 8, at 4),
+// the launch's own routing: expert ids (8, at 16) and weights (8 floats, at 24).
+constexpr int kCntInts = 32;
 
 // Kernel parameters.  Two sizes: launches with at most 4 windows and 4 weight
 // tensors (nearly all of them) pass about 1.6 KB instead of 18 KB per launch.
@@ -104,6 +106,10 @@ struct KParamsT {
     const int32_t *expert_idx;
     int32_t n_jobs, n_x, nb, total_groups;
     int32_t stages, kc, slot, prefetch_early, max_terms, n_maps;
+    const float *route_logits;   // non-null: route inside the launch (see LaunchDesc)
+    int32_t *route_idx_out;
+    float *route_w_out;
+    int32_t route_n, route_k;
 };
 using KParamsSmall = KParamsT<4, 4>;
 using KParamsLarge = KParamsT<kMaxJobs, kMaxMaps>;
@@ -395,6 +401,69 @@ __device__ __forceinline__ const uint8_t *term_matrix(const int32_t *expert_idx,
     return W;
 }
 
+// Top-k of n logits by one warp (ties to the lower index; the same order as
+// the standalone router) and the softmax over the k selected, into idx/w.
+__device__ __forceinline__ void route_warp(const float *__restrict__ logits, int n, int k,
+                                           int32_t *idx, float *w)
+{
+    const int lane = threadIdx.x & 31;
+    // Experts lane + 32*m, m < 32 (n <= 1024), all loaded at once; a missing
+    // expert counts as already taken.
+    float lv[32];
+    uint32_t taken = 0;   // bit m: expert lane + 32*m already selected
+#pragma unroll
+    for (int m = 0; m < 32; ++m) {
+        const bool has = lane + 32 * m < n;
+        lv[m] = has ? logits[lane + 32 * m] : 0.f;
+        if (!has) taken |= 1u << m;
+    }
+    float sel[kMaxTerms];
+#pragma unroll
+    for (int r = 0; r < kMaxTerms; ++r) {
+        if (r >= k) break;
+        float v = -INFINITY;
+        int i = 0x7fffffff;
+#pragma unroll
+        for (int m = 0; m < 32; ++m) {
+            if ((taken >> m) & 1u) continue;
+            const float v2 = lv[m];
+            const int i2 = lane + 32 * m;
+            if (v2 > v || (v2 == v && i2 < i)) {
+                v = v2;
+                i = i2;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
+            const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
+            if (v2 > v || (v2 == v && i2 < i)) {
+                v = v2;
+                i = i2;
+            }
+        }
+        if ((i & 31) == lane) taken |= 1u << (i >> 5);
+        sel[r] = v;
+        if (lane == 0) idx[r] = i;
+    }
+    if (lane == 0) {
+        const float m = sel[0];
+        float e[kMaxTerms];
+        float sum = 0.f;
+#pragma unroll
+        for (int r = 0; r < kMaxTerms; ++r) {
+            if (r >= k) break;
+            e[r] = expf(sel[r] - m);
+            sum += e[r];
+        }
+#pragma unroll
+        for (int r = 0; r < kMaxTerms; ++r) {
+            if (r >= k) break;
+            w[r] = e[r] / sum;
+        }
+    }
+}
+
 // Modes: kModeTensor -- rows are 16-byte aligned and each chunk of a warp (32
 // rows x kc blocks) is one 2-D tensor copy issued by lane 0.  kModeFlat --
 // one 1-D bulk copy per (group, term) into a CTA-wide ring.  kModePerLane -- any
@@ -443,9 +512,13 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, MODE>())
     const int g_hi = (int)((int64_t)(blockIdx.x + 1) * G_total / gridDim.x);
 
     // This warp's K part, in blocks.
-    const int nG = (nb + F::G - 1) / F::G;
-    const int kb_lo = min(nb, F::G * (warp * nG / kNW));
-    const int kb_hi = min(nb, F::G * ((warp + 1) * nG / kNW));
+    // Split granularity: the format's 16-byte group when rows are 16-byte
+    // aligned (tensor copies need it), single blocks otherwise.  Either way it
+    // depends only on (format, in_dim).
+    const int GS = RB % 16 == 0 ? F::G : 1;
+    const int nG = (nb + GS - 1) / GS;
+    const int kb_lo = min(nb, GS * (warp * nG / kNW));
+    const int kb_hi = min(nb, GS * ((warp + 1) * nG / kNW));
     const int n_chunks = (kb_hi - kb_lo + KC - 1) / KC;
     // Items a cursor walks per (group, term): this warp's chunks, or one
     // CTA-wide stage in flat mode.
@@ -469,7 +542,15 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, MODE>())
         for (int i = threadIdx.x; i < words; i += kThreads) dst[i] = src[i];
     }
     fence_barrier_init();
+    int32_t *s_eidx = cnt + 16;
+    float *s_ew = reinterpret_cast<float *>(cnt + 24);
+    if (p.route_logits && warp == 0) route_warp(p.route_logits, p.route_n, p.route_k, s_eidx, s_ew);
     __syncthreads();
+    const int32_t *eidx = p.route_logits ? s_eidx : p.expert_idx;
+    if (p.route_logits && blockIdx.x == 0 && (int)threadIdx.x < p.route_k && p.route_idx_out) {
+        p.route_idx_out[threadIdx.x] = s_eidx[threadIdx.x];
+        p.route_w_out[threadIdx.x] = s_ew[threadIdx.x];
+    }
 
     uint8_t *my_slots = slots + (size_t)warp * ST * kRows * SLOT;
     uint64_t *my_bars = bars + warp * ST;
@@ -487,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, MODE>())
             if (lane == 0) {
                 const Term &T = J.term[cu.t];
                 int64_t y = J.row0 + (int64_t)(cu.g - J.group_begin) * kRows;
-                if (T.expert_slot >= 0) y += (int64_t)p.expert_idx[T.expert_slot] * J.expert_rows;
+                if (T.expert_slot >= 0) y += (int64_t)eidx[T.expert_slot] * J.expert_rows;
                 const int x = (kb_lo + cu.c * KC) * F::BS / 2;   // uint16 units
                 mbar_arrive_expect_tx(bar, (uint32_t)(kRows * SLOT));
                 tma_2d_g2s(dst, &p.maps[T.tmap], x, (int)y, bar);
@@ -497,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, MODE>())
             // boundaries, with 16-byte cp.async (issued by all lanes at once).
             const int64_t rowrel = (int64_t)(cu.g - J.group_begin) * kRows + lane;
             if (rowrel < J.n_rows) {
-                const uint8_t *W = term_matrix(p.expert_idx, J, cu.t, RB);
+                const uint8_t *W = term_matrix(eidx, J, cu.t, RB);
                 const int kb = kb_lo + cu.c * KC;
                 const int kn = min(KC, kb_hi - kb);
                 const uintptr_t s = reinterpret_cast<uintptr_t>(W + (J.row0 + rowrel) * RB +
@@ -520,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, MODE>())
         const int64_t rel = (int64_t)(cu.g - J.group_begin) * kRows;
         const int64_t nr = min((int64_t)kRows, (int64_t)J.n_rows - rel);
         const uintptr_t src =
-            reinterpret_cast<uintptr_t>(term_matrix(p.expert_idx, J, cu.t, RB) + (J.row0 + rel) * RB);
+            reinterpret_cast<uintptr_t>(term_matrix(eidx, J, cu.t, RB) + (J.row0 + rel) * RB);
         const uintptr_t a = src & ~(uintptr_t)15;
         const uintptr_t e = (src + (uintptr_t)(nr * RB) + 15) & ~(uintptr_t)15;
         mbar_arrive_expect_tx(&bars[st], (uint32_t)(e - a));
@@ -624,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, MODE>())
             float acc = 0.f;
             uintptr_t row_src = 0;
             if (!FLAT && !aligned && row_ok)
-                row_src = reinterpret_cast<uintptr_t>(term_matrix(p.expert_idx, J, t, RB) +
+                row_src = reinterpret_cast<uintptr_t>(term_matrix(eidx, J, t, RB) +
                                                       (J.row0 + rowrel) * RB);
             const XRec *xr_row = xrec + (size_t)J.term[t].xslot * nb;
             if constexpr (FLAT) {
@@ -635,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, MODE>())
                 mbar_wait_bounded(&bars[st], cph, &g_device_status);
                 if (row_ok && kb_hi > kb_lo) {
                     const uintptr_t src = reinterpret_cast<uintptr_t>(
-                        term_matrix(p.expert_idx, J, t, RB) + (J.row0 + rowrel - lane) * RB);
+                        term_matrix(eidx, J, t, RB) + (J.row0 + rowrel - lane) * RB);
                     const uintptr_t rp = reinterpret_cast<uintptr_t>(slots + (size_t)st * SLOT) +
                                          (src & 15) + (uintptr_t)((int64_t)lane * RB) +
                                          (uintptr_t)kb_lo * F::BS;
@@ -708,6 +789,8 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, MODE>())
                         gate = dot;
                     else
                         yacc = gate / (1.f + expf(-gate)) * dot;
+                } else if (J.combine == kCombineRouted) {
+                    yacc = fmaf(s_ew[J.term[t].expert_slot], dot, yacc);
                 } else if (J.weights) {
                     yacc = fmaf(J.weights[t], dot, yacc);
                 } else {
@@ -827,10 +910,14 @@ rf_status launch_fmt(const KP &p, int grid, size_t smem, bool pdl, cudaStream_t 
 {
     static std::once_flag attr_once[64];
     const int maxs = dev_info(dev).max_smem_block;
-    std::call_once(attr_once[dev & 63], [maxs] {
-        cudaFuncSetAttribute(rowwin_kernel<FMT, MODE, KP>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, maxs);
+    static bool attr_ok[64];
+    std::call_once(attr_once[dev & 63], [maxs, dev] {
+        attr_ok[dev & 63] = cudaFuncSetAttribute(rowwin_kernel<FMT, MODE, KP>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 maxs) == cudaSuccess;
+        cudaGetLastError();
     });
+    if (!attr_ok[dev & 63]) return RF_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
@@ -994,7 +1081,10 @@ rf_status launch_rowwin(const LaunchDesc &d, cudaStream_t stream)
     if (d.n_jobs > 0 && !d.jobs) return RF_ERR_INVALID_ARG;
     for (int s = 0; s < d.n_x; ++s)
         if (!d.x[s]) return RF_ERR_INVALID_ARG;
-    if (d.any_expert && !d.expert_idx) return RF_ERR_INVALID_ARG;
+    if (d.any_expert && !d.expert_idx && !d.route_logits) return RF_ERR_INVALID_ARG;
+    if (d.route_logits && (d.route_n < 1 || d.route_n > 1024 || d.route_k < 1 ||
+                           d.route_k > kMaxTerms || d.route_k > d.route_n))
+        return RF_ERR_INVALID_ARG;
     const int64_t nb64 = d.in_dim / 32;
     if (nb64 > (1 << 24)) return RF_ERR_TOO_LARGE;
     const int nb = (int)nb64;
@@ -1013,7 +1103,9 @@ rf_status launch_rowwin(const LaunchDesc &d, cudaStream_t stream)
             if ((reinterpret_cast<uintptr_t>(T.W) & 15u) != 0) return RF_ERR_MISALIGNED;
             if (T.xslot < 0 || T.xslot >= d.n_x) return RF_ERR_INVALID_ARG;
             if (T.expert_slot >= kMaxTerms) return RF_ERR_INVALID_ARG;
-            if (T.expert_slot >= 0 && (!d.expert_idx || J.expert_rows <= 0))
+            if (T.expert_slot >= 0 && ((!d.expert_idx && !d.route_logits) || J.expert_rows <= 0))
+                return RF_ERR_INVALID_ARG;
+            if (T.expert_slot >= 0 && d.route_logits && T.expert_slot >= d.route_k)
                 return RF_ERR_INVALID_ARG;
         }
     }
@@ -1151,7 +1243,14 @@ static rf_status launch_merged(const LaunchDesc &d, int nb, int64_t RB, cudaStre
             p.stages = stages;
             p.kc = geo.kc;
             p.slot = geo.slot;
-            p.prefetch_early = (d.pdl && !d.any_expert) ? 1 : 0;
+            // Weights may be fetched before the previous grid finishes unless
+            // their rows come from a routing result that grid writes.
+            p.prefetch_early = (d.pdl && (!d.any_expert || d.route_logits)) ? 1 : 0;
+            p.route_logits = d.route_logits;
+            p.route_idx_out = d.route_idx_out;
+            p.route_w_out = d.route_w_out;
+            p.route_n = d.route_n;
+            p.route_k = d.route_k;
             p.max_terms = max_terms;
             p.n_maps = n_maps;
             return RF_OK;

@@ -18,6 +18,7 @@ constexpr int kMaxX = 8;       // distinct activation vectors per launch
 enum Combine : int32_t {
     kCombineSum = 0,     // y = sum_t weight_t * dot_t (weight 1 when weights == nullptr)
     kCombineSwiGLU = 1,  // y = silu(dot_0) * dot_1  (gate, up)
+    kCombineRouted = 2,  // y = sum_t w[expert_slot_t] * dot_t, w from the launch's own routing
 };
 enum Act : int32_t { kActNone = 0, kActGelu = 1 };
 
@@ -55,6 +56,14 @@ struct LaunchDesc {
     const int32_t *expert_idx = nullptr;   // device, for expert_slot terms
     bool pdl = false;                      // programmatic dependent launch
     bool any_expert = false;               // some term resolves an expert on device
+    // Routing computed inside the launch (instead of expert_idx): top route_k
+    // of route_n logits (ties to the lower index) and a softmax over the k
+    // selected; CTA 0 also stores them to route_idx_out / route_w_out.  The
+    // logits must not be written by the kernel this launch is chained to.
+    const float *route_logits = nullptr;
+    int route_n = 0, route_k = 0;
+    int32_t *route_idx_out = nullptr;
+    float *route_w_out = nullptr;
 };
 
 // Validates and launches the row-window GEMV kernel (in batches of kMaxJobs

@@ -189,8 +189,11 @@ rf_status rf_moe_ffn(int fmt, const float *router_logits, int n_expert, int top_
                                          align256(sizeof(float) * kMaxTopK));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    rf_status st = launch_router(router_logits, n_expert, top_k, idx, wts, s);
-    if (st != RF_OK) return st;
+    // Routing happens inside both launches (every CTA ranks the logits
+    // itself), so no launch waits for a separate router and the down
+    // launch's weight copies can start while gate/up still runs.  The first
+    // launch also stores the routing result in the workspace.
+    rf_status st = RF_OK;
 
     // Gate/up: one job per (selected expert k, row window j); the SwiGLU
     // epilogue writes h_k[window].
@@ -219,9 +222,13 @@ rf_status rf_moe_ffn(int fmt, const float *router_logits, int n_expert, int top_
     d1.n_jobs = nj;
     d1.x[0] = x;
     d1.n_x = 1;
-    d1.expert_idx = idx;
     d1.any_expert = true;
-    d1.pdl = true;
+    d1.pdl = false;
+    d1.route_logits = router_logits;
+    d1.route_n = n_expert;
+    d1.route_k = top_k;
+    d1.route_idx_out = idx;
+    d1.route_w_out = wts;
     st = launch_rowwin(d1, s);
     if (st != RF_OK) return st;
 
@@ -234,13 +241,12 @@ rf_status rf_moe_ffn(int fmt, const float *router_logits, int n_expert, int top_
         const int64_t r0 = j * br_embd;
         for (int k = 0; k < top_k; ++k) J.term[k] = Term{static_cast<const uint8_t *>(down), k, k, 0, 0};
         J.y = y + r0;
-        J.weights = wts;
         J.row0 = r0;
         J.expert_rows = n_embd;
         J.expert_count = n_expert;
         J.n_rows = (int32_t)(r0 + br_embd < n_embd ? br_embd : n_embd - r0);
         J.n_terms = top_k;
-        J.combine = kCombineSum;
+        J.combine = kCombineRouted;
     }
     LaunchDesc d2;
     d2.fmt = fmt;
@@ -249,9 +255,11 @@ rf_status rf_moe_ffn(int fmt, const float *router_logits, int n_expert, int top_
     d2.n_jobs = nj;
     for (int k = 0; k < top_k; ++k) d2.x[k] = h + (int64_t)k * n_ff;
     d2.n_x = top_k;
-    d2.expert_idx = idx;
     d2.any_expert = true;
     d2.pdl = true;
+    d2.route_logits = router_logits;
+    d2.route_n = n_expert;
+    d2.route_k = top_k;
     return launch_rowwin(d2, s);
 }
 
