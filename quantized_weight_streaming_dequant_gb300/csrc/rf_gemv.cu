@@ -471,17 +471,27 @@ __device__ __forceinline__ void route_warp(const float *__restrict__ logits, int
 // Minimum CTAs per SM the register budget is sized for: 272-byte aligned
 // chunks (Q8_0, MXFP4) need more registers and their shared memory allows
 // one CTA per SM anyway.
-constexpr int kModePerLane = 0, kModeTensor = 1, kModeFlat = 2;
+// kModeTensorWS -- tensor copies issued by a ninth, producer warp (lane w feeds
+// warp w's ring, waiting on the ring's "slot released" barriers), so the eight
+// consumer warps only wait, decode and accumulate.
+constexpr int kModePerLane = 0, kModeTensor = 1, kModeFlat = 2, kModeTensorWS = 3;
+
+template <int MODE>
+constexpr int threads_of() { return MODE == kModeTensorWS ? kThreads + 32 : kThreads; }
 
 template <int FMT, int MODE>
-constexpr int min_ctas() { return (MODE == kModeTensor && FMT != RF_Q4_0) ? 1 : 2; }
+constexpr int min_ctas()
+{
+    return ((MODE == kModeTensor || MODE == kModeTensorWS) && FMT != RF_Q4_0) ? 1 : 2;
+}
 
 template <int FMT, int MODE, class KP>
-__global__ void __launch_bounds__(kThreads, min_ctas<FMT, MODE>())
+__global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
     rowwin_kernel(const __grid_constant__ KP p)
 {
     using F = FmtT<FMT>;
-    constexpr bool TMA = MODE == kModeTensor;
+    constexpr bool WS = MODE == kModeTensorWS;
+    constexpr bool TMA = MODE == kModeTensor || WS;
     constexpr bool FLAT = MODE == kModeFlat;
     extern __shared__ __align__(128) uint8_t smem[];
 
@@ -497,8 +507,10 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, MODE>())
     size_t off = ((size_t)p.n_x * nb * sizeof(XRec) + 127) & ~(size_t)127;
     uint8_t *slots = smem + off;
     off += FLAT ? (size_t)ST * SLOT : (size_t)kNW * ST * kRows * SLOT;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + off);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + off);   // slot filled
     off += (size_t)(FLAT ? ST : kNW * ST) * sizeof(uint64_t);
+    uint64_t *ebars = reinterpret_cast<uint64_t *>(smem + off);  // producer mode: slot released
+    if constexpr (WS) off += (size_t)kNW * ST * sizeof(uint64_t);
     float *red = reinterpret_cast<float *>(smem + off);   // [2][NT][kNW][32]
     off += (size_t)2 * NT * kNW * 32 * sizeof(float);
     int *cnt = reinterpret_cast<int *>(smem + off);       // arrivals per parity, then groups done
@@ -526,6 +538,11 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, MODE>())
 
     if constexpr (FLAT) {
         if ((int)threadIdx.x < ST) mbar_init(&bars[threadIdx.x], 1);
+    } else if constexpr (WS) {
+        if (warp < kNW && lane < ST) {
+            mbar_init(&bars[warp * ST + lane], 1);
+            mbar_init(&ebars[warp * ST + lane], 1);
+        }
     } else {
         if (lane < ST) mbar_init(&bars[warp * ST + lane], TMA ? 1 : 32);
     }
@@ -539,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, MODE>())
         const int words = n_jobs * (int)(sizeof(Job) / 4);
         const uint32_t *src = reinterpret_cast<const uint32_t *>(p.jobs);
         uint32_t *dst = reinterpret_cast<uint32_t *>(jobs);
-        for (int i = threadIdx.x; i < words; i += kThreads) dst[i] = src[i];
+        for (int i = threadIdx.x; i < words; i += blockDim.x) dst[i] = src[i];
     }
     fence_barrier_init();
     int32_t *s_eidx = cnt + 16;
@@ -624,7 +641,41 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, MODE>())
     // kernel writes).  A CTA that becomes resident while the previous kernel
     // runs then holds its first chunks by the time the activations exist.
     int primed = 0;
-    if (p.prefetch_early) {
+    if constexpr (WS) {
+        if (warp == kNW) {
+            // Producer: lane w walks warp w's chunks and refills each slot
+            // as soon as warp w has released it (first round: all free).
+            if (!p.prefetch_early) pdl_wait();   // rows may depend on a previous grid
+            if (lane < kNW) {
+                const int w = lane;
+                const int kbl = min(nb, GS * (w * nG / kNW));
+                const int kbh = min(nb, GS * ((w + 1) * nG / kNW));
+                const int nch = (kbh - kbl + KC - 1) / KC;
+                Cursor c{g_lo, 0, 0, 0, g_lo < g_hi && nch > 0};
+                if (c.valid) cursor_fix_job(jobs, n_jobs, c);
+                uint8_t *wslots = slots + (size_t)w * ST * kRows * SLOT;
+                int st = 0;
+                uint32_t ph = 0;
+                while (c.valid) {
+                    mbar_wait_bounded(&ebars[w * ST + st], ph ^ 1u, &g_device_status);
+                    const Job &J = jobs[c.j];
+                    const Term &T = J.term[c.t];
+                    int64_t y = J.row0 + (int64_t)(c.g - J.group_begin) * kRows;
+                    if (T.expert_slot >= 0) y += (int64_t)eidx[T.expert_slot] * J.expert_rows;
+                    const int x = (kbl + c.c * KC) * F::BS / 2;   // uint16 units
+                    mbar_arrive_expect_tx(&bars[w * ST + st], (uint32_t)(kRows * SLOT));
+                    tma_2d_g2s(wslots + (size_t)st * kRows * SLOT, &p.maps[T.tmap], x, (int)y,
+                               &bars[w * ST + st]);
+                    cursor_advance(jobs, n_jobs, c, nch, g_hi);
+                    if (++st == ST) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            return;
+        }
+    } else if (p.prefetch_early) {
         for (; primed < ST && ic.valid; ++primed) prime(primed);
     }
     pdl_launch_dependents();
@@ -659,7 +710,8 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, MODE>())
                 for (int i = 0; i < 8; ++i) v[ps][i] = 0.f;
             }
         }
-        for (int s = primed; s < ST && ic.valid; ++s) prime(s);
+        if constexpr (!WS)
+            for (int s = primed; s < ST && ic.valid; ++s) prime(s);
 #pragma unroll
         for (int ps = 0; ps < kXPre; ++ps)
             if (ps < passes) xrec_build<FMT>(v[ps], threadIdx.x & 3, act[ps], &xrec[rec[ps]]);
@@ -672,7 +724,10 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, MODE>())
             xrec_build<FMT>(w, threadIdx.x & 3, a, &xrec[rc]);
         }
     }
-    __syncthreads();
+    if constexpr (WS)
+        asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");   // consumer warps only
+    else
+        __syncthreads();
 
     int cs = 0;          // stage of the next chunk to consume
     uint32_t cph = 0;    // its mbarrier phase parity
@@ -735,8 +790,9 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, MODE>())
                 if (ic.valid) cursor_advance(jobs, n_jobs, ic, 1, g_hi);
             }
             for (int c = 0; c < (FLAT ? 0 : n_chunks); ++c) {
-                mbar_wait_bounded(&my_bars[cs], cph, &g_device_status);
-                const uint8_t *slot = my_slots + ((size_t)cs * kRows + lane) * SLOT;
+                const int cur = cs;
+                mbar_wait_bounded(&my_bars[cur], cph, &g_device_status);
+                const uint8_t *slot = my_slots + ((size_t)cur * kRows + lane) * SLOT;
                 if (++cs == ST) {
                     cs = 0;
                     cph ^= 1u;
@@ -749,7 +805,9 @@ __global__ void __launch_bounds__(kThreads, min_ctas<FMT, MODE>())
                     GroupRegs<FMT> r;
                     load_group<FMT>(slot, r);
                     __syncwarp();
-                    if (ic.valid) {
+                    if constexpr (WS) {
+                        if (lane == 0) mbar_arrive(&ebars[warp * ST + cur]);
+                    } else if (ic.valid) {
                         issue(ic);
                         cursor_advance(jobs, n_jobs, ic, n_chunks, g_hi);
                     }
@@ -864,11 +922,11 @@ ChunkGeom chunk_geom(int fmt, bool aligned)
 int flat_slot(int64_t row_bytes) { return (int)((kRows * row_bytes + 32 + 127) / 128 * 128); }
 
 size_t smem_bytes(int n_x, int nb, int stages, int slot, int max_terms, int n_jobs,
-                  bool flat = false)
+                  bool flat = false, bool ws = false)
 {
     return (((size_t)n_x * nb * sizeof(XRec) + 127) & ~(size_t)127) +
            (flat ? (size_t)stages * slot : (size_t)kNW * stages * kRows * slot) +
-           (size_t)(flat ? stages : kNW * stages) * sizeof(uint64_t) +
+           (size_t)(flat ? stages : kNW * stages * (ws ? 2 : 1)) * sizeof(uint64_t) +
            (size_t)2 * max_terms * kNW * 32 * sizeof(float) + kCntInts * sizeof(int) +
            (size_t)n_jobs * sizeof(Job);
 }
@@ -920,7 +978,7 @@ rf_status launch_fmt(const KP &p, int grid, size_t smem, bool pdl, cudaStream_t 
     if (!attr_ok[dev & 63]) return RF_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(threads_of<MODE>());
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -950,6 +1008,8 @@ rf_status launch_any(int fmt, int mode, const KP &p, int grid, size_t smem, bool
                      cudaStream_t stream, int dev)
 {
     if (mode == kModeTensor) return launch_mode<kModeTensor>(fmt, p, grid, smem, pdl, stream, dev);
+    if (mode == kModeTensorWS)
+        return launch_mode<kModeTensorWS>(fmt, p, grid, smem, pdl, stream, dev);
     if (mode == kModeFlat) return launch_mode<kModeFlat>(fmt, p, grid, smem, pdl, stream, dev);
     return launch_mode<kModePerLane>(fmt, p, grid, smem, pdl, stream, dev);
 }
@@ -1147,7 +1207,8 @@ static rf_status launch_merged(const LaunchDesc &d, int nb, int64_t RB, cudaStre
     for (int i = 0; i < d.n_jobs; ++i) max_terms = std::max(max_terms, (int)d.jobs[i].n_terms);
     const int nj_max = std::min(d.n_jobs, kMaxJobs);
     const size_t per2 = (size_t)di.max_smem_sm / 2 - (size_t)di.reserved_per_block;
-    int mode = aligned ? kModeTensor : kModePerLane;
+    int mode = aligned ? kModeTensorWS : kModePerLane;
+    const bool ws = mode == kModeTensorWS;
     int ctas_per_sm = 0, stages = 0;
     // Misaligned rows: stage whole 32-row groups when two of them fit (two
     // CTAs per SM if possible).
@@ -1173,17 +1234,19 @@ static rf_status launch_merged(const LaunchDesc &d, int nb, int64_t RB, cudaStre
     // least 2 stages; else one CTA with up to 4 stages.
     const bool two_ok = !aligned || d.fmt == RF_Q4_0;   // register budget (min_ctas)
     for (int st = 4; st >= 2 && !ctas_per_sm && two_ok; --st)
-        if (smem_bytes(d.n_x, nb, st, geo.slot, max_terms, nj_max) <= per2) {
+        if (smem_bytes(d.n_x, nb, st, geo.slot, max_terms, nj_max, false, ws) <= per2) {
             ctas_per_sm = 2;
             stages = st;
         }
     for (int st = 4; st >= 1 && !ctas_per_sm; --st)
-        if (smem_bytes(d.n_x, nb, st, geo.slot, max_terms, nj_max) <= (size_t)di.max_smem_block) {
+        if (smem_bytes(d.n_x, nb, st, geo.slot, max_terms, nj_max, false, ws) <=
+            (size_t)di.max_smem_block) {
             ctas_per_sm = 1;
             stages = st;
         }
     if (!ctas_per_sm) return RF_ERR_TOO_LARGE;
-    const size_t smem = smem_bytes(d.n_x, nb, stages, geo.slot, max_terms, nj_max, mode == kModeFlat);
+    const size_t smem =
+        smem_bytes(d.n_x, nb, stages, geo.slot, max_terms, nj_max, mode == kModeFlat, ws);
 
     // Launch in batches of kMaxJobs windows.
     for (int base = 0; base < d.n_jobs; base += kMaxJobs) {
