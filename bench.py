@@ -187,9 +187,12 @@ def build_dense_layers(torch, rf, device, copies: int, seed: int):
 
 
 def dense_outputs(torch, device):
+    import quantized_weight_streaming_dequant_gb300 as rf
     d, f = syn.C2["d_model"], syn.C2["d_ff"]
-    return {k: torch.empty(n, dtype=torch.float32, device=device)
-            for k, n in (("q", d), ("k", d), ("v", d), ("o", d), ("h", f), ("y", d))}
+    out = {k: torch.empty(n, dtype=torch.float32, device=device)
+           for k, n in (("q", d), ("k", d), ("v", d), ("o", d), ("h", f), ("y", d))}
+    out["hd"] = rf.ffn_workspace(f, device)   # h's digits, handed from gate/up to down
+    return out
 
 
 def run_dense(args, torch, rf, device, rank, world, dist):
@@ -293,7 +296,7 @@ def per_phase_times(torch, rf, layers, x, attn, x_ffn, out, stream, reps):
             rf.gemv(fmt, L.wo, 0, d, d, attn, out["o"], stream=stream)
             ev[2].record(stream)
             rf.ffn_swiglu(fmt, L.w_gate, L.w_up, L.w_down, f, d, x_ffn, out["y"], out["h"],
-                          stream=stream)
+                          stream=stream, workspace=out["hd"])
             ev[3].record(stream)
             torch.cuda.synchronize()
             acc["qkv"] += ev[0].elapsed_time(ev[1])

@@ -173,6 +173,19 @@ RF_API rf_status rf_ffn_swiglu_ex(int fmt, const void *gate, const void *up, con
                                   int64_t n_ff, int64_t n_embd, const float *x, float *y,
                                   float *h, unsigned flags, void *stream);
 
+/* Bytes of workspace rf_ffn_swiglu_ws takes for n_ff activations (80 bytes
+ * per 32); 0 if n_ff is not a positive multiple of 32. */
+RF_API size_t rf_ffn_workspace_bytes(int64_t n_ff);
+
+/* rf_ffn_swiglu_ex with a device workspace of rf_ffn_workspace_bytes(n_ff)
+ * bytes (16-byte aligned; NULL = none): the first launch also writes the
+ * fixed-point digits of h that the second launch multiplies by, so the down
+ * projection copies them instead of rebuilding them from h.  Results are
+ * bit-identical to rf_ffn_swiglu_ex.  The workspace is overwritten. */
+RF_API rf_status rf_ffn_swiglu_ws(int fmt, const void *gate, const void *up, const void *down,
+                                  int64_t n_ff, int64_t n_embd, const float *x, float *y,
+                                  float *h, void *workspace, unsigned flags, void *stream);
+
 /* ------------------------------------------- host-streamed row windows */
 /* An arena is a bounded ring of device memory plus a copy stream and events
  * (neurostream, "How it works" 6: every in-flight block holds a byte
@@ -243,7 +256,9 @@ RF_API rf_status rf_stream_stats_get(const rf_arena *arena, rf_stream_stats *out
 RF_API rf_status rf_moe_route(const float *logits, int n_expert, int top_k, int32_t *idx,
                               float *w, void *stream);
 
-/* Bytes of caller scratch rf_moe_ffn needs (routing result + activations). */
+/* Bytes of caller scratch rf_moe_ffn needs (routing result, activations and
+ * their fixed-point digits); 0 if top_k is out of range or n_ff is not a
+ * positive multiple of 32. */
 RF_API size_t rf_moe_workspace_bytes(int top_k, int64_t n_ff, int64_t n_embd,
                                      int64_t block_rows);
 
@@ -268,7 +283,8 @@ RF_API rf_status rf_moe_ffn(int fmt, const float *router_logits, int n_expert, i
  * must not call cudaMalloc/cudaFree because those synchronize the device.
  * (The source pages have no counterpart to this entry point.)
  * The scratch it needs lives in a fixed device array inside the library,
- * RF_MOE_STATIC_MAX_H floats of activations plus the routing result, which
+ * RF_MOE_STATIC_MAX_H floats of activations, their digits (80 bytes per 32)
+ * and the routing result, which
  * every GPU that loads the library keeps until the process exits.  Limit:
  * top_k * n_ff <= RF_MOE_STATIC_MAX_H, else RF_ERR_TOO_LARGE before any work.
  * The first call on a device looks up the array's device address (once per

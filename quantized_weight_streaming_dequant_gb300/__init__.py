@@ -61,6 +61,8 @@ _SIGS = {
     "rf_swiglu": ([_P, _P, _P, _I64, _P], _I),
     "rf_gelu": ([_P, _P, _I64, _P], _I),
     "rf_ffn_swiglu": ([_I, _P, _P, _P, _I64, _I64, _P, _P, _P, _P], _I),
+    "rf_ffn_workspace_bytes": ([_I64], _SZ),
+    "rf_ffn_swiglu_ws": ([_I, _P, _P, _P, _I64, _I64, _P, _P, _P, _P, ctypes.c_uint, _P], _I),
     "rf_arena_create": ([_SZ, ctypes.POINTER(_P)], _I),
     "rf_arena_destroy": ([_P], None),
     "rf_stream_plan": ([_I, _I64, _I64, _I64, _I, _SZ, ctypes.POINTER(_I64),
@@ -183,14 +185,23 @@ def gelu(z, h=None, stream=None):
     return h
 
 
+def ffn_workspace(n_ff: int, device):
+    """Device workspace for ffn_swiglu's digit hand-off between its launches."""
+    import torch
+    return torch.empty(lib().rf_ffn_workspace_bytes(n_ff), dtype=torch.uint8, device=device)
+
+
 def ffn_swiglu(fmt: int, gate, up, down, n_ff: int, n_embd: int, x, y=None, h=None,
-               stream=None, flags: int = 0):
+               stream=None, flags: int = 0, workspace=None):
+    """rf_ffn_swiglu_ws (workspace: from ffn_workspace, or None)."""
     import torch
     y = torch.empty(n_embd, dtype=torch.float32, device=x.device) if y is None else y
     h = torch.empty(n_ff, dtype=torch.float32, device=x.device) if h is None else h
-    _check(lib().rf_ffn_swiglu_ex(fmt, _dev_ptr(gate, "gate"), _dev_ptr(up, "up"),
+    _check(lib().rf_ffn_swiglu_ws(fmt, _dev_ptr(gate, "gate"), _dev_ptr(up, "up"),
                                   _dev_ptr(down, "down"), n_ff, n_embd, _dev_ptr(x, "x"),
-                                  _dev_ptr(y, "y"), _dev_ptr(h, "h"), flags, _stream(stream)),
+                                  _dev_ptr(y, "y"), _dev_ptr(h, "h"),
+                                  _dev_ptr(workspace, "workspace") if workspace is not None
+                                  else None, flags, _stream(stream)),
            "rf_ffn_swiglu")
     return y, h
 

@@ -252,6 +252,18 @@ rf_status rf_ffn_swiglu_ex(int fmt, const void *gate, const void *up, const void
                            int64_t n_ff, int64_t n_embd, const float *x, float *y, float *h,
                            unsigned flags, void *stream)
 {
+    return rf_ffn_swiglu_ws(fmt, gate, up, down, n_ff, n_embd, x, y, h, nullptr, flags, stream);
+}
+
+size_t rf_ffn_workspace_bytes(int64_t n_ff)
+{
+    return n_ff > 0 && n_ff % 32 == 0 ? xrec_bytes(n_ff) : 0;
+}
+
+rf_status rf_ffn_swiglu_ws(int fmt, const void *gate, const void *up, const void *down,
+                           int64_t n_ff, int64_t n_embd, const float *x, float *y, float *h,
+                           void *workspace, unsigned flags, void *stream)
+{
     if (!fmt_ok(fmt)) return RF_ERR_UNSUPPORTED_FMT;
     if (!gate || !up || !down || !x || !y || !h || n_ff <= 0 || n_embd <= 0 ||
         n_ff % 32 != 0 || n_embd % 32 != 0)
@@ -259,6 +271,7 @@ rf_status rf_ffn_swiglu_ex(int fmt, const void *gate, const void *up, const void
     if (n_ff > 0x7fffffffLL || n_embd > 0x7fffffffLL) return RF_ERR_TOO_LARGE;
     for (const void *p : {gate, up, down})
         if ((reinterpret_cast<uintptr_t>(p) & 15u) != 0) return RF_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return RF_ERR_MISALIGNED;
     if (const rf_status c = check_in_dim(fmt, n_embd, 1)) return c;
     if (const rf_status c = check_in_dim(fmt, n_ff, 1)) return c;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -279,6 +292,8 @@ rf_status rf_ffn_swiglu_ex(int fmt, const void *gate, const void *up, const void
     d1.x[0] = x;
     d1.n_x = 1;
     d1.pdl = (flags & RF_CHAIN) != 0;
+    d1.xr_out = workspace;   // with a workspace, phase 1 also writes h's digits
+    d1.xr_y_base = h;
     rf_status st = launch_rowwin(d1, s);
     if (st != RF_OK) return st;
     // Phase 2: walk down by output dimension (programmatic dependent launch:
@@ -298,6 +313,7 @@ rf_status rf_ffn_swiglu_ex(int fmt, const void *gate, const void *up, const void
     d2.x[0] = h;
     d2.n_x = 1;
     d2.pdl = true;
+    d2.xr_in = workspace;    // ... which phase 2 copies instead of building
     return launch_rowwin(d2, s);
 }
 

@@ -109,6 +109,9 @@ struct KParamsT {
     const float *route_logits;   // non-null: route inside the launch (see LaunchDesc)
     int32_t *route_idx_out;
     float *route_w_out;
+    XRec *xr_out;                // activation digits out / in (see LaunchDesc)
+    const float *xr_y_base;
+    const XRec *xr_in;
     int32_t route_n, route_k;
 };
 using KParamsSmall = KParamsT<4, 4>;
@@ -201,6 +204,44 @@ __device__ __forceinline__ void xrec_build(const float (&v)[8], int part, bool a
         out->scale = exp2i(-s);
         out->pad[0] = out->pad[1] = 0;
     }
+}
+
+// Digits of one 32-element block held one element per lane (lane j = element
+// j), written to *out: the same record xrec_build makes from those values.
+// All 32 lanes must call it.
+template <int FMT>
+__device__ __forceinline__ void xrec_emit(float v, XRec *out)
+{
+    const int lane = threadIdx.x & 31;
+    float m = fabsf(v);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const int biased = (int)(__float_as_uint(m) >> 23);
+    const int e = biased == 0 ? -125 : biased - 126;
+    const int s = 15 - e;
+    const float f1 = exp2i(min(s, 127)), f2 = exp2i(max(s - 127, 0));
+    const float t = (v * f1) * f2 + 12582912.0f;
+    const int X = max(-32767, min(32767, (int)(__float_as_uint(t) - 0x4b400000u)));
+    int sum = X;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    // Lane L < 16 assembles plane L >> 3, word L & 7.
+    const int w = lane & 7;
+    const uint32_t a = (uint32_t)__shfl_sync(0xffffffffu, X, elem_of<FMT>(w, 0));
+    const uint32_t b = (uint32_t)__shfl_sync(0xffffffffu, X, elem_of<FMT>(w, 1));
+    const uint32_t c = (uint32_t)__shfl_sync(0xffffffffu, X, elem_of<FMT>(w, 2));
+    const uint32_t d = (uint32_t)__shfl_sync(0xffffffffu, X, elem_of<FMT>(w, 3));
+    const uint32_t sel = lane < 8 ? 0x0040u : 0x0051u;
+    const uint32_t word = prmt(prmt(a, b, sel), prmt(c, d, sel), 0x5410u);
+    uint32_t *o32 = reinterpret_cast<uint32_t *>(out);
+    if (lane < 16)
+        o32[lane] = word;
+    else if (lane == 16)
+        o32[16] = (uint32_t)(FMT == RF_Q4_0 ? -8 * sum : 0);
+    else if (lane == 17)
+        o32[17] = __float_as_uint(exp2i(-s));
+    else if (lane < 20)
+        o32[lane] = 0;
 }
 
 // Integer dot of one block's quant words with the block's digit planes;
@@ -681,10 +722,33 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
     pdl_launch_dependents();
     pdl_wait();
 
-    // Activation digits for every x of the launch, once per CTA, four lanes
-    // per 32-element block.  The first kXPre passes' loads go out before the
-    // remaining weight copies, so they do not queue behind them.
-    {
+    // Activation digits for every x of the launch, once per CTA: copied when
+    // the launch that produced the activations also wrote their digits,
+    // otherwise built by four lanes per 32-element block.  The first kXPre
+    // passes' loads go out before the remaining weight copies, so they do not
+    // queue behind them.
+    if (p.xr_in) {
+        const int n16 = p.n_x * nb * (int)(sizeof(XRec) / 16);
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.xr_in);
+        uint4 *dst = reinterpret_cast<uint4 *>(xrec);
+        constexpr int kU = 8;
+        for (int base = 0; base < n16; base += kU * kThreads) {
+            uint4 t[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int i = base + u * kThreads + (int)threadIdx.x;
+                if (i < n16) t[u] = src[i];
+            }
+            if constexpr (!WS)
+                if (base == 0)
+                    for (int s = primed; s < ST && ic.valid; ++s) prime(s);
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int i = base + u * kThreads + (int)threadIdx.x;
+                if (i < n16) dst[i] = t[u];
+            }
+        }
+    } else {
         constexpr int kXPre = 8;
         const int n_rec = p.n_x * nb;
         const int passes = (4 * n_rec + kThreads - 1) / kThreads;
@@ -855,11 +919,12 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
                     yacc = t == 0 ? dot : yacc + dot;
                 }
             }
-            if (row_ok) {
-                float out = yacc;
-                if (J.act == kActGelu) out = 0.5f * out * (1.f + erff(out * 0.70710678118654752f));
-                J.y[rowrel] = out;
-            }
+            float out = yacc;
+            if (J.act == kActGelu) out = 0.5f * out * (1.f + erff(out * 0.70710678118654752f));
+            if (row_ok) J.y[rowrel] = out;
+            if (p.xr_out)
+                xrec_emit<FMT>(row_ok ? out : 0.f,
+                               p.xr_out + ((J.y - p.xr_y_base) + (rowrel - lane)) / kRows);
             __syncwarp();
             if (lane == 0) {
                 cnt[par] = 0;
@@ -1007,7 +1072,6 @@ template <class KP>
 rf_status launch_any(int fmt, int mode, const KP &p, int grid, size_t smem, bool pdl,
                      cudaStream_t stream, int dev)
 {
-    if (mode == kModeTensor) return launch_mode<kModeTensor>(fmt, p, grid, smem, pdl, stream, dev);
     if (mode == kModeTensorWS)
         return launch_mode<kModeTensorWS>(fmt, p, grid, smem, pdl, stream, dev);
     if (mode == kModeFlat) return launch_mode<kModeFlat>(fmt, p, grid, smem, pdl, stream, dev);
@@ -1142,6 +1206,15 @@ rf_status launch_rowwin(const LaunchDesc &d, cudaStream_t stream)
     for (int s = 0; s < d.n_x; ++s)
         if (!d.x[s]) return RF_ERR_INVALID_ARG;
     if (d.any_expert && !d.expert_idx && !d.route_logits) return RF_ERR_INVALID_ARG;
+    if (d.xr_out) {
+        if (!d.xr_y_base || (reinterpret_cast<uintptr_t>(d.xr_out) & 15u) != 0)
+            return RF_ERR_INVALID_ARG;
+        for (int i = 0; i < d.n_jobs; ++i)
+            if ((d.jobs[i].y - d.xr_y_base) % kRows != 0 || d.jobs[i].n_rows % kRows != 0 ||
+                d.jobs[i].y < d.xr_y_base)
+                return RF_ERR_INVALID_ARG;
+    }
+    if (d.xr_in && (reinterpret_cast<uintptr_t>(d.xr_in) & 15u) != 0) return RF_ERR_MISALIGNED;
     if (d.route_logits && (d.route_n < 1 || d.route_n > 1024 || d.route_k < 1 ||
                            d.route_k > kMaxTerms || d.route_k > d.route_n))
         return RF_ERR_INVALID_ARG;
@@ -1314,6 +1387,9 @@ static rf_status launch_merged(const LaunchDesc &d, int nb, int64_t RB, cudaStre
             p.route_w_out = d.route_w_out;
             p.route_n = d.route_n;
             p.route_k = d.route_k;
+            p.xr_out = static_cast<XRec *>(d.xr_out);
+            p.xr_y_base = d.xr_y_base;
+            p.xr_in = static_cast<const XRec *>(d.xr_in);
             p.max_terms = max_terms;
             p.n_maps = n_maps;
             return RF_OK;

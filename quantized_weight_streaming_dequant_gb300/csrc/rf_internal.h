@@ -64,7 +64,18 @@ struct LaunchDesc {
     int route_n = 0, route_k = 0;
     int32_t *route_idx_out = nullptr;
     float *route_w_out = nullptr;
+    // Activation digits (80 bytes per 32 activations) written by this launch
+    // for every full 32-output block of its jobs, indexed by the outputs'
+    // position from xr_y_base (jobs must start and end on 32-output
+    // boundaries from it), and digits read instead of built: slot s of the
+    // launch's activations is records [s*in_dim/32, (s+1)*in_dim/32) of xr_in.
+    void *xr_out = nullptr;
+    const float *xr_y_base = nullptr;
+    const void *xr_in = nullptr;
 };
+
+// Bytes of activation digits for n activations (n a multiple of 32).
+constexpr size_t xrec_bytes(int64_t n) { return (size_t)(n / 32) * 80; }
 
 // Validates and launches the row-window GEMV kernel (in batches of kMaxJobs
 // windows).  Host-side argument checks return an error before anything is

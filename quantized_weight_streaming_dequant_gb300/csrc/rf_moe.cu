@@ -91,7 +91,8 @@ size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
 
 // Scratch for rf_moe_ffn_noalloc: routing result (two 256-byte slots) and up
 // to RF_MOE_STATIC_MAX_H activations, laid out like an rf_moe_ffn workspace.
-constexpr size_t kStaticScratchBytes = 512 + sizeof(float) * (size_t)RF_MOE_STATIC_MAX_H;
+constexpr size_t kStaticScratchBytes =
+    512 + sizeof(float) * (size_t)RF_MOE_STATIC_MAX_H + xrec_bytes(RF_MOE_STATIC_MAX_H);
 static __device__ __align__(256) unsigned char g_moe_scratch[kStaticScratchBytes];
 
 // Device address of g_moe_scratch per device.  In host code the symbol is
@@ -151,8 +152,10 @@ size_t rf_moe_workspace_bytes(int top_k, int64_t n_ff, int64_t n_embd, int64_t b
     (void)n_embd;
     (void)block_rows;
     if (top_k < 1 || top_k > kMaxTopK || n_ff <= 0) return 0;
+    if (n_ff % 32 != 0) return 0;
     return align256(sizeof(int32_t) * kMaxTopK) + align256(sizeof(float) * kMaxTopK) +
-           align256(sizeof(float) * (size_t)top_k * (size_t)n_ff);
+           align256(sizeof(float) * (size_t)top_k * (size_t)n_ff) +
+           xrec_bytes((int64_t)top_k * n_ff);
 }
 
 rf_status rf_moe_ffn(int fmt, const float *router_logits, int n_expert, int top_k,
@@ -187,6 +190,9 @@ rf_status rf_moe_ffn(int fmt, const float *router_logits, int n_expert, int top_
     float *wts = reinterpret_cast<float *>(ws + align256(sizeof(int32_t) * kMaxTopK));
     float *h = reinterpret_cast<float *>(ws + align256(sizeof(int32_t) * kMaxTopK) +
                                          align256(sizeof(float) * kMaxTopK));
+    // Digits of h, written by the gate/up launch and read by the down launch.
+    void *hdig = ws + align256(sizeof(int32_t) * kMaxTopK) + align256(sizeof(float) * kMaxTopK) +
+                 align256(sizeof(float) * (size_t)top_k * (size_t)n_ff);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     // Routing happens inside both launches (every CTA ranks the logits
@@ -229,6 +235,8 @@ rf_status rf_moe_ffn(int fmt, const float *router_logits, int n_expert, int top_
     d1.route_k = top_k;
     d1.route_idx_out = idx;
     d1.route_w_out = wts;
+    d1.xr_out = hdig;
+    d1.xr_y_base = h;
     st = launch_rowwin(d1, s);
     if (st != RF_OK) return st;
 
@@ -260,6 +268,7 @@ rf_status rf_moe_ffn(int fmt, const float *router_logits, int n_expert, int top_
     d2.route_logits = router_logits;
     d2.route_n = n_expert;
     d2.route_k = top_k;
+    d2.xr_in = hdig;
     return launch_rowwin(d2, s);
 }
 

@@ -32,7 +32,8 @@ class DenseLayer:
     w_down: object
 
     def step(self, x, attn, x_ffn, out, stream=None, chain: bool = True):
-        """out: dict of device tensors q, k, v, o, h, y (preallocated).  With
+        """out: dict of device tensors q, k, v, o, h, y (preallocated), and
+        optionally hd, an ffn_workspace for h's digits.  With
         `chain`, each launch copies its (static) weights while the previous
         kernel on the stream drains (RF_CHAIN)."""
         d = self.d_model
@@ -41,7 +42,7 @@ class DenseLayer:
                                     (self.wv, 0, d, x, out["v"])], stream=stream, flags=fl)
         rf.gemv(self.fmt, self.wo, 0, d, d, attn, out["o"], stream=stream, flags=fl)
         rf.ffn_swiglu(self.fmt, self.w_gate, self.w_up, self.w_down, self.d_ff, d, x_ffn,
-                      out["y"], out["h"], stream=stream, flags=fl)
+                      out["y"], out["h"], stream=stream, flags=fl, workspace=out.get("hd"))
 
     def weight_bytes(self) -> int:
         rb_d = rf.row_bytes(self.fmt, self.d_model)

@@ -109,7 +109,11 @@ def test_argument_errors_before_any_gpu_work(L):
     assert L.rf_moe_route(p16, 4, 5, p16, p16, None) == 1
     assert L.rf_moe_route(p16, 4, 0, p16, p16, None) == 1
     assert L.rf_moe_route(p16, 2000, 2, p16, p16, None) == 1
-    assert L.rf_moe_workspace_bytes(4, 2880, 2880, 512) == 256 + 256 + 4 * 2880 * 4
+    # routing (2 x 256 B), h (top_k x n_ff floats), h's digits (80 B per 32)
+    assert L.rf_moe_workspace_bytes(4, 2880, 2880, 512) == 256 + 256 + 4 * 2880 * 4 + 4 * 2880 // 32 * 80
+    assert L.rf_moe_workspace_bytes(4, 2890, 2880, 512) == 0
+    assert L.rf_ffn_workspace_bytes(11008) == 11008 // 32 * 80
+    assert L.rf_ffn_workspace_bytes(100) == 0 and L.rf_ffn_workspace_bytes(0) == 0
     assert L.rf_moe_workspace_bytes(0, 2880, 2880, 512) == 0
     # activations
     assert L.rf_swiglu(None, p16, p16, 4, None) == 1

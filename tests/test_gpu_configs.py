@@ -51,8 +51,9 @@ def test_streamed_q8_0_gemv_512x2048(rf):
 
 def test_dense_q4_0_layer_4096_11008(rf):
     """One dense decode layer: QKV batched, O, gate/up + SwiGLU, down; every row
-    of every projection against the oracle; chained and unchained launches give
-    identical bits."""
+    of every projection against the oracle; chained and unchained launches, and
+    the FFN with and without the digit hand-off workspace, give identical
+    bits."""
     import torch
     from quantized_weight_streaming_dequant_gb300.layer import DenseLayer
     fmt, d, f = syn.Q4_0, syn.C2["d_model"], syn.C2["d_ff"]
@@ -63,15 +64,18 @@ def test_dense_q4_0_layer_4096_11008(rf):
     L = DenseLayer(fmt, d, f, *[dev_tensor(m) for m in mats])
     x, attn, x_ffn = (syn.normal_f32(d, 101), syn.normal_f32(d, 102), syn.normal_f32(d, 103))
     outs = []
-    for chain in (False, True):
+    for chain, digits in ((False, False), (True, False), (True, True)):
         out = {k: torch.empty(n, device="cuda") for k, n in
                (("q", d), ("k", d), ("v", d), ("o", d), ("h", f), ("y", d))}
+        if digits:   # gate/up hands h's digits to down through a workspace
+            out["hd"] = rf.ffn_workspace(f, "cuda")
         L.step(dev_tensor(x), dev_tensor(attn), dev_tensor(x_ffn), out, chain=chain)
         torch.cuda.synchronize()
-        outs.append({k: v.cpu().numpy() for k, v in out.items()})
-    for k in outs[0]:
-        assert np.array_equal(bits(outs[0][k]), bits(outs[1][k])), k
-    o = outs[1]
+        outs.append({k: v.cpu().numpy() for k, v in out.items() if k != "hd"})
+    for other in outs[1:]:
+        for k in outs[0]:
+            assert np.array_equal(bits(outs[0][k]), bits(other[k])), k
+    o = outs[2]
     for name, M, inp in (("q", mats[0], x), ("k", mats[1], x), ("v", mats[2], x),
                          ("o", mats[3], attn)):
         assert_gemv_close(o[name], oracle.gemv(fmt, M, 0, d, d, inp), gemv_tol(fmt, M, 0, d, d, inp),

@@ -183,6 +183,14 @@ def test_ffn_swiglu_parity(rf, fmt, n_ff, n_embd):
     # down, checked on the GPU's own h
     y_ref = oracle.gemv(fmt, D, 0, n_embd, n_ff, h.astype(np.float64))
     assert_gemv_close(y, y_ref, gemv_tol(fmt, D, 0, n_embd, n_ff, h), "y")
+    # with the digit hand-off workspace: the same bits (the digits gate/up
+    # writes are the ones down would build from h)
+    ws = rf.ffn_workspace(n_ff, "cuda")
+    for _ in range(2):
+        y2, h2 = rf.ffn_swiglu(fmt, dev_tensor(G), dev_tensor(U), dev_tensor(D), n_ff, n_embd,
+                               dev_tensor(x), workspace=ws)
+        assert np.array_equal(h2.cpu().numpy().view(np.uint32), h.view(np.uint32))
+        assert np.array_equal(y2.cpu().numpy().view(np.uint32), y.view(np.uint32))
 
 
 # ------------------------------------------------------------ streaming
