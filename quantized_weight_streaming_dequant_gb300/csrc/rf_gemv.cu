@@ -48,6 +48,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -93,8 +94,17 @@ struct FmtT<RF_MXFP4> {
 
 constexpr int kMaxMaps = 16;   // distinct weight tensors per launch (tensor-map path)
 // Shared ints: group counters (4), flat-mode stage counters (up to 8, at 4),
-// the launch's own routing: expert ids (8, at 16) and weights (8 floats, at 24).
-constexpr int kCntInts = 32;
+// the launch's own routing: expert ids (8, at 16) and weights (8 floats, at
+// 24), and the producer-mode queue of upcoming groups (8, at 32).
+constexpr int kCntInts = 40;
+constexpr int kGroupQ = 8;
+// Group tickets of launches scheduled dynamically (producer mode): a launch
+// takes slot (launch sequence number mod kSchedSlots), its CTAs take groups
+// past their first from it with atomicAdd, and the CTA that draws the last
+// ticket puts it back to zero.  Slots are reused only kSchedSlots launches
+// later, so launches that may overlap never share one.
+constexpr int kSchedSlots = 1024;
+__device__ unsigned int g_sched[kSchedSlots];
 
 // Kernel parameters.  Two sizes: launches with at most 4 windows and 4 weight
 // tensors (nearly all of them) pass about 1.6 KB instead of 18 KB per launch.
@@ -113,6 +123,7 @@ struct KParamsT {
     const float *xr_y_base;
     const XRec *xr_in;
     int32_t route_n, route_k;
+    int32_t sched_slot;          // >= 0: dynamic group scheduling (producer mode)
 };
 using KParamsSmall = KParamsT<4, 4>;
 using KParamsLarge = KParamsT<kMaxJobs, kMaxMaps>;
@@ -556,6 +567,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
     off += (size_t)2 * NT * kNW * 32 * sizeof(float);
     int *cnt = reinterpret_cast<int *>(smem + off);       // arrivals per parity, then groups done
     int *emp = cnt + 4;                                   // flat mode: readers done per stage
+    volatile int *gq = cnt + 32;                          // producer mode: upcoming groups
     off += kCntInts * sizeof(int);
     Job *jobs = reinterpret_cast<Job *>(smem + off);      // this launch's jobs, read once
     const int n_jobs = p.n_jobs;
@@ -684,35 +696,82 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
     int primed = 0;
     if constexpr (WS) {
         if (warp == kNW) {
-            // Producer: lane w walks warp w's chunks and refills each slot
-            // as soon as warp w has released it (first round: all free).
+            // Producer.  Groups come from the static range [g_lo, g_hi) or,
+            // scheduled dynamically, the CTA's own first group (blockIdx.x)
+            // and then tickets (the next one drawn a group ahead).  For each
+            // group, lane w copies warp w's chunks, refilling each slot as
+            // soon as warp w has released it; a warp with no chunks gets one
+            // empty arrival per group instead.  The group index goes to the
+            // shared queue before its first arrival; a negative index ends it.
             if (!p.prefetch_early) pdl_wait();   // rows may depend on a previous grid
-            if (lane < kNW) {
-                const int w = lane;
-                const int kbl = min(nb, GS * (w * nG / kNW));
-                const int kbh = min(nb, GS * ((w + 1) * nG / kNW));
-                const int nch = (kbh - kbl + KC - 1) / KC;
-                Cursor c{g_lo, 0, 0, 0, g_lo < g_hi && nch > 0};
-                if (c.valid) cursor_fix_job(jobs, n_jobs, c);
-                uint8_t *wslots = slots + (size_t)w * ST * kRows * SLOT;
-                int st = 0;
-                uint32_t ph = 0;
-                while (c.valid) {
-                    mbar_wait_bounded(&ebars[w * ST + st], ph ^ 1u, &g_device_status);
-                    const Job &J = jobs[c.j];
-                    const Term &T = J.term[c.t];
-                    int64_t y = J.row0 + (int64_t)(c.g - J.group_begin) * kRows;
+            const bool dyn = p.sched_slot >= 0;
+            const int total = p.total_groups;
+            auto draw = [&]() -> int {
+                int t = 0;
+                if (lane == 0) {
+                    t = (int)atomicAdd(&g_sched[p.sched_slot], 1u);
+                    if (t == total - 1) g_sched[p.sched_slot] = 0;   // last ticket
+                }
+                t = __shfl_sync(0xffffffffu, t, 0);
+                const int ng = (int)gridDim.x + t;
+                return ng < total ? ng : -1;
+            };
+            const int w = lane & (kNW - 1);
+            const int kbl = min(nb, GS * (w * nG / kNW));
+            const int kbh = min(nb, GS * ((w + 1) * nG / kNW));
+            const int nch = lane < kNW ? (kbh - kbl + KC - 1) / KC : 0;
+            int max_nch = nch;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) max_nch = max(max_nch, __shfl_xor_sync(0xffffffffu, max_nch, o));
+            uint8_t *wslots = slots + (size_t)w * ST * kRows * SLOT;
+            int st = 0;
+            uint32_t ph = 0;
+            auto acquire = [&] {   // next slot of warp w, once warp w released it
+                mbar_wait_bounded(&ebars[w * ST + st], ph ^ 1u, &g_device_status);
+            };
+            auto advance = [&] {
+                if (++st == ST) {
+                    st = 0;
+                    ph ^= 1u;
+                }
+            };
+            int g = dyn ? (int)blockIdx.x : (g_lo < g_hi ? g_lo : -1);
+            int gnext = g < 0 ? -1 : (dyn ? draw() : (g + 1 < g_hi ? g + 1 : -1));
+            int jj = 0;
+            for (int gi = 0;; ++gi) {
+                if (lane == 0) gq[gi & (kGroupQ - 1)] = g;
+                __syncwarp();
+                if (g < 0) {
+                    if (lane < kNW) {
+                        acquire();
+                        mbar_arrive(&bars[w * ST + st]);
+                    }
+                    break;
+                }
+                while (jj < n_jobs && g >= jobs[jj].group_begin + groups_of(jobs[jj])) ++jj;
+                const Job &J = jobs[jj];
+                if (lane < kNW && nch == 0) {
+                    acquire();
+                    mbar_arrive(&bars[w * ST + st]);
+                    advance();
+                }
+                for (int t = 0; t < J.n_terms; ++t) {
+                    const Term &T = J.term[t];
+                    int64_t y = J.row0 + (int64_t)(g - J.group_begin) * kRows;
                     if (T.expert_slot >= 0) y += (int64_t)eidx[T.expert_slot] * J.expert_rows;
-                    const int x = (kbl + c.c * KC) * F::BS / 2;   // uint16 units
-                    mbar_arrive_expect_tx(&bars[w * ST + st], (uint32_t)(kRows * SLOT));
-                    tma_2d_g2s(wslots + (size_t)st * kRows * SLOT, &p.maps[T.tmap], x, (int)y,
-                               &bars[w * ST + st]);
-                    cursor_advance(jobs, n_jobs, c, nch, g_hi);
-                    if (++st == ST) {
-                        st = 0;
-                        ph ^= 1u;
+                    for (int c = 0; c < max_nch; ++c) {
+                        if (c < nch) {
+                            acquire();
+                            const int x = (kbl + c * KC) * F::BS / 2;   // uint16 units
+                            mbar_arrive_expect_tx(&bars[w * ST + st], (uint32_t)(kRows * SLOT));
+                            tma_2d_g2s(wslots + (size_t)st * kRows * SLOT, &p.maps[T.tmap], x,
+                                       (int)y, &bars[w * ST + st]);
+                            advance();
+                        }
                     }
                 }
+                g = gnext;
+                gnext = g < 0 ? -1 : (dyn ? draw() : (g + 1 < g_hi ? g + 1 : -1));
             }
             return;
         }
@@ -796,14 +855,31 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
     int cs = 0;          // stage of the next chunk to consume
     uint32_t cph = 0;    // its mbarrier phase parity
     int j = 0;
-    for (int g = g_lo; g < g_hi; ++g) {
+    for (int gi = 0, g = g_lo;; ++gi, ++g) {
+        if constexpr (WS) {
+            // The producer names the group before the arrival that fills (or,
+            // for a warp without chunks, only signals) this warp's next slot.
+            mbar_wait_bounded(&my_bars[cs], cph, &g_device_status);
+            g = gq[gi & (kGroupQ - 1)];
+            if (g < 0) break;
+            if (n_chunks == 0) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ebars[warp * ST + cs]);
+                if (++cs == ST) {
+                    cs = 0;
+                    cph ^= 1u;
+                }
+            }
+        } else if (g >= g_hi) {
+            break;
+        }
         while (j < n_jobs && g >= jobs[j].group_begin + groups_of(jobs[j])) ++j;
         const Job &J = jobs[j];
         const int n_terms = J.n_terms;
         const bool aligned = TMA || J.aligned;
         const int64_t rowrel = (int64_t)(g - J.group_begin) * kRows + lane;
         const bool row_ok = rowrel < J.n_rows;
-        const int gi = g - g_lo, par = gi & 1;
+        const int par = gi & 1;
         float *red_g = red + (size_t)par * NT * kNW * 32;
         // The partial buffer of this parity was last used by group gi-2; wait
         // until that group has been combined.
@@ -1089,6 +1165,8 @@ struct MapKey {
         return base == o.base && rows == o.rows && rb == o.rb && chunk == o.chunk && dev == o.dev;
     }
 };
+std::atomic<uint32_t> g_sched_seq{0};
+
 constexpr int kMapCache = 64;
 std::mutex g_map_mu;
 MapKey g_map_key[kMapCache];
@@ -1360,10 +1438,17 @@ static rf_status launch_merged(const LaunchDesc &d, int nb, int64_t RB, cudaStre
             for (int m = 0; m < n_maps; ++m)
                 if (extent[m] > 0x7fffffffLL) return RF_ERR_TOO_LARGE;
         }
-        // Same number of groups (or one fewer) on every CTA.
+        // Producer mode: one group per CTA to start with, the rest drawn as
+        // CTAs finish (no tail from an uneven split of groups over SMs).
+        // Other modes: the same number of groups (or one fewer) on every CTA.
         const int max_grid = ctas_per_sm * di.sms;
         const int per_cta = (total + max_grid - 1) / max_grid;
-        const int grid = (total + per_cta - 1) / per_cta;
+        const int grid = mode == kModeTensorWS ? std::min(total, max_grid)
+                                               : (total + per_cta - 1) / per_cta;
+        const int sched_slot =
+            mode == kModeTensorWS && total > grid
+                ? (int)(g_sched_seq.fetch_add(1, std::memory_order_relaxed) % kSchedSlots)
+                : -1;
 
         auto fill = [&](auto &p) -> rf_status {
             std::memcpy(p.jobs, jobs, sizeof(Job) * nj);
@@ -1390,6 +1475,7 @@ static rf_status launch_merged(const LaunchDesc &d, int nb, int64_t RB, cudaStre
             p.xr_out = static_cast<XRec *>(d.xr_out);
             p.xr_y_base = d.xr_y_base;
             p.xr_in = static_cast<const XRec *>(d.xr_in);
+            p.sched_slot = sched_slot;
             p.max_terms = max_terms;
             p.n_maps = n_maps;
             return RF_OK;
