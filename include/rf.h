@@ -186,6 +186,19 @@ RF_API rf_status rf_ffn_swiglu_ws(int fmt, const void *gate, const void *up, con
                                   int64_t n_ff, int64_t n_embd, const float *x, float *y,
                                   float *h, void *workspace, unsigned flags, void *stream);
 
+/* Zero-copy variant of rf_gemv (hipfire PR #793, "Summary": the "pcie"
+ * execution of a spilled layer, where the GPU kernels read host-mapped
+ * weights over the link; "Design notes": the host memory is allocated mapped
+ * and the device pointer is its host-mapped alias): the kernel reads the rows
+ * straight from page-locked host memory over the link, with no arena and no
+ * copy engine.  host_W: page-locked, device-mapped host
+ * pointer to row 0 of the [out][in] matrix (16-byte aligned); x, y: device.
+ * Output is bit-identical to rf_gemv on the same bytes.
+ * Errors: as rf_gemv; RF_ERR_NOT_PINNED if host_W is not page-locked and
+ * mapped. */
+RF_API rf_status rf_gemv_host(int fmt, const void *host_W, int64_t row_start, int64_t row_end,
+                              int64_t in_dim, const float *x, float *y, void *stream);
+
 /* ------------------------------------------- host-streamed row windows */
 /* An arena is a bounded ring of device memory plus a copy stream and events
  * (neurostream, "How it works" 6: every in-flight block holds a byte

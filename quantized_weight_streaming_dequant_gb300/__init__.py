@@ -62,6 +62,7 @@ _SIGS = {
     "rf_gelu": ([_P, _P, _I64, _P], _I),
     "rf_ffn_swiglu": ([_I, _P, _P, _P, _I64, _I64, _P, _P, _P, _P], _I),
     "rf_ffn_workspace_bytes": ([_I64], _SZ),
+    "rf_gemv_host": ([_I, _P, _I64, _I64, _I64, _P, _P, _P], _I),
     "rf_ffn_swiglu_ws": ([_I, _P, _P, _P, _I64, _I64, _P, _P, _P, _P, ctypes.c_uint, _P], _I),
     "rf_arena_create": ([_SZ, ctypes.POINTER(_P)], _I),
     "rf_arena_destroy": ([_P], None),
@@ -183,6 +184,20 @@ def gelu(z, h=None, stream=None):
     _check(lib().rf_gelu(_dev_ptr(z, "z"), _dev_ptr(h, "h"), z.numel(), _stream(stream)),
            "rf_gelu")
     return h
+
+
+def gemv_host(fmt: int, host_W, row_start: int, row_end: int, in_dim: int, x, y=None,
+              stream=None):
+    """rf_gemv_host: host_W is a page-locked CPU tensor (uint8) read in place."""
+    import torch
+    if host_W.is_cuda or not host_W.is_contiguous():
+        raise ValueError("host_W must be a contiguous CPU tensor")
+    if y is None:
+        y = torch.empty(max(row_end - row_start, 0), dtype=torch.float32, device=x.device)
+    _check(lib().rf_gemv_host(fmt, host_W.data_ptr(), row_start, row_end, in_dim,
+                              _dev_ptr(x, "x"), _dev_ptr(y, "y") if y.numel() else 1,
+                              _stream(stream)), "rf_gemv_host")
+    return y
 
 
 def ffn_workspace(n_ff: int, device):

@@ -176,6 +176,42 @@ rf_status rf_gemv_ex(int fmt, const void *W, int64_t row_start, int64_t row_end,
     return launch_rowwin(d, static_cast<cudaStream_t>(stream));
 }
 
+rf_status rf_gemv_host(int fmt, const void *host_W, int64_t row_start, int64_t row_end,
+                       int64_t in_dim, const float *x, float *y, void *stream)
+{
+    if (!fmt_ok(fmt)) return RF_ERR_UNSUPPORTED_FMT;
+    if (!host_W || !x || !y || in_dim <= 0 || in_dim % 32 != 0 || row_start < 0 ||
+        row_end < row_start)
+        return RF_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(host_W) & 15u) != 0) return RF_ERR_MISALIGNED;
+    if (row_end - row_start > 0x7fffffffLL) return RF_ERR_TOO_LARGE;
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, host_W) != cudaSuccess) {
+        cudaGetLastError();
+        return RF_ERR_NOT_PINNED;
+    }
+    if (attr.type != cudaMemoryTypeHost || !attr.devicePointer) return RF_ERR_NOT_PINNED;
+    if (row_end == row_start) return RF_OK;
+    if (const rf_status c = check_in_dim(fmt, in_dim, 1)) return c;
+    Job J;
+    std::memset(&J, 0, sizeof(J));
+    J.term[0] = Term{static_cast<const uint8_t *>(attr.devicePointer), 0, -1, 0, 0};
+    J.y = y;
+    J.row0 = row_start;
+    J.n_rows = (int32_t)(row_end - row_start);
+    J.n_terms = 1;
+    J.combine = kCombineSum;
+    LaunchDesc d;
+    d.fmt = fmt;
+    d.in_dim = in_dim;
+    d.jobs = &J;
+    d.n_jobs = 1;
+    d.x[0] = x;
+    d.n_x = 1;
+    d.host_weights = true;
+    return launch_rowwin(d, static_cast<cudaStream_t>(stream));
+}
+
 rf_status rf_gemv_batch(int fmt, int64_t in_dim, int n_windows, const rf_window *windows,
                         void *stream)
 {

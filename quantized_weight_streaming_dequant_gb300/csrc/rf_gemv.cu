@@ -644,20 +644,22 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
                 tma_2d_g2s(dst, &p.maps[T.tmap], x, (int)y, bar);
             }
         } else {
-            // Each lane copies its own row's chunk, rounded out to 16-byte
-            // boundaries, with 16-byte cp.async (issued by all lanes at once).
-            const int64_t rowrel = (int64_t)(cu.g - J.group_begin) * kRows + lane;
-            if (rowrel < J.n_rows) {
-                const uint8_t *W = term_matrix(eidx, J, cu.t, RB);
-                const int kb = kb_lo + cu.c * KC;
-                const int kn = min(KC, kb_hi - kb);
-                const uintptr_t s = reinterpret_cast<uintptr_t>(W + (J.row0 + rowrel) * RB +
-                                                                (int64_t)kb * F::BS);
+            // Row r's chunk, rounded out to 16-byte boundaries, goes to row r's
+            // slot; the warp copies one row at a time, lane i taking its i-th
+            // 16 bytes, so each copy instruction reads contiguous bytes (which
+            // matters most over the host link).
+            const int64_t rel0 = (int64_t)(cu.g - J.group_begin) * kRows;
+            const int nr = (int)min((int64_t)kRows, (int64_t)J.n_rows - rel0);
+            const uint8_t *W = term_matrix(eidx, J, cu.t, RB);
+            const int kb = kb_lo + cu.c * KC;
+            const int kn = min(KC, kb_hi - kb);
+            uintptr_t s = reinterpret_cast<uintptr_t>(W + (J.row0 + rel0) * RB + (int64_t)kb * F::BS);
+            for (int r = 0; r < nr; ++r, s += (uintptr_t)RB) {
                 const uintptr_t a = s & ~(uintptr_t)15;
-                const uintptr_t e = (s + (uintptr_t)kn * F::BS + 15) & ~(uintptr_t)15;
-                uint8_t *d = dst + (size_t)lane * SLOT;
-                for (uintptr_t q = a; q < e; q += 16, d += 16)
-                    cp_async16(d, reinterpret_cast<const void *>(q));
+                const int n16 = (int)(((s + (uintptr_t)kn * F::BS + 15) & ~(uintptr_t)15) - a) >> 4;
+                for (int i = lane; i < n16; i += 32)
+                    cp_async16(dst + (size_t)r * SLOT + 16 * i,
+                               reinterpret_cast<const void *>(a + 16 * (uintptr_t)i));
             }
             cp_async_arrive(bar);
         }
@@ -1358,12 +1360,14 @@ static rf_status launch_merged(const LaunchDesc &d, int nb, int64_t RB, cudaStre
     for (int i = 0; i < d.n_jobs; ++i) max_terms = std::max(max_terms, (int)d.jobs[i].n_terms);
     const int nj_max = std::min(d.n_jobs, kMaxJobs);
     const size_t per2 = (size_t)di.max_smem_sm / 2 - (size_t)di.reserved_per_block;
-    int mode = aligned ? kModeTensorWS : kModePerLane;
+    // Mapped host memory is read with per-lane 16-byte copies (plain loads of
+    // the link), never with tensor or bulk copies.
+    int mode = aligned && !d.host_weights ? kModeTensorWS : kModePerLane;
     const bool ws = mode == kModeTensorWS;
     int ctas_per_sm = 0, stages = 0;
     // Misaligned rows: stage whole 32-row groups when two of them fit (two
     // CTAs per SM if possible).
-    if (!aligned) {
+    if (!aligned && !d.host_weights) {
         const int fs = flat_slot(RB);
         for (int st = 3; st >= 2 && !ctas_per_sm; --st)
             if (smem_bytes(d.n_x, nb, st, fs, max_terms, nj_max, true) <= per2) {
@@ -1383,7 +1387,7 @@ static rf_status launch_merged(const LaunchDesc &d, int nb, int64_t RB, cudaStre
     }
     // Otherwise per-warp rings: prefer two CTAs per SM (16 warps) with at
     // least 2 stages; else one CTA with up to 4 stages.
-    const bool two_ok = !aligned || d.fmt == RF_Q4_0;   // register budget (min_ctas)
+    const bool two_ok = mode == kModePerLane || d.fmt == RF_Q4_0;   // register budget (min_ctas)
     for (int st = 4; st >= 2 && !ctas_per_sm && two_ok; --st)
         if (smem_bytes(d.n_x, nb, st, geo.slot, max_terms, nj_max, false, ws) <= per2) {
             ctas_per_sm = 2;
@@ -1416,7 +1420,7 @@ static rf_status launch_merged(const LaunchDesc &d, int nb, int64_t RB, cudaStre
         const void *bases[kMaxMaps];
         int64_t extent[kMaxMaps];
         int n_maps = 0;
-        if (aligned) {
+        if (mode == kModeTensorWS) {
             for (int i = 0; i < nj; ++i) {
                 Job &J = jobs[i];
                 for (int t = 0; t < J.n_terms; ++t) {

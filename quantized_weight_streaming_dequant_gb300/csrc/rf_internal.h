@@ -56,6 +56,7 @@ struct LaunchDesc {
     const int32_t *expert_idx = nullptr;   // device, for expert_slot terms
     bool pdl = false;                      // programmatic dependent launch
     bool any_expert = false;               // some term resolves an expert on device
+    bool host_weights = false;             // weights are mapped page-locked host memory
     // Routing computed inside the launch (instead of expert_idx): top route_k
     // of route_n logits (ties to the lower index) and a softmax over the k
     // selected; CTA 0 also stores them to route_idx_out / route_w_out.  The

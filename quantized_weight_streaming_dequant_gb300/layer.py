@@ -9,7 +9,8 @@ DenseLayer -- one dense decode layer held resident in HBM: the Q, K and V
   down).  The attention core between QKV and O is not part of this library; its
   output is an input here.
 StreamedFFN -- a dense FFN whose weights stay in page-locked host memory: up
-  (host-streamed), GELU, down (host-streamed), all through one arena.
+  (host-streamed), GELU, down (host-streamed), all through one arena; or the
+  same FFN read in place over the host link (zero copy).
 """
 from __future__ import annotations
 
@@ -68,6 +69,13 @@ class StreamedFFN:
         rf.gelu(u, h, stream=stream)
         arena.stream_linear(self.fmt, self.host_down, self.d_ff, 0, self.d_model, block_rows,
                             depth, h, y, stream=stream)
+
+    def step_zero_copy(self, x, u, h, y, stream=None):
+        """The same FFN with both projections read in place from page-locked
+        host memory (rf_gemv_host): no arena, no copy engine."""
+        rf.gemv_host(self.fmt, self.host_up, 0, self.d_ff, self.d_model, x, u, stream=stream)
+        rf.gelu(u, h, stream=stream)
+        rf.gemv_host(self.fmt, self.host_down, 0, self.d_model, self.d_ff, h, y, stream=stream)
 
     def weight_bytes(self) -> int:
         return (self.d_ff * rf.row_bytes(self.fmt, self.d_model) +

@@ -333,3 +333,24 @@ def test_moe_ffn_small(rf, fmt):
 
 def test_moe_ffn_whole_expert_windows(rf):
     moe_check(rf, syn.MXFP4, 12, 2880, 2880, 2, 0, seed=50)
+
+
+# ------------------------------------------------------------- zero copy
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_gemv_host_zero_copy_bit_identical_to_resident(rf, fmt):
+    """The zero-copy arm reads page-locked host memory in place and gives the
+    resident GEMV's bits, for aligned and misaligned rows and a ragged window."""
+    import torch
+    for rows, in_dim, (r0, r1) in ((700, 4096, (3, 700)), (300, 2880, (0, 299))):
+        W = syn.quant_matrix(fmt, rows, in_dim, seed=61)
+        x = dev_tensor(syn.normal_f32(in_dim, 62))
+        resident = rf.gemv(fmt, dev_tensor(W), r0, r1, in_dim, x).cpu().numpy()
+        host = torch.from_numpy(W).pin_memory()
+        y = rf.gemv_host(fmt, host, r0, r1, in_dim, x).cpu().numpy()
+        assert np.array_equal(bits(y), bits(resident)), (rows, in_dim)
+        ref = oracle.gemv(fmt, W, r0, r1, in_dim, syn.normal_f32(in_dim, 62))
+        assert_gemv_close(y, ref, gemv_tol(fmt, W, r0, r1, in_dim, syn.normal_f32(in_dim, 62)))
+    with pytest.raises(rf.RFError) as e:   # pageable memory is refused
+        rf.gemv_host(fmt, torch.from_numpy(W), 0, 8, in_dim, x)
+    assert e.value.code == 3
