@@ -290,6 +290,20 @@ RF_API rf_status rf_moe_ffn(int fmt, const float *router_logits, int n_expert, i
                             int64_t n_embd, int64_t block_rows, const float *x, float *y,
                             void *workspace, void *stream);
 
+/* rf_moe_ffn over stacked expert tensors held in page-locked, device-mapped
+ * host memory (neurostream, "How it works" 2: only the routed experts' rows
+ * are read; hipfire PR #793, "Summary": GPU kernels reading host-mapped
+ * weights over the link).  The kernels read the selected experts' rows in
+ * place over the host link; routing never leaves the device, so no host
+ * round trip decides what to read.  Results are bit-identical to rf_moe_ffn
+ * on the same bytes.  Errors: as rf_moe_ffn; RF_ERR_NOT_PINNED if a tensor is
+ * not page-locked and mapped. */
+RF_API rf_status rf_moe_ffn_host(int fmt, const float *router_logits, int n_expert, int top_k,
+                                 const void *host_gate, const void *host_up,
+                                 const void *host_down, int64_t n_ff, int64_t n_embd,
+                                 int64_t block_rows, const float *x, float *y, void *workspace,
+                                 void *stream);
+
 /* rf_moe_ffn without a workspace argument, for callers that cannot allocate
  * device memory: for example an engine that plans all of its device memory
  * once at start-up and forbids allocations afterwards, or a decode loop that

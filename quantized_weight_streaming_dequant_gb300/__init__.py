@@ -74,6 +74,7 @@ _SIGS = {
     "rf_moe_workspace_bytes": ([_I, _I64, _I64, _I64], _SZ),
     "rf_moe_ffn": ([_I, _P, _I, _I, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P], _I),
     "rf_moe_ffn_noalloc": ([_I, _P, _I, _I, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P], _I),
+    "rf_moe_ffn_host": ([_I, _P, _I, _I, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P], _I),
     "rf_device_status": ([], _I),
 }
 
@@ -314,6 +315,24 @@ def moe_ffn_noalloc(fmt: int, logits, top_k: int, gate, up, down, n_ff: int, n_e
                                     _dev_ptr(x, "x"), _dev_ptr(y, "y"), _stream(stream)),
            "rf_moe_ffn_noalloc")
     return y
+
+
+def moe_ffn_host(fmt: int, logits, top_k: int, gate, up, down, n_ff: int, n_embd: int,
+                 block_rows: int, x, y=None, workspace=None, stream=None):
+    """rf_moe_ffn_host: gate/up/down are page-locked CPU tensors read in place."""
+    import torch
+    for t in (gate, up, down):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("expert tensors must be contiguous CPU tensors")
+    y = torch.empty(n_embd, dtype=torch.float32, device=x.device) if y is None else y
+    if workspace is None:
+        workspace = moe_workspace(top_k, n_ff, n_embd, block_rows, x.device)
+    _check(lib().rf_moe_ffn_host(fmt, _dev_ptr(logits, "logits"), logits.numel(), top_k,
+                                 gate.data_ptr(), up.data_ptr(), down.data_ptr(), n_ff, n_embd,
+                                 block_rows, _dev_ptr(x, "x"), _dev_ptr(y, "y"),
+                                 _dev_ptr(workspace, "workspace"), _stream(stream)),
+           "rf_moe_ffn_host")
+    return y, workspace
 
 
 def moe_workspace_views(workspace, top_k: int, n_ff: int):

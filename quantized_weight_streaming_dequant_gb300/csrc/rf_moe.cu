@@ -158,10 +158,16 @@ size_t rf_moe_workspace_bytes(int top_k, int64_t n_ff, int64_t n_embd, int64_t b
            xrec_bytes((int64_t)top_k * n_ff);
 }
 
-rf_status rf_moe_ffn(int fmt, const float *router_logits, int n_expert, int top_k,
-                     const void *gate, const void *up, const void *down, int64_t n_ff,
-                     int64_t n_embd, int64_t block_rows, const float *x, float *y,
-                     void *workspace, void *stream)
+}  // extern "C"
+
+namespace {
+
+// The routed FFN; host = the stacked tensors are page-locked, device-mapped
+// host memory read in place (gate, up, down are their device aliases).
+rf_status moe_ffn(int fmt, const float *router_logits, int n_expert, int top_k, const void *gate,
+                  const void *up, const void *down, int64_t n_ff, int64_t n_embd,
+                  int64_t block_rows, const float *x, float *y, void *workspace, void *stream,
+                  bool host)
 {
     if (!fmt_ok(fmt)) return RF_ERR_UNSUPPORTED_FMT;
     if (!router_logits || !gate || !up || !down || !x || !y || !workspace)
@@ -229,6 +235,7 @@ rf_status rf_moe_ffn(int fmt, const float *router_logits, int n_expert, int top_
     d1.x[0] = x;
     d1.n_x = 1;
     d1.any_expert = true;
+    d1.host_weights = host;
     d1.pdl = false;
     d1.route_logits = router_logits;
     d1.route_n = n_expert;
@@ -264,12 +271,49 @@ rf_status rf_moe_ffn(int fmt, const float *router_logits, int n_expert, int top_
     for (int k = 0; k < top_k; ++k) d2.x[k] = h + (int64_t)k * n_ff;
     d2.n_x = top_k;
     d2.any_expert = true;
+    d2.host_weights = host;
     d2.pdl = true;
     d2.route_logits = router_logits;
     d2.route_n = n_expert;
     d2.route_k = top_k;
     d2.xr_in = hdig;
     return launch_rowwin(d2, s);
+}
+
+// Device alias of a page-locked, mapped host pointer, or nullptr.
+const void *mapped_alias(const void *host)
+{
+    cudaPointerAttributes attr;
+    if (!host || cudaPointerGetAttributes(&attr, host) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return attr.type == cudaMemoryTypeHost ? attr.devicePointer : nullptr;
+}
+
+}  // namespace
+
+extern "C" {
+
+rf_status rf_moe_ffn(int fmt, const float *router_logits, int n_expert, int top_k,
+                     const void *gate, const void *up, const void *down, int64_t n_ff,
+                     int64_t n_embd, int64_t block_rows, const float *x, float *y,
+                     void *workspace, void *stream)
+{
+    return moe_ffn(fmt, router_logits, n_expert, top_k, gate, up, down, n_ff, n_embd, block_rows,
+                   x, y, workspace, stream, false);
+}
+
+rf_status rf_moe_ffn_host(int fmt, const float *router_logits, int n_expert, int top_k,
+                          const void *host_gate, const void *host_up, const void *host_down,
+                          int64_t n_ff, int64_t n_embd, int64_t block_rows, const float *x,
+                          float *y, void *workspace, void *stream)
+{
+    if (!host_gate || !host_up || !host_down) return RF_ERR_INVALID_ARG;
+    const void *g = mapped_alias(host_gate), *u = mapped_alias(host_up), *d = mapped_alias(host_down);
+    if (!g || !u || !d) return RF_ERR_NOT_PINNED;
+    return moe_ffn(fmt, router_logits, n_expert, top_k, g, u, d, n_ff, n_embd, block_rows, x, y,
+                   workspace, stream, true);
 }
 
 rf_status rf_moe_ffn_noalloc(int fmt, const float *router_logits, int n_expert, int top_k,

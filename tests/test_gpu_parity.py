@@ -354,3 +354,24 @@ def test_gemv_host_zero_copy_bit_identical_to_resident(rf, fmt):
     with pytest.raises(rf.RFError) as e:   # pageable memory is refused
         rf.gemv_host(fmt, torch.from_numpy(W), 0, 8, in_dim, x)
     assert e.value.code == 3
+
+
+def test_moe_ffn_host_zero_copy_bit_identical(rf):
+    """The routed FFN over expert tensors in page-locked host memory, read in
+    place, gives rf_moe_ffn's bits (two tokens with different routing)."""
+    import torch
+    fmt, E, n_ff, n_embd, top_k, br = syn.MXFP4, 16, 320, 2880, 4, 64
+    G = syn.stacked_experts(fmt, E, n_ff, n_embd, 80)
+    U = syn.stacked_experts(fmt, E, n_ff, n_embd, 81)
+    D = syn.stacked_experts(fmt, E, n_embd, n_ff, 82)
+    x = dev_tensor(syn.normal_f32(n_embd, 83))
+    hg, hu, hd = (torch.from_numpy(a).pin_memory() for a in (G, U, D))
+    Gd, Ud, Dd = dev_tensor(G), dev_tensor(U), dev_tensor(D)
+    for seed in (84, 85):
+        logits = dev_tensor(syn.router_logits(E, seed))
+        y_dev, _ = rf.moe_ffn(fmt, logits, top_k, Gd, Ud, Dd, n_ff, n_embd, br, x)
+        y_host, _ = rf.moe_ffn_host(fmt, logits, top_k, hg, hu, hd, n_ff, n_embd, br, x)
+        assert np.array_equal(bits(y_host.cpu().numpy()), bits(y_dev.cpu().numpy())), seed
+    with pytest.raises(rf.RFError) as e:   # pageable memory is refused
+        rf.moe_ffn_host(fmt, logits, top_k, torch.from_numpy(G), hu, hd, n_ff, n_embd, br, x)
+    assert e.value.code == 3
