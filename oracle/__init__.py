@@ -7,9 +7,10 @@ the CUDA path.  The arithmetic lives in ``rf_oracle.c`` (plain C, fp64); this
 module only builds it with gcc and marshals numpy arrays through ctypes.
 
 Every function cites the page passage it follows in ``rf_oracle.c``.  Parity
-status: the MXFP4 block layout and the GELU activation of the host-streamed
-FFN are "parity unpinned" by the pages themselves (no page prints them); they
-are pinned in tests by the OCP MX format definition and the GELU identities.
+status: the MXFP4 block layout, the GELU activation of the host-streamed FFN
+and Q4_K's scale packing and quant order are "parity unpinned" by the pages
+themselves (no page prints them); they are pinned in tests by the OCP MX
+format definition, the GELU identities and a reduction of Q4_K to Q4_0.
 """
 from __future__ import annotations
 
@@ -25,8 +26,8 @@ _SRC = _HERE / "rf_oracle.c"
 _LIBDIR = _HERE / "_lib"
 _SO = _LIBDIR / "liboracle.so"
 
-Q4_0, Q8_0, MXFP4 = 2, 8, 39
-FORMATS = {"Q4_0": Q4_0, "Q8_0": Q8_0, "MXFP4": MXFP4}
+Q4_0, Q8_0, MXFP4, Q4_K = 2, 8, 39, 12
+FORMATS = {"Q4_0": Q4_0, "Q8_0": Q8_0, "MXFP4": MXFP4, "Q4_K": Q4_K}
 
 
 def build(force: bool = False) -> Path:
@@ -70,6 +71,9 @@ def _declare(L: ctypes.CDLL) -> None:
     L.orc_block_bytes.restype = _I64
     L.orc_row_bytes.argtypes = [_I, _I64]
     L.orc_row_bytes.restype = _I64
+    L.orc_block_elems.argtypes = [_I]
+    L.orc_block_elems.restype = _I64
+    L.orc_q4k_scale_min.argtypes = [_P, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]
     L.orc_dequant_block.argtypes = [_I, _P, _P]
     L.orc_dequantize.argtypes = [_I, _P, _I64, _P]
     L.orc_gemv.argtypes = [_I, _P, _I64, _I64, _I64, _P, _P]
@@ -122,12 +126,24 @@ def row_bytes(fmt: int, in_dim: int) -> int:
     return lib().orc_row_bytes(fmt, in_dim)
 
 
+def block_elems(fmt: int) -> int:
+    return lib().orc_block_elems(fmt)
+
+
+def q4k_scale_min(scale_bytes, j: int):
+    """(scale, min) of Q4_K sub-block j from its 12 scale bytes."""
+    b = np.ascontiguousarray(scale_bytes, dtype=np.uint8)
+    sc, m = _I(0), _I(0)
+    lib().orc_q4k_scale_min(_ptr(b), j, ctypes.byref(sc), ctypes.byref(m))
+    return sc.value, m.value
+
+
 def dequantize(fmt: int, W, n_blocks: int | None = None) -> np.ndarray:
     """Dequantize consecutive blocks to float32 (exact values)."""
     Wb = _u8(W)
     if n_blocks is None:
         n_blocks = Wb.size // block_bytes(fmt)
-    out = np.empty(32 * n_blocks, dtype=np.float32)
+    out = np.empty(block_elems(fmt) * n_blocks, dtype=np.float32)
     _check(lib().orc_dequantize(fmt, _ptr(Wb), n_blocks, _ptr(out)), "dequantize")
     return out
 

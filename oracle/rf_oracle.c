@@ -24,6 +24,11 @@
  *            6. arena) and the two-phase FFN paragraph.
  *   [NS-BUGS] neurostream, "Bugs worth knowing about": the pipeline holds
  *            depth+1 blocks, not depth.
+ *   [RF-M5K] RAMforge, "Milestone 5 - Native Quantized Tensor Support": Q4_K =
+ *            256 elements in 144 B: 2 B half d, 2 B half dmin, 12 B of scales
+ *            (8 scales and 8 mins packed as 6-bit values), 128 B of 4-bit
+ *            quants; an element is d*sc*q - dmin*m with (sc, m) its
+ *            sub-block's scale and min.
  *
  * Readings where the pages are silent (each is also listed in the design doc):
  *   - fp16 scale: IEEE-754 binary16, little endian, first two bytes.
@@ -34,6 +39,18 @@
  *     same nibble order as Q4_0.  E2M1 code bits are s e1 e0 m with exponent
  *     bias 1.  PARITY UNPINNED by the pages (only the 17-byte size is pinned,
  *     through the 4.41 MB figure); pinned here by the OCP MX definition.
+ *   - Q4_K (the pages name the unpacking get_scale_min_k4 but print neither
+ *     it nor the quant order; reading: the GGML layout).  Sub-block j (32
+ *     elements, j = 0..7) has a 6-bit scale and a 6-bit min.  For j < 4 they
+ *     are the low 6 bits of scale bytes j and j+4; for j >= 4 the scale is
+ *     the low nibble of byte j+4 plus the top two bits of byte j-4 (as bits
+ *     4-5), and the min is the high nibble of byte j+4 plus the top two bits
+ *     of byte j (as bits 4-5).  Quant byte 32*i + l holds element 64*i + l in
+ *     its low nibble (sub-block 2i) and element 64*i + 32 + l in its high
+ *     nibble (sub-block 2i+1).  The value d*sc*q - dmin*m is computed
+ *     exactly (fp64) and rounded once to float.  PARITY UNPINNED by the pages
+ *     for the scale packing and the quant order (the 144-byte size and the
+ *     formula are theirs); pinned here by a reduction to Q4_0.
  *   - GEMV accumulation: fp64, index order.
  *   - Router: the k largest fp32 logits, ties to the lower expert index,
  *     weights = softmax over the k selected logits.
@@ -52,6 +69,7 @@
 #define ORC_Q4_0 2
 #define ORC_Q8_0 8
 #define ORC_MXFP4 39
+#define ORC_Q4_K 12
 
 #define ORC_OK 0
 #define ORC_EINVAL 1
@@ -107,24 +125,61 @@ int64_t orc_block_bytes(int fmt)
     case ORC_Q8_0: return 34;   /* [RF-M5] */
     case ORC_Q4_0: return 18;   /* [RF-M5] */
     case ORC_MXFP4: return 17;  /* 1 scale byte + 16 code bytes */
+    case ORC_Q4_K: return 144;  /* [RF-M5K] */
     default: return 0;
     }
 }
 
+/* Elements per block: 32, or 256 for Q4_K's super-block. */
+int64_t orc_block_elems(int fmt)
+{
+    return fmt == ORC_Q4_K ? 256 : (orc_block_bytes(fmt) ? 32 : 0);
+}
+
 int64_t orc_row_bytes(int fmt, int64_t in_dim)
 {
-    int64_t bb = orc_block_bytes(fmt);
-    if (bb == 0 || in_dim <= 0 || in_dim % 32 != 0)
+    int64_t bb = orc_block_bytes(fmt), be = orc_block_elems(fmt);
+    if (bb == 0 || in_dim <= 0 || in_dim % be != 0)
         return 0;
-    return (in_dim / 32) * bb;
+    return (in_dim / be) * bb;
+}
+
+/* Q4_K sub-block j's 6-bit scale and min from the 12 scale bytes. */
+void orc_q4k_scale_min(const uint8_t *sc12, int j, int *sc, int *m)
+{
+    if (j < 4) {
+        *sc = sc12[j] & 63;
+        *m = sc12[j + 4] & 63;
+    } else {
+        *sc = (sc12[j + 4] & 15) | ((sc12[j - 4] >> 6) << 4);
+        *m = (sc12[j + 4] >> 4) | ((sc12[j] >> 6) << 4);
+    }
 }
 
 /* ------------------------------------------------------- block dequantize */
 
-/* Decode one 32-element block into out[0..31] (float; every value exact). */
+/* Decode one block into out[0..elems-1] (float; Q8_0, Q4_0 and MXFP4 values
+ * are exact, Q4_K values are the exact value rounded once). */
 int orc_dequant_block(int fmt, const uint8_t *blk, float *out)
 {
     int j;
+    if (fmt == ORC_Q4_K) {
+        double d = orc_fp16_to_double((uint16_t)(blk[0] | (blk[1] << 8)));
+        double dmin = orc_fp16_to_double((uint16_t)(blk[2] | (blk[3] << 8)));
+        const uint8_t *sc12 = blk + 4, *qs = blk + 16;
+        int i, l;
+        for (i = 0; i < 4; i++) {
+            int sc0, m0, sc1, m1;
+            orc_q4k_scale_min(sc12, 2 * i, &sc0, &m0);
+            orc_q4k_scale_min(sc12, 2 * i + 1, &sc1, &m1);
+            for (l = 0; l < 32; l++) {
+                int lo = qs[32 * i + l] & 15, hi = qs[32 * i + l] >> 4;
+                out[64 * i + l] = (float)(d * sc0 * lo - dmin * m0);
+                out[64 * i + 32 + l] = (float)(d * sc1 * hi - dmin * m1);
+            }
+        }
+        return ORC_OK;
+    }
     if (fmt == ORC_Q8_0) {
         double d = orc_fp16_to_double((uint16_t)(blk[0] | (blk[1] << 8)));
         for (j = 0; j < 32; j++) {
@@ -159,11 +214,11 @@ int orc_dequant_block(int fmt, const uint8_t *blk, float *out)
 /* Dequantize n_blocks consecutive blocks into out[32*n_blocks]. */
 int orc_dequantize(int fmt, const uint8_t *W, int64_t n_blocks, float *out)
 {
-    int64_t bb = orc_block_bytes(fmt), b;
+    int64_t bb = orc_block_bytes(fmt), be = orc_block_elems(fmt), b;
     if (bb == 0 || n_blocks < 0)
         return ORC_EINVAL;
     for (b = 0; b < n_blocks; b++) {
-        int rc = orc_dequant_block(fmt, W + b * bb, out + 32 * b);
+        int rc = orc_dequant_block(fmt, W + b * bb, out + be * b);
         if (rc)
             return rc;
     }
@@ -179,8 +234,9 @@ int orc_gemv_d(int fmt, const uint8_t *W, int64_t row_start, int64_t row_end,
                int64_t in_dim, const double *x, double *y)
 {
     int64_t rb = orc_row_bytes(fmt, in_dim), bb = orc_block_bytes(fmt);
-    int64_t r, b, nb = in_dim / 32;
-    float w[32];
+    int64_t be = orc_block_elems(fmt);
+    int64_t r, b, nb = be ? in_dim / be : 0;
+    float w[256];
     int j;
     if (rb == 0 || row_start < 0 || row_end < row_start)
         return ORC_EINVAL;
@@ -189,8 +245,8 @@ int orc_gemv_d(int fmt, const uint8_t *W, int64_t row_start, int64_t row_end,
         double acc = 0.0;
         for (b = 0; b < nb; b++) {
             orc_dequant_block(fmt, row + b * bb, w);
-            for (j = 0; j < 32; j++)
-                acc += (double)w[j] * x[b * 32 + j];
+            for (j = 0; j < be; j++)
+                acc += (double)w[j] * x[b * be + j];
         }
         y[r - row_start] = acc;
     }
@@ -218,8 +274,9 @@ int orc_row_norms(int fmt, const uint8_t *W, int64_t row_start, int64_t row_end,
                   int64_t in_dim, double *norms)
 {
     int64_t rb = orc_row_bytes(fmt, in_dim), bb = orc_block_bytes(fmt);
-    int64_t r, b, nb = in_dim / 32;
-    float w[32];
+    int64_t be = orc_block_elems(fmt);
+    int64_t r, b, nb = be ? in_dim / be : 0;
+    float w[256];
     int j;
     if (rb == 0 || row_start < 0 || row_end < row_start)
         return ORC_EINVAL;
@@ -227,7 +284,7 @@ int orc_row_norms(int fmt, const uint8_t *W, int64_t row_start, int64_t row_end,
         double s = 0.0;
         for (b = 0; b < nb; b++) {
             orc_dequant_block(fmt, W + r * rb + b * bb, w);
-            for (j = 0; j < 32; j++)
+            for (j = 0; j < be; j++)
                 s += (double)w[j] * (double)w[j];
         }
         norms[r - row_start] = sqrt(s);

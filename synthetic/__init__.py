@@ -11,6 +11,10 @@ Distributions (the workloads' statement):
            independent uniform nibbles); d = fp16(U[1e-3, 2e-2]).
   MXFP4  : each 4-bit E2M1 code uniform over its 16 values (random bytes);
            scale exponent byte E = 127 + U{-8, ..., -2}.
+  Q4_K   : 256-element super-blocks of 144 B; quant bytes and the 12 packed
+           scale bytes uniform random (so every 6-bit scale and min is
+           uniform over [0, 63]); d = fp16(U[1e-4, 1e-3]), dmin =
+           fp16(U[1e-4, 1e-3]).
   x      : fp32 N(0, 1); router logits fp32 N(0, 1).
 
 Reproducibility: rows are generated in fixed chunks of ``CHUNK_ROWS`` rows,
@@ -23,12 +27,13 @@ from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
-Q4_0, Q8_0, MXFP4 = 2, 8, 39
-FMT_IDS = {"Q4_0": Q4_0, "Q8_0": Q8_0, "MXFP4": MXFP4}
+Q4_0, Q8_0, MXFP4, Q4_K = 2, 8, 39, 12
+FMT_IDS = {"Q4_0": Q4_0, "Q8_0": Q8_0, "MXFP4": MXFP4, "Q4_K": Q4_K}
 FMT_NAMES = {v: k for k, v in FMT_IDS.items()}
 # (block bytes, quant bytes after the scale, scale bytes)
-_LAYOUT = {Q8_0: (34, 32, 2), Q4_0: (18, 16, 2), MXFP4: (17, 16, 1)}
-DEFAULT_SCALE = {Q8_0: (1e-3, 1e-2), Q4_0: (1e-3, 2e-2), MXFP4: (-8, -2)}
+_LAYOUT = {Q8_0: (34, 32, 2), Q4_0: (18, 16, 2), MXFP4: (17, 16, 1), Q4_K: (144, 140, 4)}
+DEFAULT_SCALE = {Q8_0: (1e-3, 1e-2), Q4_0: (1e-3, 2e-2), MXFP4: (-8, -2), Q4_K: (1e-4, 1e-3)}
+_ELEMS = {Q8_0: 32, Q4_0: 32, MXFP4: 32, Q4_K: 256}
 CHUNK_ROWS = 1024
 
 
@@ -36,15 +41,19 @@ def block_bytes(fmt: int) -> int:
     return _LAYOUT[fmt][0]
 
 
+def block_elems(fmt: int) -> int:
+    return _ELEMS[fmt]
+
+
 def row_bytes(fmt: int, in_dim: int) -> int:
-    assert in_dim % 32 == 0
-    return in_dim // 32 * _LAYOUT[fmt][0]
+    assert in_dim % _ELEMS[fmt] == 0
+    return in_dim // _ELEMS[fmt] * _LAYOUT[fmt][0]
 
 
 def _fill_rows(fmt: int, out: np.ndarray, in_dim: int, seed: int, chunk: int,
                scale_range) -> None:
     rows = out.shape[0]
-    nb = in_dim // 32
+    nb = in_dim // _ELEMS[fmt]
     bb, nq, ns = _LAYOUT[fmt]
     rng = np.random.default_rng([seed, chunk])
     blk = out.reshape(rows, nb, bb)
@@ -54,7 +63,10 @@ def _fill_rows(fmt: int, out: np.ndarray, in_dim: int, seed: int, chunk: int,
     else:
         blk[:, :, ns:] = rng.integers(0, 256, size=(rows, nb, nq), dtype=np.uint8)
     lo, hi = scale_range
-    if fmt == MXFP4:
+    if fmt == Q4_K:   # d and dmin, both fp16
+        dd = rng.uniform(lo, hi, size=(rows, nb, 2)).astype("<f2")
+        blk[:, :, 0:4] = dd.view(np.uint8).reshape(rows, nb, 4)
+    elif fmt == MXFP4:
         blk[:, :, 0] = (127 + rng.integers(lo, hi + 1, size=(rows, nb))).astype(np.uint8)
     else:
         d = rng.uniform(lo, hi, size=(rows, nb)).astype("<f2")
