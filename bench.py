@@ -171,9 +171,9 @@ def h2d_probe(torch, device, nbytes: int, reps: int = 5):
 
 # ------------------------------------------------------------- workloads
 
-def build_dense_layers(torch, rf, device, copies: int, seed: int):
+def build_dense_layers(torch, rf, device, copies: int, seed: int, fmt: int = syn.Q4_0):
     from quantized_weight_streaming_dequant_gb300.layer import DenseLayer
-    fmt, d, f = syn.Q4_0, syn.C2["d_model"], syn.C2["d_ff"]
+    d, f = syn.C2["d_model"], syn.C2["d_ff"]
     layers = []
     for c in range(copies):
         s = seed * 1000 + 10 * c
@@ -332,6 +332,41 @@ def dense_e2e(torch, layers, out, device, stream, steps):
     return {"value": wbytes * steps / dt / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": int(h_in.numel() * 4), "d2h_bytes_per_step": int(h_out.numel() * 4),
             "ms_per_step": dt / steps * 1e3, "steps": steps}
+
+
+def run_dense_format(torch, rf, device, fmt: int, steps: int = 2000):
+    """The 4096/11008 dense layer with its weights in another format (same
+    layer copies > L2, same four launches, one CUDA graph per round of
+    copies): whole-step weight GB/s."""
+    layers = build_dense_layers(torch, rf, device, syn.C2["copies"], syn.C2["seed"], fmt)
+    d = syn.C2["d_model"]
+    x, attn, x_ffn = (torch.from_numpy(syn.normal_f32(d, s)).to(device) for s in (101, 102, 103))
+    out = dense_outputs(torch, device)
+    stream = torch.cuda.Stream(device)
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        for L in layers:
+            L.step(x, attn, x_ffn, out, stream=stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for L in layers:
+            L.step(x, attn, x_ffn, out, stream=stream)
+    rounds = max(1, steps // len(layers))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g.replay()
+        e0.record(stream)
+        for _ in range(rounds):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / (rounds * len(layers))
+    wbytes = layers[0].weight_bytes()
+    del g, layers
+    return {"ms_per_step": ms, "weight_bytes_per_step": wbytes,
+            "value": wbytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "steps": rounds * syn.C2["copies"]}
 
 
 def run_streamed_gemv(torch, rf, device, depth: int, reps: int = 50):
@@ -754,6 +789,9 @@ def main():
             extra["streamed_gemv_q8_0_512x2048"] = [run_streamed_gemv(torch, rf, device, dp)
                                                     for dp in (4, 1)]
             extra["moe_mxfp4"] = run_moe(torch, rf, device)
+            q4k = run_dense_format(torch, rf, device, syn.Q4_K)
+            q4k["frac_of_hbm_peak"] = q4k["value"] / peak
+            extra["dense_layer_q4_k"] = q4k
             if args.ffn_layers > 0:
                 extra["streamed_ffn_q8_0"] = run_streamed_ffn(torch, rf, device, args.ffn_layers)
             if args.sweep:

@@ -53,15 +53,27 @@ extern "C" {
  *   RF_MXFP4: 17 B per 32 weights: E8M0 scale byte E, then 16 bytes of FP4
  *             E2M1 codes in the Q4_0 nibble order; w = e2m1(c) * 2^(E-127)
  *             (named by neurostream, "The idea"; layout per the OCP MX
- *             definition, which the pages do not print). */
+ *             definition, which the pages do not print).
+ *   RF_Q4_K : 144 B per 256 weights (a super-block of eight 32-weight
+ *             sub-blocks): fp16 d, fp16 dmin, 12 bytes of 6-bit scales and
+ *             mins, 128 bytes of 4-bit q; w = d*sc*q - dmin*m with (sc, m)
+ *             the sub-block's scale and min (RAMforge, "Milestone 5 - Native
+ *             Quantized Tensor Support").  The unpacking and quant order
+ *             follow the GGML layout (the page names but does not print
+ *             them): sub-block j < 4 takes the low 6 bits of scale bytes j
+ *             and j+4; j >= 4 the low/high nibble of byte j+4 plus the top
+ *             two bits of bytes j-4 / j; quant byte 32i+l holds weight 64i+l
+ *             (low nibble) and 64i+32+l (high nibble).  in_dim must be a
+ *             multiple of 256 for this format. */
 #define RF_Q4_0 2
 #define RF_Q8_0 8
 #define RF_MXFP4 39
+#define RF_Q4_K 12
 
 typedef enum rf_status {
     RF_OK = 0,
-    RF_ERR_INVALID_ARG = 1,     /* null pointer, bad size, in_dim % 32 != 0, ... */
-    RF_ERR_UNSUPPORTED_FMT = 2, /* fmt is not one of RF_Q4_0, RF_Q8_0, RF_MXFP4 */
+    RF_ERR_INVALID_ARG = 1,     /* null pointer, bad size, in_dim not a whole number of blocks, ... */
+    RF_ERR_UNSUPPORTED_FMT = 2, /* fmt is not one of RF_Q4_0, RF_Q8_0, RF_MXFP4, RF_Q4_K */
     RF_ERR_NOT_PINNED = 3,      /* a host weight pointer is not page-locked */
     RF_ERR_ARENA_TOO_SMALL = 4, /* depth+1 one-row blocks do not fit the arena */
     RF_ERR_CUDA = 5,            /* a CUDA runtime call or launch failed */
@@ -77,11 +89,12 @@ RF_API const char *rf_status_str(int status);
 /* Library ABI version (major*10000 + minor*100 + patch). */
 RF_API int rf_version(void);
 
-/* Bytes per 32-weight block: 18 (Q4_0), 34 (Q8_0), 17 (MXFP4); 0 if unknown. */
+/* Bytes per block: 18 (Q4_0), 34 (Q8_0), 17 (MXFP4) per 32 weights, 144 (Q4_K)
+ * per 256 weights; 0 if unknown. */
 RF_API size_t rf_block_bytes(int fmt);
 
-/* Bytes per row of in_dim weights (in_dim/32 blocks); 0 if fmt is unknown or
- * in_dim is not a positive multiple of 32. */
+/* Bytes per row of in_dim weights (in_dim/32 blocks, in_dim/256 for Q4_K); 0
+ * if fmt is unknown or in_dim is not a positive whole number of blocks. */
 RF_API size_t rf_row_bytes(int fmt, int64_t in_dim);
 
 /* Largest in_dim the GEMV kernels accept for `fmt` with `n_x` distinct
@@ -91,8 +104,9 @@ RF_API int64_t rf_max_in_dim(int fmt, int n_x);
 
 /* ------------------------------------------------------------- dequantize */
 /* Decode n_blocks consecutive blocks at W (device) into out (device,
- * 32*n_blocks floats).  Every dequantized value is exactly representable in
- * fp32, so the result is bit-exact.  Errors: RF_ERR_UNSUPPORTED_FMT,
+ * 32*n_blocks floats, 256*n_blocks for Q4_K).  Q8_0, Q4_0 and MXFP4 values
+ * are exactly representable in fp32; a Q4_K value is the exact d*sc*q -
+ * dmin*m rounded once; so the result is bit-exact against that definition.  Errors: RF_ERR_UNSUPPORTED_FMT,
  * RF_ERR_INVALID_ARG (null pointer, n_blocks < 0). */
 RF_API rf_status rf_dequantize(int fmt, const void *W, int64_t n_blocks, float *out,
                                void *stream);

@@ -16,9 +16,10 @@ PKG = Path(__file__).resolve().parent
 SO = PKG / "_lib" / "librf.so"
 HEADER = PKG.parent / "include" / "rf.h"
 
-Q4_0, Q8_0, MXFP4 = 2, 8, 39
-FORMATS = {"Q4_0": Q4_0, "Q8_0": Q8_0, "MXFP4": MXFP4}
-BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, MXFP4: 17}
+Q4_0, Q8_0, Q4_K, MXFP4 = 2, 8, 12, 39
+FORMATS = {"Q4_0": Q4_0, "Q8_0": Q8_0, "Q4_K": Q4_K, "MXFP4": MXFP4}
+BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q4_K: 144, MXFP4: 17}
+BLOCK_ELEMS = {Q4_0: 32, Q8_0: 32, Q4_K: 256, MXFP4: 32}
 
 OK = 0
 CHAIN = 1   # RF_CHAIN launch flag
@@ -145,7 +146,7 @@ def dequantize(fmt: int, W, n_blocks: int | None = None, out=None, stream=None):
     if n_blocks is None:
         n_blocks = W.numel() // BLOCK_BYTES[fmt]
     if out is None:
-        out = torch.empty(32 * n_blocks, dtype=torch.float32, device=W.device)
+        out = torch.empty(BLOCK_ELEMS[fmt] * n_blocks, dtype=torch.float32, device=W.device)
     _check(lib().rf_dequantize(fmt, _dev_ptr(W, "W"), n_blocks, _dev_ptr(out, "out"),
                                _stream(stream)), "rf_dequantize")
     return out

@@ -37,6 +37,33 @@ __global__ void dequant_kernel(const uint8_t *__restrict__ W, int64_t n_blocks,
 {
     const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= n_blocks) return;
+    if constexpr (FMT == RF_Q4_K) {
+        // d*sc and dmin*m are exact in fp32 (11-bit times 6-bit significands)
+        // and so is d*sc*q, so one fused multiply-add rounds the exact value
+        // once.
+        float *o = out + 256 * b;
+        const uint8_t *p = W + 144 * b;
+        const float d = __half2float(__ushort_as_half((unsigned short)(p[0] | (p[1] << 8))));
+        const float dmin = __half2float(__ushort_as_half((unsigned short)(p[2] | (p[3] << 8))));
+        const uint8_t *sc = p + 4, *qs = p + 16;
+        for (int j = 0; j < 8; ++j) {
+            int s, m;
+            if (j < 4) {
+                s = sc[j] & 63;
+                m = sc[j + 4] & 63;
+            } else {
+                s = (sc[j + 4] & 15) | ((sc[j - 4] >> 6) << 4);
+                m = (sc[j + 4] >> 4) | ((sc[j] >> 6) << 4);
+            }
+            const float ds = d * (float)s, dm = dmin * (float)m;
+            const uint8_t *q = qs + 32 * (j >> 1);
+            for (int l = 0; l < 32; ++l) {
+                const int v = (j & 1) ? (q[l] >> 4) : (q[l] & 15);
+                o[32 * j + l] = fmaf(ds, (float)v, -dm);
+            }
+        }
+        return;
+    }
     float *o = out + 32 * b;
     if constexpr (FMT == RF_Q8_0) {
         const uint8_t *p = W + 34 * b;
@@ -116,8 +143,8 @@ size_t rf_block_bytes(int fmt) { return block_bytes_of(fmt); }
 
 size_t rf_row_bytes(int fmt, int64_t in_dim)
 {
-    if (!fmt_ok(fmt) || in_dim <= 0 || in_dim % 32 != 0) return 0;
-    return (size_t)(in_dim / 32) * block_bytes_of(fmt);
+    if (!fmt_ok(fmt) || in_dim <= 0 || in_dim % block_elems_of(fmt) != 0) return 0;
+    return (size_t)(in_dim / block_elems_of(fmt)) * block_bytes_of(fmt);
 }
 
 int64_t rf_max_in_dim(int fmt, int n_x) { return max_in_dim(fmt, n_x); }
@@ -135,6 +162,7 @@ rf_status rf_dequantize(int fmt, const void *W, int64_t n_blocks, float *out, vo
     switch (fmt) {
     case RF_Q4_0: dequant_kernel<RF_Q4_0><<<(unsigned)grid, threads, 0, s>>>(w, n_blocks, out); break;
     case RF_Q8_0: dequant_kernel<RF_Q8_0><<<(unsigned)grid, threads, 0, s>>>(w, n_blocks, out); break;
+    case RF_Q4_K: dequant_kernel<RF_Q4_K><<<(unsigned)grid, threads, 0, s>>>(w, n_blocks, out); break;
     default: dequant_kernel<RF_MXFP4><<<(unsigned)grid, threads, 0, s>>>(w, n_blocks, out); break;
     }
     return last_cuda_error();
@@ -150,7 +178,7 @@ rf_status rf_gemv_ex(int fmt, const void *W, int64_t row_start, int64_t row_end,
                      const float *x, float *y, unsigned flags, void *stream)
 {
     if (!fmt_ok(fmt)) return RF_ERR_UNSUPPORTED_FMT;
-    if (!W || !x || !y || in_dim <= 0 || in_dim % 32 != 0 || row_start < 0 ||
+    if (!W || !x || !y || in_dim <= 0 || in_dim % block_elems_of(fmt) != 0 || row_start < 0 ||
         row_end < row_start)
         return RF_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(W) & 15u) != 0) return RF_ERR_MISALIGNED;
@@ -180,7 +208,7 @@ rf_status rf_gemv_host(int fmt, const void *host_W, int64_t row_start, int64_t r
                        int64_t in_dim, const float *x, float *y, void *stream)
 {
     if (!fmt_ok(fmt)) return RF_ERR_UNSUPPORTED_FMT;
-    if (!host_W || !x || !y || in_dim <= 0 || in_dim % 32 != 0 || row_start < 0 ||
+    if (!host_W || !x || !y || in_dim <= 0 || in_dim % block_elems_of(fmt) != 0 || row_start < 0 ||
         row_end < row_start)
         return RF_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(host_W) & 15u) != 0) return RF_ERR_MISALIGNED;
@@ -222,7 +250,7 @@ rf_status rf_gemv_batch_ex(int fmt, int64_t in_dim, int n_windows, const rf_wind
                            unsigned flags, void *stream)
 {
     if (!fmt_ok(fmt)) return RF_ERR_UNSUPPORTED_FMT;
-    if (in_dim <= 0 || in_dim % 32 != 0 || n_windows < 0 || (n_windows > 0 && !windows))
+    if (in_dim <= 0 || in_dim % block_elems_of(fmt) != 0 || n_windows < 0 || (n_windows > 0 && !windows))
         return RF_ERR_INVALID_ARG;
     if (n_windows > kMaxJobs) return RF_ERR_TOO_LARGE;
     Job jobs[kMaxJobs];
@@ -302,7 +330,7 @@ rf_status rf_ffn_swiglu_ws(int fmt, const void *gate, const void *up, const void
 {
     if (!fmt_ok(fmt)) return RF_ERR_UNSUPPORTED_FMT;
     if (!gate || !up || !down || !x || !y || !h || n_ff <= 0 || n_embd <= 0 ||
-        n_ff % 32 != 0 || n_embd % 32 != 0)
+        n_ff % block_elems_of(fmt) != 0 || n_embd % block_elems_of(fmt) != 0)
         return RF_ERR_INVALID_ARG;
     if (n_ff > 0x7fffffffLL || n_embd > 0x7fffffffLL) return RF_ERR_TOO_LARGE;
     for (const void *p : {gate, up, down})

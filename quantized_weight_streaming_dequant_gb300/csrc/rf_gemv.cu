@@ -81,15 +81,21 @@ template <int FMT>
 struct FmtT;
 template <>
 struct FmtT<RF_Q4_0> {
-    static constexpr int BS = 18, HDR = 2, QW = 4, G = 8;
+    static constexpr int BS = 18, HDR = 2, QW = 4, G = 8, RPB = 1;
 };
 template <>
 struct FmtT<RF_Q8_0> {
-    static constexpr int BS = 34, HDR = 2, QW = 8, G = 8;
+    static constexpr int BS = 34, HDR = 2, QW = 8, G = 8, RPB = 1;
 };
 template <>
 struct FmtT<RF_MXFP4> {
-    static constexpr int BS = 17, HDR = 1, QW = 4, G = 16;
+    static constexpr int BS = 17, HDR = 1, QW = 4, G = 16, RPB = 1;
+};
+// Q4_K: a "block" is the 256-weight super-block (144 B, always 16-byte
+// aligned); it has RPB = 8 activation digit records, one per sub-block.
+template <>
+struct FmtT<RF_Q4_K> {
+    static constexpr int BS = 144, HDR = 4, QW = 4, G = 1, RPB = 8;
 };
 
 constexpr int kMaxMaps = 16;   // distinct weight tensors per launch (tensor-map path)
@@ -211,7 +217,7 @@ __device__ __forceinline__ void xrec_build(const float (&v)[8], int part, bool a
         out->p1[2 * part + hh] = prmt(prmt(a, b, 0x0051u), prmt(c, d, 0x0051u), 0x5410u);
     }
     if (part == 0) {
-        out->corr = FMT == RF_Q4_0 ? -8 * sum : 0;
+        out->corr = FMT == RF_Q4_0 ? -8 * sum : (FMT == RF_Q4_K ? sum : 0);
         out->scale = exp2i(-s);
         out->pad[0] = out->pad[1] = 0;
     }
@@ -248,11 +254,53 @@ __device__ __forceinline__ void xrec_emit(float v, XRec *out)
     if (lane < 16)
         o32[lane] = word;
     else if (lane == 16)
-        o32[16] = (uint32_t)(FMT == RF_Q4_0 ? -8 * sum : 0);
+        o32[16] = (uint32_t)(FMT == RF_Q4_0 ? -8 * sum : (FMT == RF_Q4_K ? sum : 0));
     else if (lane == 17)
         o32[17] = __float_as_uint(exp2i(-s));
     else if (lane < 20)
         o32[lane] = 0;
+}
+
+// One Q4_K super-block held as 36 words (d and dmin, 3 words of packed 6-bit
+// scales and mins, 32 quant words) against its 8 digit records: sub-block j
+// contributes (d*sc_j * sum_l q_l X_l - dmin*m_j * sum_l X_l) * 2^-s_j.  Quant
+// word 4+8i+k holds weights 4k..4k+3 of sub-block 2i in its low nibbles and of
+// sub-block 2i+1 in its high nibbles; the high ones stay in place (16*q) and
+// the exact sums are divided by 16.
+__device__ __forceinline__ float q4k_superblock(const uint32_t *v, const XRec *xr, float acc)
+{
+    const float d = __half2float(__ushort_as_half((unsigned short)(v[0] & 0xffffu)));
+    const float dmin = __half2float(__ushort_as_half((unsigned short)(v[0] >> 16)));
+    const uint32_t s0 = v[1], s1 = v[2], s2 = v[3];
+    const uint32_t scA = s0 & 0x3f3f3f3fu;                                       // sc 0..3
+    const uint32_t mA = s1 & 0x3f3f3f3fu;                                        // m 0..3
+    const uint32_t scB = (s2 & 0x0f0f0f0fu) | ((s0 >> 2) & 0x30303030u);         // sc 4..7
+    const uint32_t mB = ((s2 >> 4) & 0x0f0f0f0fu) | ((s1 >> 2) & 0x30303030u);  // m 4..7
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int sh = 8 * (j & 3);
+        const float sc = (float)(((j < 4 ? scA : scB) >> sh) & 0xffu);
+        const float m = (float)(((j < 4 ? mA : mB) >> sh) & 0xffu);
+        const XRec &x = xr[j];
+        const uint4 *P0 = reinterpret_cast<const uint4 *>(x.p0);
+        const uint4 *P1 = reinterpret_cast<const uint4 *>(x.p1);
+        const uint4 a0 = P0[0], a1 = P0[1], b0 = P1[0], b1 = P1[1];
+        const uint32_t p0[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const uint32_t p1[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        const uint32_t *q = v + 4 + 8 * (j >> 1);
+        const uint32_t mask = (j & 1) ? 0xf0f0f0f0u : 0x0f0f0f0fu;
+        int t0 = 0, t1 = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t n = q[k] & mask;
+            t0 = dp4a_uu(n, p0[k], t0);
+            t1 = dp4a_us(n, p1[k], t1);
+        }
+        const int idot = (j & 1) ? (t1 >> 4) * 256 + (t0 >> 4) : t1 * 256 + t0;
+        const float t = fmaf((float)idot, d * sc, -((float)x.corr * (dmin * m)));
+        acc = fmaf(t, x.scale, acc);
+    }
+    return acc;
 }
 
 // Integer dot of one block's quant words with the block's digit planes;
@@ -362,6 +410,7 @@ template <int FMT>
 __device__ __forceinline__ float compute_group(const GroupRegs<FMT> &r, const XRec *xr, float acc)
 {
     using F = FmtT<FMT>;
+    if constexpr (FMT == RF_Q4_K) return q4k_superblock(r.v, xr, acc);
 #pragma unroll
     for (int b = 0; b < F::G; ++b) {
         const int o = b * F::BS;
@@ -384,7 +433,7 @@ __device__ __forceinline__ float chunk_aligned(const uint8_t *src, int kn, const
     for (int g0 = 0; g0 < kn; g0 += F::G) {
         GroupRegs<FMT> r;
         load_group<FMT>(src + g0 * F::BS, r);
-        acc = compute_group<FMT>(r, xr + g0, acc);
+        acc = compute_group<FMT>(r, xr + g0 * F::RPB, acc);
     }
     return acc;
 }
@@ -395,6 +444,20 @@ __device__ __forceinline__ float chunk_generic(const uint8_t *slot, int phi, int
                                                const XRec *xr, float acc)
 {
     using F = FmtT<FMT>;
+    if constexpr (FMT == RF_Q4_K) {
+        // Super-blocks at any 4-byte phase (rows of 144-byte blocks are always
+        // 16-byte aligned, so this only serves unaligned slots).
+        for (int b = 0; b < kn; ++b) {
+            const int o = phi + b * F::BS;
+            const uint32_t *wp = reinterpret_cast<const uint32_t *>(slot + (o & ~3));
+            const int sh = 8 * (o & 3);
+            uint32_t w[36];
+#pragma unroll
+            for (int k = 0; k < 36; ++k) w[k] = __funnelshift_r(wp[k], wp[k + 1], sh);
+            acc = q4k_superblock(w, xr + b * F::RPB, acc);
+        }
+        return acc;
+    }
     for (int b = 0; b < kn; ++b) {
         const int o = phi + b * F::BS;
         uint32_t hdr;
@@ -534,7 +597,9 @@ constexpr int threads_of() { return MODE == kModeTensorWS ? kThreads + 32 : kThr
 template <int FMT, int MODE>
 constexpr int min_ctas()
 {
-    return ((MODE == kModeTensor || MODE == kModeTensorWS) && FMT != RF_Q4_0) ? 1 : 2;
+    return ((MODE == kModeTensor || MODE == kModeTensorWS) && FMT != RF_Q4_0 && FMT != RF_Q4_K)
+               ? 1
+               : 2;
 }
 
 template <int FMT, int MODE, class KP>
@@ -556,7 +621,8 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     XRec *xrec = reinterpret_cast<XRec *>(smem);
-    size_t off = ((size_t)p.n_x * nb * sizeof(XRec) + 127) & ~(size_t)127;
+    const int nrx = nb * F::RPB;   // digit records per activation vector
+    size_t off = ((size_t)p.n_x * nrx * sizeof(XRec) + 127) & ~(size_t)127;
     uint8_t *slots = smem + off;
     off += FLAT ? (size_t)ST * SLOT : (size_t)kNW * ST * kRows * SLOT;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + off);   // slot filled
@@ -789,7 +855,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
     // passes' loads go out before the remaining weight copies, so they do not
     // queue behind them.
     if (p.xr_in) {
-        const int n16 = p.n_x * nb * (int)(sizeof(XRec) / 16);
+        const int n16 = p.n_x * nrx * (int)(sizeof(XRec) / 16);
         const uint4 *src = reinterpret_cast<const uint4 *>(p.xr_in);
         uint4 *dst = reinterpret_cast<uint4 *>(xrec);
         constexpr int kU = 8;
@@ -811,13 +877,13 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
         }
     } else {
         constexpr int kXPre = 8;
-        const int n_rec = p.n_x * nb;
+        const int n_rec = p.n_x * nrx;
         const int passes = (4 * n_rec + kThreads - 1) / kThreads;
         auto pass_src = [&](int ps, bool &active, int &rec) -> const float * {
             const int idx = ps * kThreads + (int)threadIdx.x;
             active = idx < 4 * n_rec;
             rec = active ? idx >> 2 : 0;
-            const int sl = rec / nb, b = rec - sl * nb;
+            const int sl = rec / nrx, b = rec - sl * nrx;
             return p.x[sl] + 32 * (int64_t)b;
         };
         float v[kXPre][8];
@@ -904,7 +970,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
             if (!FLAT && !aligned && row_ok)
                 row_src = reinterpret_cast<uintptr_t>(term_matrix(eidx, J, t, RB) +
                                                       (J.row0 + rowrel) * RB);
-            const XRec *xr_row = xrec + (size_t)J.term[t].xslot * nb;
+            const XRec *xr_row = xrec + (size_t)J.term[t].xslot * nrx;
             if constexpr (FLAT) {
                 // Every warp waits for the stage (so none runs ahead of the
                 // ring), reads its K part of its lane's row, then counts
@@ -918,7 +984,8 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
                                          (src & 15) + (uintptr_t)((int64_t)lane * RB) +
                                          (uintptr_t)kb_lo * F::BS;
                     acc = chunk_generic<FMT>(reinterpret_cast<const uint8_t *>(rp & ~(uintptr_t)3),
-                                             (int)(rp & 3), kb_hi - kb_lo, xr_row + kb_lo, acc);
+                                             (int)(rp & 3), kb_hi - kb_lo,
+                                             xr_row + kb_lo * F::RPB, acc);
                 }
                 if (++cs == ST) {
                     cs = 0;
@@ -953,14 +1020,14 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
                         issue(ic);
                         cursor_advance(jobs, n_jobs, ic, n_chunks, g_hi);
                     }
-                    acc = compute_group<FMT>(r, xr_row + kb, acc);
+                    acc = compute_group<FMT>(r, xr_row + kb * F::RPB, acc);
                     continue;
                 }
                 if (aligned) {
-                    acc = chunk_aligned<FMT>(slot, kn, xr_row + kb, acc);
+                    acc = chunk_aligned<FMT>(slot, kn, xr_row + kb * F::RPB, acc);
                 } else {
                     const int phi = (int)((row_src + (uintptr_t)kb * F::BS) & 15);
-                    acc = chunk_generic<FMT>(slot, phi, kn, xr_row + kb, acc);
+                    acc = chunk_generic<FMT>(slot, phi, kn, xr_row + kb * F::RPB, acc);
                 }
                 __syncwarp();
                 if (ic.valid) {
@@ -1036,7 +1103,7 @@ const DevInfo &dev_info(int dev)
     return g_dev[dev & 63];
 }
 
-int fmt_group(int fmt) { return fmt == RF_MXFP4 ? 16 : 8; }
+int fmt_group(int fmt) { return fmt == RF_MXFP4 ? 16 : (fmt == RF_Q4_K ? 1 : 8); }
 
 // Chunk of `kc` blocks and its slot size.  Aligned rows copy exactly KC*BS
 // bytes; others need up to 15 bytes of rounding on either side.  Slots are an
@@ -1054,7 +1121,7 @@ ChunkGeom chunk_geom(int fmt, bool aligned)
         const int kc = fmt_group(fmt);
         return {kc, kc * bs};
     }
-    const int kc = 8;
+    const int kc = fmt == RF_Q4_K ? 1 : 8;
     int n = (kc * bs + 30 + 15) / 16 * 16;
     if ((n / 16) % 2 == 0) n += 16;
     return {kc, n};
@@ -1064,10 +1131,11 @@ ChunkGeom chunk_geom(int fmt, bool aligned)
 // rounding at both ends and a word of overrun for the last row's decode.
 int flat_slot(int64_t row_bytes) { return (int)((kRows * row_bytes + 32 + 127) / 128 * 128); }
 
-size_t smem_bytes(int n_x, int nb, int stages, int slot, int max_terms, int n_jobs,
+// nrx: activation digit records per x (in_dim / 32).
+size_t smem_bytes(int n_x, int nrx, int stages, int slot, int max_terms, int n_jobs,
                   bool flat = false, bool ws = false)
 {
-    return (((size_t)n_x * nb * sizeof(XRec) + 127) & ~(size_t)127) +
+    return (((size_t)n_x * nrx * sizeof(XRec) + 127) & ~(size_t)127) +
            (flat ? (size_t)stages * slot : (size_t)kNW * stages * kRows * slot) +
            (size_t)(flat ? stages : kNW * stages * (ws ? 2 : 1)) * sizeof(uint64_t) +
            (size_t)2 * max_terms * kNW * 32 * sizeof(float) + kCntInts * sizeof(int) +
@@ -1142,6 +1210,7 @@ rf_status launch_mode(int fmt, const KP &p, int grid, size_t smem, bool pdl, cud
     switch (fmt) {
     case RF_Q4_0: return launch_fmt<RF_Q4_0, MODE>(p, grid, smem, pdl, stream, dev);
     case RF_Q8_0: return launch_fmt<RF_Q8_0, MODE>(p, grid, smem, pdl, stream, dev);
+    case RF_Q4_K: return launch_fmt<RF_Q4_K, MODE>(p, grid, smem, pdl, stream, dev);
     default: return launch_fmt<RF_MXFP4, MODE>(p, grid, smem, pdl, stream, dev);
     }
 }
@@ -1209,7 +1278,10 @@ rf_status read_and_clear_device_status()
     return static_cast<rf_status>(v);
 }
 
-bool fmt_ok(int fmt) { return fmt == RF_Q4_0 || fmt == RF_Q8_0 || fmt == RF_MXFP4; }
+bool fmt_ok(int fmt)
+{
+    return fmt == RF_Q4_0 || fmt == RF_Q8_0 || fmt == RF_MXFP4 || fmt == RF_Q4_K;
+}
 
 size_t block_bytes_of(int fmt)
 {
@@ -1217,6 +1289,7 @@ size_t block_bytes_of(int fmt)
     case RF_Q4_0: return 18;
     case RF_Q8_0: return 34;
     case RF_MXFP4: return 17;
+    case RF_Q4_K: return 144;
     default: return 0;
     }
 }
@@ -1245,7 +1318,8 @@ int64_t max_in_dim(int fmt, int n_x)
     const int slot = std::max(chunk_geom(fmt, true).slot, chunk_geom(fmt, false).slot);
     const size_t fixed = smem_bytes(n_x, 0, 1, slot, kMaxTerms, kMaxJobs);
     if (maxs <= fixed) return 0;
-    return (int64_t)((maxs - fixed) / ((size_t)n_x * sizeof(XRec))) * 32;
+    const int64_t elems = (int64_t)((maxs - fixed) / ((size_t)n_x * sizeof(XRec))) * 32;
+    return elems / block_elems_of(fmt) * block_elems_of(fmt);
 }
 
 rf_status check_in_dim(int fmt, int64_t in_dim, int n_x)
@@ -1280,7 +1354,7 @@ static rf_status launch_merged(const LaunchDesc &d, int nb, int64_t RB, cudaStre
 rf_status launch_rowwin(const LaunchDesc &d, cudaStream_t stream)
 {
     if (!fmt_ok(d.fmt)) return RF_ERR_UNSUPPORTED_FMT;
-    if (d.in_dim <= 0 || d.in_dim % 32 != 0) return RF_ERR_INVALID_ARG;
+    if (d.in_dim <= 0 || d.in_dim % block_elems_of(d.fmt) != 0) return RF_ERR_INVALID_ARG;
     if (d.n_jobs < 0 || d.n_x < 1 || d.n_x > kMaxX) return RF_ERR_INVALID_ARG;
     if (d.n_jobs > 0 && !d.jobs) return RF_ERR_INVALID_ARG;
     for (int s = 0; s < d.n_x; ++s)
@@ -1298,7 +1372,7 @@ rf_status launch_rowwin(const LaunchDesc &d, cudaStream_t stream)
     if (d.route_logits && (d.route_n < 1 || d.route_n > 1024 || d.route_k < 1 ||
                            d.route_k > kMaxTerms || d.route_k > d.route_n))
         return RF_ERR_INVALID_ARG;
-    const int64_t nb64 = d.in_dim / 32;
+    const int64_t nb64 = d.in_dim / block_elems_of(d.fmt);
     if (nb64 > (1 << 24)) return RF_ERR_TOO_LARGE;
     const int nb = (int)nb64;
     const int64_t RB = nb64 * (int64_t)block_bytes_of(d.fmt);
@@ -1344,6 +1418,7 @@ rf_status launch_rowwin(const LaunchDesc &d, cudaStream_t stream)
 
 static rf_status launch_merged(const LaunchDesc &d, int nb, int64_t RB, cudaStream_t stream)
 {
+    const int nrx = (int)(d.in_dim / 32);   // activation digit records per x
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();
@@ -1370,12 +1445,12 @@ static rf_status launch_merged(const LaunchDesc &d, int nb, int64_t RB, cudaStre
     if (!aligned && !d.host_weights) {
         const int fs = flat_slot(RB);
         for (int st = 3; st >= 2 && !ctas_per_sm; --st)
-            if (smem_bytes(d.n_x, nb, st, fs, max_terms, nj_max, true) <= per2) {
+            if (smem_bytes(d.n_x, nrx, st, fs, max_terms, nj_max, true) <= per2) {
                 ctas_per_sm = 2;
                 stages = st;
             }
         for (int st = 4; st >= 2 && !ctas_per_sm; --st)
-            if (smem_bytes(d.n_x, nb, st, fs, max_terms, nj_max, true) <=
+            if (smem_bytes(d.n_x, nrx, st, fs, max_terms, nj_max, true) <=
                 (size_t)di.max_smem_block) {
                 ctas_per_sm = 1;
                 stages = st;
@@ -1387,21 +1462,22 @@ static rf_status launch_merged(const LaunchDesc &d, int nb, int64_t RB, cudaStre
     }
     // Otherwise per-warp rings: prefer two CTAs per SM (16 warps) with at
     // least 2 stages; else one CTA with up to 4 stages.
-    const bool two_ok = mode == kModePerLane || d.fmt == RF_Q4_0;   // register budget (min_ctas)
+    const bool two_ok = mode == kModePerLane || d.fmt == RF_Q4_0 ||
+                        d.fmt == RF_Q4_K;   // register budget (min_ctas)
     for (int st = 4; st >= 2 && !ctas_per_sm && two_ok; --st)
-        if (smem_bytes(d.n_x, nb, st, geo.slot, max_terms, nj_max, false, ws) <= per2) {
+        if (smem_bytes(d.n_x, nrx, st, geo.slot, max_terms, nj_max, false, ws) <= per2) {
             ctas_per_sm = 2;
             stages = st;
         }
     for (int st = 4; st >= 1 && !ctas_per_sm; --st)
-        if (smem_bytes(d.n_x, nb, st, geo.slot, max_terms, nj_max, false, ws) <=
+        if (smem_bytes(d.n_x, nrx, st, geo.slot, max_terms, nj_max, false, ws) <=
             (size_t)di.max_smem_block) {
             ctas_per_sm = 1;
             stages = st;
         }
     if (!ctas_per_sm) return RF_ERR_TOO_LARGE;
     const size_t smem =
-        smem_bytes(d.n_x, nb, stages, geo.slot, max_terms, nj_max, mode == kModeFlat, ws);
+        smem_bytes(d.n_x, nrx, stages, geo.slot, max_terms, nj_max, mode == kModeFlat, ws);
 
     // Launch in batches of kMaxJobs windows.
     for (int base = 0; base < d.n_jobs; base += kMaxJobs) {

@@ -175,7 +175,8 @@ rf_status moe_ffn(int fmt, const float *router_logits, int n_expert, int top_k, 
     if (n_expert < 1 || n_expert > kRouterThreads || top_k < 1 || top_k > kMaxTopK ||
         top_k > n_expert)
         return RF_ERR_INVALID_ARG;
-    if (n_ff <= 0 || n_embd <= 0 || n_ff % 32 != 0 || n_embd % 32 != 0 || block_rows < 0)
+    if (n_ff <= 0 || n_embd <= 0 || n_ff % block_elems_of(fmt) != 0 ||
+        n_embd % block_elems_of(fmt) != 0 || block_rows < 0)
         return RF_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return RF_ERR_MISALIGNED;
     for (const void *p : {gate, up, down})

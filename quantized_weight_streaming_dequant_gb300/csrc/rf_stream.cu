@@ -74,10 +74,10 @@ rf_status rf_stream_plan(int fmt, int64_t in_dim, int64_t n_rows, int64_t block_
                          size_t *peak_bytes)
 {
     if (!fmt_ok(fmt)) return RF_ERR_UNSUPPORTED_FMT;
-    if (in_dim <= 0 || in_dim % 32 != 0 || n_rows < 0 || block_rows < 0 || depth < 0 ||
+    if (in_dim <= 0 || in_dim % block_elems_of(fmt) != 0 || n_rows < 0 || block_rows < 0 || depth < 0 ||
         depth > rf_arena::kMaxSlots - 1)
         return RF_ERR_INVALID_ARG;
-    const int64_t rb = (in_dim / 32) * (int64_t)block_bytes_of(fmt);
+    const int64_t rb = (in_dim / block_elems_of(fmt)) * (int64_t)block_bytes_of(fmt);
     const int64_t eff = plan_rows(rb, n_rows, block_rows, depth, arena_bytes);
     if (eff < 0) return RF_ERR_ARENA_TOO_SMALL;
     const int64_t nblk = n_rows == 0 ? 0 : (n_rows + eff - 1) / eff;
@@ -176,7 +176,7 @@ rf_status rf_stream_linear(int fmt, const void *host_W, int64_t in_dim, int64_t 
                            const float *x, float *y, void *stream)
 {
     if (!fmt_ok(fmt)) return RF_ERR_UNSUPPORTED_FMT;
-    if (!host_W || !a || !x || !y || in_dim <= 0 || in_dim % 32 != 0 || row_start < 0 ||
+    if (!host_W || !a || !x || !y || in_dim <= 0 || in_dim % block_elems_of(fmt) != 0 || row_start < 0 ||
         row_end < row_start || block_rows < 0 || depth < 0 || depth > rf_arena::kMaxSlots - 1)
         return RF_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(host_W) & 15u) != 0) return RF_ERR_MISALIGNED;
@@ -188,7 +188,7 @@ rf_status rf_stream_linear(int fmt, const void *host_W, int64_t in_dim, int64_t 
     }
     if (attr.type != cudaMemoryTypeHost) return RF_ERR_NOT_PINNED;
     const int64_t n_rows = row_end - row_start;
-    const int64_t rb = (in_dim / 32) * (int64_t)block_bytes_of(fmt);
+    const int64_t rb = (in_dim / block_elems_of(fmt)) * (int64_t)block_bytes_of(fmt);
     const int64_t eff = plan_rows(rb, std::max<int64_t>(n_rows, 1), block_rows, depth, a->bytes);
     if (eff < 0) return RF_ERR_ARENA_TOO_SMALL;
     if (n_rows == 0) return RF_OK;

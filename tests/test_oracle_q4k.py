@@ -49,7 +49,8 @@ def test_scale_unpacking_hand_table(golden_dir):
     assert n == 3
 
 
-def test_hand_block_bit_exact(golden_dir):
+def hand_block(golden_dir):
+    """The worked block of the golden file: (144 raw bytes, 256 expected floats)."""
     (head, quants, expect), = list(_lines(golden_dir, "block"))
     blk = np.zeros(144, dtype=np.uint8)
     hb = [int(h, 16) for h in head.split()]
@@ -65,6 +66,11 @@ def test_hand_block_bit_exact(golden_dir):
         for e in range(int(a), int(b or a) + 1):
             want[e] = fv
     assert None not in want
+    return blk, want
+
+
+def test_hand_block_bit_exact(golden_dir):
+    blk, want = hand_block(golden_dir)
     got = oracle.dequantize(Q4_K, blk, 1)
     assert [f32_bits(float(g)) for g in got] == [f32_bits(w) for w in want]
 
