@@ -127,22 +127,6 @@ __device__ __forceinline__ void tma_2d_g2s(void *dst, const void *tmap, int x, i
         : "memory");
 }
 
-// L2 prefetch of the box a tma_2d_g2s with the same map and coordinates
-// would copy (no shared memory, no completion to wait for).
-__device__ __forceinline__ void tma_2d_prefetch_l2(const void *tmap, int x, int y)
-{
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(tmap)),
-                 "r"(x), "r"(y)
-                 : "memory");
-}
-
-// L2 prefetch of `bytes` bytes at `src` (both multiples of 16).
-__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 // ------------------------------------------------------ programmatic launch
 // Wait until the grids this launch depends on have completed and flushed
 // (no-op when launched without a programmatic dependency).

@@ -1460,8 +1460,19 @@ static rf_status launch_merged(const LaunchDesc &d, int nb, int64_t RB, cudaStre
             geo = {1, fs};
         }
     }
-    // Otherwise per-warp rings: prefer two CTAs per SM (16 warps) with at
-    // least 2 stages; else one CTA with up to 4 stages.
+    // Otherwise per-warp rings.  Producer mode with at most four 32-row groups
+    // per SM: one CTA per SM with the deepest ring that fits (up to 6 stages;
+    // fewer, deeper CTAs stream such launches faster).  Else prefer two CTAs
+    // per SM (16 warps) with at least 2 stages; else one CTA with up to 4.
+    int64_t all_groups = 0;
+    for (int i = 0; i < d.n_jobs; ++i) all_groups += (d.jobs[i].n_rows + kRows - 1) / kRows;
+    const bool deep = mode == kModeTensorWS && all_groups <= 4 * (int64_t)di.sms;
+    for (int st = 6; st >= 2 && !ctas_per_sm && deep; --st)
+        if (smem_bytes(d.n_x, nrx, st, geo.slot, max_terms, nj_max, false, ws) <=
+            (size_t)di.max_smem_block) {
+            ctas_per_sm = 1;
+            stages = st;
+        }
     const bool two_ok = mode == kModePerLane || d.fmt == RF_Q4_0 ||
                         d.fmt == RF_Q4_K;   // register budget (min_ctas)
     for (int st = 4; st >= 2 && !ctas_per_sm && two_ok; --st)
