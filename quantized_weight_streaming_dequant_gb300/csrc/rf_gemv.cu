@@ -849,76 +849,132 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
     pdl_launch_dependents();
     pdl_wait();
 
-    // Activation digits for every x of the launch, once per CTA: copied when
-    // the launch that produced the activations also wrote their digits,
-    // otherwise built by four lanes per 32-element block.  The first kXPre
-    // passes' loads go out before the remaining weight copies, so they do not
+    // Activation digits, copied when the launch that produced the activations
+    // also wrote their digits, otherwise built by four lanes per 32-element
+    // block.  Producer mode: every consumer warp reads only the records of its
+    // own K part, so it prepares just those and starts at once (no CTA-wide
+    // barrier).  Other modes: all records once per CTA, the first kXPre
+    // passes' loads issued before the remaining weight copies so they do not
     // queue behind them.
-    if (p.xr_in) {
-        const int n16 = p.n_x * nrx * (int)(sizeof(XRec) / 16);
-        const uint4 *src = reinterpret_cast<const uint4 *>(p.xr_in);
-        uint4 *dst = reinterpret_cast<uint4 *>(xrec);
-        constexpr int kU = 8;
-        for (int base = 0; base < n16; base += kU * kThreads) {
-            uint4 t[kU];
+    if constexpr (WS) {
+        const int rlo = kb_lo * F::RPB, nrw = (kb_hi - kb_lo) * F::RPB;
+        const int total = p.n_x * nrw;   // records this warp prepares
+        if (total > 0 && p.xr_in) {
+            constexpr int kV = (int)(sizeof(XRec) / 16);
+            constexpr int kU = 8;
+            const uint4 *src = reinterpret_cast<const uint4 *>(p.xr_in);
+            uint4 *dst = reinterpret_cast<uint4 *>(xrec);
+            const int n16 = total * kV;
+            for (int base = 0; base < n16; base += kU * 32) {
+                uint4 t[kU];
+                int at[kU];
 #pragma unroll
-            for (int u = 0; u < kU; ++u) {
-                const int i = base + u * kThreads + (int)threadIdx.x;
-                if (i < n16) t[u] = src[i];
+                for (int u = 0; u < kU; ++u) {
+                    const int i = base + u * 32 + lane;
+                    at[u] = 0;
+                    if (i < n16) {
+                        const int r = i / kV, h = i - kV * r;
+                        const int sl = r / nrw, k = r - sl * nrw;
+                        at[u] = (sl * nrx + rlo + k) * kV + h;
+                        t[u] = src[at[u]];
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kU; ++u)
+                    if (base + u * 32 + lane < n16) dst[at[u]] = t[u];
             }
-            if constexpr (!WS)
+        } else if (total > 0) {
+            constexpr int kXPre = 4;
+            const int passes = (total + 7) / 8;
+            auto pass_src = [&](int ps, bool &active, int &rec) -> const float * {
+                const int r = ps * 8 + (lane >> 2);
+                active = r < total;
+                const int rr = active ? r : 0;
+                const int sl = rr / nrw, k = rr - sl * nrw;
+                rec = sl * nrx + rlo + k;
+                return p.x[sl] + 32 * (int64_t)(rlo + k);
+            };
+            for (int ps0 = 0; ps0 < passes; ps0 += kXPre) {
+                float v[kXPre][8];
+                bool act[kXPre];
+                int rec[kXPre];
+#pragma unroll
+                for (int u = 0; u < kXPre; ++u) {
+                    act[u] = false;
+                    rec[u] = 0;
+                    if (ps0 + u < passes) {
+                        const float *xb = pass_src(ps0 + u, act[u], rec[u]);
+                        xrec_load<FMT>(xb, lane & 3, act[u], v[u]);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kXPre; ++u)
+                    if (ps0 + u < passes) xrec_build<FMT>(v[u], lane & 3, act[u], &xrec[rec[u]]);
+            }
+        }
+        __syncwarp();
+    } else {
+        if (p.xr_in) {
+            const int n16 = p.n_x * nrx * (int)(sizeof(XRec) / 16);
+            const uint4 *src = reinterpret_cast<const uint4 *>(p.xr_in);
+            uint4 *dst = reinterpret_cast<uint4 *>(xrec);
+            constexpr int kU = 8;
+            for (int base = 0; base < n16; base += kU * kThreads) {
+                uint4 t[kU];
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int i = base + u * kThreads + (int)threadIdx.x;
+                    if (i < n16) t[u] = src[i];
+                }
                 if (base == 0)
                     for (int s = primed; s < ST && ic.valid; ++s) prime(s);
 #pragma unroll
-            for (int u = 0; u < kU; ++u) {
-                const int i = base + u * kThreads + (int)threadIdx.x;
-                if (i < n16) dst[i] = t[u];
+                for (int u = 0; u < kU; ++u) {
+                    const int i = base + u * kThreads + (int)threadIdx.x;
+                    if (i < n16) dst[i] = t[u];
+                }
             }
-        }
-    } else {
-        constexpr int kXPre = 8;
-        const int n_rec = p.n_x * nrx;
-        const int passes = (4 * n_rec + kThreads - 1) / kThreads;
-        auto pass_src = [&](int ps, bool &active, int &rec) -> const float * {
-            const int idx = ps * kThreads + (int)threadIdx.x;
-            active = idx < 4 * n_rec;
-            rec = active ? idx >> 2 : 0;
-            const int sl = rec / nrx, b = rec - sl * nrx;
-            return p.x[sl] + 32 * (int64_t)b;
-        };
-        float v[kXPre][8];
-        bool act[kXPre];
-        int rec[kXPre];
+        } else {
+            constexpr int kXPre = 8;
+            const int n_rec = p.n_x * nrx;
+            const int passes = (4 * n_rec + kThreads - 1) / kThreads;
+            auto pass_src = [&](int ps, bool &active, int &rec) -> const float * {
+                const int idx = ps * kThreads + (int)threadIdx.x;
+                active = idx < 4 * n_rec;
+                rec = active ? idx >> 2 : 0;
+                const int sl = rec / nrx, b = rec - sl * nrx;
+                return p.x[sl] + 32 * (int64_t)b;
+            };
+            float v[kXPre][8];
+            bool act[kXPre];
+            int rec[kXPre];
 #pragma unroll
-        for (int ps = 0; ps < kXPre; ++ps) {
-            act[ps] = false;
-            rec[ps] = 0;
-            if (ps < passes) {
-                const float *xb = pass_src(ps, act[ps], rec[ps]);
-                xrec_load<FMT>(xb, threadIdx.x & 3, act[ps], v[ps]);
-            } else {
+            for (int ps = 0; ps < kXPre; ++ps) {
+                act[ps] = false;
+                rec[ps] = 0;
+                if (ps < passes) {
+                    const float *xb = pass_src(ps, act[ps], rec[ps]);
+                    xrec_load<FMT>(xb, threadIdx.x & 3, act[ps], v[ps]);
+                } else {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) v[ps][i] = 0.f;
+                    for (int i = 0; i < 8; ++i) v[ps][i] = 0.f;
+                }
             }
-        }
-        if constexpr (!WS)
             for (int s = primed; s < ST && ic.valid; ++s) prime(s);
 #pragma unroll
-        for (int ps = 0; ps < kXPre; ++ps)
-            if (ps < passes) xrec_build<FMT>(v[ps], threadIdx.x & 3, act[ps], &xrec[rec[ps]]);
-        for (int ps = kXPre; ps < passes; ++ps) {
-            bool a = false;
-            int rc = 0;
-            const float *xb = pass_src(ps, a, rc);
-            float w[8];
-            xrec_load<FMT>(xb, threadIdx.x & 3, a, w);
-            xrec_build<FMT>(w, threadIdx.x & 3, a, &xrec[rc]);
+            for (int ps = 0; ps < kXPre; ++ps)
+                if (ps < passes) xrec_build<FMT>(v[ps], threadIdx.x & 3, act[ps], &xrec[rec[ps]]);
+            for (int ps = kXPre; ps < passes; ++ps) {
+                bool a = false;
+                int rc = 0;
+                const float *xb = pass_src(ps, a, rc);
+                float w[8];
+                xrec_load<FMT>(xb, threadIdx.x & 3, a, w);
+                xrec_build<FMT>(w, threadIdx.x & 3, a, &xrec[rc]);
+            }
         }
-    }
-    if constexpr (WS)
-        asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");   // consumer warps only
-    else
         __syncthreads();
+    }
 
     int cs = 0;          // stage of the next chunk to consume
     uint32_t cph = 0;    // its mbarrier phase parity
