@@ -318,6 +318,79 @@ RF_API rf_status rf_moe_ffn_host(int fmt, const float *router_logits, int n_expe
                                  int64_t block_rows, const float *x, float *y, void *workspace,
                                  void *stream);
 
+/* --------------------------------------------- host-streamed MoE experts */
+/* Expert cache: device memory for `slots` whole experts (each expert's n_ff
+ * gate rows, n_ff up rows and n_embd down rows, raw block bytes) of one fmt
+ * and shape, with a host-side directory keyed by (host gate tensor, expert
+ * index) and least-recently-used replacement (neurostream, "How it works" 1
+ * and 3: the slab cache of expert windows; windows it holds are not read
+ * again).  Owns its device memory and events; used by one host thread at a
+ * time.  Errors: RF_ERR_INVALID_ARG for a bad shape or slots < 1,
+ * RF_ERR_UNSUPPORTED_FMT, RF_ERR_OOM. */
+typedef struct rf_expert_cache rf_expert_cache;
+RF_API rf_status rf_expert_cache_create(int fmt, int64_t n_ff, int64_t n_embd, int slots,
+                                        rf_expert_cache **out);
+/* Waits for the cache's outstanding copies and readers, then frees it.  NULL
+ * is a no-op. */
+RF_API void rf_expert_cache_destroy(rf_expert_cache *cache);
+
+typedef struct rf_expert_cache_stats {
+    uint64_t lookups;          /* selected experts looked up */
+    uint64_t hits;             /* ... found in the cache (nothing read from the host) */
+    uint64_t fills;            /* ... streamed into a cache slot */
+    uint64_t bypasses;         /* ... streamed through the arena (no free slot) */
+    uint64_t evictions;        /* fills that replaced another expert */
+    uint64_t bytes_streamed;   /* host->device expert bytes enqueued */
+    uint64_t bytes_cached;     /* expert bytes read from the cache instead */
+    int32_t slots, used;       /* capacity and occupied slots */
+} rf_expert_cache_stats;
+RF_API rf_status rf_expert_cache_stats_get(const rf_expert_cache *cache,
+                                           rf_expert_cache_stats *out);
+
+/* Routed SwiGLU FFN with the stacked expert tensors in page-locked host
+ * memory, read through one layer-wide prefetch plan (neurostream, "How it
+ * works" 3: because routing has named every expert the layer touches, one
+ * plan covers all active experts x gate/up/down in the order they are
+ * consumed, chopped into blocks; the prefetcher keeps `depth` blocks in
+ * flight and refills as each retires, so a block finishing in gate/up
+ * immediately pulls in one of down; windows the cache holds are skipped;
+ * "What the numbers taught us": a per-projection pipeline drains at every
+ * projection, the shared plan does not).
+ *
+ * Steps: the router kernel writes the top_k experts and weights to the
+ * workspace; their ids are copied to the host (the call blocks until the
+ * routing result and everything before it on `stream` is done; it is not
+ * capturable in a CUDA graph); the host then enqueues, without blocking:
+ *   gate/up -- one launch for the cached experts; for every other expert,
+ *              per block of block_rows rows its gate and up rows (copied
+ *              into a cache slot, or through the arena when no slot is
+ *              free) and a launch with the SwiGLU epilogue;
+ *   down    -- per block of block_rows output rows, the rows of every
+ *              selected expert (from the cache or copied) in one launch that
+ *              forms sum_k w_k * down_k . h_k in selection order.
+ * All copies go through the arena's copy stream in that order; a slot is
+ * reused only after the launch reading it.  Outputs are bit-identical to
+ * rf_moe_ffn on the same bytes.
+ *
+ * host_gate, host_up: (n_expert, n_ff, n_embd); host_down: (n_expert,
+ * n_embd, n_ff); page-locked, 16-byte aligned.  block_rows: a multiple of 32
+ * (0 = whole windows), shrunk to a multiple of 32 until depth+1 blocks of
+ * the longer rows fit the arena.  depth: 1..64 with depth+1 >= max(2,
+ * top_k) (a down launch holds top_k blocks at once).  cache: NULL (every
+ * expert streams through the arena) or a cache of the same fmt and shape.
+ * workspace: rf_moe_workspace_bytes(top_k, n_ff, n_embd, block_rows) bytes
+ * of device memory, 256-byte aligned; it receives the routing result and h as
+ * rf_moe_ffn's does.
+ * Errors: as rf_moe_ffn; RF_ERR_NOT_PINNED for pageable tensors;
+ * RF_ERR_ARENA_TOO_SMALL if 32-row blocks do not fit; RF_ERR_INVALID_ARG if
+ * `stream` is capturing or the cache's shape differs. */
+RF_API rf_status rf_moe_ffn_streamed(int fmt, const float *router_logits, int n_expert,
+                                     int top_k, const void *host_gate, const void *host_up,
+                                     const void *host_down, int64_t n_ff, int64_t n_embd,
+                                     int64_t block_rows, int depth, rf_arena *arena,
+                                     rf_expert_cache *cache, const float *x, float *y,
+                                     void *workspace, void *stream);
+
 /* rf_moe_ffn without a workspace argument, for callers that cannot allocate
  * device memory: for example an engine that plans all of its device memory
  * once at start-up and forbids allocations afterwards, or a decode loop that

@@ -46,6 +46,14 @@ class StreamStats(ctypes.Structure):
                 ("slots", ctypes.c_int32), ("last_block_rows", ctypes.c_int32)]
 
 
+class ExpertCacheStats(ctypes.Structure):
+    _fields_ = [("lookups", ctypes.c_uint64), ("hits", ctypes.c_uint64),
+                ("fills", ctypes.c_uint64), ("bypasses", ctypes.c_uint64),
+                ("evictions", ctypes.c_uint64), ("bytes_streamed", ctypes.c_uint64),
+                ("bytes_cached", ctypes.c_uint64), ("slots", ctypes.c_int32),
+                ("used", ctypes.c_int32)]
+
+
 _P, _I64, _I, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
 _SIGS = {
     "rf_status_str": ([_I], ctypes.c_char_p),
@@ -76,6 +84,11 @@ _SIGS = {
     "rf_moe_ffn": ([_I, _P, _I, _I, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P], _I),
     "rf_moe_ffn_noalloc": ([_I, _P, _I, _I, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P], _I),
     "rf_moe_ffn_host": ([_I, _P, _I, _I, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P], _I),
+    "rf_expert_cache_create": ([_I, _I64, _I64, _I, ctypes.POINTER(_P)], _I),
+    "rf_expert_cache_destroy": ([_P], None),
+    "rf_expert_cache_stats_get": ([_P, ctypes.POINTER(ExpertCacheStats)], _I),
+    "rf_moe_ffn_streamed": ([_I, _P, _I, _I, _P, _P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _P, _P,
+                             _P], _I),
     "rf_device_status": ([], _I),
 }
 
@@ -271,6 +284,55 @@ class Arena:
         s = StreamStats()
         _check(lib().rf_stream_stats_get(self.handle, ctypes.byref(s)), "rf_stream_stats_get")
         return {k: getattr(s, k) for k, _ in StreamStats._fields_}
+
+
+class ExpertCache:
+    """Device cache of whole experts (rf_expert_cache_create)."""
+
+    def __init__(self, fmt: int, n_ff: int, n_embd: int, slots: int):
+        h = _P()
+        _check(lib().rf_expert_cache_create(fmt, n_ff, n_embd, slots, ctypes.byref(h)),
+               "rf_expert_cache_create")
+        self.handle = h
+
+    def close(self) -> None:
+        if self.handle is not None and self.handle.value:
+            lib().rf_expert_cache_destroy(self.handle)
+        self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def stats(self) -> dict:
+        s = ExpertCacheStats()
+        _check(lib().rf_expert_cache_stats_get(self.handle, ctypes.byref(s)),
+               "rf_expert_cache_stats_get")
+        return {k: getattr(s, k) for k, _ in ExpertCacheStats._fields_}
+
+
+def moe_ffn_streamed(fmt: int, logits, top_k: int, host_gate, host_up, host_down, n_ff: int,
+                     n_embd: int, block_rows: int, depth: int, arena: "Arena", x, cache=None,
+                     y=None, workspace=None, stream=None):
+    """rf_moe_ffn_streamed: experts in page-locked CPU tensors, one layer-wide
+    prefetch plan through `arena`, an optional ExpertCache."""
+    import torch
+    for t, nm in ((host_gate, "host_gate"), (host_up, "host_up"), (host_down, "host_down")):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{nm} must be a contiguous CPU tensor")
+    y = torch.empty(n_embd, dtype=torch.float32, device=x.device) if y is None else y
+    if workspace is None:
+        workspace = moe_workspace(top_k, n_ff, n_embd, block_rows, x.device)
+    _check(lib().rf_moe_ffn_streamed(fmt, _dev_ptr(logits, "logits"), logits.numel(), top_k,
+                                     host_gate.data_ptr(), host_up.data_ptr(),
+                                     host_down.data_ptr(), n_ff, n_embd, block_rows, depth,
+                                     arena.handle, cache.handle if cache is not None else None,
+                                     _dev_ptr(x, "x"), _dev_ptr(y, "y"),
+                                     _dev_ptr(workspace, "workspace"), _stream(stream)),
+           "rf_moe_ffn_streamed")
+    return y, workspace
 
 
 def moe_route(logits, top_k: int, stream=None):

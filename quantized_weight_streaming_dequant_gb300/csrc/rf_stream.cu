@@ -30,33 +30,14 @@
 #include <mutex>
 #include <new>
 
-#include "rf_internal.h"
+#include "rf_arena.h"
 
 using namespace rf;
 
-struct rf_arena {
-    static constexpr int kMaxSlots = 65;   // depth <= 64
-    uint8_t *base = nullptr;
-    size_t bytes = 0;          // capacity promised to the caller
-    size_t alloc_bytes = 0;    // allocation (capacity + alignment slack)
-    int device = 0;
-    cudaStream_t copy_stream = nullptr;
-    cudaEvent_t copied[kMaxSlots] = {};
-    cudaEvent_t freed[kMaxSlots] = {};
-    bool freed_recorded[kMaxSlots] = {};
-    cudaEvent_t fork = nullptr;       // joins the copy stream to the caller's stream
-    unsigned long long epoch = 0;     // 0: eager; else the id of the capture
-    int next_slot = 0;
-    int last_slots = 0;
-    size_t last_stride = 0;
-    rf_stream_stats stats = {};
-    std::mutex mu;
-};
+namespace rf {
 
-namespace {
-
-int64_t plan_rows(int64_t row_bytes, int64_t n_rows, int64_t block_rows, int depth,
-                  size_t arena_bytes)
+int64_t arena_plan_rows(int64_t row_bytes, int64_t n_rows, int64_t block_rows, int depth,
+                        size_t arena_bytes)
 {
     int64_t want = (block_rows == 0 || block_rows > n_rows) ? n_rows : block_rows;
     if (want < 1) want = 1;
@@ -65,7 +46,71 @@ int64_t plan_rows(int64_t row_bytes, int64_t n_rows, int64_t block_rows, int dep
     return std::min(want, fit);
 }
 
-}  // namespace
+rf_status arena_prepare(rf_arena *a, cudaStream_t s, int slots, size_t stride)
+{
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    unsigned long long cap_id = 0;
+    if (cudaStreamGetCaptureInfo(s, &cap, &cap_id) != cudaSuccess) {
+        cudaGetLastError();
+        return RF_ERR_CUDA;
+    }
+    if (cap == cudaStreamCaptureStatusInvalidated) return RF_ERR_CUDA;
+    const unsigned long long epoch = cap == cudaStreamCaptureStatusActive ? cap_id : 0;
+    if (epoch != a->epoch) {
+        // The slot-free events belong to another epoch: order this walk
+        // after all work already enqueued on `s` (which includes every
+        // earlier reader of the slots when the graph is launched there).
+        if (cudaEventRecord(a->fork, s) != cudaSuccess ||
+            cudaStreamWaitEvent(a->copy_stream, a->fork, 0) != cudaSuccess)
+            return RF_ERR_CUDA;
+        for (int i = 0; i < rf_arena::kMaxSlots; ++i) a->freed_recorded[i] = false;
+        a->next_slot = 0;
+        a->last_slots = slots;
+        a->last_stride = stride;
+        a->epoch = epoch;
+    }
+    // A new slot layout overlaps the old one: the copy stream first waits for
+    // every old slot's last reader.
+    if (a->last_slots != slots || a->last_stride != stride) {
+        for (int i = 0; i < rf_arena::kMaxSlots; ++i)
+            if (a->freed_recorded[i] &&
+                cudaStreamWaitEvent(a->copy_stream, a->freed[i], 0) != cudaSuccess)
+                return RF_ERR_CUDA;
+        a->next_slot = 0;
+        a->last_slots = slots;
+        a->last_stride = stride;
+    }
+    return RF_OK;
+}
+
+rf_status arena_fetch(rf_arena *a, cudaStream_t s, const void *src, size_t bytes, int *slot_out,
+                      uint8_t **dst_out)
+{
+    const int slot = a->next_slot;
+    a->next_slot = (a->next_slot + 1) % a->last_slots;
+    uint8_t *dst = a->base + (size_t)slot * a->last_stride;
+    // Reservation: the slot's previous readers must have finished with it.
+    if (a->freed_recorded[slot] &&
+        cudaStreamWaitEvent(a->copy_stream, a->freed[slot], 0) != cudaSuccess)
+        return RF_ERR_CUDA;
+    if (cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, a->copy_stream) != cudaSuccess ||
+        cudaEventRecord(a->copied[slot], a->copy_stream) != cudaSuccess ||
+        cudaStreamWaitEvent(s, a->copied[slot], 0) != cudaSuccess)
+        return RF_ERR_CUDA;
+    a->stats.bytes_copied += bytes;
+    *slot_out = slot;
+    *dst_out = dst;
+    return RF_OK;
+}
+
+rf_status arena_release(rf_arena *a, cudaStream_t s, int slot)
+{
+    if (cudaEventRecord(a->freed[slot], s) != cudaSuccess) return RF_ERR_CUDA;
+    a->freed_recorded[slot] = true;
+    return RF_OK;
+}
+
+}  // namespace rf
 
 extern "C" {
 
@@ -78,7 +123,7 @@ rf_status rf_stream_plan(int fmt, int64_t in_dim, int64_t n_rows, int64_t block_
         depth > rf_arena::kMaxSlots - 1)
         return RF_ERR_INVALID_ARG;
     const int64_t rb = (in_dim / block_elems_of(fmt)) * (int64_t)block_bytes_of(fmt);
-    const int64_t eff = plan_rows(rb, n_rows, block_rows, depth, arena_bytes);
+    const int64_t eff = arena_plan_rows(rb, n_rows, block_rows, depth, arena_bytes);
     if (eff < 0) return RF_ERR_ARENA_TOO_SMALL;
     const int64_t nblk = n_rows == 0 ? 0 : (n_rows + eff - 1) / eff;
     // Peak: the bytes of a block being multiplied plus the depth blocks
@@ -127,6 +172,12 @@ rf_status rf_arena_create(size_t bytes, rf_arena **out)
         rf_arena_destroy(a);
         return RF_ERR_CUDA;
     }
+    if (cudaMallocHost(&a->route_host, sizeof(int32_t) * kMaxTerms) != cudaSuccess) {
+        cudaGetLastError();
+        a->route_host = nullptr;
+        rf_arena_destroy(a);
+        return RF_ERR_OOM;
+    }
     for (int i = 0; i < rf_arena::kMaxSlots; ++i) {
         if (cudaEventCreateWithFlags(&a->copied[i], cudaEventDisableTiming) != cudaSuccess ||
             cudaEventCreateWithFlags(&a->freed[i], cudaEventDisableTiming) != cudaSuccess) {
@@ -160,6 +211,7 @@ void rf_arena_destroy(rf_arena *a)
     }
     if (a->copy_stream) cudaStreamDestroy(a->copy_stream);
     if (a->base) cudaFree(a->base);
+    if (a->route_host) cudaFreeHost(a->route_host);
     cudaSetDevice(prev);
     delete a;
 }
@@ -189,7 +241,7 @@ rf_status rf_stream_linear(int fmt, const void *host_W, int64_t in_dim, int64_t 
     if (attr.type != cudaMemoryTypeHost) return RF_ERR_NOT_PINNED;
     const int64_t n_rows = row_end - row_start;
     const int64_t rb = (in_dim / block_elems_of(fmt)) * (int64_t)block_bytes_of(fmt);
-    const int64_t eff = plan_rows(rb, std::max<int64_t>(n_rows, 1), block_rows, depth, a->bytes);
+    const int64_t eff = arena_plan_rows(rb, std::max<int64_t>(n_rows, 1), block_rows, depth, a->bytes);
     if (eff < 0) return RF_ERR_ARENA_TOO_SMALL;
     if (n_rows == 0) return RF_OK;
     if (eff > 0x7fffffffLL) return RF_ERR_TOO_LARGE;
@@ -199,38 +251,7 @@ rf_status rf_stream_linear(int fmt, const void *host_W, int64_t in_dim, int64_t 
     const size_t stride = ((size_t)(eff * rb) + 255) & ~(size_t)255;
     if ((size_t)slots * stride > a->alloc_bytes) return RF_ERR_ARENA_TOO_SMALL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-    unsigned long long cap_id = 0;
-    if (cudaStreamGetCaptureInfo(s, &cap, &cap_id) != cudaSuccess) {
-        cudaGetLastError();
-        return RF_ERR_CUDA;
-    }
-    if (cap == cudaStreamCaptureStatusInvalidated) return RF_ERR_CUDA;
-    const unsigned long long epoch = cap == cudaStreamCaptureStatusActive ? cap_id : 0;
-    if (epoch != a->epoch) {
-        // The slot-free events belong to another epoch: order this walk
-        // after all work already enqueued on `stream` (which includes every
-        // earlier reader of the slots when the graph is launched there).
-        if (cudaEventRecord(a->fork, s) != cudaSuccess ||
-            cudaStreamWaitEvent(a->copy_stream, a->fork, 0) != cudaSuccess)
-            return RF_ERR_CUDA;
-        for (int i = 0; i < rf_arena::kMaxSlots; ++i) a->freed_recorded[i] = false;
-        a->next_slot = 0;
-        a->last_slots = slots;
-        a->last_stride = stride;
-        a->epoch = epoch;
-    }
-    // A new slot layout overlaps the old one: the copy stream first waits for
-    // every old slot's last reader.
-    if (a->last_slots != slots || a->last_stride != stride) {
-        for (int i = 0; i < rf_arena::kMaxSlots; ++i)
-            if (a->freed_recorded[i] &&
-                cudaStreamWaitEvent(a->copy_stream, a->freed[i], 0) != cudaSuccess)
-                return RF_ERR_CUDA;
-        a->next_slot = 0;
-        a->last_slots = slots;
-        a->last_stride = stride;
-    }
+    if (const rf_status st = arena_prepare(a, s, slots, stride)) return st;
     const uint8_t *hw = static_cast<const uint8_t *>(host_W);
     size_t peak = 0;
     rf_stream_plan(fmt, in_dim, n_rows, block_rows, depth, a->bytes, nullptr, nullptr, &peak);
@@ -238,19 +259,10 @@ rf_status rf_stream_linear(int fmt, const void *host_W, int64_t in_dim, int64_t 
     int64_t blocks = 0;
     for (int64_t r0 = row_start; r0 < row_end; r0 += eff) {
         const int64_t nr = std::min(eff, row_end - r0);
-        const int slot = a->next_slot;
-        a->next_slot = (a->next_slot + 1) % slots;
-        uint8_t *dst = a->base + (size_t)slot * stride;
-        const size_t bytes = (size_t)(nr * rb);
-        // Reservation: the slot's previous GEMV must have finished reading it.
-        if (a->freed_recorded[slot] &&
-            cudaStreamWaitEvent(a->copy_stream, a->freed[slot], 0) != cudaSuccess)
-            return RF_ERR_CUDA;
-        if (cudaMemcpyAsync(dst, hw + r0 * rb, bytes, cudaMemcpyHostToDevice, a->copy_stream) !=
-                cudaSuccess ||
-            cudaEventRecord(a->copied[slot], a->copy_stream) != cudaSuccess ||
-            cudaStreamWaitEvent(s, a->copied[slot], 0) != cudaSuccess)
-            return RF_ERR_CUDA;
+        int slot = 0;
+        uint8_t *dst = nullptr;
+        if (const rf_status st = arena_fetch(a, s, hw + r0 * rb, (size_t)(nr * rb), &slot, &dst))
+            return st;
         Job J;
         std::memset(&J, 0, sizeof(J));
         J.term[0] = Term{dst, 0, -1, 0, 0};
@@ -268,9 +280,7 @@ rf_status rf_stream_linear(int fmt, const void *host_W, int64_t in_dim, int64_t 
         const rf_status st = launch_rowwin(d, s);
         if (st != RF_OK) return st;
         // Retire: the slot is free once this GEMV has run.
-        if (cudaEventRecord(a->freed[slot], s) != cudaSuccess) return RF_ERR_CUDA;
-        a->freed_recorded[slot] = true;
-        a->stats.bytes_copied += bytes;
+        if (const rf_status st2 = arena_release(a, s, slot)) return st2;
         ++blocks;
     }
     a->stats.calls += 1;

@@ -15,7 +15,8 @@ Distributions (the workloads' statement):
            scale bytes uniform random (so every 6-bit scale and min is
            uniform over [0, 63]); d = fp16(U[1e-4, 1e-3]), dmin =
            fp16(U[1e-4, 1e-3]).
-  x      : fp32 N(0, 1); router logits fp32 N(0, 1).
+  x      : fp32 N(0, 1); router logits fp32 N(0, 1) (or, for expert-cache
+           runs, a fixed per-expert bias 0.5*N(0,1) plus N(0,1) per token).
 
 Reproducibility: rows are generated in fixed chunks of ``CHUNK_ROWS`` rows,
 each from ``numpy.random.default_rng([seed, chunk])``, so the bytes depend
@@ -109,6 +110,16 @@ def normal_f32(n: int, seed: int) -> np.ndarray:
 
 def router_logits(n_expert: int, seed: int) -> np.ndarray:
     return np.random.default_rng([seed, 0x1061]).standard_normal(n_expert).astype(np.float32)
+
+
+def skewed_router_logits(n_expert: int, n_tokens: int, seed: int,
+                         skew: float = 0.5) -> np.ndarray:
+    """(n_tokens, n_expert) logits with expert popularity: a fixed per-expert
+    bias skew*N(0,1) plus N(0,1) per token.  skew = 0.5 makes the most
+    popular 20 % of 128 experts take about 57 % of the top-4 selections."""
+    rng = np.random.default_rng([seed, 0x5e1])
+    bias = skew * rng.standard_normal(n_expert)
+    return (bias[None, :] + rng.standard_normal((n_tokens, n_expert))).astype(np.float32)
 
 
 # ----------------------------------------------------------------- workloads
