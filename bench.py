@@ -492,8 +492,9 @@ def run_moe(torch, rf, device, steps: int = 200):
 
 def run_moe_streamed(torch, rf, device, hG, hU, hD, x, active, tokens: int = 60):
     """The same MoE with its experts in page-locked host memory read through
-    the layer-wide prefetch plan (rf_moe_ffn_streamed: block_rows 512, depth
-    4, 256 MiB arena) with expert caches of 0, 16 and 32 experts, on router
+    the layer-wide prefetch plan (rf_moe_ffn_streamed: depth 4, 256 MiB
+    arena, whole windows, and 512-row blocks without a cache) with expert
+    caches of 0, 16, 32 and 64 experts, on router
     logits with expert popularity (the top 20 % of experts take about 57 %
     of the selections).  Host wall time per token (each call waits for its
     routing result), after 16 warm-up tokens that fill the cache."""
@@ -508,14 +509,14 @@ def run_moe_streamed(torch, rf, device, hG, hU, hD, x, active, tokens: int = 60)
     arena = rf.Arena(256 << 20)
     h2d = h2d_probe(torch, device, 256 << 20)
     per_expert = 2 * n_ff * rf.row_bytes(fmt, n_embd) + n_embd * rf.row_bytes(fmt, n_ff)
-    out = {"block_rows": 512, "depth": 4, "arena_bytes": 256 << 20, "tokens": tokens,
+    out = {"depth": 4, "arena_bytes": 256 << 20, "tokens": tokens,
            "h2d_probe_256mib_gbs": h2d, "router_skew": 0.5, "budgets": []}
     try:
-        for slots in (0, 16, 32):
+        for slots, br in ((0, 512), (0, 0), (16, 0), (32, 0), (64, 0)):
             cache = rf.ExpertCache(fmt, n_ff, n_embd, slots) if slots else None
             with torch.cuda.stream(s):
                 for t in range(warm):
-                    rf.moe_ffn_streamed(fmt, logits[t], k, hG, hU, hD, n_ff, n_embd, 512, 4, arena,
+                    rf.moe_ffn_streamed(fmt, logits[t], k, hG, hU, hD, n_ff, n_embd, br, 4, arena,
                                         x, cache=cache, y=y, workspace=ws, stream=s)
             torch.cuda.synchronize()
             st0 = cache.stats() if cache else None
@@ -523,12 +524,13 @@ def run_moe_streamed(torch, rf, device, hG, hU, hD, x, active, tokens: int = 60)
             t0 = time.perf_counter()
             with torch.cuda.stream(s):
                 for t in range(warm, warm + tokens):
-                    rf.moe_ffn_streamed(fmt, logits[t], k, hG, hU, hD, n_ff, n_embd, 512, 4, arena,
+                    rf.moe_ffn_streamed(fmt, logits[t], k, hG, hU, hD, n_ff, n_embd, br, 4, arena,
                                         x, cache=cache, y=y, workspace=ws, stream=s)
             torch.cuda.synchronize()
             dt = (time.perf_counter() - t0) / tokens
             arena_bytes = arena.stats()["bytes_copied"] - a0
-            row = {"cache_experts": slots, "cache_bytes": slots * per_expert,
+            row = {"cache_experts": slots, "block_rows": br or "whole",
+                   "cache_bytes": slots * per_expert,
                    "ms_per_token": dt * 1e3, "active_gbs": active / dt / 1e9}
             if cache:
                 st = cache.stats()
