@@ -30,7 +30,7 @@
  *            quants; an element is d*sc*q - dmin*m with (sc, m) its
  *            sub-block's scale and min.
  *
- * Readings where the pages are silent (each is also listed in the design doc):
+ * Readings where the pages are silent:
  *   - fp16 scale: IEEE-754 binary16, little endian, first two bytes.
  *   - Q4_0 nibble order: element j (j<16) is the low nibble of quant byte j,
  *     element j+16 is its high nibble (the GGUF convention).
