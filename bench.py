@@ -409,6 +409,49 @@ def run_dense_format(torch, rf, device, fmt: int, steps: int = 2000):
             "value": wbytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "steps": rounds * syn.C2["copies"]}
 
 
+def run_multi_token(torch, rf, device, reps: int = 50):
+    """Several tokens through one resident matrix per launch (rf_gemv_multi):
+    the 11008x4096 Q4_0 gate projection, eight copies (203 MB, > L2) walked
+    round-robin in one CUDA graph of chained launches, for 1, 2, 4 and 8
+    tokens.  value = weight bytes per second; token_gbs = the same times the
+    tokens (what separate launches per token would have to stream)."""
+    fmt, rows, in_dim = syn.Q4_0, syn.C2["d_ff"], syn.C2["d_model"]
+    Ws = [torch.from_numpy(syn.quant_matrix(fmt, rows, in_dim, 70 + c, threads=8)).to(device)
+          for c in range(8)]
+    nbytes = Ws[0].numel()
+    s = torch.cuda.Stream(device)
+    s.wait_stream(torch.cuda.current_stream())
+    out = []
+    for n_tok in (1, 2, 4, 8):
+        X = torch.from_numpy(np.stack([syn.normal_f32(in_dim, 900 + t) for t in range(n_tok)])).to(
+            device)
+        Y = torch.empty(n_tok, rows, device=device)
+
+        def walk():
+            for W in Ws:
+                rf.gemv_multi(fmt, W, 0, rows, in_dim, X, Y, stream=s, flags=rf.CHAIN)
+        with torch.cuda.stream(s):
+            walk()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            walk()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                g.replay()
+            e0.record(s)
+            for _ in range(reps):
+                g.replay()
+            e1.record(s)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (reps * len(Ws))
+        out.append({"tokens": n_tok, "us_per_launch": us, "value": nbytes / us / 1e3,
+                    "unit": "GB/s", "token_gbs": n_tok * nbytes / us / 1e3})
+        del g
+    return {"matrix": f"Q4_0 {rows}x{in_dim}", "copies": len(Ws), "bytes": nbytes, "rows": out}
+
+
 def run_streamed_gemv(torch, rf, device, depth: int, reps: int = 50):
     """Q8_0 512x2048 streamed from pinned host memory in 128-row blocks, eager
     calls and the same calls captured into one CUDA graph."""
@@ -894,6 +937,7 @@ def main():
             extra["streamed_gemv_q8_0_512x2048"] = [run_streamed_gemv(torch, rf, device, dp)
                                                     for dp in (4, 1)]
             extra["moe_mxfp4"] = run_moe(torch, rf, device)
+            extra["multi_token_q4_0"] = run_multi_token(torch, rf, device)
             q4k = run_dense_format(torch, rf, device, syn.Q4_K)
             q4k["frac_of_hbm_peak"] = q4k["value"] / peak
             extra["dense_layer_q4_k"] = q4k

@@ -200,6 +200,21 @@ RF_API rf_status rf_ffn_swiglu_ws(int fmt, const void *gate, const void *up, con
                                   int64_t n_ff, int64_t n_embd, const float *x, float *y,
                                   float *h, void *workspace, unsigned flags, void *stream);
 
+/* Several tokens through one row window (a decode batch, or a small prefill
+ * chunk): Y[t][r - row_start] = sum_i W[r,i] * X[t][i] for t < n_tok, all in
+ * ONE launch that walks the window's rows once (neurostream, "What the
+ * numbers taught us": tokens that share one pass over the weights cost
+ * little more than one).  The rows are copied to shared memory once per
+ * token from L2, so HBM sees each weight byte about once per call.  Every
+ * token's row is bit-identical to rf_gemv on that token alone.
+ * X: n_tok rows of in_dim floats, ldx floats apart; Y: n_tok rows of
+ * row_end-row_start floats, ldy floats apart.  All device.  flags as
+ * rf_gemv_ex.  Errors: as rf_gemv; RF_ERR_TOO_LARGE for n_tok > 8;
+ * RF_ERR_INVALID_ARG for n_tok < 1, ldx < in_dim or ldy < rows. */
+RF_API rf_status rf_gemv_multi(int fmt, const void *W, int64_t row_start, int64_t row_end,
+                               int64_t in_dim, int n_tok, const float *X, int64_t ldx, float *Y,
+                               int64_t ldy, unsigned flags, void *stream);
+
 /* Zero-copy variant of rf_gemv (hipfire PR #793, "Summary": the "pcie"
  * execution of a spilled layer, where the GPU kernels read host-mapped
  * weights over the link; "Design notes": the host memory is allocated mapped

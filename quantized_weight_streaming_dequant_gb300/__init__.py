@@ -72,6 +72,7 @@ _SIGS = {
     "rf_ffn_swiglu": ([_I, _P, _P, _P, _I64, _I64, _P, _P, _P, _P], _I),
     "rf_ffn_workspace_bytes": ([_I64], _SZ),
     "rf_gemv_host": ([_I, _P, _I64, _I64, _I64, _P, _P, _P], _I),
+    "rf_gemv_multi": ([_I, _P, _I64, _I64, _I64, _I, _P, _I64, _P, _I64, ctypes.c_uint, _P], _I),
     "rf_ffn_swiglu_ws": ([_I, _P, _P, _P, _I64, _I64, _P, _P, _P, _P, ctypes.c_uint, _P], _I),
     "rf_arena_create": ([_SZ, ctypes.POINTER(_P)], _I),
     "rf_arena_destroy": ([_P], None),
@@ -174,6 +175,24 @@ def gemv(fmt: int, W, row_start: int, row_end: int, in_dim: int, x, y=None, stre
                             _dev_ptr(y, "y") if y.numel() else 1, flags, _stream(stream)),
            "rf_gemv")
     return y
+
+
+def gemv_multi(fmt: int, W, row_start: int, row_end: int, in_dim: int, X, Y=None, stream=None,
+               flags: int = 0):
+    """rf_gemv_multi: X is (n_tok, in_dim) float32 on the device (rows may be
+    strided); returns Y (n_tok, row_end - row_start)."""
+    import torch
+    if X.dim() != 2 or X.stride(1) != 1:
+        raise ValueError("X must be 2-D with unit stride along in_dim")
+    n_tok = X.shape[0]
+    if Y is None:
+        Y = torch.empty(n_tok, max(row_end - row_start, 0), dtype=torch.float32, device=X.device)
+    if Y.dim() != 2 or Y.stride(1) != 1:
+        raise ValueError("Y must be 2-D with unit stride along the rows")
+    _check(lib().rf_gemv_multi(fmt, _dev_ptr(W, "W"), row_start, row_end, in_dim, n_tok,
+                               X.data_ptr(), X.stride(0), Y.data_ptr(), Y.stride(0), flags,
+                               _stream(stream)), "rf_gemv_multi")
+    return Y
 
 
 def gemv_batch(fmt: int, in_dim: int, windows, stream=None, flags: int = 0):

@@ -204,6 +204,41 @@ rf_status rf_gemv_ex(int fmt, const void *W, int64_t row_start, int64_t row_end,
     return launch_rowwin(d, static_cast<cudaStream_t>(stream));
 }
 
+rf_status rf_gemv_multi(int fmt, const void *W, int64_t row_start, int64_t row_end, int64_t in_dim,
+                        int n_tok, const float *X, int64_t ldx, float *Y, int64_t ldy,
+                        unsigned flags, void *stream)
+{
+    if (!fmt_ok(fmt)) return RF_ERR_UNSUPPORTED_FMT;
+    if (!W || !X || !Y || in_dim <= 0 || in_dim % block_elems_of(fmt) != 0 || row_start < 0 ||
+        row_end < row_start || n_tok < 1 || ldx < in_dim || ldy < row_end - row_start)
+        return RF_ERR_INVALID_ARG;
+    if (n_tok > kMaxTerms || n_tok > kMaxX) return RF_ERR_TOO_LARGE;
+    if ((reinterpret_cast<uintptr_t>(W) & 15u) != 0) return RF_ERR_MISALIGNED;
+    if (row_end - row_start > 0x7fffffffLL) return RF_ERR_TOO_LARGE;
+    if (row_end == row_start) return RF_OK;
+    if (const rf_status c = check_in_dim(fmt, in_dim, n_tok)) return c;
+    // One job whose terms are the same matrix against each token's
+    // activations; each term's dot goes to its own output row.
+    Job J;
+    std::memset(&J, 0, sizeof(J));
+    for (int t = 0; t < n_tok; ++t) J.term[t] = Term{static_cast<const uint8_t *>(W), t, -1, 0, 0};
+    J.y = Y;
+    J.y_stride = ldy;
+    J.row0 = row_start;
+    J.n_rows = (int32_t)(row_end - row_start);
+    J.n_terms = n_tok;
+    J.combine = kCombineEach;
+    LaunchDesc d;
+    d.fmt = fmt;
+    d.in_dim = in_dim;
+    d.jobs = &J;
+    d.n_jobs = 1;
+    for (int t = 0; t < n_tok; ++t) d.x[t] = X + (int64_t)t * ldx;
+    d.n_x = n_tok;
+    d.pdl = (flags & RF_CHAIN) != 0;
+    return launch_rowwin(d, static_cast<cudaStream_t>(stream));
+}
+
 rf_status rf_gemv_host(int fmt, const void *host_W, int64_t row_start, int64_t row_end,
                        int64_t in_dim, const float *x, float *y, void *stream)
 {

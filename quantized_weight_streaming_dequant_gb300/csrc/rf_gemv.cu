@@ -1107,6 +1107,10 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
                 float dot = rt[0];
 #pragma unroll
                 for (int w = 1; w < kNW; ++w) dot += rt[w * 32];
+                if (J.combine == kCombineEach) {
+                    if (row_ok) J.y[t * J.y_stride + rowrel] = dot;
+                    continue;
+                }
                 if (J.combine == kCombineSwiGLU) {
                     if (t == 0)
                         gate = dot;
@@ -1122,7 +1126,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
             }
             float out = yacc;
             if (J.act == kActGelu) out = 0.5f * out * (1.f + erff(out * 0.70710678118654752f));
-            if (row_ok) J.y[rowrel] = out;
+            if (row_ok && J.combine != kCombineEach) J.y[rowrel] = out;
             if (p.xr_out)
                 xrec_emit<FMT>(row_ok ? out : 0.f,
                                p.xr_out + ((J.y - p.xr_y_base) + (rowrel - lane)) / kRows);
@@ -1392,7 +1396,7 @@ bool continues(const Job &A, const Job &B)
 {
     if (A.n_terms != B.n_terms || A.combine != B.combine || A.act != B.act ||
         A.weights != B.weights || A.expert_rows != B.expert_rows ||
-        A.expert_count != B.expert_count)
+        A.expert_count != B.expert_count || A.y_stride != B.y_stride)
         return false;
     if (B.row0 != A.row0 + A.n_rows || B.y != A.y + A.n_rows) return false;
     if ((int64_t)A.n_rows + B.n_rows > 0x7fffffffLL) return false;
@@ -1440,6 +1444,9 @@ rf_status launch_rowwin(const LaunchDesc &d, cudaStream_t stream)
             return RF_ERR_INVALID_ARG;
         if (J.n_rows > 0 && !J.y) return RF_ERR_INVALID_ARG;
         if (J.combine == kCombineSwiGLU && J.n_terms != 2) return RF_ERR_INVALID_ARG;
+        if (J.combine == kCombineEach &&
+            (d.xr_out || (J.n_terms > 1 && J.y_stride < (int64_t)J.n_rows)))
+            return RF_ERR_INVALID_ARG;
         for (int t = 0; t < J.n_terms; ++t) {
             const Term &T = J.term[t];
             if (!T.W) return RF_ERR_INVALID_ARG;

@@ -19,6 +19,7 @@ enum Combine : int32_t {
     kCombineSum = 0,     // y = sum_t weight_t * dot_t (weight 1 when weights == nullptr)
     kCombineSwiGLU = 1,  // y = silu(dot_0) * dot_1  (gate, up)
     kCombineRouted = 2,  // y = sum_t w[expert_slot_t] * dot_t, w from the launch's own routing
+    kCombineEach = 3,    // y[t * y_stride + r] = dot_t: one output row per term (batched tokens)
 };
 enum Act : int32_t { kActNone = 0, kActGelu = 1 };
 
@@ -38,6 +39,7 @@ struct Job {
     int64_t row0;
     int64_t expert_rows;
     int64_t expert_count;   // experts in the stacked tensor (expert terms)
+    int64_t y_stride;       // kCombineEach: floats between the terms' output rows
     int32_t n_rows;
     int32_t n_terms;
     int32_t combine;
