@@ -49,14 +49,15 @@ def test_streamed_q8_0_gemv_512x2048(rf):
         arena.close()
 
 
-def test_dense_q4_0_layer_4096_11008(rf):
-    """One dense decode layer: QKV batched, O, gate/up + SwiGLU, down; every row
-    of every projection against the oracle; chained and unchained launches, and
-    the FFN with and without the digit hand-off workspace, give identical
-    bits."""
+@pytest.mark.parametrize("fmt", [syn.Q4_0, syn.Q4_K])
+def test_dense_layer_4096_11008(rf, fmt):
+    """One dense decode layer (Q4_0, and the same layer in Q4_K): QKV batched,
+    O, gate/up + SwiGLU, down; every row of every projection against the
+    oracle; chained and unchained launches, and the FFN with and without the
+    digit hand-off workspace, give identical bits."""
     import torch
     from quantized_weight_streaming_dequant_gb300.layer import DenseLayer
-    fmt, d, f = syn.Q4_0, syn.C2["d_model"], syn.C2["d_ff"]
+    d, f = syn.C2["d_model"], syn.C2["d_ff"]
     s = syn.C2["seed"] * 1000
     mats = [syn.quant_matrix(fmt, d, d, s + i, threads=8) for i in range(4)]
     mats += [syn.quant_matrix(fmt, f, d, s + 4, threads=8), syn.quant_matrix(fmt, f, d, s + 5, threads=8),
@@ -94,6 +95,38 @@ def test_moe_mxfp4_128x2880x2880_top4(rf):
     c = syn.C3
     moe_check(rf, c["fmt"], c["n_expert"], c["n_ff"], c["n_embd"], c["top_k"], c["block_rows"],
               seed=c["seed"])
+
+
+def test_moe_mxfp4_128x2880x2880_streamed_as_benched(rf):
+    """The routed MoE with its experts in page-locked host memory, through the
+    layer-wide prefetch plan in the benchmark's configuration (whole windows,
+    depth 4, 256 MiB arena, a 32-expert cache, popular experts): every token
+    bit-identical to the resident rf_moe_ffn, which the test above checks
+    against the oracle."""
+    import torch
+    c = syn.C3
+    fmt, E, n_ff, n_embd, k = c["fmt"], c["n_expert"], c["n_ff"], c["n_embd"], c["top_k"]
+    G = syn.stacked_experts(fmt, E, n_ff, n_embd, c["seed"], threads=8)
+    U = syn.stacked_experts(fmt, E, n_ff, n_embd, c["seed"] + 1, threads=8)
+    D = syn.stacked_experts(fmt, E, n_embd, n_ff, c["seed"] + 2, threads=8)
+    Gd, Ud, Dd = (dev_tensor(a) for a in (G, U, D))
+    hG, hU, hD = (torch.from_numpy(a).pin_memory() for a in (G, U, D))
+    x = dev_tensor(syn.normal_f32(n_embd, c["seed"] + 3))
+    logits = torch.from_numpy(syn.skewed_router_logits(E, 12, 11)).cuda()
+    arena = rf.Arena(256 << 20)
+    cache = rf.ExpertCache(fmt, n_ff, n_embd, 32)
+    try:
+        for t in range(12):
+            y_ref, _ = rf.moe_ffn(fmt, logits[t], k, Gd, Ud, Dd, n_ff, n_embd, c["block_rows"], x)
+            y, _ = rf.moe_ffn_streamed(fmt, logits[t], k, hG, hU, hD, n_ff, n_embd, 0, 4, arena,
+                                       x, cache=cache)
+            assert np.array_equal(bits(y.cpu().numpy()), bits(y_ref.cpu().numpy())), t
+        st = cache.stats()
+        assert st["lookups"] == 12 * k and st["hits"] + st["fills"] + st["bypasses"] == 12 * k
+    finally:
+        torch.cuda.synchronize()
+        cache.close()
+        arena.close()
 
 
 def test_streamed_ffn_q8_0_24576x6144_sampled(rf):
