@@ -47,10 +47,10 @@ def test_status_strings(L):
     assert L.rf_version() >= 100
 
 
-@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("fmt", FMTS + [rf.Q4_K])
 def test_sizes_match_oracle(L, fmt):
     assert rf.block_bytes(fmt) == oracle.block_bytes(fmt)
-    for in_dim in (32, 64, 2048, 2880, 4096, 11008, 24576):
+    for in_dim in (32, 64, 256, 2048, 2880, 4096, 11008, 24576):
         assert rf.row_bytes(fmt, in_dim) == oracle.row_bytes(fmt, in_dim)
     assert rf.row_bytes(fmt, 33) == 0 and rf.row_bytes(fmt, 0) == 0
     assert rf.block_bytes(7) == 0
@@ -121,6 +121,41 @@ def test_argument_errors_before_any_gpu_work(L):
     # stream: bad depth
     assert L.rf_stream_linear(rf.Q8_0, p16, 32, 0, 1, 1, -1, p16, p16, p16, None) == 1
     assert L.rf_stream_linear(rf.Q8_0, p16, 32, 0, 1, 1, 65, p16, p16, p16, None) == 1
+
+
+def test_newer_entry_points_check_arguments_first(L):
+    """rf_gemv_multi, the expert cache and rf_moe_ffn_streamed refuse bad
+    arguments before touching the GPU."""
+    buf = (ctypes.c_uint8 * 8192)()
+    p = (ctypes.addressof(buf) + 255) & ~255
+    # rf_gemv_multi(fmt, W, r0, r1, in_dim, n_tok, X, ldx, Y, ldy, flags, stream)
+    assert L.rf_gemv_multi(7, p, 0, 4, 32, 2, p, 32, p, 4, 0, None) == 2
+    assert L.rf_gemv_multi(rf.Q4_0, p, 0, 4, 32, 0, p, 32, p, 4, 0, None) == 1
+    assert L.rf_gemv_multi(rf.Q4_0, p, 0, 4, 32, 2, p, 31, p, 4, 0, None) == 1
+    assert L.rf_gemv_multi(rf.Q4_0, p, 0, 4, 32, 2, p, 32, p, 3, 0, None) == 1
+    assert L.rf_gemv_multi(rf.Q4_0, p, 0, 4, 32, 9, p, 32, p, 4, 0, None) == 9
+    assert L.rf_gemv_multi(rf.Q4_0, p + 4, 0, 4, 32, 2, p, 32, p, 4, 0, None) == 8
+    assert L.rf_gemv_multi(rf.Q4_0, p, 4, 4, 32, 2, p, 32, p, 4, 0, None) == 0   # no rows
+    assert L.rf_gemv_multi(rf.Q4_K, p, 0, 4, 288, 2, p, 288, p, 4, 0, None) == 1  # not 256-multiple
+    # rf_expert_cache_create(fmt, n_ff, n_embd, slots, out)
+    h = ctypes.c_void_p()
+    assert L.rf_expert_cache_create(7, 64, 64, 2, ctypes.byref(h)) == 2
+    assert L.rf_expert_cache_create(rf.Q4_0, 48, 64, 2, ctypes.byref(h)) == 1
+    assert L.rf_expert_cache_create(rf.Q4_0, 64, 64, 0, ctypes.byref(h)) == 1
+    assert L.rf_expert_cache_create(rf.Q4_0, 64, 64, 1025, ctypes.byref(h)) == 1
+    assert L.rf_expert_cache_create(rf.Q4_0, 64, 64, 2, None) == 1
+    assert L.rf_expert_cache_stats_get(None, ctypes.byref(rf.ExpertCacheStats())) == 1
+    L.rf_expert_cache_destroy(None)   # no-op
+    # rf_moe_ffn_streamed(fmt, logits, E, k, hG, hU, hD, n_ff, n_embd, br, depth, arena, cache,
+    #                     x, y, workspace, stream)
+    ms = L.rf_moe_ffn_streamed
+    assert ms(7, p, 8, 2, p, p, p, 64, 64, 32, 3, p, None, p, p, p, None) == 2
+    assert ms(rf.Q4_0, p, 8, 2, p, p, p, 64, 64, 32, 3, None, None, p, p, p, None) == 1  # arena
+    assert ms(rf.Q4_0, p, 8, 9, p, p, p, 64, 64, 32, 8, p, None, p, p, p, None) == 1     # k > E
+    assert ms(rf.Q4_0, p, 8, 2, p, p, p, 64, 64, 48, 3, p, None, p, p, p, None) == 1     # rows
+    assert ms(rf.Q4_0, p, 8, 4, p, p, p, 64, 64, 32, 2, p, None, p, p, p, None) == 1     # depth
+    assert ms(rf.Q4_0, p, 8, 2, p, p, p, 64, 64, 32, 3, p, None, p, p, p + 16, None) == 8
+    assert ms(rf.Q4_0, p, 8, 2, p + 8, p, p, 64, 64, 32, 3, p, None, p, p, p, None) == 8
 
 
 @pytest.mark.skipif(has_gpu(), reason="checks the behaviour on a machine without a GPU")
