@@ -28,9 +28,10 @@
 //     (s from the block maximum) split into two byte planes.  The block dot
 //     sum_j q_j X_j is then exact dp4a chains over the raw quant bytes (Q8_0
 //     bytes are used as they are; Q4_0 nibbles are masked in place, the high
-//     ones scaled by 16; MXFP4 codes go through a byte-permute lookup of
-//     2*e2m1), and one fp32 FMA per block applies d * 2^-s.  Q4_0's "-8" is
-//     the per-block constant -8 * sum_j X_j.
+//     ones scaled by 16; MXFP4 codes go through two byte-permute lookups
+//     whose sum is 128 + 2*e2m1), and one fp32 FMA per block applies
+//     d * 2^-s.  Q4_0's "-8" and the MXFP4 offset are per-block constants
+//     (-8 and -128 times sum_j X_j).
 //     Error: |x_j - X_j*2^-s| <= 2^-15 * max|x_block|, so by Cauchy-Schwarz
 //     the activation rounding moves y_r by at most sqrt(32)*2^-15*||W_r||*||x||
 //     (< 1.8e-4 * ||W_r||*||x||), inside the parity tolerance 1e-3*||W_r||*||x||.
@@ -71,7 +72,7 @@ constexpr int kRows = 32;   // rows per group (one per lane)
 struct __align__(16) XRec {
     uint32_t p0[8];   // byte 0 of X (unsigned), 4 elements per word
     uint32_t p1[8];   // byte 1 of X (signed: X >> 8)
-    int32_t corr;     // Q4_0: -8 * sum_j X_j (else 0)
+    int32_t corr;     // per-format multiple of sum_j X_j (see xrec_corr)
     float scale;      // 2^-s
     int32_t pad[2];
 };
@@ -155,6 +156,18 @@ __device__ __forceinline__ float exp2i(int k)
                      : __uint_as_float(1u << (k + 149));
 }
 
+// The record's per-block integer correction, from sum_j X_j: Q4_0's "-8"
+// (-8 * sum), the offset of the MXFP4 lookup (-128 * sum), and Q4_K's sum
+// itself (its min term); Q8_0 needs none.
+template <int FMT>
+__device__ __forceinline__ int32_t xrec_corr(int sum)
+{
+    if constexpr (FMT == RF_Q4_0) return -8 * sum;
+    else if constexpr (FMT == RF_MXFP4) return -128 * sum;
+    else if constexpr (FMT == RF_Q4_K) return sum;
+    else return 0;
+}
+
 // Fixed-point digits of one 32-element activation block, computed by a quad
 // of consecutive lanes: lane `part` of the quad owns plane words 2*part and
 // 2*part+1 (8 elements).  xrec_load fetches the lane's 8 elements (in plane
@@ -217,7 +230,7 @@ __device__ __forceinline__ void xrec_build(const float (&v)[8], int part, bool a
         out->p1[2 * part + hh] = prmt(prmt(a, b, 0x0051u), prmt(c, d, 0x0051u), 0x5410u);
     }
     if (part == 0) {
-        out->corr = FMT == RF_Q4_0 ? -8 * sum : (FMT == RF_Q4_K ? sum : 0);
+        out->corr = xrec_corr<FMT>(sum);
         out->scale = exp2i(-s);
         out->pad[0] = out->pad[1] = 0;
     }
@@ -254,7 +267,7 @@ __device__ __forceinline__ void xrec_emit(float v, XRec *out)
     if (lane < 16)
         o32[lane] = word;
     else if (lane == 16)
-        o32[16] = (uint32_t)(FMT == RF_Q4_0 ? -8 * sum : (FMT == RF_Q4_K ? sum : 0));
+        o32[16] = (uint32_t)xrec_corr<FMT>(sum);
     else if (lane == 17)
         o32[17] = __float_as_uint(exp2i(-s));
     else if (lane < 20)
@@ -338,30 +351,29 @@ __device__ __forceinline__ float block_idot(const uint32_t (&q)[FmtT<FMT>::QW], 
         }
         return (float)((b + d) * 256 + a + c);
     } else {
-        // MXFP4: 2*e2m1 as signed bytes through a byte-permute lookup.
-        // Positive table {0,1,2,3,4,6,8,12}, negative table its negation;
-        // the sign bit of each code picks between them.
-        constexpr uint32_t kPosLo = 0x03020100u, kPosHi = 0x0c080604u;
-        constexpr uint32_t kNegLo = 0xfdfeff00u, kNegHi = 0xf4f8fafcu;
+        // MXFP4: each code c = (s, i) stands for v = +-u_i with u_i = 2*e2m1
+        // in {0,1,2,3,4,6,8,12}.  Two byte-permute lookups give, per byte,
+        // P = 2*u_i when s = 0 and 0 when s = 1 (the selector's top bit is
+        // the sign bit, which replicates the table byte's clear top bit), and
+        // M = 128 - u_i (the magnitude bits alone).  P + M = 128 + v lies in
+        // [116, 140], so one 32-bit add forms all four bytes without carries;
+        // the record's corr holds -128 * sum_j X_j and removes the offset.
+        constexpr uint32_t kTwoLo = 0x06040200u, kTwoHi = 0x18100c08u;
+        constexpr uint32_t kOffLo = 0x7d7e7f80u, kOffHi = 0x74787a7cu;
         int a = 0, b = 0, c = 0, d = 0;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const uint32_t v = q[k];
             const uint32_t m = v & 0x77777777u;
-            const uint32_t vs = v << 4;
-            const uint32_t mh = m >> 16;
-            const uint32_t pa = prmt(kPosLo, kPosHi, m), na = prmt(kNegLo, kNegHi, m);
-            const uint32_t sa = prmt(vs, v, 0xd9c8u);   // sign masks of the 4 codes
-            const uint32_t pb = prmt(kPosLo, kPosHi, mh), nb = prmt(kNegLo, kNegHi, mh);
-            const uint32_t sb = prmt(vs, v, 0xfbeau);
-            const uint32_t wa = (pa & ~sa) | (na & sa);
-            const uint32_t wb = (pb & ~sb) | (nb & sb);
-            a = dp4a_su(wa, p0[2 * k], a);
-            b = dp4a_ss(wa, p1[2 * k], b);
-            c = dp4a_su(wb, p0[2 * k + 1], c);
-            d = dp4a_ss(wb, p1[2 * k + 1], d);
+            const uint32_t vh = v >> 16, mh = m >> 16;
+            const uint32_t wa = prmt(kTwoLo, kTwoHi, v) + prmt(kOffLo, kOffHi, m);
+            const uint32_t wb = prmt(kTwoLo, kTwoHi, vh) + prmt(kOffLo, kOffHi, mh);
+            a = dp4a_uu(wa, p0[2 * k], a);
+            b = dp4a_us(wa, p1[2 * k], b);
+            c = dp4a_uu(wb, p0[2 * k + 1], c);
+            d = dp4a_us(wb, p1[2 * k + 1], d);
         }
-        return (float)((b + d) * 256 + a + c);
+        return (float)((b + d) * 256 + a + c + r.corr);
     }
 }
 
