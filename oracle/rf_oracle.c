@@ -394,7 +394,10 @@ double orc_gelu(double z) { return 0.5 * z * (1.0 + erf(z / sqrt(2.0))); }
 
 /* [NS-HOW] 2: the router names the k active experts.  Pick the k largest
  * logits (ties to the lower index) in descending order, then weight them by a
- * softmax over the selected logits. */
+ * softmax over the selected logits.  The pages say nothing of NaN logits: a
+ * NaN counts as -infinity, for the ranking and for the weights. */
+static double router_value(float v) { return isnan(v) ? -INFINITY : (double)v; }
+
 int orc_router_topk(const float *logits, int n_expert, int top_k, int *idx, double *w)
 {
     int k, e;
@@ -410,16 +413,16 @@ int orc_router_topk(const float *logits, int n_expert, int top_k, int *idx, doub
         for (e = 0; e < n_expert; e++) {
             if (taken[e])
                 continue;
-            if (best < 0 || logits[e] > logits[best])
+            if (best < 0 || router_value(logits[e]) > router_value(logits[best]))
                 best = e;   /* strict '>' keeps the lower index on ties */
         }
         taken[best] = 1;
         idx[k] = best;
     }
     free(taken);
-    m = (double)logits[idx[0]];
+    m = router_value(logits[idx[0]]);
     for (k = 0; k < top_k; k++) {
-        w[k] = exp((double)logits[idx[k]] - m);
+        w[k] = exp(router_value(logits[idx[k]]) - m);
         s += w[k];
     }
     for (k = 0; k < top_k; k++)

@@ -300,6 +300,36 @@ def test_router_topk_bruteforce(n_expert, top_k):
         assert all(w[i] >= w[i + 1] for i in range(top_k - 1))
 
 
+@pytest.mark.parametrize("n_expert,top_k", [(4, 4), (8, 3), (40, 8), (128, 4)])
+def test_router_nan_counts_as_minus_infinity(n_expert, top_k):
+    """Reading: a NaN logit ranks as -inf (ties to the lower index) and weighs
+    as -inf.  Brute force over inputs mixing NaN, -inf, +-0 and numbers, down to
+    fewer finite logits than top_k."""
+    rng = np.random.default_rng(n_expert + 100 * top_k)
+    for trial in range(30):
+        logits = rng.standard_normal(n_expert).astype(np.float32)
+        kind = rng.integers(0, 4, n_expert)
+        logits[kind == 0] = np.nan
+        logits[kind == 1] = -np.inf
+        if trial % 5 == 0:
+            logits[:] = np.nan
+            logits[rng.integers(n_expert)] = 1.0
+        if trial % 7 == 1:
+            logits[0], logits[-1] = -0.0, 0.0            # signed zeros tie
+            logits[1:-1] = np.nan
+        idx, w = oracle.router_topk(logits, top_k)
+        rank = np.where(np.isnan(logits), -np.inf, logits.astype(np.float64))
+        want = sorted(range(n_expert), key=lambda e: (-rank[e], e))[:top_k]
+        assert list(idx) == want, trial
+        sel = rank[want]
+        if np.isfinite(sel[0]):
+            ex = np.exp(sel - sel[0])
+            assert np.allclose(w, ex / ex.sum(), rtol=1e-12, atol=0)
+            assert all(w[i] == 0.0 for i in range(top_k) if sel[i] == -np.inf)
+        else:                                             # every selected logit is -inf
+            assert np.isnan(w).all()
+
+
 def test_router_equal_logits_uniform():
     idx, w = oracle.router_topk(np.full(128, 0.25, np.float32), 4)
     assert list(idx) == [0, 1, 2, 3]
