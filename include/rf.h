@@ -293,6 +293,9 @@ RF_API rf_status rf_stream_stats_get(const rf_arena *arena, rf_stream_stats *out
 /* Device top-k router (neurostream, "How it works" 2: the router names the
  * active experts and only those are read): idx[k] = the k-th largest logit's
  * expert (ties to the lower index), w[k] = softmax over the selected logits.
+ * A NaN logit counts as -inf (the pages leave NaN undefined), so the k
+ * indices are always distinct experts in [0, n_expert).  The routed FFNs
+ * below rank their logits the same way.
  * logits: device n_expert floats; idx: device top_k int32; w: device top_k
  * floats.  1 <= top_k <= min(n_expert, 8), n_expert <= 1024. */
 RF_API rf_status rf_moe_route(const float *logits, int n_expert, int top_k, int32_t *idx,

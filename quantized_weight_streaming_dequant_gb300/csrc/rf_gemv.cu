@@ -528,67 +528,83 @@ __device__ __forceinline__ const uint8_t *term_matrix(const int32_t *expert_idx,
     return W;
 }
 
+// Order-preserving unsigned key of a float that is not NaN (-0 and +0 equal).
+__device__ __forceinline__ uint32_t route_key(float v)
+{
+    const uint32_t u = __float_as_uint(v + 0.0f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 // Top-k of n logits by one warp (ties to the lower index; the same order as
 // the standalone router) and the softmax over the k selected, into idx/w.
+// A NaN logit counts as -inf.  Lane L holds experts L + 32*m, m < NM (slots
+// past n hold -inf with an index above every real one, so they are never
+// chosen while k <= n).  Each round takes the warp's largest key and then the
+// lowest index holding it with two warp reductions; only the winning lane
+// rescans its own NM slots.  The rounds are a rolled loop: the routing runs
+// once per launch from a cold instruction cache, so short code matters more
+// than instruction count.
+template <int NM>
+__device__ __forceinline__ void route_warp_n(const float *__restrict__ logits, int n, int k,
+                                             int32_t *idx, float *w)
+{
+    const int lane = threadIdx.x & 31;
+    float lv[NM];
+#pragma unroll
+    for (int m = 0; m < NM; ++m) {
+        const int e = lane + 32 * m;
+        const float v = e < n ? logits[e] : -INFINITY;
+        lv[m] = v != v ? -INFINITY : v;
+    }
+    uint32_t taken = 0;
+    float bv = -INFINITY;   // this lane's first largest untaken slot
+    int bm = -1;
+    auto local_best = [&] {
+        bv = -INFINITY;
+        bm = -1;
+#pragma unroll
+        for (int m = 0; m < NM; ++m)
+            if (!((taken >> m) & 1u) && (bm < 0 || lv[m] > bv)) {
+                bv = lv[m];
+                bm = m;
+            }
+    };
+    local_best();
+#pragma unroll 1
+    for (int r = 0; r < k; ++r) {
+        const uint32_t key = bm < 0 ? 0u : route_key(bv);
+        const uint32_t top = __reduce_max_sync(0xffffffffu, key);
+        const uint32_t win = __reduce_min_sync(
+            0xffffffffu, (bm >= 0 && key == top) ? (uint32_t)(lane + 32 * bm) : 0xffffffffu);
+        if ((int)(win & 31u) == lane) {
+            idx[r] = (int32_t)win;
+            w[r] = bv;
+            taken |= 1u << bm;
+            local_best();
+        }
+    }
+    __syncwarp();
+    if (lane == 0) {
+        const float m = w[0];
+        float sum = 0.f;
+#pragma unroll 1
+        for (int r = 0; r < k; ++r) {
+            const float e = expf(w[r] - m);
+            w[r] = e;
+            sum += e;
+        }
+#pragma unroll 1
+        for (int r = 0; r < k; ++r) w[r] = w[r] / sum;
+    }
+}
+
 __device__ __forceinline__ void route_warp(const float *__restrict__ logits, int n, int k,
                                            int32_t *idx, float *w)
 {
-    const int lane = threadIdx.x & 31;
-    // Experts lane + 32*m, m < 32 (n <= 1024), all loaded at once; a missing
-    // expert counts as already taken.
-    float lv[32];
-    uint32_t taken = 0;   // bit m: expert lane + 32*m already selected
-#pragma unroll
-    for (int m = 0; m < 32; ++m) {
-        const bool has = lane + 32 * m < n;
-        lv[m] = has ? logits[lane + 32 * m] : 0.f;
-        if (!has) taken |= 1u << m;
-    }
-    float sel[kMaxTerms];
-#pragma unroll
-    for (int r = 0; r < kMaxTerms; ++r) {
-        if (r >= k) break;
-        float v = -INFINITY;
-        int i = 0x7fffffff;
-#pragma unroll
-        for (int m = 0; m < 32; ++m) {
-            if ((taken >> m) & 1u) continue;
-            const float v2 = lv[m];
-            const int i2 = lane + 32 * m;
-            if (v2 > v || (v2 == v && i2 < i)) {
-                v = v2;
-                i = i2;
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
-            const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
-            if (v2 > v || (v2 == v && i2 < i)) {
-                v = v2;
-                i = i2;
-            }
-        }
-        if ((i & 31) == lane) taken |= 1u << (i >> 5);
-        sel[r] = v;
-        if (lane == 0) idx[r] = i;
-    }
-    if (lane == 0) {
-        const float m = sel[0];
-        float e[kMaxTerms];
-        float sum = 0.f;
-#pragma unroll
-        for (int r = 0; r < kMaxTerms; ++r) {
-            if (r >= k) break;
-            e[r] = expf(sel[r] - m);
-            sum += e[r];
-        }
-#pragma unroll
-        for (int r = 0; r < kMaxTerms; ++r) {
-            if (r >= k) break;
-            w[r] = e[r] / sum;
-        }
-    }
+    if (n <= 128)
+        route_warp_n<4>(logits, n, k, idx, w);
+    else
+        route_warp_n<32>(logits, n, k, idx, w);
 }
 
 // Modes: kModeTensor -- rows are 16-byte aligned and each chunk of a warp (32

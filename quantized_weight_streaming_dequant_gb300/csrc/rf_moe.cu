@@ -20,7 +20,8 @@ constexpr int kRouterThreads = 1024;
 constexpr int kMaxTopK = kMaxTerms;
 
 // One CTA: k rounds of a block-wide argmax (largest logit, lowest index on
-// ties), then a softmax over the k selected logits.
+// ties; a NaN logit counts as -inf), then a softmax over the k selected
+// logits.
 __global__ void __launch_bounds__(kRouterThreads) router_kernel(const float *__restrict__ logits,
                                                                 int n_expert, int top_k,
                                                                 int32_t *__restrict__ idx,
@@ -32,7 +33,8 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const float *__r
     __shared__ float s_logit[kMaxTopK];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n_warps = blockDim.x >> 5;
-    const float v0 = tid < n_expert ? logits[tid] : -FLT_MAX;
+    const float lg = tid < n_expert ? logits[tid] : -FLT_MAX;
+    const float v0 = lg != lg ? -INFINITY : lg;   // a NaN logit counts as -inf
     bool taken = tid >= n_expert;
     for (int k = 0; k < top_k; ++k) {
         float v = taken ? -INFINITY : v0;

@@ -293,6 +293,49 @@ def test_moe_route_matches_oracle(rf, n_expert, top_k):
         assert np.allclose(w.cpu().numpy(), w_ref, rtol=1e-6, atol=1e-7)
 
 
+def special_logits(n_expert, trial, rng):
+    """Logits mixing NaN, -inf, signed zeros and numbers (down to a single
+    finite one), for the routing edge cases."""
+    lg = rng.standard_normal(n_expert).astype(np.float32)
+    kind = rng.integers(0, 4, n_expert)
+    lg[kind == 0] = np.nan
+    lg[kind == 1] = -np.inf
+    if trial % 4 == 0:
+        lg[:] = np.nan
+        lg[rng.integers(n_expert)] = 2.0
+    if trial % 4 == 1:
+        lg[:] = np.nan
+        lg[0], lg[-1] = -0.0, 0.0
+    return lg
+
+
+@pytest.mark.parametrize("n_expert,top_k", [(128, 4), (8, 8), (300, 8), (33, 3)])
+def test_route_nan_and_infinite_logits(rf, n_expert, top_k):
+    """A NaN logit counts as -inf: the standalone router and the routing inside
+    the MoE launch both name the oracle's experts (always distinct and in
+    range, even with fewer finite logits than top_k) and the same weights."""
+    rng = np.random.default_rng(n_expert * 31 + top_k)
+    fmt, n_ff, n_embd = syn.Q4_0, 64, 64
+    G = dev_tensor(syn.stacked_experts(fmt, n_expert, n_ff, n_embd, 1))
+    U = dev_tensor(syn.stacked_experts(fmt, n_expert, n_ff, n_embd, 2))
+    D = dev_tensor(syn.stacked_experts(fmt, n_expert, n_embd, n_ff, 3))
+    x = dev_tensor(syn.normal_f32(n_embd, 4))
+    for trial in range(8):
+        lg = special_logits(n_expert, trial, rng)
+        idx_ref, w_ref = oracle.router_topk(lg, top_k)
+        idx, w = rf.moe_route(dev_tensor(lg), top_k)
+        _, ws = rf.moe_ffn(fmt, dev_tensor(lg), top_k, G, U, D, n_ff, n_embd, 0, x)
+        idx2, w2, _ = rf.moe_workspace_views(ws, top_k, n_ff)
+        assert idx.cpu().numpy().tolist() == idx_ref.tolist(), trial
+        assert idx2.cpu().numpy().tolist() == idx_ref.tolist(), trial
+        wa, wb = w.cpu().numpy(), w2.cpu().numpy()
+        assert np.array_equal(np.isnan(wa), np.isnan(w_ref)), trial
+        ok = ~np.isnan(w_ref)
+        assert np.allclose(wa[ok], w_ref[ok], rtol=1e-6, atol=1e-7), trial
+        assert np.array_equal(wa.view(np.uint32), wb.view(np.uint32)), trial
+    assert rf.device_status() == rf.OK
+
+
 def moe_check(rf, fmt, E, n_ff, n_embd, top_k, block_rows, seed):
     G = syn.stacked_experts(fmt, E, n_ff, n_embd, seed)
     U = syn.stacked_experts(fmt, E, n_ff, n_embd, seed + 1)
