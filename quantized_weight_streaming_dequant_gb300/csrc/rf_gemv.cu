@@ -131,6 +131,7 @@ struct KParamsT {
     const XRec *xr_in;
     int32_t route_n, route_k;
     int32_t sched_slot;          // >= 0: dynamic group scheduling (producer mode)
+    int32_t chained;             // launched behind a previous grid (dependency wait)
 };
 using KParamsSmall = KParamsT<4, 4>;
 using KParamsLarge = KParamsT<kMaxJobs, kMaxMaps>;
@@ -699,22 +700,35 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.maps[threadIdx.x]))
                          : "memory");
     }
+    // Routing inside the launch.  A launch that waits on a previous grid, or
+    // whose activations come as digits, ranks its logits first thing (warp 0,
+    // while the other warps copy the job table) so that its weight copies can
+    // start early.  A launch with nothing to wait for ranks them later, while
+    // warps 1.. build the activation digits (route_late, below).
+    int32_t *s_eidx = cnt + 16;
+    float *s_ew = reinterpret_cast<float *>(cnt + 24);
+    const bool route_late = !WS && p.route_logits && !p.chained && !p.xr_in;
+    const bool route_now = p.route_logits && !route_late;
+    if (route_now && warp == 0) route_warp(p.route_logits, p.route_n, p.route_k, s_eidx, s_ew);
     {   // copy the job table out of parameter space in one parallel pass
         const int words = n_jobs * (int)(sizeof(Job) / 4);
         const uint32_t *src = reinterpret_cast<const uint32_t *>(p.jobs);
         uint32_t *dst = reinterpret_cast<uint32_t *>(jobs);
-        for (int i = threadIdx.x; i < words; i += blockDim.x) dst[i] = src[i];
+        const int skip = route_now ? 32 : 0;
+        if ((int)threadIdx.x >= skip)
+            for (int i = (int)threadIdx.x - skip; i < words; i += (int)blockDim.x - skip)
+                dst[i] = src[i];
     }
     fence_barrier_init();
-    int32_t *s_eidx = cnt + 16;
-    float *s_ew = reinterpret_cast<float *>(cnt + 24);
-    if (p.route_logits && warp == 0) route_warp(p.route_logits, p.route_n, p.route_k, s_eidx, s_ew);
     __syncthreads();
     const int32_t *eidx = p.route_logits ? s_eidx : p.expert_idx;
-    if (p.route_logits && blockIdx.x == 0 && (int)threadIdx.x < p.route_k && p.route_idx_out) {
-        p.route_idx_out[threadIdx.x] = s_eidx[threadIdx.x];
-        p.route_w_out[threadIdx.x] = s_ew[threadIdx.x];
-    }
+    auto write_route = [&] {
+        if (blockIdx.x == 0 && (int)threadIdx.x < p.route_k && p.route_idx_out) {
+            p.route_idx_out[threadIdx.x] = s_eidx[threadIdx.x];
+            p.route_w_out[threadIdx.x] = s_ew[threadIdx.x];
+        }
+    };
+    if (route_now) write_route();
 
     uint8_t *my_slots = slots + (size_t)warp * ST * kRows * SLOT;
     uint64_t *my_bars = bars + warp * ST;
@@ -962,12 +976,23 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
                     if (i < n16) dst[i] = t[u];
                 }
             }
+        } else if (route_late && warp == 0) {
+            // Warp 0 ranks the logits while warps 1.. build the digits.  In
+            // flat mode (one thread issues every copy) it then starts the first
+            // stages at once; otherwise the copies start after the barrier.
+            route_warp(p.route_logits, p.route_n, p.route_k, s_eidx, s_ew);
+            if constexpr (FLAT) {
+                __syncwarp();
+                for (; primed < ST && ic.valid; ++primed) prime(primed);
+            }
         } else {
             constexpr int kXPre = 8;
+            const int xt = route_late ? (int)threadIdx.x - 32 : (int)threadIdx.x;
+            const int xn = route_late ? kThreads - 32 : kThreads;
             const int n_rec = p.n_x * nrx;
-            const int passes = (4 * n_rec + kThreads - 1) / kThreads;
+            const int passes = (4 * n_rec + xn - 1) / xn;
             auto pass_src = [&](int ps, bool &active, int &rec) -> const float * {
-                const int idx = ps * kThreads + (int)threadIdx.x;
+                const int idx = ps * xn + xt;
                 active = idx < 4 * n_rec;
                 rec = active ? idx >> 2 : 0;
                 const int sl = rec / nrx, b = rec - sl * nrx;
@@ -982,26 +1007,38 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
                 rec[ps] = 0;
                 if (ps < passes) {
                     const float *xb = pass_src(ps, act[ps], rec[ps]);
-                    xrec_load<FMT>(xb, threadIdx.x & 3, act[ps], v[ps]);
+                    xrec_load<FMT>(xb, xt & 3, act[ps], v[ps]);
                 } else {
 #pragma unroll
                     for (int i = 0; i < 8; ++i) v[ps][i] = 0.f;
                 }
             }
-            for (int s = primed; s < ST && ic.valid; ++s) prime(s);
+            if (!route_late)
+                for (int s = primed; s < ST && ic.valid; ++s) prime(s);
 #pragma unroll
             for (int ps = 0; ps < kXPre; ++ps)
-                if (ps < passes) xrec_build<FMT>(v[ps], threadIdx.x & 3, act[ps], &xrec[rec[ps]]);
+                if (ps < passes) xrec_build<FMT>(v[ps], xt & 3, act[ps], &xrec[rec[ps]]);
             for (int ps = kXPre; ps < passes; ++ps) {
                 bool a = false;
                 int rc = 0;
                 const float *xb = pass_src(ps, a, rc);
                 float w[8];
-                xrec_load<FMT>(xb, threadIdx.x & 3, a, w);
-                xrec_build<FMT>(w, threadIdx.x & 3, a, &xrec[rc]);
+                xrec_load<FMT>(xb, xt & 3, a, w);
+                xrec_build<FMT>(w, xt & 3, a, &xrec[rc]);
             }
         }
         __syncthreads();
+        if (route_late) {
+            write_route();
+            if constexpr (FLAT) {
+                // Every thread keeps its own cursor: bring the other warps'
+                // to where warp 0's priming left its own.
+                if (warp != 0)
+                    for (; primed < ST && ic.valid; ++primed) cursor_advance(jobs, n_jobs, ic, 1, g_hi);
+            } else {
+                for (int s = primed; s < ST && ic.valid; ++s) prime(s);
+            }
+        }
     }
 
     int cs = 0;          // stage of the next chunk to consume
@@ -1649,6 +1686,7 @@ static rf_status launch_merged(const LaunchDesc &d, int nb, int64_t RB, cudaStre
             // Weights may be fetched before the previous grid finishes unless
             // their rows come from a routing result that grid writes.
             p.prefetch_early = (d.pdl && (!d.any_expert || d.route_logits)) ? 1 : 0;
+            p.chained = d.pdl ? 1 : 0;
             p.route_logits = d.route_logits;
             p.route_idx_out = d.route_idx_out;
             p.route_w_out = d.route_w_out;
