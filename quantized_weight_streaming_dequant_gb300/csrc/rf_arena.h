@@ -31,6 +31,12 @@ struct rf_arena {
     size_t last_stride = 0;
     rf_stream_stats stats = {};
     int32_t *route_host = nullptr;    // page-locked: routing ids read back for planning
+    // Lane streams: the launches of one walk's blocks go round-robin to them,
+    // so that blocks whose copies have landed run side by side.
+    static constexpr int kLanes = 4;
+    cudaStream_t lane[kLanes] = {};
+    cudaEvent_t lane_start = nullptr;         // the caller's stream at the walk's start
+    cudaEvent_t lane_done[kLanes] = {};       // a lane's last launch of the walk
     std::mutex mu;
 };
 
@@ -58,5 +64,20 @@ rf_status arena_fetch(rf_arena *a, cudaStream_t s, const void *src, size_t bytes
 // Every launch that reads `slot` is enqueued on `s`: the slot is free once
 // they have run.
 rf_status arena_release(rf_arena *a, cudaStream_t s, int slot);
+
+// Fan-out of a walk's launches over the lane streams.  begin() records the
+// caller's stream; stream(i) is the stream for the walk's i-th block (a lane,
+// which first waits for the caller's stream); end() makes the caller's stream
+// wait for every lane used.  With `on` false everything stays on the
+// caller's stream.
+struct LaneFan {
+    rf_arena *a;
+    cudaStream_t s;
+    bool on;
+    unsigned used = 0;
+    rf_status begin();
+    rf_status stream(int64_t i, cudaStream_t *out);
+    rf_status end();
+};
 
 }  // namespace rf

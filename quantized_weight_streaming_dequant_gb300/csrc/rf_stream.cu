@@ -12,9 +12,13 @@
 //
 // GB300 form: the arena is one device allocation cut into depth+1 slots.  The
 // prefetcher is a dedicated copy stream; each block is a cudaMemcpyAsync from
-// page-locked host memory into its slot, followed by an event that the compute
-// stream waits on before the fused GEMV reads the slot.  After the GEMV a
-// "slot free" event is recorded on the compute stream; the copy that next
+// page-locked host memory into its slot, followed by an event that the
+// block's GEMV waits on before it reads the slot.  The GEMVs of a walk of 8
+// or more small blocks go round-robin to the arena's lane streams (rows are
+// disjoint), so a block whose copy has landed does not queue behind the
+// previous block's GEMV; the lanes start after the caller's stream and the
+// caller's stream waits for all of them at the end of the walk.  After a
+// GEMV a "slot free" event is recorded on its lane; the copy that next
 // reuses the slot waits on it.  Reservations and back-pressure are therefore
 // stream-ordered dependencies: the host enqueues a whole walk without
 // blocking, and consecutive calls keep the copy engine busy across call
@@ -110,6 +114,38 @@ rf_status arena_release(rf_arena *a, cudaStream_t s, int slot)
     return RF_OK;
 }
 
+rf_status LaneFan::begin()
+{
+    if (on && cudaEventRecord(a->lane_start, s) != cudaSuccess) return RF_ERR_CUDA;
+    return RF_OK;
+}
+
+rf_status LaneFan::stream(int64_t i, cudaStream_t *out)
+{
+    if (!on) {
+        *out = s;
+        return RF_OK;
+    }
+    const int l = (int)(i % rf_arena::kLanes);
+    if (!(used & (1u << l))) {
+        if (cudaStreamWaitEvent(a->lane[l], a->lane_start, 0) != cudaSuccess) return RF_ERR_CUDA;
+        used |= 1u << l;
+    }
+    *out = a->lane[l];
+    return RF_OK;
+}
+
+rf_status LaneFan::end()
+{
+    for (int l = 0; l < rf_arena::kLanes; ++l)
+        if (used & (1u << l))
+            if (cudaEventRecord(a->lane_done[l], a->lane[l]) != cudaSuccess ||
+                cudaStreamWaitEvent(s, a->lane_done[l], 0) != cudaSuccess)
+                return RF_ERR_CUDA;
+    used = 0;
+    return RF_OK;
+}
+
 }  // namespace rf
 
 extern "C" {
@@ -167,11 +203,19 @@ rf_status rf_arena_create(size_t bytes, rf_arena **out)
         delete a;
         return RF_ERR_CUDA;
     }
-    if (cudaEventCreateWithFlags(&a->fork, cudaEventDisableTiming) != cudaSuccess) {
+    if (cudaEventCreateWithFlags(&a->fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&a->lane_start, cudaEventDisableTiming) != cudaSuccess) {
         cudaGetLastError();
         rf_arena_destroy(a);
         return RF_ERR_CUDA;
     }
+    for (int l = 0; l < rf_arena::kLanes; ++l)
+        if (cudaStreamCreateWithFlags(&a->lane[l], cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&a->lane_done[l], cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();
+            rf_arena_destroy(a);
+            return RF_ERR_CUDA;
+        }
     if (cudaMallocHost(&a->route_host, sizeof(int32_t) * kMaxTerms) != cudaSuccess) {
         cudaGetLastError();
         a->route_host = nullptr;
@@ -201,7 +245,14 @@ void rf_arena_destroy(rf_arena *a)
     // wait for both before freeing.  (Launches of captured graphs are the
     // caller's to finish.)
     if (a->copy_stream) cudaStreamSynchronize(a->copy_stream);
+    for (int l = 0; l < rf_arena::kLanes; ++l)
+        if (a->lane[l]) cudaStreamSynchronize(a->lane[l]);
     if (a->fork) cudaEventDestroy(a->fork);
+    if (a->lane_start) cudaEventDestroy(a->lane_start);
+    for (int l = 0; l < rf_arena::kLanes; ++l) {
+        if (a->lane_done[l]) cudaEventDestroy(a->lane_done[l]);
+        if (a->lane[l]) cudaStreamDestroy(a->lane[l]);
+    }
     for (int i = 0; i < rf_arena::kMaxSlots; ++i) {
         if (a->freed[i]) {
             if (a->freed_recorded[i] && a->epoch == 0) cudaEventSynchronize(a->freed[i]);
@@ -256,12 +307,22 @@ rf_status rf_stream_linear(int fmt, const void *host_W, int64_t in_dim, int64_t 
     size_t peak = 0;
     rf_stream_plan(fmt, in_dim, n_rows, block_rows, depth, a->bytes, nullptr, nullptr, &peak);
 
+    // Blocks run side by side on the lane streams (their rows are disjoint)
+    // when they are small (at most 1 MiB: a block's GEMV, a few CTAs, then
+    // takes longer than its copy) and the walk has at least two blocks per
+    // lane (a fan-out costs a fork and a join per walk, which a short walk
+    // does not earn back; in a CUDA graph each is a cross-branch dependency).
+    LaneFan fan{a, s,
+                eff * rb <= (int64_t)(1 << 20) && (n_rows + eff - 1) / eff >= 2 * rf_arena::kLanes};
+    if (const rf_status st = fan.begin()) return st;
     int64_t blocks = 0;
     for (int64_t r0 = row_start; r0 < row_end; r0 += eff) {
         const int64_t nr = std::min(eff, row_end - r0);
         int slot = 0;
         uint8_t *dst = nullptr;
-        if (const rf_status st = arena_fetch(a, s, hw + r0 * rb, (size_t)(nr * rb), &slot, &dst))
+        cudaStream_t cs = s;
+        if (const rf_status st = fan.stream(blocks, &cs)) return st;
+        if (const rf_status st = arena_fetch(a, cs, hw + r0 * rb, (size_t)(nr * rb), &slot, &dst))
             return st;
         Job J;
         std::memset(&J, 0, sizeof(J));
@@ -277,12 +338,13 @@ rf_status rf_stream_linear(int fmt, const void *host_W, int64_t in_dim, int64_t 
         d.n_jobs = 1;
         d.x[0] = x;
         d.n_x = 1;
-        const rf_status st = launch_rowwin(d, s);
+        const rf_status st = launch_rowwin(d, cs);
         if (st != RF_OK) return st;
         // Retire: the slot is free once this GEMV has run.
-        if (const rf_status st2 = arena_release(a, s, slot)) return st2;
+        if (const rf_status st2 = arena_release(a, cs, slot)) return st2;
         ++blocks;
     }
+    if (const rf_status st = fan.end()) return st;
     a->stats.calls += 1;
     a->stats.blocks += (uint64_t)blocks;
     a->stats.peak_bytes = std::max<uint64_t>(a->stats.peak_bytes, peak);

@@ -241,7 +241,8 @@ def test_stream_linear_captured_in_cuda_graph(rf):
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s):
-            arena.stream_linear(fmt, host, in_dim, 0, 600, 96, 3, xd, yg[:600], stream=s)
+            # 10 blocks (fanned out over the lane streams), then 4 (one stream)
+            arena.stream_linear(fmt, host, in_dim, 0, 600, 64, 3, xd, yg[:600], stream=s)
             arena.stream_linear(fmt, host, in_dim, 600, rows, 128, 2, xd, yg[600:], stream=s)
         for rep in range(3):
             yg.fill_(float("nan"))
@@ -253,6 +254,54 @@ def test_stream_linear_captured_in_cuda_graph(rf):
         again = arena.stream_linear(fmt, host, in_dim, 0, rows, 64, 4, xd).cpu().numpy()
         assert np.array_equal(bits(again), bits(eager))
         del g
+    finally:
+        torch.cuda.synchronize()
+        arena.close()
+
+
+@pytest.mark.parametrize("captured", [False, True])
+def test_stream_linear_lanes_ordered_with_caller_stream(rf, captured):
+    """A walk of many blocks (fanned out over the arena's lane streams) sees
+    activations written on the caller's stream just before it, and work on the
+    caller's stream just after it sees every block's rows."""
+    import torch
+    fmt, rows, in_dim = syn.Q4_0, 4096, 4096
+    W = syn.quant_matrix(fmt, rows, in_dim, seed=93)
+    xs = [dev_tensor(syn.normal_f32(in_dim, 94 + i)) for i in range(3)]
+    Wd = dev_tensor(W)
+    want = [rf.gemv(fmt, Wd, 0, rows, in_dim, x).cpu().numpy() for x in xs]
+    host = torch.from_numpy(W).pin_memory()
+    arena = rf.Arena(256 << 20)
+    s = torch.cuda.Stream()
+    x = torch.empty(in_dim, device="cuda")
+    y = torch.empty(rows, device="cuda")
+    big = torch.empty(64 << 20, device="cuda")
+    outs = [torch.empty(rows, device="cuda") for _ in xs]
+
+    def walk():
+        for i, xi in enumerate(xs):
+            big.fill_(float(i))                    # a slow kernel ahead of x
+            x.copy_(xi)
+            arena.stream_linear(fmt, host, in_dim, 0, rows, 64, 4, x, y, stream=s)
+            outs[i].copy_(y)
+            y.fill_(float("nan"))
+    try:
+        torch.cuda.synchronize()
+        if captured:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                walk()
+            for _ in range(2):
+                with torch.cuda.stream(s):
+                    g.replay()
+                torch.cuda.synchronize()
+            del g
+        else:
+            with torch.cuda.stream(s):
+                walk()
+            torch.cuda.synchronize()
+        for i in range(len(xs)):
+            assert np.array_equal(bits(outs[i].cpu().numpy()), bits(want[i])), i
     finally:
         torch.cuda.synchronize()
         arena.close()
