@@ -888,6 +888,21 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
     } else if (p.prefetch_early) {
         for (; primed < ST && ic.valid; ++primed) prime(primed);
     }
+    // A chained launch brings the activations it will read into L2 while the
+    // previous grid drains (L2 is the coherence point, so lines that grid
+    // still writes stay current): each consumer warp its own K range in
+    // producer mode, else the whole vectors spread over the CTA.  Activations
+    // the weight stream has evicted then cost an L2 hit after the wait
+    // instead of a DRAM round trip.
+    if (p.chained && !p.xr_in) {
+        const int lo = WS ? kb_lo * F::RPB * 32 : 0;
+        const int hi = WS ? kb_hi * F::RPB * 32 : nrx * 32;
+        const int t0 = WS ? lane : (int)threadIdx.x;
+        const int nt = WS ? 32 : kThreads;
+        for (int sl = 0; sl < p.n_x; ++sl)
+            for (int e = lo + 32 * t0; e < hi; e += 32 * nt)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(p.x[sl] + e));
+    }
     pdl_launch_dependents();
     pdl_wait();
 
