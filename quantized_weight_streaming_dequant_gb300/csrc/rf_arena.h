@@ -65,6 +65,19 @@ rf_status arena_fetch(rf_arena *a, cudaStream_t s, const void *src, size_t bytes
 // they have run.
 rf_status arena_release(rf_arena *a, cudaStream_t s, int slot);
 
+// A walk whose n blocks (n <= slots) all fit in the ring at once: takes n
+// consecutive slots (from the next slot when they do not wrap, else from
+// slot 0), copies the blocks -- contiguous host rows: n-1 blocks of
+// block_bytes, then last_bytes -- with one copy (two when the slot pitch
+// exceeds the block) after the slots' previous readers, and makes `s` wait
+// for it.  Block i lands at *base + i * slot pitch; *first_slot is the first
+// slot taken.
+rf_status arena_fetch_run(rf_arena *a, cudaStream_t s, const void *src, size_t block_bytes,
+                          int n, size_t last_bytes, int *first_slot, uint8_t **base);
+
+// Releases the n slots from first_slot once the launches on `s` have run.
+rf_status arena_release_run(rf_arena *a, cudaStream_t s, int first_slot, int n);
+
 // Fan-out of a walk's launches over the lane streams.  begin() records the
 // caller's stream; stream(i) is the stream for the walk's i-th block (a lane,
 // which first waits for the caller's stream); end() makes the caller's stream

@@ -114,6 +114,46 @@ rf_status arena_release(rf_arena *a, cudaStream_t s, int slot)
     return RF_OK;
 }
 
+rf_status arena_fetch_run(rf_arena *a, cudaStream_t s, const void *src, size_t block_bytes,
+                          int n, size_t last_bytes, int *first_slot, uint8_t **base)
+{
+    const int first = a->next_slot + n <= a->last_slots ? a->next_slot : 0;
+    a->next_slot = (first + n) % a->last_slots;
+    for (int k = first; k < first + n; ++k)
+        if (a->freed_recorded[k] && cudaStreamWaitEvent(a->copy_stream, a->freed[k], 0) != cudaSuccess)
+            return RF_ERR_CUDA;
+    uint8_t *dst = a->base + (size_t)first * a->last_stride;
+    const uint8_t *hsrc = static_cast<const uint8_t *>(src);
+    const size_t full = (size_t)(n - 1) * block_bytes;
+    if (a->last_stride == block_bytes) {
+        // Slots packed back to back: the whole run is one contiguous copy.
+        if (cudaMemcpyAsync(dst, hsrc, full + last_bytes, cudaMemcpyHostToDevice,
+                            a->copy_stream) != cudaSuccess)
+            return RF_ERR_CUDA;
+    } else {
+        if ((n > 1 && cudaMemcpy2DAsync(dst, a->last_stride, hsrc, block_bytes, block_bytes,
+                                        (size_t)(n - 1), cudaMemcpyHostToDevice,
+                                        a->copy_stream) != cudaSuccess) ||
+            cudaMemcpyAsync(dst + (size_t)(n - 1) * a->last_stride, hsrc + full, last_bytes,
+                            cudaMemcpyHostToDevice, a->copy_stream) != cudaSuccess)
+            return RF_ERR_CUDA;
+    }
+    if (cudaEventRecord(a->copied[first], a->copy_stream) != cudaSuccess ||
+        cudaStreamWaitEvent(s, a->copied[first], 0) != cudaSuccess)
+        return RF_ERR_CUDA;
+    a->stats.bytes_copied += full + last_bytes;
+    *first_slot = first;
+    *base = dst;
+    return RF_OK;
+}
+
+rf_status arena_release_run(rf_arena *a, cudaStream_t s, int first_slot, int n)
+{
+    for (int k = first_slot; k < first_slot + n; ++k)
+        if (const rf_status st = arena_release(a, s, k)) return st;
+    return RF_OK;
+}
+
 rf_status LaneFan::begin()
 {
     if (on && cudaEventRecord(a->lane_start, s) != cudaSuccess) return RF_ERR_CUDA;
@@ -306,6 +346,50 @@ rf_status rf_stream_linear(int fmt, const void *host_W, int64_t in_dim, int64_t 
     const uint8_t *hw = static_cast<const uint8_t *>(host_W);
     size_t peak = 0;
     rf_stream_plan(fmt, in_dim, n_rows, block_rows, depth, a->bytes, nullptr, nullptr, &peak);
+
+    // A walk whose blocks all fit in the ring at once (at most depth+1 of
+    // them) needs no slot reuse: its blocks go over the link as one copy and
+    // through one launch (each block its own window: with packed slots they
+    // are consecutive rows of one matrix and merge into one window; else at
+    // most 16 distinct slot bases, the tensor maps a launch holds).  Per-block
+    // copies and launches would only add their fixed costs.
+    const int64_t nblk = (n_rows + eff - 1) / eff;
+    const bool packed = stride == (size_t)(eff * rb);
+    if (nblk > 1 && nblk <= slots && (packed || nblk <= 16)) {
+        int first = 0;
+        uint8_t *base = nullptr;
+        const int64_t last_rows = n_rows - (nblk - 1) * eff;
+        if (const rf_status st = arena_fetch_run(a, s, hw + row_start * rb, (size_t)(eff * rb),
+                                                 (int)nblk, (size_t)(last_rows * rb), &first, &base))
+            return st;
+        static thread_local Job run_jobs[rf_arena::kMaxSlots];
+        for (int64_t i = 0; i < nblk; ++i) {
+            Job &J = run_jobs[i];
+            std::memset(&J, 0, sizeof(J));
+            J.term[0] = Term{packed ? base : base + (size_t)i * stride, 0, -1, 0, 0};
+            J.row0 = packed ? i * eff : 0;
+            J.y = y + i * eff;
+            J.n_rows = (int32_t)(i + 1 < nblk ? eff : last_rows);
+            J.n_terms = 1;
+            J.combine = kCombineSum;
+        }
+        LaunchDesc d;
+        d.fmt = fmt;
+        d.in_dim = in_dim;
+        d.jobs = run_jobs;
+        d.n_jobs = (int)nblk;
+        d.x[0] = x;
+        d.n_x = 1;
+        if (const rf_status st = launch_rowwin(d, s)) return st;
+        if (const rf_status st = arena_release_run(a, s, first, (int)nblk)) return st;
+        a->stats.calls += 1;
+        a->stats.blocks += (uint64_t)nblk;
+        a->stats.peak_bytes = std::max<uint64_t>(a->stats.peak_bytes, peak);
+        a->stats.slot_bytes = stride;
+        a->stats.slots = slots;
+        a->stats.last_block_rows = (int32_t)eff;
+        return RF_OK;
+    }
 
     // Blocks run side by side on the lane streams (their rows are disjoint)
     // when they are small (at most 1 MiB: a block's GEMV, a few CTAs, then

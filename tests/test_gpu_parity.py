@@ -259,6 +259,48 @@ def test_stream_linear_captured_in_cuda_graph(rf):
         arena.close()
 
 
+@pytest.mark.parametrize("fmt", FMTS)
+def test_stream_linear_whole_walk_in_ring(rf, fmt):
+    """Walks whose blocks all fit in the ring at once take one copy and one
+    launch: packed slots (128-row blocks, 7 blocks in 8 slots) and slots with
+    a pitch above the block (7-row blocks, 15 blocks in 16 slots); bit-exact
+    against the resident GEMV, eager twice in a row and replayed from a graph."""
+    import torch
+    in_dim = 2880 if fmt == syn.MXFP4 else 2048
+    W = syn.quant_matrix(fmt, 900, in_dim, seed=41)
+    x = dev_tensor(syn.normal_f32(in_dim, 42))
+    Wd = dev_tensor(W)
+    host = torch.from_numpy(W).pin_memory()
+    arena = rf.Arena(256 << 20)
+    s = torch.cuda.Stream()
+    try:
+        for r0, r1, block_rows, depth in ((7, 900, 128, 7), (3, 103, 7, 15)):
+            want = rf.gemv(fmt, Wd, r0, r1, in_dim, x).cpu().numpy()
+            copied0 = arena.stats()["bytes_copied"]
+            for _ in range(2):
+                y = arena.stream_linear(fmt, host, in_dim, r0, r1, block_rows, depth, x)
+                assert np.array_equal(bits(y.cpu().numpy()), bits(want)), (block_rows, depth)
+            st = arena.stats()
+            assert st["last_block_rows"] == block_rows and st["slots"] == depth + 1
+            assert st["bytes_copied"] - copied0 == 2 * (r1 - r0) * rf.row_bytes(fmt, in_dim)
+            yg = torch.full((r1 - r0,), float("nan"), device="cuda")
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                arena.stream_linear(fmt, host, in_dim, r0, r1, block_rows, depth, x, yg, stream=s)
+            for _ in range(2):
+                yg.fill_(float("nan"))
+                torch.cuda.synchronize()
+                with torch.cuda.stream(s):
+                    g.replay()
+                torch.cuda.synchronize()
+                assert np.array_equal(bits(yg.cpu().numpy()), bits(want)), (block_rows, "graph")
+            del g
+    finally:
+        torch.cuda.synchronize()
+        arena.close()
+
+
 @pytest.mark.parametrize("captured", [False, True])
 def test_stream_linear_lanes_ordered_with_caller_stream(rf, captured):
     """A walk of many blocks (fanned out over the arena's lane streams) sees
