@@ -668,8 +668,11 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
     const int n_jobs = p.n_jobs;
 
     const int G_total = p.total_groups;
-    const int g_lo = (int)((int64_t)blockIdx.x * G_total / gridDim.x);
-    const int g_hi = (int)((int64_t)(blockIdx.x + 1) * G_total / gridDim.x);
+    // Static ranges: every CTA `base` groups, the first `extra` CTAs one
+    // more (with two CTAs per SM the extras then land on distinct SMs).
+    const int g_base = G_total / (int)gridDim.x, g_extra = G_total - g_base * (int)gridDim.x;
+    const int g_lo = (int)blockIdx.x * g_base + min((int)blockIdx.x, g_extra);
+    const int g_hi = g_lo + g_base + ((int)blockIdx.x < g_extra ? 1 : 0);
 
     // This warp's K part, in blocks.
     // Split granularity: the format's 16-byte group when rows are 16-byte
@@ -931,7 +934,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
                     at[u] = 0;
                     if (i < n16) {
                         const int r = i / kV, h = i - kV * r;
-                        const int sl = r / nrw, k = r - sl * nrw;
+                        const int sl = p.n_x == 1 ? 0 : r / nrw, k = r - sl * nrw;
                         at[u] = (sl * nrx + rlo + k) * kV + h;
                         t[u] = src[at[u]];
                     }
@@ -947,7 +950,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
                 const int r = ps * 8 + (lane >> 2);
                 active = r < total;
                 const int rr = active ? r : 0;
-                const int sl = rr / nrw, k = rr - sl * nrw;
+                const int sl = p.n_x == 1 ? 0 : rr / nrw, k = rr - sl * nrw;
                 rec = sl * nrx + rlo + k;
                 return p.x[sl] + 32 * (int64_t)(rlo + k);
             };
@@ -1010,7 +1013,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
                 const int idx = ps * xn + xt;
                 active = idx < 4 * n_rec;
                 rec = active ? idx >> 2 : 0;
-                const int sl = rec / nrx, b = rec - sl * nrx;
+                const int sl = p.n_x == 1 ? 0 : rec / nrx, b = rec - sl * nrx;
                 return p.x[sl] + 32 * (int64_t)b;
             };
             float v[kXPre][8];
@@ -1677,8 +1680,9 @@ static rf_status launch_merged(const LaunchDesc &d, int nb, int64_t RB, cudaStre
         // Other modes: the same number of groups (or one fewer) on every CTA.
         const int max_grid = ctas_per_sm * di.sms;
         const int per_cta = (total + max_grid - 1) / max_grid;
-        const int grid = mode == kModeTensorWS ? std::min(total, max_grid)
-                                               : (total + per_cta - 1) / per_cta;
+        const int grid = (mode == kModeTensorWS || (mode == kModeFlat && ctas_per_sm == 2))
+                             ? std::min(total, max_grid)
+                             : (total + per_cta - 1) / per_cta;
         const int sched_slot =
             mode == kModeTensorWS && total > grid
                 ? (int)(g_sched_seq.fetch_add(1, std::memory_order_relaxed) % kSchedSlots)
