@@ -96,7 +96,7 @@ struct FmtT<RF_MXFP4> {
 // aligned); it has RPB = 8 activation digit records, one per sub-block.
 template <>
 struct FmtT<RF_Q4_K> {
-    static constexpr int BS = 144, HDR = 4, QW = 4, G = 1, RPB = 8;
+    static constexpr int BS = 144, G = 1, RPB = 8;
 };
 
 constexpr int kMaxMaps = 16;   // distinct weight tensors per launch (tensor-map path)
@@ -423,18 +423,21 @@ template <int FMT>
 __device__ __forceinline__ float compute_group(const GroupRegs<FMT> &r, const XRec *xr, float acc)
 {
     using F = FmtT<FMT>;
-    if constexpr (FMT == RF_Q4_K) return q4k_superblock(r.v, xr, acc);
+    if constexpr (FMT == RF_Q4_K) {
+        return q4k_superblock(r.v, xr, acc);
+    } else {
 #pragma unroll
-    for (int b = 0; b < F::G; ++b) {
-        const int o = b * F::BS;
-        const uint32_t hdr = word_at(r.v, o);
-        uint32_t q[F::QW];
+        for (int b = 0; b < F::G; ++b) {
+            const int o = b * F::BS;
+            const uint32_t hdr = word_at(r.v, o);
+            uint32_t q[F::QW];
 #pragma unroll
-        for (int k = 0; k < F::QW; ++k) q[k] = word_at(r.v, o + F::HDR + 4 * k);
-        const XRec &x = xr[b];
-        acc = fmaf(block_idot<FMT>(q, x), block_scale<FMT>(hdr, x.scale), acc);
+            for (int k = 0; k < F::QW; ++k) q[k] = word_at(r.v, o + F::HDR + 4 * k);
+            const XRec &x = xr[b];
+            acc = fmaf(block_idot<FMT>(q, x), block_scale<FMT>(hdr, x.scale), acc);
+        }
+        return acc;
     }
-    return acc;
 }
 
 // Aligned chunk: `kn` blocks (a multiple of G) at a 16-byte aligned address.
@@ -470,27 +473,28 @@ __device__ __forceinline__ float chunk_generic(const uint8_t *slot, int phi, int
             acc = q4k_superblock(w, xr + b * F::RPB, acc);
         }
         return acc;
-    }
-    for (int b = 0; b < kn; ++b) {
-        const int o = phi + b * F::BS;
-        uint32_t hdr;
-        if constexpr (FMT == RF_MXFP4)
-            hdr = slot[o];
-        else
-            hdr = *reinterpret_cast<const uint16_t *>(slot + o);   // o is even
-        const int qa = o + F::HDR;
-        const uint32_t *wp = reinterpret_cast<const uint32_t *>(slot + (qa & ~3));
-        const int sh = 8 * (qa & 3);
-        uint32_t w[F::QW + 1];
+    } else {
+        for (int b = 0; b < kn; ++b) {
+            const int o = phi + b * F::BS;
+            uint32_t hdr;
+            if constexpr (FMT == RF_MXFP4)
+                hdr = slot[o];
+            else
+                hdr = *reinterpret_cast<const uint16_t *>(slot + o);   // o is even
+            const int qa = o + F::HDR;
+            const uint32_t *wp = reinterpret_cast<const uint32_t *>(slot + (qa & ~3));
+            const int sh = 8 * (qa & 3);
+            uint32_t w[F::QW + 1];
 #pragma unroll
-        for (int k = 0; k <= F::QW; ++k) w[k] = wp[k];
-        uint32_t q[F::QW];
+            for (int k = 0; k <= F::QW; ++k) w[k] = wp[k];
+            uint32_t q[F::QW];
 #pragma unroll
-        for (int k = 0; k < F::QW; ++k) q[k] = __funnelshift_r(w[k], w[k + 1], sh);
-        const XRec &r = xr[b];
-        acc = fmaf(block_idot<FMT>(q, r), block_scale<FMT>(hdr, r.scale), acc);
+            for (int k = 0; k < F::QW; ++k) q[k] = __funnelshift_r(w[k], w[k + 1], sh);
+            const XRec &r = xr[b];
+            acc = fmaf(block_idot<FMT>(q, r), block_scale<FMT>(hdr, r.scale), acc);
+        }
+        return acc;
     }
-    return acc;
 }
 
 // Walks the (group, term, chunk) items of one warp in order.
