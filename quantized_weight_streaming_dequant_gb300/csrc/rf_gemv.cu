@@ -15,14 +15,14 @@
 //     format's alignment group, nG = ceil(nb/G)); the CTA sums the 8 warp
 //     partials of a row in warp order.  The split depends only on (format,
 //     in_dim), so a row's result is the same in every window and every launch.
-//   * Weights move global -> shared with 1-D bulk copies (TMA), one copy per
-//     lane per chunk of kc blocks, into a per-warp ring of `stages` slots
-//     guarded by mbarriers (expect_tx byte counts).  A copy starts at the
-//     16-byte boundary at or before the chunk and ends at the one at or after
-//     it, so any row alignment works; rows that are 16-byte aligned (row bytes
-//     a multiple of 16) are copied exactly and decoded with static 16-byte
-//     shared loads.  Chunk and slot sizes are launch parameters chosen so that
-//     two CTAs fit on an SM when shared memory allows.
+//   * Weights move global -> shared through rings of `stages` slots guarded
+//     by mbarriers, in one of three modes chosen per launch from the row
+//     bytes: rows that are 16-byte aligned go as 2-D tensor copies (32 rows x
+//     one group of blocks per warp chunk) issued by a ninth, producer warp;
+//     misaligned rows whose 32-row group fits a stage go as one 1-D bulk copy
+//     per (group, term) into a CTA-wide ring; other rows, and weights in mapped
+//     host memory, go as 16-byte cp.async per lane, rounded out to 16-byte
+//     boundaries.  Slot sizes and ring depths are launch parameters.
 //   * Integer dot products.  Each 32-element activation block is turned once
 //     per CTA into a fixed-point integer X = rint(x * 2^s) with |X| < 2^15
 //     (s from the block maximum) split into two byte planes.  The block dot
@@ -612,27 +612,25 @@ __device__ __forceinline__ void route_warp(const float *__restrict__ logits, int
         route_warp_n<32>(logits, n, k, idx, w);
 }
 
-// Modes: kModeTensor -- rows are 16-byte aligned and each chunk of a warp (32
-// rows x kc blocks) is one 2-D tensor copy issued by lane 0.  kModeFlat --
-// one 1-D bulk copy per (group, term) into a CTA-wide ring.  kModePerLane -- any
-// alignment; each lane copies its own row's chunk with a 1-D bulk copy.
-// Minimum CTAs per SM the register budget is sized for: 272-byte aligned
-// chunks (Q8_0, MXFP4) need more registers and their shared memory allows
-// one CTA per SM anyway.
-// kModeTensorWS -- tensor copies issued by a ninth, producer warp (lane w feeds
-// warp w's ring, waiting on the ring's "slot released" barriers), so the eight
-// consumer warps only wait, decode and accumulate.
-constexpr int kModePerLane = 0, kModeTensor = 1, kModeFlat = 2, kModeTensorWS = 3;
+// Modes: kModeTensorWS -- rows are 16-byte aligned; each chunk of a warp (32
+// rows x one group of blocks) is one 2-D tensor copy issued by a ninth,
+// producer warp (lane w feeds warp w's ring, waiting on the ring's "slot
+// released" barriers), so the eight consumer warps only wait, decode and
+// accumulate.  kModeFlat -- one 1-D bulk copy per (group, term) into a
+// CTA-wide ring.  kModePerLane -- any alignment (and mapped host memory);
+// the warp copies its rows' chunks with 16-byte cp.async.
+constexpr int kModePerLane = 0, kModeFlat = 2, kModeTensorWS = 3;
 
 template <int MODE>
 constexpr int threads_of() { return MODE == kModeTensorWS ? kThreads + 32 : kThreads; }
 
+// Minimum CTAs per SM the register budget is sized for: 272-byte aligned
+// chunks (Q8_0, MXFP4) need more registers and their shared memory allows
+// one CTA per SM anyway.
 template <int FMT, int MODE>
 constexpr int min_ctas()
 {
-    return ((MODE == kModeTensor || MODE == kModeTensorWS) && FMT != RF_Q4_0 && FMT != RF_Q4_K)
-               ? 1
-               : 2;
+    return (MODE == kModeTensorWS && FMT != RF_Q4_0 && FMT != RF_Q4_K) ? 1 : 2;
 }
 
 template <int FMT, int MODE, class KP>
@@ -641,7 +639,6 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
 {
     using F = FmtT<FMT>;
     constexpr bool WS = MODE == kModeTensorWS;
-    constexpr bool TMA = MODE == kModeTensor || WS;
     constexpr bool FLAT = MODE == kModeFlat;
     extern __shared__ __align__(128) uint8_t smem[];
 
@@ -699,10 +696,10 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
             mbar_init(&ebars[warp * ST + lane], 1);
         }
     } else {
-        if (lane < ST) mbar_init(&bars[warp * ST + lane], TMA ? 1 : 32);
+        if (lane < ST) mbar_init(&bars[warp * ST + lane], 32);
     }
     if (threadIdx.x < kCntInts) cnt[threadIdx.x] = 0;
-    if constexpr (TMA) {
+    if constexpr (WS) {
         if ((int)threadIdx.x < p.n_maps)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.maps[threadIdx.x]))
                          : "memory");
@@ -744,40 +741,29 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
     if (ic.valid) cursor_fix_job(jobs, n_jobs, ic);
     int is = 0;   // stage of the next copy
 
+    // Per-lane mode: row r's chunk, rounded out to 16-byte boundaries, goes
+    // to row r's slot; the warp copies one row at a time, lane i taking its
+    // i-th 16 bytes, so each copy instruction reads contiguous bytes (which
+    // matters most over the host link).
     auto issue = [&](const Cursor &cu) {
         uint64_t *bar = &my_bars[is];
         uint8_t *dst = my_slots + (size_t)is * kRows * SLOT;
         if (++is == ST) is = 0;
         const Job &J = jobs[cu.j];
-        if constexpr (TMA) {
-            if (lane == 0) {
-                const Term &T = J.term[cu.t];
-                int64_t y = J.row0 + (int64_t)(cu.g - J.group_begin) * kRows;
-                if (T.expert_slot >= 0) y += (int64_t)eidx[T.expert_slot] * J.expert_rows;
-                const int x = (kb_lo + cu.c * KC) * F::BS / 2;   // uint16 units
-                mbar_arrive_expect_tx(bar, (uint32_t)(kRows * SLOT));
-                tma_2d_g2s(dst, &p.maps[T.tmap], x, (int)y, bar);
-            }
-        } else {
-            // Row r's chunk, rounded out to 16-byte boundaries, goes to row r's
-            // slot; the warp copies one row at a time, lane i taking its i-th
-            // 16 bytes, so each copy instruction reads contiguous bytes (which
-            // matters most over the host link).
-            const int64_t rel0 = (int64_t)(cu.g - J.group_begin) * kRows;
-            const int nr = (int)min((int64_t)kRows, (int64_t)J.n_rows - rel0);
-            const uint8_t *W = term_matrix(eidx, J, cu.t, RB);
-            const int kb = kb_lo + cu.c * KC;
-            const int kn = min(KC, kb_hi - kb);
-            uintptr_t s = reinterpret_cast<uintptr_t>(W + (J.row0 + rel0) * RB + (int64_t)kb * F::BS);
-            for (int r = 0; r < nr; ++r, s += (uintptr_t)RB) {
-                const uintptr_t a = s & ~(uintptr_t)15;
-                const int n16 = (int)(((s + (uintptr_t)kn * F::BS + 15) & ~(uintptr_t)15) - a) >> 4;
-                for (int i = lane; i < n16; i += 32)
-                    cp_async16(dst + (size_t)r * SLOT + 16 * i,
-                               reinterpret_cast<const void *>(a + 16 * (uintptr_t)i));
-            }
-            cp_async_arrive(bar);
+        const int64_t rel0 = (int64_t)(cu.g - J.group_begin) * kRows;
+        const int nr = (int)min((int64_t)kRows, (int64_t)J.n_rows - rel0);
+        const uint8_t *W = term_matrix(eidx, J, cu.t, RB);
+        const int kb = kb_lo + cu.c * KC;
+        const int kn = min(KC, kb_hi - kb);
+        uintptr_t s = reinterpret_cast<uintptr_t>(W + (J.row0 + rel0) * RB + (int64_t)kb * F::BS);
+        for (int r = 0; r < nr; ++r, s += (uintptr_t)RB) {
+            const uintptr_t a = s & ~(uintptr_t)15;
+            const int n16 = (int)(((s + (uintptr_t)kn * F::BS + 15) & ~(uintptr_t)15) - a) >> 4;
+            for (int i = lane; i < n16; i += 32)
+                cp_async16(dst + (size_t)r * SLOT + 16 * i,
+                           reinterpret_cast<const void *>(a + 16 * (uintptr_t)i));
         }
+        cp_async_arrive(bar);
     };
 
     // Flat mode: the rows of (group, term) of cursor `cu`, back to back, into
@@ -1087,7 +1073,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
         while (j < n_jobs && g >= jobs[j].group_begin + groups_of(jobs[j])) ++j;
         const Job &J = jobs[j];
         const int n_terms = J.n_terms;
-        const bool aligned = TMA || J.aligned;
+        const bool aligned = WS || J.aligned;
         const int64_t rowrel = (int64_t)(g - J.group_begin) * kRows + lane;
         const bool row_ok = rowrel < J.n_rows;
         const int par = gi & 1;
@@ -1151,18 +1137,13 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
                 }
                 const int kb = kb_lo + c * KC;
                 const int kn = min(KC, kb_hi - kb);
-                if constexpr (TMA) {
+                if constexpr (WS) {
                     // A chunk is exactly one group: copy it to registers, hand
-                    // the slot straight back to the copy engine, then compute.
+                    // the slot straight back to the producer, then compute.
                     GroupRegs<FMT> r;
                     load_group<FMT>(slot, r);
                     __syncwarp();
-                    if constexpr (WS) {
-                        if (lane == 0) mbar_arrive(&ebars[warp * ST + cur]);
-                    } else if (ic.valid) {
-                        issue(ic);
-                        cursor_advance(jobs, n_jobs, ic, n_chunks, g_hi);
-                    }
+                    if (lane == 0) mbar_arrive(&ebars[warp * ST + cur]);
                     acc = compute_group<FMT>(r, xr_row + kb * F::RPB, acc);
                     continue;
                 }
