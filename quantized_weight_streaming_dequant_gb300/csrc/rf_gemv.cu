@@ -440,6 +440,39 @@ __device__ __forceinline__ float compute_group(const GroupRegs<FMT> &r, const XR
     }
 }
 
+// Blocks [B0, B1) of a group held in registers (words of the group past
+// those blocks need not be loaded yet).
+template <int FMT, int B0, int B1>
+__device__ __forceinline__ float compute_blocks(const GroupRegs<FMT> &r, const XRec *xr, float acc)
+{
+    using F = FmtT<FMT>;
+#pragma unroll
+    for (int b = B0; b < B1; ++b) {
+        const int o = b * F::BS;
+        const uint32_t hdr = word_at(r.v, o);
+        uint32_t q[F::QW];
+#pragma unroll
+        for (int k = 0; k < F::QW; ++k) q[k] = word_at(r.v, o + F::HDR + 4 * k);
+        const XRec &x = xr[b];
+        acc = fmaf(block_idot<FMT>(q, x), block_scale<FMT>(hdr, x.scale), acc);
+    }
+    return acc;
+}
+
+// 16-byte words [I0, I1) of a group from shared memory into registers.
+template <int FMT, int I0, int I1>
+__device__ __forceinline__ void load_group_part(const uint8_t *src, GroupRegs<FMT> &r)
+{
+#pragma unroll
+    for (int i = I0; i < I1; ++i) {
+        const uint4 t = reinterpret_cast<const uint4 *>(src)[i];
+        r.v[4 * i] = t.x;
+        r.v[4 * i + 1] = t.y;
+        r.v[4 * i + 2] = t.z;
+        r.v[4 * i + 3] = t.w;
+    }
+}
+
 // Aligned chunk: `kn` blocks (a multiple of G) at a 16-byte aligned address.
 template <int FMT>
 __device__ __forceinline__ float chunk_aligned(const uint8_t *src, int kn, const XRec *xr,
@@ -1137,7 +1170,20 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
                 }
                 const int kb = kb_lo + c * KC;
                 const int kn = min(KC, kb_hi - kb);
-                if constexpr (WS) {
+                if constexpr (WS && FMT == RF_MXFP4) {
+                    // 16 blocks of 17 bytes: the first 8 come from the first
+                    // 9 16-byte words; decode them before loading the rest,
+                    // so that fewer words are live at once.
+                    GroupRegs<FMT> r;
+                    load_group_part<FMT, 0, 9>(slot, r);
+                    acc = compute_blocks<FMT, 0, 8>(r, xr_row + kb * F::RPB, acc);
+                    load_group_part<FMT, 9, 17>(slot, r);
+                    r.v[68] = 0;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ebars[warp * ST + cur]);
+                    acc = compute_blocks<FMT, 8, 16>(r, xr_row + kb * F::RPB, acc);
+                    continue;
+                } else if constexpr (WS) {
                     // A chunk is exactly one group: copy it to registers, hand
                     // the slot straight back to the producer, then compute.
                     GroupRegs<FMT> r;
