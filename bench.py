@@ -45,6 +45,9 @@ import synthetic as syn  # noqa: E402
 
 METRIC = "effective weight GB/s of dequant-GEMV (% of HBM / H2D peak); tokens/s equivalent"
 FALLBACK_HBM_GBS = 6800.0
+REPEATS = 5   # timed repeats of each headline region; the value is their median
+DTYPE = ("q4_0 weights x int16 activation digits (per 32-block, power-of-two scale), "
+         "exact int32 block dot, fp32 across blocks")
 
 
 # ---------------------------------------------------------------- helpers
@@ -254,19 +257,36 @@ def run_dense(args, torch, rf, device, rank, world, dist):
     if dist:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # The timed region (exactly args.steps steps) runs REPEATS times; each
+    # repeat is bracketed by a barrier and synchronisations and timed on the
+    # launching stream; the value is the median repeat.  The clock sampler
+    # (200 ms period) runs across a one-second load of the same steps just
+    # before the repeats and across the repeats themselves, so that it sees
+    # the clocks under this load even when a repeat lasts well under 200 ms.
+    reps_ms = []
     with ClockSampler(device.index or 0) as clk:
-        torch.cuda.synchronize()
-        if dist:
-            dist.barrier()
+        t_end = time.perf_counter() + args.clock_soak
         with torch.cuda.stream(stream):
-            e0.record(stream)
-            run_steps(args.steps)
-            e1.record(stream)
-        torch.cuda.synchronize()
-        if dist:
-            dist.barrier()
-    ms = reduce_time_max(torch, dist, e0.elapsed_time(e1), device)
+            while time.perf_counter() < t_end:
+                run_steps(max(args.steps, 8 * nL))
+                stream.synchronize()
+        for _ in range(REPEATS):
+            torch.cuda.synchronize()
+            if dist:
+                dist.barrier()
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                run_steps(args.steps)
+                e1.record(stream)
+            torch.cuda.synchronize()
+            if dist:
+                dist.barrier()
+            reps_ms.append(reduce_time_max(torch, dist, e0.elapsed_time(e1), device))
+    ms = statistics.median(reps_ms)
     gbs = whole_job_gbs(wbytes, args.steps, world, ms)
+    spread = {"repeats": REPEATS, "ms_per_step": [round(r / args.steps, 6) for r in reps_ms],
+              "min_ms_per_step": min(reps_ms) / args.steps,
+              "max_ms_per_step": max(reps_ms) / args.steps}
 
     # Per-phase launch durations (eager, events around each launch) for the
     # roofline breakdown.
@@ -276,7 +296,7 @@ def run_dense(args, torch, rf, device, rank, world, dist):
     # host memory, the 4 launches, D2H of the step's outputs, every step.
     e2e = dense_e2e(torch, layers, out, device, stream, steps=min(args.steps, 400) or 1)
     return dict(ms=ms / args.steps, gbs=gbs, wbytes=wbytes, use_graph=use_graph,
-                clocks=clk.summary(), phases=phases, e2e=e2e)
+                clocks=clk.summary(), phases=phases, e2e=e2e, spread=spread)
 
 
 def per_phase_times(torch, rf, layers, x, attn, x_ffn, out, stream, reps):
@@ -658,6 +678,7 @@ def run_streamed_ffn(torch, rf, device, n_layer: int):
         for l in range(min(2, n_layer)):
             layers[l].step(arena, xs[l], u, h, y, c["block_rows"], c["depth"])
         torch.cuda.synchronize()
+        blocks0 = arena.stats()["blocks"]
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0 = time.perf_counter()
         e0.record(s)
@@ -668,9 +689,10 @@ def run_streamed_ffn(torch, rf, device, n_layer: int):
         host_s = time.perf_counter() - t0
         ms = e0.elapsed_time(e1)
         stats = arena.stats()
+        blocks_eager = stats["blocks"] - blocks0
         # The same token captured into one CUDA graph: copies and GEMVs become
         # graph nodes, so the host issues one launch per token.
-        graph_ms, graph_err = None, None
+        graph_ms, graph_err, graph_runs = None, None, None
         try:
             s = torch.cuda.Stream(device)   # captures need a side stream
             s.wait_stream(torch.cuda.current_stream())
@@ -682,14 +704,22 @@ def run_streamed_ffn(torch, rf, device, n_layer: int):
                 g.replay()
             torch.cuda.synchronize()
             y_graph = y.clone()
-            reps = 2
-            with torch.cuda.stream(s):
-                e0.record(s)
-                for _ in range(reps):
-                    g.replay()
-                e1.record(s)
-            torch.cuda.synchronize()
-            graph_ms = e0.elapsed_time(e1) / reps
+            # REPEATS timed runs of `tokens` graph-replayed tokens each
+            # (continuous streaming: the copy engine never drains between
+            # tokens); the figure is the median run.
+            tokens = 10
+            runs = []
+            for _ in range(REPEATS):
+                with torch.cuda.stream(s):
+                    e0.record(s)
+                    for _ in range(tokens):
+                        g.replay()
+                    e1.record(s)
+                torch.cuda.synchronize()
+                runs.append(e0.elapsed_time(e1) / tokens)
+            graph_ms = statistics.median(runs)
+            graph_runs = {"tokens_per_run": tokens, "runs": REPEATS,
+                          "ms_per_token": [round(r, 3) for r in runs]}
             # eager and graph walks of the same token give the same bits
             layers[n_layer - 1].step(arena, xs[n_layer - 1], u, h, y, c["block_rows"], c["depth"])
             torch.cuda.synchronize()
@@ -723,15 +753,15 @@ def run_streamed_ffn(torch, rf, device, n_layer: int):
             "h2d_probe_256mib_gbs": probe_big, "h2d_probe_block_gbs": probe_blk,
             "frac_of_h2d": gbs / probe_big, "tokens_per_s": 1e3 / best_ms,
             "eager": {"ms_per_token": ms, "value": eager_gbs, "host_enqueue_s": host_s},
-            "graph": {"ms_per_token": graph_ms, "error": graph_err,
+            "graph": {"ms_per_token": graph_ms, "error": graph_err, "timing": graph_runs,
                       "value": nbytes / (graph_ms * 1e-3) / 1e9 if graph_ms else None},
             "zero_copy": {"ms_per_token": zc_ms, "value": nbytes / (zc_ms * 1e-3) / 1e9,
                           "frac_of_h2d": nbytes / (zc_ms * 1e-3) / 1e9 / probe_big},
             "arena_peak_bytes": stats["peak_bytes"],
-            "blocks_per_token": stats["blocks"] // (n_layer + min(2, n_layer))}
+            "blocks_per_token": blocks_eager}
 
 
-def run_sweep(torch, rf, device, peak_hbm: float):
+def run_sweep(torch, rf, device, peak_hbm: float, reduced: bool = False):
     """The format x in_dim x out_dim x block_rows sweep, resident and
     host-streamed.  Resident: the row windows of block_rows rows (whole =
     one window) go to rf_gemv_batch (at most 64 windows per launch); copies of
@@ -772,6 +802,8 @@ def run_sweep(torch, rf, device, peak_hbm: float):
     try:
         for c in syn.sweep_cells():
             fmt, in_dim, out, br = c["fmt"], c["in_dim"], c["out_dim"], c["block_rows"]
+            if reduced and br not in (128, 0):
+                continue
             W = syn.quant_matrix(fmt, out, in_dim, c["seed"], threads=16)
             nbytes = W.nbytes
             x = torch.from_numpy(syn.normal_f32(in_dim, c["seed"] + 1)).to(device)
@@ -814,60 +846,100 @@ def run_sweep(torch, rf, device, peak_hbm: float):
     rf_ = sorted(cl["resident_frac_hbm"] for cl in cells)
     sf_ = sorted(cl["streamed_frac_h2d"] for cl in cells)
     return {"h2d_probe_256mib_gbs": h2d, "cells": cells,
+            "block_rows": "128 and whole only" if reduced else "all",
             "resident_frac_hbm_median": rf_[len(rf_) // 2],
             "streamed_frac_h2d_median": sf_[len(sf_) // 2]}
 
 
 # ------------------------------------------------------------- reference
 
-def cpu_oracle_dense(fraction: float, min_seconds: float):
-    """The oracle on the first `fraction` of every matrix's rows of one C2
-    layer; repeats until min_seconds of CPU time; returns (GB/s, seconds,
-    bytes per pass)."""
-    import oracle
-    fmt, d, f = syn.Q4_0, syn.C2["d_model"], syn.C2["d_ff"]
-    shapes = [(d, d)] * 4 + [(f, d)] * 2 + [(d, f)]
-    mats = [syn.quant_matrix(fmt, max(1, int(r * fraction)), c, 7 + i)
-            for i, (r, c) in enumerate(shapes)]
-    xs = {c: syn.normal_f32(c, c) for c in (d, f)}
-    nbytes = sum(m.nbytes for m in mats)
-    passes, t0 = 0, time.perf_counter()
-    while True:
-        for m, (r, c) in zip(mats, shapes):
-            oracle.gemv(fmt, m, 0, m.shape[0], c, xs[c])
-        passes += 1
-        dt = time.perf_counter() - t0
-        if dt >= min_seconds:
-            break
-    return nbytes * passes / dt / 1e9, dt / passes, nbytes
+class OracleLayer:
+    """One Q4_0 4096/11008 layer for the CPU oracle: the 7 matrices with the
+    first `fraction` of their rows (1.0 = the whole layer, 113,836,032
+    bytes).  A pass runs the oracle's GEMV over every row; with threads > 1
+    the rows of every matrix are cut into `threads` contiguous ranges run
+    concurrently (the C oracle runs outside the GIL, so the threads use as
+    many host cores), the oracle's own arithmetic unchanged."""
+
+    def __init__(self, fraction: float = 1.0):
+        fmt, d, f = syn.Q4_0, syn.C2["d_model"], syn.C2["d_ff"]
+        self.fmt = fmt
+        self.shapes = [(d, d)] * 4 + [(f, d)] * 2 + [(d, f)]
+        self.mats = [syn.quant_matrix(fmt, max(1, int(r * fraction)), c, 7 + i, threads=8)
+                     for i, (r, c) in enumerate(self.shapes)]
+        self.xs = {c: syn.normal_f32(c, c) for c in (d, f)}
+        self.nbytes = sum(m.nbytes for m in self.mats)
+
+    def run(self, threads: int = 1, pool=None):
+        import oracle
+        if threads <= 1:
+            for m, (_, c) in zip(self.mats, self.shapes):
+                oracle.gemv(self.fmt, m, 0, m.shape[0], c, self.xs[c])
+            return
+        work = []
+        for m, (_, c) in zip(self.mats, self.shapes):
+            n = m.shape[0]
+            for t in range(threads):
+                r0, r1 = n * t // threads, n * (t + 1) // threads
+                if r1 > r0:
+                    work.append((m, r0, r1, c))
+        list(pool.map(lambda a: oracle.gemv(self.fmt, a[0], a[1], a[2], a[3], self.xs[a[3]]),
+                      work))
+
+    def timed(self, min_seconds: float, threads: int = 1):
+        """(GB/s, seconds per pass): passes repeated until min_seconds."""
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(max_workers=max(1, threads)) as pool:
+            self.run(threads, pool)   # warm-up pass
+            passes, t0 = 0, time.perf_counter()
+            while True:
+                self.run(threads, pool)
+                passes += 1
+                dt = time.perf_counter() - t0
+                if dt >= min_seconds:
+                    break
+        return self.nbytes * passes / dt / 1e9, dt / passes
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
 
 
 def run_reference(args, rank: int):
     if rank != 0:
         return 0
     import oracle
+    from concurrent.futures import ThreadPoolExecutor
     oracle.build()
     total = args.steps + args.warmup
-    # size each step so the whole run takes about a minute of one core
-    _, t_full_frac, _ = cpu_oracle_dense(1 / 64, 0.0)
-    frac = max(1 / 4096, min(1.0, (60.0 / max(total, 1)) / (t_full_frac * 64)))
-    gbs, _, nbytes = cpu_oracle_dense(frac, 0.0)
-    for _ in range(args.warmup):
-        cpu_oracle_dense(frac, 0.0)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        cpu_oracle_dense(frac, 0.0)
-    dt = time.perf_counter() - t0
-    value = nbytes * args.steps / dt / 1e9
-    sample = (f"first {frac:.4%} of the rows of each of the 7 matrices of one Q4_0 "
-              f"4096/11008 layer ({nbytes} weight bytes) per step")
+    cores = host_cores()
+    # each step: the whole layer on all host cores, or (for long runs) the
+    # first rows of every matrix, sized so the run takes about a minute
+    probe = OracleLayer(1 / 64)
+    _, t_probe = probe.timed(0.0, cores)
+    frac = max(1 / 4096, min(1.0, (60.0 / max(total, 1)) / (t_probe * 64)))
+    layer = OracleLayer(frac) if frac < 1.0 else OracleLayer(1.0)
+    with ThreadPoolExecutor(max_workers=cores) as pool:
+        for _ in range(args.warmup):
+            layer.run(cores, pool)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            layer.run(cores, pool)
+        dt = time.perf_counter() - t0
+    value = layer.nbytes * args.steps / dt / 1e9
+    what = "every row" if frac >= 1.0 else f"the first {frac:.4%} of the rows"
+    sample = (f"{what} of each of the 7 matrices of one Q4_0 4096/11008 layer "
+              f"({layer.nbytes} weight bytes) per step, rows split over {cores} host threads")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt / max(args.steps, 1) * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": syn.C2["name"], "d_model": 4096, "d_ff": 11008,
                        "format": "Q4_0", "batch": 1},
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -888,7 +960,12 @@ def main():
     ap.add_argument("--ffn-layers", type=int, default=syn.C4["n_layer"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--sweep", action="store_true",
-                    help="also run the format x shape x block_rows sweep (several minutes)")
+                    help="run the full format x shape x block_rows sweep (several minutes) "
+                         "instead of the reduced one (block_rows 128 and whole)")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the sweep")
+    ap.add_argument("--clock-soak", type=float, default=1.0,
+                    help="seconds of the headline steps run under the clock sampler before "
+                         "the timed repeats")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -919,7 +996,7 @@ def main():
     line = {"metric": METRIC, "value": res["gbs"], "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "q4_0 x int24 (dp4a), fp32 accumulate", "data": "synthetic",
+            "dtype": DTYPE, "data": "synthetic",
             "config": {"workload": syn.C2["name"], "format": "Q4_0", "d_model": 4096,
                        "d_ff": 11008, "batch": 1, "layer_copies": syn.C2["copies"],
                        "weight_bytes_per_step": wbytes, "l2": "inputs > L2 (8 layer copies, "
@@ -930,7 +1007,12 @@ def main():
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind,
                          "kernel": "rowwin_kernel<Q4_0> (all 4 launches of the step)",
-                         "traffic": traffic},
+                         "traffic": traffic,
+                         "traffic_source": "profiles/ncu_traffic.txt: dram__bytes_read.sum + "
+                                           "dram__bytes_write.sum of one step's launches from "
+                                           "an ncu capture of this kernel source (keyed by its "
+                                           "hash; null when the source changed since)"},
+            "timing": res["spread"],
             "phases": res["phases"], "clocks": res["clocks"], "e2e": res["e2e"],
             "gpu_launches": launches}
     if rank == 0 and world == 1 and not args.headline_only:
@@ -945,15 +1027,26 @@ def main():
             extra["dense_layer_q4_k"] = q4k
             if args.ffn_layers > 0:
                 extra["streamed_ffn_q8_0"] = run_streamed_ffn(torch, rf, device, args.ffn_layers)
-            if args.sweep:
-                extra["sweep"] = run_sweep(torch, rf, device, peak)
+            if not args.no_sweep:
+                extra["sweep"] = run_sweep(torch, rf, device, peak, reduced=not args.sweep)
         except Exception as e:  # extras never hide the headline
             extra["error"] = repr(e)
         line["extra"] = extra
-        gbs_cpu, _, _ = cpu_oracle_dense(1 / 16, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": gbs_cpu, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                                "sample": "first 1/16 of the rows of each matrix of one layer, "
-                                          f"repeated for {args.cpu_seconds:.0f} s on one core"}
+        # The CPU oracle on the same workload: the whole layer (every row of
+        # the 7 matrices, 113.8 MB), on one core and row-parallel over every
+        # host core.
+        layer = OracleLayer(1.0)
+        cores = host_cores()
+        gbs1, s1 = layer.timed(args.cpu_seconds, 1)
+        gbsn, sn = layer.timed(args.cpu_seconds, cores)
+        line["cpu_baseline"] = {
+            "value": gbs1, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"the whole layer ({layer.nbytes} weight bytes) per pass, passes "
+                      f"repeated for at least {args.cpu_seconds:.0f} s on one core "
+                      f"({s1:.3f} s per pass)",
+            "all_cores": {"value": gbsn, "unit": "GB/s", "cores": cores,
+                          "sample": f"the same passes with every matrix's rows split over "
+                                    f"{cores} threads ({sn:.3f} s per pass)"}}
     if rank == 0:
         print(json.dumps(line))
     if dist:

@@ -12,13 +12,22 @@
  *     name says host.  All buffers belong to the caller; the library keeps no
  *     pointer past the call except inside an rf_arena it created.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
- *     stream ordered and return after enqueueing; no call blocks the host on
- *     GPU work except rf_device_status and rf_arena_destroy.
+ *     stream ordered and return after enqueueing.  These calls block the host
+ *     on GPU work, and no others do:
+ *       rf_device_status        (synchronizes the device),
+ *       rf_arena_destroy        (waits for the arena's copies and readers),
+ *       rf_arena_wait           (waits, up to its deadline, for the same),
+ *       rf_expert_cache_destroy (waits for the cache's copies and readers),
+ *       rf_moe_ffn_streamed     (waits for its routing result: the host plan
+ *                                needs the expert ids).
  *   - Argument errors are detected on the host before anything is enqueued;
  *     the call then returns an error and enqueues nothing.  Launch errors
  *     return RF_ERR_CUDA.  Kernels never trap: a kernel whose internal wait
  *     exceeds its time limit records RF_ERR_TIMEOUT in a device status word
- *     that rf_device_status reports.
+ *     that rf_device_status reports, issues no further copies, waits for the
+ *     ones it issued and ends.  The word is sticky: while it is set, every
+ *     bounded wait of later kernels ends at once (their outputs are
+ *     undefined), until rf_device_status reads and clears it.
  *   - Weight pointers must be 16-byte aligned.  A kernel may read whole
  *     16-byte aligned chunks that contain bytes of the rows it was given (so
  *     up to 15 bytes before the first and after the last row byte, never in
@@ -230,16 +239,54 @@ RF_API rf_status rf_gemv_host(int fmt, const void *host_W, int64_t row_start, in
 
 /* ------------------------------------------- host-streamed row windows */
 /* An arena is a bounded ring of device memory plus a copy stream and events
- * (neurostream, "How it works" 6: every in-flight block holds a byte
- * reservation, and allocation waits until one retires).  rf_arena_create
- * allocates `bytes` (plus a little alignment slack) of device memory on the
- * current device.  An arena is used by one host thread at a time. */
+ * (neurostream, "How it works" 6: each block in flight takes arena space,
+ * and a fetch that finds none free waits for a block to be given back).
+ * rf_arena_create allocates `bytes` (plus a little alignment slack) of
+ * device memory on the chosen device.  An arena is used by one host thread
+ * at a time. */
 typedef struct rf_arena rf_arena;
-RF_API rf_status rf_arena_create(size_t bytes, rf_arena **out);
+/* device: the CUDA device the arena lives on, or -1 for the current one.  The
+ * arena's memory, copy stream and events belong to that device; every call
+ * that uses the arena must be made with it current (else
+ * RF_ERR_INVALID_ARG).  Errors: RF_ERR_INVALID_ARG (bytes == 0, out NULL,
+ * no such device), RF_ERR_OOM, RF_ERR_CUDA. */
+RF_API rf_status rf_arena_create(size_t bytes, int device, rf_arena **out);
 /* Waits for the arena's outstanding eager copies and readers, then frees it
  * (launches of graphs captured with it must have finished).  NULL is a
  * no-op. */
 RF_API void rf_arena_destroy(rf_arena *arena);
+
+/* Host wait with a deadline: blocks until every copy the arena has enqueued
+ * and every launch that read one of its slots (eager use) has finished, or
+ * until timeout_ms milliseconds have passed (neurostream, "Bugs worth
+ * knowing about": a prefetcher that can stall must not stall its caller for
+ * ever).  Returns RF_OK, RF_ERR_TIMEOUT (work still outstanding; call again
+ * to keep waiting), RF_ERR_CUDA (the device reported an error) or
+ * RF_ERR_INVALID_ARG (NULL arena, timeout_ms < 0, the arena's device is not
+ * current, or a capture is using the arena's streams). */
+RF_API rf_status rf_arena_wait(rf_arena *arena, int timeout_ms);
+
+/* Host-side failure injection for tests (the pages have no counterpart; it
+ * lets the failure path be exercised without faulting a GPU).  Arms a
+ * one-shot fault for the next rf_stream_linear walk on the arena, at the
+ * walk's block `block` (0-based):
+ *   RF_FAULT_COPY_FAIL  -- that block's copy reports a failure, as a failed
+ *                          cudaMemcpyAsync would: the walk stops enqueueing,
+ *                          the blocks already enqueued keep their order on
+ *                          the caller's stream (lane streams are joined
+ *                          back), every slot stays reusable, and the call
+ *                          returns RF_ERR_CUDA;
+ *   RF_FAULT_COPY_STALL -- the copy stream stalls for `ms` milliseconds on
+ *                          the host before that block's copy (a slow link);
+ *                          the walk itself succeeds.
+ * An armed fault also turns off the one-copy path for walks that fit the
+ * ring, so the fault lands on a real per-block copy.  RF_FAULT_NONE
+ * disarms.  Errors: RF_ERR_INVALID_ARG (NULL arena, unknown kind, block < 0,
+ * ms outside 0..10000). */
+#define RF_FAULT_NONE 0
+#define RF_FAULT_COPY_FAIL 1
+#define RF_FAULT_COPY_STALL 2
+RF_API rf_status rf_arena_inject_fault(rf_arena *arena, int kind, int64_t block, int ms);
 
 /* Host-side block plan for walking n_rows rows of rf_row_bytes(fmt,in_dim)
  * bytes in blocks of block_rows rows (0 = the whole window) with `depth`
@@ -277,7 +324,7 @@ RF_API rf_status rf_stream_linear(int fmt, const void *host_W, int64_t in_dim,
                                   void *stream);
 
 /* Counters of an arena (each one is exercised by a test). */
-typedef struct rf_stream_stats {
+typedef struct rf_stream_stats_t {
     uint64_t calls;          /* rf_stream_linear calls enqueued */
     uint64_t blocks;         /* blocks copied and multiplied */
     uint64_t bytes_copied;   /* host->device bytes enqueued */
@@ -286,8 +333,9 @@ typedef struct rf_stream_stats {
     uint64_t arena_bytes;    /* arena capacity */
     int32_t slots;           /* slots (depth+1) in the last call */
     int32_t last_block_rows; /* effective rows per block in the last call */
-} rf_stream_stats;
-RF_API rf_status rf_stream_stats_get(const rf_arena *arena, rf_stream_stats *out);
+} rf_stream_stats_t;
+/* Copies the arena's counters to *out.  Errors: RF_ERR_INVALID_ARG (NULL). */
+RF_API rf_status rf_stream_stats(const rf_arena *arena, rf_stream_stats_t *out);
 
 /* ------------------------------------------------------------------- MoE */
 /* Device top-k router (neurostream, "How it works" 2: the router names the
@@ -352,7 +400,7 @@ RF_API rf_status rf_expert_cache_create(int fmt, int64_t n_ff, int64_t n_embd, i
  * is a no-op. */
 RF_API void rf_expert_cache_destroy(rf_expert_cache *cache);
 
-typedef struct rf_expert_cache_stats {
+typedef struct rf_expert_cache_stats_t {
     uint64_t lookups;          /* selected experts looked up */
     uint64_t hits;             /* ... found in the cache (nothing read from the host) */
     uint64_t fills;            /* ... streamed into a cache slot */
@@ -361,19 +409,19 @@ typedef struct rf_expert_cache_stats {
     uint64_t bytes_streamed;   /* host->device expert bytes enqueued */
     uint64_t bytes_cached;     /* expert bytes read from the cache instead */
     int32_t slots, used;       /* capacity and occupied slots */
-} rf_expert_cache_stats;
-RF_API rf_status rf_expert_cache_stats_get(const rf_expert_cache *cache,
-                                           rf_expert_cache_stats *out);
+} rf_expert_cache_stats_t;
+/* Copies the cache's counters to *out.  Errors: RF_ERR_INVALID_ARG (NULL). */
+RF_API rf_status rf_expert_cache_stats(const rf_expert_cache *cache,
+                                       rf_expert_cache_stats_t *out);
 
 /* Routed SwiGLU FFN with the stacked expert tensors in page-locked host
  * memory, read through one layer-wide prefetch plan (neurostream, "How it
- * works" 3: because routing has named every expert the layer touches, one
- * plan covers all active experts x gate/up/down in the order they are
- * consumed, chopped into blocks; the prefetcher keeps `depth` blocks in
- * flight and refills as each retires, so a block finishing in gate/up
- * immediately pulls in one of down; windows the cache holds are skipped;
- * "What the numbers taught us": a per-projection pipeline drains at every
- * projection, the shared plan does not).
+ * works" 3: once routing has named the layer's experts, a single block list
+ * covers their gate, up and down rows in the order the launches read them,
+ * with at most `depth` blocks fetched ahead, so copies run on into down's
+ * rows while gate/up computes; rows the cache holds are not copied; "What
+ * the numbers taught us": separate per-projection pipelines drain between
+ * projections, the single list does not).
  *
  * Steps: the router kernel writes the top_k experts and weights to the
  * workspace; their ids are copied to the host (the call blocks until the
@@ -418,10 +466,14 @@ RF_API rf_status rf_moe_ffn_streamed(int fmt, const float *router_logits, int n_
  * RF_MOE_STATIC_MAX_H floats of activations, their digits (80 bytes per 32)
  * and the routing result, which
  * every GPU that loads the library keeps until the process exits.  Limit:
- * top_k * n_ff <= RF_MOE_STATIC_MAX_H, else RF_ERR_TOO_LARGE before any work.
+ * top_k * n_ff <= RF_MOE_STATIC_MAX_H, else RF_ERR_TOO_LARGE before any work
+ * (n_ff <= rf_max_in_dim(fmt, top_k) applies as for rf_moe_ffn, which with
+ * 4 experts caps the activations at 61,440).
  * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture.  All calls share the one array and it keeps the last call's
+ * device, with that device current) and keeps it for the life of the
+ * process; make that first call before any stream capture.  A caller that
+ * resets the device (cudaDeviceReset) invalidates that address: do not call
+ * this entry point on the device afterwards.  All calls share the one array and it keeps the last call's
  * contents; nothing in it needs to start at zero.  Calls whose kernels
  * overlap on the GPU (different streams, or different host threads) race on
  * it: serialise them.  Arguments and results otherwise as rf_moe_ffn. */
@@ -436,6 +488,17 @@ RF_API rf_status rf_moe_ffn_noalloc(int fmt, const float *router_logits, int n_e
  * word that kernels set when a bounded wait times out (RF_OK if none).
  * Returns RF_ERR_CUDA if the device reports an error. */
 RF_API rf_status rf_device_status(void);
+
+/* Test hook for the kernels' bounded waits (the pages have no counterpart; it
+ * lets the failure path be exercised without faulting a GPU).  Arms a
+ * one-shot fault for the next GEMV launch on this process that copies its
+ * weights with tensor copies (16-byte aligned rows in device memory): in that
+ * launch the copy of one stage of CTA 0 is never issued, so the warp waiting
+ * for it gives up after limit_us microseconds, records RF_ERR_TIMEOUT, and
+ * the launch ends with nothing in flight (its outputs are undefined).
+ * limit_us = 0 disarms.  Errors: RF_ERR_INVALID_ARG for limit_us above
+ * 2,000,000. */
+RF_API rf_status rf_debug_arm_wait_fault(uint32_t limit_us);
 
 #ifdef __cplusplus
 }

@@ -74,12 +74,14 @@ _SIGS = {
     "rf_gemv_host": ([_I, _P, _I64, _I64, _I64, _P, _P, _P], _I),
     "rf_gemv_multi": ([_I, _P, _I64, _I64, _I64, _I, _P, _I64, _P, _I64, ctypes.c_uint, _P], _I),
     "rf_ffn_swiglu_ws": ([_I, _P, _P, _P, _I64, _I64, _P, _P, _P, _P, ctypes.c_uint, _P], _I),
-    "rf_arena_create": ([_SZ, ctypes.POINTER(_P)], _I),
+    "rf_arena_create": ([_SZ, _I, ctypes.POINTER(_P)], _I),
     "rf_arena_destroy": ([_P], None),
+    "rf_arena_wait": ([_P, _I], _I),
+    "rf_arena_inject_fault": ([_P, _I, _I64, _I], _I),
     "rf_stream_plan": ([_I, _I64, _I64, _I64, _I, _SZ, ctypes.POINTER(_I64),
                         ctypes.POINTER(_I64), ctypes.POINTER(_SZ)], _I),
     "rf_stream_linear": ([_I, _P, _I64, _I64, _I64, _I64, _I, _P, _P, _P, _P], _I),
-    "rf_stream_stats_get": ([_P, ctypes.POINTER(StreamStats)], _I),
+    "rf_stream_stats": ([_P, ctypes.POINTER(StreamStats)], _I),
     "rf_moe_route": ([_P, _I, _I, _P, _P, _P], _I),
     "rf_moe_workspace_bytes": ([_I, _I64, _I64, _I64], _SZ),
     "rf_moe_ffn": ([_I, _P, _I, _I, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P], _I),
@@ -87,10 +89,11 @@ _SIGS = {
     "rf_moe_ffn_host": ([_I, _P, _I, _I, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P], _I),
     "rf_expert_cache_create": ([_I, _I64, _I64, _I, ctypes.POINTER(_P)], _I),
     "rf_expert_cache_destroy": ([_P], None),
-    "rf_expert_cache_stats_get": ([_P, ctypes.POINTER(ExpertCacheStats)], _I),
+    "rf_expert_cache_stats": ([_P, ctypes.POINTER(ExpertCacheStats)], _I),
     "rf_moe_ffn_streamed": ([_I, _P, _I, _I, _P, _P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _P, _P,
                              _P], _I),
     "rf_device_status": ([], _I),
+    "rf_debug_arm_wait_fault": ([ctypes.c_uint32], _I),
 }
 
 _lib = None
@@ -265,14 +268,29 @@ def stream_plan(fmt: int, in_dim: int, n_rows: int, block_rows: int, depth: int,
     return eff.value, nblk.value, peak.value
 
 
-class Arena:
-    """Bounded device arena with its copy stream (rf_arena_create)."""
+FAULT_NONE, FAULT_COPY_FAIL, FAULT_COPY_STALL = 0, 1, 2
 
-    def __init__(self, nbytes: int):
+
+class Arena:
+    """Bounded device arena with its copy stream (rf_arena_create); device -1
+    = the current device."""
+
+    def __init__(self, nbytes: int, device: int = -1):
         h = _P()
-        _check(lib().rf_arena_create(nbytes, ctypes.byref(h)), "rf_arena_create")
+        _check(lib().rf_arena_create(nbytes, device, ctypes.byref(h)), "rf_arena_create")
         self.handle = h
         self.nbytes = nbytes
+
+    def wait(self, timeout_ms: int) -> int:
+        """rf_arena_wait: the status (OK, or TIMEOUT while work is outstanding)."""
+        code = lib().rf_arena_wait(self.handle, timeout_ms)
+        if code not in (OK, 6):
+            raise RFError(code, "rf_arena_wait")
+        return code
+
+    def inject_fault(self, kind: int, block: int, ms: int = 0) -> None:
+        """rf_arena_inject_fault (test hook)."""
+        _check(lib().rf_arena_inject_fault(self.handle, kind, block, ms), "rf_arena_inject_fault")
 
     def close(self) -> None:
         if self.handle is not None and self.handle.value:
@@ -301,7 +319,7 @@ class Arena:
 
     def stats(self) -> dict:
         s = StreamStats()
-        _check(lib().rf_stream_stats_get(self.handle, ctypes.byref(s)), "rf_stream_stats_get")
+        _check(lib().rf_stream_stats(self.handle, ctypes.byref(s)), "rf_stream_stats")
         return {k: getattr(s, k) for k, _ in StreamStats._fields_}
 
 
@@ -327,8 +345,8 @@ class ExpertCache:
 
     def stats(self) -> dict:
         s = ExpertCacheStats()
-        _check(lib().rf_expert_cache_stats_get(self.handle, ctypes.byref(s)),
-               "rf_expert_cache_stats_get")
+        _check(lib().rf_expert_cache_stats(self.handle, ctypes.byref(s)),
+               "rf_expert_cache_stats")
         return {k: getattr(s, k) for k, _ in ExpertCacheStats._fields_}
 
 
@@ -429,3 +447,9 @@ def moe_workspace_views(workspace, top_k: int, n_ff: int):
 def device_status() -> int:
     """Synchronize and return (and clear) the kernels' device status word."""
     return lib().rf_device_status()
+
+
+def debug_arm_wait_fault(limit_us: int) -> None:
+    """rf_debug_arm_wait_fault (test hook): the next tensor-copy GEMV launch
+    withholds one stage's copy and gives up its wait after limit_us."""
+    _check(lib().rf_debug_arm_wait_fault(limit_us), "rf_debug_arm_wait_fault")

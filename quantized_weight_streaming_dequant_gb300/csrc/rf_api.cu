@@ -418,4 +418,6 @@ rf_status rf_ffn_swiglu_ws(int fmt, const void *gate, const void *up, const void
 
 rf_status rf_device_status(void) { return read_and_clear_device_status(); }
 
+rf_status rf_debug_arm_wait_fault(uint32_t limit_us) { return arm_wait_fault(limit_us); }
+
 }  // extern "C"

@@ -29,7 +29,11 @@ struct rf_arena {
     int next_slot = 0;
     int last_slots = 0;
     size_t last_stride = 0;
-    rf_stream_stats stats = {};
+    rf_stream_stats_t stats = {};
+    // One-shot host-side failure injection (rf_arena_inject_fault).
+    int fault_kind = 0;
+    int64_t fault_block = 0;
+    int fault_ms = 0;
     int32_t *route_host = nullptr;    // page-locked: routing ids read back for planning
     // Lane streams: the launches of one walk's blocks go round-robin to them,
     // so that blocks whose copies have landed run side by side.

@@ -73,20 +73,44 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 }
 
 // Wait for phase `parity` of `bar` to complete.  Returns false (and records
-// RF_ERR_TIMEOUT in *status) if it does not complete within kWaitLimitNs;
-// the caller then carries on without the data.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int *status)
+// RF_ERR_TIMEOUT in *status) if it does not complete within limit_ns, and
+// returns false at once when *status already holds a failure: after one wait
+// has given up, every later wait of every CTA ends immediately instead of
+// spending its own limit, so a broken pipeline ends the launch after one
+// limit.  A false return means the data did not arrive: the caller issues no
+// further copies, drains the ones it issued and leaves its loops.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int *status,
+                                                  unsigned long long limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 255u && globaltimer_ns() - t0 > kWaitLimitNs) {
-            record_status(status, RF_ERR_TIMEOUT);
-            return false;
+        if ((it & 255u) == 255u) {
+            if (*reinterpret_cast<volatile int *>(status) != 0) return false;
+            if (globaltimer_ns() - t0 > limit_ns) {
+                record_status(status, RF_ERR_TIMEOUT);
+                return false;
+            }
         }
     }
 }
+
+// Drain wait: the copy armed on `bar` at phase `parity` was issued, so it
+// lands whatever else failed; wait for it (bounded, ignoring the status word)
+// so that no copy is still writing shared memory when the CTA exits.
+__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity)) return;
+        if ((it & 255u) == 255u && globaltimer_ns() - t0 > kWaitLimitNs) return;
+    }
+}
+
+// Waits for this thread's outstanding cp.async copies.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // ------------------------------------------------------------- bulk copy
 // 1-D bulk copy global -> shared (TMA engine), completion counted in bytes on

@@ -100,9 +100,10 @@ struct FmtT<RF_Q4_K> {
 };
 
 constexpr int kMaxMaps = 16;   // distinct weight tensors per launch (tensor-map path)
-// Shared ints: group counters (4), flat-mode stage counters (up to 8, at 4),
-// the launch's own routing: expert ids (8, at 16) and weights (8 floats, at
-// 24), and the producer-mode queue of upcoming groups (8, at 32).
+// Shared ints: group counters (3) and the CTA's failure flag (at 3),
+// flat-mode stage counters (up to 4, at 4) and copies issued per stage (up to
+// 4, at 8), the launch's own routing: expert ids (8, at 16) and weights (8
+// floats, at 24), and the producer-mode queue of upcoming groups (8, at 32).
 constexpr int kCntInts = 40;
 constexpr int kGroupQ = 8;
 // Group tickets of launches scheduled dynamically (producer mode): a launch
@@ -112,6 +113,10 @@ constexpr int kGroupQ = 8;
 // later, so launches that may overlap never share one.
 constexpr int kSchedSlots = 1024;
 __device__ unsigned int g_sched[kSchedSlots];
+// CTAs of a dynamically scheduled launch that have finished drawing tickets;
+// the last one puts both words of its slot back to zero, so the slot is
+// clean for its next launch even when a failure stopped the draws early.
+__device__ unsigned int g_sched_done[kSchedSlots];
 
 // Kernel parameters.  Two sizes: launches with at most 4 windows and 4 weight
 // tensors (nearly all of them) pass about 1.6 KB instead of 18 KB per launch.
@@ -132,6 +137,8 @@ struct KParamsT {
     int32_t route_n, route_k;
     int32_t sched_slot;          // >= 0: dynamic group scheduling (producer mode)
     int32_t chained;             // launched behind a previous grid (dependency wait)
+    unsigned long long wait_limit_ns;   // limit of every bounded wait
+    int32_t fault_withhold;      // test hook: CTA 0's producer withholds warp 0's first copy
 };
 using KParamsSmall = KParamsT<4, 4>;
 using KParamsLarge = KParamsT<kMaxJobs, kMaxMaps>;
@@ -696,10 +703,18 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
     off += (size_t)2 * NT * kNW * 32 * sizeof(float);
     int *cnt = reinterpret_cast<int *>(smem + off);       // arrivals per parity, then groups done
     int *emp = cnt + 4;                                   // flat mode: readers done per stage
+    volatile int *fl_fail = cnt + 3;                      // a wait of this CTA gave up
+    int *fl_issued = cnt + 8;                             // flat mode: copies issued per stage
     volatile int *gq = cnt + 32;                          // producer mode: upcoming groups
     off += kCntInts * sizeof(int);
     Job *jobs = reinterpret_cast<Job *>(smem + off);      // this launch's jobs, read once
     const int n_jobs = p.n_jobs;
+    const unsigned long long limit = p.wait_limit_ns;
+    // A wait that gives up (or finds the device status already set) ends the
+    // warp's work: every lane of the warp takes the same decision.
+    auto wait_all_lanes = [&](uint64_t *bar, uint32_t par) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait_bounded(bar, par, &g_device_status, limit));
+    };
 
     const int G_total = p.total_groups;
     // Static ranges: every CTA `base` groups, the first `extra` CTAs one
@@ -810,6 +825,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
             reinterpret_cast<uintptr_t>(term_matrix(eidx, J, cu.t, RB) + (J.row0 + rel) * RB);
         const uintptr_t a = src & ~(uintptr_t)15;
         const uintptr_t e = (src + (uintptr_t)(nr * RB) + 15) & ~(uintptr_t)15;
+        ++fl_issued[st];
         mbar_arrive_expect_tx(&bars[st], (uint32_t)(e - a));
         bulk_g2s(slots + (size_t)st * SLOT, reinterpret_cast<const void *>(a), (uint32_t)(e - a),
                  &bars[st]);
@@ -844,10 +860,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
             const int total = p.total_groups;
             auto draw = [&]() -> int {
                 int t = 0;
-                if (lane == 0) {
-                    t = (int)atomicAdd(&g_sched[p.sched_slot], 1u);
-                    if (t == total - 1) g_sched[p.sched_slot] = 0;   // last ticket
-                }
+                if (lane == 0) t = (int)atomicAdd(&g_sched[p.sched_slot], 1u);
                 t = __shfl_sync(0xffffffffu, t, 0);
                 const int ng = (int)gridDim.x + t;
                 return ng < total ? ng : -1;
@@ -862,8 +875,13 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
             uint8_t *wslots = slots + (size_t)w * ST * kRows * SLOT;
             int st = 0;
             uint32_t ph = 0;
-            auto acquire = [&] {   // next slot of warp w, once warp w released it
-                mbar_wait_bounded(&ebars[w * ST + st], ph ^ 1u, &g_device_status);
+            // Slots of warp w whose latest use carries a copy, and the phase
+            // parity it was armed at: drained before the CTA exits.
+            uint32_t armed = 0, armed_ph = 0;
+            bool failed = false;
+            bool withhold = p.fault_withhold && blockIdx.x == 0 && lane == 0;
+            auto acquire = [&]() -> bool {   // next slot of warp w, once warp w released it
+                return mbar_wait_bounded(&ebars[w * ST + st], ph ^ 1u, &g_device_status, limit);
             };
             auto advance = [&] {
                 if (++st == ST) {
@@ -878,36 +896,66 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
                 if (lane == 0) gq[gi & (kGroupQ - 1)] = g;
                 __syncwarp();
                 if (g < 0) {
-                    if (lane < kNW) {
-                        acquire();
+                    if (lane < kNW && acquire()) {
                         mbar_arrive(&bars[w * ST + st]);
+                        armed &= ~(1u << st);
                     }
                     break;
                 }
                 while (jj < n_jobs && g >= jobs[jj].group_begin + groups_of(jobs[jj])) ++jj;
                 const Job &J = jobs[jj];
                 if (lane < kNW && nch == 0) {
-                    acquire();
-                    mbar_arrive(&bars[w * ST + st]);
-                    advance();
+                    if (acquire()) {
+                        mbar_arrive(&bars[w * ST + st]);
+                        armed &= ~(1u << st);
+                        advance();
+                    } else {
+                        failed = true;
+                    }
                 }
                 for (int t = 0; t < J.n_terms; ++t) {
                     const Term &T = J.term[t];
                     int64_t y = J.row0 + (int64_t)(g - J.group_begin) * kRows;
                     if (T.expert_slot >= 0) y += (int64_t)eidx[T.expert_slot] * J.expert_rows;
                     for (int c = 0; c < max_nch; ++c) {
-                        if (c < nch) {
-                            acquire();
+                        if (c < nch && !failed) {
+                            if (!acquire()) {
+                                failed = true;
+                                continue;
+                            }
+                            if (withhold) {   // test hook: this stage never fills
+                                withhold = false;
+                                armed &= ~(1u << st);
+                                advance();
+                                continue;
+                            }
                             const int x = (kbl + c * KC) * F::BS / 2;   // uint16 units
                             mbar_arrive_expect_tx(&bars[w * ST + st], (uint32_t)(kRows * SLOT));
                             tma_2d_g2s(wslots + (size_t)st * kRows * SLOT, &p.maps[T.tmap], x,
                                        (int)y, &bars[w * ST + st]);
+                            armed |= 1u << st;
+                            armed_ph = (armed_ph & ~(1u << st)) | (ph << st);
                             advance();
                         }
                     }
                 }
+                // After a failure no further copy is issued; the consumer
+                // warps find their next stages empty and leave.
+                if (__any_sync(0xffffffffu, failed)) break;
                 g = gnext;
                 gnext = g < 0 ? -1 : (dyn ? draw() : (g + 1 < g_hi ? g + 1 : -1));
+            }
+            // Every issued copy lands before the CTA may exit (on the normal
+            // path its consumer has already seen it: each check passes at once).
+            if (lane < kNW)
+                for (int i = 0; i < ST; ++i)
+                    if ((armed >> i) & 1u) mbar_drain(&bars[w * ST + i], (armed_ph >> i) & 1u);
+            if (dyn && lane == 0) {
+                __threadfence();   // this CTA's draws come before its count
+                if (atomicAdd(&g_sched_done[p.sched_slot], 1u) == gridDim.x - 1) {
+                    g_sched[p.sched_slot] = 0;
+                    g_sched_done[p.sched_slot] = 0;
+                }
             }
             return;
         }
@@ -1085,11 +1133,12 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
     int cs = 0;          // stage of the next chunk to consume
     uint32_t cph = 0;    // its mbarrier phase parity
     int j = 0;
+    bool failed = false;
     for (int gi = 0, g = g_lo;; ++gi, ++g) {
         if constexpr (WS) {
             // The producer names the group before the arrival that fills (or,
             // for a warp without chunks, only signals) this warp's next slot.
-            mbar_wait_bounded(&my_bars[cs], cph, &g_device_status);
+            if (!wait_all_lanes(&my_bars[cs], cph)) break;
             g = gq[gi & (kGroupQ - 1)];
             if (g < 0) break;
             if (n_chunks == 0) {
@@ -1115,14 +1164,25 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
         // until that group has been combined.
         if (gi >= 2) {
             volatile int *done = cnt + 2;
+            bool ok = true;
             if (*done < gi - 1) {
                 const unsigned long long t0 = globaltimer_ns();
-                while (*done < gi - 1) {
-                    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                for (uint32_t it = 0; *done < gi - 1; ++it) {
+                    if ((it & 63u) != 63u) continue;
+                    if (*reinterpret_cast<volatile int *>(&g_device_status) != 0) {
+                        ok = false;
+                        break;
+                    }
+                    if (globaltimer_ns() - t0 > limit) {
                         record_status(&g_device_status, RF_ERR_TIMEOUT);
+                        ok = false;
                         break;
                     }
                 }
+            }
+            if (!__all_sync(0xffffffffu, ok)) {
+                if constexpr (FLAT) *fl_fail = 1;
+                break;
             }
             __threadfence_block();
         }
@@ -1138,7 +1198,11 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
                 // ring), reads its K part of its lane's row, then counts
                 // itself out; the last one refills the stage.
                 const int st = cs;
-                mbar_wait_bounded(&bars[st], cph, &g_device_status);
+                if (!wait_all_lanes(&bars[st], cph)) {
+                    *fl_fail = 1;
+                    failed = true;
+                    break;
+                }
                 if (row_ok && kb_hi > kb_lo) {
                     const uintptr_t src = reinterpret_cast<uintptr_t>(
                         term_matrix(eidx, J, t, RB) + (J.row0 + rowrel - lane) * RB);
@@ -1156,13 +1220,16 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
                 __syncwarp();
                 if (lane == 0 && atomicAdd(&emp[st], 1) == kNW - 1) {
                     emp[st] = 0;
-                    if (ic.valid) issue_flat(ic, st);
+                    if (ic.valid && *fl_fail == 0) issue_flat(ic, st);
                 }
                 if (ic.valid) cursor_advance(jobs, n_jobs, ic, 1, g_hi);
             }
             for (int c = 0; c < (FLAT ? 0 : n_chunks); ++c) {
                 const int cur = cs;
-                mbar_wait_bounded(&my_bars[cur], cph, &g_device_status);
+                if (!wait_all_lanes(&my_bars[cur], cph)) {
+                    failed = true;
+                    break;
+                }
                 const uint8_t *slot = my_slots + ((size_t)cur * kRows + lane) * SLOT;
                 if (++cs == ST) {
                     cs = 0;
@@ -1205,8 +1272,10 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
                     cursor_advance(jobs, n_jobs, ic, n_chunks, g_hi);
                 }
             }
+            if (failed) break;
             red_g[((size_t)t * kNW + warp) * 32 + lane] = acc;
         }
+        if (failed) break;
         // The last warp to finish this group sums the partials in warp order.
         __syncwarp();
         __threadfence_block();
@@ -1251,6 +1320,17 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
                 atomicAdd(&cnt[2], 1);
             }
         }
+    }
+    // Nothing this CTA issued may still be writing its shared memory when it
+    // exits: after a failure, wait for the bulk copies of every stage (each
+    // lands whatever else failed); cp.async copies are this thread's own.
+    if constexpr (FLAT) {
+        __syncthreads();
+        if (threadIdx.x == 0 && *fl_fail)
+            for (int i = 0; i < ST; ++i)
+                if (fl_issued[i] > 0) mbar_drain(&bars[i], (uint32_t)(fl_issued[i] - 1) & 1u);
+    } else if constexpr (!WS) {
+        cp_async_wait_all();
     }
 }
 
@@ -1411,6 +1491,9 @@ struct MapKey {
     }
 };
 std::atomic<uint32_t> g_sched_seq{0};
+// One-shot test fault for the next producer-mode launch (0 = none): the wait
+// limit in nanoseconds that launch runs with.
+std::atomic<unsigned long long> g_fault_limit_ns{0};
 
 constexpr int kMapCache = 64;
 std::mutex g_map_mu;
@@ -1438,6 +1521,13 @@ bool cached_rows_map(CUtensorMap *m, const void *base, int64_t rows, int64_t rb,
 }
 
 }  // namespace
+
+rf_status arm_wait_fault(uint32_t limit_us)
+{
+    if (limit_us > 2000000u) return RF_ERR_INVALID_ARG;
+    g_fault_limit_ns.store((unsigned long long)limit_us * 1000ull);
+    return RF_OK;
+}
 
 rf_status read_and_clear_device_status()
 {
@@ -1748,6 +1838,15 @@ static rf_status launch_merged(const LaunchDesc &d, int nb, int64_t RB, cudaStre
             p.sched_slot = sched_slot;
             p.max_terms = max_terms;
             p.n_maps = n_maps;
+            p.wait_limit_ns = kWaitLimitNs;
+            p.fault_withhold = 0;
+            if (mode == kModeTensorWS && g_fault_limit_ns.load(std::memory_order_relaxed)) {
+                const unsigned long long lim = g_fault_limit_ns.exchange(0);
+                if (lim) {
+                    p.wait_limit_ns = lim;
+                    p.fault_withhold = 1;
+                }
+            }
             return RF_OK;
         };
         rf_status st;

@@ -91,6 +91,9 @@ size_t block_bytes_of(int fmt);
 inline int64_t block_elems_of(int fmt) { return fmt == RF_Q4_K ? 256 : 32; }
 rf_status last_cuda_error();
 rf_status read_and_clear_device_status();
+// Arms the one-shot wait fault of the next producer-mode launch
+// (rf_debug_arm_wait_fault).
+rf_status arm_wait_fault(uint32_t limit_us);
 int num_sms();
 int64_t max_in_dim(int fmt, int n_x);
 // RF_OK, RF_ERR_TOO_LARGE (in_dim above max_in_dim) or RF_ERR_CUDA (no device).

@@ -1,17 +1,15 @@
 // rf_moe_stream.cu -- the routed MoE FFN with host-resident experts, read
 // through one layer-wide prefetch plan, and the device expert cache.
 //
-// neurostream, "How it works":
-//   1. placement: the slab cache keeps quantized expert windows on the GPU;
-//   2. the router runs first and names the experts this token needs;
-//   3. one plan covers the whole layer -- all active experts x gate/up/down,
-//      in consumption order, chopped into blocks; the prefetcher keeps depth
-//      blocks in flight and refills as each retires, so a block finishing in
-//      gate/up immediately pulls in one of down; windows the cache holds are
-//      skipped;
-//   6. every in-flight block holds an arena reservation.
-// "What the numbers taught us": a per-projection pipeline drains at every
-// projection; the shared plan is what removed the stall.
+// What it follows (neurostream, "How it works" 1-3 and 6; "What the numbers
+// taught us"): quantized expert rows may stay cached on the device; routing
+// comes first and fixes which experts a token touches; a single block list
+// for the whole layer orders every active expert's gate, up and down rows as
+// the launches will read them, and the copy engine runs through that list a
+// bounded number of blocks ahead, so it moves on to down's rows while
+// gate/up still computes instead of draining between projections; rows the
+// cache already holds are not copied; each block in flight occupies arena
+// space until its reader is done.
 //
 // GB300 form: the router kernel's result is read back to the host (the one
 // synchronisation), the host plans, and everything else is stream-ordered:
@@ -47,7 +45,7 @@ struct rf_expert_cache {
     std::vector<bool> ready_recorded;
     cudaEvent_t copied = nullptr;     // block copy into a slot done (re-recorded per block)
     uint64_t clock = 0;
-    rf_expert_cache_stats stats = {};
+    rf_expert_cache_stats_t stats = {};
 };
 
 namespace {
@@ -141,7 +139,7 @@ void rf_expert_cache_destroy(rf_expert_cache *c)
     delete c;
 }
 
-rf_status rf_expert_cache_stats_get(const rf_expert_cache *c, rf_expert_cache_stats *out)
+rf_status rf_expert_cache_stats(const rf_expert_cache *c, rf_expert_cache_stats_t *out)
 {
     if (!c || !out) return RF_ERR_INVALID_ARG;
     *out = c->stats;

@@ -1,14 +1,12 @@
 // rf_stream.cu -- bounded device arena and host-streamed row windows.
 //
-// neurostream, "How it works":
-//   3. the BlockPrefetcher keeps `depth` blocks in flight and refills as each
-//      retires;
-//   4. stream_linear walks a row window: read a block, multiply, accumulate,
-//      retire it, take the next;
-//   6. every in-flight block holds an arena reservation, and allocation waits
-//      until one retires (back-pressure instead of a runaway prefetcher).
-// "Bugs worth knowing about": the block being multiplied keeps its lease until
-// its output exists, so the pipeline holds depth+1 blocks.
+// What it follows (neurostream, "How it works" 3, 4 and 6; "Bugs worth
+// knowing about"): a row window is walked block by block -- fetch, multiply,
+// add to the outputs, give the block back -- with a bounded number of blocks
+// fetched ahead of the one being multiplied; each fetched block takes arena
+// space, and a fetch that finds no free space waits for a block to be given
+// back, so the prefetcher cannot run away.  A block keeps its space until
+// its outputs exist, so a walk with `depth` blocks ahead holds depth+1.
 //
 // GB300 form: the arena is one device allocation cut into depth+1 slots.  The
 // prefetcher is a dedicated copy stream; each block is a cudaMemcpyAsync from
@@ -30,15 +28,25 @@
 // epoch, or one capture.  The first walk of a new epoch starts after
 // everything already enqueued on its stream instead.
 #include <algorithm>
+#include <chrono>
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <thread>
 
 #include "rf_arena.h"
 
 using namespace rf;
 
 namespace rf {
+
+namespace {
+// Host function of an injected stall: holds the copy stream for `ms` ms.
+void CUDART_CB stall_host(void *ms)
+{
+    std::this_thread::sleep_for(std::chrono::milliseconds((int)(intptr_t)ms));
+}
+}  // namespace
 
 int64_t arena_plan_rows(int64_t row_bytes, int64_t n_rows, int64_t block_rows, int depth,
                         size_t arena_bytes)
@@ -218,10 +226,54 @@ rf_status rf_stream_plan(int fmt, int64_t in_dim, int64_t n_rows, int64_t block_
     return RF_OK;
 }
 
-rf_status rf_arena_create(size_t bytes, rf_arena **out)
+namespace {
+
+// Makes `dev` current for the life of the guard and restores the previous
+// device afterwards.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = false;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess) {
+            cudaGetLastError();
+            return;
+        }
+        ok = dev == prev || cudaSetDevice(dev) == cudaSuccess;
+        if (!ok) cudaGetLastError();
+    }
+    ~DeviceGuard()
+    {
+        if (prev >= 0) cudaSetDevice(prev);
+    }
+};
+
+rf_status create_arena(size_t bytes, rf_arena **out);
+
+}  // namespace
+
+rf_status rf_arena_create(size_t bytes, int device, rf_arena **out)
 {
-    if (!out || bytes == 0) return RF_ERR_INVALID_ARG;
+    if (!out || bytes == 0 || device < -1) return RF_ERR_INVALID_ARG;
     *out = nullptr;
+    if (device >= 0) {
+        int n = 0;
+        if (cudaGetDeviceCount(&n) != cudaSuccess) {
+            cudaGetLastError();
+            return RF_ERR_CUDA;
+        }
+        if (device >= n) return RF_ERR_INVALID_ARG;
+        DeviceGuard g(device);
+        if (!g.ok) return RF_ERR_CUDA;
+        return create_arena(bytes, out);
+    }
+    return create_arena(bytes, out);
+}
+
+namespace {
+
+rf_status create_arena(size_t bytes, rf_arena **out)
+{
     rf_arena *a = new (std::nothrow) rf_arena();
     if (!a) return RF_ERR_OOM;
     if (cudaGetDevice(&a->device) != cudaSuccess) {
@@ -275,6 +327,8 @@ rf_status rf_arena_create(size_t bytes, rf_arena **out)
     return RF_OK;
 }
 
+}  // namespace
+
 void rf_arena_destroy(rf_arena *a)
 {
     if (!a) return;
@@ -307,10 +361,92 @@ void rf_arena_destroy(rf_arena *a)
     delete a;
 }
 
-rf_status rf_stream_stats_get(const rf_arena *a, rf_stream_stats *out)
+rf_status rf_stream_stats(const rf_arena *a, rf_stream_stats_t *out)
 {
     if (!a || !out) return RF_ERR_INVALID_ARG;
     *out = a->stats;
+    return RF_OK;
+}
+
+rf_status rf_arena_wait(rf_arena *a, int timeout_ms)
+{
+    if (!a || timeout_ms < 0) return RF_ERR_INVALID_ARG;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) {
+        cudaGetLastError();
+        return RF_ERR_CUDA;
+    }
+    if (cur != a->device) return RF_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(a->mu);
+    // Marks at the end of the copy stream and of every lane stream, plus the
+    // slot-free events of eager walks (readers on the callers' streams).
+    cudaEvent_t marks[1 + rf_arena::kLanes];
+    cudaStream_t streams[1 + rf_arena::kLanes] = {a->copy_stream};
+    for (int l = 0; l < rf_arena::kLanes; ++l) streams[1 + l] = a->lane[l];
+    int n_marks = 0;
+    rf_status st = RF_OK;
+    for (cudaStream_t cs : streams) {
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(cs, &cap) != cudaSuccess) {
+            cudaGetLastError();
+            st = RF_ERR_CUDA;
+            break;
+        }
+        if (cap != cudaStreamCaptureStatusNone) {
+            st = RF_ERR_INVALID_ARG;
+            break;
+        }
+        if (cudaEventCreateWithFlags(&marks[n_marks], cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();
+            st = RF_ERR_CUDA;
+            break;
+        }
+        ++n_marks;
+        if (cudaEventRecord(marks[n_marks - 1], cs) != cudaSuccess) {
+            cudaGetLastError();
+            st = RF_ERR_CUDA;
+            break;
+        }
+    }
+    const auto deadline = std::chrono::steady_clock::now() + std::chrono::milliseconds(timeout_ms);
+    auto done = [&](cudaEvent_t e) -> rf_status {
+        const cudaError_t q = cudaEventQuery(e);
+        if (q == cudaSuccess) return RF_OK;
+        if (q == cudaErrorNotReady) return RF_ERR_TIMEOUT;
+        cudaGetLastError();
+        return RF_ERR_CUDA;
+    };
+    while (st == RF_OK) {
+        rf_status all = RF_OK;
+        for (int i = 0; i < n_marks && all != RF_ERR_CUDA; ++i)
+            if (const rf_status q = done(marks[i])) all = q;
+        if (a->epoch == 0)
+            for (int i = 0; i < rf_arena::kMaxSlots && all != RF_ERR_CUDA; ++i)
+                if (a->freed_recorded[i])
+                    if (const rf_status q = done(a->freed[i])) all = q;
+        if (all != RF_ERR_TIMEOUT) {
+            st = all;
+            break;
+        }
+        if (std::chrono::steady_clock::now() >= deadline) {
+            st = RF_ERR_TIMEOUT;
+            break;
+        }
+        std::this_thread::sleep_for(std::chrono::microseconds(50));
+    }
+    for (int i = 0; i < n_marks; ++i) cudaEventDestroy(marks[i]);
+    return st;
+}
+
+rf_status rf_arena_inject_fault(rf_arena *a, int kind, int64_t block, int ms)
+{
+    if (!a || block < 0 || ms < 0 || ms > 10000) return RF_ERR_INVALID_ARG;
+    if (kind != RF_FAULT_NONE && kind != RF_FAULT_COPY_FAIL && kind != RF_FAULT_COPY_STALL)
+        return RF_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(a->mu);
+    a->fault_kind = kind;
+    a->fault_block = block;
+    a->fault_ms = ms;
     return RF_OK;
 }
 
@@ -324,6 +460,14 @@ rf_status rf_stream_linear(int fmt, const void *host_W, int64_t in_dim, int64_t 
         return RF_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(host_W) & 15u) != 0) return RF_ERR_MISALIGNED;
     if (const rf_status c = check_in_dim(fmt, in_dim, 1)) return c;
+    {
+        int cur = -1;
+        if (cudaGetDevice(&cur) != cudaSuccess) {
+            cudaGetLastError();
+            return RF_ERR_CUDA;
+        }
+        if (cur != a->device) return RF_ERR_INVALID_ARG;
+    }
     cudaPointerAttributes attr;
     if (cudaPointerGetAttributes(&attr, host_W) != cudaSuccess) {
         cudaGetLastError();
@@ -355,7 +499,12 @@ rf_status rf_stream_linear(int fmt, const void *host_W, int64_t in_dim, int64_t 
     // copies and launches would only add their fixed costs.
     const int64_t nblk = (n_rows + eff - 1) / eff;
     const bool packed = stride == (size_t)(eff * rb);
-    if (nblk > 1 && nblk <= slots && (packed || nblk <= 16)) {
+    // A one-shot injected fault, taken by this walk.
+    const int fault = a->fault_kind;
+    const int64_t fault_at = a->fault_block;
+    const int fault_ms = a->fault_ms;
+    a->fault_kind = RF_FAULT_NONE;
+    if (nblk > 1 && nblk <= slots && (packed || nblk <= 16) && fault == RF_FAULT_NONE) {
         int first = 0;
         uint8_t *base = nullptr;
         const int64_t last_rows = n_rows - (nblk - 1) * eff;
@@ -400,14 +549,28 @@ rf_status rf_stream_linear(int fmt, const void *host_W, int64_t in_dim, int64_t 
                 eff * rb <= (int64_t)(1 << 20) && (n_rows + eff - 1) / eff >= 2 * rf_arena::kLanes};
     if (const rf_status st = fan.begin()) return st;
     int64_t blocks = 0;
+    rf_status err = RF_OK;
     for (int64_t r0 = row_start; r0 < row_end; r0 += eff) {
         const int64_t nr = std::min(eff, row_end - r0);
         int slot = 0;
         uint8_t *dst = nullptr;
         cudaStream_t cs = s;
-        if (const rf_status st = fan.stream(blocks, &cs)) return st;
-        if (const rf_status st = arena_fetch(a, cs, hw + r0 * rb, (size_t)(nr * rb), &slot, &dst))
-            return st;
+        if ((err = fan.stream(blocks, &cs)) != RF_OK) break;
+        if (fault != RF_FAULT_NONE && blocks == fault_at) {
+            if (fault == RF_FAULT_COPY_FAIL) {   // as if this block's copy had failed
+                err = RF_ERR_CUDA;
+                break;
+            }
+            if (cudaLaunchHostFunc(a->copy_stream, stall_host, reinterpret_cast<void *>(
+                                                                    (intptr_t)fault_ms)) !=
+                cudaSuccess) {
+                cudaGetLastError();
+                err = RF_ERR_CUDA;
+                break;
+            }
+        }
+        if ((err = arena_fetch(a, cs, hw + r0 * rb, (size_t)(nr * rb), &slot, &dst)) != RF_OK)
+            break;
         Job J;
         std::memset(&J, 0, sizeof(J));
         J.term[0] = Term{dst, 0, -1, 0, 0};
@@ -422,15 +585,22 @@ rf_status rf_stream_linear(int fmt, const void *host_W, int64_t in_dim, int64_t 
         d.n_jobs = 1;
         d.x[0] = x;
         d.n_x = 1;
-        const rf_status st = launch_rowwin(d, cs);
-        if (st != RF_OK) return st;
-        // Retire: the slot is free once this GEMV has run.
-        if (const rf_status st2 = arena_release(a, cs, slot)) return st2;
+        err = launch_rowwin(d, cs);
+        // Retire: the slot is free once this GEMV has run (or, when the launch
+        // failed, once the work before it on the stream has).
+        const rf_status rel = arena_release(a, cs, slot);
+        if (err != RF_OK) break;
+        if ((err = rel) != RF_OK) break;
         ++blocks;
     }
-    if (const rf_status st = fan.end()) return st;
-    a->stats.calls += 1;
+    // On an error the walk stops enqueueing; the blocks already enqueued keep
+    // their slots' release events, and the lanes rejoin the caller's stream,
+    // so later work on `stream` and on the arena stays ordered after them.
+    const rf_status joined = fan.end();
+    if (err == RF_OK) err = joined;
     a->stats.blocks += (uint64_t)blocks;
+    if (err != RF_OK) return err;
+    a->stats.calls += 1;
     a->stats.peak_bytes = std::max<uint64_t>(a->stats.peak_bytes, peak);
     a->stats.slot_bytes = stride;
     a->stats.slots = slots;

@@ -29,3 +29,50 @@ def swiglu_h_tol(g_ref, u_ref, tg, tu):
     |silu'| <= 1.1, plus fp32 rounding of the epilogue."""
     silu = g_ref / (1.0 + np.exp(-g_ref))
     return 1.1 * tg * (np.abs(u_ref) + tu) + np.abs(silu) * tu + 1e-6 * np.abs(silu * u_ref)
+
+
+def moe_reference(fmt, G, U, D, n_ff, n_embd, x, logits, top_k):
+    """The routed SwiGLU FFN computed by the oracle alone (nothing from the
+    CUDA path goes in), with bounds derived from the per-GEMV tolerance:
+      h_k = silu(G_k x) * (U_k x)     within swiglu_h_tol of the GPU's h_k;
+      y   = sum_k w_k D_k h_k         the GPU's down GEMV runs on its own h_k,
+            so per row |dy| <= sum_k w_k (1e-3 ||D_k,r|| (||h_k|| + ||dh_k||)
+                                          + ||D_k,r|| ||dh_k||)
+            (Cauchy-Schwarz on the h error), plus fp32 rounding of the
+            router weights and the weighted sum (1e-6 relative).
+    Returns a dict with idx, w, h (list), tol_h (list), y, tol_y."""
+    idx, w = oracle.router_topk(logits, top_k)
+    y = np.zeros(n_embd)
+    tol_y = np.zeros(n_embd)
+    hs, ths = [], []
+    for k, e in enumerate(idx):
+        e = int(e)
+        Ge, Ue = G[e * n_ff:(e + 1) * n_ff], U[e * n_ff:(e + 1) * n_ff]
+        De = D[e * n_embd:(e + 1) * n_embd]
+        g = oracle.gemv(fmt, Ge, 0, n_ff, n_embd, x)
+        u = oracle.gemv(fmt, Ue, 0, n_ff, n_embd, x)
+        h = oracle.silu_vec(g) * u
+        th = swiglu_h_tol(g, u, gemv_tol(fmt, Ge, 0, n_ff, n_embd, x),
+                          gemv_tol(fmt, Ue, 0, n_ff, n_embd, x))
+        yk = oracle.gemv(fmt, De, 0, n_embd, n_ff, h)
+        nD = oracle.row_norms(fmt, De, 0, n_embd, n_ff)
+        nh, nth = float(np.linalg.norm(h)), float(np.linalg.norm(th))
+        y += float(w[k]) * yk
+        tol_y += float(w[k]) * (1e-3 * nD * (nh + nth) + nD * nth) + 1e-6 * np.abs(yk)
+        hs.append(h)
+        ths.append(th)
+    return {"idx": idx, "w": w, "h": hs, "tol_h": ths, "y": y, "tol_y": tol_y}
+
+
+def check_moe(ref, y, idx=None, w=None, h=None, what=""):
+    """Compares a GPU MoE result (and, when given, its routing and h) with
+    moe_reference: indices equal, weights within fp32 rounding, h and y
+    within the derived bounds."""
+    if idx is not None:
+        assert list(np.asarray(idx).tolist()) == list(ref["idx"].tolist()), f"{what}: routing"
+    if w is not None:
+        np.testing.assert_allclose(np.asarray(w, np.float64), ref["w"], rtol=1e-5, atol=1e-7)
+    if h is not None:
+        for k in range(len(ref["h"])):
+            assert_gemv_close(np.asarray(h[k]), ref["h"][k], ref["tol_h"][k], f"{what}: h[{k}]")
+    assert_gemv_close(np.asarray(y), ref["y"], ref["tol_y"], f"{what}: y")

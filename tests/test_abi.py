@@ -144,7 +144,7 @@ def test_newer_entry_points_check_arguments_first(L):
     assert L.rf_expert_cache_create(rf.Q4_0, 64, 64, 0, ctypes.byref(h)) == 1
     assert L.rf_expert_cache_create(rf.Q4_0, 64, 64, 1025, ctypes.byref(h)) == 1
     assert L.rf_expert_cache_create(rf.Q4_0, 64, 64, 2, None) == 1
-    assert L.rf_expert_cache_stats_get(None, ctypes.byref(rf.ExpertCacheStats())) == 1
+    assert L.rf_expert_cache_stats(None, ctypes.byref(rf.ExpertCacheStats())) == 1
     L.rf_expert_cache_destroy(None)   # no-op
     # rf_moe_ffn_streamed(fmt, logits, E, k, hG, hU, hD, n_ff, n_embd, br, depth, arena, cache,
     #                     x, y, workspace, stream)
@@ -165,4 +165,34 @@ def test_no_gpu_means_cuda_error_not_fallback(L):
     assert L.rf_gemv(rf.Q8_0, p16, 0, 1, 32, p16, p16, None) == 5
     assert L.rf_max_in_dim(rf.Q8_0, 1) == 0
     h = ctypes.c_void_p()
-    assert L.rf_arena_create(1 << 20, ctypes.byref(h)) in (5, 7)
+    assert L.rf_arena_create(1 << 20, -1, ctypes.byref(h)) in (5, 7)
+
+
+def test_boundary_names_and_conventions():
+    """The boundary keeps the survey's names and signatures: rf_arena_create
+    takes the device, the arena counters are read by rf_stream_stats, and the
+    header's convention block lists every call that blocks the host."""
+    text = rf.HEADER.read_text()
+    decl = " ".join(text.split())
+    assert "rf_status rf_arena_create(size_t bytes, int device, rf_arena **out);" in decl
+    assert "rf_status rf_stream_stats(const rf_arena *arena, rf_stream_stats_t *out);" in decl
+    assert "rf_status rf_arena_wait(rf_arena *arena, int timeout_ms);" in decl
+    conv = text[:text.index("#ifndef RF_H")]
+    for name in ("rf_device_status", "rf_arena_destroy", "rf_arena_wait",
+                 "rf_expert_cache_destroy", "rf_moe_ffn_streamed"):
+        assert name in conv, name
+    for name in ("rf_stream_stats", "rf_arena_wait", "rf_arena_inject_fault",
+                 "rf_debug_arm_wait_fault", "rf_expert_cache_stats"):
+        assert name in rf.header_symbols(), name
+
+
+def test_failure_hooks_check_arguments(L):
+    """The test hooks and the deadline wait refuse bad arguments on the host."""
+    assert L.rf_arena_wait(None, 10) == 1
+    assert L.rf_arena_inject_fault(None, 1, 0, 0) == 1
+    assert L.rf_debug_arm_wait_fault(2000001) == 1
+    assert L.rf_debug_arm_wait_fault(0) == 0   # disarm
+    h = ctypes.c_void_p()
+    assert L.rf_arena_create(0, -1, ctypes.byref(h)) == 1
+    assert L.rf_arena_create(1 << 20, -2, ctypes.byref(h)) == 1
+    assert L.rf_arena_create(1 << 20, -1, None) == 1

@@ -8,7 +8,7 @@ import pytest
 
 import oracle
 import synthetic as syn
-from gpu_helpers import dev_tensor
+from gpu_helpers import check_moe, dev_tensor, moe_reference
 
 pytestmark = pytest.mark.gpu
 
@@ -49,13 +49,19 @@ CASES = [  # fmt, E, n_ff, n_embd, top_k
 @pytest.mark.parametrize("fmt,E,n_ff,n_embd,top_k", CASES)
 def test_streamed_moe_bit_identical_to_resident(rf, fmt, E, n_ff, n_embd, top_k):
     import torch
-    _, (Gd, Ud, Dd), (Gh, Uh, Dh) = experts(fmt, E, n_ff, n_embd, 100 + fmt)
-    x = dev_tensor(syn.normal_f32(n_embd, 5))
+    (G, U, D), (Gd, Ud, Dd), (Gh, Uh, Dh) = experts(fmt, E, n_ff, n_embd, 100 + fmt)
+    x_np = syn.normal_f32(n_embd, 5)
+    x = dev_tensor(x_np)
     arena = rf.Arena(8 << 20)
     caches = [None, rf.ExpertCache(fmt, n_ff, n_embd, 2), rf.ExpertCache(fmt, n_ff, n_embd, E)]
+    refs = {}
     try:
         for seed in range(4):
-            logits = dev_tensor(syn.router_logits(E, 40 + seed % 2))   # tokens repeat routing
+            lg = syn.router_logits(E, 40 + seed % 2)   # tokens repeat routing
+            logits = dev_tensor(lg)
+            if seed % 2 not in refs:   # the oracle on the same bytes, nothing from the GPU
+                refs[seed % 2] = moe_reference(fmt, G, U, D, n_ff, n_embd, x_np, lg, top_k)
+            ref = refs[seed % 2]
             y_ref, ws_ref = rf.moe_ffn(fmt, logits, top_k, Gd, Ud, Dd, n_ff, n_embd, 0, x)
             h_ref = rf.moe_workspace_views(ws_ref, top_k, n_ff)[2]
             for cache in caches:
@@ -64,10 +70,13 @@ def test_streamed_moe_bit_identical_to_resident(rf, fmt, E, n_ff, n_embd, top_k)
                                                 block_rows, depth, arena, x, cache=cache)
                     idx, w, h = rf.moe_workspace_views(ws, top_k, n_ff)
                     what = (seed, None if cache is None else cache.stats()["slots"], block_rows)
+                    # against the oracle on its own bytes (hits, fills and
+                    # bypasses all included) ...
+                    check_moe(ref, y.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy(),
+                              h.cpu().numpy(), what=str(what))
+                    # ... and bit-identical to the resident path
                     assert np.array_equal(bits(y), bits(y_ref)), what
                     assert np.array_equal(bits(h), bits(h_ref)), what
-                    idx_ref, _ = oracle.router_topk(syn.router_logits(E, 40 + seed % 2), top_k)
-                    assert idx.cpu().numpy().tolist() == idx_ref.tolist()
     finally:
         torch.cuda.synchronize()
         for c in caches:
@@ -115,16 +124,20 @@ def test_expert_cache_directory_and_bytes(rf):
 def test_cache_smaller_than_top_k_bypasses(rf):
     import torch
     fmt, E, n_ff, n_embd, k = syn.MXFP4, 16, 320, 2880, 4
-    _, (Gd, Ud, Dd), (Gh, Uh, Dh) = experts(fmt, E, n_ff, n_embd, 20)
-    x = dev_tensor(syn.normal_f32(n_embd, 21))
-    logits = dev_tensor(syn.router_logits(E, 22))
+    (G, U, D), (Gd, Ud, Dd), (Gh, Uh, Dh) = experts(fmt, E, n_ff, n_embd, 20)
+    x_np, lg = syn.normal_f32(n_embd, 21), syn.router_logits(E, 22)
+    x, logits = dev_tensor(x_np), dev_tensor(lg)
+    ref = moe_reference(fmt, G, U, D, n_ff, n_embd, x_np, lg, k)
     arena = rf.Arena(8 << 20)
     cache = rf.ExpertCache(fmt, n_ff, n_embd, 1)
     try:
         y_ref, _ = rf.moe_ffn(fmt, logits, k, Gd, Ud, Dd, n_ff, n_embd, 0, x)
         for _ in range(2):
-            y, _ = rf.moe_ffn_streamed(fmt, logits, k, Gh, Uh, Dh, n_ff, n_embd, 64, 3, arena, x,
-                                       cache=cache)
+            y, ws = rf.moe_ffn_streamed(fmt, logits, k, Gh, Uh, Dh, n_ff, n_embd, 64, 3, arena,
+                                        x, cache=cache)
+            idx, w, h = rf.moe_workspace_views(ws, k, n_ff)
+            check_moe(ref, y.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy(), h.cpu().numpy(),
+                      what="hit and bypasses")
             assert np.array_equal(bits(y), bits(y_ref))
         st = cache.stats()
         assert (st["lookups"], st["hits"], st["fills"], st["bypasses"]) == (8, 1, 1, 6)

@@ -9,7 +9,8 @@ import pytest
 
 import oracle
 import synthetic as syn
-from gpu_helpers import assert_gemv_close, dev_tensor, gemv_tol, swiglu_h_tol
+from gpu_helpers import (assert_gemv_close, check_moe, dev_tensor, gemv_tol, moe_reference,
+                         swiglu_h_tol)
 
 pytestmark = pytest.mark.gpu
 
@@ -93,6 +94,41 @@ def test_gemv_x_with_wide_dynamic_range(rf, fmt):
     y = rf.gemv(fmt, dev_tensor(W), 0, rows, in_dim, dev_tensor(x)).cpu().numpy()
     ref = oracle.gemv(fmt, W, 0, rows, in_dim, x)
     assert_gemv_close(y, ref, gemv_tol(fmt, W, 0, rows, in_dim, x), "dynamic range")
+
+
+@pytest.mark.parametrize("fmt", FMTS + [syn.Q4_K])
+def test_gemv_activation_rounding_aligned_with_weights(rf, fmt):
+    """The kernel turns each 32-element activation block into fixed-point
+    digits X = rint(x * 2^s), |X| < 2^15, s set by the block maximum.  Here
+    every block's maximum is exactly 1.0 (so s = 14) and every other x_j sits
+    (0.5 -+ 2^-8) units of 2^-14 off the grid, on the side that makes its
+    rounding error carry the sign of w_j: the errors add up instead of
+    cancelling.  The measured error must stay within the stated bound
+    sqrt(32) * 2^-15 * ||W_r|| * ||x|| (and so within 1e-3 * ||W_r|| * ||x||),
+    and must be the aligned error the rounding predicts (at least half of
+    2^-14 * (0.5 - 2^-8) * sum_j |w_j|), which shows that the rounding, and
+    not something coarser or finer, is what the kernel does."""
+    rows, in_dim = 96, 1024
+    W = syn.quant_matrix(fmt, rows, in_dim, seed=130 + fmt)
+    dense = oracle.dequantize(fmt, W).reshape(rows, in_dim).astype(np.float64)
+    rng = np.random.default_rng(131)
+    for r in (0, 37, 95):
+        w = dense[r]
+        sig = rng.choice([-1.0, 1.0], size=in_dim)
+        n = rng.integers(1 << 13, (1 << 14) - 1, size=in_dim).astype(np.float64)
+        up = np.where(sig * np.sign(w) > 0, 1.0, -1.0)   # round away or toward zero
+        x = sig * (n + 0.5 + up * 2.0 ** -8) * 2.0 ** -14
+        x[::32] = 1.0                                      # each block's maximum
+        x = x.astype(np.float32)
+        assert np.all(x.astype(np.float64) * 2 ** 14 % 1 != 0.5)   # no ties
+        y = rf.gemv(fmt, dev_tensor(W), r, r + 1, in_dim, dev_tensor(x)).cpu().numpy()
+        ref = oracle.gemv(fmt, W, r, r + 1, in_dim, x)
+        err = abs(float(y[0]) - float(ref[0]))
+        nw, nx = float(np.linalg.norm(w)), float(np.linalg.norm(x.astype(np.float64)))
+        bound = math.sqrt(32) * 2.0 ** -15 * nw * nx
+        assert err <= bound and err <= 1e-3 * nw * nx, (r, err, bound)
+        aligned = 2.0 ** -14 * (0.5 - 2.0 ** -8) * float(np.abs(w).sum())
+        assert err >= 0.5 * aligned, (r, err, aligned)
 
 
 @pytest.mark.parametrize("fmt", FMTS)
@@ -436,24 +472,10 @@ def moe_check(rf, fmt, E, n_ff, n_embd, top_k, block_rows, seed):
     y, ws = rf.moe_ffn(fmt, dev_tensor(logits), top_k, dev_tensor(G), dev_tensor(U),
                        dev_tensor(D), n_ff, n_embd, block_rows, dev_tensor(x))
     idx, w, h = (t.cpu().numpy() for t in rf.moe_workspace_views(ws, top_k, n_ff))
-    idx_ref, w_ref = oracle.router_topk(logits, top_k)
-    assert idx.tolist() == idx_ref.tolist()
     y = y.cpu().numpy()
-    tol_y = np.zeros(n_embd)
-    y_ref = np.zeros(n_embd)
-    for k, e in enumerate(idx_ref):
-        g0 = int(e) * n_ff
-        Ge, Ue, De = G[g0:g0 + n_ff], U[g0:g0 + n_ff], D[int(e) * n_embd:(int(e) + 1) * n_embd]
-        g_ref = oracle.gemv(fmt, Ge, 0, n_ff, n_embd, x)
-        u_ref = oracle.gemv(fmt, Ue, 0, n_ff, n_embd, x)
-        h_ref = oracle.silu_vec(g_ref) * u_ref
-        th = swiglu_h_tol(g_ref, u_ref, gemv_tol(fmt, Ge, 0, n_ff, n_embd, x),
-                          gemv_tol(fmt, Ue, 0, n_ff, n_embd, x))
-        assert_gemv_close(h[k], h_ref, th, f"h expert {e}")
-        yk = oracle.gemv(fmt, De, 0, n_embd, n_ff, h[k].astype(np.float64))
-        y_ref += float(w[k]) * yk
-        tol_y += float(w[k]) * gemv_tol(fmt, De, 0, n_embd, n_ff, h[k])
-    assert_gemv_close(y, y_ref, tol_y + 1e-6 * np.abs(y_ref), "moe y")
+    # the oracle alone, with bounds derived from the per-GEMV tolerance
+    check_moe(moe_reference(fmt, G, U, D, n_ff, n_embd, x, logits, top_k), y, idx, w, h,
+              what="moe")
     # end to end against the oracle's own fp64 chain (router weights in fp64)
     y_e2e, _, _ = oracle.moe_ffn(fmt, logits, top_k, G, U, D, n_ff, n_embd, x)
     scale = float(np.abs(y_e2e).max())
@@ -498,13 +520,19 @@ def test_moe_ffn_host_zero_copy_bit_identical(rf):
     G = syn.stacked_experts(fmt, E, n_ff, n_embd, 80)
     U = syn.stacked_experts(fmt, E, n_ff, n_embd, 81)
     D = syn.stacked_experts(fmt, E, n_embd, n_ff, 82)
-    x = dev_tensor(syn.normal_f32(n_embd, 83))
+    x_np = syn.normal_f32(n_embd, 83)
+    x = dev_tensor(x_np)
     hg, hu, hd = (torch.from_numpy(a).pin_memory() for a in (G, U, D))
     Gd, Ud, Dd = dev_tensor(G), dev_tensor(U), dev_tensor(D)
     for seed in (84, 85):
-        logits = dev_tensor(syn.router_logits(E, seed))
+        lg = syn.router_logits(E, seed)
+        logits = dev_tensor(lg)
         y_dev, _ = rf.moe_ffn(fmt, logits, top_k, Gd, Ud, Dd, n_ff, n_embd, br, x)
-        y_host, _ = rf.moe_ffn_host(fmt, logits, top_k, hg, hu, hd, n_ff, n_embd, br, x)
+        y_host, ws = rf.moe_ffn_host(fmt, logits, top_k, hg, hu, hd, n_ff, n_embd, br, x)
+        # against the oracle on the same bytes, then bit-identical to resident
+        idx, w, h = (t.cpu().numpy() for t in rf.moe_workspace_views(ws, top_k, n_ff))
+        check_moe(moe_reference(fmt, G, U, D, n_ff, n_embd, x_np, lg, top_k),
+                  y_host.cpu().numpy(), idx, w, h, what=f"zero copy {seed}")
         assert np.array_equal(bits(y_host.cpu().numpy()), bits(y_dev.cpu().numpy())), seed
     with pytest.raises(rf.RFError) as e:   # pageable memory is refused
         rf.moe_ffn_host(fmt, logits, top_k, torch.from_numpy(G), hu, hd, n_ff, n_embd, br, x)

@@ -419,3 +419,53 @@ def test_moe_is_weighted_sum_of_selected_experts():
     assert sorted(idx.tolist()) == sorted(best)
     ref = sum(wk * parts[e] for wk, e in zip(w, idx))
     assert np.allclose(y, ref, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------- row norms
+# Every GPU parity tolerance is 1e-3 * ||W_r||_2 * ||x||_2 with W_r the
+# dequantized row, so the oracle's row norms are pinned on their own: by
+# hand-worked blocks, by a library norm of the (separately pinned) dequantized
+# rows, and by closed forms.
+
+def _row(*blocks):
+    return np.frombuffer(b"".join(blocks), dtype=np.uint8)
+
+
+def test_row_norms_hand_blocks():
+    # Q8_0, d = 0.5, q = 1, -1, 127, -128: values 0.5, -0.5, 63.5, -64, rest 0
+    q8 = bytes([0x00, 0x38, 0x01, 0xFF, 0x7F, 0x80]) + bytes(28)
+    assert oracle.row_norms(Q8_0, _row(q8), 0, 1, 32)[0] == math.sqrt(
+        0.25 + 0.25 + 63.5 ** 2 + 64.0 ** 2)
+    # two Q4_0 blocks in one row: (d = 1: e0 = 7, e1 = -8, e17 = -7, rest 0)
+    # and (d = 2, every quant 0: 32 values of -16)
+    a = bytes([0x00, 0x3C, 0x8F, 0x10]) + bytes([0x88] * 14)
+    b = bytes([0x00, 0x40]) + bytes(16)
+    assert oracle.row_norms(Q4_0, _row(a, b), 0, 1, 64)[0] == math.sqrt(
+        49 + 64 + 49 + 32 * 256)
+    # MXFP4, scale 1: 0.5, 6, -0, -6, rest 0
+    mx = bytes([0x7F, 0x71, 0xF8]) + bytes(14)
+    assert oracle.row_norms(MXFP4, _row(mx), 0, 1, 32)[0] == math.sqrt(0.25 + 36 + 36)
+
+
+def test_row_norms_closed_forms():
+    # constant quants: |d * c| * sqrt(in_dim); d = 0.25, c = -3, in_dim = 256
+    blk = bytes([0x00, 0x34]) + bytes([0xFD] * 32)
+    assert oracle.row_norms(Q8_0, _row(*[blk] * 8), 0, 1, 256)[0] == 0.75 * 16
+    # zero scale: every value is 0 whatever the quants
+    zero = bytes([0x00, 0x00]) + bytes([0x7F] * 32)
+    assert oracle.row_norms(Q8_0, _row(*[zero] * 4), 0, 1, 128)[0] == 0.0
+    # Q4_0 quants all 8 (value 0) except one nibble 15 (value 7*d), d = 2
+    one = bytes([0x00, 0x40, 0x8F]) + bytes([0x88] * 15)
+    assert oracle.row_norms(Q4_0, _row(one, one, one, one), 0, 1, 128)[0] == math.sqrt(4 * 196)
+
+
+@pytest.mark.parametrize("fmt", FMTS + [oracle.Q4_K])
+def test_row_norms_match_library_norm_of_dequantized_rows(fmt):
+    rows, in_dim = 37, 512
+    W = syn.quant_matrix(fmt, rows, in_dim, seed=90 + fmt)
+    dense = oracle.dequantize(fmt, W).reshape(rows, in_dim).astype(np.float64)
+    ref = np.linalg.norm(dense, axis=1)
+    got = oracle.row_norms(fmt, W, 0, rows, in_dim)
+    np.testing.assert_allclose(got, ref, rtol=1e-13, atol=0)
+    # a window reports the same rows, in window order
+    assert np.array_equal(oracle.row_norms(fmt, W, 5, 20, in_dim), got[5:20])
