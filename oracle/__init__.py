@@ -7,10 +7,11 @@ the CUDA path.  The arithmetic lives in ``rf_oracle.c`` (plain C, fp64); this
 module only builds it with gcc and marshals numpy arrays through ctypes.
 
 Every function cites the page passage it follows in ``rf_oracle.c``.  Parity
-status: the MXFP4 block layout, the GELU activation of the host-streamed FFN
-and Q4_K's scale packing and quant order are "parity unpinned" by the pages
-themselves (no page prints them); they are pinned in tests by the OCP MX
-format definition, the GELU identities and a reduction of Q4_K to Q4_0.
+status: the MXFP4 block layout, the GELU activation of the host-streamed FFN,
+Q4_K's scale packing and quant order, and the Q6_K layout are "parity
+unpinned" by the pages themselves (no page prints them); they are pinned in
+tests by the OCP MX format definition, the GELU identities, a reduction of
+Q4_K to Q4_0 and a reduction of Q6_K to Q8_0.
 """
 from __future__ import annotations
 
@@ -26,8 +27,8 @@ _SRC = _HERE / "rf_oracle.c"
 _LIBDIR = _HERE / "_lib"
 _SO = _LIBDIR / "liboracle.so"
 
-Q4_0, Q8_0, MXFP4, Q4_K = 2, 8, 39, 12
-FORMATS = {"Q4_0": Q4_0, "Q8_0": Q8_0, "MXFP4": MXFP4, "Q4_K": Q4_K}
+Q4_0, Q8_0, MXFP4, Q4_K, Q6_K = 2, 8, 39, 12, 14
+FORMATS = {"Q4_0": Q4_0, "Q8_0": Q8_0, "MXFP4": MXFP4, "Q4_K": Q4_K, "Q6_K": Q6_K}
 
 
 def build(force: bool = False) -> Path:
@@ -74,6 +75,8 @@ def _declare(L: ctypes.CDLL) -> None:
     L.orc_block_elems.argtypes = [_I]
     L.orc_block_elems.restype = _I64
     L.orc_q4k_scale_min.argtypes = [_P, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]
+    L.orc_q6k_quant.argtypes = [_P, _I]
+    L.orc_q6k_quant.restype = _I
     L.orc_dequant_block.argtypes = [_I, _P, _P]
     L.orc_dequantize.argtypes = [_I, _P, _I64, _P]
     L.orc_gemv.argtypes = [_I, _P, _I64, _I64, _I64, _P, _P]
@@ -128,6 +131,12 @@ def row_bytes(fmt: int, in_dim: int) -> int:
 
 def block_elems(fmt: int) -> int:
     return lib().orc_block_elems(fmt)
+
+
+def q6k_quant(block, e: int) -> int:
+    """Q6_K element e's 6-bit quant (0..63) from one 210-byte block."""
+    b = np.ascontiguousarray(block, dtype=np.uint8)
+    return lib().orc_q6k_quant(_ptr(b), e)
 
 
 def q4k_scale_min(scale_bytes, j: int):

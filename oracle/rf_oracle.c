@@ -29,6 +29,11 @@
  *            (8 scales and 8 mins packed as 6-bit values), 128 B of 4-bit
  *            quants; an element is d*sc*q - dmin*m with (sc, m) its
  *            sub-block's scale and min.
+ *   [RF-M5Q6] RAMforge, "Milestone 5 - Native Quantized Tensor Support" (and
+ *            its legacy tensor list): Q6_K is one of the K-quant block
+ *            layouts; neurostream, "Supported" models list: Q6_K decoded
+ *            bit-exact against the reference GGUF implementation.  Neither
+ *            page prints the layout.
  *
  * Readings where the pages are silent:
  *   - fp16 scale: IEEE-754 binary16, little endian, first two bytes.
@@ -57,6 +62,16 @@
  *   - SwiGLU: silu(g)*u with silu(z) = z/(1+exp(-z)); GELU (erf form) for the
  *     host-streamed dense FFN, whose activation no page states: PARITY
  *     UNPINNED by the pages (pinned by the GELU identities).
+ *   - Q6_K (the GGML layout; PARITY UNPINNED by the pages, which name the
+ *     format only): 256 elements in 210 B -- 128 B of low 4-bit quant parts
+ *     (ql), 64 B of high 2-bit parts (qh), 16 signed 8-bit scales, then an
+ *     fp16 d.  Element e = 128*n + 32*k + l (half n, quarter k, lane l < 32)
+ *     has q = low | high << 4 with low the low nibble (k = 0, 1) or high
+ *     nibble (k = 2, 3) of ql[64*n + l + 32*(k & 1)] and high = bits
+ *     2k..2k+1 of qh[32*n + l]; its value is d * scale[e / 16] * (q - 32).
+ *     Every such value needs at most 24 significant bits (11 + 8 + 6 bits),
+ *     so it is exact in float.  Pinned in tests by hand-worked bytes and by
+ *     a reduction to Q8_0.
  *
  * Floating point: all arithmetic in double; dequantized weights are returned
  * as float (every value d*q, d*(q-8) and e2m1*2^k is exactly representable).
@@ -70,6 +85,7 @@
 #define ORC_Q8_0 8
 #define ORC_MXFP4 39
 #define ORC_Q4_K 12
+#define ORC_Q6_K 14
 
 #define ORC_OK 0
 #define ORC_EINVAL 1
@@ -126,14 +142,27 @@ int64_t orc_block_bytes(int fmt)
     case ORC_Q4_0: return 18;   /* [RF-M5] */
     case ORC_MXFP4: return 17;  /* 1 scale byte + 16 code bytes */
     case ORC_Q4_K: return 144;  /* [RF-M5K] */
+    case ORC_Q6_K: return 210;  /* 128 + 64 + 16 + 2, the Q6_K reading */
     default: return 0;
     }
 }
 
-/* Elements per block: 32, or 256 for Q4_K's super-block. */
+/* Elements per block: 32, or 256 for the K-quant super-blocks. */
 int64_t orc_block_elems(int fmt)
 {
-    return fmt == ORC_Q4_K ? 256 : (orc_block_bytes(fmt) ? 32 : 0);
+    if (fmt == ORC_Q4_K || fmt == ORC_Q6_K)
+        return 256;
+    return orc_block_bytes(fmt) ? 32 : 0;
+}
+
+/* Q6_K element e's 6-bit quant (0..63) from the ql and qh parts. */
+int orc_q6k_quant(const uint8_t *blk, int e)
+{
+    int n = e / 128, k = (e % 128) / 32, l = e % 32;
+    int lowbyte = blk[64 * n + l + 32 * (k & 1)];
+    int low = k < 2 ? (lowbyte & 15) : (lowbyte >> 4);
+    int high = (blk[128 + 32 * n + l] >> (2 * k)) & 3;
+    return low | (high << 4);
 }
 
 int64_t orc_row_bytes(int fmt, int64_t in_dim)
@@ -178,6 +207,13 @@ int orc_dequant_block(int fmt, const uint8_t *blk, float *out)
                 out[64 * i + 32 + l] = (float)(d * sc1 * hi - dmin * m1);
             }
         }
+        return ORC_OK;
+    }
+    if (fmt == ORC_Q6_K) {
+        double d = orc_fp16_to_double((uint16_t)(blk[208] | (blk[209] << 8)));
+        const int8_t *scale = (const int8_t *)(blk + 192);
+        for (j = 0; j < 256; j++)
+            out[j] = (float)(d * (double)scale[j / 16] * (double)(orc_q6k_quant(blk, j) - 32));
         return ORC_OK;
     }
     if (fmt == ORC_Q8_0) {

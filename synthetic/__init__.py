@@ -15,6 +15,10 @@ Distributions (the workloads' statement):
            scale bytes uniform random (so every 6-bit scale and min is
            uniform over [0, 63]); d = fp16(U[1e-4, 1e-3]), dmin =
            fp16(U[1e-4, 1e-3]).
+  Q6_K   : 256-element super-blocks of 210 B: the 192 quant bytes (low and
+           high parts) and the 16 signed scale bytes uniform random (every
+           6-bit quant uniform over [0, 63], every scale over [-128, 127]),
+           then d = fp16(U[1e-4, 1e-3]) in the last two bytes.
   x      : fp32 N(0, 1); router logits fp32 N(0, 1) (or, for expert-cache
            runs, a fixed per-expert bias 0.5*N(0,1) plus N(0,1) per token).
 
@@ -28,13 +32,17 @@ from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
-Q4_0, Q8_0, MXFP4, Q4_K = 2, 8, 39, 12
-FMT_IDS = {"Q4_0": Q4_0, "Q8_0": Q8_0, "MXFP4": MXFP4, "Q4_K": Q4_K}
+Q4_0, Q8_0, MXFP4, Q4_K, Q6_K = 2, 8, 39, 12, 14
+FMT_IDS = {"Q4_0": Q4_0, "Q8_0": Q8_0, "MXFP4": MXFP4, "Q4_K": Q4_K, "Q6_K": Q6_K}
 FMT_NAMES = {v: k for k, v in FMT_IDS.items()}
 # (block bytes, quant bytes after the scale, scale bytes)
-_LAYOUT = {Q8_0: (34, 32, 2), Q4_0: (18, 16, 2), MXFP4: (17, 16, 1), Q4_K: (144, 140, 4)}
-DEFAULT_SCALE = {Q8_0: (1e-3, 1e-2), Q4_0: (1e-3, 2e-2), MXFP4: (-8, -2), Q4_K: (1e-4, 1e-3)}
-_ELEMS = {Q8_0: 32, Q4_0: 32, MXFP4: 32, Q4_K: 256}
+# (Q6_K keeps its fp16 scale in the last two bytes; the other 208 are drawn
+# uniformly.)
+_LAYOUT = {Q8_0: (34, 32, 2), Q4_0: (18, 16, 2), MXFP4: (17, 16, 1), Q4_K: (144, 140, 4),
+           Q6_K: (210, 208, 2)}
+DEFAULT_SCALE = {Q8_0: (1e-3, 1e-2), Q4_0: (1e-3, 2e-2), MXFP4: (-8, -2), Q4_K: (1e-4, 1e-3),
+                 Q6_K: (1e-4, 1e-3)}
+_ELEMS = {Q8_0: 32, Q4_0: 32, MXFP4: 32, Q4_K: 256, Q6_K: 256}
 CHUNK_ROWS = 1024
 
 
@@ -61,6 +69,11 @@ def _fill_rows(fmt: int, out: np.ndarray, in_dim: int, seed: int, chunk: int,
     if fmt == Q8_0:
         q = rng.integers(-127, 128, size=(rows, nb, nq), dtype=np.int8)
         blk[:, :, ns:] = q.view(np.uint8)
+    elif fmt == Q6_K:
+        blk[:, :, :nq] = rng.integers(0, 256, size=(rows, nb, nq), dtype=np.uint8)
+        d = rng.uniform(*scale_range, size=(rows, nb)).astype("<f2")
+        blk[:, :, nq:] = d.view(np.uint8).reshape(rows, nb, 2)
+        return
     else:
         blk[:, :, ns:] = rng.integers(0, 256, size=(rows, nb, nq), dtype=np.uint8)
     lo, hi = scale_range

@@ -459,7 +459,7 @@ def test_row_norms_closed_forms():
     assert oracle.row_norms(Q4_0, _row(one, one, one, one), 0, 1, 128)[0] == math.sqrt(4 * 196)
 
 
-@pytest.mark.parametrize("fmt", FMTS + [oracle.Q4_K])
+@pytest.mark.parametrize("fmt", FMTS + [oracle.Q4_K, oracle.Q6_K])
 def test_row_norms_match_library_norm_of_dequantized_rows(fmt):
     rows, in_dim = 37, 512
     W = syn.quant_matrix(fmt, rows, in_dim, seed=90 + fmt)
