@@ -1022,9 +1022,10 @@ def main():
                                                     for dp in (4, 1)]
             extra["moe_mxfp4"] = run_moe(torch, rf, device)
             extra["multi_token_q4_0"] = run_multi_token(torch, rf, device)
-            q4k = run_dense_format(torch, rf, device, syn.Q4_K)
-            q4k["frac_of_hbm_peak"] = q4k["value"] / peak
-            extra["dense_layer_q4_k"] = q4k
+            for name, fmt in (("dense_layer_q4_k", syn.Q4_K), ("dense_layer_q6_k", syn.Q6_K)):
+                r = run_dense_format(torch, rf, device, fmt)
+                r["frac_of_hbm_peak"] = r["value"] / peak
+                extra[name] = r
             if args.ffn_layers > 0:
                 extra["streamed_ffn_q8_0"] = run_streamed_ffn(torch, rf, device, args.ffn_layers)
             if not args.no_sweep:

@@ -73,16 +73,28 @@ extern "C" {
  *             and j+4; j >= 4 the low/high nibble of byte j+4 plus the top
  *             two bits of bytes j-4 / j; quant byte 32i+l holds weight 64i+l
  *             (low nibble) and 64i+32+l (high nibble).  in_dim must be a
- *             multiple of 256 for this format. */
+ *             multiple of 256 for this format.
+ *   RF_Q6_K : 210 B per 256 weights: 128 bytes of low 4-bit quant parts (ql),
+ *             64 bytes of high 2-bit parts (qh), 16 signed 8-bit scales (one
+ *             per 16 weights), fp16 d last; w = d*scale*(q-32).  RAMforge
+ *             ("Milestone 5 - Native Quantized Tensor Support") lists the
+ *             format and neurostream's model list decodes it, but neither
+ *             prints the layout; it follows the GGML layout: weight
+ *             128n+32k+l takes the low (k < 2) or high (k >= 2) nibble of ql
+ *             byte 64n+32(k&1)+l and bit pair 2k of qh byte 32n+l as its top
+ *             two bits.  Every value is exact in fp32.  in_dim must be a
+ *             multiple of 256; rows never take tensor copies (210-byte
+ *             super-blocks), so they are staged whole or copied per lane. */
 #define RF_Q4_0 2
 #define RF_Q8_0 8
 #define RF_MXFP4 39
 #define RF_Q4_K 12
+#define RF_Q6_K 14
 
 typedef enum rf_status {
     RF_OK = 0,
     RF_ERR_INVALID_ARG = 1,     /* null pointer, bad size, in_dim not a whole number of blocks, ... */
-    RF_ERR_UNSUPPORTED_FMT = 2, /* fmt is not one of RF_Q4_0, RF_Q8_0, RF_MXFP4, RF_Q4_K */
+    RF_ERR_UNSUPPORTED_FMT = 2, /* fmt is not one of RF_Q4_0, RF_Q8_0, RF_MXFP4, RF_Q4_K, RF_Q6_K */
     RF_ERR_NOT_PINNED = 3,      /* a host weight pointer is not page-locked */
     RF_ERR_ARENA_TOO_SMALL = 4, /* depth+1 one-row blocks do not fit the arena */
     RF_ERR_CUDA = 5,            /* a CUDA runtime call or launch failed */
@@ -99,10 +111,11 @@ RF_API const char *rf_status_str(int status);
 RF_API int rf_version(void);
 
 /* Bytes per block: 18 (Q4_0), 34 (Q8_0), 17 (MXFP4) per 32 weights, 144 (Q4_K)
- * per 256 weights; 0 if unknown. */
+ * and 210 (Q6_K) per 256 weights; 0 if unknown. */
 RF_API size_t rf_block_bytes(int fmt);
 
-/* Bytes per row of in_dim weights (in_dim/32 blocks, in_dim/256 for Q4_K); 0
+/* Bytes per row of in_dim weights (in_dim/32 blocks, in_dim/256 for Q4_K and
+ * Q6_K); 0
  * if fmt is unknown or in_dim is not a positive whole number of blocks. */
 RF_API size_t rf_row_bytes(int fmt, int64_t in_dim);
 
@@ -113,9 +126,10 @@ RF_API int64_t rf_max_in_dim(int fmt, int n_x);
 
 /* ------------------------------------------------------------- dequantize */
 /* Decode n_blocks consecutive blocks at W (device) into out (device,
- * 32*n_blocks floats, 256*n_blocks for Q4_K).  Q8_0, Q4_0 and MXFP4 values
- * are exactly representable in fp32; a Q4_K value is the exact d*sc*q -
- * dmin*m rounded once; so the result is bit-exact against that definition.  Errors: RF_ERR_UNSUPPORTED_FMT,
+ * 32*n_blocks floats, 256*n_blocks for Q4_K and Q6_K).  Q8_0, Q4_0, MXFP4
+ * and Q6_K values are exactly representable in fp32; a Q4_K value is the
+ * exact d*sc*q - dmin*m rounded once; so the result is bit-exact against
+ * that definition.  Errors: RF_ERR_UNSUPPORTED_FMT,
  * RF_ERR_INVALID_ARG (null pointer, n_blocks < 0). */
 RF_API rf_status rf_dequantize(int fmt, const void *W, int64_t n_blocks, float *out,
                                void *stream);

@@ -16,10 +16,10 @@ PKG = Path(__file__).resolve().parent
 SO = PKG / "_lib" / "librf.so"
 HEADER = PKG.parent / "include" / "rf.h"
 
-Q4_0, Q8_0, Q4_K, MXFP4 = 2, 8, 12, 39
-FORMATS = {"Q4_0": Q4_0, "Q8_0": Q8_0, "Q4_K": Q4_K, "MXFP4": MXFP4}
-BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q4_K: 144, MXFP4: 17}
-BLOCK_ELEMS = {Q4_0: 32, Q8_0: 32, Q4_K: 256, MXFP4: 32}
+Q4_0, Q8_0, Q4_K, Q6_K, MXFP4 = 2, 8, 12, 14, 39
+FORMATS = {"Q4_0": Q4_0, "Q8_0": Q8_0, "Q4_K": Q4_K, "Q6_K": Q6_K, "MXFP4": MXFP4}
+BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q4_K: 144, Q6_K: 210, MXFP4: 17}
+BLOCK_ELEMS = {Q4_0: 32, Q8_0: 32, Q4_K: 256, Q6_K: 256, MXFP4: 32}
 
 OK = 0
 CHAIN = 1   # RF_CHAIN launch flag

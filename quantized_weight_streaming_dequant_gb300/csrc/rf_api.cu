@@ -37,7 +37,24 @@ __global__ void dequant_kernel(const uint8_t *__restrict__ W, int64_t n_blocks,
 {
     const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= n_blocks) return;
-    if constexpr (FMT == RF_Q4_K) {
+    if constexpr (FMT == RF_Q6_K) {
+        // Weight e = 128n + 32k + l: q = low | high << 4 from ql byte
+        // 64n + 32(k&1) + l (low nibble for k < 2, high for k >= 2) and the
+        // bit pair 2k of qh byte 128 + 32n + l; w = d * scale[e/16] * (q-32).
+        // d * scale is exact in fp32 (11 x 8 significant bits) and so is its
+        // product with q - 32 (6 more), so the result is exact.
+        float *o = out + 256 * b;
+        const uint8_t *p = W + 210 * b;
+        const float d = __half2float(__ushort_as_half((unsigned short)(p[208] | (p[209] << 8))));
+        for (int e = 0; e < 256; ++e) {
+            const int n = e >> 7, k = (e >> 5) & 3, l = e & 31;
+            const int lb = p[64 * n + 32 * (k & 1) + l];
+            const int low = k < 2 ? (lb & 15) : (lb >> 4);
+            const int high = (p[128 + 32 * n + l] >> (2 * k)) & 3;
+            o[e] = (d * (float)(int8_t)p[192 + (e >> 4)]) * (float)((low | (high << 4)) - 32);
+        }
+        return;
+    } else if constexpr (FMT == RF_Q4_K) {
         // d*sc and dmin*m are exact in fp32 (11-bit times 6-bit significands)
         // and so is d*sc*q, so one fused multiply-add rounds the exact value
         // once.
@@ -163,6 +180,7 @@ rf_status rf_dequantize(int fmt, const void *W, int64_t n_blocks, float *out, vo
     case RF_Q4_0: dequant_kernel<RF_Q4_0><<<(unsigned)grid, threads, 0, s>>>(w, n_blocks, out); break;
     case RF_Q8_0: dequant_kernel<RF_Q8_0><<<(unsigned)grid, threads, 0, s>>>(w, n_blocks, out); break;
     case RF_Q4_K: dequant_kernel<RF_Q4_K><<<(unsigned)grid, threads, 0, s>>>(w, n_blocks, out); break;
+    case RF_Q6_K: dequant_kernel<RF_Q6_K><<<(unsigned)grid, threads, 0, s>>>(w, n_blocks, out); break;
     default: dequant_kernel<RF_MXFP4><<<(unsigned)grid, threads, 0, s>>>(w, n_blocks, out); break;
     }
     return last_cuda_error();

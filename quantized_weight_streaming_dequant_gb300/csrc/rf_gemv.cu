@@ -72,9 +72,10 @@ constexpr int kRows = 32;   // rows per group (one per lane)
 struct __align__(16) XRec {
     uint32_t p0[8];   // byte 0 of X (unsigned), 4 elements per word
     uint32_t p1[8];   // byte 1 of X (signed: X >> 8)
-    int32_t corr;     // per-format multiple of sum_j X_j (see xrec_corr)
+    int32_t corr;     // per-format multiple of sum_j X_j (see xrec_corr);
+                      // Q6_K: sum of X_j over elements 0..15
     float scale;      // 2^-s
-    int32_t pad[2];
+    int32_t pad[2];   // Q6_K: pad[0] = sum of X_j over elements 16..31
 };
 static_assert(sizeof(XRec) == 80, "XRec layout");
 
@@ -97,6 +98,13 @@ struct FmtT<RF_MXFP4> {
 template <>
 struct FmtT<RF_Q4_K> {
     static constexpr int BS = 144, G = 1, RPB = 8;
+};
+// Q6_K: the 256-weight super-block is 210 B (never a whole number of 16-byte
+// units, so its rows are always staged whole or copied per lane); one scale
+// per 16 weights, so its digit records carry both 16-element sums.
+template <>
+struct FmtT<RF_Q6_K> {
+    static constexpr int BS = 210, G = 1, RPB = 8;
 };
 
 constexpr int kMaxMaps = 16;   // distinct weight tensors per launch (tensor-map path)
@@ -228,6 +236,7 @@ __device__ __forceinline__ void xrec_build(const float (&v)[8], int part, bool a
         sum += X[i];
     }
     sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    const int half_sum = sum;   // parts 0, 1: elements 0..15; parts 2, 3: 16..31
     sum += __shfl_xor_sync(0xffffffffu, sum, 2);
     if (!active) return;
 #pragma unroll
@@ -238,9 +247,12 @@ __device__ __forceinline__ void xrec_build(const float (&v)[8], int part, bool a
         out->p1[2 * part + hh] = prmt(prmt(a, b, 0x0051u), prmt(c, d, 0x0051u), 0x5410u);
     }
     if (part == 0) {
-        out->corr = xrec_corr<FMT>(sum);
+        out->corr = FMT == RF_Q6_K ? half_sum : xrec_corr<FMT>(sum);
         out->scale = exp2i(-s);
-        out->pad[0] = out->pad[1] = 0;
+        if (FMT != RF_Q6_K) out->pad[0] = 0;
+        out->pad[1] = 0;
+    } else if (FMT == RF_Q6_K && part == 2) {
+        out->pad[0] = half_sum;
     }
 }
 
@@ -260,9 +272,11 @@ __device__ __forceinline__ void xrec_emit(float v, XRec *out)
     const float f1 = exp2i(min(s, 127)), f2 = exp2i(max(s - 127, 0));
     const float t = (v * f1) * f2 + 12582912.0f;
     const int X = max(-32767, min(32767, (int)(__float_as_uint(t) - 0x4b400000u)));
-    int sum = X;
+    int hs = X;   // sum over this lane's 16-element half, then over all 32
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    for (int o = 1; o < 16; o <<= 1) hs += __shfl_xor_sync(0xffffffffu, hs, o);
+    const int sum = hs + __shfl_xor_sync(0xffffffffu, hs, 16);
+    const int h0 = __shfl_sync(0xffffffffu, hs, 0), h1 = __shfl_sync(0xffffffffu, hs, 16);
     // Lane L < 16 assembles plane L >> 3, word L & 7.
     const int w = lane & 7;
     const uint32_t a = (uint32_t)__shfl_sync(0xffffffffu, X, elem_of<FMT>(w, 0));
@@ -275,11 +289,11 @@ __device__ __forceinline__ void xrec_emit(float v, XRec *out)
     if (lane < 16)
         o32[lane] = word;
     else if (lane == 16)
-        o32[16] = (uint32_t)xrec_corr<FMT>(sum);
+        o32[16] = (uint32_t)(FMT == RF_Q6_K ? h0 : xrec_corr<FMT>(sum));
     else if (lane == 17)
         o32[17] = __float_as_uint(exp2i(-s));
     else if (lane < 20)
-        o32[lane] = 0;
+        o32[lane] = (FMT == RF_Q6_K && lane == 18) ? (uint32_t)h1 : 0u;
 }
 
 // One Q4_K super-block held as 36 words (d and dmin, 3 words of packed 6-bit
@@ -320,6 +334,65 @@ __device__ __forceinline__ float q4k_superblock(const uint32_t *v, const XRec *x
         const int idot = (j & 1) ? (t1 >> 4) * 256 + (t0 >> 4) : t1 * 256 + t0;
         const float t = fmaf((float)idot, d * sc, -((float)x.corr * (dmin * m)));
         acc = fmaf(t, x.scale, acc);
+    }
+    return acc;
+}
+
+// One Q6_K super-block starting `o` bytes (o even) into a 4-byte aligned
+// buffer, against its 8 digit records.  Record j = 4n + k (half n, quarter
+// k) covers weights 128n + 32k + l, l < 32: quant q = low | high << 4 with
+// low the low (k < 2) or high (k >= 2) nibble of ql byte 64n + 32(k&1) + l
+// and high the bit pair 2k of qh byte 32n + l; weight = d * sc * (q - 32)
+// with one signed scale per 16 weights.  Per 16 weights the exact integer
+// sum_l (q_l - 32) X_l (|.| < 2^24) becomes a float, times its scale, and
+// the record's pair times d * 2^-s joins the fp32 accumulator.  Reads one
+// word past the block (the buffers leave room for it); the bytes it
+// brings in are masked off.
+__device__ __forceinline__ float q6k_superblock(const uint8_t *buf, int o, const XRec *xr,
+                                                float acc)
+{
+    const uint32_t *wp = reinterpret_cast<const uint32_t *>(buf + (o & ~3));
+    const int sh = 8 * (o & 3);
+    auto word = [&](int i) { return __funnelshift_r(wp[i], wp[i + 1], sh); };
+    const uint32_t sw[4] = {word(48), word(49), word(50), word(51)};   // 16 scale bytes
+    const float d = __half2float(__ushort_as_half((unsigned short)(word(52) & 0xffffu)));
+#pragma unroll
+    for (int n = 0; n < 2; ++n) {
+        uint32_t ql[16], qh[8];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) ql[i] = word(16 * n + i);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) qh[i] = word(32 + 8 * n + i);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const XRec &x = xr[4 * n + k];
+            const uint4 *P0 = reinterpret_cast<const uint4 *>(x.p0);
+            const uint4 *P1 = reinterpret_cast<const uint4 *>(x.p1);
+            const uint4 a0 = P0[0], a1 = P0[1], b0 = P1[0], b1 = P1[1];
+            const uint32_t p0[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const uint32_t p1[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            int lo0 = 0, lo1 = 0, hi0 = 0, hi1 = 0;   // sub-blocks of weights 0..15, 16..31
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t w = ql[8 * (k & 1) + i];
+                const uint32_t low = (k < 2 ? w : (w >> 4)) & 0x0f0f0f0fu;
+                const uint32_t high = ((qh[i] >> (2 * k)) & 0x03030303u) << 4;
+                const uint32_t q = low | high;
+                if (i < 4) {
+                    lo0 = dp4a_uu(q, p0[i], lo0);
+                    lo1 = dp4a_us(q, p1[i], lo1);
+                } else {
+                    hi0 = dp4a_uu(q, p0[i], hi0);
+                    hi1 = dp4a_us(q, p1[i], hi1);
+                }
+            }
+            const int dot_a = lo1 * 256 + lo0 - 32 * x.corr;
+            const int dot_b = hi1 * 256 + hi0 - 32 * x.pad[0];
+            const uint32_t sc = sw[2 * n + (k >> 1)] >> (16 * (k & 1));
+            const float sc_a = (float)(int8_t)(sc & 0xffu), sc_b = (float)(int8_t)((sc >> 8) & 0xffu);
+            const float t = fmaf((float)dot_b, sc_b, (float)dot_a * sc_a);
+            acc = fmaf(t, d * x.scale, acc);
+        }
     }
     return acc;
 }
@@ -500,7 +573,10 @@ __device__ __forceinline__ float chunk_generic(const uint8_t *slot, int phi, int
                                                const XRec *xr, float acc)
 {
     using F = FmtT<FMT>;
-    if constexpr (FMT == RF_Q4_K) {
+    if constexpr (FMT == RF_Q6_K) {
+        for (int b = 0; b < kn; ++b) acc = q6k_superblock(slot, phi + b * F::BS, xr + b * F::RPB, acc);
+        return acc;
+    } else if constexpr (FMT == RF_Q4_K) {
         // Super-blocks at any 4-byte phase (rows of 144-byte blocks are always
         // 16-byte aligned, so this only serves unaligned slots).
         for (int b = 0; b < kn; ++b) {
@@ -1260,7 +1336,10 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
                     acc = compute_group<FMT>(r, xr_row + kb * F::RPB, acc);
                     continue;
                 }
-                if (aligned) {
+                if constexpr (FMT == RF_Q6_K) {
+                    const int phi = (int)((row_src + (uintptr_t)kb * F::BS) & 15);
+                    acc = chunk_generic<FMT>(slot, phi, kn, xr_row + kb * F::RPB, acc);
+                } else if (aligned) {
                     acc = chunk_aligned<FMT>(slot, kn, xr_row + kb * F::RPB, acc);
                 } else {
                     const int phi = (int)((row_src + (uintptr_t)kb * F::BS) & 15);
@@ -1357,7 +1436,7 @@ const DevInfo &dev_info(int dev)
     return g_dev[dev & 63];
 }
 
-int fmt_group(int fmt) { return fmt == RF_MXFP4 ? 16 : (fmt == RF_Q4_K ? 1 : 8); }
+int fmt_group(int fmt) { return fmt == RF_MXFP4 ? 16 : (fmt == RF_Q4_K || fmt == RF_Q6_K ? 1 : 8); }
 
 // Chunk of `kc` blocks and its slot size.  Aligned rows copy exactly KC*BS
 // bytes; others need up to 15 bytes of rounding on either side.  Slots are an
@@ -1375,7 +1454,7 @@ ChunkGeom chunk_geom(int fmt, bool aligned)
         const int kc = fmt_group(fmt);
         return {kc, kc * bs};
     }
-    const int kc = fmt == RF_Q4_K ? 1 : 8;
+    const int kc = fmt == RF_Q4_K || fmt == RF_Q6_K ? 1 : 8;
     int n = (kc * bs + 30 + 15) / 16 * 16;
     if ((n / 16) % 2 == 0) n += 16;
     return {kc, n};
@@ -1465,6 +1544,9 @@ rf_status launch_mode(int fmt, const KP &p, int grid, size_t smem, bool pdl, cud
     case RF_Q4_0: return launch_fmt<RF_Q4_0, MODE>(p, grid, smem, pdl, stream, dev);
     case RF_Q8_0: return launch_fmt<RF_Q8_0, MODE>(p, grid, smem, pdl, stream, dev);
     case RF_Q4_K: return launch_fmt<RF_Q4_K, MODE>(p, grid, smem, pdl, stream, dev);
+    case RF_Q6_K:   // 210-byte super-blocks never take tensor copies
+        if constexpr (MODE == kModeTensorWS) return RF_ERR_INVALID_ARG;
+        else return launch_fmt<RF_Q6_K, MODE>(p, grid, smem, pdl, stream, dev);
     default: return launch_fmt<RF_MXFP4, MODE>(p, grid, smem, pdl, stream, dev);
     }
 }
@@ -1544,7 +1626,8 @@ rf_status read_and_clear_device_status()
 
 bool fmt_ok(int fmt)
 {
-    return fmt == RF_Q4_0 || fmt == RF_Q8_0 || fmt == RF_MXFP4 || fmt == RF_Q4_K;
+    return fmt == RF_Q4_0 || fmt == RF_Q8_0 || fmt == RF_MXFP4 || fmt == RF_Q4_K ||
+           fmt == RF_Q6_K;
 }
 
 size_t block_bytes_of(int fmt)
@@ -1554,6 +1637,7 @@ size_t block_bytes_of(int fmt)
     case RF_Q8_0: return 34;
     case RF_MXFP4: return 17;
     case RF_Q4_K: return 144;
+    case RF_Q6_K: return 210;
     default: return 0;
     }
 }
@@ -1695,8 +1779,9 @@ static rf_status launch_merged(const LaunchDesc &d, int nb, int64_t RB, cudaStre
     if (di.max_smem_block == 0) return RF_ERR_CUDA;
 
     // Rows are 16-byte aligned when the row bytes are (weights are 16-byte
-    // aligned): then chunks are copied exactly.
-    const bool aligned = RB % 16 == 0;
+    // aligned): then chunks are copied exactly.  Q6_K's 210-byte super-blocks
+    // never fill whole 16-byte units, so its rows take the other modes.
+    const bool aligned = RB % 16 == 0 && d.fmt != RF_Q6_K;
     ChunkGeom geo = chunk_geom(d.fmt, aligned);
     int max_terms = 1;
     for (int i = 0; i < d.n_jobs; ++i) max_terms = std::max(max_terms, (int)d.jobs[i].n_terms);

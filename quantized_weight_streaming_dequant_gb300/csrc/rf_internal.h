@@ -87,8 +87,8 @@ rf_status launch_rowwin(const LaunchDesc &d, cudaStream_t stream);
 
 bool fmt_ok(int fmt);
 size_t block_bytes_of(int fmt);
-// Weights per block: 32, or 256 for Q4_K's super-block.
-inline int64_t block_elems_of(int fmt) { return fmt == RF_Q4_K ? 256 : 32; }
+// Weights per block: 32, or 256 for the K-quant super-blocks.
+inline int64_t block_elems_of(int fmt) { return fmt == RF_Q4_K || fmt == RF_Q6_K ? 256 : 32; }
 rf_status last_cuda_error();
 rf_status read_and_clear_device_status();
 // Arms the one-shot wait fault of the next producer-mode launch

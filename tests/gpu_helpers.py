@@ -76,3 +76,38 @@ def check_moe(ref, y, idx=None, w=None, h=None, what=""):
         for k in range(len(ref["h"])):
             assert_gemv_close(np.asarray(h[k]), ref["h"][k], ref["tol_h"][k], f"{what}: h[{k}]")
     assert_gemv_close(np.asarray(y), ref["y"], ref["tol_y"], f"{what}: y")
+
+
+# |d/dz gelu(z)| = |Phi(z) + z phi(z)| <= 1.129 (its maximum, at z = sqrt(2))
+GELU_SLOPE_MAX = 1.13
+
+
+def chained_y_tol(fmt, Dm, rows, in_dim, h, th):
+    """Bound on |y_gpu - D h_ref| per row of D (rows: a list) when the GPU's
+    down GEMV runs on its own h = h_ref + dh with |dh| <= th elementwise:
+    1e-3 ||D_r|| ||h_gpu|| + ||D_r|| ||dh|| <= ||D_r|| (1e-3 (||h|| + ||th||)
+    + ||th||) (Cauchy-Schwarz)."""
+    nD = np.array([oracle.row_norms(fmt, Dm, int(r), int(r) + 1, in_dim)[0] for r in rows])
+    nh, nth = float(np.linalg.norm(h)), float(np.linalg.norm(th))
+    return nD * (1e-3 * (nh + nth) + nth)
+
+
+def ffn_reference(fmt, G, U, D, n_ff, n_embd, x, act="swiglu", rows=None):
+    """The two-phase FFN by the oracle alone (no GPU value goes in):
+    swiglu: h = silu(G x) * (U x); gelu: h = gelu(U x) (G unused); then
+    y[r] = D_r . h for r in rows (default all).  Returns h, its bound tol_h,
+    y and its bound tol_y, derived from the per-GEMV tolerance."""
+    u = oracle.gemv(fmt, U, 0, n_ff, n_embd, x)
+    tu = gemv_tol(fmt, U, 0, n_ff, n_embd, x)
+    if act == "swiglu":
+        g = oracle.gemv(fmt, G, 0, n_ff, n_embd, x)
+        h = oracle.silu_vec(g) * u
+        th = swiglu_h_tol(g, u, gemv_tol(fmt, G, 0, n_ff, n_embd, x), tu)
+    else:
+        h = oracle.gelu_vec(u)
+        th = GELU_SLOPE_MAX * tu + 1e-6 * np.abs(h)
+    rows = list(range(n_embd)) if rows is None else [int(r) for r in rows]
+    y = np.array([oracle.gemv(fmt, D, r, r + 1, n_ff, h)[0] for r in rows]) if len(rows) < n_embd \
+        else oracle.gemv(fmt, D, 0, n_embd, n_ff, h)
+    tol_y = chained_y_tol(fmt, D, rows, n_ff, h, th) + 1e-6 * np.abs(y)
+    return {"u": u, "tol_u": tu, "h": h, "tol_h": th, "y": y, "tol_y": tol_y, "rows": rows}

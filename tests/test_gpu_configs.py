@@ -6,7 +6,7 @@ import pytest
 
 import oracle
 import synthetic as syn
-from gpu_helpers import assert_gemv_close, dev_tensor, gemv_tol, swiglu_h_tol
+from gpu_helpers import assert_gemv_close, dev_tensor, ffn_reference, gemv_tol
 
 pytestmark = pytest.mark.gpu
 
@@ -81,13 +81,9 @@ def test_dense_layer_4096_11008(rf, fmt):
                          ("o", mats[3], attn)):
         assert_gemv_close(o[name], oracle.gemv(fmt, M, 0, d, d, inp), gemv_tol(fmt, M, 0, d, d, inp),
                           name)
-    g_ref = oracle.gemv(fmt, mats[4], 0, f, d, x_ffn)
-    u_ref = oracle.gemv(fmt, mats[5], 0, f, d, x_ffn)
-    h_ref = oracle.silu_vec(g_ref) * u_ref
-    assert_gemv_close(o["h"], h_ref, swiglu_h_tol(g_ref, u_ref, gemv_tol(fmt, mats[4], 0, f, d, x_ffn),
-                                                  gemv_tol(fmt, mats[5], 0, f, d, x_ffn)), "h")
-    assert_gemv_close(o["y"], oracle.gemv(fmt, mats[6], 0, d, f, o["h"].astype(np.float64)),
-                      gemv_tol(fmt, mats[6], 0, d, f, o["h"]), "y")
+    ref = ffn_reference(fmt, mats[4], mats[5], mats[6], f, d, x_ffn)
+    assert_gemv_close(o["h"], ref["h"], ref["tol_h"], "h")
+    assert_gemv_close(o["y"], ref["y"], ref["tol_y"], "y")
 
 
 def test_moe_mxfp4_128x2880x2880_top4(rf):
@@ -131,8 +127,9 @@ def test_moe_mxfp4_128x2880x2880_streamed_as_benched(rf):
 
 def test_streamed_ffn_q8_0_24576x6144_sampled(rf):
     """Two layers of the host-streamed FFN at full size (256 MiB arena,
-    512-row blocks, depth 4); 256 sampled rows of each projection against the
-    oracle, fed the GPU's own intermediate activations."""
+    512-row blocks, depth 4) against the oracle's own chain (up, GELU, down):
+    256 sampled rows of up, every activation, 256 sampled rows of down, with
+    bounds derived from the per-GEMV tolerance."""
     import torch
     from quantized_weight_streaming_dequant_gb300.layer import StreamedFFN
     c = syn.C4
@@ -154,13 +151,12 @@ def test_streamed_ffn_q8_0_24576x6144_sampled(rf):
             torch.cuda.synchronize()
             u_, h_, y_ = u.cpu().numpy(), h.cpu().numpy(), y.cpu().numpy()
             W_up, W_dn = up.numpy(), dn.numpy()
-            for r in rng.choice(f, 256, replace=False):
-                ref = oracle.gemv(fmt, W_up, int(r), int(r) + 1, d, x)
-                assert_gemv_close(u_[r:r + 1], ref, gemv_tol(fmt, W_up, int(r), int(r) + 1, d, x))
-            assert np.allclose(h_, oracle.gelu_vec(u_), rtol=1e-5, atol=1e-6)
-            for r in rng.choice(d, 256, replace=False):
-                ref = oracle.gemv(fmt, W_dn, int(r), int(r) + 1, f, h_.astype(np.float64))
-                assert_gemv_close(y_[r:r + 1], ref, gemv_tol(fmt, W_dn, int(r), int(r) + 1, f, h_))
+            rows_dn = np.sort(rng.choice(d, 256, replace=False))
+            ref = ffn_reference(fmt, None, W_up, W_dn, f, d, x, act="gelu", rows=rows_dn)
+            rows_up = rng.choice(f, 256, replace=False)
+            assert_gemv_close(u_[rows_up], ref["u"][rows_up], ref["tol_u"][rows_up], "up")
+            assert_gemv_close(h_, ref["h"], ref["tol_h"], "gelu")
+            assert_gemv_close(y_[rows_dn], ref["y"], ref["tol_y"], "down")
         st = arena.stats()
         assert st["last_block_rows"] == 512 and st["slots"] == 5
         assert st["peak_bytes"] == 5 * 512 * rf.row_bytes(fmt, f)

@@ -9,8 +9,8 @@ import pytest
 
 import oracle
 import synthetic as syn
-from gpu_helpers import (assert_gemv_close, check_moe, dev_tensor, gemv_tol, moe_reference,
-                         swiglu_h_tol)
+from gpu_helpers import (assert_gemv_close, check_moe, dev_tensor, ffn_reference, gemv_tol,
+                         moe_reference)
 
 pytestmark = pytest.mark.gpu
 
@@ -211,14 +211,10 @@ def test_ffn_swiglu_parity(rf, fmt, n_ff, n_embd):
     y, h = rf.ffn_swiglu(fmt, dev_tensor(G), dev_tensor(U), dev_tensor(D), n_ff, n_embd,
                          dev_tensor(x))
     y, h = y.cpu().numpy(), h.cpu().numpy()
-    g_ref = oracle.gemv(fmt, G, 0, n_ff, n_embd, x)
-    u_ref = oracle.gemv(fmt, U, 0, n_ff, n_embd, x)
-    tg, tu = gemv_tol(fmt, G, 0, n_ff, n_embd, x), gemv_tol(fmt, U, 0, n_ff, n_embd, x)
-    h_ref = oracle.silu_vec(g_ref) * u_ref
-    assert_gemv_close(h, h_ref, swiglu_h_tol(g_ref, u_ref, tg, tu), "h")
-    # down, checked on the GPU's own h
-    y_ref = oracle.gemv(fmt, D, 0, n_embd, n_ff, h.astype(np.float64))
-    assert_gemv_close(y, y_ref, gemv_tol(fmt, D, 0, n_embd, n_ff, h), "y")
+    # the oracle's own chain, with bounds derived from the per-GEMV tolerance
+    ref = ffn_reference(fmt, G, U, D, n_ff, n_embd, x)
+    assert_gemv_close(h, ref["h"], ref["tol_h"], "h")
+    assert_gemv_close(y, ref["y"], ref["tol_y"], "y")
     # with the digit hand-off workspace: the same bits (the digits gate/up
     # writes are the ones down would build from h)
     ws = rf.ffn_workspace(n_ff, "cuda")

@@ -8,7 +8,8 @@ import pytest
 
 import oracle
 import synthetic as syn
-from gpu_helpers import assert_gemv_close, dev_tensor, gemv_tol, swiglu_h_tol
+from gpu_helpers import (assert_gemv_close, check_moe, dev_tensor, ffn_reference, gemv_tol,
+                         moe_reference)
 
 pytestmark = pytest.mark.gpu
 
@@ -137,12 +138,9 @@ def test_ffn_swiglu_parity(rf):
     y, h = rf.ffn_swiglu(Q4_K, dev_tensor(G), dev_tensor(U), dev_tensor(D), n_ff, n_embd,
                          dev_tensor(x))
     y, h = y.cpu().numpy(), h.cpu().numpy()
-    g_ref = oracle.gemv(Q4_K, G, 0, n_ff, n_embd, x)
-    u_ref = oracle.gemv(Q4_K, U, 0, n_ff, n_embd, x)
-    tg, tu = gemv_tol(Q4_K, G, 0, n_ff, n_embd, x), gemv_tol(Q4_K, U, 0, n_ff, n_embd, x)
-    assert_gemv_close(h, oracle.silu_vec(g_ref) * u_ref, swiglu_h_tol(g_ref, u_ref, tg, tu), "h")
-    y_ref = oracle.gemv(Q4_K, D, 0, n_embd, n_ff, h.astype(np.float64))
-    assert_gemv_close(y, y_ref, gemv_tol(Q4_K, D, 0, n_embd, n_ff, h), "y")
+    ref = ffn_reference(Q4_K, G, U, D, n_ff, n_embd, x)
+    assert_gemv_close(h, ref["h"], ref["tol_h"], "h")
+    assert_gemv_close(y, ref["y"], ref["tol_y"], "y")
     ws = rf.ffn_workspace(n_ff, "cuda")
     y2, h2 = rf.ffn_swiglu(Q4_K, dev_tensor(G), dev_tensor(U), dev_tensor(D), n_ff, n_embd,
                            dev_tensor(x), workspace=ws)
@@ -178,18 +176,5 @@ def test_moe_ffn(rf):
     y, ws = rf.moe_ffn(Q4_K, dev_tensor(logits), top_k, dev_tensor(G), dev_tensor(U),
                        dev_tensor(D), n_ff, n_embd, br, dev_tensor(x))
     idx, w, h = (t.cpu().numpy() for t in rf.moe_workspace_views(ws, top_k, n_ff))
-    idx_ref, _ = oracle.router_topk(logits, top_k)
-    assert idx.tolist() == idx_ref.tolist()
-    y = y.cpu().numpy()
-    y_ref, tol_y = np.zeros(n_embd), np.zeros(n_embd)
-    for k, e in enumerate(idx_ref):
-        Ge, Ue = G[int(e) * n_ff:(int(e) + 1) * n_ff], U[int(e) * n_ff:(int(e) + 1) * n_ff]
-        De = D[int(e) * n_embd:(int(e) + 1) * n_embd]
-        g_ref = oracle.gemv(Q4_K, Ge, 0, n_ff, n_embd, x)
-        u_ref = oracle.gemv(Q4_K, Ue, 0, n_ff, n_embd, x)
-        th = swiglu_h_tol(g_ref, u_ref, gemv_tol(Q4_K, Ge, 0, n_ff, n_embd, x),
-                          gemv_tol(Q4_K, Ue, 0, n_ff, n_embd, x))
-        assert_gemv_close(h[k], oracle.silu_vec(g_ref) * u_ref, th, f"h expert {e}")
-        y_ref += float(w[k]) * oracle.gemv(Q4_K, De, 0, n_embd, n_ff, h[k].astype(np.float64))
-        tol_y += float(w[k]) * gemv_tol(Q4_K, De, 0, n_embd, n_ff, h[k])
-    assert_gemv_close(y, y_ref, tol_y + 1e-6 * np.abs(y_ref), "moe y")
+    check_moe(moe_reference(Q4_K, G, U, D, n_ff, n_embd, x, logits, top_k), y.cpu().numpy(),
+              idx, w, h, what="Q4_K moe")
