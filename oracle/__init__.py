@@ -75,6 +75,10 @@ def _declare(L: ctypes.CDLL) -> None:
     L.orc_block_elems.argtypes = [_I]
     L.orc_block_elems.restype = _I64
     L.orc_q4k_scale_min.argtypes = [_P, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]
+    L.orc_swiglu_clamped.argtypes = [ctypes.c_double] * 4
+    L.orc_swiglu_clamped.restype = ctypes.c_double
+    L.orc_moe_ffn_biased.argtypes = [_I, _P, _I, _I, _P, _P, _P, _P, _P, _P, ctypes.c_double,
+                                     ctypes.c_double, _I64, _I64, _P, _P, _P, _P, _P]
     L.orc_q6k_quant.argtypes = [_P, _I]
     L.orc_q6k_quant.restype = _I
     L.orc_dequant_block.argtypes = [_I, _P, _P]
@@ -250,3 +254,33 @@ def gelu_vec(z) -> np.ndarray:
 
 def silu_vec(z) -> np.ndarray:
     return np.array([silu(float(v)) for v in np.asarray(z).reshape(-1)], dtype=np.float64)
+
+
+def swiglu_clamped(g: float, u: float, alpha: float, limit: float) -> float:
+    """The biased experts' clamped SwiGLU (reading in rf_oracle.c)."""
+    return lib().orc_swiglu_clamped(g, u, alpha, limit)
+
+
+def _opt_f64(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.float64)
+
+
+def moe_ffn_biased(fmt: int, logits, top_k: int, gate, up, down, gate_bias, up_bias, down_bias,
+                   alpha: float, limit: float, n_ff: int, n_embd: int, x):
+    """Routed MoE over biased experts with the clamped SwiGLU; biases are
+    (n_expert, n_ff), (n_expert, n_ff), (n_expert, n_embd) arrays or None.
+    Returns (y, idx, w, h) with h the selected experts' activations."""
+    lf = np.ascontiguousarray(logits, dtype=np.float32)
+    g, u, d = _u8(gate), _u8(up), _u8(down)
+    gb, ub, db = _opt_f64(gate_bias), _opt_f64(up_bias), _opt_f64(down_bias)
+    xf = np.ascontiguousarray(x, dtype=np.float32)
+    y = np.empty(n_embd, dtype=np.float64)
+    idx = np.empty(top_k, dtype=np.int32)
+    w = np.empty(top_k, dtype=np.float64)
+    h = np.empty((top_k, n_ff), dtype=np.float64)
+    ptr = lambda a: None if a is None else _ptr(a)   # noqa: E731
+    _check(lib().orc_moe_ffn_biased(fmt, _ptr(lf), lf.size, top_k, _ptr(g), _ptr(u), _ptr(d),
+                                    ptr(gb), ptr(ub), ptr(db), float(alpha), float(limit), n_ff,
+                                    n_embd, _ptr(xf), _ptr(y), _ptr(idx), _ptr(w), _ptr(h)),
+           "moe_ffn_biased")
+    return y, idx, w, h

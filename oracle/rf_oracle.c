@@ -29,6 +29,8 @@
  *            (8 scales and 8 mins packed as 6-bit values), 128 B of 4-bit
  *            quants; an element is d*sc*q - dmin*m with (sc, m) its
  *            sub-block's scale and min.
+ *   [NS-OSS] neurostream, "GPT-OSS-120B": GPT-OSS adds biased projections and
+ *            experts and a clamped SwiGLU (no constants printed).
  *   [RF-M5Q6] RAMforge, "Milestone 5 - Native Quantized Tensor Support" (and
  *            its legacy tensor list): Q6_K is one of the K-quant block
  *            layouts; neurostream, "Supported" models list: Q6_K decoded
@@ -72,6 +74,18 @@
  *     Every such value needs at most 24 significant bits (11 + 8 + 6 bits),
  *     so it is exact in float.  Pinned in tests by hand-worked bytes and by
  *     a reduction to Q8_0.
+ *
+ *   - Biased experts with the clamped SwiGLU ([NS-OSS]; PARITY UNPINNED by
+ *     the pages, which print no formula or constant).  Reading, from the
+ *     public GPT-OSS reference release (its model code's swiglu and MoE
+ *     block): per expert, g = G x + b_g, u = U x + b_u, then
+ *     g' = min(g, limit), u' = max(-limit, min(u, limit)),
+ *     h = g' * sigmoid(alpha * g') * (u' + 1), and the expert's output is
+ *     D h + b_d; the combine is sum_k w_k (D_k h_k + b_d,k).  The release's
+ *     constants are alpha = 1.702 and limit = 7.0; both are arguments here.
+ *     Pinned in tests by a reduction to the plain SwiGLU MoE (alpha = 1,
+ *     limit = +inf, b_u = -1, other biases 0), by bias-only closed forms and
+ *     by the clamp making the output independent of weights it cuts off.
  *
  * Floating point: all arithmetic in double; dequantized weights are returned
  * as float (every value d*q, d*(q-8) and e2m1*2^k is exactly representable).
@@ -426,6 +440,14 @@ double orc_silu(double z) { return z / (1.0 + exp(-z)); }
 
 double orc_gelu(double z) { return 0.5 * z * (1.0 + erf(z / sqrt(2.0))); }
 
+/* Clamped SwiGLU of the biased experts ([NS-OSS] reading above). */
+double orc_swiglu_clamped(double g, double u, double alpha, double limit)
+{
+    double gc = g < limit ? g : limit;
+    double uc = u < -limit ? -limit : (u > limit ? limit : u);
+    return gc / (1.0 + exp(-alpha * gc)) * (uc + 1.0);
+}
+
 /* ----------------------------------------------------------------- router */
 
 /* [NS-HOW] 2: the router names the k active experts.  Pick the k largest
@@ -528,6 +550,59 @@ int orc_moe_ffn(int fmt, const float *logits, int n_expert, int top_k,
             y[r] += w[k] * yk[r];
     }
 out:
+    free(yk);
+    return rc;
+}
+
+/* Routed MoE over biased experts with the clamped SwiGLU ([NS-OSS] reading
+ * above; [NS-IDEA], [NS-HOW] 2-4 for the routing and row windows).  gate/up
+ * are (n_expert, n_ff, n_embd), down is (n_expert, n_embd, n_ff); gate_bias
+ * and up_bias are (n_expert, n_ff) and down_bias (n_expert, n_embd) doubles,
+ * any of them NULL for zero.  y = sum_k w_k (D_k h_k + b_d,k) in selection
+ * order; idx/w receive the routing; h_out (top_k * n_ff, may be NULL)
+ * receives each selected expert's h. */
+int orc_moe_ffn_biased(int fmt, const float *logits, int n_expert, int top_k,
+                       const uint8_t *gate, const uint8_t *up, const uint8_t *down,
+                       const double *gate_bias, const double *up_bias,
+                       const double *down_bias, double alpha, double limit,
+                       int64_t n_ff, int64_t n_embd, const float *x, double *y,
+                       int *idx, double *w, double *h_out)
+{
+    double *g = (double *)malloc(sizeof(double) * (size_t)n_ff);
+    double *u = (double *)malloc(sizeof(double) * (size_t)n_ff);
+    double *yk = (double *)malloc(sizeof(double) * (size_t)n_embd);
+    int k, rc = ORC_ENOMEM;
+    int64_t i, r;
+    if (!g || !u || !yk)
+        goto out;
+    rc = orc_router_topk(logits, n_expert, top_k, idx, w);
+    if (rc)
+        goto out;
+    for (r = 0; r < n_embd; r++)
+        y[r] = 0.0;
+    for (k = 0; k < top_k; k++) {
+        int64_t e = idx[k];
+        rc = orc_gemv(fmt, gate, e * n_ff, (e + 1) * n_ff, n_embd, x, g);
+        if (!rc)
+            rc = orc_gemv(fmt, up, e * n_ff, (e + 1) * n_ff, n_embd, x, u);
+        if (rc)
+            goto out;
+        for (i = 0; i < n_ff; i++) {
+            double gb = g[i] + (gate_bias ? gate_bias[e * n_ff + i] : 0.0);
+            double ub = u[i] + (up_bias ? up_bias[e * n_ff + i] : 0.0);
+            g[i] = orc_swiglu_clamped(gb, ub, alpha, limit);
+        }
+        if (h_out)
+            memcpy(h_out + (int64_t)k * n_ff, g, sizeof(double) * (size_t)n_ff);
+        rc = orc_gemv_d(fmt, down, e * n_embd, (e + 1) * n_embd, n_ff, g, yk);
+        if (rc)
+            goto out;
+        for (r = 0; r < n_embd; r++)
+            y[r] += w[k] * (yk[r] + (down_bias ? down_bias[e * n_embd + r] : 0.0));
+    }
+out:
+    free(g);
+    free(u);
     free(yk);
     return rc;
 }
