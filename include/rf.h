@@ -398,6 +398,30 @@ RF_API rf_status rf_moe_ffn_host(int fmt, const float *router_logits, int n_expe
                                  int64_t block_rows, const float *x, float *y, void *workspace,
                                  void *stream);
 
+/* Routed FFN over biased experts with the clamped SwiGLU (neurostream,
+ * "GPT-OSS-120B": GPT-OSS adds biased projections and experts and a clamped
+ * SwiGLU; the page prints no formula, so the form follows the public GPT-OSS
+ * reference release): for each selected expert e (weight w_k),
+ *     g = G_e x + gate_bias[e],  u = U_e x + up_bias[e],
+ *     g' = min(g, limit),  u' = min(max(u, -limit), limit),
+ *     h = g' * sigmoid(alpha * g') * (u' + 1),
+ *     y = sum_k w_k * (D_e h + down_bias[e])      (selection order).
+ * The release uses alpha = 1.702 and limit = 7.  Routing, layouts, launches
+ * (two: gate/up with this epilogue, then down) and the workspace are those
+ * of rf_moe_ffn; with alpha = 1, limit = +inf, up_bias = -1 and no other
+ * bias the result is rf_moe_ffn's.  gate_bias, up_bias: (n_expert, n_ff)
+ * fp32; down_bias: (n_expert, n_embd) fp32; device, 4-byte aligned; any may
+ * be NULL (no bias).  NaN activations are outside the contract.
+ * Errors: as rf_moe_ffn; RF_ERR_INVALID_ARG for a NaN or infinite alpha or a
+ * limit that is not positive (+inf is allowed: no clamp); RF_ERR_MISALIGNED
+ * for a misaligned bias. */
+RF_API rf_status rf_moe_ffn_biased(int fmt, const float *router_logits, int n_expert,
+                                   int top_k, const void *gate, const void *up, const void *down,
+                                   const float *gate_bias, const float *up_bias,
+                                   const float *down_bias, float alpha, float limit,
+                                   int64_t n_ff, int64_t n_embd, int64_t block_rows,
+                                   const float *x, float *y, void *workspace, void *stream);
+
 /* --------------------------------------------- host-streamed MoE experts */
 /* Expert cache: device memory for `slots` whole experts (each expert's n_ff
  * gate rows, n_ff up rows and n_embd down rows, raw block bytes) of one fmt

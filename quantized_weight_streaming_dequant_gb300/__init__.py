@@ -85,6 +85,8 @@ _SIGS = {
     "rf_moe_route": ([_P, _I, _I, _P, _P, _P], _I),
     "rf_moe_workspace_bytes": ([_I, _I64, _I64, _I64], _SZ),
     "rf_moe_ffn": ([_I, _P, _I, _I, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P], _I),
+    "rf_moe_ffn_biased": ([_I, _P, _I, _I, _P, _P, _P, _P, _P, _P, ctypes.c_float,
+                           ctypes.c_float, _I64, _I64, _I64, _P, _P, _P, _P], _I),
     "rf_moe_ffn_noalloc": ([_I, _P, _I, _I, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P], _I),
     "rf_moe_ffn_host": ([_I, _P, _I, _I, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P], _I),
     "rf_expert_cache_create": ([_I, _I64, _I64, _I, ctypes.POINTER(_P)], _I),
@@ -402,6 +404,25 @@ def moe_ffn(fmt: int, logits, top_k: int, gate, up, down, n_ff: int, n_embd: int
                             _dev_ptr(gate, "gate"), _dev_ptr(up, "up"), _dev_ptr(down, "down"),
                             n_ff, n_embd, block_rows, _dev_ptr(x, "x"), _dev_ptr(y, "y"),
                             _dev_ptr(workspace, "workspace"), _stream(stream)), "rf_moe_ffn")
+    return y, workspace
+
+
+def moe_ffn_biased(fmt: int, logits, top_k: int, gate, up, down, gate_bias, up_bias, down_bias,
+                   alpha: float, limit: float, n_ff: int, n_embd: int, block_rows: int, x,
+                   y=None, workspace=None, stream=None):
+    """rf_moe_ffn_biased: biases are device float32 tensors (or None)."""
+    import torch
+    y = torch.empty(n_embd, dtype=torch.float32, device=x.device) if y is None else y
+    if workspace is None:
+        workspace = moe_workspace(top_k, n_ff, n_embd, block_rows, x.device)
+    opt = lambda t, nm: None if t is None else _dev_ptr(t, nm)   # noqa: E731
+    _check(lib().rf_moe_ffn_biased(fmt, _dev_ptr(logits, "logits"), logits.numel(), top_k,
+                                   _dev_ptr(gate, "gate"), _dev_ptr(up, "up"),
+                                   _dev_ptr(down, "down"), opt(gate_bias, "gate_bias"),
+                                   opt(up_bias, "up_bias"), opt(down_bias, "down_bias"),
+                                   alpha, limit, n_ff, n_embd, block_rows, _dev_ptr(x, "x"),
+                                   _dev_ptr(y, "y"), _dev_ptr(workspace, "workspace"),
+                                   _stream(stream)), "rf_moe_ffn_biased")
     return y, workspace
 
 

@@ -1369,15 +1369,26 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
                 float dot = rt[0];
 #pragma unroll
                 for (int w = 1; w < kNW; ++w) dot += rt[w * 32];
+                const Term &T = J.term[t];
+                if (T.bias && row_ok) {   // biased projection: the row's bias joins its dot
+                    int64_t bi = J.row0 + rowrel;
+                    if (T.expert_slot >= 0) bi += (int64_t)eidx[T.expert_slot] * J.expert_rows;
+                    dot += T.bias[bi];
+                }
                 if (J.combine == kCombineEach) {
                     if (row_ok) J.y[t * J.y_stride + rowrel] = dot;
                     continue;
                 }
                 if (J.combine == kCombineSwiGLU) {
-                    if (t == 0)
+                    if (t == 0) {
                         gate = dot;
-                    else
+                    } else if (J.act == kActClampSwiGLU) {
+                        const float g = fminf(gate, J.limit);
+                        const float u = fminf(fmaxf(dot, -J.limit), J.limit);
+                        yacc = g / (1.f + expf(-J.alpha * g)) * (u + 1.f);
+                    } else {
                         yacc = gate / (1.f + expf(-gate)) * dot;
+                    }
                 } else if (J.combine == kCombineRouted) {
                     yacc = fmaf(s_ew[J.term[t].expert_slot], dot, yacc);
                 } else if (J.weights) {
@@ -1684,13 +1695,14 @@ bool continues(const Job &A, const Job &B)
 {
     if (A.n_terms != B.n_terms || A.combine != B.combine || A.act != B.act ||
         A.weights != B.weights || A.expert_rows != B.expert_rows ||
-        A.expert_count != B.expert_count || A.y_stride != B.y_stride)
+        A.expert_count != B.expert_count || A.y_stride != B.y_stride ||
+        A.alpha != B.alpha || A.limit != B.limit)
         return false;
     if (B.row0 != A.row0 + A.n_rows || B.y != A.y + A.n_rows) return false;
     if ((int64_t)A.n_rows + B.n_rows > 0x7fffffffLL) return false;
     for (int t = 0; t < A.n_terms; ++t)
         if (A.term[t].W != B.term[t].W || A.term[t].xslot != B.term[t].xslot ||
-            A.term[t].expert_slot != B.term[t].expert_slot)
+            A.term[t].expert_slot != B.term[t].expert_slot || A.term[t].bias != B.term[t].bias)
             return false;
     return true;
 }

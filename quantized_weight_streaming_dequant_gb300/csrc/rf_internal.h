@@ -21,7 +21,10 @@ enum Combine : int32_t {
     kCombineRouted = 2,  // y = sum_t w[expert_slot_t] * dot_t, w from the launch's own routing
     kCombineEach = 3,    // y[t * y_stride + r] = dot_t: one output row per term (batched tokens)
 };
-enum Act : int32_t { kActNone = 0, kActGelu = 1 };
+// Activation of the output row.  kActClampSwiGLU changes kCombineSwiGLU to
+// the biased experts' clamped form: g' = min(g, limit), u' = clamp(u, -limit,
+// limit), y = g' * sigmoid(alpha * g') * (u' + 1).
+enum Act : int32_t { kActNone = 0, kActGelu = 1, kActClampSwiGLU = 2 };
 
 struct Term {
     const uint8_t *W;     // row 0 of the matrix (or of the stacked tensor)
@@ -29,6 +32,7 @@ struct Term {
     int32_t expert_slot;  // >= 0: add expert_idx[expert_slot]*expert_rows rows to W
     int32_t tmap;         // filled by the launcher: tensor map of W (aligned rows)
     int32_t pad;
+    const float *bias;    // or nullptr: added to the row's dot (indexed like W's rows)
 };
 
 // One window of rows [row0, row0+n_rows) taken from every term's matrix.
@@ -46,6 +50,7 @@ struct Job {
     int32_t act;
     int32_t group_begin;    // filled by the launcher
     int32_t aligned;        // filled by the launcher
+    float alpha, limit;     // kActClampSwiGLU constants
 };
 
 struct LaunchDesc {

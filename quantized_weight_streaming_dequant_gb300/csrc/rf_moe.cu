@@ -164,12 +164,20 @@ size_t rf_moe_workspace_bytes(int top_k, int64_t n_ff, int64_t n_embd, int64_t b
 
 namespace {
 
+// Biased experts with the clamped SwiGLU (rf_moe_ffn_biased); all zero /
+// off for the plain routed FFN.
+struct ExpertBias {
+    const float *gate = nullptr, *up = nullptr, *down = nullptr;
+    bool clamp = false;
+    float alpha = 0.f, limit = 0.f;
+};
+
 // The routed FFN; host = the stacked tensors are page-locked, device-mapped
 // host memory read in place (gate, up, down are their device aliases).
 rf_status moe_ffn(int fmt, const float *router_logits, int n_expert, int top_k, const void *gate,
                   const void *up, const void *down, int64_t n_ff, int64_t n_embd,
                   int64_t block_rows, const float *x, float *y, void *workspace, void *stream,
-                  bool host)
+                  bool host, const ExpertBias &eb = ExpertBias())
 {
     if (!fmt_ok(fmt)) return RF_ERR_UNSUPPORTED_FMT;
     if (!router_logits || !gate || !up || !down || !x || !y || !workspace)
@@ -219,8 +227,8 @@ rf_status moe_ffn(int fmt, const float *router_logits, int n_expert, int top_k, 
             Job &J = jobs[nj++];
             std::memset(&J, 0, sizeof(J));
             const int64_t r0 = j * br_ff;
-            J.term[0] = Term{static_cast<const uint8_t *>(gate), 0, k, 0, 0};
-            J.term[1] = Term{static_cast<const uint8_t *>(up), 0, k, 0, 0};
+            J.term[0] = Term{static_cast<const uint8_t *>(gate), 0, k, 0, 0, eb.gate};
+            J.term[1] = Term{static_cast<const uint8_t *>(up), 0, k, 0, 0, eb.up};
             J.y = h + (int64_t)k * n_ff + r0;
             J.row0 = r0;
             J.expert_rows = n_ff;
@@ -228,6 +236,11 @@ rf_status moe_ffn(int fmt, const float *router_logits, int n_expert, int top_k, 
             J.n_rows = (int32_t)(r0 + br_ff < n_ff ? br_ff : n_ff - r0);
             J.n_terms = 2;
             J.combine = kCombineSwiGLU;
+            if (eb.clamp) {
+                J.act = kActClampSwiGLU;
+                J.alpha = eb.alpha;
+                J.limit = eb.limit;
+            }
         }
     }
     LaunchDesc d1;
@@ -257,7 +270,8 @@ rf_status moe_ffn(int fmt, const float *router_logits, int n_expert, int top_k, 
         Job &J = jobs[nj++];
         std::memset(&J, 0, sizeof(J));
         const int64_t r0 = j * br_embd;
-        for (int k = 0; k < top_k; ++k) J.term[k] = Term{static_cast<const uint8_t *>(down), k, k, 0, 0};
+        for (int k = 0; k < top_k; ++k)
+            J.term[k] = Term{static_cast<const uint8_t *>(down), k, k, 0, 0, eb.down};
         J.y = y + r0;
         J.row0 = r0;
         J.expert_rows = n_embd;
@@ -317,6 +331,28 @@ rf_status rf_moe_ffn_host(int fmt, const float *router_logits, int n_expert, int
     if (!g || !u || !d) return RF_ERR_NOT_PINNED;
     return moe_ffn(fmt, router_logits, n_expert, top_k, g, u, d, n_ff, n_embd, block_rows, x, y,
                    workspace, stream, true);
+}
+
+rf_status rf_moe_ffn_biased(int fmt, const float *router_logits, int n_expert, int top_k,
+                            const void *gate, const void *up, const void *down,
+                            const float *gate_bias, const float *up_bias, const float *down_bias,
+                            float alpha, float limit, int64_t n_ff, int64_t n_embd,
+                            int64_t block_rows, const float *x, float *y, void *workspace,
+                            void *stream)
+{
+    if (!(alpha == alpha) || alpha == INFINITY || alpha == -INFINITY || !(limit > 0.f))
+        return RF_ERR_INVALID_ARG;   // NaN or infinite alpha; limit NaN or not positive
+    for (const float *b : {gate_bias, up_bias, down_bias})
+        if ((reinterpret_cast<uintptr_t>(b) & 3u) != 0) return RF_ERR_MISALIGNED;
+    ExpertBias eb;
+    eb.gate = gate_bias;
+    eb.up = up_bias;
+    eb.down = down_bias;
+    eb.clamp = true;
+    eb.alpha = alpha;
+    eb.limit = limit;
+    return moe_ffn(fmt, router_logits, n_expert, top_k, gate, up, down, n_ff, n_embd, block_rows,
+                   x, y, workspace, stream, false, eb);
 }
 
 rf_status rf_moe_ffn_noalloc(int fmt, const float *router_logits, int n_expert, int top_k,

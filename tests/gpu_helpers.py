@@ -111,3 +111,47 @@ def ffn_reference(fmt, G, U, D, n_ff, n_embd, x, act="swiglu", rows=None):
         else oracle.gemv(fmt, D, 0, n_embd, n_ff, h)
     tol_y = chained_y_tol(fmt, D, rows, n_ff, h, th) + 1e-6 * np.abs(y)
     return {"u": u, "tol_u": tu, "h": h, "tol_h": th, "y": y, "tol_y": tol_y, "rows": rows}
+
+
+def swiglu_clamped_h_tol(g, u, tg, tu, alpha, limit):
+    """Bound on |h_gpu - h_ref| for the clamped SwiGLU h = f(g') (u' + 1),
+    f(z) = z sigmoid(alpha z), g' = min(g, limit), u' = clamp(u, +-limit),
+    given |dg| <= tg, |du| <= tu: both clamps are 1-Lipschitz and
+    |f'| <= 1.1 for every alpha (f'(z) = s(t) + t s(t)(1 - s(t)), t = alpha z,
+    whose maximum is 1.0998), so |dh| <= 1.1 tg (|u' + 1| + tu) + |f(g')| tu,
+    plus fp32 rounding of the epilogue."""
+    gc, uc = np.minimum(g, limit), np.clip(u, -limit, limit)
+    f = gc / (1.0 + np.exp(-alpha * gc))
+    return 1.1 * tg * (np.abs(uc + 1.0) + tu) + np.abs(f) * tu + 1e-6 * np.abs(f * (uc + 1.0))
+
+
+def moe_reference_biased(fmt, G, U, D, n_ff, n_embd, x, logits, top_k, gate_bias, up_bias,
+                         down_bias, alpha, limit):
+    """moe_reference for the biased experts with the clamped SwiGLU: y and h
+    from the oracle's own chain (oracle.moe_ffn_biased), bounds derived from
+    the per-GEMV tolerance (the fp32 bias additions add 1e-7 relative)."""
+    y, idx, w, h = oracle.moe_ffn_biased(fmt, logits, top_k, G, U, D, gate_bias, up_bias,
+                                         down_bias, alpha, limit, n_ff, n_embd, x)
+    tol_y = np.zeros(n_embd)
+    hs, ths = [], []
+    clamped = 0   # gate or up values the clamp changed
+    for k, e in enumerate(idx):
+        e = int(e)
+        Ge, Ue = G[e * n_ff:(e + 1) * n_ff], U[e * n_ff:(e + 1) * n_ff]
+        De = D[e * n_embd:(e + 1) * n_embd]
+        bg = 0.0 if gate_bias is None else np.asarray(gate_bias, np.float64)[e]
+        bu = 0.0 if up_bias is None else np.asarray(up_bias, np.float64)[e]
+        g = oracle.gemv(fmt, Ge, 0, n_ff, n_embd, x) + bg
+        u = oracle.gemv(fmt, Ue, 0, n_ff, n_embd, x) + bu
+        tg = gemv_tol(fmt, Ge, 0, n_ff, n_embd, x) + 1e-7 * np.abs(g)
+        tu = gemv_tol(fmt, Ue, 0, n_ff, n_embd, x) + 1e-7 * np.abs(u)
+        th = swiglu_clamped_h_tol(g, u, tg, tu, alpha, limit)
+        clamped += int((g > limit).sum() + (np.abs(u) > limit).sum())
+        yk = oracle.gemv(fmt, De, 0, n_embd, n_ff, h[k])
+        bd = 0.0 if down_bias is None else np.asarray(down_bias, np.float64)[e]
+        tol_y += float(w[k]) * (chained_y_tol(fmt, De, range(n_embd), n_ff, h[k], th)
+                                + 1e-6 * (np.abs(yk) + np.abs(bd)))
+        hs.append(h[k])
+        ths.append(th)
+    return {"idx": idx, "w": w, "h": hs, "tol_h": ths, "y": y, "tol_y": tol_y,
+            "clamped": clamped}
