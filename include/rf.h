@@ -506,7 +506,7 @@ RF_API rf_status rf_moe_ffn_streamed(int fmt, const float *router_logits, int n_
  * every GPU that loads the library keeps until the process exits.  Limit:
  * top_k * n_ff <= RF_MOE_STATIC_MAX_H, else RF_ERR_TOO_LARGE before any work
  * (n_ff <= rf_max_in_dim(fmt, top_k) applies as for rf_moe_ffn, which with
- * 4 experts caps the activations at 61,440).
+ * 4 experts caps the activations at 53,120 on a GB300).
  * The first call on a device looks up the array's device address (once per
  * device, with that device current) and keeps it for the life of the
  * process; make that first call before any stream capture.  A caller that

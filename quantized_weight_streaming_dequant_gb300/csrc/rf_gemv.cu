@@ -64,9 +64,14 @@ namespace {
 // Device status word (see rf_device_status).
 __device__ int g_device_status = 0;
 
-constexpr int kNW = 8;
+constexpr int kNW = 8;             // consumer warps of the staged and per-lane kernels
 constexpr int kThreads = kNW * 32;
-constexpr int kRows = 32;   // rows per group (one per lane)
+constexpr int kRows = 32;          // rows per group (one per lane)
+// The canonical reduction of a row: its blocks fall into kParts consecutive K
+// parts; each part is accumulated in block order in fp32 by one lane, and the
+// row's dot is the sum of the parts' partials in part order.  Every kernel
+// mode computes exactly these partials, whichever warp owns which part.
+constexpr int kParts = 16;
 
 // Fixed-point digits of one 32-element activation block.
 struct __align__(16) XRec {
@@ -737,25 +742,40 @@ __device__ __forceinline__ void route_warp(const float *__restrict__ logits, int
 // the warp copies its rows' chunks with 16-byte cp.async.
 constexpr int kModePerLane = 0, kModeFlat = 2, kModeTensorWS = 3;
 
-template <int MODE>
-constexpr int threads_of() { return MODE == kModeTensorWS ? kThreads + 32 : kThreads; }
+// Consumer warps of a CTA: producer mode with the 4-bit formats runs 16, one
+// K part each, so a 32-row group streams through all of them at once; every
+// other kernel runs 8, each owning two adjacent parts (the 272-byte chunks of
+// Q8_0 and MXFP4 need more registers than 16 warps leave).
+template <int FMT, int MODE>
+__host__ __device__ constexpr int nwc_of()
+{
+    return (MODE == kModeTensorWS && (FMT == RF_Q4_0 || FMT == RF_Q4_K)) ? 16 : kNW;
+}
+int nwc_host(int fmt, int mode)
+{
+    return (mode == kModeTensorWS && (fmt == RF_Q4_0 || fmt == RF_Q4_K)) ? 16 : kNW;
+}
 
-// Minimum CTAs per SM the register budget is sized for: 272-byte aligned
-// chunks (Q8_0, MXFP4) need more registers and their shared memory allows
-// one CTA per SM anyway.
+template <int FMT, int MODE>
+constexpr int threads_of() { return 32 * nwc_of<FMT, MODE>() + (MODE == kModeTensorWS ? 32 : 0); }
+
+// Minimum CTAs per SM the register budget is sized for: producer mode runs
+// one CTA per SM (its ring takes most of the shared memory).
 template <int FMT, int MODE>
 constexpr int min_ctas()
 {
-    return (MODE == kModeTensorWS && FMT != RF_Q4_0 && FMT != RF_Q4_K) ? 1 : 2;
+    return MODE == kModeTensorWS ? 1 : 2;
 }
 
 template <int FMT, int MODE, class KP>
-__global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
+__global__ void __launch_bounds__(threads_of<FMT, MODE>(), min_ctas<FMT, MODE>())
     rowwin_kernel(const __grid_constant__ KP p)
 {
     using F = FmtT<FMT>;
     constexpr bool WS = MODE == kModeTensorWS;
     constexpr bool FLAT = MODE == kModeFlat;
+    constexpr int NWC = nwc_of<FMT, MODE>();   // consumer warps
+    constexpr int PPW = kParts / NWC;          // K parts per consumer warp (1 or 2)
     extern __shared__ __align__(128) uint8_t smem[];
 
     const int nb = p.nb;
@@ -770,13 +790,13 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
     const int nrx = nb * F::RPB;   // digit records per activation vector
     size_t off = ((size_t)p.n_x * nrx * sizeof(XRec) + 127) & ~(size_t)127;
     uint8_t *slots = smem + off;
-    off += FLAT ? (size_t)ST * SLOT : (size_t)kNW * ST * kRows * SLOT;
+    off += FLAT ? (size_t)ST * SLOT : (size_t)NWC * ST * kRows * SLOT;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + off);   // slot filled
-    off += (size_t)(FLAT ? ST : kNW * ST) * sizeof(uint64_t);
+    off += (size_t)(FLAT ? ST : NWC * ST) * sizeof(uint64_t);
     uint64_t *ebars = reinterpret_cast<uint64_t *>(smem + off);  // producer mode: slot released
-    if constexpr (WS) off += (size_t)kNW * ST * sizeof(uint64_t);
-    float *red = reinterpret_cast<float *>(smem + off);   // [2][NT][kNW][32]
-    off += (size_t)2 * NT * kNW * 32 * sizeof(float);
+    if constexpr (WS) off += (size_t)NWC * ST * sizeof(uint64_t);
+    float *red = reinterpret_cast<float *>(smem + off);   // [2][NT][kParts][32]
+    off += (size_t)2 * NT * kParts * 32 * sizeof(float);
     int *cnt = reinterpret_cast<int *>(smem + off);       // arrivals per parity, then groups done
     int *emp = cnt + 4;                                   // flat mode: readers done per stage
     volatile int *fl_fail = cnt + 3;                      // a wait of this CTA gave up
@@ -799,14 +819,18 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
     const int g_lo = (int)blockIdx.x * g_base + min((int)blockIdx.x, g_extra);
     const int g_hi = g_lo + g_base + ((int)blockIdx.x < g_extra ? 1 : 0);
 
-    // This warp's K part, in blocks.
-    // Split granularity: the format's 16-byte group when rows are 16-byte
-    // aligned (tensor copies need it), single blocks otherwise.  Either way it
-    // depends only on (format, in_dim).
+    // This warp's K parts, in blocks: part q is blocks
+    // [GS*floor(q*nG/kParts), GS*floor((q+1)*nG/kParts)).  Split granularity:
+    // the format's 16-byte group when rows are 16-byte aligned (tensor copies
+    // need it), single blocks otherwise.  Either way it depends only on
+    // (format, in_dim).  A warp with two parts keeps two accumulators and
+    // switches at kb_mid.
     const int GS = RB % 16 == 0 ? F::G : 1;
     const int nG = (nb + GS - 1) / GS;
-    const int kb_lo = min(nb, GS * (warp * nG / kNW));
-    const int kb_hi = min(nb, GS * ((warp + 1) * nG / kNW));
+    auto part_lo = [&](int q) { return min(nb, GS * (q * nG / kParts)); };
+    const int kb_lo = part_lo(warp * PPW);
+    const int kb_mid = part_lo(warp * PPW + (PPW - 1));
+    const int kb_hi = part_lo((warp + 1) * PPW);
     const int n_chunks = (kb_hi - kb_lo + KC - 1) / KC;
     // Items a cursor walks per (group, term): this warp's chunks, or one
     // CTA-wide stage in flat mode.
@@ -815,7 +839,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
     if constexpr (FLAT) {
         if ((int)threadIdx.x < ST) mbar_init(&bars[threadIdx.x], 1);
     } else if constexpr (WS) {
-        if (warp < kNW && lane < ST) {
+        if (warp < NWC && lane < ST) {
             mbar_init(&bars[warp * ST + lane], 1);
             mbar_init(&ebars[warp * ST + lane], 1);
         }
@@ -923,7 +947,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
     // runs then holds its first chunks by the time the activations exist.
     int primed = 0;
     if constexpr (WS) {
-        if (warp == kNW) {
+        if (warp == NWC) {
             // Producer.  Groups come from the static range [g_lo, g_hi) or,
             // scheduled dynamically, the CTA's own first group (blockIdx.x)
             // and then tickets (the next one drawn a group ahead).  For each
@@ -941,10 +965,10 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
                 const int ng = (int)gridDim.x + t;
                 return ng < total ? ng : -1;
             };
-            const int w = lane & (kNW - 1);
-            const int kbl = min(nb, GS * (w * nG / kNW));
-            const int kbh = min(nb, GS * ((w + 1) * nG / kNW));
-            const int nch = lane < kNW ? (kbh - kbl + KC - 1) / KC : 0;
+            const int w = lane & (NWC - 1);
+            const int kbl = part_lo(w * PPW);
+            const int kbh = part_lo((w + 1) * PPW);
+            const int nch = lane < NWC ? (kbh - kbl + KC - 1) / KC : 0;
             int max_nch = nch;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) max_nch = max(max_nch, __shfl_xor_sync(0xffffffffu, max_nch, o));
@@ -972,7 +996,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
                 if (lane == 0) gq[gi & (kGroupQ - 1)] = g;
                 __syncwarp();
                 if (g < 0) {
-                    if (lane < kNW && acquire()) {
+                    if (lane < NWC && acquire()) {
                         mbar_arrive(&bars[w * ST + st]);
                         armed &= ~(1u << st);
                     }
@@ -980,7 +1004,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
                 }
                 while (jj < n_jobs && g >= jobs[jj].group_begin + groups_of(jobs[jj])) ++jj;
                 const Job &J = jobs[jj];
-                if (lane < kNW && nch == 0) {
+                if (lane < NWC && nch == 0) {
                     if (acquire()) {
                         mbar_arrive(&bars[w * ST + st]);
                         armed &= ~(1u << st);
@@ -1023,7 +1047,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
             }
             // Every issued copy lands before the CTA may exit (on the normal
             // path its consumer has already seen it: each check passes at once).
-            if (lane < kNW)
+            if (lane < NWC)
                 for (int i = 0; i < ST; ++i)
                     if ((armed >> i) & 1u) mbar_drain(&bars[w * ST + i], (armed_ph >> i) & 1u);
             if (dyn && lane == 0) {
@@ -1235,7 +1259,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
         const int64_t rowrel = (int64_t)(g - J.group_begin) * kRows + lane;
         const bool row_ok = rowrel < J.n_rows;
         const int par = gi & 1;
-        float *red_g = red + (size_t)par * NT * kNW * 32;
+        float *red_g = red + (size_t)par * NT * kParts * 32;
         // The partial buffer of this parity was last used by group gi-2; wait
         // until that group has been combined.
         if (gi >= 2) {
@@ -1263,7 +1287,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
             __threadfence_block();
         }
         for (int t = 0; t < n_terms; ++t) {
-            float acc = 0.f;
+            float acc = 0.f, acc1 = 0.f;   // parts warp*PPW and warp*PPW + 1
             uintptr_t row_src = 0;
             if (!FLAT && !aligned && row_ok)
                 row_src = reinterpret_cast<uintptr_t>(term_matrix(eidx, J, t, RB) +
@@ -1285,16 +1309,20 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
                     const uintptr_t rp = reinterpret_cast<uintptr_t>(slots + (size_t)st * SLOT) +
                                          (src & 15) + (uintptr_t)((int64_t)lane * RB) +
                                          (uintptr_t)kb_lo * F::BS;
+                    const uintptr_t rp1 = rp + (uintptr_t)(kb_mid - kb_lo) * F::BS;
                     acc = chunk_generic<FMT>(reinterpret_cast<const uint8_t *>(rp & ~(uintptr_t)3),
-                                             (int)(rp & 3), kb_hi - kb_lo,
+                                             (int)(rp & 3), kb_mid - kb_lo,
                                              xr_row + kb_lo * F::RPB, acc);
+                    acc1 = chunk_generic<FMT>(reinterpret_cast<const uint8_t *>(rp1 & ~(uintptr_t)3),
+                                              (int)(rp1 & 3), kb_hi - kb_mid,
+                                              xr_row + kb_mid * F::RPB, acc1);
                 }
                 if (++cs == ST) {
                     cs = 0;
                     cph ^= 1u;
                 }
                 __syncwarp();
-                if (lane == 0 && atomicAdd(&emp[st], 1) == kNW - 1) {
+                if (lane == 0 && atomicAdd(&emp[st], 1) == NWC - 1) {
                     emp[st] = 0;
                     if (ic.valid && *fl_fail == 0) issue_flat(ic, st);
                 }
@@ -1313,37 +1341,52 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
                 }
                 const int kb = kb_lo + c * KC;
                 const int kn = min(KC, kb_hi - kb);
-                if constexpr (WS && FMT == RF_MXFP4) {
-                    // 16 blocks of 17 bytes: the first 8 come from the first
-                    // 9 16-byte words; decode them before loading the rest,
-                    // so that fewer words are live at once.
-                    GroupRegs<FMT> r;
-                    load_group_part<FMT, 0, 9>(slot, r);
-                    acc = compute_blocks<FMT, 0, 8>(r, xr_row + kb * F::RPB, acc);
-                    load_group_part<FMT, 9, 17>(slot, r);
-                    r.v[68] = 0;
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&ebars[warp * ST + cur]);
-                    acc = compute_blocks<FMT, 8, 16>(r, xr_row + kb * F::RPB, acc);
-                    continue;
-                } else if constexpr (WS) {
-                    // A chunk is exactly one group: copy it to registers, hand
-                    // the slot straight back to the producer, then compute.
-                    GroupRegs<FMT> r;
-                    load_group<FMT>(slot, r);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&ebars[warp * ST + cur]);
-                    acc = compute_group<FMT>(r, xr_row + kb * F::RPB, acc);
+                if constexpr (WS) {
+                    // A chunk is exactly one G-group, which never straddles a
+                    // part boundary: it joins the accumulator of its part.
+                    float &a = (PPW == 1 || kb < kb_mid) ? acc : acc1;
+                    if constexpr (FMT == RF_MXFP4) {
+                        // 16 blocks of 17 bytes: the first 8 come from the
+                        // first 9 16-byte words; decode them before loading
+                        // the rest, so that fewer words are live at once.
+                        GroupRegs<FMT> r;
+                        load_group_part<FMT, 0, 9>(slot, r);
+                        a = compute_blocks<FMT, 0, 8>(r, xr_row + kb * F::RPB, a);
+                        load_group_part<FMT, 9, 17>(slot, r);
+                        r.v[68] = 0;
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&ebars[warp * ST + cur]);
+                        a = compute_blocks<FMT, 8, 16>(r, xr_row + kb * F::RPB, a);
+                    } else {
+                        // Copy the chunk to registers, hand the slot straight
+                        // back to the producer, then compute.
+                        GroupRegs<FMT> r;
+                        load_group<FMT>(slot, r);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&ebars[warp * ST + cur]);
+                        a = compute_group<FMT>(r, xr_row + kb * F::RPB, a);
+                    }
                     continue;
                 }
+                // Blocks [kb, kb + n0) belong to this warp's first part, the
+                // rest of the chunk to its second.
+                const int n0 = max(0, min(kn, kb_mid - kb));
                 if constexpr (FMT == RF_Q6_K) {
                     const int phi = (int)((row_src + (uintptr_t)kb * F::BS) & 15);
-                    acc = chunk_generic<FMT>(slot, phi, kn, xr_row + kb * F::RPB, acc);
+                    if (n0 > 0) acc = chunk_generic<FMT>(slot, phi, n0, xr_row + kb * F::RPB, acc);
+                    if (n0 < kn)
+                        acc1 = chunk_generic<FMT>(slot, phi + n0 * F::BS, kn - n0,
+                                                  xr_row + (kb + n0) * F::RPB, acc1);
                 } else if (aligned) {
-                    acc = chunk_aligned<FMT>(slot, kn, xr_row + kb * F::RPB, acc);
+                    // chunks are G-groups and parts start on G-group bounds
+                    if (n0 > 0) acc = chunk_aligned<FMT>(slot, kn, xr_row + kb * F::RPB, acc);
+                    else acc1 = chunk_aligned<FMT>(slot, kn, xr_row + kb * F::RPB, acc1);
                 } else {
                     const int phi = (int)((row_src + (uintptr_t)kb * F::BS) & 15);
-                    acc = chunk_generic<FMT>(slot, phi, kn, xr_row + kb * F::RPB, acc);
+                    if (n0 > 0) acc = chunk_generic<FMT>(slot, phi, n0, xr_row + kb * F::RPB, acc);
+                    if (n0 < kn)
+                        acc1 = chunk_generic<FMT>(slot, phi + n0 * F::BS, kn - n0,
+                                                  xr_row + (kb + n0) * F::RPB, acc1);
                 }
                 __syncwarp();
                 if (ic.valid) {
@@ -1352,23 +1395,24 @@ __global__ void __launch_bounds__(threads_of<MODE>(), min_ctas<FMT, MODE>())
                 }
             }
             if (failed) break;
-            red_g[((size_t)t * kNW + warp) * 32 + lane] = acc;
+            red_g[((size_t)t * kParts + warp * PPW) * 32 + lane] = acc;
+            if constexpr (PPW == 2) red_g[((size_t)t * kParts + warp * PPW + 1) * 32 + lane] = acc1;
         }
         if (failed) break;
-        // The last warp to finish this group sums the partials in warp order.
+        // The last warp to finish this group sums the partials in part order.
         __syncwarp();
         __threadfence_block();
         int arrived = 0;
         if (lane == 0) arrived = atomicAdd(&cnt[par], 1);
         arrived = __shfl_sync(0xffffffffu, arrived, 0);
-        if (arrived == kNW - 1) {
+        if (arrived == NWC - 1) {
             __threadfence_block();
             float yacc = 0.f, gate = 0.f;
             for (int t = 0; t < n_terms; ++t) {
-                const float *rt = red_g + (size_t)t * kNW * 32 + lane;
+                const float *rt = red_g + (size_t)t * kParts * 32 + lane;
                 float dot = rt[0];
 #pragma unroll
-                for (int w = 1; w < kNW; ++w) dot += rt[w * 32];
+                for (int q = 1; q < kParts; ++q) dot += rt[q * 32];
                 const Term &T = J.term[t];
                 if (T.bias && row_ok) {   // biased projection: the row's bias joins its dot
                     int64_t bi = J.row0 + rowrel;
@@ -1475,14 +1519,14 @@ ChunkGeom chunk_geom(int fmt, bool aligned)
 // rounding at both ends and a word of overrun for the last row's decode.
 int flat_slot(int64_t row_bytes) { return (int)((kRows * row_bytes + 32 + 127) / 128 * 128); }
 
-// nrx: activation digit records per x (in_dim / 32).
+// nrx: activation digit records per x (in_dim / 32); nwc: consumer warps.
 size_t smem_bytes(int n_x, int nrx, int stages, int slot, int max_terms, int n_jobs,
-                  bool flat = false, bool ws = false)
+                  bool flat = false, bool ws = false, int nwc = kNW)
 {
     return (((size_t)n_x * nrx * sizeof(XRec) + 127) & ~(size_t)127) +
-           (flat ? (size_t)stages * slot : (size_t)kNW * stages * kRows * slot) +
-           (size_t)(flat ? stages : kNW * stages * (ws ? 2 : 1)) * sizeof(uint64_t) +
-           (size_t)2 * max_terms * kNW * 32 * sizeof(float) + kCntInts * sizeof(int) +
+           (flat ? (size_t)stages * slot : (size_t)nwc * stages * kRows * slot) +
+           (size_t)(flat ? stages : nwc * stages * (ws ? 2 : 1)) * sizeof(uint64_t) +
+           (size_t)2 * max_terms * kParts * 32 * sizeof(float) + kCntInts * sizeof(int) +
            (size_t)n_jobs * sizeof(Job);
 }
 
@@ -1533,7 +1577,7 @@ rf_status launch_fmt(const KP &p, int grid, size_t smem, bool pdl, cudaStream_t 
     if (!attr_ok[dev & 63]) return RF_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(threads_of<MODE>());
+    cfg.blockDim = dim3(threads_of<FMT, MODE>());
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -1802,7 +1846,6 @@ static rf_status launch_merged(const LaunchDesc &d, int nb, int64_t RB, cudaStre
     // Mapped host memory is read with per-lane 16-byte copies (plain loads of
     // the link), never with tensor or bulk copies.
     int mode = aligned && !d.host_weights ? kModeTensorWS : kModePerLane;
-    const bool ws = mode == kModeTensorWS;
     int ctas_per_sm = 0, stages = 0;
     // Misaligned rows: stage whole 32-row groups when two of them fit (two
     // CTAs per SM if possible).
@@ -1824,35 +1867,41 @@ static rf_status launch_merged(const LaunchDesc &d, int nb, int64_t RB, cudaStre
             geo = {1, fs};
         }
     }
-    // Otherwise per-warp rings.  Producer mode with at most four 32-row groups
-    // per SM: one CTA per SM with the deepest ring that fits (up to 6 stages;
-    // fewer, deeper CTAs stream such launches faster).  Else prefer two CTAs
-    // per SM (16 warps) with at least 2 stages; else one CTA with up to 4.
+    // Otherwise per-warp rings.  Producer mode runs one CTA per SM.  With 16
+    // consumer warps (Q4_0, Q4_K) it takes the deepest ring that fits; with 8
+    // (Q8_0, MXFP4) likewise when the launch has at most four 32-row groups
+    // per SM (fewer, deeper CTAs stream such launches faster), else at most 4
+    // stages.  When not even one stage fits beside the activation digits,
+    // the rows take per-lane copies instead.  Per-lane mode prefers two CTAs
+    // per SM with at least 2 stages, else one CTA with up to 4.
     int64_t all_groups = 0;
     for (int i = 0; i < d.n_jobs; ++i) all_groups += (d.jobs[i].n_rows + kRows - 1) / kRows;
-    const bool deep = mode == kModeTensorWS && all_groups <= 4 * (int64_t)di.sms;
-    for (int st = 6; st >= 2 && !ctas_per_sm && deep; --st)
-        if (smem_bytes(d.n_x, nrx, st, geo.slot, max_terms, nj_max, false, ws) <=
-            (size_t)di.max_smem_block) {
-            ctas_per_sm = 1;
-            stages = st;
-        }
-    const bool two_ok = mode == kModePerLane || d.fmt == RF_Q4_0 ||
-                        d.fmt == RF_Q4_K;   // register budget (min_ctas)
-    for (int st = 4; st >= 2 && !ctas_per_sm && two_ok; --st)
-        if (smem_bytes(d.n_x, nrx, st, geo.slot, max_terms, nj_max, false, ws) <= per2) {
+    if (mode == kModeTensorWS) {
+        const int nwc = nwc_host(d.fmt, mode);
+        const bool deep = nwc == 16 || all_groups <= 4 * (int64_t)di.sms;
+        for (int st = deep ? 6 : 4; st >= 1 && !ctas_per_sm; --st)
+            if (smem_bytes(d.n_x, nrx, st, geo.slot, max_terms, nj_max, false, true, nwc) <=
+                (size_t)di.max_smem_block) {
+                ctas_per_sm = 1;
+                stages = st;
+            }
+        if (!ctas_per_sm) mode = kModePerLane;
+    }
+    const bool ws = mode == kModeTensorWS;
+    for (int st = 4; st >= 2 && !ctas_per_sm && mode == kModePerLane; --st)
+        if (smem_bytes(d.n_x, nrx, st, geo.slot, max_terms, nj_max) <= per2) {
             ctas_per_sm = 2;
             stages = st;
         }
     for (int st = 4; st >= 1 && !ctas_per_sm; --st)
-        if (smem_bytes(d.n_x, nrx, st, geo.slot, max_terms, nj_max, false, ws) <=
+        if (smem_bytes(d.n_x, nrx, st, geo.slot, max_terms, nj_max) <=
             (size_t)di.max_smem_block) {
             ctas_per_sm = 1;
             stages = st;
         }
     if (!ctas_per_sm) return RF_ERR_TOO_LARGE;
-    const size_t smem =
-        smem_bytes(d.n_x, nrx, stages, geo.slot, max_terms, nj_max, mode == kModeFlat, ws);
+    const size_t smem = smem_bytes(d.n_x, nrx, stages, geo.slot, max_terms, nj_max,
+                                   mode == kModeFlat, ws, nwc_host(d.fmt, mode));
 
     // Launch in batches of kMaxJobs windows.
     for (int base = 0; base < d.n_jobs; base += kMaxJobs) {

@@ -7,7 +7,7 @@ the caller passes only inputs and outputs.
 Checked through the C ABI against rf_moe_ffn (which takes a caller-allocated
 workspace) and against the CPU oracle on the same bytes, on two calls in a
 row with different routing, so the second call runs on scratch the first one
-left behind; once at the largest size the kernels take (94 % of the array);
+left behind; once at the largest size the kernels take (81 % of the array);
 and one 32-row step over the array's limit must be refused.  This file is collected last; it
 passes on its own in a fresh process and after the other tests.
 """
@@ -80,11 +80,11 @@ def test_noalloc_matches_workspace_entry_point_twice(rf, fmt):
 def test_noalloc_at_the_largest_size_the_kernels_take(rf):
     # The down launch keeps all top_k activation vectors' digits in shared
     # memory, so n_ff is also capped by rf_max_in_dim(fmt, top_k): with 4
-    # experts the largest n_ff is 15,360, and 4 * 15,360 = 61,440 of the
-    # array's 65,536 activations (94 %) are used.
+    # experts that is 13,280 on a GB300, so 4 * 13,280 = 53,120 of the
+    # array's 65,536 activations (81 %) are used.
     top_k = 4
     n_ff = min(MAX_H // top_k, rf.max_in_dim(syn.Q4_0, top_k)) // 32 * 32
-    assert top_k * n_ff > 0.9 * MAX_H
+    assert top_k * n_ff > 0.75 * MAX_H
     _run_twice(rf, syn.Q4_0, 8, n_ff, 256, top_k, 0, seed=90)
 
 
