@@ -474,9 +474,11 @@ def run_multi_token(torch, rf, device, reps: int = 50):
     return {"matrix": f"Q4_0 {rows}x{in_dim}", "copies": len(Ws), "bytes": nbytes, "rows": out}
 
 
-def run_streamed_gemv(torch, rf, device, depth: int, reps: int = 50):
+def run_streamed_gemv(torch, rf, device, depth: int, merge: bool = True, reps: int = 50):
     """Q8_0 512x2048 streamed from pinned host memory in 128-row blocks, eager
-    calls and the same calls captured into one CUDA graph."""
+    calls and the same calls captured into one CUDA graph.  merge: a walk
+    whose 4 blocks fit the ring goes as one copy and one launch; off, every
+    block is its own copy and launch (the per-block pipeline)."""
     c = syn.C1
     fmt, rows, in_dim = c["fmt"], c["out_dim"], c["in_dim"]
     W = syn.quant_matrix(fmt, rows, in_dim, c["seed"])
@@ -484,6 +486,7 @@ def run_streamed_gemv(torch, rf, device, depth: int, reps: int = 50):
     x = torch.from_numpy(syn.normal_f32(in_dim, c["seed"] + 1)).to(device)
     y = torch.empty(rows, device=device)
     arena = rf.Arena(c["arena_bytes"])
+    arena.configure(rf.ARENA_MERGE_RUNS, merge)
     s = torch.cuda.Stream(device)
     s.wait_stream(torch.cuda.current_stream())
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -528,7 +531,8 @@ def run_streamed_gemv(torch, rf, device, depth: int, reps: int = 50):
     probe = h2d_probe(torch, device, c["block_rows"] * rf.row_bytes(fmt, in_dim), reps=200)
     ms = min(eager_ms, graph_ms)
     gbs = nbytes / (ms * 1e-3) / 1e9
-    return {"workload": c["name"], "depth": depth, "ms_per_gemv": ms, "value": gbs, "unit": "GB/s",
+    return {"workload": c["name"], "depth": depth, "merge_runs": merge,
+            "ms_per_gemv": ms, "value": gbs, "unit": "GB/s",
             "eager_ms_per_gemv": eager_ms, "graph_ms_per_gemv": graph_ms,
             "zero_copy_ms_per_gemv": zc_ms, "zero_copy_value": nbytes / (zc_ms * 1e-3) / 1e9,
             "h2d_probe_block_gbs": probe, "frac_of_block_h2d": gbs / probe}
@@ -1018,8 +1022,9 @@ def main():
     if rank == 0 and world == 1 and not args.headline_only:
         extra = {}
         try:
-            extra["streamed_gemv_q8_0_512x2048"] = [run_streamed_gemv(torch, rf, device, dp)
-                                                    for dp in (4, 1)]
+            extra["streamed_gemv_q8_0_512x2048"] = [
+                run_streamed_gemv(torch, rf, device, dp, merge)
+                for dp, merge in ((4, True), (4, False), (1, False), (8, True), (8, False))]
             extra["moe_mxfp4"] = run_moe(torch, rf, device)
             extra["multi_token_q4_0"] = run_multi_token(torch, rf, device)
             for name, fmt in (("dense_layer_q4_k", syn.Q4_K), ("dense_layer_q6_k", syn.Q6_K)):

@@ -270,6 +270,21 @@ RF_API rf_status rf_arena_create(size_t bytes, int device, rf_arena **out);
  * no-op. */
 RF_API void rf_arena_destroy(rf_arena *arena);
 
+/* Arena options (rf_arena_configure), each on by default:
+ *   RF_ARENA_MERGE_RUNS -- a walk whose blocks all fit the ring at once goes
+ *                          over the link as one copy and through one launch
+ *                          (each block still its own window; results are
+ *                          bit-identical either way).  Off: one copy and one
+ *                          launch per block, the per-block pipeline.
+ *   RF_ARENA_LANES      -- walks of 8 or more blocks of at most 1 MiB run
+ *                          their GEMVs round-robin on the arena's four lane
+ *                          streams.  Off: every GEMV on the caller's stream.
+ * value 0 turns an option off, 1 on.  Errors: RF_ERR_INVALID_ARG (NULL
+ * arena, unknown option, value not 0 or 1). */
+#define RF_ARENA_MERGE_RUNS 1
+#define RF_ARENA_LANES 2
+RF_API rf_status rf_arena_configure(rf_arena *arena, int option, int value);
+
 /* Host wait with a deadline: blocks until every copy the arena has enqueued
  * and every launch that read one of its slots (eager use) has finished, or
  * until timeout_ms milliseconds have passed (neurostream, "Bugs worth

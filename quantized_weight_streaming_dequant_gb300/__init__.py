@@ -78,6 +78,7 @@ _SIGS = {
     "rf_arena_destroy": ([_P], None),
     "rf_arena_wait": ([_P, _I], _I),
     "rf_arena_inject_fault": ([_P, _I, _I64, _I], _I),
+    "rf_arena_configure": ([_P, _I, _I], _I),
     "rf_stream_plan": ([_I, _I64, _I64, _I64, _I, _SZ, ctypes.POINTER(_I64),
                         ctypes.POINTER(_I64), ctypes.POINTER(_SZ)], _I),
     "rf_stream_linear": ([_I, _P, _I64, _I64, _I64, _I64, _I, _P, _P, _P, _P], _I),
@@ -271,6 +272,7 @@ def stream_plan(fmt: int, in_dim: int, n_rows: int, block_rows: int, depth: int,
 
 
 FAULT_NONE, FAULT_COPY_FAIL, FAULT_COPY_STALL = 0, 1, 2
+ARENA_MERGE_RUNS, ARENA_LANES = 1, 2
 
 
 class Arena:
@@ -289,6 +291,11 @@ class Arena:
         if code not in (OK, 6):
             raise RFError(code, "rf_arena_wait")
         return code
+
+    def configure(self, option: int, value: bool) -> None:
+        """rf_arena_configure: ARENA_MERGE_RUNS / ARENA_LANES on or off."""
+        _check(lib().rf_arena_configure(self.handle, option, int(bool(value))),
+               "rf_arena_configure")
 
     def inject_fault(self, kind: int, block: int, ms: int = 0) -> None:
         """rf_arena_inject_fault (test hook)."""

@@ -30,6 +30,8 @@ struct rf_arena {
     int last_slots = 0;
     size_t last_stride = 0;
     rf_stream_stats_t stats = {};
+    bool merge_runs = true;           // RF_ARENA_MERGE_RUNS
+    bool use_lanes = true;            // RF_ARENA_LANES
     // One-shot host-side failure injection (rf_arena_inject_fault).
     int fault_kind = 0;
     int64_t fault_block = 0;

@@ -438,6 +438,19 @@ rf_status rf_arena_wait(rf_arena *a, int timeout_ms)
     return st;
 }
 
+rf_status rf_arena_configure(rf_arena *a, int option, int value)
+{
+    if (!a || (value != 0 && value != 1)) return RF_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(a->mu);
+    if (option == RF_ARENA_MERGE_RUNS)
+        a->merge_runs = value != 0;
+    else if (option == RF_ARENA_LANES)
+        a->use_lanes = value != 0;
+    else
+        return RF_ERR_INVALID_ARG;
+    return RF_OK;
+}
+
 rf_status rf_arena_inject_fault(rf_arena *a, int kind, int64_t block, int ms)
 {
     if (!a || block < 0 || ms < 0 || ms > 10000) return RF_ERR_INVALID_ARG;
@@ -504,7 +517,8 @@ rf_status rf_stream_linear(int fmt, const void *host_W, int64_t in_dim, int64_t 
     const int64_t fault_at = a->fault_block;
     const int fault_ms = a->fault_ms;
     a->fault_kind = RF_FAULT_NONE;
-    if (nblk > 1 && nblk <= slots && (packed || nblk <= 16) && fault == RF_FAULT_NONE) {
+    if (nblk > 1 && nblk <= slots && (packed || nblk <= 16) && fault == RF_FAULT_NONE &&
+        a->merge_runs) {
         int first = 0;
         uint8_t *base = nullptr;
         const int64_t last_rows = n_rows - (nblk - 1) * eff;
@@ -546,7 +560,8 @@ rf_status rf_stream_linear(int fmt, const void *host_W, int64_t in_dim, int64_t 
     // lane (a fan-out costs a fork and a join per walk, which a short walk
     // does not earn back; in a CUDA graph each is a cross-branch dependency).
     LaneFan fan{a, s,
-                eff * rb <= (int64_t)(1 << 20) && (n_rows + eff - 1) / eff >= 2 * rf_arena::kLanes};
+                a->use_lanes && eff * rb <= (int64_t)(1 << 20) &&
+                    (n_rows + eff - 1) / eff >= 2 * rf_arena::kLanes};
     if (const rf_status st = fan.begin()) return st;
     int64_t blocks = 0;
     rf_status err = RF_OK;

@@ -190,6 +190,7 @@ def test_failure_hooks_check_arguments(L):
     """The test hooks and the deadline wait refuse bad arguments on the host."""
     assert L.rf_arena_wait(None, 10) == 1
     assert L.rf_arena_inject_fault(None, 1, 0, 0) == 1
+    assert L.rf_arena_configure(None, 1, 0) == 1
     assert L.rf_debug_arm_wait_fault(2000001) == 1
     assert L.rf_debug_arm_wait_fault(0) == 0   # disarm
     h = ctypes.c_void_p()

@@ -131,3 +131,29 @@ def test_stream_copy_stall_host_wait_deadline(rf):
     finally:
         torch.cuda.synchronize()
         arena.close()
+
+
+def test_arena_options_keep_bits(rf):
+    """Turning off the one-copy merge of walks that fit the ring, or the lane
+    streams, changes how blocks are copied and launched, not the result."""
+    import torch
+    fmt, rows, in_dim = syn.Q8_0, 512, 2048
+    W_np = syn.quant_matrix(fmt, rows, in_dim, seed=330)
+    host = torch.from_numpy(W_np).pin_memory()
+    x = dev_tensor(syn.normal_f32(in_dim, 331))
+    y_res = rf.gemv(fmt, dev_tensor(W_np), 0, rows, in_dim, x)
+    arena = rf.Arena(8 << 20)
+    try:
+        for merge in (True, False):
+            for lanes in (True, False):
+                arena.configure(rf.ARENA_MERGE_RUNS, merge)
+                arena.configure(rf.ARENA_LANES, lanes)
+                for br, depth in ((128, 4), (32, 8), (16, 2)):
+                    b0 = arena.stats()["blocks"]
+                    y = arena.stream_linear(fmt, host, in_dim, 0, rows, br, depth, x)
+                    torch.cuda.synchronize()
+                    assert np.array_equal(bits(y), bits(y_res)), (merge, lanes, br, depth)
+                    assert arena.stats()["blocks"] - b0 == rows // br
+    finally:
+        torch.cuda.synchronize()
+        arena.close()
