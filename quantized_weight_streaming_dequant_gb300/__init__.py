@@ -72,6 +72,8 @@ _SIGS = {
     "rf_ffn_swiglu": ([_I, _P, _P, _P, _I64, _I64, _P, _P, _P, _P], _I),
     "rf_ffn_workspace_bytes": ([_I64], _SZ),
     "rf_gemv_host": ([_I, _P, _I64, _I64, _I64, _P, _P, _P], _I),
+    "rf_gemm": ([_I, _P, _I64, _I64, _I64, _I, _P, _I64, _P, _I64, _P, _SZ, _P], _I),
+    "rf_gemm_workspace_bytes": ([_I, _I64, _I], _SZ),
     "rf_gemv_multi": ([_I, _P, _I64, _I64, _I64, _I, _P, _I64, _P, _I64, ctypes.c_uint, _P], _I),
     "rf_ffn_swiglu_ws": ([_I, _P, _P, _P, _I64, _I64, _P, _P, _P, _P, ctypes.c_uint, _P], _I),
     "rf_arena_create": ([_SZ, _I, ctypes.POINTER(_P)], _I),
@@ -198,6 +200,34 @@ def gemv_multi(fmt: int, W, row_start: int, row_end: int, in_dim: int, X, Y=None
     _check(lib().rf_gemv_multi(fmt, _dev_ptr(W, "W"), row_start, row_end, in_dim, n_tok,
                                X.data_ptr(), X.stride(0), Y.data_ptr(), Y.stride(0), flags,
                                _stream(stream)), "rf_gemv_multi")
+    return Y
+
+
+def gemm_workspace_bytes(fmt: int, in_dim: int, n_tok: int) -> int:
+    return int(lib().rf_gemm_workspace_bytes(fmt, in_dim, n_tok))
+
+
+def gemm(fmt: int, W, row_start: int, row_end: int, in_dim: int, X, Y=None, workspace=None,
+         stream=None):
+    """rf_gemm (tensor cores): X is (n_tok, in_dim) float32 on the device
+    (rows may be strided); returns Y (n_tok, row_end - row_start).  The
+    workspace (a uint8 device tensor) is allocated when not given."""
+    import torch
+    if X.dim() != 2 or X.stride(1) != 1:
+        raise ValueError("X must be 2-D with unit stride along in_dim")
+    n_tok = X.shape[0]
+    if Y is None:
+        Y = torch.empty(n_tok, max(row_end - row_start, 0), dtype=torch.float32, device=X.device)
+    if Y.dim() != 2 or Y.stride(1) != 1:
+        raise ValueError("Y must be 2-D with unit stride along the rows")
+    need = gemm_workspace_bytes(fmt, in_dim, n_tok)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=X.device)
+    ws, ws_bytes = (workspace.data_ptr(), workspace.numel() * workspace.element_size()) \
+        if workspace is not None else (None, 0)
+    _check(lib().rf_gemm(fmt, _dev_ptr(W, "W"), row_start, row_end, in_dim, n_tok,
+                         X.data_ptr(), X.stride(0), Y.data_ptr(), Y.stride(0), ws, ws_bytes,
+                         _stream(stream)), "rf_gemm")
     return Y
 
 

@@ -434,7 +434,13 @@ rf_status rf_ffn_swiglu_ws(int fmt, const void *gate, const void *up, const void
     return launch_rowwin(d2, s);
 }
 
-rf_status rf_device_status(void) { return read_and_clear_device_status(); }
+rf_status rf_device_status(void)
+{
+    const rf_status a = read_and_clear_device_status();
+    if (a == RF_ERR_CUDA) return a;
+    const rf_status b = read_and_clear_gemm_status();
+    return a != RF_OK ? a : b;
+}
 
 rf_status rf_debug_arm_wait_fault(uint32_t limit_us) { return arm_wait_fault(limit_us); }
 

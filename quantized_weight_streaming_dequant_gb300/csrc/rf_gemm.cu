@@ -1,0 +1,967 @@
+// rf_gemm.cu -- prefill dequant-GEMM on the fifth-generation tensor cores.
+//
+// What it computes (neurostream, "What the numbers taught us": a prompt or
+// an image prefills through one pass over the weights for the whole chunk of
+// tokens): Y[t][r - row_start] = sum_i w[r,i] * X[t][i] for every row r of a
+// window and every token t of the chunk.  Unlike batch-1 decode this is a
+// dense contraction (2 * n_tok flops per weight), so it runs on tcgen05.mma.
+//
+// Main path (rows 16-byte aligned, gemm_tc_kernel):
+//   * A pre-pass rounds X to fp16 once, into the operand layout of the MMA
+//     (tiles of N tokens x 64 inputs, K-major core matrices), in a caller
+//     workspace.
+//   * A CTA owns 128 rows x N tokens (N = 64, 128 or 256) and accumulates
+//     the whole of K in tensor memory (N fp32 columns).
+//   * One thread streams the raw quantized bytes of its 128 rows, a chunk
+//     of 8 or 16 blocks at a time, with 2-D tensor copies into a ring; one
+//     thread streams the fp16 activation tiles with 1-D bulk copies.
+//   * Eight decoder warps turn each 64-input slice of the raw rows into
+//     fp16 weights w = d * q (one rounding; MXFP4 values are exact) in the
+//     core-matrix layout; two groups of four warps take alternate slices.
+//   * One thread issues four tcgen05.mma (M=128, N, K=16) per slice and
+//     commits them to the slice's "empty" barrier; the last commit releases
+//     the epilogue, which reads the accumulator out of tensor memory.
+//   Error: w and x each carry one fp16 rounding (relative 2^-11, absolute
+//   2^-25 below the normal range), accumulation is fp32.
+//
+// General path (any row alignment, gemm_exact_kernel): one 32-weight block
+// per stage, decoded to its exact quant values; the block scale is applied
+// in fp32 after each block's MMA, so only x is rounded.
+//
+// Every wait is bounded; after a failure every role stops, copies and MMAs
+// already issued are waited for, and tensor memory is freed on every path.
+#include <cuda_fp16.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <type_traits>
+
+#include "rf_device.cuh"
+#include "rf_internal.h"
+
+namespace rf {
+namespace {
+
+__device__ int g_gemm_status = 0;   // bounded-wait failures (read by rf_device_status)
+
+constexpr int kGM = 128;       // rows per CTA (MMA M)
+constexpr int kGN = 64;        // tokens per CTA (MMA N)
+constexpr int kGK = 32;        // K per stage: one quantization block
+constexpr int kGStages = 4;
+constexpr int kGThreads = 288; // warps 0-3 epilogue, 4-7 producers, 8 MMA + TMEM
+constexpr int kATile = kGM * kGK * 2;   // 8 KB of fp16
+constexpr int kBTile = kGN * kGK * 2;   // 4 KB of fp16
+constexpr uint32_t kTmemCols = 2 * kGN; // two accumulators of 64 fp32 columns
+
+// Byte offset of element (row r, k) of a K-major tile of 32 fp16 columns in
+// the core-matrix layout: core matrix (r/8, k/8) at (r/8)*512 + (k/8)*128,
+// its 8 rows 16 bytes apart.  So the stride between core matrices along K
+// (leading dimension) is 128 bytes and along rows (stride dimension) 512.
+__device__ __forceinline__ int cm_off(int r, int k)
+{
+    return (r >> 3) * 512 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2;
+}
+
+// Shared-memory matrix descriptor of a K-major tile without swizzle: start
+// address, leading-dimension byte offset 128 (the next core matrix along K),
+// stride-dimension byte offset `sbo` (the next 8 rows), the fixed version
+// bits.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t sbo)
+{
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(128 >> 4) << 16;
+    d |= (uint64_t)(sbo >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, fp16 A and B (the
+// same type), both K-major, M = 128, the given N.
+__host__ __device__ constexpr uint32_t idesc_of(int n)
+{
+    return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(kGM >> 4) << 24);
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(dst)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before()
+{
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after()
+{
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on `bar` when every tcgen05 operation this thread issued
+// before has completed.
+__device__ __forceinline__ void tc_commit(uint64_t *bar)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_addr(bar))
+        : "memory");
+}
+// Make this thread's generic-proxy shared-memory writes visible to the
+// tensor core (async proxy).
+__device__ __forceinline__ void fence_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// 32 TMEM lanes x 32 consecutive 32-bit columns into 32 registers per lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
+        "[%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+          "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
+          "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+          "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
+          "=r"(v[31])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait()
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// fp16 value (as bits) of a small signed integer |v| <= 2048 (exact).
+__device__ __forceinline__ uint32_t h_of_int(int v)
+{
+    return (uint32_t)__half_as_ushort(__int2half_rn(v));
+}
+
+// The 32 quant values of one block as fp16 bit pairs (q[i] holds elements
+// 2i and 2i+1), and the block's scale as fp32.
+template <int FMT>
+__device__ __forceinline__ void decode_block_h(const uint8_t *blk, uint32_t (&q)[16])
+{
+    if constexpr (FMT == RF_Q8_0) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int a = (int8_t)blk[2 + 2 * i], b = (int8_t)blk[3 + 2 * i];
+            q[i] = h_of_int(a) | (h_of_int(b) << 16);
+        }
+    } else if constexpr (FMT == RF_Q4_0) {
+        // element j < 16: low nibble of byte j; j + 16: its high nibble
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint8_t b0 = blk[2 + 2 * i], b1 = blk[3 + 2 * i];
+            q[i] = h_of_int((b0 & 15) - 8) | (h_of_int((b1 & 15) - 8) << 16);
+            q[8 + i] = h_of_int((b0 >> 4) - 8) | (h_of_int((b1 >> 4) - 8) << 16);
+        }
+    } else {
+        // MXFP4: an E2M1 code (s e1 e0 m) placed as fp16 bits s at 15 and
+        // e1 e0 m at 11..9 is exactly its value times 2^-14; the block scale
+        // carries the 2^14 back (block_scale_f).
+        auto h = [](uint32_t c) -> uint32_t { return ((c & 7u) << 9) | ((c & 8u) << 12); };
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint8_t b0 = blk[1 + 2 * i], b1 = blk[2 + 2 * i];
+            q[i] = h(b0 & 15u) | (h(b1 & 15u) << 16);
+            q[8 + i] = h(b0 >> 4) | (h(b1 >> 4) << 16);
+        }
+    }
+}
+
+template <int FMT>
+__device__ __forceinline__ float block_scale_f(const uint8_t *blk)
+{
+    if constexpr (FMT == RF_MXFP4) {
+        // 2^(E-127) times the 2^14 taken out of the decoded values
+        const uint32_t E = blk[0];
+        if (E == 255u) return __uint_as_float(0x7fc00000u);
+        if (E > 240u) return __uint_as_float(0x7f800000u);
+        return __uint_as_float((E + 14u) << 23);
+    } else {
+        return __half2float(__ushort_as_half((unsigned short)(blk[0] | (blk[1] << 8))));
+    }
+}
+
+struct ExactParams {
+    const uint8_t *W;
+    const float *X;
+    float *Y;
+    int64_t row_start, row_end, ldx, ldy, rb;   // rb: bytes per row
+    int32_t nb, n_tok;
+    unsigned long long limit;
+};
+
+template <int FMT>
+__global__ void __launch_bounds__(kGThreads, 1) gemm_exact_kernel(const __grid_constant__ ExactParams p)
+{
+    constexpr int BS = FMT == RF_Q8_0 ? 34 : (FMT == RF_Q4_0 ? 18 : 17);
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint8_t *a_tiles = smem;                                   // [stages][8 KB]
+    uint8_t *b_tiles = smem + kGStages * kATile;               // [stages][4 KB]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(b_tiles + kGStages * kBTile);
+    uint64_t *full = bars, *empty = bars + kGStages;           // operand stages
+    uint64_t *acc_full = bars + 2 * kGStages, *acc_empty = acc_full + 2;
+    uint64_t *done = acc_empty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+    volatile int *stop = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t row0 = p.row_start + (int64_t)blockIdx.x * kGM;
+    const int tok0 = blockIdx.y * kGN;
+    const int nb = p.nb;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kGStages; ++s) {
+            mbar_init(&full[s], 128);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 128);
+        }
+        mbar_init(done, 1);
+        *stop = 0;
+        fence_barrier_init();
+    }
+    if (warp == 8) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    // A wait that gives up stops every role of the CTA.
+    auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
+        if (*stop) return false;
+        if (mbar_wait_bounded(bar, parity, &g_gemm_status, p.limit)) return true;
+        *stop = 1;
+        return false;
+    };
+
+    if (warp >= 4 && warp < 8) {
+        // Producers: thread i decodes row i of the tile and converts 16 of
+        // the 64 x 32 activations of each block.
+        const int i = (int)threadIdx.x - 128;
+        const int64_t r = row0 + i;
+        const bool row_ok = r < p.row_end;
+        const uint8_t *wrow = p.W + (row_ok ? r : p.row_start) * p.rb;
+        const int t = i >> 1, kk = (i & 1) * 16;
+        const bool tok_ok = tok0 + t < p.n_tok;
+        const float *xrow = p.X + (int64_t)(tok_ok ? tok0 + t : 0) * p.ldx;
+        for (int b = 0; b < nb; ++b) {
+            const int s = b % kGStages;
+            if (!__all_sync(0xffffffffu, wait(&empty[s], ((b / kGStages) & 1) ^ 1))) break;
+            uint32_t q[16];
+            if (row_ok) {
+                decode_block_h<FMT>(wrow + (int64_t)b * BS, q);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 16; ++k) q[k] = 0;
+            }
+            uint8_t *at = a_tiles + s * kATile;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                *reinterpret_cast<uint4 *>(at + cm_off(i, 8 * c)) =
+                    make_uint4(q[4 * c], q[4 * c + 1], q[4 * c + 2], q[4 * c + 3]);
+            uint8_t *bt = b_tiles + s * kBTile;
+            uint32_t xh[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                float x0 = 0.f, x1 = 0.f;
+                if (tok_ok) {
+                    x0 = xrow[32 * (int64_t)b + kk + 2 * k];
+                    x1 = xrow[32 * (int64_t)b + kk + 2 * k + 1];
+                }
+                xh[k] = (uint32_t)__half_as_ushort(__float2half_rn(x0)) |
+                        ((uint32_t)__half_as_ushort(__float2half_rn(x1)) << 16);
+            }
+            *reinterpret_cast<uint4 *>(bt + cm_off(t, kk)) = make_uint4(xh[0], xh[1], xh[2], xh[3]);
+            *reinterpret_cast<uint4 *>(bt + cm_off(t, kk + 8)) = make_uint4(xh[4], xh[5], xh[6], xh[7]);
+            fence_async_smem();
+            mbar_arrive(&full[s]);
+        }
+    } else if (warp == 8) {
+        // MMA issue: one thread.
+        if (lane == 0) {
+            int issued = 0;
+            for (int b = 0; b < nb; ++b) {
+                const int s = b % kGStages, buf = b & 1;
+                if (!wait(&full[s], (b / kGStages) & 1)) break;
+                if (!wait(&acc_empty[buf], ((b >> 1) & 1) ^ 1)) break;
+                tc_fence_after();
+                const uint32_t a = smem_addr(a_tiles + s * kATile);
+                const uint32_t bb = smem_addr(b_tiles + s * kBTile);
+                const uint32_t d = tmem + (uint32_t)(buf * kGN);
+                tc_mma(d, smem_desc(a, 512), smem_desc(bb, 512), idesc_of(kGN), 0);
+                tc_mma(d, smem_desc(a + 256, 512), smem_desc(bb + 256, 512), idesc_of(kGN), 1);
+                tc_commit(&empty[s]);
+                tc_commit(&acc_full[buf]);
+                ++issued;
+            }
+            // Every issued MMA completes before TMEM is freed.
+            if (issued) {
+                tc_commit(done);
+                mbar_drain(done, 0);
+            }
+        }
+        __syncwarp();
+    } else {
+        // Epilogue: thread e owns row e of the tile, TMEM lane e.
+        const int e = (int)threadIdx.x;
+        const int64_t r = row0 + e;
+        const bool row_ok = r < p.row_end;
+        const uint8_t *wrow = p.W + (row_ok ? r : p.row_start) * p.rb;
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        float acc[kGN];
+#pragma unroll
+        for (int n = 0; n < kGN; ++n) acc[n] = 0.f;
+        float scale = row_ok ? block_scale_f<FMT>(wrow) : 0.f;
+        for (int b = 0; b < nb; ++b) {
+            const int buf = b & 1;
+            const float sc = scale;
+            if (row_ok && b + 1 < nb) scale = block_scale_f<FMT>(wrow + (int64_t)(b + 1) * BS);
+            if (!__all_sync(0xffffffffu, wait(&acc_full[buf], (b >> 1) & 1))) break;
+            tc_fence_after();
+            uint32_t v[32];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                tmem_ld32(lane_base + (uint32_t)(buf * kGN + 32 * h), v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int n = 0; n < 32; ++n) acc[32 * h + n] = fmaf(sc, __uint_as_float(v[n]), acc[32 * h + n]);
+            }
+            tc_fence_before();
+            mbar_arrive(&acc_empty[buf]);
+        }
+        if (row_ok && !*stop) {
+            const int64_t y_row = r - p.row_start;
+#pragma unroll
+            for (int n = 0; n < kGN; ++n)
+                if (tok0 + n < p.n_tok) p.Y[(int64_t)(tok0 + n) * p.ldy + y_row] = acc[n];
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 8) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+constexpr size_t kExactSmem = (size_t)kGStages * (kATile + kBTile) + (2 * kGStages + 5) * 8 + 16;
+
+template <int FMT>
+rf_status launch_exact(const ExactParams &p, dim3 grid, cudaStream_t s)
+{
+    static std::once_flag once[64];
+    static bool ok[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return RF_ERR_CUDA;
+    }
+    std::call_once(once[dev & 63], [dev] {
+        ok[dev & 63] = cudaFuncSetAttribute(gemm_exact_kernel<FMT>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            (int)kExactSmem) == cudaSuccess;
+        cudaGetLastError();
+    });
+    if (!ok[dev & 63]) return RF_ERR_CUDA;
+    gemm_exact_kernel<FMT><<<grid, kGThreads, kExactSmem, s>>>(p);
+    return last_cuda_error();
+}
+
+// ---------------------------------------------------------------- main path
+constexpr int kTK = 64;                  // inputs per operand slice: two blocks
+constexpr int kTThreads = 384;           // 12 warps
+constexpr int kATileT = kGM * kTK * 2;   // fp16 weight tile of one slice (16 KB)
+constexpr int kDecWarp0 = 4;             // warps 4-11 decode, then read out
+
+// Raw chunk of each format: BPC blocks of each of the 128 rows per tensor
+// copy (BPC * BS is a multiple of 16, so every chunk starts on a 16-byte
+// boundary of a 16-byte aligned row), R chunks in flight.
+template <int FMT> struct RawCfg;
+template <> struct RawCfg<RF_Q4_0> { static constexpr int BS = 18, BPC = 8, R = 3; };
+template <> struct RawCfg<RF_Q8_0> { static constexpr int BS = 34, BPC = 8, R = 2; };
+template <> struct RawCfg<RF_MXFP4> { static constexpr int BS = 17, BPC = 16, R = 2; };
+
+// Slots of the operand ring (a decoded-weight tile and an activation tile
+// each) for a token tile of N.  The two decoder groups take alternate
+// slices, so a ring of at least two slots keeps every parity wait within
+// one phase of its barrier.
+template <int N> __host__ __device__ constexpr int tc_stages() { return N == 256 ? 3 : (N == 128 ? 4 : 6); }
+
+template <int FMT, int N>
+constexpr size_t tc_smem()
+{
+    using RC = RawCfg<FMT>;
+    return (size_t)tc_stages<N>() * (kATileT + N * kTK * 2) +
+           (size_t)RC::R * kGM * RC::BPC * RC::BS + 16 +
+           (size_t)(3 * tc_stages<N>() + 2 * RC::R + 2) * 8 + 16;
+}
+
+struct TcParams {
+    CUtensorMap wmap;   // the window's rows as uint16 columns; boxes of one chunk x 128 rows
+    const uint8_t *Xp;  // fp16 activation tiles: [token tile][slice][N x 64]
+    float *Y;
+    int64_t ldy;
+    int32_t rows, n_tok, nst, nch;   // nst: 64-input slices; nch: raw chunks
+    unsigned long long limit;
+};
+
+__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// Bytes [OFF, OFF + NB) of a 16-byte aligned row slot: the 16-byte units
+// holding them, as words; word<P>, half<P> and byte<P> read at OFF + P.
+template <int OFF, int NB>
+struct RawWin {
+    static constexpr int A = OFF & ~15;
+    static constexpr int NU = (OFF + NB - 1 - A) / 16 + 1;
+    uint32_t w[4 * NU];
+    __device__ __forceinline__ void load(const uint8_t *slot)
+    {
+#pragma unroll
+        for (int u = 0; u < NU; ++u) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(slot + A + 16 * u);
+            w[4 * u] = v.x;
+            w[4 * u + 1] = v.y;
+            w[4 * u + 2] = v.z;
+            w[4 * u + 3] = v.w;
+        }
+    }
+    template <int P> __device__ __forceinline__ uint32_t word() const
+    {
+        constexpr int B = OFF - A + P;
+        if constexpr (B % 4 == 0) return w[B / 4];
+        else return __funnelshift_r(w[B / 4], w[B / 4 + 1], 8 * (B % 4));
+    }
+    template <int P> __device__ __forceinline__ uint32_t half() const
+    {
+        constexpr int B = OFF - A + P;
+        static_assert(B % 2 == 0, "fp16 scale at an odd byte");
+        return (w[B / 4] >> (8 * (B % 4))) & 0xFFFFu;
+    }
+    template <int P> __device__ __forceinline__ uint32_t byte() const
+    {
+        constexpr int B = OFF - A + P;
+        return (w[B / 4] >> (8 * (B % 4))) & 0xFFu;
+    }
+};
+
+// One block of 32 weights as 16 fp16 pairs (out[m] holds elements 2m and
+// 2m+1).  Q4_0: element j < 16 is the low nibble of byte j, j + 16 its high
+// nibble; 0x6400 | n is the fp16 value 1024 + n, so subtracting 1032 gives
+// n - 8 exactly and one multiply by d rounds the weight once.
+__device__ __forceinline__ void q4_0_pairs(uint32_t d, const uint32_t (&qs)[4], uint32_t *out)
+{
+    const uint32_t dd = d | (d << 16);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t t01 = prmt(qs[j], 0u, 0x4140u), t23 = prmt(qs[j], 0u, 0x4342u);
+        out[2 * j] = hmul2(hsub2((t01 & 0x000F000Fu) | 0x64006400u, 0x64086408u), dd);
+        out[2 * j + 1] = hmul2(hsub2((t23 & 0x000F000Fu) | 0x64006400u, 0x64086408u), dd);
+        out[8 + 2 * j] = hmul2(hsub2(((t01 >> 4) & 0x000F000Fu) | 0x64006400u, 0x64086408u), dd);
+        out[9 + 2 * j] = hmul2(hsub2(((t23 >> 4) & 0x000F000Fu) | 0x64006400u, 0x64086408u), dd);
+    }
+}
+// Q8_0: byte j is element j (int8); with the sign bit flipped, 0x6400 | u is
+// 1024 + q + 128, so subtracting 1152 gives q exactly.
+__device__ __forceinline__ void q8_0_pairs(uint32_t d, const uint32_t (&qs)[8], uint32_t *out)
+{
+    const uint32_t dd = d | (d << 16);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t v = qs[j] ^ 0x80808080u;
+        out[2 * j] = hmul2(hsub2(prmt(v, 0x64646464u, 0x5140u), 0x64806480u), dd);
+        out[2 * j + 1] = hmul2(hsub2(prmt(v, 0x64646464u, 0x7362u), 0x64806480u), dd);
+    }
+}
+// fp16 bits of 2^k: normal for k >= -14, subnormal down to 2^-24, 0 below,
+// infinity above 2^15.
+__device__ __forceinline__ uint32_t pow2_h(int k)
+{
+    if (k > 15) return 0x7C00u;
+    if (k >= -14) return (uint32_t)(k + 15) << 10;
+    if (k >= -24) return 1u << (k + 24);
+    return 0u;
+}
+// MXFP4: an E2M1 code (s e1 e0 m) placed as fp16 bits s at 15 and e1 e0 m at
+// 11..9 is exactly its value times 2^-14 (e = 0 lands on the fp16
+// subnormals); the block scale 2^(E-127) then enters as 2^(E-113), one exact
+// multiply whenever the product is representable.  Element order as Q4_0.
+__device__ __forceinline__ void mxfp4_pairs(uint32_t E, const uint32_t (&qs)[4], uint32_t *out)
+{
+    uint32_t s1, s2 = 0u;
+    if (E == 255u) s1 = 0x7E00u;                       // NaN scale
+    else if (E <= 128u) s1 = pow2_h((int)E - 113);
+    else { s1 = 0x7400u; s2 = pow2_h((int)E - 127); }  // 2^14, then 2^(E-127)
+    const uint32_t ss = s1 | (s1 << 16);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t t01 = prmt(qs[j], 0u, 0x4140u), t23 = prmt(qs[j], 0u, 0x4342u);
+        out[2 * j] = hmul2(((t01 << 9) & 0x0E000E00u) | ((t01 << 12) & 0x80008000u), ss);
+        out[2 * j + 1] = hmul2(((t23 << 9) & 0x0E000E00u) | ((t23 << 12) & 0x80008000u), ss);
+        out[8 + 2 * j] = hmul2(((t01 << 5) & 0x0E000E00u) | ((t01 << 8) & 0x80008000u), ss);
+        out[9 + 2 * j] = hmul2(((t23 << 5) & 0x0E000E00u) | ((t23 << 8) & 0x80008000u), ss);
+    }
+    if (s2) {
+        const uint32_t s22 = s2 | (s2 << 16);
+#pragma unroll
+        for (int m = 0; m < 16; ++m) out[m] = hmul2(out[m], s22);
+    }
+}
+
+// Slice Q of a raw chunk (blocks 2Q and 2Q+1 of one row) as 32 fp16 pairs.
+template <int FMT, int Q>
+__device__ __forceinline__ void decode_slice(const uint8_t *slot, uint32_t (&out)[32])
+{
+    using RC = RawCfg<FMT>;
+    RawWin<Q * 2 * RC::BS, 2 * RC::BS> win;
+    win.load(slot);
+    if constexpr (FMT == RF_Q4_0) {
+        const uint32_t q0[4] = {win.template word<2>(), win.template word<6>(),
+                                win.template word<10>(), win.template word<14>()};
+        const uint32_t q1[4] = {win.template word<20>(), win.template word<24>(),
+                                win.template word<28>(), win.template word<32>()};
+        q4_0_pairs(win.template half<0>(), q0, out);
+        q4_0_pairs(win.template half<18>(), q1, out + 16);
+    } else if constexpr (FMT == RF_Q8_0) {
+        const uint32_t q0[8] = {win.template word<2>(),  win.template word<6>(),
+                                win.template word<10>(), win.template word<14>(),
+                                win.template word<18>(), win.template word<22>(),
+                                win.template word<26>(), win.template word<30>()};
+        const uint32_t q1[8] = {win.template word<36>(), win.template word<40>(),
+                                win.template word<44>(), win.template word<48>(),
+                                win.template word<52>(), win.template word<56>(),
+                                win.template word<60>(), win.template word<64>()};
+        q8_0_pairs(win.template half<0>(), q0, out);
+        q8_0_pairs(win.template half<34>(), q1, out + 16);
+    } else {
+        const uint32_t q0[4] = {win.template word<1>(), win.template word<5>(),
+                                win.template word<9>(), win.template word<13>()};
+        const uint32_t q1[4] = {win.template word<18>(), win.template word<22>(),
+                                win.template word<26>(), win.template word<30>()};
+        mxfp4_pairs(win.template byte<0>(), q0, out);
+        mxfp4_pairs(win.template byte<17>(), q1, out + 16);
+    }
+}
+
+// Compile-time loop over the slices of a chunk: f(integral_constant<Q>) for
+// Q = Q0 .. QN-1 while it returns true.
+template <int Q0, int QN>
+struct SliceLoop {
+    template <class F> __device__ __forceinline__ static bool run(F &f)
+    {
+        if (!f(std::integral_constant<int, Q0>())) return false;
+        return SliceLoop<Q0 + 1, QN>::run(f);
+    }
+};
+template <int QN>
+struct SliceLoop<QN, QN> {
+    template <class F> __device__ __forceinline__ static bool run(F &) { return true; }
+};
+
+template <int FMT, int N>
+__global__ void __launch_bounds__(kTThreads, 1) gemm_tc_kernel(const __grid_constant__ TcParams p)
+{
+    using RC = RawCfg<FMT>;
+    constexpr int S = tc_stages<N>(), R = RC::R, CB = RC::BPC * RC::BS, QPC = RC::BPC / 2;
+    constexpr int BT = N * kTK * 2;   // fp16 activation tile of one slice
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint8_t *a_t = smem;                 // [S][16 KB]
+    uint8_t *b_t = a_t + S * kATileT;    // [S][BT]
+    uint8_t *raw = b_t + S * BT;         // [R][128 rows][CB]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(raw + (size_t)R * kGM * CB + 16);
+    // full: the slot's weights decoded and its activations landed (one
+    // arrival per decoder warp); bfull: the activation copy's bytes; empty:
+    // the slot's MMAs done.
+    uint64_t *full = bars, *bfull = bars + S, *empty = bars + 2 * S;
+    uint64_t *rfull = bars + 3 * S, *rempty = rfull + R;
+    uint64_t *accf = rempty + R, *mdone = accf + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mdone + 1);
+    volatile int *stop = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tt = blockIdx.x, rt = blockIdx.y;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 4);
+            mbar_init(&bfull[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int r = 0; r < R; ++r) {
+            mbar_init(&rfull[r], 1);
+            mbar_init(&rempty[r], 8);
+        }
+        mbar_init(accf, 1);
+        mbar_init(mdone, 1);
+        *stop = 0;
+        fence_barrier_init();
+    }
+    if (warp == 3) {
+        tmem_alloc(tmem_slot, (uint32_t)N);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*stop) return false;
+        if (mbar_wait_bounded(bar, parity, &g_gemm_status, p.limit)) return true;
+        *stop = 1;
+        return false;
+    };
+
+    if (warp == 0) {
+        // Raw rows: one 2-D tensor copy per chunk of 128 rows.
+        if (lane == 0) {
+            int issued = 0;
+            for (int c = 0; c < p.nch; ++c) {
+                const int rs = c % R;
+                if (!wait(&rempty[rs], ((c / R) & 1) ^ 1)) break;
+                mbar_arrive_expect_tx(&rfull[rs], (uint32_t)(kGM * CB));
+                tma_2d_g2s(raw + (size_t)rs * kGM * CB, &p.wmap, c * (CB / 2), rt * kGM, &rfull[rs]);
+                ++issued;
+            }
+            for (int c = max(0, issued - R); c < issued; ++c) mbar_drain(&rfull[c % R], (c / R) & 1);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // Activation tiles: one 1-D bulk copy per slice.
+        if (lane == 0) {
+            const uint8_t *xs = p.Xp + (size_t)tt * p.nst * BT;
+            int issued = 0;
+            for (int b = 0; b < p.nst; ++b) {
+                const int s = b % S;
+                if (!wait(&empty[s], ((b / S) & 1) ^ 1)) break;
+                mbar_arrive_expect_tx(&bfull[s], (uint32_t)BT);
+                bulk_g2s(b_t + (size_t)s * BT, xs + (size_t)b * BT, (uint32_t)BT, &bfull[s]);
+                ++issued;
+            }
+            for (int b = max(0, issued - S); b < issued; ++b) mbar_drain(&bfull[b % S], (b / S) & 1);
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // MMA issue: four K=16 steps per slice into one accumulator.  The
+        // descriptors of slot 0 are built once; a slot and a K step move
+        // the start-address field (address / 16, well inside its 14 bits).
+        if (lane == 0) {
+            int issued = 0;
+            bool failed = false;
+            const uint64_t ad0 = smem_desc(smem_addr(a_t), 1024);
+            const uint64_t bd0 = smem_desc(smem_addr(b_t), 1024);
+            int s = 0;
+            uint32_t ph = 0;
+            for (int b = 0; b < p.nst; ++b) {
+                if (!wait(&full[s], ph)) {
+                    failed = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t ad = ad0 + (uint64_t)((s * kATileT) >> 4);
+                const uint64_t bd = bd0 + (uint64_t)((s * BT) >> 4);
+                tc_mma(tmem, ad, bd, idesc_of(N), b != 0);
+#pragma unroll
+                for (int kk = 1; kk < kTK / 16; ++kk)
+                    tc_mma(tmem, ad + 16 * kk, bd + 16 * kk, idesc_of(N), 1u);
+                tc_commit(&empty[s]);
+                ++issued;
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!failed) {
+                tc_commit(accf);
+            } else if (issued) {
+                // Every issued MMA completes before tensor memory is freed.
+                tc_commit(mdone);
+                mbar_drain(mdone, 0);
+            }
+        }
+        __syncwarp();
+    } else if (warp >= kDecWarp0) {
+        // Decoders: warp group `grp` takes the slices of its parity; thread
+        // i of a group owns row i of the tile (tensor-memory lane i).
+        const int dw = warp - kDecWarp0;
+        const int grp = dw >> 2;
+        const int i = (dw & 3) * 32 + lane;
+        bool ok = true;
+        for (int c = 0; c < p.nch && ok; ++c) {
+            const int rs = c % R;
+            if (!__all_sync(0xffffffffu, wait(&rfull[rs], (c / R) & 1))) break;
+            const uint8_t *slot = raw + (size_t)rs * kGM * CB + (size_t)i * CB;
+            auto one = [&](auto qc) -> bool {
+                constexpr int Q = decltype(qc)::value;
+                if ((Q & 1) != grp) return true;
+                const int b = c * QPC + Q;
+                if (b >= p.nst) return true;
+                const int s = b % S;
+                const uint32_t ph = (b / S) & 1;
+                if (!__all_sync(0xffffffffu, wait(&empty[s], ph ^ 1))) return false;
+                uint32_t out[32];
+                decode_slice<FMT, Q>(slot, out);
+                uint8_t *at = a_t + (size_t)s * kATileT + (i >> 3) * 1024 + (i & 7) * 16;
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8)
+                    *reinterpret_cast<uint4 *>(at + c8 * 128) =
+                        make_uint4(out[4 * c8], out[4 * c8 + 1], out[4 * c8 + 2], out[4 * c8 + 3]);
+                fence_async_smem();
+                // The slot is complete once its activation tile has landed
+                // too; one arrival per warp.
+                if (!__all_sync(0xffffffffu, wait(&bfull[s], ph))) return false;
+                if (lane == 0) mbar_arrive(&full[s]);
+                return true;
+            };
+            ok = SliceLoop<0, QPC>::run(one);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&rempty[rs]);
+        }
+        // Epilogue: the group's half of the accumulator columns.
+        if (__all_sync(0xffffffffu, wait(accf, 0))) {
+            tc_fence_after();
+            const int64_t row = (int64_t)rt * kGM + i;
+            const bool row_ok = row < p.rows;
+            const uint32_t tb = tmem + ((uint32_t)((dw & 3) * 32) << 16);
+            const int tok0 = tt * N;
+#pragma unroll 1
+            for (int cc = grp * (N / 2); cc < (grp + 1) * (N / 2); cc += 32) {
+                uint32_t v[32];
+                tmem_ld32(tb + (uint32_t)cc, v);
+                tmem_ld_wait();
+                if (row_ok) {
+#pragma unroll
+                    for (int n = 0; n < 32; ++n)
+                        if (tok0 + cc + n < p.n_tok)
+                            p.Y[(int64_t)(tok0 + cc + n) * p.ldy + row] = __uint_as_float(v[n]);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 3) {
+        tc_fence_after();
+        tmem_dealloc(tmem, (uint32_t)N);
+    }
+}
+
+// X (fp32 rows ldx apart) -> fp16 tiles [token tile][slice][N x 64] in the
+// K-major core-matrix layout: element (t, k) of a tile at (t/8)*1024 +
+// (k/8)*128 + (t%8)*16 + (k%8)*2; 16-byte unit u of the whole buffer holds
+// tokens and inputs such that the unit index within a tile is
+// (t/8)*64 + (k/8)*8 + t%8.  Tokens past n_tok and inputs past in_dim are 0.
+template <int N>
+__global__ void __launch_bounds__(256) x16_kernel(const float *X, int64_t ldx, int n_tok,
+                                                  int64_t in_dim, int nst, int64_t units,
+                                                  uint8_t *Xp)
+{
+    for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < units;
+         u += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t tile = u / (N * 8);
+        const int w = (int)(u % (N * 8));
+        const int t = (w >> 6) * 8 + (w & 7), c = (w >> 3) & 7;
+        const int64_t tok = (tile / nst) * N + t;
+        const int64_t k0 = (tile % nst) * kTK + c * 8;
+        uint32_t h[4] = {0u, 0u, 0u, 0u};
+        if (tok < n_tok && k0 < in_dim) {
+            const float *x = X + tok * ldx + k0;
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+                h[m] = (uint32_t)__half_as_ushort(__float2half_rn(x[2 * m])) |
+                       ((uint32_t)__half_as_ushort(__float2half_rn(x[2 * m + 1])) << 16);
+        }
+        *reinterpret_cast<uint4 *>(Xp + u * 16) = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+}
+
+// Token tile of the main path for a chunk of n_tok tokens.
+int tc_n(int n_tok) { return n_tok <= 64 ? 64 : (n_tok <= 128 ? 128 : 256); }
+
+// The main path takes rows whose byte length is a multiple of 16.
+bool tc_rows_ok(int fmt, int64_t in_dim)
+{
+    return ((in_dim / 32) * (int64_t)block_bytes_of(fmt)) % 16 == 0;
+}
+
+size_t tc_workspace(int64_t in_dim, int n_tok)
+{
+    const int64_t N = tc_n(n_tok);
+    const int64_t ntt = (n_tok + N - 1) / N, nst = (in_dim + kTK - 1) / kTK;
+    return (size_t)(ntt * N) * (size_t)nst * kTK * 2;
+}
+
+template <int FMT, int N>
+rf_status launch_tc_n(const TcParams &p, const float *X, int64_t ldx, int64_t in_dim,
+                      uint8_t *Xp, dim3 grid, cudaStream_t s)
+{
+    static_assert(tc_smem<FMT, N>() <= 232448, "rings exceed the 227 KB of shared memory");
+    static std::once_flag once[64];
+    static bool ok[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return RF_ERR_CUDA;
+    }
+    std::call_once(once[dev & 63], [dev] {
+        ok[dev & 63] = cudaFuncSetAttribute(gemm_tc_kernel<FMT, N>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            (int)tc_smem<FMT, N>()) == cudaSuccess;
+        cudaGetLastError();
+    });
+    if (!ok[dev & 63]) return RF_ERR_CUDA;
+    const int64_t units = (int64_t)grid.x * N * p.nst * 8;
+    const int xb = (int)std::min<int64_t>((units + 255) / 256, (int64_t)num_sms() * 8);
+    x16_kernel<N><<<xb, 256, 0, s>>>(X, ldx, p.n_tok, in_dim, p.nst, units, Xp);
+    if (last_cuda_error() != RF_OK) return RF_ERR_CUDA;
+    gemm_tc_kernel<FMT, N><<<grid, kTThreads, tc_smem<FMT, N>(), s>>>(p);
+    return last_cuda_error();
+}
+
+template <int FMT>
+rf_status launch_tc(const TcParams &p, const float *X, int64_t ldx, int64_t in_dim, uint8_t *Xp,
+                    dim3 grid, cudaStream_t s)
+{
+    switch (tc_n(p.n_tok)) {
+    case 64: return launch_tc_n<FMT, 64>(p, X, ldx, in_dim, Xp, grid, s);
+    case 128: return launch_tc_n<FMT, 128>(p, X, ldx, in_dim, Xp, grid, s);
+    default: return launch_tc_n<FMT, 256>(p, X, ldx, in_dim, Xp, grid, s);
+    }
+}
+
+}  // namespace
+
+rf_status read_and_clear_gemm_status()
+{
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_gemm_status, sizeof(int)) != cudaSuccess) return RF_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_gemm_status, &zero, sizeof(int)) != cudaSuccess)
+            return RF_ERR_CUDA;
+    }
+    return static_cast<rf_status>(v);
+}
+
+}  // namespace rf
+
+using namespace rf;
+
+extern "C" {
+
+size_t rf_gemm_workspace_bytes(int fmt, int64_t in_dim, int n_tok)
+{
+    if ((fmt != RF_Q4_0 && fmt != RF_Q8_0 && fmt != RF_MXFP4) || in_dim <= 0 || in_dim % 32 != 0 ||
+        n_tok <= 0 || !tc_rows_ok(fmt, in_dim))
+        return 0;
+    return tc_workspace(in_dim, n_tok);
+}
+
+rf_status rf_gemm(int fmt, const void *W, int64_t row_start, int64_t row_end, int64_t in_dim,
+                  int n_tok, const float *X, int64_t ldx, float *Y, int64_t ldy, void *workspace,
+                  size_t workspace_bytes, void *stream)
+{
+    if (fmt != RF_Q4_0 && fmt != RF_Q8_0 && fmt != RF_MXFP4) return RF_ERR_UNSUPPORTED_FMT;
+    if (!W || !X || !Y || in_dim <= 0 || in_dim % 32 != 0 || row_start < 0 ||
+        row_end < row_start || n_tok < 0 || ldx < in_dim || ldy < row_end - row_start)
+        return RF_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(W) & 15u) != 0) return RF_ERR_MISALIGNED;
+    if (in_dim / 32 > 0x7fffffffLL || (row_end - row_start + kGM - 1) / kGM > 65535 ||
+        (n_tok + kGN - 1) / kGN > 65535)
+        return RF_ERR_TOO_LARGE;
+    const bool tc = tc_rows_ok(fmt, in_dim);
+    const size_t need = tc && n_tok > 0 ? tc_workspace(in_dim, n_tok) : 0;
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) return RF_ERR_INVALID_ARG;
+        if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return RF_ERR_MISALIGNED;
+    }
+    if (row_end == row_start || n_tok == 0) return RF_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t rb = (in_dim / 32) * (int64_t)block_bytes_of(fmt);
+    if (tc) {
+        TcParams p;
+        std::memset(&p, 0, sizeof(p));
+        const int cb = fmt == RF_Q4_0 ? 144 : 272;   // chunk bytes of the format
+        if (!encode_u16_map(&p.wmap, static_cast<const uint8_t *>(W) + row_start * rb,
+                            (uint64_t)(rb / 2), (uint64_t)(row_end - row_start), (uint64_t)rb,
+                            (uint32_t)(cb / 2), (uint32_t)kGM))
+            return RF_ERR_CUDA;
+        p.Xp = static_cast<const uint8_t *>(workspace);
+        p.Y = Y;
+        p.ldy = ldy;
+        p.rows = (int32_t)(row_end - row_start);
+        p.n_tok = n_tok;
+        p.nst = (int32_t)((in_dim + kTK - 1) / kTK);
+        p.nch = (int32_t)((rb + cb - 1) / cb);
+        p.limit = 2000000000ull;
+        const int N = tc_n(n_tok);
+        const dim3 grid((unsigned)((n_tok + N - 1) / N), (unsigned)((row_end - row_start + kGM - 1) / kGM));
+        uint8_t *Xp = static_cast<uint8_t *>(workspace);
+        switch (fmt) {
+        case RF_Q4_0: return launch_tc<RF_Q4_0>(p, X, ldx, in_dim, Xp, grid, s);
+        case RF_Q8_0: return launch_tc<RF_Q8_0>(p, X, ldx, in_dim, Xp, grid, s);
+        default: return launch_tc<RF_MXFP4>(p, X, ldx, in_dim, Xp, grid, s);
+        }
+    }
+    ExactParams p;
+    p.W = static_cast<const uint8_t *>(W);
+    p.X = X;
+    p.Y = Y;
+    p.row_start = row_start;
+    p.row_end = row_end;
+    p.ldx = ldx;
+    p.ldy = ldy;
+    p.rb = rb;
+    p.nb = (int32_t)(in_dim / 32);
+    p.n_tok = n_tok;
+    p.limit = 2000000000ull;
+    const dim3 grid((unsigned)((row_end - row_start + kGM - 1) / kGM), (unsigned)((n_tok + kGN - 1) / kGN));
+    switch (fmt) {
+    case RF_Q4_0: return launch_exact<RF_Q4_0>(p, grid, s);
+    case RF_Q8_0: return launch_exact<RF_Q8_0>(p, grid, s);
+    default: return launch_exact<RF_MXFP4>(p, grid, s);
+    }
+}
+
+}  // extern "C"

@@ -1659,6 +1659,21 @@ bool cached_rows_map(CUtensorMap *m, const void *base, int64_t rows, int64_t rb,
 
 }  // namespace
 
+bool encode_u16_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows,
+                    uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 rf_status arm_wait_fault(uint32_t limit_us)
 {
     if (limit_us > 2000000u) return RF_ERR_INVALID_ARG;

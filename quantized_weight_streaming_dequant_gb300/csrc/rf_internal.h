@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "rf.h"
@@ -96,6 +97,13 @@ size_t block_bytes_of(int fmt);
 inline int64_t block_elems_of(int fmt) { return fmt == RF_Q4_K || fmt == RF_Q6_K ? 256 : 32; }
 rf_status last_cuda_error();
 rf_status read_and_clear_device_status();
+// 2-D tiled tensor map of uint16 elements: `rows` rows of `cols` elements,
+// `row_bytes` apart (a multiple of 16), boxes of box_cols x box_rows, no
+// swizzle, zero fill outside.  False if the driver refuses it.
+bool encode_u16_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows,
+                    uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows);
+// The prefill GEMM's own status word (bounded waits), read and cleared.
+rf_status read_and_clear_gemm_status();
 // Arms the one-shot wait fault of the next producer-mode launch
 // (rf_debug_arm_wait_fault).
 rf_status arm_wait_fault(uint32_t limit_us);
