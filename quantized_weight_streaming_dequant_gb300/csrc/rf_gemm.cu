@@ -523,26 +523,42 @@ __device__ __forceinline__ uint32_t pow2_h(int k)
     if (k >= -24) return 1u << (k + 24);
     return 0u;
 }
-// MXFP4: an E2M1 code (s e1 e0 m) placed as fp16 bits s at 15 and e1 e0 m at
-// 11..9 is exactly its value times 2^-14 (e = 0 lands on the fp16
-// subnormals); the block scale 2^(E-127) then enters as 2^(E-113), one exact
-// multiply whenever the product is representable.  Element order as Q4_0.
+// Two E2M1 codes (the low 8 bits of `lo8`: low nibble, high nibble) as an
+// fp16 pair (low half, high half), exactly.
+__device__ __forceinline__ uint32_t e2m1x2_h2(uint32_t lo8)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+        : "=r"(r)
+        : "r"(lo8));
+    return r;
+}
+// MXFP4: byte j holds element j (low nibble) and j + 16 (high nibble), as
+// Q4_0.  Adjacent elements are paired into one byte (x | x >> 4 puts the
+// nibbles of bytes 2i and 2i+1 together in byte 2i), converted exactly, and
+// scaled by 2^(E-127): one exact multiply whenever the product is
+// representable; outside fp16's exponent range the scale goes in two steps
+// (2^15 then the rest, or 2^-12 then the rest), so the weight is rounded
+// once.
 __device__ __forceinline__ void mxfp4_pairs(uint32_t E, const uint32_t (&qs)[4], uint32_t *out)
 {
     uint32_t s1, s2 = 0u;
+    const int k = (int)E - 127;
     if (E == 255u) s1 = 0x7E00u;                       // NaN scale
-    else if (E <= 128u) s1 = pow2_h((int)E - 113);
-    else { s1 = 0x7400u; s2 = pow2_h((int)E - 127); }  // 2^14, then 2^(E-127)
+    else if (k >= -24 && k <= 15) s1 = pow2_h(k);
+    else if (k > 15) { s1 = 0x7800u; s2 = pow2_h(min(k - 15, 15)); }
+    else { s1 = 0x0C00u; s2 = k + 12 >= -24 ? pow2_h(k + 12) : 0u; }
     const uint32_t ss = s1 | (s1 << 16);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const uint32_t t01 = prmt(qs[j], 0u, 0x4140u), t23 = prmt(qs[j], 0u, 0x4342u);
-        out[2 * j] = hmul2(((t01 << 9) & 0x0E000E00u) | ((t01 << 12) & 0x80008000u), ss);
-        out[2 * j + 1] = hmul2(((t23 << 9) & 0x0E000E00u) | ((t23 << 12) & 0x80008000u), ss);
-        out[8 + 2 * j] = hmul2(((t01 << 5) & 0x0E000E00u) | ((t01 << 8) & 0x80008000u), ss);
-        out[9 + 2 * j] = hmul2(((t23 << 5) & 0x0E000E00u) | ((t23 << 8) & 0x80008000u), ss);
+        const uint32_t lo = qs[j] & 0x0F0F0F0Fu, hi = (qs[j] >> 4) & 0x0F0F0F0Fu;
+        const uint32_t pl = lo | (lo >> 4), ph = hi | (hi >> 4);
+        out[2 * j] = hmul2(e2m1x2_h2(pl), ss);
+        out[2 * j + 1] = hmul2(e2m1x2_h2(pl >> 16), ss);
+        out[8 + 2 * j] = hmul2(e2m1x2_h2(ph), ss);
+        out[9 + 2 * j] = hmul2(e2m1x2_h2(ph >> 16), ss);
     }
-    if (s2) {
+    if (E != 255u && (k < -24 || k > 15)) {
         const uint32_t s22 = s2 | (s2 << 16);
 #pragma unroll
         for (int m = 0; m < 16; ++m) out[m] = hmul2(out[m], s22);
