@@ -63,6 +63,17 @@ def load_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def load_tensor_peak():
+    """Measured dense bf16 TF/s (burst), else the fallback figure."""
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            return float(json.loads(p.read_text())["bf16_tflops"]), "measured"
+        except Exception:
+            pass
+    return 1900.0, "fallback"
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for name in ("rf_gemv.cu", "rf_device.cuh", "rf_internal.h"):
@@ -472,6 +483,68 @@ def run_multi_token(torch, rf, device, reps: int = 50):
                     "unit": "GB/s", "token_gbs": n_tok * nbytes / us / 1e3})
         del g
     return {"matrix": f"Q4_0 {rows}x{in_dim}", "copies": len(Ws), "bytes": nbytes, "rows": out}
+
+
+def run_prefill(torch, rf, device, tensor_peak: float, reps: int = 5):
+    """Chunks of tokens through one resident matrix per call (rf_gemm, the
+    tensor-core prefill dequant-GEMM): the 11008x4096 Q4_0 gate projection,
+    eight copies (203 MB, > L2) walked round-robin in one CUDA graph, for 8,
+    64, 512 and 2048 tokens.  Each call includes its activation pre-pass.
+    value = TF/s (2 * rows * in_dim * tokens per call); weight_gbs = weight
+    bytes per second; vs_gemv_multi = the same tokens through rf_gemv_multi
+    in launches of eight tokens, timed the same way, over this call."""
+    fmt, rows, in_dim = syn.Q4_0, syn.C2["d_ff"], syn.C2["d_model"]
+    Ws = [torch.from_numpy(syn.quant_matrix(fmt, rows, in_dim, 70 + c, threads=8)).to(device)
+          for c in range(8)]
+    nbytes = Ws[0].numel()
+    s = torch.cuda.Stream(device)
+    s.wait_stream(torch.cuda.current_stream())
+
+    def timed(walk, calls):
+        with torch.cuda.stream(s):
+            walk()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            walk()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                g.replay()
+            e0.record(s)
+            for _ in range(reps):
+                g.replay()
+            e1.record(s)
+        torch.cuda.synchronize()
+        del g
+        return e0.elapsed_time(e1) * 1e3 / (reps * calls)
+
+    out = []
+    for n_tok in (8, 64, 512, 2048):
+        X = torch.randn(n_tok, in_dim, generator=torch.Generator(device=device).manual_seed(n_tok),
+                        device=device)
+        Y = torch.empty(n_tok, rows, device=device)
+        ws = torch.empty(rf.gemm_workspace_bytes(fmt, in_dim, n_tok), dtype=torch.uint8,
+                         device=device)
+
+        def walk_gemm():
+            for W in Ws:
+                rf.gemm(fmt, W, 0, rows, in_dim, X, Y, workspace=ws, stream=s)
+
+        def walk_multi():
+            for W in Ws:
+                for c in range(0, n_tok, 8):
+                    rf.gemv_multi(fmt, W, 0, rows, in_dim, X[c:c + 8], Y[c:c + 8], stream=s)
+        us = timed(walk_gemm, len(Ws))
+        tf = 2.0 * rows * in_dim * n_tok / us / 1e6
+        row = {"tokens": n_tok, "us_per_call": us, "value": tf, "unit": "TF/s",
+               "frac_of_tensor_peak": tf / tensor_peak, "weight_gbs": nbytes / us / 1e3}
+        if n_tok <= 64:
+            row["vs_gemv_multi"] = timed(walk_multi, len(Ws)) / us
+        out.append(row)
+    return {"matrix": f"Q4_0 {rows}x{in_dim}", "copies": len(Ws), "bytes": nbytes,
+            "tensor_peak_tflops": tensor_peak, "peak_source": "measured bf16 burst (else the "
+            "fallback); fp16 operands run at the same nominal rate", "rows": out}
 
 
 def run_streamed_gemv(torch, rf, device, depth: int, merge: bool = True, reps: int = 50):
@@ -1027,6 +1100,7 @@ def main():
                 for dp, merge in ((4, True), (4, False), (1, False), (8, True), (8, False))]
             extra["moe_mxfp4"] = run_moe(torch, rf, device)
             extra["multi_token_q4_0"] = run_multi_token(torch, rf, device)
+            extra["prefill_q4_0"] = run_prefill(torch, rf, device, load_tensor_peak()[0])
             for name, fmt in (("dense_layer_q4_k", syn.Q4_K), ("dense_layer_q6_k", syn.Q6_K)):
                 r = run_dense_format(torch, rf, device, fmt)
                 r["frac_of_hbm_peak"] = r["value"] / peak
