@@ -281,6 +281,9 @@ def run_dense(args, torch, rf, device, rank, world, dist):
             while time.perf_counter() < t_end:
                 run_steps(max(args.steps, 8 * nL))
                 stream.synchronize()
+        # An NVTX range marks the timed repeats, so a profiler can select
+        # exactly the timed steps (ncu --nvtx --nvtx-include "rf_timed/").
+        torch.cuda.nvtx.range_push("rf_timed")
         for _ in range(REPEATS):
             torch.cuda.synchronize()
             if dist:
@@ -293,6 +296,7 @@ def run_dense(args, torch, rf, device, rank, world, dist):
             if dist:
                 dist.barrier()
             reps_ms.append(reduce_time_max(torch, dist, e0.elapsed_time(e1), device))
+        torch.cuda.nvtx.range_pop()
     ms = statistics.median(reps_ms)
     gbs = whole_job_gbs(wbytes, args.steps, world, ms)
     spread = {"repeats": REPEATS, "ms_per_step": [round(r / args.steps, 6) for r in reps_ms],

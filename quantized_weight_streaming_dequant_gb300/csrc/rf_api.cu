@@ -2,6 +2,8 @@
 // windows, elementwise activations and the two-phase dense SwiGLU FFN.
 #include <cuda_fp16.h>
 
+#include <algorithm>
+
 #include <cstring>
 
 #include "rf_device.cuh"
@@ -31,74 +33,80 @@ __device__ __forceinline__ float e8m0_value(uint32_t E)
     return E == 0u ? __uint_as_float(0x00400000u) : __uint_as_float(E << 23);
 }
 
+// Weight e of one block, exactly as the format defines it (one rounding to
+// fp32 where the value is not exact; the same operations as the oracle).
 template <int FMT>
-__global__ void dequant_kernel(const uint8_t *__restrict__ W, int64_t n_blocks,
-                               float *__restrict__ out)
+__device__ __forceinline__ float block_elem(const uint8_t *p, int e)
 {
-    const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (b >= n_blocks) return;
     if constexpr (FMT == RF_Q6_K) {
         // Weight e = 128n + 32k + l: q = low | high << 4 from ql byte
         // 64n + 32(k&1) + l (low nibble for k < 2, high for k >= 2) and the
         // bit pair 2k of qh byte 128 + 32n + l; w = d * scale[e/16] * (q-32).
         // d * scale is exact in fp32 (11 x 8 significant bits) and so is its
         // product with q - 32 (6 more), so the result is exact.
-        float *o = out + 256 * b;
-        const uint8_t *p = W + 210 * b;
         const float d = __half2float(__ushort_as_half((unsigned short)(p[208] | (p[209] << 8))));
-        for (int e = 0; e < 256; ++e) {
-            const int n = e >> 7, k = (e >> 5) & 3, l = e & 31;
-            const int lb = p[64 * n + 32 * (k & 1) + l];
-            const int low = k < 2 ? (lb & 15) : (lb >> 4);
-            const int high = (p[128 + 32 * n + l] >> (2 * k)) & 3;
-            o[e] = (d * (float)(int8_t)p[192 + (e >> 4)]) * (float)((low | (high << 4)) - 32);
-        }
-        return;
+        const int n = e >> 7, k = (e >> 5) & 3, l = e & 31;
+        const int lb = p[64 * n + 32 * (k & 1) + l];
+        const int low = k < 2 ? (lb & 15) : (lb >> 4);
+        const int high = (p[128 + 32 * n + l] >> (2 * k)) & 3;
+        return (d * (float)(int8_t)p[192 + (e >> 4)]) * (float)((low | (high << 4)) - 32);
     } else if constexpr (FMT == RF_Q4_K) {
         // d*sc and dmin*m are exact in fp32 (11-bit times 6-bit significands)
         // and so is d*sc*q, so one fused multiply-add rounds the exact value
         // once.
-        float *o = out + 256 * b;
-        const uint8_t *p = W + 144 * b;
         const float d = __half2float(__ushort_as_half((unsigned short)(p[0] | (p[1] << 8))));
         const float dmin = __half2float(__ushort_as_half((unsigned short)(p[2] | (p[3] << 8))));
         const uint8_t *sc = p + 4, *qs = p + 16;
-        for (int j = 0; j < 8; ++j) {
-            int s, m;
-            if (j < 4) {
-                s = sc[j] & 63;
-                m = sc[j + 4] & 63;
-            } else {
-                s = (sc[j + 4] & 15) | ((sc[j - 4] >> 6) << 4);
-                m = (sc[j + 4] >> 4) | ((sc[j] >> 6) << 4);
-            }
-            const float ds = d * (float)s, dm = dmin * (float)m;
-            const uint8_t *q = qs + 32 * (j >> 1);
-            for (int l = 0; l < 32; ++l) {
-                const int v = (j & 1) ? (q[l] >> 4) : (q[l] & 15);
-                o[32 * j + l] = fmaf(ds, (float)v, -dm);
-            }
+        const int j = e >> 5, l = e & 31;
+        int sv, m;
+        if (j < 4) {
+            sv = sc[j] & 63;
+            m = sc[j + 4] & 63;
+        } else {
+            sv = (sc[j + 4] & 15) | ((sc[j - 4] >> 6) << 4);
+            m = (sc[j + 4] >> 4) | ((sc[j] >> 6) << 4);
         }
-        return;
-    }
-    float *o = out + 32 * b;
-    if constexpr (FMT == RF_Q8_0) {
-        const uint8_t *p = W + 34 * b;
+        const uint8_t q = qs[32 * (j >> 1) + l];
+        const int v = (j & 1) ? (q >> 4) : (q & 15);
+        return fmaf(d * (float)sv, (float)v, -(dmin * (float)m));
+    } else if constexpr (FMT == RF_Q8_0) {
         const float d = __half2float(__ushort_as_half((unsigned short)(p[0] | (p[1] << 8))));
-        for (int j = 0; j < 32; ++j) o[j] = d * (float)(int8_t)p[2 + j];
+        return d * (float)(int8_t)p[2 + e];
     } else if constexpr (FMT == RF_Q4_0) {
-        const uint8_t *p = W + 18 * b;
         const float d = __half2float(__ushort_as_half((unsigned short)(p[0] | (p[1] << 8))));
-        for (int j = 0; j < 16; ++j) {
-            o[j] = d * (float)((int)(p[2 + j] & 15) - 8);
-            o[j + 16] = d * (float)((int)(p[2 + j] >> 4) - 8);
-        }
+        const int q = e < 16 ? (p[2 + e] & 15) : (p[2 + e - 16] >> 4);
+        return d * (float)(q - 8);
     } else {
-        const uint8_t *p = W + 17 * b;
-        const float s = e8m0_value(p[0]);
-        for (int j = 0; j < 16; ++j) {
-            o[j] = e2m1_value(p[1 + j] & 15u) * s;
-            o[j + 16] = e2m1_value(p[1 + j] >> 4) * s;
+        const uint32_t c = e < 16 ? (p[1 + e] & 15u) : (uint32_t)(p[1 + e - 16] >> 4);
+        return e2m1_value(c) * e8m0_value(p[0]);
+    }
+}
+
+// Thread t writes outputs 4t .. 4t+3 (always within one block: blocks hold a
+// multiple of 4 weights), so a warp's stores are 512 contiguous bytes.
+template <int FMT>
+__global__ void dequant_kernel(const uint8_t *__restrict__ W, int64_t n_blocks,
+                               float *__restrict__ out, bool vec)
+{
+    constexpr int BE = FMT == RF_Q4_K || FMT == RF_Q6_K ? 256 : 32;
+    constexpr int BB = FMT == RF_Q8_0 ? 34 : FMT == RF_Q4_0 ? 18 : FMT == RF_MXFP4 ? 17
+                                                            : FMT == RF_Q4_K ? 144 : 210;
+    const int64_t quads = n_blocks * (BE / 4);
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < quads;
+         t += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t b = t / (BE / 4);
+        const int e0 = (int)(t % (BE / 4)) * 4;
+        const uint8_t *p = W + BB * b;
+        const float v0 = block_elem<FMT>(p, e0), v1 = block_elem<FMT>(p, e0 + 1);
+        const float v2 = block_elem<FMT>(p, e0 + 2), v3 = block_elem<FMT>(p, e0 + 3);
+        float *o = out + 4 * t;
+        if (vec) {
+            *reinterpret_cast<float4 *>(o) = make_float4(v0, v1, v2, v3);
+        } else {
+            o[0] = v0;
+            o[1] = v1;
+            o[2] = v2;
+            o[3] = v3;
         }
     }
 }
@@ -171,17 +179,19 @@ rf_status rf_dequantize(int fmt, const void *W, int64_t n_blocks, float *out, vo
     if (!fmt_ok(fmt)) return RF_ERR_UNSUPPORTED_FMT;
     if (n_blocks < 0 || (n_blocks > 0 && (!W || !out))) return RF_ERR_INVALID_ARG;
     if (n_blocks == 0) return RF_OK;
-    const int threads = 128;
-    const int64_t grid = (n_blocks + threads - 1) / threads;
-    if (grid > 0x7fffffff) return RF_ERR_TOO_LARGE;
+    const int threads = 256;
+    const int64_t quads = n_blocks * (block_elems_of(fmt) / 4);
+    if (quads / (block_elems_of(fmt) / 4) != n_blocks) return RF_ERR_TOO_LARGE;
+    const int grid = (int)std::min<int64_t>((quads + threads - 1) / threads, (int64_t)num_sms() * 8);
+    const bool vec = (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const uint8_t *w = static_cast<const uint8_t *>(W);
     switch (fmt) {
-    case RF_Q4_0: dequant_kernel<RF_Q4_0><<<(unsigned)grid, threads, 0, s>>>(w, n_blocks, out); break;
-    case RF_Q8_0: dequant_kernel<RF_Q8_0><<<(unsigned)grid, threads, 0, s>>>(w, n_blocks, out); break;
-    case RF_Q4_K: dequant_kernel<RF_Q4_K><<<(unsigned)grid, threads, 0, s>>>(w, n_blocks, out); break;
-    case RF_Q6_K: dequant_kernel<RF_Q6_K><<<(unsigned)grid, threads, 0, s>>>(w, n_blocks, out); break;
-    default: dequant_kernel<RF_MXFP4><<<(unsigned)grid, threads, 0, s>>>(w, n_blocks, out); break;
+    case RF_Q4_0: dequant_kernel<RF_Q4_0><<<grid, threads, 0, s>>>(w, n_blocks, out, vec); break;
+    case RF_Q8_0: dequant_kernel<RF_Q8_0><<<grid, threads, 0, s>>>(w, n_blocks, out, vec); break;
+    case RF_Q4_K: dequant_kernel<RF_Q4_K><<<grid, threads, 0, s>>>(w, n_blocks, out, vec); break;
+    case RF_Q6_K: dequant_kernel<RF_Q6_K><<<grid, threads, 0, s>>>(w, n_blocks, out, vec); break;
+    default: dequant_kernel<RF_MXFP4><<<grid, threads, 0, s>>>(w, n_blocks, out, vec); break;
     }
     return last_cuda_error();
 }

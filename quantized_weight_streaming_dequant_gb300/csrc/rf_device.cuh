@@ -74,21 +74,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 
 // Wait for phase `parity` of `bar` to complete.  Returns false (and records
 // RF_ERR_TIMEOUT in *status) if it does not complete within limit_ns, and
-// returns false at once when *status already holds a failure: after one wait
-// has given up, every later wait of every CTA ends immediately instead of
-// spending its own limit, so a broken pipeline ends the launch after one
-// limit.  A false return means the data did not arrive: the caller issues no
-// further copies, drains the ones it issued and leaves its loops.
+// returns false once the wait has lasted 20 us while *status holds a
+// failure: after one wait has given up, every later wait of every CTA ends
+// soon instead of spending its own limit, so a broken pipeline ends the
+// launch after one limit.  The clock starts at the 256th poll, so a wait
+// that completes quickly reads neither the timer nor the status word.  A
+// false return means the data did not arrive: the caller issues no further
+// copies, drains the ones it issued and leaves its loops.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int *status,
                                                   unsigned long long limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = globaltimer_ns();
+    unsigned long long t0 = 0;
     for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 255u) == 255u) {
-            if (*reinterpret_cast<volatile int *>(status) != 0) return false;
-            if (globaltimer_ns() - t0 > limit_ns) {
+            const unsigned long long now = globaltimer_ns();
+            if (t0 == 0) {
+                t0 = now;
+                continue;
+            }
+            const unsigned long long dt = now - t0;
+            if (dt > 20000ull && *reinterpret_cast<volatile int *>(status) != 0) return false;
+            if (dt > limit_ns) {
                 record_status(status, RF_ERR_TIMEOUT);
                 return false;
             }
