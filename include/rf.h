@@ -243,13 +243,14 @@ RF_API rf_status rf_gemv_multi(int fmt, const void *W, int64_t row_start, int64_
  * weights for the whole chunk of tokens):
  *     Y[t][r - row_start] = sum_i W[r,i] * X[t][i],  r in [row_start, row_end),
  *                                                    t < n_tok.
- * Formats: RF_Q4_0, RF_Q8_0, RF_MXFP4 (others: RF_ERR_UNSUPPORTED_FMT; for
- * one to eight tokens rf_gemv_multi serves every format).
- * Rows whose byte length is a multiple of 16 (in_dim a multiple of 256 for
- * Q4_0/Q8_0, of 512 for MXFP4) take the main path: X is first rounded to
- * fp16 into `workspace`, each weight is decoded to fp16 as d * q with one
- * rounding (MXFP4 values are exact), and tcgen05.mma accumulates the whole
- * row in fp32.  Other rows take the general path, which keeps the weights
+ * Formats: RF_Q4_0, RF_Q8_0, RF_MXFP4, RF_Q4_K (others:
+ * RF_ERR_UNSUPPORTED_FMT; for one to eight tokens rf_gemv_multi serves every
+ * format).  Rows whose byte length is a multiple of 16 (in_dim a multiple
+ * of 256 for Q4_0/Q8_0, of 512 for MXFP4, any Q4_K width) take the main
+ * path: X is first rounded to fp16 into `workspace`, each weight is decoded
+ * to fp16 as d * q with one rounding (MXFP4 values are exact; Q4_K's
+ * d*sc*q - dmin*m is rounded to fp32, then to fp16), and tcgen05.mma
+ * accumulates the whole row in fp32.  Other rows take the general path, which keeps the weights
  * exact (fp16 quant values, the block scale applied in fp32 per block) and
  * rounds only X; it needs no workspace.  |X| and |w| must stay below 65504.
  * W: device, row 0 of the [out][in] matrix, 16-byte aligned; X: n_tok rows
@@ -258,8 +259,9 @@ RF_API rf_status rf_gemv_multi(int fmt, const void *W, int64_t row_start, int64_
  * rf_gemm_workspace_bytes(fmt, in_dim, n_tok) bytes (NULL when that is 0),
  * owned by the caller and overwritten; it must not be used by another call
  * that is in flight.  All device.  Errors: RF_ERR_INVALID_ARG (null
- * pointer, in_dim not a positive multiple of 32, bad window, n_tok < 0,
- * ldx < in_dim, ldy < rows, workspace missing or too small);
+ * pointer, in_dim not a positive multiple of the format's block (32, or
+ * 256 for Q4_K), bad window, n_tok < 0, ldx < in_dim, ldy < rows,
+ * workspace missing or too small);
  * RF_ERR_MISALIGNED (W or workspace not 16-byte aligned); RF_ERR_TOO_LARGE
  * (more than 4,194,240 tokens or 8,388,480 rows).  Empty work is a no-op.
  * A bounded internal wait that gives up is reported by rf_device_status as

@@ -404,13 +404,15 @@ constexpr int kTThreads = 384;           // 12 warps
 constexpr int kATileT = kGM * kTK * 2;   // fp16 weight tile of one slice (16 KB)
 constexpr int kDecWarp0 = 4;             // warps 4-11 decode, then read out
 
-// Raw chunk of each format: BPC blocks of each of the 128 rows per tensor
-// copy (BPC * BS is a multiple of 16, so every chunk starts on a 16-byte
-// boundary of a 16-byte aligned row), R chunks in flight.
+// Raw chunk of each format: BPC blocks (of BE weights, BS bytes) of each of
+// the 128 rows per tensor copy (BPC * BS is a multiple of 16, so every chunk
+// starts on a 16-byte boundary of a 16-byte aligned row), R chunks in
+// flight; a chunk holds QPC 64-input slices.
 template <int FMT> struct RawCfg;
-template <> struct RawCfg<RF_Q4_0> { static constexpr int BS = 18, BPC = 8, R = 3; };
-template <> struct RawCfg<RF_Q8_0> { static constexpr int BS = 34, BPC = 8, R = 2; };
-template <> struct RawCfg<RF_MXFP4> { static constexpr int BS = 17, BPC = 16, R = 2; };
+template <> struct RawCfg<RF_Q4_0> { static constexpr int BS = 18, BE = 32, BPC = 8, R = 3; };
+template <> struct RawCfg<RF_Q8_0> { static constexpr int BS = 34, BE = 32, BPC = 8, R = 2; };
+template <> struct RawCfg<RF_MXFP4> { static constexpr int BS = 17, BE = 32, BPC = 16, R = 2; };
+template <> struct RawCfg<RF_Q4_K> { static constexpr int BS = 144, BE = 256, BPC = 1, R = 3; };
 
 // Slots of the operand ring (a decoded-weight tile and an activation tile
 // each) for a token tile of N.  The two decoder groups take alternate
@@ -436,6 +438,10 @@ struct TcParams {
     unsigned long long limit;
 };
 
+__device__ __forceinline__ uint32_t h2_bits(__half2 h)
+{
+    return (uint32_t)__half_as_ushort(__low2half(h)) | ((uint32_t)__half_as_ushort(__high2half(h)) << 16);
+}
 __device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b)
 {
     uint32_t r;
@@ -565,10 +571,66 @@ __device__ __forceinline__ void mxfp4_pairs(uint32_t E, const uint32_t (&qs)[4],
     }
 }
 
-// Slice Q of a raw chunk (blocks 2Q and 2Q+1 of one row) as 32 fp16 pairs.
+// Q4_K slice Q of a 256-weight super-block (16-byte aligned in its slot):
+// sub-blocks 2Q (low nibbles of quant bytes 32Q..32Q+31) and 2Q+1 (their high
+// nibbles).  Scale and min of sub-block j are 6-bit fields of the 12 scale
+// bytes: j < 4 the low 6 bits of bytes j and j+4; j >= 4 a nibble of byte j+4
+// with the top two bits of bytes j-4 and j.  Each weight is d*sc*q - dmin*m
+// by one fused multiply-add in fp32 (d*sc, dmin*m and d*sc*q are exact),
+// then rounded to fp16.
+template <int Q>
+__device__ __forceinline__ void q4k_slice(const uint8_t *slot, uint32_t (&out)[32])
+{
+    const uint4 h = *reinterpret_cast<const uint4 *>(slot);
+    const uint4 qa = *reinterpret_cast<const uint4 *>(slot + 16 + 32 * Q);
+    const uint4 qb = *reinterpret_cast<const uint4 *>(slot + 32 + 32 * Q);
+    const float d = __half2float(__ushort_as_half((unsigned short)(h.x & 0xFFFFu)));
+    const float dmin = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
+    const uint32_t sw[3] = {h.y, h.z, h.w};   // the 12 scale bytes
+    auto sb = [&](int i) -> uint32_t { return (sw[i >> 2] >> (8 * (i & 3))) & 0xFFu; };
+    float ds[2], dm[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        constexpr int j0 = 2 * Q;
+        const int j = j0 + t;
+        uint32_t sc, m;
+        if (j < 4) {
+            sc = sb(j) & 63u;
+            m = sb(j + 4) & 63u;
+        } else {
+            sc = (sb(j + 4) & 15u) | ((sb(j - 4) >> 6) << 4);
+            m = (sb(j + 4) >> 4) | ((sb(j) >> 6) << 4);
+        }
+        ds[t] = d * (float)sc;
+        dm[t] = dmin * (float)m;
+    }
+    const uint32_t qw[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+    // 0x4B000000 | n is the fp32 value 2^23 + n, so subtracting 2^23 gives n.
+    auto w = [](uint32_t nib, float s, float mm) {
+        return fmaf(s, __uint_as_float(0x4B000000u | nib) - 8388608.f, -mm);
+    };
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t v = qw[k];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const uint32_t b0 = (v >> (16 * e)) & 0xFFu, b1 = (v >> (16 * e + 8)) & 0xFFu;
+            out[2 * k + e] = h2_bits(__floats2half2_rn(w(b0 & 15u, ds[0], dm[0]), w(b1 & 15u, ds[0], dm[0])));
+            out[16 + 2 * k + e] =
+                h2_bits(__floats2half2_rn(w(b0 >> 4, ds[1], dm[1]), w(b1 >> 4, ds[1], dm[1])));
+        }
+    }
+}
+
+// Slice Q of a raw chunk (blocks 2Q and 2Q+1 of one row, or a quarter of a
+// Q4_K super-block) as 32 fp16 pairs.
 template <int FMT, int Q>
 __device__ __forceinline__ void decode_slice(const uint8_t *slot, uint32_t (&out)[32])
 {
+    if constexpr (FMT == RF_Q4_K) {
+        q4k_slice<Q>(slot, out);
+        return;
+    } else {
     using RC = RawCfg<FMT>;
     RawWin<Q * 2 * RC::BS, 2 * RC::BS> win;
     win.load(slot);
@@ -598,6 +660,7 @@ __device__ __forceinline__ void decode_slice(const uint8_t *slot, uint32_t (&out
         mxfp4_pairs(win.template byte<0>(), q0, out);
         mxfp4_pairs(win.template byte<17>(), q1, out + 16);
     }
+    }
 }
 
 // Compile-time loop over the slices of a chunk: f(integral_constant<Q>) for
@@ -619,7 +682,8 @@ template <int FMT, int N>
 __global__ void __launch_bounds__(kTThreads, 1) gemm_tc_kernel(const __grid_constant__ TcParams p)
 {
     using RC = RawCfg<FMT>;
-    constexpr int S = tc_stages<N>(), R = RC::R, CB = RC::BPC * RC::BS, QPC = RC::BPC / 2;
+    constexpr int S = tc_stages<N>(), R = RC::R, CB = RC::BPC * RC::BS;
+    constexpr int QPC = RC::BPC * RC::BE / kTK;
     constexpr int BT = N * kTK * 2;   // fp16 activation tile of one slice
     extern __shared__ __align__(1024) uint8_t smem[];
     uint8_t *a_t = smem;                 // [S][16 KB]
@@ -835,10 +899,16 @@ __global__ void __launch_bounds__(256) x16_kernel(const float *X, int64_t ldx, i
 // Token tile of the main path for a chunk of n_tok tokens.
 int tc_n(int n_tok) { return n_tok <= 64 ? 64 : (n_tok <= 128 ? 128 : 256); }
 
-// The main path takes rows whose byte length is a multiple of 16.
+// The main path takes rows whose byte length is a multiple of 16 (always
+// true for Q4_K's 144-byte super-blocks).
 bool tc_rows_ok(int fmt, int64_t in_dim)
 {
-    return ((in_dim / 32) * (int64_t)block_bytes_of(fmt)) % 16 == 0;
+    return ((in_dim / block_elems_of(fmt)) * (int64_t)block_bytes_of(fmt)) % 16 == 0;
+}
+
+bool gemm_fmt_ok(int fmt)
+{
+    return fmt == RF_Q4_0 || fmt == RF_Q8_0 || fmt == RF_MXFP4 || fmt == RF_Q4_K;
 }
 
 size_t tc_workspace(int64_t in_dim, int n_tok)
@@ -908,8 +978,8 @@ extern "C" {
 
 size_t rf_gemm_workspace_bytes(int fmt, int64_t in_dim, int n_tok)
 {
-    if ((fmt != RF_Q4_0 && fmt != RF_Q8_0 && fmt != RF_MXFP4) || in_dim <= 0 || in_dim % 32 != 0 ||
-        n_tok <= 0 || !tc_rows_ok(fmt, in_dim))
+    if (!gemm_fmt_ok(fmt) || in_dim <= 0 || in_dim % block_elems_of(fmt) != 0 || n_tok <= 0 ||
+        !tc_rows_ok(fmt, in_dim))
         return 0;
     return tc_workspace(in_dim, n_tok);
 }
@@ -918,8 +988,8 @@ rf_status rf_gemm(int fmt, const void *W, int64_t row_start, int64_t row_end, in
                   int n_tok, const float *X, int64_t ldx, float *Y, int64_t ldy, void *workspace,
                   size_t workspace_bytes, void *stream)
 {
-    if (fmt != RF_Q4_0 && fmt != RF_Q8_0 && fmt != RF_MXFP4) return RF_ERR_UNSUPPORTED_FMT;
-    if (!W || !X || !Y || in_dim <= 0 || in_dim % 32 != 0 || row_start < 0 ||
+    if (!gemm_fmt_ok(fmt)) return RF_ERR_UNSUPPORTED_FMT;
+    if (!W || !X || !Y || in_dim <= 0 || in_dim % block_elems_of(fmt) != 0 || row_start < 0 ||
         row_end < row_start || n_tok < 0 || ldx < in_dim || ldy < row_end - row_start)
         return RF_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(W) & 15u) != 0) return RF_ERR_MISALIGNED;
@@ -934,11 +1004,11 @@ rf_status rf_gemm(int fmt, const void *W, int64_t row_start, int64_t row_end, in
     }
     if (row_end == row_start || n_tok == 0) return RF_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int64_t rb = (in_dim / 32) * (int64_t)block_bytes_of(fmt);
+    const int64_t rb = (in_dim / block_elems_of(fmt)) * (int64_t)block_bytes_of(fmt);
     if (tc) {
         TcParams p;
         std::memset(&p, 0, sizeof(p));
-        const int cb = fmt == RF_Q4_0 ? 144 : 272;   // chunk bytes of the format
+        const int cb = fmt == RF_Q4_0 || fmt == RF_Q4_K ? 144 : 272;   // chunk bytes
         if (!encode_u16_map(&p.wmap, static_cast<const uint8_t *>(W) + row_start * rb,
                             (uint64_t)(rb / 2), (uint64_t)(row_end - row_start), (uint64_t)rb,
                             (uint32_t)(cb / 2), (uint32_t)kGM))
@@ -957,9 +1027,11 @@ rf_status rf_gemm(int fmt, const void *W, int64_t row_start, int64_t row_end, in
         switch (fmt) {
         case RF_Q4_0: return launch_tc<RF_Q4_0>(p, X, ldx, in_dim, Xp, grid, s);
         case RF_Q8_0: return launch_tc<RF_Q8_0>(p, X, ldx, in_dim, Xp, grid, s);
+        case RF_Q4_K: return launch_tc<RF_Q4_K>(p, X, ldx, in_dim, Xp, grid, s);
         default: return launch_tc<RF_MXFP4>(p, X, ldx, in_dim, Xp, grid, s);
         }
     }
+    if (fmt == RF_Q4_K) return RF_ERR_UNSUPPORTED_FMT;   // its rows are always aligned
     ExactParams p;
     p.W = static_cast<const uint8_t *>(W);
     p.X = X;

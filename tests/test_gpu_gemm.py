@@ -12,8 +12,9 @@ rounds only x, so the same bound covers it):
     times the sum of |products| (allowing truncating adds).
   So |y - y_ref| <= (2^-10 + 2^-22 + in_dim * 2^-23) * S
                     + 2^-25 * 1.001 * (sum|w| + sum|x|),
-  with S = sum_i |w_i| |x_i|.  The path's parity bar, 1e-3 * ||W_r|| * ||x||,
-  is checked as well.
+  with S = sum_i |w_i| |x_i|.  Q4_K weights take one fp32 rounding (the
+  fused d*sc*q - dmin*m) before the fp16 one, which adds 2^-23 * S.  The
+  path's parity bar, 1e-3 * ||W_r|| * ||x||, is checked as well.
 """
 import numpy as np
 import pytest
@@ -45,7 +46,8 @@ def derived_bound(fmt, W, r0, r1, in_dim, X):
     Wa = np.abs(Wd)
     S = Xa @ Wa.T
     lin = 2.0 ** -25 * 1.001 * (Wa.sum(axis=1)[None, :] + Xa.sum(axis=1)[:, None])
-    return (2.0 ** -10 + 2.0 ** -22 + in_dim * 2.0 ** -23) * S + lin
+    extra = 2.0 ** -23 if fmt == syn.Q4_K else 0.0
+    return (2.0 ** -10 + 2.0 ** -22 + extra + in_dim * 2.0 ** -23) * S + lin
 
 
 def check_gemm(fmt, W, r0, r1, in_dim, X, Y):
@@ -81,6 +83,9 @@ CASES = [  # fmt, rows, in_dim, window, n_tok
     (syn.MXFP4, 200, 2880, (0, 200), 40),    # 1,530-byte rows: general path
     (syn.Q4_0, 96, 4064, (0, 96), 9),        # 2,286-byte rows: general path
     (syn.Q8_0, 130, 2080, (2, 130), 66),     # 2,210-byte rows: general path
+    (syn.Q4_K, 128, 256, (0, 128), 64),      # one super-block per row
+    (syn.Q4_K, 300, 4096, (5, 300), 70),
+    (syn.Q4_K, 257, 2048, (1, 257), 300),    # two 256-token tiles, ragged
 ]
 
 
@@ -148,8 +153,8 @@ def test_gemm_refusals_and_empty_work(rf):
     fmt, rows, in_dim = syn.Q4_0, 64, 256
     W = dev_tensor(syn.quant_matrix(fmt, rows, in_dim, 2))
     X = torch.zeros(4, in_dim, device="cuda")
-    with pytest.raises(rf.RFError) as e:                       # K-quant: not served
-        rf.gemm(syn.Q4_K, W, 0, rows, in_dim, X)
+    with pytest.raises(rf.RFError) as e:                       # Q6_K: not served
+        rf.gemm(syn.Q6_K, W, 0, rows, in_dim, X)
     assert e.value.code == 2   # RF_ERR_UNSUPPORTED_FMT
     with pytest.raises(rf.RFError) as e:                       # workspace too small
         rf.gemm(fmt, W, 0, rows, in_dim, X, workspace=torch.empty(16, dtype=torch.uint8,
