@@ -580,11 +580,13 @@ RF_API rf_status rf_device_status(void);
 
 /* Test hook for the kernels' bounded waits (the pages have no counterpart; it
  * lets the failure path be exercised without faulting a GPU).  Arms a
- * one-shot fault for the next GEMV launch on this process that copies its
- * weights with tensor copies (16-byte aligned rows in device memory): in that
- * launch the copy of one stage of CTA 0 is never issued, so the warp waiting
- * for it gives up after limit_us microseconds, records RF_ERR_TIMEOUT, and
- * the launch ends with nothing in flight (its outputs are undefined).
+ * one-shot fault for the next launch on this process that copies with
+ * tensor copies: a GEMV over 16-byte aligned rows in device memory, or an
+ * rf_gemm on its main path.  In that launch one copy of its first CTA is
+ * never issued (a stage of the GEMV's weights; the GEMM's second activation
+ * tile), so the warps waiting for it give up after limit_us microseconds,
+ * record RF_ERR_TIMEOUT, and the launch ends with nothing in flight (its
+ * outputs are undefined).
  * limit_us = 0 disarms.  Errors: RF_ERR_INVALID_ARG for limit_us above
  * 2,000,000. */
 RF_API rf_status rf_debug_arm_wait_fault(uint32_t limit_us);

@@ -435,6 +435,7 @@ struct TcParams {
     float *Y;
     int64_t ldy;
     int32_t rows, n_tok, nst, nch;   // nst: 64-input slices; nch: raw chunks
+    int32_t withhold;                // test hook: CTA (0, 0) never copies this slice's activations
     unsigned long long limit;
 };
 
@@ -751,15 +752,19 @@ __global__ void __launch_bounds__(kTThreads, 1) gemm_tc_kernel(const __grid_cons
         // Activation tiles: one 1-D bulk copy per slice.
         if (lane == 0) {
             const uint8_t *xs = p.Xp + (size_t)tt * p.nst * BT;
-            int issued = 0;
+            const int skip = (tt == 0 && rt == 0) ? p.withhold : -1;
+            int next = 0;   // slices [0, next) have been issued (but `skip`)
             for (int b = 0; b < p.nst; ++b) {
                 const int s = b % S;
                 if (!wait(&empty[s], ((b / S) & 1) ^ 1)) break;
+                next = b + 1;
+                if (b == skip) continue;
                 mbar_arrive_expect_tx(&bfull[s], (uint32_t)BT);
                 bulk_g2s(b_t + (size_t)s * BT, xs + (size_t)b * BT, (uint32_t)BT, &bfull[s]);
-                ++issued;
             }
-            for (int b = max(0, issued - S); b < issued; ++b) mbar_drain(&bfull[b % S], (b / S) & 1);
+            // Every copy issued lands before the CTA can exit.
+            for (int b = max(0, next - S); b < next; ++b)
+                if (b != skip) mbar_drain(&bfull[b % S], (b / S) & 1);
         }
         __syncwarp();
     } else if (warp == 2) {
@@ -1021,6 +1026,11 @@ rf_status rf_gemm(int fmt, const void *W, int64_t row_start, int64_t row_end, in
         p.nst = (int32_t)((in_dim + kTK - 1) / kTK);
         p.nch = (int32_t)((rb + cb - 1) / cb);
         p.limit = 2000000000ull;
+        p.withhold = -1;
+        if (const unsigned long long lim = take_wait_fault()) {
+            p.limit = lim;
+            p.withhold = p.nst > 1 ? 1 : 0;
+        }
         const int N = tc_n(n_tok);
         const dim3 grid((unsigned)((n_tok + N - 1) / N), (unsigned)((row_end - row_start + kGM - 1) / kGM));
         uint8_t *Xp = static_cast<uint8_t *>(workspace);

@@ -1674,6 +1674,8 @@ bool encode_u16_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t ro
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+unsigned long long take_wait_fault() { return g_fault_limit_ns.exchange(0); }
+
 rf_status arm_wait_fault(uint32_t limit_us)
 {
     if (limit_us > 2000000u) return RF_ERR_INVALID_ARG;

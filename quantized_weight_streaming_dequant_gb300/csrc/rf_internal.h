@@ -107,6 +107,9 @@ rf_status read_and_clear_gemm_status();
 // Arms the one-shot wait fault of the next producer-mode launch
 // (rf_debug_arm_wait_fault).
 rf_status arm_wait_fault(uint32_t limit_us);
+// The armed wait limit in ns (0 if none), disarming it: the next launch
+// that takes it withholds one copy.
+unsigned long long take_wait_fault();
 int num_sms();
 int64_t max_in_dim(int fmt, int n_x);
 // RF_OK, RF_ERR_TOO_LARGE (in_dim above max_in_dim) or RF_ERR_CUDA (no device).

@@ -3,6 +3,7 @@ worth knowing about": a stalled prefetcher must neither deadlock nor
 poison the arena).
 
 * A kernel's bounded wait: a test hook makes the producer of one launch
+  (the GEMV's producer warp, or the prefill GEMM's activation copier)
   withhold one stage's copy, with the wait limit cut to 1 ms.  The launch
   must end quickly with RF_ERR_TIMEOUT in the device status word and nothing
   in flight, and the next call on the device must be correct.
@@ -68,6 +69,39 @@ def test_kernel_wait_timeout_ends_launch_and_device_recovers(rf, rows):
         y = rf.gemv(fmt, W, 0, rows, in_dim, x)
         torch.cuda.synchronize()
         assert np.array_equal(bits(y), bits(y_ok))
+    assert rf.device_status() == rf.OK
+
+
+def test_gemm_wait_timeout_ends_launch_and_device_recovers(rf):
+    """The prefill GEMM under the same hook: CTA (0, 0) never copies slice 1's
+    activation tile, its decoders give up after 1 ms, every role stops,
+    drains what it issued and frees its tensor memory; the next calls are
+    bit-identical to the call before the fault."""
+    import torch
+    fmt, rows, in_dim, n_tok = syn.Q4_0, 384, 1024, 70
+    W_np = syn.quant_matrix(fmt, rows, in_dim, seed=310)
+    X_np = np.stack([syn.normal_f32(in_dim, 320 + t) for t in range(n_tok)])
+    W, X = dev_tensor(W_np), dev_tensor(X_np)
+    Y_ok = rf.gemm(fmt, W, 0, rows, in_dim, X)
+    assert rf.device_status() == rf.OK
+    for t in (0, n_tok - 1):
+        ref = oracle.gemv(fmt, W_np, 0, rows, in_dim, X_np[t])
+        assert_gemv_close(Y_ok[t].cpu().numpy(), ref,
+                          gemv_tol(fmt, W_np, 0, rows, in_dim, X_np[t]), f"token {t}")
+
+    rf.debug_arm_wait_fault(1000)
+    t0 = time.perf_counter()
+    rf.gemm(fmt, W, 0, rows, in_dim, X)
+    status = rf.device_status()
+    dt = time.perf_counter() - t0
+    assert status == TIMEOUT
+    assert dt < 1.0, f"the failed launch took {dt:.3f} s: waits did not end early"
+    assert rf.device_status() == rf.OK
+
+    for _ in range(3):
+        Y = rf.gemm(fmt, W, 0, rows, in_dim, X)
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(Y), bits(Y_ok))
     assert rf.device_status() == rf.OK
 
 
