@@ -489,15 +489,16 @@ def run_multi_token(torch, rf, device, reps: int = 50):
     return {"matrix": f"Q4_0 {rows}x{in_dim}", "copies": len(Ws), "bytes": nbytes, "rows": out}
 
 
-def run_prefill(torch, rf, device, tensor_peak: float, reps: int = 5):
+def run_prefill(torch, rf, device, tensor_peak: float, reps: int = 5, fmt: int = syn.Q4_0,
+                tokens=(8, 64, 512, 2048)):
     """Chunks of tokens through one resident matrix per call (rf_gemm, the
-    tensor-core prefill dequant-GEMM): the 11008x4096 Q4_0 gate projection,
-    eight copies (203 MB, > L2) walked round-robin in one CUDA graph, for 8,
-    64, 512 and 2048 tokens.  Each call includes its activation pre-pass.
+    tensor-core prefill dequant-GEMM): the 11008x4096 gate projection in
+    `fmt`, eight copies (> L2) walked round-robin in one CUDA graph, for each
+    chunk size in `tokens`.  Each call includes its activation pre-pass.
     value = TF/s (2 * rows * in_dim * tokens per call); weight_gbs = weight
     bytes per second; vs_gemv_multi = the same tokens through rf_gemv_multi
     in launches of eight tokens, timed the same way, over this call."""
-    fmt, rows, in_dim = syn.Q4_0, syn.C2["d_ff"], syn.C2["d_model"]
+    rows, in_dim = syn.C2["d_ff"], syn.C2["d_model"]
     Ws = [torch.from_numpy(syn.quant_matrix(fmt, rows, in_dim, 70 + c, threads=8)).to(device)
           for c in range(8)]
     nbytes = Ws[0].numel()
@@ -524,7 +525,7 @@ def run_prefill(torch, rf, device, tensor_peak: float, reps: int = 5):
         return e0.elapsed_time(e1) * 1e3 / (reps * calls)
 
     out = []
-    for n_tok in (8, 64, 512, 2048):
+    for n_tok in tokens:
         X = torch.randn(n_tok, in_dim, generator=torch.Generator(device=device).manual_seed(n_tok),
                         device=device)
         Y = torch.empty(n_tok, rows, device=device)
@@ -546,7 +547,8 @@ def run_prefill(torch, rf, device, tensor_peak: float, reps: int = 5):
         if n_tok <= 64:
             row["vs_gemv_multi"] = timed(walk_multi, len(Ws)) / us
         out.append(row)
-    return {"matrix": f"Q4_0 {rows}x{in_dim}", "copies": len(Ws), "bytes": nbytes,
+    name = next(k for k, v in rf.FORMATS.items() if v == fmt)
+    return {"matrix": f"{name} {rows}x{in_dim}", "copies": len(Ws), "bytes": nbytes,
             "tensor_peak_tflops": tensor_peak, "peak_source": "measured bf16 burst (else the "
             "fallback); fp16 operands run at the same nominal rate", "rows": out}
 
@@ -1105,6 +1107,8 @@ def main():
             extra["moe_mxfp4"] = run_moe(torch, rf, device)
             extra["multi_token_q4_0"] = run_multi_token(torch, rf, device)
             extra["prefill_q4_0"] = run_prefill(torch, rf, device, load_tensor_peak()[0])
+            extra["prefill_q4_k"] = run_prefill(torch, rf, device, load_tensor_peak()[0],
+                                                fmt=syn.Q4_K, tokens=(64, 512, 2048))
             for name, fmt in (("dense_layer_q4_k", syn.Q4_K), ("dense_layer_q6_k", syn.Q6_K)):
                 r = run_dense_format(torch, rf, device, fmt)
                 r["frac_of_hbm_peak"] = r["value"] / peak
