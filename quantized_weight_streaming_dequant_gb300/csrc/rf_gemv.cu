@@ -152,6 +152,7 @@ struct KParamsT {
     int32_t chained;             // launched behind a previous grid (dependency wait)
     unsigned long long wait_limit_ns;   // limit of every bounded wait
     int32_t fault_withhold;      // test hook: CTA 0's producer withholds warp 0's first copy
+    int32_t row_bulk;            // per-lane mode over device memory: one bulk copy per row
 };
 using KParamsSmall = KParamsT<4, 4>;
 using KParamsLarge = KParamsT<kMaxJobs, kMaxMaps>;
@@ -844,7 +845,7 @@ __global__ void __launch_bounds__(threads_of<FMT, MODE>(), min_ctas<FMT, MODE>()
             mbar_init(&ebars[warp * ST + lane], 1);
         }
     } else {
-        if (lane < ST) mbar_init(&bars[warp * ST + lane], 32);
+        if (lane < ST) mbar_init(&bars[warp * ST + lane], p.row_bulk ? 1 : 32);
     }
     if (threadIdx.x < kCntInts) cnt[threadIdx.x] = 0;
     if constexpr (WS) {
@@ -888,15 +889,28 @@ __global__ void __launch_bounds__(threads_of<FMT, MODE>(), min_ctas<FMT, MODE>()
     Cursor ic{g_lo, 0, 0, 0, g_lo < g_hi && cur_chunks > 0};
     if (ic.valid) cursor_fix_job(jobs, n_jobs, ic);
     int is = 0;   // stage of the next copy
+    uint32_t iph = 0;                  // its phase parity
+    uint32_t armed = 0, armed_ph = 0;  // row-bulk copies not yet seen landed, and their parity
 
     // Per-lane mode: row r's chunk, rounded out to 16-byte boundaries, goes
-    // to row r's slot; the warp copies one row at a time, lane i taking its
-    // i-th 16 bytes, so each copy instruction reads contiguous bytes (which
-    // matters most over the host link).
+    // to row r's slot.  Device memory: lane r issues one 1-D bulk copy of its
+    // row's chunk (the copy engine takes 32 requests per chunk; 16-byte
+    // cp.async of every piece made the warp wait on hundreds of outstanding
+    // requests per chunk), lane 0 arming the stage with the chunk's total
+    // bytes.  Mapped host memory: the warp copies one row at a time, lane i
+    // taking its i-th 16 bytes, so each copy instruction reads contiguous
+    // bytes of the link.
     auto issue = [&](const Cursor &cu) {
         uint64_t *bar = &my_bars[is];
         uint8_t *dst = my_slots + (size_t)is * kRows * SLOT;
-        if (++is == ST) is = 0;
+        if (p.row_bulk) {
+            armed |= 1u << is;
+            armed_ph = (armed_ph & ~(1u << is)) | (iph << is);
+        }
+        if (++is == ST) {
+            is = 0;
+            iph ^= 1u;
+        }
         const Job &J = jobs[cu.j];
         const int64_t rel0 = (int64_t)(cu.g - J.group_begin) * kRows;
         const int nr = (int)min((int64_t)kRows, (int64_t)J.n_rows - rel0);
@@ -904,6 +918,21 @@ __global__ void __launch_bounds__(threads_of<FMT, MODE>(), min_ctas<FMT, MODE>()
         const int kb = kb_lo + cu.c * KC;
         const int kn = min(KC, kb_hi - kb);
         uintptr_t s = reinterpret_cast<uintptr_t>(W + (J.row0 + rel0) * RB + (int64_t)kb * F::BS);
+        if (p.row_bulk) {
+            uintptr_t a = 0;
+            uint32_t bytes = 0;
+            if (lane < nr) {
+                const uintptr_t sl = s + (uintptr_t)lane * (uintptr_t)RB;
+                a = sl & ~(uintptr_t)15;
+                bytes = (uint32_t)(((sl + (uintptr_t)kn * F::BS + 15) & ~(uintptr_t)15) - a);
+            }
+            const uint32_t total = __reduce_add_sync(0xffffffffu, bytes);
+            if (lane == 0) mbar_arrive_expect_tx(bar, total);
+            __syncwarp();
+            if (bytes)
+                bulk_g2s(dst + (size_t)lane * SLOT, reinterpret_cast<const void *>(a), bytes, bar);
+            return;
+        }
         for (int r = 0; r < nr; ++r, s += (uintptr_t)RB) {
             const uintptr_t a = s & ~(uintptr_t)15;
             const int n16 = (int)(((s + (uintptr_t)kn * F::BS + 15) & ~(uintptr_t)15) - a) >> 4;
@@ -1334,6 +1363,7 @@ __global__ void __launch_bounds__(threads_of<FMT, MODE>(), min_ctas<FMT, MODE>()
                     failed = true;
                     break;
                 }
+                armed &= ~(1u << cur);
                 const uint8_t *slot = my_slots + ((size_t)cur * kRows + lane) * SLOT;
                 if (++cs == ST) {
                     cs = 0;
@@ -1465,6 +1495,11 @@ __global__ void __launch_bounds__(threads_of<FMT, MODE>(), min_ctas<FMT, MODE>()
                 if (fl_issued[i] > 0) mbar_drain(&bars[i], (uint32_t)(fl_issued[i] - 1) & 1u);
     } else if constexpr (!WS) {
         cp_async_wait_all();
+        // Row-bulk copies issued into stages this warp never consumed land
+        // before the CTA exits.
+        if (lane == 0)
+            for (int st = 0; st < ST; ++st)
+                if (armed & (1u << st)) mbar_drain(&my_bars[st], (armed_ph >> st) & 1u);
     }
 }
 
@@ -1873,7 +1908,12 @@ static rf_status launch_merged(const LaunchDesc &d, int nb, int64_t RB, cudaStre
                 ctas_per_sm = 2;
                 stages = st;
             }
-        for (int st = 4; st >= 2 && !ctas_per_sm; --st)
+        // One CTA per SM: Q6_K's super-block decode costs so much per byte
+        // that the CTA-wide stage (refilled only when all 8 warps are done
+        // with it) leaves the copy engine idle; its rows take per-lane
+        // bulk copies instead, where every warp pipelines its own chunks
+        // (the 4096/11008 Q6_K layer: 2.11 vs 1.73 TB/s).
+        for (int st = 4; st >= 2 && !ctas_per_sm && d.fmt != RF_Q6_K; --st)
             if (smem_bytes(d.n_x, nrx, st, fs, max_terms, nj_max, true) <=
                 (size_t)di.max_smem_block) {
                 ctas_per_sm = 1;
@@ -2003,6 +2043,7 @@ static rf_status launch_merged(const LaunchDesc &d, int nb, int64_t RB, cudaStre
             p.n_maps = n_maps;
             p.wait_limit_ns = kWaitLimitNs;
             p.fault_withhold = 0;
+            p.row_bulk = (mode == kModePerLane && !d.host_weights) ? 1 : 0;
             if (mode == kModeTensorWS && g_fault_limit_ns.load(std::memory_order_relaxed)) {
                 const unsigned long long lim = g_fault_limit_ns.exchange(0);
                 if (lim) {
