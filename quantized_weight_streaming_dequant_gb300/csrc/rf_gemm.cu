@@ -15,9 +15,10 @@
 //   * One thread streams the raw quantized bytes of its 128 rows, a chunk
 //     of 8 or 16 blocks at a time, with 2-D tensor copies into a ring; one
 //     thread streams the fp16 activation tiles with 1-D bulk copies.
-//   * Eight decoder warps turn each 64-input slice of the raw rows into
+//   * Twelve decoder warps turn each 64-input slice of the raw rows into
 //     fp16 weights w = d * q (one rounding; MXFP4 values are exact) in the
-//     core-matrix layout; two groups of four warps take alternate slices.
+//     core-matrix layout; three groups of four warps take the slices
+//     round-robin.
 //   * One thread issues four tcgen05.mma (M=128, N, K=16) per slice and
 //     commits them to the slice's "empty" barrier; the last commit releases
 //     the epilogue, which reads the accumulator out of tensor memory.
@@ -400,9 +401,13 @@ rf_status launch_exact(const ExactParams &p, dim3 grid, cudaStream_t s)
 
 // ---------------------------------------------------------------- main path
 constexpr int kTK = 64;                  // inputs per operand slice: two blocks
-constexpr int kTThreads = 384;           // 12 warps
+// Decoder groups of four warps, taking slices round-robin.  A group's waits
+// stay within one phase of each ring barrier only while the groups are no
+// more than the ring's slots (checked per instantiation).
+constexpr int kDecGroups = 3;
+constexpr int kTThreads = 128 + 128 * kDecGroups;   // 4 role warps + the decoders
 constexpr int kATileT = kGM * kTK * 2;   // fp16 weight tile of one slice (16 KB)
-constexpr int kDecWarp0 = 4;             // warps 4-11 decode, then read out
+constexpr int kDecWarp0 = 4;             // warps 4.. decode, then read out
 
 // Raw chunk of each format: BPC blocks (of BE weights, BS bytes) of each of
 // the 128 rows per tensor copy (BPC * BS is a multiple of 16, so every chunk
@@ -415,9 +420,9 @@ template <> struct RawCfg<RF_MXFP4> { static constexpr int BS = 17, BE = 32, BPC
 template <> struct RawCfg<RF_Q4_K> { static constexpr int BS = 144, BE = 256, BPC = 1, R = 3; };
 
 // Slots of the operand ring (a decoded-weight tile and an activation tile
-// each) for a token tile of N.  The two decoder groups take alternate
-// slices, so a ring of at least two slots keeps every parity wait within
-// one phase of its barrier.
+// each) for a token tile of N.  The decoder groups take the slices
+// round-robin, so a ring of at least as many slots as groups keeps every
+// parity wait within one phase of its barrier.
 template <int N> __host__ __device__ constexpr int tc_stages() { return N == 256 ? 3 : (N == 128 ? 4 : 6); }
 
 template <int FMT, int N>
@@ -711,7 +716,7 @@ __global__ void __launch_bounds__(kTThreads, 1) gemm_tc_kernel(const __grid_cons
         }
         for (int r = 0; r < R; ++r) {
             mbar_init(&rfull[r], 1);
-            mbar_init(&rempty[r], 8);
+            mbar_init(&rempty[r], 4 * kDecGroups);
         }
         mbar_init(accf, 1);
         mbar_init(mdone, 1);
@@ -807,7 +812,7 @@ __global__ void __launch_bounds__(kTThreads, 1) gemm_tc_kernel(const __grid_cons
         }
         __syncwarp();
     } else if (warp >= kDecWarp0) {
-        // Decoders: warp group `grp` takes the slices of its parity; thread
+        // Decoders: warp group `grp` takes every kDecGroups-th slice; thread
         // i of a group owns row i of the tile (tensor-memory lane i).
         const int dw = warp - kDecWarp0;
         const int grp = dw >> 2;
@@ -819,8 +824,8 @@ __global__ void __launch_bounds__(kTThreads, 1) gemm_tc_kernel(const __grid_cons
             const uint8_t *slot = raw + (size_t)rs * kGM * CB + (size_t)i * CB;
             auto one = [&](auto qc) -> bool {
                 constexpr int Q = decltype(qc)::value;
-                if ((Q & 1) != grp) return true;
                 const int b = c * QPC + Q;
+                if (b % kDecGroups != grp) return true;
                 if (b >= p.nst) return true;
                 const int s = b % S;
                 const uint32_t ph = (b / S) & 1;
@@ -851,7 +856,7 @@ __global__ void __launch_bounds__(kTThreads, 1) gemm_tc_kernel(const __grid_cons
             const uint32_t tb = tmem + ((uint32_t)((dw & 3) * 32) << 16);
             const int tok0 = tt * N;
 #pragma unroll 1
-            for (int cc = grp * (N / 2); cc < (grp + 1) * (N / 2); cc += 32) {
+            for (int cc = grp * 32; cc < N; cc += 32 * kDecGroups) {
                 uint32_t v[32];
                 tmem_ld32(tb + (uint32_t)cc, v);
                 tmem_ld_wait();
@@ -928,6 +933,7 @@ rf_status launch_tc_n(const TcParams &p, const float *X, int64_t ldx, int64_t in
                       uint8_t *Xp, dim3 grid, cudaStream_t s)
 {
     static_assert(tc_smem<FMT, N>() <= 232448, "rings exceed the 227 KB of shared memory");
+    static_assert(kDecGroups <= tc_stages<N>(), "more decoder groups than ring slots");
     static std::once_flag once[64];
     static bool ok[64];
     int dev = 0;
