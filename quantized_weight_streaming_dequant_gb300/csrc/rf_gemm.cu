@@ -13,12 +13,13 @@
 //   * A CTA owns 128 rows x N tokens (N = 64, 128 or 256) and accumulates
 //     the whole of K in tensor memory (N fp32 columns).
 //   * One thread streams the raw quantized bytes of its 128 rows, a chunk
-//     of 8 or 16 blocks at a time, with 2-D tensor copies into a ring; one
-//     thread streams the fp16 activation tiles with 1-D bulk copies.
+//     of 8 or 16 blocks (one Q4_K super-block) at a time, with 2-D tensor
+//     copies into a ring; one thread streams the fp16 activation tiles with
+//     1-D bulk copies.
 //   * Twelve decoder warps turn each 64-input slice of the raw rows into
-//     fp16 weights w = d * q (one rounding; MXFP4 values are exact) in the
-//     core-matrix layout; three groups of four warps take the slices
-//     round-robin.
+//     fp16 weights w = d * q (one rounding; MXFP4 values are exact; Q4_K's
+//     d*sc*q - dmin*m is rounded to fp32 first) in the core-matrix layout;
+//     three groups of four warps take the slices round-robin.
 //   * One thread issues four tcgen05.mma (M=128, N, K=16) per slice and
 //     commits them to the slice's "empty" barrier; the last commit releases
 //     the epilogue, which reads the accumulator out of tensor memory.
@@ -46,7 +47,8 @@ namespace {
 
 __device__ int g_gemm_status = 0;   // bounded-wait failures (read by rf_device_status)
 
-constexpr int kGM = 128;       // rows per CTA (MMA M)
+constexpr int kGM = 128;       // rows per CTA (MMA M), both paths
+// General path:
 constexpr int kGN = 64;        // tokens per CTA (MMA N)
 constexpr int kGK = 32;        // K per stage: one quantization block
 constexpr int kGStages = 4;
