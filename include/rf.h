@@ -581,10 +581,11 @@ RF_API rf_status rf_device_status(void);
 /* Test hook for the kernels' bounded waits (the pages have no counterpart; it
  * lets the failure path be exercised without faulting a GPU).  Arms a
  * one-shot fault for the next launch on this process that copies with
- * tensor copies: a GEMV over 16-byte aligned rows in device memory, or an
- * rf_gemm on its main path.  In that launch one copy of its first CTA is
- * never issued (a stage of the GEMV's weights; the GEMM's second activation
- * tile), so the warps waiting for it give up after limit_us microseconds,
+ * tensor or bulk copies: a GEMV over device memory whose rows are 16-byte
+ * aligned or take per-row bulk copies, or an rf_gemm on its main path.  In
+ * that launch one copy of its first CTA is never issued (a stage of the
+ * GEMV's weights; the GEMM's second activation tile), so the warps waiting
+ * for it give up after limit_us microseconds,
  * record RF_ERR_TIMEOUT, and the launch ends with nothing in flight (its
  * outputs are undefined).
  * limit_us = 0 disarms.  Errors: RF_ERR_INVALID_ARG for limit_us above

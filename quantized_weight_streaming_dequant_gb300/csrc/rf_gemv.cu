@@ -151,7 +151,7 @@ struct KParamsT {
     int32_t sched_slot;          // >= 0: dynamic group scheduling (producer mode)
     int32_t chained;             // launched behind a previous grid (dependency wait)
     unsigned long long wait_limit_ns;   // limit of every bounded wait
-    int32_t fault_withhold;      // test hook: CTA 0's producer withholds warp 0's first copy
+    int32_t fault_withhold;      // test hook: CTA 0 withholds warp 0's first copy
     int32_t row_bulk;            // per-lane mode over device memory: one bulk copy per row
 };
 using KParamsSmall = KParamsT<4, 4>;
@@ -891,6 +891,7 @@ __global__ void __launch_bounds__(threads_of<FMT, MODE>(), min_ctas<FMT, MODE>()
     int is = 0;   // stage of the next copy
     uint32_t iph = 0;                  // its phase parity
     uint32_t armed = 0, armed_ph = 0;  // row-bulk copies not yet seen landed, and their parity
+    bool lane_withhold = p.fault_withhold && p.row_bulk && blockIdx.x == 0 && warp == 0;
 
     // Per-lane mode: row r's chunk, rounded out to 16-byte boundaries, goes
     // to row r's slot.  Device memory: lane r issues one 1-D bulk copy of its
@@ -903,6 +904,14 @@ __global__ void __launch_bounds__(threads_of<FMT, MODE>(), min_ctas<FMT, MODE>()
     auto issue = [&](const Cursor &cu) {
         uint64_t *bar = &my_bars[is];
         uint8_t *dst = my_slots + (size_t)is * kRows * SLOT;
+        if (lane_withhold) {   // test hook: this stage is never armed and never fills
+            lane_withhold = false;
+            if (++is == ST) {
+                is = 0;
+                iph ^= 1u;
+            }
+            return;
+        }
         if (p.row_bulk) {
             armed |= 1u << is;
             armed_ph = (armed_ph & ~(1u << is)) | (iph << is);
@@ -2044,7 +2053,8 @@ static rf_status launch_merged(const LaunchDesc &d, int nb, int64_t RB, cudaStre
             p.wait_limit_ns = kWaitLimitNs;
             p.fault_withhold = 0;
             p.row_bulk = (mode == kModePerLane && !d.host_weights) ? 1 : 0;
-            if (mode == kModeTensorWS && g_fault_limit_ns.load(std::memory_order_relaxed)) {
+            if ((mode == kModeTensorWS || p.row_bulk) &&
+                g_fault_limit_ns.load(std::memory_order_relaxed)) {
                 const unsigned long long lim = g_fault_limit_ns.exchange(0);
                 if (lim) {
                     p.wait_limit_ns = lim;

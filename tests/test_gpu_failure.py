@@ -2,9 +2,10 @@
 worth knowing about": a stalled prefetcher must neither deadlock nor
 poison the arena).
 
-* A kernel's bounded wait: a test hook makes the producer of one launch
-  (the GEMV's producer warp, or the prefill GEMM's activation copier)
-  withhold one stage's copy, with the wait limit cut to 1 ms.  The launch
+* A kernel's bounded wait: a test hook makes one launch withhold one
+  stage's copy (the GEMV's producer warp, a warp of a GEMV whose rows take
+  per-row bulk copies, or the prefill GEMM's activation copier), with the
+  wait limit cut to 1 ms.  The launch
   must end quickly with RF_ERR_TIMEOUT in the device status word and nothing
   in flight, and the next call on the device must be correct.
 * The host streamer: an injected copy failure at block k stops the walk,
@@ -65,6 +66,37 @@ def test_kernel_wait_timeout_ends_launch_and_device_recovers(rf, rows):
     assert rf.device_status() == rf.OK   # read and cleared
 
     # the device and the ticket slots are clean: later launches are correct
+    for _ in range(3):
+        y = rf.gemv(fmt, W, 0, rows, in_dim, x)
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(y), bits(y_ok))
+    assert rf.device_status() == rf.OK
+
+
+def test_per_lane_bulk_wait_timeout_ends_launch_and_device_recovers(rf):
+    """The same hook on a launch whose rows take per-row bulk copies (Q6_K
+    rows of 9,030 bytes): warp 0 of the first CTA never arms its first
+    stage, gives up after 1 ms, and every warp drains the stages it armed;
+    the next calls give the bits of the call before the fault."""
+    import torch
+    fmt, rows, in_dim = syn.Q6_K, 512, 11008
+    W_np = syn.quant_matrix(fmt, rows, in_dim, seed=330)
+    x_np = syn.normal_f32(in_dim, 331)
+    W, x = dev_tensor(W_np), dev_tensor(x_np)
+    y_ok = rf.gemv(fmt, W, 0, rows, in_dim, x)
+    assert rf.device_status() == rf.OK
+    ref = oracle.gemv(fmt, W_np, 0, rows, in_dim, x_np)
+    assert_gemv_close(y_ok.cpu().numpy(), ref, gemv_tol(fmt, W_np, 0, rows, in_dim, x_np))
+
+    rf.debug_arm_wait_fault(1000)
+    t0 = time.perf_counter()
+    rf.gemv(fmt, W, 0, rows, in_dim, x)
+    status = rf.device_status()
+    dt = time.perf_counter() - t0
+    assert status == TIMEOUT
+    assert dt < 1.0, f"the failed launch took {dt:.3f} s: waits did not end early"
+    assert rf.device_status() == rf.OK
+
     for _ in range(3):
         y = rf.gemv(fmt, W, 0, rows, in_dim, x)
         torch.cuda.synchronize()
