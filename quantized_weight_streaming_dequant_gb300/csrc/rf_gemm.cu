@@ -442,7 +442,10 @@ struct TcParams {
     float *Y;
     int64_t ldy;
     int32_t rows, n_tok, nst, nch;   // nst: 64-input slices; nch: raw chunks
-    int32_t withhold;                // test hook: CTA (0, 0) never copies this slice's activations
+    int32_t ntt;                     // token tiles; tile index = token tile + ntt * row tile
+    int32_t full_tiles;              // tiles [0, full_tiles) take one CTA each; the rest two,
+    int32_t split_c;                 // chunks [0, split_c) and [split_c, nch), summed into Y
+    int32_t withhold;                // test hook: CTA 0 never copies this slice's activations
     unsigned long long limit;
 };
 
@@ -708,7 +711,20 @@ __global__ void __launch_bounds__(kTThreads, 1) gemm_tc_kernel(const __grid_cons
     volatile int *stop = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tt = blockIdx.x, rt = blockIdx.y;
+    // This CTA's tile and K range: a whole tile, or one half of a tile of
+    // the last partial wave (split at a raw-chunk boundary; the two halves
+    // add their sums into a zeroed Y, which is exact in order: a + b = b + a).
+    int tile = (int)blockIdx.x, half = -1;
+    if (tile >= p.full_tiles) {
+        const int j = tile - p.full_tiles;
+        tile = p.full_tiles + (j >> 1);
+        half = j & 1;
+    }
+    const int tt = tile % p.ntt, rt = tile / p.ntt;
+    const int c_lo = half == 1 ? p.split_c : 0;
+    const int c_hi = half == 0 ? p.split_c : p.nch;
+    const int b_lo = c_lo * QPC;
+    const int b_hi = min(c_hi * QPC, p.nst);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -744,34 +760,35 @@ __global__ void __launch_bounds__(kTThreads, 1) gemm_tc_kernel(const __grid_cons
     if (warp == 0) {
         // Raw rows: one 2-D tensor copy per chunk of 128 rows.
         if (lane == 0) {
-            int issued = 0;
-            for (int c = 0; c < p.nch; ++c) {
-                const int rs = c % R;
-                if (!wait(&rempty[rs], ((c / R) & 1) ^ 1)) break;
+            int issued = 0;   // chunks c_lo .. c_lo + issued - 1; ring position = c - c_lo
+            for (int c = c_lo; c < c_hi; ++c) {
+                const int cl = c - c_lo, rs = cl % R;
+                if (!wait(&rempty[rs], ((cl / R) & 1) ^ 1)) break;
                 mbar_arrive_expect_tx(&rfull[rs], (uint32_t)(kGM * CB));
                 tma_2d_g2s(raw + (size_t)rs * kGM * CB, &p.wmap, c * (CB / 2), rt * kGM, &rfull[rs]);
                 ++issued;
             }
-            for (int c = max(0, issued - R); c < issued; ++c) mbar_drain(&rfull[c % R], (c / R) & 1);
+            for (int cl = max(0, issued - R); cl < issued; ++cl)
+                mbar_drain(&rfull[cl % R], (cl / R) & 1);
         }
         __syncwarp();
     } else if (warp == 1) {
         // Activation tiles: one 1-D bulk copy per slice.
         if (lane == 0) {
             const uint8_t *xs = p.Xp + (size_t)tt * p.nst * BT;
-            const int skip = (tt == 0 && rt == 0) ? p.withhold : -1;
-            int next = 0;   // slices [0, next) have been issued (but `skip`)
-            for (int b = 0; b < p.nst; ++b) {
-                const int s = b % S;
-                if (!wait(&empty[s], ((b / S) & 1) ^ 1)) break;
-                next = b + 1;
+            const int skip = blockIdx.x == 0 ? p.withhold : -1;
+            int next = 0;   // local slices [0, next) have been issued (but `skip`)
+            for (int b = b_lo; b < b_hi; ++b) {
+                const int bl = b - b_lo, s = bl % S;
+                if (!wait(&empty[s], ((bl / S) & 1) ^ 1)) break;
+                next = bl + 1;
                 if (b == skip) continue;
                 mbar_arrive_expect_tx(&bfull[s], (uint32_t)BT);
                 bulk_g2s(b_t + (size_t)s * BT, xs + (size_t)b * BT, (uint32_t)BT, &bfull[s]);
             }
             // Every copy issued lands before the CTA can exit.
-            for (int b = max(0, next - S); b < next; ++b)
-                if (b != skip) mbar_drain(&bfull[b % S], (b / S) & 1);
+            for (int bl = max(0, next - S); bl < next; ++bl)
+                if (b_lo + bl != skip) mbar_drain(&bfull[bl % S], (bl / S) & 1);
         }
         __syncwarp();
     } else if (warp == 2) {
@@ -785,7 +802,7 @@ __global__ void __launch_bounds__(kTThreads, 1) gemm_tc_kernel(const __grid_cons
             const uint64_t bd0 = smem_desc(smem_addr(b_t), 1024);
             int s = 0;
             uint32_t ph = 0;
-            for (int b = 0; b < p.nst; ++b) {
+            for (int b = b_lo; b < b_hi; ++b) {
                 if (!wait(&full[s], ph)) {
                     failed = true;
                     break;
@@ -793,7 +810,7 @@ __global__ void __launch_bounds__(kTThreads, 1) gemm_tc_kernel(const __grid_cons
                 tc_fence_after();
                 const uint64_t ad = ad0 + (uint64_t)((s * kATileT) >> 4);
                 const uint64_t bd = bd0 + (uint64_t)((s * BT) >> 4);
-                tc_mma(tmem, ad, bd, idesc_of(N), b != 0);
+                tc_mma(tmem, ad, bd, idesc_of(N), b != b_lo);
 #pragma unroll
                 for (int kk = 1; kk < kTK / 16; ++kk)
                     tc_mma(tmem, ad + 16 * kk, bd + 16 * kk, idesc_of(N), 1u);
@@ -820,17 +837,18 @@ __global__ void __launch_bounds__(kTThreads, 1) gemm_tc_kernel(const __grid_cons
         const int grp = dw >> 2;
         const int i = (dw & 3) * 32 + lane;
         bool ok = true;
-        for (int c = 0; c < p.nch && ok; ++c) {
-            const int rs = c % R;
-            if (!__all_sync(0xffffffffu, wait(&rfull[rs], (c / R) & 1))) break;
+        for (int c = c_lo; c < c_hi && ok; ++c) {
+            const int cl = c - c_lo, rs = cl % R;
+            if (!__all_sync(0xffffffffu, wait(&rfull[rs], (cl / R) & 1))) break;
             const uint8_t *slot = raw + (size_t)rs * kGM * CB + (size_t)i * CB;
             auto one = [&](auto qc) -> bool {
                 constexpr int Q = decltype(qc)::value;
                 const int b = c * QPC + Q;
-                if (b % kDecGroups != grp) return true;
-                if (b >= p.nst) return true;
-                const int s = b % S;
-                const uint32_t ph = (b / S) & 1;
+                if (b >= b_hi) return true;
+                const int bl = b - b_lo;   // ring position of the slice
+                if (bl % kDecGroups != grp) return true;
+                const int s = bl % S;
+                const uint32_t ph = (bl / S) & 1;
                 if (!__all_sync(0xffffffffu, wait(&empty[s], ph ^ 1))) return false;
                 uint32_t out[32];
                 decode_slice<FMT, Q>(slot, out);
@@ -865,8 +883,11 @@ __global__ void __launch_bounds__(kTThreads, 1) gemm_tc_kernel(const __grid_cons
                 if (row_ok) {
 #pragma unroll
                     for (int n = 0; n < 32; ++n)
-                        if (tok0 + cc + n < p.n_tok)
-                            p.Y[(int64_t)(tok0 + cc + n) * p.ldy + row] = __uint_as_float(v[n]);
+                        if (tok0 + cc + n < p.n_tok) {
+                            float *y = p.Y + (int64_t)(tok0 + cc + n) * p.ldy + row;
+                            if (half < 0) *y = __uint_as_float(v[n]);
+                            else atomicAdd(y, __uint_as_float(v[n]));
+                        }
                 }
             }
         }
@@ -905,6 +926,22 @@ __global__ void __launch_bounds__(256) x16_kernel(const float *X, int64_t ldx, i
                        ((uint32_t)__half_as_ushort(__float2half_rn(x[2 * m + 1])) << 16);
         }
         *reinterpret_cast<uint4 *>(Xp + u * 16) = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+}
+
+// Zeroes Y over tiles [t0, t0 + ntiles) (tile = token tile + ntt * row
+// tile), whose two K halves are then added into it.
+__global__ void __launch_bounds__(256) zero_tiles_kernel(float *Y, int64_t ldy, int rows, int n_tok,
+                                                         int ntt, int N, int t0, int ntiles)
+{
+    const int64_t per = (int64_t)N * kGM;
+    for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < (int64_t)ntiles * per;
+         u += (int64_t)gridDim.x * blockDim.x) {
+        const int tile = t0 + (int)(u / per);
+        const int w = (int)(u % per);
+        const int tok = (tile % ntt) * N + w / kGM;
+        const int row = (tile / ntt) * kGM + w % kGM;
+        if (tok < n_tok && row < rows) Y[(int64_t)tok * ldy + row] = 0.f;
     }
 }
 
@@ -950,7 +987,14 @@ rf_status launch_tc_n(const TcParams &p, const float *X, int64_t ldx, int64_t in
         cudaGetLastError();
     });
     if (!ok[dev & 63]) return RF_ERR_CUDA;
-    const int64_t units = (int64_t)grid.x * N * p.nst * 8;
+    const int ntiles = (int)grid.x - p.full_tiles;   // CTAs past the whole tiles, two per split tile
+    if (ntiles > 0) {
+        const int nsplit = ntiles / 2;
+        const int zb = (int)std::min<int64_t>(((int64_t)nsplit * N * kGM + 255) / 256, (int64_t)num_sms() * 8);
+        zero_tiles_kernel<<<zb, 256, 0, s>>>(p.Y, p.ldy, p.rows, p.n_tok, p.ntt, N, p.full_tiles, nsplit);
+        if (last_cuda_error() != RF_OK) return RF_ERR_CUDA;
+    }
+    const int64_t units = (int64_t)p.ntt * N * p.nst * 8;
     const int xb = (int)std::min<int64_t>((units + 255) / 256, (int64_t)num_sms() * 8);
     x16_kernel<N><<<xb, 256, 0, s>>>(X, ldx, p.n_tok, in_dim, p.nst, units, Xp);
     if (last_cuda_error() != RF_OK) return RF_ERR_CUDA;
@@ -1040,7 +1084,16 @@ rf_status rf_gemm(int fmt, const void *W, int64_t row_start, int64_t row_end, in
             p.withhold = p.nst > 1 ? 1 : 0;
         }
         const int N = tc_n(n_tok);
-        const dim3 grid((unsigned)((n_tok + N - 1) / N), (unsigned)((row_end - row_start + kGM - 1) / kGM));
+        p.ntt = (n_tok + N - 1) / N;
+        const int64_t tiles = (int64_t)p.ntt * ((row_end - row_start + kGM - 1) / kGM);
+        // A last partial wave of at most half the SMs is split in K, so that
+        // it takes half a tile's time instead of a whole one.
+        const int sms = num_sms();
+        const int64_t last = tiles % sms;
+        p.full_tiles = (int32_t)tiles;
+        p.split_c = p.nch / 2;
+        if (last > 0 && 2 * last <= sms && p.nch >= 2) p.full_tiles = (int32_t)(tiles - last);
+        const dim3 grid((unsigned)(p.full_tiles + 2 * (tiles - p.full_tiles)));
         uint8_t *Xp = static_cast<uint8_t *>(workspace);
         switch (fmt) {
         case RF_Q4_0: return launch_tc<RF_Q4_0>(p, X, ldx, in_dim, Xp, grid, s);
