@@ -245,33 +245,36 @@ RF_API rf_status rf_gemv_multi(int fmt, const void *W, int64_t row_start, int64_
  *                                                    t < n_tok.
  * Formats: RF_Q4_0, RF_Q8_0, RF_MXFP4, RF_Q4_K (others:
  * RF_ERR_UNSUPPORTED_FMT; for one to eight tokens rf_gemv_multi serves every
- * format).  Rows whose byte length is a multiple of 16 (in_dim a multiple
- * of 256 for Q4_0/Q8_0, of 512 for MXFP4, any Q4_K width) take the main
- * path: X is first rounded to fp16 into `workspace`, each weight is decoded
- * to fp16 as d * q with one rounding (MXFP4 values are exact; Q4_K's
- * d*sc*q - dmin*m is rounded to fp32, then to fp16), and tcgen05.mma
- * accumulates the whole row in fp32.  Other rows take the general path, which keeps the weights
- * exact (fp16 quant values, the block scale applied in fp32 per block) and
- * rounds only X; it needs no workspace.  |X| and |w| must stay below 65504.
+ * format).  X is first rounded to fp16 into `workspace`, each weight is
+ * decoded to fp16 as d * q with one rounding (MXFP4 values are exact;
+ * Q4_K's d*sc*q - dmin*m is rounded to fp32, then to fp16), and
+ * tcgen05.mma accumulates the whole row in fp32.  Rows whose byte length is
+ * a multiple of 16 (in_dim a multiple of 256 for Q4_0/Q8_0, of 512 for
+ * MXFP4, any Q4_K width) are staged by tensor copies; other rows are read
+ * by the decoding threads directly, with the same arithmetic.  |X| and |w|
+ * must stay below 65504.
  * W: device, row 0 of the [out][in] matrix, 16-byte aligned; X: n_tok rows
  * of in_dim floats, ldx floats apart; Y: n_tok rows, ldy floats apart;
  * workspace: device, 16-byte aligned, at least
- * rf_gemm_workspace_bytes(fmt, in_dim, n_tok) bytes (NULL when that is 0),
+ * rf_gemm_workspace_bytes(fmt, in_dim, n_tok) bytes (may be NULL when
+ * n_tok is 0),
  * owned by the caller and overwritten; it must not be used by another call
  * that is in flight.  All device.  Errors: RF_ERR_INVALID_ARG (null
  * pointer, in_dim not a positive multiple of the format's block (32, or
  * 256 for Q4_K), bad window, n_tok < 0, ldx < in_dim, ldy < rows,
  * workspace missing or too small);
  * RF_ERR_MISALIGNED (W or workspace not 16-byte aligned); RF_ERR_TOO_LARGE
- * (more than 4,194,240 tokens or 8,388,480 rows).  Empty work is a no-op.
+ * (ceil(rows / 128) * ceil(n_tok / T) above 2^30 - 1, T the token tile:
+ * 64 up to 64 tokens, 128 up to 128, else 256).  Empty work is a no-op.
  * A bounded internal wait that gives up is reported by rf_device_status as
  * RF_ERR_TIMEOUT. */
 RF_API rf_status rf_gemm(int fmt, const void *W, int64_t row_start, int64_t row_end,
                          int64_t in_dim, int n_tok, const float *X, int64_t ldx, float *Y,
                          int64_t ldy, void *workspace, size_t workspace_bytes, void *stream);
 
-/* Bytes of workspace rf_gemm needs for (fmt, in_dim, n_tok): 0 when the
- * general path serves it or the arguments are invalid. */
+/* Bytes of workspace rf_gemm needs for (fmt, in_dim, n_tok): the fp16
+ * activation tiles, T * ceil(n_tok / T) tokens x ceil(in_dim / 64) * 64
+ * inputs x 2 bytes (T as above); 0 when the arguments are invalid. */
 RF_API size_t rf_gemm_workspace_bytes(int fmt, int64_t in_dim, int n_tok);
 
 /* Zero-copy variant of rf_gemv (hipfire PR #793, "Summary": the "pcie"
@@ -582,7 +585,7 @@ RF_API rf_status rf_device_status(void);
  * lets the failure path be exercised without faulting a GPU).  Arms a
  * one-shot fault for the next launch on this process that copies with
  * tensor or bulk copies: a GEMV over device memory whose rows are 16-byte
- * aligned or take per-row bulk copies, or an rf_gemm on its main path.  In
+ * aligned or take per-row bulk copies, or an rf_gemm.  In
  * that launch one copy of its first CTA is never issued (a stage of the
  * GEMV's weights; the GEMM's second activation tile), so the warps waiting
  * for it give up after limit_us microseconds,

@@ -6,16 +6,19 @@
 // window and every token t of the chunk.  Unlike batch-1 decode this is a
 // dense contraction (2 * n_tok flops per weight), so it runs on tcgen05.mma.
 //
-// Main path (rows 16-byte aligned, gemm_tc_kernel):
+// gemm_tc_kernel:
 //   * A pre-pass rounds X to fp16 once, into the operand layout of the MMA
 //     (tiles of N tokens x 64 inputs, K-major core matrices), in a caller
 //     workspace.
 //   * A CTA owns 128 rows x N tokens (N = 64, 128 or 256) and accumulates
 //     the whole of K in tensor memory (N fp32 columns).
-//   * One thread streams the raw quantized bytes of its 128 rows, a chunk
-//     of 8 or 16 blocks (one Q4_K super-block) at a time, with 2-D tensor
-//     copies into a ring; one thread streams the fp16 activation tiles with
-//     1-D bulk copies.
+//   * Rows whose byte length is a multiple of 16: one thread streams the
+//     raw quantized bytes of its 128 rows, a chunk of 8 or 16 blocks (one
+//     Q4_K super-block) at a time, with 2-D tensor copies into a ring.
+//     Other rows (a tensor map cannot describe them): each decoder thread
+//     reads its row's raw bytes itself with aligned 4-byte loads, the next
+//     slice's while it decodes the current one.
+//   * One thread streams the fp16 activation tiles with 1-D bulk copies.
 //   * Twelve decoder warps turn each 64-input slice of the raw rows into
 //     fp16 weights w = d * q (one rounding; MXFP4 values are exact; Q4_K's
 //     d*sc*q - dmin*m is rounded to fp32 first) in the core-matrix layout;
@@ -25,10 +28,6 @@
 //     the epilogue, which reads the accumulator out of tensor memory.
 //   Error: w and x each carry one fp16 rounding (relative 2^-11, absolute
 //   2^-25 below the normal range), accumulation is fp32.
-//
-// General path (any row alignment, gemm_exact_kernel): one 32-weight block
-// per stage, decoded to its exact quant values; the block scale is applied
-// in fp32 after each block's MMA, so only x is rounded.
 //
 // Every wait is bounded; after a failure every role stops, copies and MMAs
 // already issued are waited for, and tensor memory is freed on every path.
@@ -47,24 +46,7 @@ namespace {
 
 __device__ int g_gemm_status = 0;   // bounded-wait failures (read by rf_device_status)
 
-constexpr int kGM = 128;       // rows per CTA (MMA M), both paths
-// General path:
-constexpr int kGN = 64;        // tokens per CTA (MMA N)
-constexpr int kGK = 32;        // K per stage: one quantization block
-constexpr int kGStages = 4;
-constexpr int kGThreads = 288; // warps 0-3 epilogue, 4-7 producers, 8 MMA + TMEM
-constexpr int kATile = kGM * kGK * 2;   // 8 KB of fp16
-constexpr int kBTile = kGN * kGK * 2;   // 4 KB of fp16
-constexpr uint32_t kTmemCols = 2 * kGN; // two accumulators of 64 fp32 columns
-
-// Byte offset of element (row r, k) of a K-major tile of 32 fp16 columns in
-// the core-matrix layout: core matrix (r/8, k/8) at (r/8)*512 + (k/8)*128,
-// its 8 rows 16 bytes apart.  So the stride between core matrices along K
-// (leading dimension) is 128 bytes and along rows (stride dimension) 512.
-__device__ __forceinline__ int cm_off(int r, int k)
-{
-    return (r >> 3) * 512 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2;
-}
+constexpr int kGM = 128;       // rows per CTA (MMA M)
 
 // Shared-memory matrix descriptor of a K-major tile without swizzle: start
 // address, leading-dimension byte offset 128 (the next core matrix along K),
@@ -158,250 +140,6 @@ __device__ __forceinline__ void tmem_ld_wait()
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// fp16 value (as bits) of a small signed integer |v| <= 2048 (exact).
-__device__ __forceinline__ uint32_t h_of_int(int v)
-{
-    return (uint32_t)__half_as_ushort(__int2half_rn(v));
-}
-
-// The 32 quant values of one block as fp16 bit pairs (q[i] holds elements
-// 2i and 2i+1), and the block's scale as fp32.
-template <int FMT>
-__device__ __forceinline__ void decode_block_h(const uint8_t *blk, uint32_t (&q)[16])
-{
-    if constexpr (FMT == RF_Q8_0) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int a = (int8_t)blk[2 + 2 * i], b = (int8_t)blk[3 + 2 * i];
-            q[i] = h_of_int(a) | (h_of_int(b) << 16);
-        }
-    } else if constexpr (FMT == RF_Q4_0) {
-        // element j < 16: low nibble of byte j; j + 16: its high nibble
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint8_t b0 = blk[2 + 2 * i], b1 = blk[3 + 2 * i];
-            q[i] = h_of_int((b0 & 15) - 8) | (h_of_int((b1 & 15) - 8) << 16);
-            q[8 + i] = h_of_int((b0 >> 4) - 8) | (h_of_int((b1 >> 4) - 8) << 16);
-        }
-    } else {
-        // MXFP4: an E2M1 code (s e1 e0 m) placed as fp16 bits s at 15 and
-        // e1 e0 m at 11..9 is exactly its value times 2^-14; the block scale
-        // carries the 2^14 back (block_scale_f).
-        auto h = [](uint32_t c) -> uint32_t { return ((c & 7u) << 9) | ((c & 8u) << 12); };
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint8_t b0 = blk[1 + 2 * i], b1 = blk[2 + 2 * i];
-            q[i] = h(b0 & 15u) | (h(b1 & 15u) << 16);
-            q[8 + i] = h(b0 >> 4) | (h(b1 >> 4) << 16);
-        }
-    }
-}
-
-template <int FMT>
-__device__ __forceinline__ float block_scale_f(const uint8_t *blk)
-{
-    if constexpr (FMT == RF_MXFP4) {
-        // 2^(E-127) times the 2^14 taken out of the decoded values
-        const uint32_t E = blk[0];
-        if (E == 255u) return __uint_as_float(0x7fc00000u);
-        if (E > 240u) return __uint_as_float(0x7f800000u);
-        return __uint_as_float((E + 14u) << 23);
-    } else {
-        return __half2float(__ushort_as_half((unsigned short)(blk[0] | (blk[1] << 8))));
-    }
-}
-
-struct ExactParams {
-    const uint8_t *W;
-    const float *X;
-    float *Y;
-    int64_t row_start, row_end, ldx, ldy, rb;   // rb: bytes per row
-    int32_t nb, n_tok;
-    unsigned long long limit;
-};
-
-template <int FMT>
-__global__ void __launch_bounds__(kGThreads, 1) gemm_exact_kernel(const __grid_constant__ ExactParams p)
-{
-    constexpr int BS = FMT == RF_Q8_0 ? 34 : (FMT == RF_Q4_0 ? 18 : 17);
-    extern __shared__ __align__(1024) uint8_t smem[];
-    uint8_t *a_tiles = smem;                                   // [stages][8 KB]
-    uint8_t *b_tiles = smem + kGStages * kATile;               // [stages][4 KB]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(b_tiles + kGStages * kBTile);
-    uint64_t *full = bars, *empty = bars + kGStages;           // operand stages
-    uint64_t *acc_full = bars + 2 * kGStages, *acc_empty = acc_full + 2;
-    uint64_t *done = acc_empty + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
-    volatile int *stop = reinterpret_cast<volatile int *>(tmem_slot + 1);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t row0 = p.row_start + (int64_t)blockIdx.x * kGM;
-    const int tok0 = blockIdx.y * kGN;
-    const int nb = p.nb;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kGStages; ++s) {
-            mbar_init(&full[s], 128);
-            mbar_init(&empty[s], 1);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], 128);
-        }
-        mbar_init(done, 1);
-        *stop = 0;
-        fence_barrier_init();
-    }
-    if (warp == 8) {
-        tmem_alloc(tmem_slot, kTmemCols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    // A wait that gives up stops every role of the CTA.
-    auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
-        if (*stop) return false;
-        if (mbar_wait_bounded(bar, parity, &g_gemm_status, p.limit)) return true;
-        *stop = 1;
-        return false;
-    };
-
-    if (warp >= 4 && warp < 8) {
-        // Producers: thread i decodes row i of the tile and converts 16 of
-        // the 64 x 32 activations of each block.
-        const int i = (int)threadIdx.x - 128;
-        const int64_t r = row0 + i;
-        const bool row_ok = r < p.row_end;
-        const uint8_t *wrow = p.W + (row_ok ? r : p.row_start) * p.rb;
-        const int t = i >> 1, kk = (i & 1) * 16;
-        const bool tok_ok = tok0 + t < p.n_tok;
-        const float *xrow = p.X + (int64_t)(tok_ok ? tok0 + t : 0) * p.ldx;
-        for (int b = 0; b < nb; ++b) {
-            const int s = b % kGStages;
-            if (!__all_sync(0xffffffffu, wait(&empty[s], ((b / kGStages) & 1) ^ 1))) break;
-            uint32_t q[16];
-            if (row_ok) {
-                decode_block_h<FMT>(wrow + (int64_t)b * BS, q);
-            } else {
-#pragma unroll
-                for (int k = 0; k < 16; ++k) q[k] = 0;
-            }
-            uint8_t *at = a_tiles + s * kATile;
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                *reinterpret_cast<uint4 *>(at + cm_off(i, 8 * c)) =
-                    make_uint4(q[4 * c], q[4 * c + 1], q[4 * c + 2], q[4 * c + 3]);
-            uint8_t *bt = b_tiles + s * kBTile;
-            uint32_t xh[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                float x0 = 0.f, x1 = 0.f;
-                if (tok_ok) {
-                    x0 = xrow[32 * (int64_t)b + kk + 2 * k];
-                    x1 = xrow[32 * (int64_t)b + kk + 2 * k + 1];
-                }
-                xh[k] = (uint32_t)__half_as_ushort(__float2half_rn(x0)) |
-                        ((uint32_t)__half_as_ushort(__float2half_rn(x1)) << 16);
-            }
-            *reinterpret_cast<uint4 *>(bt + cm_off(t, kk)) = make_uint4(xh[0], xh[1], xh[2], xh[3]);
-            *reinterpret_cast<uint4 *>(bt + cm_off(t, kk + 8)) = make_uint4(xh[4], xh[5], xh[6], xh[7]);
-            fence_async_smem();
-            mbar_arrive(&full[s]);
-        }
-    } else if (warp == 8) {
-        // MMA issue: one thread.
-        if (lane == 0) {
-            int issued = 0;
-            for (int b = 0; b < nb; ++b) {
-                const int s = b % kGStages, buf = b & 1;
-                if (!wait(&full[s], (b / kGStages) & 1)) break;
-                if (!wait(&acc_empty[buf], ((b >> 1) & 1) ^ 1)) break;
-                tc_fence_after();
-                const uint32_t a = smem_addr(a_tiles + s * kATile);
-                const uint32_t bb = smem_addr(b_tiles + s * kBTile);
-                const uint32_t d = tmem + (uint32_t)(buf * kGN);
-                tc_mma(d, smem_desc(a, 512), smem_desc(bb, 512), idesc_of(kGN), 0);
-                tc_mma(d, smem_desc(a + 256, 512), smem_desc(bb + 256, 512), idesc_of(kGN), 1);
-                tc_commit(&empty[s]);
-                tc_commit(&acc_full[buf]);
-                ++issued;
-            }
-            // Every issued MMA completes before TMEM is freed.
-            if (issued) {
-                tc_commit(done);
-                mbar_drain(done, 0);
-            }
-        }
-        __syncwarp();
-    } else {
-        // Epilogue: thread e owns row e of the tile, TMEM lane e.
-        const int e = (int)threadIdx.x;
-        const int64_t r = row0 + e;
-        const bool row_ok = r < p.row_end;
-        const uint8_t *wrow = p.W + (row_ok ? r : p.row_start) * p.rb;
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-        float acc[kGN];
-#pragma unroll
-        for (int n = 0; n < kGN; ++n) acc[n] = 0.f;
-        float scale = row_ok ? block_scale_f<FMT>(wrow) : 0.f;
-        for (int b = 0; b < nb; ++b) {
-            const int buf = b & 1;
-            const float sc = scale;
-            if (row_ok && b + 1 < nb) scale = block_scale_f<FMT>(wrow + (int64_t)(b + 1) * BS);
-            if (!__all_sync(0xffffffffu, wait(&acc_full[buf], (b >> 1) & 1))) break;
-            tc_fence_after();
-            uint32_t v[32];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                tmem_ld32(lane_base + (uint32_t)(buf * kGN + 32 * h), v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int n = 0; n < 32; ++n) acc[32 * h + n] = fmaf(sc, __uint_as_float(v[n]), acc[32 * h + n]);
-            }
-            tc_fence_before();
-            mbar_arrive(&acc_empty[buf]);
-        }
-        if (row_ok && !*stop) {
-            const int64_t y_row = r - p.row_start;
-#pragma unroll
-            for (int n = 0; n < kGN; ++n)
-                if (tok0 + n < p.n_tok) p.Y[(int64_t)(tok0 + n) * p.ldy + y_row] = acc[n];
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 8) {
-        tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
-    }
-}
-
-constexpr size_t kExactSmem = (size_t)kGStages * (kATile + kBTile) + (2 * kGStages + 5) * 8 + 16;
-
-template <int FMT>
-rf_status launch_exact(const ExactParams &p, dim3 grid, cudaStream_t s)
-{
-    static std::once_flag once[64];
-    static bool ok[64];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-        cudaGetLastError();
-        return RF_ERR_CUDA;
-    }
-    std::call_once(once[dev & 63], [dev] {
-        ok[dev & 63] = cudaFuncSetAttribute(gemm_exact_kernel<FMT>,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            (int)kExactSmem) == cudaSuccess;
-        cudaGetLastError();
-    });
-    if (!ok[dev & 63]) return RF_ERR_CUDA;
-    gemm_exact_kernel<FMT><<<grid, kGThreads, kExactSmem, s>>>(p);
-    return last_cuda_error();
-}
-
-// ---------------------------------------------------------------- main path
 constexpr int kTK = 64;                  // inputs per operand slice: two blocks
 // Decoder groups of four warps, taking slices round-robin.  A group's waits
 // stay within one phase of each ring barrier only while the groups are no
@@ -425,23 +163,30 @@ template <> struct RawCfg<RF_Q4_K> { static constexpr int BS = 144, BE = 256, BP
 // each) for a token tile of N.  The decoder groups take the slices
 // round-robin, so a ring of at least as many slots as groups keeps every
 // parity wait within one phase of its barrier.
-template <int N> __host__ __device__ constexpr int tc_stages() { return N == 256 ? 3 : (N == 128 ? 4 : 6); }
+// DIRECT: the decoders read the raw rows themselves (no raw ring), so the
+// operand ring can be deeper.
+template <int N, bool DIRECT> __host__ __device__ constexpr int tc_stages()
+{
+    return DIRECT ? (N == 256 ? 4 : (N == 128 ? 6 : 8)) : (N == 256 ? 3 : (N == 128 ? 4 : 6));
+}
 
-template <int FMT, int N>
+template <int FMT, int N, bool DIRECT>
 constexpr size_t tc_smem()
 {
     using RC = RawCfg<FMT>;
-    return (size_t)tc_stages<N>() * (kATileT + N * kTK * 2) +
-           (size_t)RC::R * kGM * RC::BPC * RC::BS + 16 +
-           (size_t)(3 * tc_stages<N>() + 2 * RC::R + 2) * 8 + 16;
+    return (size_t)tc_stages<N, DIRECT>() * (kATileT + N * kTK * 2) +
+           (DIRECT ? 0 : (size_t)RC::R * kGM * RC::BPC * RC::BS) + 16 +
+           (size_t)(3 * tc_stages<N, DIRECT>() + 2 * RC::R + 2) * 8 + 16;
 }
 
 struct TcParams {
     CUtensorMap wmap;   // the window's rows as uint16 columns; boxes of one chunk x 128 rows
+    const uint8_t *Wd;  // direct mode: row 0 of the window
+    int64_t rb;         // direct mode: bytes per row
     const uint8_t *Xp;  // fp16 activation tiles: [token tile][slice][N x 64]
     float *Y;
     int64_t ldy;
-    int32_t rows, n_tok, nst, nch;   // nst: 64-input slices; nch: raw chunks
+    int32_t rows, n_tok, nst, nch;   // nst: 64-input slices; nch: raw chunks (slices if direct)
     int32_t ntt;                     // token tiles; tile index = token tile + ntt * row tile
     int32_t full_tiles;              // tiles [0, full_tiles) take one CTA each; the rest two,
     int32_t split_c;                 // chunks [0, split_c) and [split_c, nch), summed into Y
@@ -633,18 +378,11 @@ __device__ __forceinline__ void q4k_slice(const uint8_t *slot, uint32_t (&out)[3
     }
 }
 
-// Slice Q of a raw chunk (blocks 2Q and 2Q+1 of one row, or a quarter of a
-// Q4_K super-block) as 32 fp16 pairs.
-template <int FMT, int Q>
-__device__ __forceinline__ void decode_slice(const uint8_t *slot, uint32_t (&out)[32])
+// One slice (two 32-weight blocks) as 32 fp16 pairs, from a window whose
+// word<P>, half<P> and byte<P> read the slice's byte P.
+template <int FMT, class Win>
+__device__ __forceinline__ void decode_win(const Win &win, uint32_t (&out)[32])
 {
-    if constexpr (FMT == RF_Q4_K) {
-        q4k_slice<Q>(slot, out);
-        return;
-    } else {
-    using RC = RawCfg<FMT>;
-    RawWin<Q * 2 * RC::BS, 2 * RC::BS> win;
-    win.load(slot);
     if constexpr (FMT == RF_Q4_0) {
         const uint32_t q0[4] = {win.template word<2>(), win.template word<6>(),
                                 win.template word<10>(), win.template word<14>()};
@@ -671,8 +409,93 @@ __device__ __forceinline__ void decode_slice(const uint8_t *slot, uint32_t (&out
         mxfp4_pairs(win.template byte<0>(), q0, out);
         mxfp4_pairs(win.template byte<17>(), q1, out + 16);
     }
+}
+
+// Slice Q of a raw chunk (blocks 2Q and 2Q+1 of one row, or a quarter of a
+// Q4_K super-block) as 32 fp16 pairs.
+template <int FMT, int Q>
+__device__ __forceinline__ void decode_slice(const uint8_t *slot, uint32_t (&out)[32])
+{
+    if constexpr (FMT == RF_Q4_K) {
+        q4k_slice<Q>(slot, out);
+    } else {
+        using RC = RawCfg<FMT>;
+        RawWin<Q * 2 * RC::BS, 2 * RC::BS> win;
+        win.load(slot);
+        decode_win<FMT>(win, out);
     }
 }
+
+// A slice's NB bytes as words starting at its first byte (one word of
+// slack for the funnel of the last unaligned read).
+template <int NB>
+struct SliceWin {
+    uint32_t w[(NB + 3) / 4 + 1];
+    template <int P> __device__ __forceinline__ uint32_t word() const
+    {
+        if constexpr (P % 4 == 0) return w[P / 4];
+        else return __funnelshift_r(w[P / 4], w[P / 4 + 1], 8 * (P % 4));
+    }
+    template <int P> __device__ __forceinline__ uint32_t half() const
+    {
+        static_assert(P % 2 == 0, "fp16 scale at an odd byte");
+        return (w[P / 4] >> (8 * (P % 4))) & 0xFFFFu;
+    }
+    template <int P> __device__ __forceinline__ uint32_t byte() const
+    {
+        return (w[P / 4] >> (8 * (P % 4))) & 0xFFu;
+    }
+};
+
+// Rows whose byte length is not a multiple of 16 cannot be described by a
+// tensor map, so their decoders read the raw bytes themselves: the aligned
+// 4-byte words that hold a slice's nb bytes (never a word past the one
+// holding its last byte; bytes past nb are cleared, so a final slice of one
+// block decodes zeros for its second), read through the non-coherent path,
+// then shifted by the slice's byte phase into a window that starts at it.
+template <int FMT>
+struct DirectSlice {
+    static constexpr int NB = 2 * RawCfg<FMT>::BS;
+    static constexpr int NW = (3 + NB + 3) / 4;   // words covering NB bytes at any phase
+    uint32_t w[NW];
+    uint32_t sh;
+    __device__ __forceinline__ void load(const uint8_t *a, int nb)
+    {
+        const uintptr_t ua = reinterpret_cast<uintptr_t>(a);
+        const uint32_t *a4 = reinterpret_cast<const uint32_t *>(ua & ~(uintptr_t)3);
+        sh = 8u * (uint32_t)(ua & 3);
+        const int end = (int)(ua & 3) + nb;   // bytes from the first word's start to the slice's end
+#pragma unroll
+        for (int j = 0; j < NW; ++j) {
+            const int rem = end - 4 * j;      // bytes of word j that belong to the slice
+            const uint32_t v = rem > 0 ? __ldg(a4 + j) : 0u;
+            w[j] = rem >= 4 ? v : v & ((1u << (8 * (rem > 0 ? rem : 0))) - 1u);
+        }
+    }
+    __device__ __forceinline__ void zero()
+    {
+#pragma unroll
+        for (int j = 0; j < NW; ++j) w[j] = 0u;
+        sh = 0u;
+    }
+    // Slice b of a row of rb bytes at `row`: NB bytes, or one block at the
+    // end of a row whose inputs are an odd number of blocks; zeros for a
+    // row past the window.
+    __device__ __forceinline__ void fetch(const uint8_t *row, int b, int64_t rb, bool row_ok)
+    {
+        const int64_t off = (int64_t)b * NB;
+        if (row_ok) load(row + off, rb - off < NB ? (int)(rb - off) : NB);
+        else zero();
+    }
+    __device__ __forceinline__ void to(SliceWin<NB> &win) const
+    {
+        constexpr int NO = (NB + 3) / 4 + 1;
+        static_assert(NO <= NW, "window wider than the words read");
+#pragma unroll
+        for (int j = 0; j < NO; ++j)
+            win.w[j] = __funnelshift_r(w[j], j + 1 < NW ? w[j + 1] : 0u, sh);
+    }
+};
 
 // Compile-time loop over the slices of a chunk: f(integral_constant<Q>) for
 // Q = Q0 .. QN-1 while it returns true.
@@ -689,18 +512,20 @@ struct SliceLoop<QN, QN> {
     template <class F> __device__ __forceinline__ static bool run(F &) { return true; }
 };
 
-template <int FMT, int N>
+template <int FMT, int N, bool DIRECT>
 __global__ void __launch_bounds__(kTThreads, 1) gemm_tc_kernel(const __grid_constant__ TcParams p)
 {
     using RC = RawCfg<FMT>;
-    constexpr int S = tc_stages<N>(), R = RC::R, CB = RC::BPC * RC::BS;
-    constexpr int QPC = RC::BPC * RC::BE / kTK;
+    constexpr int S = tc_stages<N, DIRECT>(), R = RC::R, CB = RC::BPC * RC::BS;
+    // Slices per raw chunk; in direct mode every slice is its own "chunk"
+    // (the unit of the last-wave K split).
+    constexpr int QPC = DIRECT ? 1 : RC::BPC * RC::BE / kTK;
     constexpr int BT = N * kTK * 2;   // fp16 activation tile of one slice
     extern __shared__ __align__(1024) uint8_t smem[];
     uint8_t *a_t = smem;                 // [S][16 KB]
     uint8_t *b_t = a_t + S * kATileT;    // [S][BT]
-    uint8_t *raw = b_t + S * BT;         // [R][128 rows][CB]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(raw + (size_t)R * kGM * CB + 16);
+    uint8_t *raw = b_t + S * BT;         // [R][128 rows][CB] (none in direct mode)
+    uint64_t *bars = reinterpret_cast<uint64_t *>(raw + (DIRECT ? 0 : (size_t)R * kGM * CB) + 16);
     // full: the slot's weights decoded and its activations landed (one
     // arrival per decoder warp); bfull: the activation copy's bytes; empty:
     // the slot's MMAs done.
@@ -759,7 +584,7 @@ __global__ void __launch_bounds__(kTThreads, 1) gemm_tc_kernel(const __grid_cons
 
     if (warp == 0) {
         // Raw rows: one 2-D tensor copy per chunk of 128 rows.
-        if (lane == 0) {
+        if (!DIRECT && lane == 0) {
             int issued = 0;   // chunks c_lo .. c_lo + issued - 1; ring position = c - c_lo
             for (int c = c_lo; c < c_hi; ++c) {
                 const int cl = c - c_lo, rs = cl % R;
@@ -836,7 +661,45 @@ __global__ void __launch_bounds__(kTThreads, 1) gemm_tc_kernel(const __grid_cons
         const int dw = warp - kDecWarp0;
         const int grp = dw >> 2;
         const int i = (dw & 3) * 32 + lane;
-        bool ok = true;
+        // The decoded weight tile of slot s and this row, written in the
+        // core-matrix layout, fenced to the async proxy; once the slot's
+        // activation tile has landed too, one arrival per warp.
+        auto publish = [&](int s, uint32_t ph, const uint32_t (&out)[32]) -> bool {
+            uint8_t *at = a_t + (size_t)s * kATileT + (i >> 3) * 1024 + (i & 7) * 16;
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8)
+                *reinterpret_cast<uint4 *>(at + c8 * 128) =
+                    make_uint4(out[4 * c8], out[4 * c8 + 1], out[4 * c8 + 2], out[4 * c8 + 3]);
+            fence_async_smem();
+            if (!__all_sync(0xffffffffu, wait(&bfull[s], ph))) return false;
+            if (lane == 0) mbar_arrive(&full[s]);
+            return true;
+        };
+        if constexpr (DIRECT) {
+            // This group's slices b_lo + grp, + kDecGroups, ...; the raw
+            // words of the next one are read before this one is decoded.
+            constexpr int SB = 2 * RC::BS;   // bytes per slice
+            const int64_t row = (int64_t)rt * kGM + i;
+            const bool row_ok = row < p.rows;   // rows past the window decode zeros
+            const uint8_t *rowp = p.Wd + (row_ok ? row : 0) * p.rb;
+            DirectSlice<FMT> nxt;
+            int bl = grp;
+            if (b_lo + bl < b_hi) nxt.fetch(rowp, b_lo + bl, p.rb, row_ok);
+            for (; b_lo + bl < b_hi; bl += kDecGroups) {
+                const DirectSlice<FMT> cur = nxt;
+                const int bn = b_lo + bl + kDecGroups;
+                if (bn < b_hi) nxt.fetch(rowp, bn, p.rb, row_ok);
+                const int s = bl % S;
+                const uint32_t ph = (bl / S) & 1;
+                if (!__all_sync(0xffffffffu, wait(&empty[s], ph ^ 1))) break;
+                SliceWin<SB> win;
+                cur.to(win);
+                uint32_t out[32];
+                decode_win<FMT>(win, out);
+                if (!publish(s, ph, out)) break;
+            }
+        }
+        bool ok = !DIRECT;
         for (int c = c_lo; c < c_hi && ok; ++c) {
             const int cl = c - c_lo, rs = cl % R;
             if (!__all_sync(0xffffffffu, wait(&rfull[rs], (cl / R) & 1))) break;
@@ -852,17 +715,7 @@ __global__ void __launch_bounds__(kTThreads, 1) gemm_tc_kernel(const __grid_cons
                 if (!__all_sync(0xffffffffu, wait(&empty[s], ph ^ 1))) return false;
                 uint32_t out[32];
                 decode_slice<FMT, Q>(slot, out);
-                uint8_t *at = a_t + (size_t)s * kATileT + (i >> 3) * 1024 + (i & 7) * 16;
-#pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8)
-                    *reinterpret_cast<uint4 *>(at + c8 * 128) =
-                        make_uint4(out[4 * c8], out[4 * c8 + 1], out[4 * c8 + 2], out[4 * c8 + 3]);
-                fence_async_smem();
-                // The slot is complete once its activation tile has landed
-                // too; one arrival per warp.
-                if (!__all_sync(0xffffffffu, wait(&bfull[s], ph))) return false;
-                if (lane == 0) mbar_arrive(&full[s]);
-                return true;
+                return publish(s, ph, out);
             };
             ok = SliceLoop<0, QPC>::run(one);
             __syncwarp();
@@ -948,8 +801,8 @@ __global__ void __launch_bounds__(256) zero_tiles_kernel(float *Y, int64_t ldy, 
 // Token tile of the main path for a chunk of n_tok tokens.
 int tc_n(int n_tok) { return n_tok <= 64 ? 64 : (n_tok <= 128 ? 128 : 256); }
 
-// The main path takes rows whose byte length is a multiple of 16 (always
-// true for Q4_K's 144-byte super-blocks).
+// Rows whose byte length is a multiple of 16 (always true for Q4_K's
+// 144-byte super-blocks) are copied by tensor maps; others are read directly.
 bool tc_rows_ok(int fmt, int64_t in_dim)
 {
     return ((in_dim / block_elems_of(fmt)) * (int64_t)block_bytes_of(fmt)) % 16 == 0;
@@ -967,12 +820,12 @@ size_t tc_workspace(int64_t in_dim, int n_tok)
     return (size_t)(ntt * N) * (size_t)nst * kTK * 2;
 }
 
-template <int FMT, int N>
+template <int FMT, int N, bool DIRECT>
 rf_status launch_tc_n(const TcParams &p, const float *X, int64_t ldx, int64_t in_dim,
                       uint8_t *Xp, dim3 grid, cudaStream_t s)
 {
-    static_assert(tc_smem<FMT, N>() <= 232448, "rings exceed the 227 KB of shared memory");
-    static_assert(kDecGroups <= tc_stages<N>(), "more decoder groups than ring slots");
+    static_assert(tc_smem<FMT, N, DIRECT>() <= 232448, "rings exceed the 227 KB of shared memory");
+    static_assert(kDecGroups <= tc_stages<N, DIRECT>(), "more decoder groups than ring slots");
     static std::once_flag once[64];
     static bool ok[64];
     int dev = 0;
@@ -981,9 +834,9 @@ rf_status launch_tc_n(const TcParams &p, const float *X, int64_t ldx, int64_t in
         return RF_ERR_CUDA;
     }
     std::call_once(once[dev & 63], [dev] {
-        ok[dev & 63] = cudaFuncSetAttribute(gemm_tc_kernel<FMT, N>,
+        ok[dev & 63] = cudaFuncSetAttribute(gemm_tc_kernel<FMT, N, DIRECT>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            (int)tc_smem<FMT, N>()) == cudaSuccess;
+                                            (int)tc_smem<FMT, N, DIRECT>()) == cudaSuccess;
         cudaGetLastError();
     });
     if (!ok[dev & 63]) return RF_ERR_CUDA;
@@ -998,18 +851,18 @@ rf_status launch_tc_n(const TcParams &p, const float *X, int64_t ldx, int64_t in
     const int xb = (int)std::min<int64_t>((units + 255) / 256, (int64_t)num_sms() * 8);
     x16_kernel<N><<<xb, 256, 0, s>>>(X, ldx, p.n_tok, in_dim, p.nst, units, Xp);
     if (last_cuda_error() != RF_OK) return RF_ERR_CUDA;
-    gemm_tc_kernel<FMT, N><<<grid, kTThreads, tc_smem<FMT, N>(), s>>>(p);
+    gemm_tc_kernel<FMT, N, DIRECT><<<grid, kTThreads, tc_smem<FMT, N, DIRECT>(), s>>>(p);
     return last_cuda_error();
 }
 
-template <int FMT>
+template <int FMT, bool DIRECT>
 rf_status launch_tc(const TcParams &p, const float *X, int64_t ldx, int64_t in_dim, uint8_t *Xp,
                     dim3 grid, cudaStream_t s)
 {
     switch (tc_n(p.n_tok)) {
-    case 64: return launch_tc_n<FMT, 64>(p, X, ldx, in_dim, Xp, grid, s);
-    case 128: return launch_tc_n<FMT, 128>(p, X, ldx, in_dim, Xp, grid, s);
-    default: return launch_tc_n<FMT, 256>(p, X, ldx, in_dim, Xp, grid, s);
+    case 64: return launch_tc_n<FMT, 64, DIRECT>(p, X, ldx, in_dim, Xp, grid, s);
+    case 128: return launch_tc_n<FMT, 128, DIRECT>(p, X, ldx, in_dim, Xp, grid, s);
+    default: return launch_tc_n<FMT, 256, DIRECT>(p, X, ldx, in_dim, Xp, grid, s);
     }
 }
 
@@ -1035,8 +888,7 @@ extern "C" {
 
 size_t rf_gemm_workspace_bytes(int fmt, int64_t in_dim, int n_tok)
 {
-    if (!gemm_fmt_ok(fmt) || in_dim <= 0 || in_dim % block_elems_of(fmt) != 0 || n_tok <= 0 ||
-        !tc_rows_ok(fmt, in_dim))
+    if (!gemm_fmt_ok(fmt) || in_dim <= 0 || in_dim % block_elems_of(fmt) != 0 || n_tok <= 0)
         return 0;
     return tc_workspace(in_dim, n_tok);
 }
@@ -1050,11 +902,10 @@ rf_status rf_gemm(int fmt, const void *W, int64_t row_start, int64_t row_end, in
         row_end < row_start || n_tok < 0 || ldx < in_dim || ldy < row_end - row_start)
         return RF_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(W) & 15u) != 0) return RF_ERR_MISALIGNED;
-    if (in_dim / 32 > 0x7fffffffLL || (row_end - row_start + kGM - 1) / kGM > 65535 ||
-        (n_tok + kGN - 1) / kGN > 65535)
-        return RF_ERR_TOO_LARGE;
-    const bool tc = tc_rows_ok(fmt, in_dim);
-    const size_t need = tc && n_tok > 0 ? tc_workspace(in_dim, n_tok) : 0;
+    const int N = tc_n(n_tok);
+    const int64_t ntt = (n_tok + N - 1) / N, nrt = (row_end - row_start + kGM - 1) / kGM;
+    if (in_dim / 32 > 0x7fffffffLL || ntt * nrt > 0x3fffffffLL) return RF_ERR_TOO_LARGE;
+    const size_t need = n_tok > 0 ? tc_workspace(in_dim, n_tok) : 0;
     if (need > 0) {
         if (!workspace || workspace_bytes < need) return RF_ERR_INVALID_ARG;
         if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return RF_ERR_MISALIGNED;
@@ -1062,64 +913,54 @@ rf_status rf_gemm(int fmt, const void *W, int64_t row_start, int64_t row_end, in
     if (row_end == row_start || n_tok == 0) return RF_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t rb = (in_dim / block_elems_of(fmt)) * (int64_t)block_bytes_of(fmt);
-    if (tc) {
-        TcParams p;
-        std::memset(&p, 0, sizeof(p));
-        const int cb = fmt == RF_Q4_0 || fmt == RF_Q4_K ? 144 : 272;   // chunk bytes
-        if (!encode_u16_map(&p.wmap, static_cast<const uint8_t *>(W) + row_start * rb,
-                            (uint64_t)(rb / 2), (uint64_t)(row_end - row_start), (uint64_t)rb,
-                            (uint32_t)(cb / 2), (uint32_t)kGM))
-            return RF_ERR_CUDA;
-        p.Xp = static_cast<const uint8_t *>(workspace);
-        p.Y = Y;
-        p.ldy = ldy;
-        p.rows = (int32_t)(row_end - row_start);
-        p.n_tok = n_tok;
-        p.nst = (int32_t)((in_dim + kTK - 1) / kTK);
-        p.nch = (int32_t)((rb + cb - 1) / cb);
-        p.limit = 2000000000ull;
-        p.withhold = -1;
-        if (const unsigned long long lim = take_wait_fault()) {
-            p.limit = lim;
-            p.withhold = p.nst > 1 ? 1 : 0;
-        }
-        const int N = tc_n(n_tok);
-        p.ntt = (n_tok + N - 1) / N;
-        const int64_t tiles = (int64_t)p.ntt * ((row_end - row_start + kGM - 1) / kGM);
-        // A last partial wave of at most half the SMs is split in K, so that
-        // it takes half a tile's time instead of a whole one.
-        const int sms = num_sms();
-        const int64_t last = tiles % sms;
-        p.full_tiles = (int32_t)tiles;
-        p.split_c = p.nch / 2;
-        if (last > 0 && 2 * last <= sms && p.nch >= 2) p.full_tiles = (int32_t)(tiles - last);
-        const dim3 grid((unsigned)(p.full_tiles + 2 * (tiles - p.full_tiles)));
-        uint8_t *Xp = static_cast<uint8_t *>(workspace);
-        switch (fmt) {
-        case RF_Q4_0: return launch_tc<RF_Q4_0>(p, X, ldx, in_dim, Xp, grid, s);
-        case RF_Q8_0: return launch_tc<RF_Q8_0>(p, X, ldx, in_dim, Xp, grid, s);
-        case RF_Q4_K: return launch_tc<RF_Q4_K>(p, X, ldx, in_dim, Xp, grid, s);
-        default: return launch_tc<RF_MXFP4>(p, X, ldx, in_dim, Xp, grid, s);
+    const bool direct = !tc_rows_ok(fmt, in_dim);
+    TcParams p;
+    std::memset(&p, 0, sizeof(p));
+    const int cb = fmt == RF_Q4_0 || fmt == RF_Q4_K ? 144 : 272;   // chunk bytes (tensor maps)
+    const uint8_t *W0 = static_cast<const uint8_t *>(W) + row_start * rb;
+    if (!direct && !encode_u16_map(&p.wmap, W0, (uint64_t)(rb / 2), (uint64_t)(row_end - row_start),
+                                   (uint64_t)rb, (uint32_t)(cb / 2), (uint32_t)kGM))
+        return RF_ERR_CUDA;
+    p.Wd = W0;
+    p.rb = rb;
+    p.Xp = static_cast<const uint8_t *>(workspace);
+    p.Y = Y;
+    p.ldy = ldy;
+    p.rows = (int32_t)(row_end - row_start);
+    p.n_tok = n_tok;
+    p.nst = (int32_t)((in_dim + kTK - 1) / kTK);
+    // The unit of the K split: a raw chunk, or a slice when rows are read directly.
+    p.nch = direct ? p.nst : (int32_t)((rb + cb - 1) / cb);
+    p.limit = 2000000000ull;
+    p.withhold = -1;
+    if (const unsigned long long lim = take_wait_fault()) {
+        p.limit = lim;
+        p.withhold = p.nst > 1 ? 1 : 0;
+    }
+    p.ntt = (int32_t)ntt;
+    const int64_t tiles = ntt * nrt;
+    // A last partial wave of at most half the SMs is split in K, so that it
+    // takes half a tile's time instead of a whole one.
+    const int sms = num_sms();
+    const int64_t last = tiles % sms;
+    p.full_tiles = (int32_t)tiles;
+    p.split_c = p.nch / 2;
+    if (last > 0 && 2 * last <= sms && p.nch >= 2) p.full_tiles = (int32_t)(tiles - last);
+    const dim3 grid((unsigned)(p.full_tiles + 2 * (tiles - p.full_tiles)));
+    uint8_t *Xp = static_cast<uint8_t *>(workspace);
+    if (direct) {
+        switch (fmt) {   // Q4_K rows are always aligned
+        case RF_Q4_0: return launch_tc<RF_Q4_0, true>(p, X, ldx, in_dim, Xp, grid, s);
+        case RF_Q8_0: return launch_tc<RF_Q8_0, true>(p, X, ldx, in_dim, Xp, grid, s);
+        case RF_MXFP4: return launch_tc<RF_MXFP4, true>(p, X, ldx, in_dim, Xp, grid, s);
+        default: return RF_ERR_UNSUPPORTED_FMT;
         }
     }
-    if (fmt == RF_Q4_K) return RF_ERR_UNSUPPORTED_FMT;   // its rows are always aligned
-    ExactParams p;
-    p.W = static_cast<const uint8_t *>(W);
-    p.X = X;
-    p.Y = Y;
-    p.row_start = row_start;
-    p.row_end = row_end;
-    p.ldx = ldx;
-    p.ldy = ldy;
-    p.rb = rb;
-    p.nb = (int32_t)(in_dim / 32);
-    p.n_tok = n_tok;
-    p.limit = 2000000000ull;
-    const dim3 grid((unsigned)((row_end - row_start + kGM - 1) / kGM), (unsigned)((n_tok + kGN - 1) / kGN));
     switch (fmt) {
-    case RF_Q4_0: return launch_exact<RF_Q4_0>(p, grid, s);
-    case RF_Q8_0: return launch_exact<RF_Q8_0>(p, grid, s);
-    default: return launch_exact<RF_MXFP4>(p, grid, s);
+    case RF_Q4_0: return launch_tc<RF_Q4_0, false>(p, X, ldx, in_dim, Xp, grid, s);
+    case RF_Q8_0: return launch_tc<RF_Q8_0, false>(p, X, ldx, in_dim, Xp, grid, s);
+    case RF_Q4_K: return launch_tc<RF_Q4_K, false>(p, X, ldx, in_dim, Xp, grid, s);
+    default: return launch_tc<RF_MXFP4, false>(p, X, ldx, in_dim, Xp, grid, s);
     }
 }
 

@@ -3,8 +3,10 @@
 over the weights).  Every (token, row) output is compared with the oracle's
 fp64 row-window matvec of that token.
 
-Tolerance, derived from the arithmetic of the main path (the general path
-rounds only x, so the same bound covers it):
+Rows whose byte length is not a multiple of 16 are read by the decoders
+directly instead of by tensor copies; the arithmetic is the same.
+
+Tolerance, derived from that arithmetic:
   * w and x each take one fp16 rounding: |dw| <= 2^-11 |w| + 2^-25,
     |dx| <= 2^-11 |x| + 2^-25 (half an fp16 subnormal step);
   * fp16 x fp16 products are exact in fp32;
@@ -69,10 +71,6 @@ def check_gemm(fmt, W, r0, r1, in_dim, X, Y):
     return worst
 
 
-def row_bytes_aligned(fmt, in_dim):
-    return syn.row_bytes(fmt, in_dim) % 16 == 0
-
-
 CASES = [  # fmt, rows, in_dim, window, n_tok
     (syn.Q4_0, 128, 256, (0, 128), 64),      # one CTA, one raw chunk
     (syn.Q4_0, 300, 4096, (5, 300), 70),     # ragged row tile, 128-token tile
@@ -80,9 +78,10 @@ CASES = [  # fmt, rows, in_dim, window, n_tok
     (syn.MXFP4, 200, 4096, (3, 200), 65),
     (syn.Q4_0, 64, 2304, (0, 64), 300),      # two 256-token tiles, nine chunks
     (syn.Q8_0, 512, 1024, (0, 512), 1),      # one token
-    (syn.MXFP4, 200, 2880, (0, 200), 40),    # 1,530-byte rows: general path
-    (syn.Q4_0, 96, 4064, (0, 96), 9),        # 2,286-byte rows: general path
-    (syn.Q8_0, 130, 2080, (2, 130), 66),     # 2,210-byte rows: general path
+    (syn.MXFP4, 200, 2880, (0, 200), 40),    # 1,530-byte rows: direct loads
+    (syn.Q4_0, 96, 4064, (0, 96), 9),        # 2,286-byte rows, odd block count: direct
+    (syn.Q8_0, 130, 2080, (2, 130), 66),     # 2,210-byte rows, odd block count: direct
+    (syn.Q4_0, 300, 2336, (7, 300), 200),    # 1,314-byte rows (phase 2 mod 4): direct
     (syn.Q4_K, 128, 256, (0, 128), 64),      # one super-block per row
     (syn.Q4_K, 300, 4096, (5, 300), 70),
     (syn.Q4_K, 257, 2048, (1, 257), 300),    # two 256-token tiles, ragged
@@ -94,8 +93,7 @@ def test_gemm_matches_oracle(rf, fmt, rows, in_dim, win, n_tok):
     W = syn.quant_matrix(fmt, rows, in_dim, seed=rows * 7 + in_dim)
     X = np.stack([syn.normal_f32(in_dim, 900 + t) for t in range(n_tok)])
     r0, r1 = win
-    need = rf.gemm_workspace_bytes(fmt, in_dim, n_tok)
-    assert (need > 0) == row_bytes_aligned(fmt, in_dim)
+    assert rf.gemm_workspace_bytes(fmt, in_dim, n_tok) > 0
     Y = rf.gemm(fmt, dev_tensor(W), r0, r1, in_dim, dev_tensor(X)).cpu().numpy()
     assert Y.shape == (n_tok, r1 - r0)
     check_gemm(fmt, W, r0, r1, in_dim, X, Y)
@@ -142,6 +140,25 @@ def test_gemm_full_size_sampled(rf):
     Y = Y.cpu().numpy()
     assert np.isfinite(Y).all()
     rng = np.random.default_rng(3)
+    toks = np.sort(rng.choice(n_tok, 8, replace=False))
+    for r in np.sort(rng.choice(rows, 64, replace=False)):
+        r = int(r)
+        check_gemm(fmt, W, r, r + 1, in_dim, X[toks], Y[toks][:, r:r + 1])
+
+
+def test_gemm_direct_full_size_sampled(rf):
+    """The 5760 x 2880 MXFP4 expert projection (1,530-byte rows, read
+    directly) at 512 tokens: 90 whole tiles, no K split; 64 sampled rows of
+    8 tokens against the oracle, every output finite."""
+    import torch
+    fmt, rows, in_dim, n_tok = syn.MXFP4, 5760, 2880, 512
+    W = syn.quant_matrix(fmt, rows, in_dim, 13, threads=8)
+    X = np.stack([syn.normal_f32(in_dim, 170 + t) for t in range(n_tok)])
+    Y = rf.gemm(fmt, dev_tensor(W), 0, rows, in_dim, dev_tensor(X))
+    torch.cuda.synchronize()
+    Y = Y.cpu().numpy()
+    assert np.isfinite(Y).all()
+    rng = np.random.default_rng(4)
     toks = np.sort(rng.choice(n_tok, 8, replace=False))
     for r in np.sort(rng.choice(rows, 64, replace=False)):
         r = int(r)
