@@ -135,6 +135,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
         : "r"(taddr)
         : "memory");
 }
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+          "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr)
+        : "memory");
+}
 __device__ __forceinline__ void tmem_ld_wait()
 {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -170,13 +181,27 @@ template <int N, bool DIRECT> __host__ __device__ constexpr int tc_stages()
     return DIRECT ? (N == 256 ? 4 : (N == 128 ? 6 : 8)) : (N == 256 ? 3 : (N == 128 ? 4 : 6));
 }
 
+// MMA issue threads.  One thread's chain per slice (barrier wait, fence,
+// four MMAs, commit: about 750 cycles) exceeds the tensor work of a slice
+// below N = 256, so where the ring allows, two threads take alternate slices
+// into two accumulators that the epilogue adds.  Issuer i then owns the slots
+// of parity i (an even ring), and each waits only on its own slots'
+// barriers, in order.  The decoder groups, which no longer see one global
+// consumption order, stay within one phase of a slot only with at least
+// six slots: a group's fill of slice b - 6 needed slice b - 6 - S consumed,
+// which by its issuer's order covers slice b - 2S when S >= 6.
+template <int N, bool DIRECT> __host__ __device__ constexpr int tc_issuers()
+{
+    return tc_stages<N, DIRECT>() % 2 == 0 && tc_stages<N, DIRECT>() >= 6 ? 2 : 1;
+}
+
 template <int FMT, int N, bool DIRECT>
 constexpr size_t tc_smem()
 {
     using RC = RawCfg<FMT>;
     return (size_t)tc_stages<N, DIRECT>() * (kATileT + N * kTK * 2) +
            (DIRECT ? 0 : (size_t)RC::R * kGM * RC::BPC * RC::BS) + 16 +
-           (size_t)(3 * tc_stages<N, DIRECT>() + 2 * RC::R + 2) * 8 + 16;
+           (size_t)(3 * tc_stages<N, DIRECT>() + 2 * RC::R + 3) * 8 + 16;
 }
 
 struct TcParams {
@@ -520,6 +545,8 @@ __global__ void __launch_bounds__(kTThreads, 1) gemm_tc_kernel(const __grid_cons
     // Slices per raw chunk; in direct mode every slice is its own "chunk"
     // (the unit of the last-wave K split).
     constexpr int QPC = DIRECT ? 1 : RC::BPC * RC::BE / kTK;
+    constexpr int NI = tc_issuers<N, DIRECT>();
+    constexpr uint32_t kCols = (uint32_t)(NI * N);   // accumulator i at columns [i*N, (i+1)*N)
     constexpr int BT = N * kTK * 2;   // fp16 activation tile of one slice
     extern __shared__ __align__(1024) uint8_t smem[];
     uint8_t *a_t = smem;                 // [S][16 KB]
@@ -531,8 +558,8 @@ __global__ void __launch_bounds__(kTThreads, 1) gemm_tc_kernel(const __grid_cons
     // the slot's MMAs done.
     uint64_t *full = bars, *bfull = bars + S, *empty = bars + 2 * S;
     uint64_t *rfull = bars + 3 * S, *rempty = rfull + R;
-    uint64_t *accf = rempty + R, *mdone = accf + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mdone + 1);
+    uint64_t *accf = rempty + R, *mdone = accf + 1;   // mdone: one per issuer
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mdone + 2);
     volatile int *stop = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -550,6 +577,7 @@ __global__ void __launch_bounds__(kTThreads, 1) gemm_tc_kernel(const __grid_cons
     const int c_hi = half == 0 ? p.split_c : p.nch;
     const int b_lo = c_lo * QPC;
     const int b_hi = min(c_hi * QPC, p.nst);
+    const int ni = b_hi - b_lo >= 2 ? NI : 1;   // issuers with slices (b_hi > b_lo always)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -561,13 +589,14 @@ __global__ void __launch_bounds__(kTThreads, 1) gemm_tc_kernel(const __grid_cons
             mbar_init(&rfull[r], 1);
             mbar_init(&rempty[r], 4 * kDecGroups);
         }
-        mbar_init(accf, 1);
-        mbar_init(mdone, 1);
+        mbar_init(accf, (uint32_t)ni);
+        mbar_init(&mdone[0], 1);
+        mbar_init(&mdone[1], 1);
         *stop = 0;
         fence_barrier_init();
     }
     if (warp == 3) {
-        tmem_alloc(tmem_slot, (uint32_t)N);
+        tmem_alloc(tmem_slot, kCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -616,18 +645,21 @@ __global__ void __launch_bounds__(kTThreads, 1) gemm_tc_kernel(const __grid_cons
                 if (b_lo + bl != skip) mbar_drain(&bfull[bl % S], (bl / S) & 1);
         }
         __syncwarp();
-    } else if (warp == 2) {
-        // MMA issue: four K=16 steps per slice into one accumulator.  The
-        // descriptors of slot 0 are built once; a slot and a K step move
-        // the start-address field (address / 16, well inside its 14 bits).
-        if (lane == 0) {
+    } else if (warp == 2 || (NI == 2 && warp == 3)) {
+        // MMA issue: four K=16 steps per slice into issuer iss's
+        // accumulator, slices iss, iss + NI, ...  The descriptors of slot 0
+        // are built once; a slot and a K step move the start-address field
+        // (address / 16, well inside its 14 bits).
+        const int iss = warp - 2;
+        if (lane == 0 && iss < ni) {
             int issued = 0;
             bool failed = false;
             const uint64_t ad0 = smem_desc(smem_addr(a_t), 1024);
             const uint64_t bd0 = smem_desc(smem_addr(b_t), 1024);
-            int s = 0;
+            const uint32_t acc = tmem + (uint32_t)(iss * N);
+            int s = iss;   // NI divides S
             uint32_t ph = 0;
-            for (int b = b_lo; b < b_hi; ++b) {
+            for (int b = b_lo + iss; b < b_hi; b += NI) {
                 if (!wait(&full[s], ph)) {
                     failed = true;
                     break;
@@ -635,14 +667,14 @@ __global__ void __launch_bounds__(kTThreads, 1) gemm_tc_kernel(const __grid_cons
                 tc_fence_after();
                 const uint64_t ad = ad0 + (uint64_t)((s * kATileT) >> 4);
                 const uint64_t bd = bd0 + (uint64_t)((s * BT) >> 4);
-                tc_mma(tmem, ad, bd, idesc_of(N), b != b_lo);
+                tc_mma(acc, ad, bd, idesc_of(N), b != b_lo + iss);
 #pragma unroll
                 for (int kk = 1; kk < kTK / 16; ++kk)
-                    tc_mma(tmem, ad + 16 * kk, bd + 16 * kk, idesc_of(N), 1u);
+                    tc_mma(acc, ad + 16 * kk, bd + 16 * kk, idesc_of(N), 1u);
                 tc_commit(&empty[s]);
                 ++issued;
-                if (++s == S) {
-                    s = 0;
+                if ((s += NI) >= S) {
+                    s -= S;
                     ph ^= 1u;
                 }
             }
@@ -650,8 +682,8 @@ __global__ void __launch_bounds__(kTThreads, 1) gemm_tc_kernel(const __grid_cons
                 tc_commit(accf);
             } else if (issued) {
                 // Every issued MMA completes before tensor memory is freed.
-                tc_commit(mdone);
-                mbar_drain(mdone, 0);
+                tc_commit(&mdone[iss]);
+                mbar_drain(&mdone[iss], 0);
             }
         }
         __syncwarp();
@@ -721,7 +753,8 @@ __global__ void __launch_bounds__(kTThreads, 1) gemm_tc_kernel(const __grid_cons
             __syncwarp();
             if (lane == 0) mbar_arrive(&rempty[rs]);
         }
-        // Epilogue: the group's half of the accumulator columns.
+        // Epilogue: the group's share of the accumulator columns (with two
+        // issuers, the sum of both accumulators: one fp32 addition).
         if (__all_sync(0xffffffffu, wait(accf, 0))) {
             tc_fence_after();
             const int64_t row = (int64_t)rt * kGM + i;
@@ -731,8 +764,22 @@ __global__ void __launch_bounds__(kTThreads, 1) gemm_tc_kernel(const __grid_cons
 #pragma unroll 1
             for (int cc = grp * 32; cc < N; cc += 32 * kDecGroups) {
                 uint32_t v[32];
-                tmem_ld32(tb + (uint32_t)cc, v);
-                tmem_ld_wait();
+                if constexpr (NI == 1) {
+                    tmem_ld32(tb + (uint32_t)cc, v);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int h = 0; h < 32; h += 16) {
+                        uint32_t a[16], c[16];
+                        tmem_ld16(tb + (uint32_t)(cc + h), a);
+                        if (ni == 2) tmem_ld16(tb + (uint32_t)(N + cc + h), c);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int n = 0; n < 16; ++n)
+                            v[h + n] = ni == 2 ? __float_as_uint(__uint_as_float(a[n]) + __uint_as_float(c[n]))
+                                               : a[n];
+                    }
+                }
                 if (row_ok) {
 #pragma unroll
                     for (int n = 0; n < 32; ++n)
@@ -749,52 +796,72 @@ __global__ void __launch_bounds__(kTThreads, 1) gemm_tc_kernel(const __grid_cons
     __syncthreads();
     if (warp == 3) {
         tc_fence_after();
-        tmem_dealloc(tmem, (uint32_t)N);
+        tmem_dealloc(tmem, kCols);
     }
 }
 
-// X (fp32 rows ldx apart) -> fp16 tiles [token tile][slice][N x 64] in the
-// K-major core-matrix layout: element (t, k) of a tile at (t/8)*1024 +
-// (k/8)*128 + (t%8)*16 + (k%8)*2; 16-byte unit u of the whole buffer holds
-// tokens and inputs such that the unit index within a tile is
-// (t/8)*64 + (k/8)*8 + t%8.  Tokens past n_tok and inputs past in_dim are 0.
+struct PrepParams {
+    const float *X;
+    int64_t ldx, in_dim, units;
+    int n_tok, nst;
+    uint8_t *Xp;
+    int xb;              // blocks [0, xb) convert X, the rest zero Y
+    float *Y;
+    int64_t ldy;
+    int rows, ntt, t0, ntiles;
+};
+
+// The pre-pass of a call, one launch:
+//  * blocks [0, xb): X (fp32 rows ldx apart) -> fp16 tiles [token tile]
+//    [slice][N x 64] in the K-major core-matrix layout: element (t, k) of a
+//    tile at (t/8)*1024 + (k/8)*128 + (t%8)*16 + (k%8)*2; 16-byte unit u of
+//    the whole buffer holds tokens and inputs such that the unit index within
+//    a tile is (t/8)*64 + (k/8)*8 + t%8.  Tokens past n_tok and inputs past
+//    in_dim are 0.
+//  * the other blocks: Y = 0 over tiles [t0, t0 + ntiles) (tile = token tile
+//    + ntt * row tile), whose two K halves are then added into it.
 template <int N>
-__global__ void __launch_bounds__(256) x16_kernel(const float *X, int64_t ldx, int n_tok,
-                                                  int64_t in_dim, int nst, int64_t units,
-                                                  uint8_t *Xp)
+__global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ PrepParams q)
 {
-    for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < units;
-         u += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t tile = u / (N * 8);
-        const int w = (int)(u % (N * 8));
-        const int t = (w >> 6) * 8 + (w & 7), c = (w >> 3) & 7;
-        const int64_t tok = (tile / nst) * N + t;
-        const int64_t k0 = (tile % nst) * kTK + c * 8;
-        uint32_t h[4] = {0u, 0u, 0u, 0u};
-        if (tok < n_tok && k0 < in_dim) {
-            const float *x = X + tok * ldx + k0;
+    if ((int)blockIdx.x < q.xb) {
+        for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < q.units;
+             u += (int64_t)q.xb * blockDim.x) {
+            const int64_t tile = u / (N * 8);
+            const int w = (int)(u % (N * 8));
+            const int t = (w >> 6) * 8 + (w & 7), c = (w >> 3) & 7;
+            const int64_t tok = (tile / q.nst) * N + t;
+            const int64_t k0 = (tile % q.nst) * kTK + c * 8;
+            uint32_t h[4] = {0u, 0u, 0u, 0u};
+            if (tok < q.n_tok && k0 < q.in_dim) {   // k0 + 8 <= in_dim (a multiple of 32)
+                const float *x = q.X + tok * q.ldx + k0;
+                float f[8];
+                if ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) {
+                    const float4 a = reinterpret_cast<const float4 *>(x)[0];
+                    const float4 b = reinterpret_cast<const float4 *>(x)[1];
+                    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+                    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+                } else {
 #pragma unroll
-            for (int m = 0; m < 4; ++m)
-                h[m] = (uint32_t)__half_as_ushort(__float2half_rn(x[2 * m])) |
-                       ((uint32_t)__half_as_ushort(__float2half_rn(x[2 * m + 1])) << 16);
+                    for (int m = 0; m < 8; ++m) f[m] = x[m];
+                }
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    h[m] = (uint32_t)__half_as_ushort(__float2half_rn(f[2 * m])) |
+                           ((uint32_t)__half_as_ushort(__float2half_rn(f[2 * m + 1])) << 16);
+            }
+            *reinterpret_cast<uint4 *>(q.Xp + u * 16) = make_uint4(h[0], h[1], h[2], h[3]);
         }
-        *reinterpret_cast<uint4 *>(Xp + u * 16) = make_uint4(h[0], h[1], h[2], h[3]);
-    }
-}
-
-// Zeroes Y over tiles [t0, t0 + ntiles) (tile = token tile + ntt * row
-// tile), whose two K halves are then added into it.
-__global__ void __launch_bounds__(256) zero_tiles_kernel(float *Y, int64_t ldy, int rows, int n_tok,
-                                                         int ntt, int N, int t0, int ntiles)
-{
-    const int64_t per = (int64_t)N * kGM;
-    for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < (int64_t)ntiles * per;
-         u += (int64_t)gridDim.x * blockDim.x) {
-        const int tile = t0 + (int)(u / per);
-        const int w = (int)(u % per);
-        const int tok = (tile % ntt) * N + w / kGM;
-        const int row = (tile / ntt) * kGM + w % kGM;
-        if (tok < n_tok && row < rows) Y[(int64_t)tok * ldy + row] = 0.f;
+    } else {
+        const int64_t per = (int64_t)N * kGM;
+        const int zb = (int)gridDim.x - q.xb;
+        for (int64_t u = (int64_t)(blockIdx.x - q.xb) * blockDim.x + threadIdx.x;
+             u < (int64_t)q.ntiles * per; u += (int64_t)zb * blockDim.x) {
+            const int tile = q.t0 + (int)(u / per);
+            const int w = (int)(u % per);
+            const int tok = (tile % q.ntt) * N + w / kGM;
+            const int row = (tile / q.ntt) * kGM + w % kGM;
+            if (tok < q.n_tok && row < q.rows) q.Y[(int64_t)tok * q.ldy + row] = 0.f;
+        }
     }
 }
 
@@ -840,16 +907,24 @@ rf_status launch_tc_n(const TcParams &p, const float *X, int64_t ldx, int64_t in
         cudaGetLastError();
     });
     if (!ok[dev & 63]) return RF_ERR_CUDA;
-    const int ntiles = (int)grid.x - p.full_tiles;   // CTAs past the whole tiles, two per split tile
-    if (ntiles > 0) {
-        const int nsplit = ntiles / 2;
-        const int zb = (int)std::min<int64_t>(((int64_t)nsplit * N * kGM + 255) / 256, (int64_t)num_sms() * 8);
-        zero_tiles_kernel<<<zb, 256, 0, s>>>(p.Y, p.ldy, p.rows, p.n_tok, p.ntt, N, p.full_tiles, nsplit);
-        if (last_cuda_error() != RF_OK) return RF_ERR_CUDA;
-    }
-    const int64_t units = (int64_t)p.ntt * N * p.nst * 8;
-    const int xb = (int)std::min<int64_t>((units + 255) / 256, (int64_t)num_sms() * 8);
-    x16_kernel<N><<<xb, 256, 0, s>>>(X, ldx, p.n_tok, in_dim, p.nst, units, Xp);
+    PrepParams q;
+    q.X = X;
+    q.ldx = ldx;
+    q.in_dim = in_dim;
+    q.units = (int64_t)p.ntt * N * p.nst * 8;
+    q.n_tok = p.n_tok;
+    q.nst = p.nst;
+    q.Xp = Xp;
+    q.Y = p.Y;
+    q.ldy = p.ldy;
+    q.rows = p.rows;
+    q.ntt = p.ntt;
+    q.t0 = p.full_tiles;
+    q.ntiles = ((int)grid.x - p.full_tiles) / 2;   // CTAs past the whole tiles, two per split tile
+    const int64_t cap = (int64_t)num_sms() * 8;
+    q.xb = (int)std::min<int64_t>((q.units + 255) / 256, cap);
+    const int zb = q.ntiles > 0 ? (int)std::min<int64_t>(((int64_t)q.ntiles * N * kGM + 255) / 256, cap) : 0;
+    prep_kernel<N><<<q.xb + zb, 256, 0, s>>>(q);
     if (last_cuda_error() != RF_OK) return RF_ERR_CUDA;
     gemm_tc_kernel<FMT, N, DIRECT><<<grid, kTThreads, tc_smem<FMT, N, DIRECT>(), s>>>(p);
     return last_cuda_error();
@@ -940,7 +1015,8 @@ rf_status rf_gemm(int fmt, const void *W, int64_t row_start, int64_t row_end, in
     p.ntt = (int32_t)ntt;
     const int64_t tiles = ntt * nrt;
     // A last partial wave of at most half the SMs is split in K, so that it
-    // takes half a tile's time instead of a whole one.
+    // takes half a tile's time instead of a whole one (with fewer tiles than
+    // SMs, every tile).
     const int sms = num_sms();
     const int64_t last = tiles % sms;
     p.full_tiles = (int32_t)tiles;
