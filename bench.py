@@ -490,17 +490,18 @@ def run_multi_token(torch, rf, device, reps: int = 50):
 
 
 def run_prefill(torch, rf, device, tensor_peak: float, reps: int = 5, fmt: int = syn.Q4_0,
-                tokens=(8, 64, 512, 2048)):
+                tokens=(8, 64, 512, 2048), shape=None, copies: int = 8):
     """Chunks of tokens through one resident matrix per call (rf_gemm, the
-    tensor-core prefill dequant-GEMM): the 11008x4096 gate projection in
-    `fmt`, eight copies (> L2) walked round-robin in one CUDA graph, for each
-    chunk size in `tokens`.  Each call includes its activation pre-pass.
-    value = TF/s (2 * rows * in_dim * tokens per call); weight_gbs = weight
-    bytes per second; vs_gemv_multi = the same tokens through rf_gemv_multi
-    in launches of eight tokens, timed the same way, over this call."""
-    rows, in_dim = syn.C2["d_ff"], syn.C2["d_model"]
+    tensor-core prefill dequant-GEMM): by default the 11008x4096 gate
+    projection in `fmt`, `copies` copies (> L2) walked round-robin in one
+    CUDA graph, for each chunk size in `tokens`.  Each call includes its
+    activation pre-pass.  value = TF/s (2 * rows * in_dim * tokens per call);
+    weight_gbs = weight bytes per second; vs_gemv_multi = the same tokens
+    through rf_gemv_multi in launches of eight tokens, timed the same way,
+    over this call."""
+    rows, in_dim = shape if shape is not None else (syn.C2["d_ff"], syn.C2["d_model"])
     Ws = [torch.from_numpy(syn.quant_matrix(fmt, rows, in_dim, 70 + c, threads=8)).to(device)
-          for c in range(8)]
+          for c in range(copies)]
     nbytes = Ws[0].numel()
     s = torch.cuda.Stream(device)
     s.wait_stream(torch.cuda.current_stream())
@@ -1109,6 +1110,11 @@ def main():
             extra["prefill_q4_0"] = run_prefill(torch, rf, device, load_tensor_peak()[0])
             extra["prefill_q4_k"] = run_prefill(torch, rf, device, load_tensor_peak()[0],
                                                 fmt=syn.Q4_K, tokens=(64, 512, 2048))
+            # 2880-wide MXFP4 rows (1,530 bytes, read directly by the decoders),
+            # one expert's gate and up rows: 5760 x 2880, 24 copies > L2.
+            extra["prefill_mxfp4_2880"] = run_prefill(
+                torch, rf, device, load_tensor_peak()[0], fmt=syn.MXFP4, tokens=(8, 64, 512, 2048),
+                shape=(2 * syn.C3["n_ff"], syn.C3["n_embd"]), copies=24)
             for name, fmt in (("dense_layer_q4_k", syn.Q4_K), ("dense_layer_q6_k", syn.Q6_K)):
                 r = run_dense_format(torch, rf, device, fmt)
                 r["frac_of_hbm_peak"] = r["value"] / peak
