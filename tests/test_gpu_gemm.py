@@ -82,6 +82,9 @@ CASES = [  # fmt, rows, in_dim, window, n_tok
     (syn.Q4_0, 96, 4064, (0, 96), 9),        # 2,286-byte rows, odd block count: direct
     (syn.Q8_0, 130, 2080, (2, 130), 66),     # 2,210-byte rows, odd block count: direct
     (syn.Q4_0, 300, 2336, (7, 300), 200),    # 1,314-byte rows (phase 2 mod 4): direct
+    (syn.Q4_0, 100, 64, (0, 100), 5),        # one slice: the second MMA issuer has none
+    (syn.Q8_0, 70, 32, (3, 70), 3),          # one block per row: a half slice
+    (syn.MXFP4, 140, 128, (0, 140), 100),    # two slices split in K: one per CTA, N = 128
     (syn.Q4_K, 128, 256, (0, 128), 64),      # one super-block per row
     (syn.Q4_K, 300, 4096, (5, 300), 70),
     (syn.Q4_K, 257, 2048, (1, 257), 300),    # two 256-token tiles, ragged
