@@ -9,9 +9,10 @@
 // gemm_tc_kernel:
 //   * A pre-pass rounds X to fp16 once, into the operand layout of the MMA
 //     (tiles of N tokens x 64 inputs, K-major core matrices), in a caller
-//     workspace.
+//     workspace; the same launch zeroes the outputs of tiles split in K.
 //   * A CTA owns 128 rows x N tokens (N = 64, 128 or 256) and accumulates
-//     the whole of K in tensor memory (N fp32 columns).
+//     the whole of K (or half of it, for a tile of a last partial wave) in
+//     tensor memory (N fp32 columns per MMA issuer).
 //   * Rows whose byte length is a multiple of 16: one thread streams the
 //     raw quantized bytes of its 128 rows, a chunk of 8 or 16 blocks (one
 //     Q4_K super-block) at a time, with 2-D tensor copies into a ring.
@@ -24,8 +25,10 @@
 //     d*sc*q - dmin*m is rounded to fp32 first) in the core-matrix layout;
 //     three groups of four warps take the slices round-robin.
 //   * One thread issues four tcgen05.mma (M=128, N, K=16) per slice and
-//     commits them to the slice's "empty" barrier; the last commit releases
-//     the epilogue, which reads the accumulator out of tensor memory.
+//     commits them to the slice's "empty" barrier (two threads, on alternate
+//     slices and separate accumulators, where the ring allows); the last
+//     commits release the epilogue, which reads the accumulators out of
+//     tensor memory.
 //   Error: w and x each carry one fp16 rounding (relative 2^-11, absolute
 //   2^-25 below the normal range), accumulation is fp32.
 //
