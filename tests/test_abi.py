@@ -158,6 +158,40 @@ def test_newer_entry_points_check_arguments_first(L):
     assert ms(rf.Q4_0, p, 8, 2, p + 8, p, p, 64, 64, 32, 3, p, None, p, p, p, None) == 8
 
 
+def test_gemm_checks_arguments_first(L):
+    """rf_gemm refuses bad arguments, and returns for empty work, before any
+    device call; rf_gemm_workspace_bytes covers at least the fp16 activation
+    tiles (tokens rounded up to the token tile, inputs to 64)."""
+    buf = (ctypes.c_uint8 * 16384)()
+    p = (ctypes.addressof(buf) + 255) & ~255
+    g = L.rf_gemm
+    ws = 8192   # 64 tokens x 64 inputs x 2 bytes: enough for in_dim 32, up to 64 tokens
+    # rf_gemm(fmt, W, r0, r1, in_dim, n_tok, X, ldx, Y, ldy, workspace, workspace_bytes, stream)
+    assert g(rf.Q6_K, p, 0, 4, 256, 4, p, 256, p, 4, p, ws, None) == 2     # not served
+    assert g(7, p, 0, 4, 32, 4, p, 32, p, 4, p, ws, None) == 2
+    assert g(rf.Q4_0, p, 0, 4, 48, 4, p, 48, p, 4, p, ws, None) == 1       # not whole blocks
+    assert g(rf.Q4_K, p, 0, 4, 288, 4, p, 288, p, 4, p, ws, None) == 1     # not whole super-blocks
+    assert g(rf.Q4_0, None, 0, 4, 32, 4, p, 32, p, 4, p, ws, None) == 1
+    assert g(rf.Q4_0, p, 4, 3, 32, 4, p, 32, p, 4, p, ws, None) == 1       # row_end < row_start
+    assert g(rf.Q4_0, p, 0, 4, 32, -1, p, 32, p, 4, p, ws, None) == 1
+    assert g(rf.Q4_0, p, 0, 4, 32, 4, p, 31, p, 4, p, ws, None) == 1       # ldx < in_dim
+    assert g(rf.Q4_0, p, 0, 4, 32, 4, p, 32, p, 3, p, ws, None) == 1       # ldy < rows
+    assert g(rf.Q4_0, p + 4, 0, 4, 32, 4, p, 32, p, 4, p, ws, None) == 8   # W not 16-byte aligned
+    assert g(rf.Q4_0, p, 0, 4, 32, 4, p, 32, p, 4, None, 0, None) == 1     # no workspace
+    assert g(rf.Q4_0, p, 0, 4, 32, 4, p, 32, p, 4, p, ws - 1, None) == 1   # too small
+    assert g(rf.Q4_0, p, 0, 4, 32, 4, p, 32, p, 4, p + 8, ws, None) == 8   # misaligned
+    big = 1 << 40
+    assert g(rf.Q4_0, p, 0, big, 32, 4, p, 32, p, big, p, ws, None) == 9   # too many tiles
+    assert g(rf.Q4_0, p, 5, 5, 32, 4, p, 32, p, 4, p, ws, None) == 0       # no rows
+    assert g(rf.Q4_0, p, 0, 4, 32, 0, p, 32, p, 4, None, 0, None) == 0     # no tokens
+    wb = L.rf_gemm_workspace_bytes
+    assert wb(rf.Q6_K, 256, 4) == 0 and wb(rf.Q4_0, 48, 4) == 0 and wb(rf.Q4_0, 64, 0) == 0
+    for fmt, in_dim, n_tok, tile in ((rf.Q4_0, 4096, 8, 64), (rf.MXFP4, 2880, 100, 128),
+                                     (rf.Q4_K, 4096, 300, 256)):
+        xp = -(-n_tok // tile) * tile * -(-in_dim // 64) * 64 * 2
+        assert wb(fmt, in_dim, n_tok) >= xp
+
+
 @pytest.mark.skipif(has_gpu(), reason="checks the behaviour on a machine without a GPU")
 def test_no_gpu_means_cuda_error_not_fallback(L):
     buf = (ctypes.c_uint8 * 4096)()
