@@ -2,6 +2,7 @@
 import numpy as np
 
 import oracle
+import synthetic as syn
 
 
 def dev_tensor(a, device="cuda"):
@@ -155,3 +156,19 @@ def moe_reference_biased(fmt, G, U, D, n_ff, n_embd, x, logits, top_k, gate_bias
         ths.append(th)
     return {"idx": idx, "w": w, "h": hs, "tol_h": ths, "y": y, "tol_y": tol_y,
             "clamped": clamped}
+
+
+def derived_gemm_bound(fmt, W, r0, r1, in_dim, X):
+    """(n_tok, rows) error bound of rf_gemm's arithmetic, from the oracle's
+    exact dequantized weights: w and x each rounded once to fp16 (relative
+    2^-11, absolute 2^-25 below the normal range), fp16 x fp16 products exact
+    in fp32, fp32 accumulation over in_dim terms bounded loosely by
+    in_dim * 2^-23 times the sum of |products| (truncating adds allowed);
+    Q4_K's weights take one fp32 rounding first (another 2^-23)."""
+    Wd = oracle.dequantize(fmt, W[r0:r1]).astype(np.float64).reshape(r1 - r0, in_dim)
+    Xa = np.abs(np.asarray(X, dtype=np.float64))
+    Wa = np.abs(Wd)
+    S = Xa @ Wa.T
+    lin = 2.0 ** -25 * 1.001 * (Wa.sum(axis=1)[None, :] + Xa.sum(axis=1)[:, None])
+    extra = 2.0 ** -23 if fmt == syn.Q4_K else 0.0
+    return (2.0 ** -10 + 2.0 ** -22 + extra + in_dim * 2.0 ** -23) * S + lin

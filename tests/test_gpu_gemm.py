@@ -23,7 +23,7 @@ import pytest
 
 import oracle
 import synthetic as syn
-from gpu_helpers import dev_tensor, gemv_tol
+from gpu_helpers import derived_gemm_bound as derived_bound, dev_tensor, gemv_tol
 
 pytestmark = pytest.mark.gpu
 
@@ -38,18 +38,6 @@ def rf():
     m.lib()
     yield m
     assert m.device_status() == m.OK
-
-
-def derived_bound(fmt, W, r0, r1, in_dim, X):
-    """(n_tok, rows) bound of the module docstring, from the oracle's exact
-    dequantized weights."""
-    Wd = oracle.dequantize(fmt, W[r0:r1]).astype(np.float64).reshape(r1 - r0, in_dim)
-    Xa = np.abs(np.asarray(X, dtype=np.float64))
-    Wa = np.abs(Wd)
-    S = Xa @ Wa.T
-    lin = 2.0 ** -25 * 1.001 * (Wa.sum(axis=1)[None, :] + Xa.sum(axis=1)[:, None])
-    extra = 2.0 ** -23 if fmt == syn.Q4_K else 0.0
-    return (2.0 ** -10 + 2.0 ** -22 + extra + in_dim * 2.0 ** -23) * S + lin
 
 
 def check_gemm(fmt, W, r0, r1, in_dim, X, Y):
