@@ -264,8 +264,9 @@ RF_API rf_status rf_gemv_multi(int fmt, const void *W, int64_t row_start, int64_
  * 256 for Q4_K), bad window, n_tok < 0, ldx < in_dim, ldy < rows,
  * workspace missing or too small);
  * RF_ERR_MISALIGNED (W or workspace not 16-byte aligned); RF_ERR_TOO_LARGE
- * (ceil(rows / 128) * ceil(n_tok / T) above 2^30 - 1, T the token tile:
- * 64 up to 64 tokens, 128 up to 128, else 256).  Empty work is a no-op.
+ * (more than 2^31 - 1 rows, or ceil(rows / 128) * ceil(n_tok / T) above
+ * 2^30 - 1, T the token tile: 64 up to 64 tokens, 128 up to 128, else 256).
+ * Empty work is a no-op.
  * A bounded internal wait that gives up is reported by rf_device_status as
  * RF_ERR_TIMEOUT. */
 RF_API rf_status rf_gemm(int fmt, const void *W, int64_t row_start, int64_t row_end,

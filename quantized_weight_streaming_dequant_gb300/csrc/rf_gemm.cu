@@ -982,7 +982,8 @@ rf_status rf_gemm(int fmt, const void *W, int64_t row_start, int64_t row_end, in
     if ((reinterpret_cast<uintptr_t>(W) & 15u) != 0) return RF_ERR_MISALIGNED;
     const int N = tc_n(n_tok);
     const int64_t ntt = (n_tok + N - 1) / N, nrt = (row_end - row_start + kGM - 1) / kGM;
-    if (in_dim / 32 > 0x7fffffffLL || ntt * nrt > 0x3fffffffLL) return RF_ERR_TOO_LARGE;
+    if (in_dim / 32 > 0x7fffffffLL || row_end - row_start > 0x7fffffffLL || ntt * nrt > 0x3fffffffLL)
+        return RF_ERR_TOO_LARGE;
     const size_t need = n_tok > 0 ? tc_workspace(in_dim, n_tok) : 0;
     if (need > 0) {
         if (!workspace || workspace_bytes < need) return RF_ERR_INVALID_ARG;

@@ -182,6 +182,7 @@ def test_gemm_checks_arguments_first(L):
     assert g(rf.Q4_0, p, 0, 4, 32, 4, p, 32, p, 4, p + 8, ws, None) == 8   # misaligned
     big = 1 << 40
     assert g(rf.Q4_0, p, 0, big, 32, 4, p, 32, p, big, p, ws, None) == 9   # too many tiles
+    assert g(rf.Q4_0, p, 0, 1 << 31, 32, 1, p, 32, p, 1 << 31, p, ws, None) == 9   # rows > 2^31 - 1
     assert g(rf.Q4_0, p, 5, 5, 32, 4, p, 32, p, 4, p, ws, None) == 0       # no rows
     assert g(rf.Q4_0, p, 0, 4, 32, 0, p, 32, p, 4, None, 0, None) == 0     # no tokens
     wb = L.rf_gemm_workspace_bytes
